@@ -1,0 +1,219 @@
+/*
+ * moe_b300.h -- C ABI of a sparsely activated Mixture-of-Experts (MoE) layer, forward pass, on one
+ * NVIDIA B300 (sm_103a).
+ *
+ * The layer computes  Output(x) = sum_i g_i(x) * E_i(x)  over the top-k experts chosen for each token
+ * ("MoE on a single card", section 1.2, the formula for Output; "MoE sparse-compute acceleration",
+ * section 2.1, NoisyTopKGating; "Tutel MoE guide", gate types top / cosine_top and capacity_factor).
+ * It runs as five steps, each of which is also an entry point:
+ *
+ *   moe_route       gate GEMM + softmax / noisy / cosine scoring + per-token top-k and gate weights
+ *   moe_dispatch    per-expert counts, capacity slots in token order, drop-on-overflow, row gather
+ *   moe_expert_ffn  grouped per-expert Linear -> GELU -> Linear over the dispatched rows only
+ *   moe_combine     gate-weighted sum of the expert outputs back into token order
+ *   moe_forward     all of the above in one call
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Ownership.  The caller allocates and owns every buffer.  The library never allocates or frees
+ *    device memory.  It keeps no state between calls except a small host-side cache of TMA tensor
+ *    descriptors (keyed by pointer and shape) and the optional trace hook (moe_trace_events).
+ *  - Pointers.  Tensor arguments are DEVICE pointers (cudaMalloc / torch CUDA tensors), contiguous,
+ *    row-major, 16-byte aligned.  `stream` is a cudaStream_t passed as void*; NULL means the legacy
+ *    default stream.
+ *  - Asynchrony.  Calls enqueue work on `stream` and return; they never synchronise.  Outputs are
+ *    valid once the stream has reached that point.  No call performs a host<->device copy.
+ *  - Validation.  Every argument is checked on the host before anything is launched.  A failed check
+ *    returns a status other than MOE_OK and launches nothing.  Nothing is thrown across the ABI.
+ *  - Device-side errors.  Kernels that wait on barriers give up after a bounded number of polls and
+ *    record an error word at the start of the workspace; moe_device_status() reads it.
+ *  - Empty input.  T = 0 is valid: every call returns MOE_OK and launches nothing.
+ *  - dtype.  x and every weight tensor share one element type (moe_config.dtype): MOE_BF16 (the tensor
+ *    core path: bf16 operands, fp32 accumulation) or MOE_F32 (fp32 FMA on CUDA cores, no TF32).  The
+ *    gate logits, scores and gate weights are always fp32; the layer output is always fp32.
+ *  - Layouts.  Linear weights use the [out_features, in_features] layout, so both GEMM operands are
+ *    contiguous along the reduction dimension:
+ *        w_gate, w_noise [E, d]      proj [cos_dim, d]      expert_emb [E, cos_dim]
+ *        w1 [E, h, d]   b1 [E, h]    w2 [E, d, h]   b2 [E, d]
+ *    with T = tokens, d = model_dim, h = hidden_size_per_expert, E = num_experts, k = top_k.
+ */
+#ifndef MOE_B300_H
+#define MOE_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes -------------------------------------------------------------------------- */
+typedef int32_t moe_status;
+#define MOE_OK                  0
+#define MOE_ERR_INVALID_ARG     1 /* a pointer, size or enum is out of its documented range          */
+#define MOE_ERR_UNSUPPORTED     2 /* valid in principle, outside what this build implements          */
+#define MOE_ERR_WORKSPACE       3 /* workspace NULL, misaligned or smaller than moe_workspace_size() */
+#define MOE_ERR_CUDA            4 /* a CUDA runtime call failed (launch, memset, descriptor encode)  */
+#define MOE_ERR_DEVICE_CHECK    5 /* a kernel's own bounds check failed (see moe_device_status)      */
+#define MOE_ERR_DEVICE_TIMEOUT  6 /* a kernel's bounded barrier wait ran out (see moe_device_status)  */
+
+/* ---- enums ----------------------------------------------------------------------------------- */
+/* Gate types.  SOFTMAX: s = x W_g^T ("single linear layer + Softmax", intelliparadigm section 2.1;
+ * Tutel top.py).  NOISY: s = x W_g^T + eps * softplus(x W_n^T) ("MoE sparse-compute acceleration",
+ * section 2.1, NoisyTopKGating; eps is supplied by the caller as an fp32 [T, E] tensor).  COSINE:
+ * s_e = cos(x P^T, emb_e) / cos_temperature (Tutel cosine_top; the projection P and the expert
+ * embeddings emb are inputs). */
+#define MOE_GATE_SOFTMAX 0
+#define MOE_GATE_NOISY   1
+#define MOE_GATE_COSINE  2
+
+/* Gate normalisation.  ALL: g = full softmax over all E scores, not renormalised (the top-1 layer of
+ * "Does the PyTorch-CUDA-v2.6 image support MoE", which multiplies by the max softmax weight).
+ * TOPK: softmax over the k selected scores (NoisyTopKGating's F.softmax(top_k_logits)). */
+#define MOE_GATE_NORM_ALL  0
+#define MOE_GATE_NORM_TOPK 1
+
+#define MOE_F32  0
+#define MOE_BF16 1
+
+/* ---- configuration -------------------------------------------------------------------------- */
+typedef struct moe_config {
+    int32_t tokens;                 /* T >= 0                                                        */
+    int32_t model_dim;              /* d, multiple of 64                                             */
+    int32_t hidden_size_per_expert; /* h, multiple of 64                                             */
+    int32_t num_experts;            /* E, 1..1024 (1..512 for the noisy gate)                        */
+    int32_t top_k;                  /* k, 1..min(E, 16)                                              */
+    int32_t capacity;               /* < 0: ceil(capacity_factor * T * k / E) evaluated in double,
+                                       left to right; >= 0: that capacity (T makes the layer dropless) */
+    double  capacity_factor;        /* > 0, used when capacity < 0                                   */
+    int32_t gate_type;              /* MOE_GATE_*                                                    */
+    int32_t gate_norm;              /* MOE_GATE_NORM_*                                               */
+    int32_t cos_dim;                /* cosine gate: projection width p, multiple of 4, 4..1024       */
+    int32_t dtype;                  /* MOE_F32 or MOE_BF16                                           */
+    double  cos_temperature;        /* cosine gate: scores are divided by this (> 0)                 */
+    int32_t flags;                  /* MOE_FLAG_* bits, 0 for the default path                       */
+    int32_t reserved;               /* must be 0                                                     */
+} moe_config;
+
+/* flags: MOE_FLAG_SIMT_FFN runs the expert FFN of a bf16 layer on CUDA cores instead of the tcgen05
+ * tensor-core kernel (a slow cross-check path); MOE_FLAG_UNFUSED_COMBINE makes moe_forward write
+ * per-row expert outputs and combine them in a separate gather pass even when k <= 2. */
+#define MOE_FLAG_SIMT_FFN         1
+#define MOE_FLAG_UNFUSED_COMBINE  2
+
+/* ---- sizes ------------------------------------------------------------------------------------ */
+/* Per-expert capacity C the dispatch step enforces, or -1 if the config is invalid. */
+int32_t moe_capacity(const moe_config* cfg);
+
+/* Upper bound on the number of dispatched rows: each expert's kept rows are padded to a multiple of
+ * 128, so rows <= min(T*k + 127*E, E*roundup(C,128)).  x_dispatched / row_token / row_gate /
+ * y_dispatched passed to moe_dispatch / moe_expert_ffn / moe_combine need this many rows.
+ * Returns -1 if the config is invalid. */
+int64_t moe_dispatch_rows(const moe_config* cfg);
+
+/* Bytes of device workspace that every entry point below accepts (one size for all of them).
+ * Returns 0 if the config is invalid.  The workspace needs no initialisation and may be reused by
+ * consecutive calls on one stream; calls running concurrently need separate workspaces. */
+size_t moe_workspace_size(const moe_config* cfg);
+
+/* ---- step 1+2: routing ------------------------------------------------------------------------ */
+/* Gate logits, scores, per-token top-k and gate weights.
+ *   x          [T, d] dtype          w_gate [E, d] dtype (all gate types except COSINE)
+ *   w_noise    [E, d] dtype          NOISY only, else NULL
+ *   noise_eps  [T, E] fp32           NOISY only, else NULL (the standard-normal draws)
+ *   proj       [cos_dim, d] dtype    COSINE only, else NULL
+ *   expert_emb [E, cos_dim] dtype    COSINE only, else NULL
+ * Outputs:
+ *   topk_idx   [T, k] int32          expert ids in rank order, best first; ties go to the lower id
+ *   topk_gate  [T, k] fp32           gate weight of each chosen expert (see MOE_GATE_NORM_*)
+ * Selection is made on the scores (before the softmax).  Scores are first computed in fp32; when two
+ * scores of a token are closer than the fp32 error bound of that token, the contenders are recomputed
+ * with a doubled-precision (float-float) dot product, so the chosen set and its order equal those of
+ * exact arithmetic except for differences below about 1e-12 of the score scale. */
+moe_status moe_route(const moe_config* cfg, const void* x, const void* w_gate, const void* w_noise,
+                     const float* noise_eps, const void* proj, const void* expert_emb,
+                     int32_t* topk_idx, float* topk_gate, void* stream);
+
+/* ---- step 3: capacity-limited dispatch -------------------------------------------------------- */
+/* Groups the (token, expert) pairs by expert ("first group the samples by their chosen expert, then
+ * run one batched matmul per group", intelliparadigm section 3.1) under a per-expert capacity C
+ * (Tutel capacity_factor; CANN MOELayer capacity_factor).  Slots are handed out in token order (for
+ * one expert, token t precedes token t+1; a token never picks an expert twice); a pair whose slot is
+ * >= C is dropped.  Outputs:
+ *   slot          [T, k] int32   slot of each pair in its expert's queue, -1 if dropped
+ *   expert_count  [E]    int32   pairs routed to each expert before the capacity limit
+ *   expert_offset [E+1]  int32   first dispatched row of each expert; expert e owns rows
+ *                                [off[e], off[e+1]), of which the first min(count[e], C) are real and
+ *                                the rest (up to a multiple of 128) are padding
+ *   row_token     [rows] int32   token of each dispatched row, -1 for padding rows
+ *   row_gate      [rows] fp32    gate weight of each dispatched row, 0 for padding rows
+ *   x_dispatched  [rows, d]      copy of x[row_token[r]] for every real row (padding rows untouched)
+ * rows = moe_dispatch_rows(cfg).  Deterministic: no result depends on thread scheduling. */
+moe_status moe_dispatch(const moe_config* cfg, const void* x, const int32_t* topk_idx,
+                        const float* topk_gate, int32_t* slot, int32_t* expert_count,
+                        int32_t* expert_offset, int32_t* row_token, float* row_gate,
+                        void* x_dispatched, void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---- steps 4+5: grouped expert FFN ------------------------------------------------------------ */
+/* For every real dispatched row r of expert e:  y_r = W2[e] GELU(W1[e] x_r + b1[e]) + b2[e], with
+ * GELU(z) = z/2 (1 + erf(z / sqrt 2)) (the expert of CANN's MOELayer example: Linear(d, 4d), GELU,
+ * Linear(4d, d); Tutel's 'ffn' expert type).  b1 / b2 may be NULL (no bias).
+ *   y_dispatched != NULL: y_dispatched [rows, d] fp32 receives y_r for each real row (padding rows
+ *                         are left untouched); `out` is ignored and may be NULL.
+ *   y_dispatched == NULL: the combine is fused into the second GEMM: out [T, d] fp32 is overwritten
+ *                         with sum_r row_gate[r] * y_r over the real rows of each token (0 for a
+ *                         token with none).  With top_k <= 2 the result is bitwise deterministic;
+ *                         with top_k > 2 the order of the fp32 additions may vary between runs.
+ * The hidden activations (bf16 for MOE_BF16, fp32 for MOE_F32) live in the workspace. */
+moe_status moe_expert_ffn(const moe_config* cfg, const void* x_dispatched,
+                          const int32_t* expert_offset, const int32_t* row_token,
+                          const float* row_gate, const void* w1, const void* b1, const void* w2,
+                          const void* b2, float* y_dispatched, float* out, void* workspace,
+                          size_t workspace_bytes, void* stream);
+
+/* ---- step 5 (unfused): combine ----------------------------------------------------------------- */
+/* out[t] = sum over j < k with slot[t,j] >= 0 of topk_gate[t,j] * y_dispatched[off[e] + slot[t,j]],
+ * e = topk_idx[t,j], summed in rank order j = 0..k-1 (deterministic); 0 for a token whose pairs were
+ * all dropped ("Output = sum_i g_i(x) E_i(x)", MoE on a single card, section 1.2).  out [T, d] fp32 is
+ * overwritten. */
+moe_status moe_combine(const moe_config* cfg, const float* y_dispatched, const int32_t* slot,
+                       const int32_t* expert_offset, const int32_t* topk_idx,
+                       const float* topk_gate, float* out, void* stream);
+
+/* ---- whole layer ------------------------------------------------------------------------------ */
+/* moe_route -> moe_dispatch -> moe_expert_ffn (+ fused or separate combine) on `stream`, with every
+ * intermediate in the workspace.  out [T, d] fp32 is overwritten.  expert_count (may be NULL)
+ * receives the per-expert pre-capacity counts.  The fused combine is used when top_k <= 2 and the
+ * gather combine otherwise, so the output is bitwise deterministic for every k. */
+moe_status moe_forward(const moe_config* cfg, const void* x, const void* w_gate,
+                       const void* w_noise, const float* noise_eps, const void* proj,
+                       const void* expert_emb, const void* w1, const void* b1, const void* w2,
+                       const void* b2, float* out, int32_t* expert_count, void* workspace,
+                       size_t workspace_bytes, void* stream);
+
+/* ---- diagnostics ------------------------------------------------------------------------------ */
+/* Synchronises `stream`, reads and clears the error word at the start of `workspace` and returns
+ * MOE_OK, MOE_ERR_DEVICE_CHECK or MOE_ERR_DEVICE_TIMEOUT.  If `info` is not NULL it receives a code
+ * saying which kernel recorded the error (0 if none). */
+moe_status moe_device_status(void* workspace, size_t workspace_bytes, int32_t* info, void* stream);
+
+/* Profiling hook.  With events != NULL (an array of `capacity` cudaEvent_t, each passed as void*),
+ * the library records events[0] on the launch stream before the first kernel it launches after this
+ * call, and events[i] right after the i-th such kernel, until `capacity` events are used; n kernels
+ * thus use n + 1 events and kernel i ran between events[i] and events[i+1].  moe_trace_count()
+ * returns how many events have been recorded.  events == NULL turns the hook off.  Not thread-safe;
+ * meant for benchmarks. */
+void    moe_trace_events(void** events, int32_t capacity);
+int32_t moe_trace_count(void);
+
+/* Number of kernels moe_forward launches for this config (for launch accounting), -1 if invalid. */
+int32_t moe_forward_launches(const moe_config* cfg);
+
+/* Human-readable name of a status code (static storage). */
+const char* moe_status_string(moe_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_B300_H */

@@ -1,0 +1,238 @@
+"""fp64 CPU oracle of the sparse MoE layer forward pass (ctypes wrapper around ``moe_oracle.c``).
+
+TEST INFRASTRUCTURE: only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline leg
+import this package.  It shares no code with ``mixture_experts_sparse_03_b300`` and imports nothing
+from it; the product path never calls it.
+
+The C file holds the arithmetic (one function per step, each citing the page it follows); this module
+only compiles it with gcc, marshals arrays and strings the steps together.  Tensors may be numpy
+float32 arrays or CPU torch tensors of dtype float32 or bfloat16 (bf16 is passed as its raw 16-bit
+pattern and widened exactly in C).
+
+Module-level functions use the oracle built from ``moe_oracle.c``; ``Oracle(path)`` binds another
+build of the same source (the mutation tests compile deliberately broken copies to check that the
+pins catch them).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+SOURCE = os.path.join(_HERE, "moe_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "_moe_oracle.so")
+
+GATE_SOFTMAX, GATE_NOISY, GATE_COSINE = 0, 1, 2
+NORM_ALL, NORM_TOPK = 0, 1
+F32, BF16 = 0, 1
+_GATE_CODES = {"softmax": GATE_SOFTMAX, "noisy": GATE_NOISY, "cosine": GATE_COSINE}
+_NORM_CODES = {"all": NORM_ALL, "topk": NORM_TOPK}
+
+
+def compile_source(src: str, out: str) -> str:
+    """gcc -O2 (no fast-math, no FMA contraction) a copy of the oracle source into a shared object."""
+    tmp = out + ".tmp%d" % os.getpid()
+    subprocess.run(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", "-o", tmp, src, "-lm"],
+                   check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def build(force: bool = False) -> str:
+    """Compile moe_oracle.c into _moe_oracle.so beside it (if missing or older than the source)."""
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(SOURCE):
+        compile_source(SOURCE, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _raw(t):
+    """(numpy array holding the exact bits, dtype code) for a float32 / bfloat16 tensor or array."""
+    if t is None:
+        return None, None
+    if hasattr(t, "detach"):  # torch tensor
+        import torch
+
+        t = t.detach().cpu().contiguous()
+        if t.dtype == torch.bfloat16:
+            return t.view(torch.int16).numpy(), BF16
+        if t.dtype == torch.float32:
+            return t.numpy(), F32
+        raise TypeError("oracle tensors must be float32 or bfloat16, got %s" % t.dtype)
+    a = np.ascontiguousarray(t)
+    if a.dtype == np.float32:
+        return a, F32
+    raise TypeError("oracle numpy arrays must be float32 (pass bf16 as a torch tensor), got %s" % a.dtype)
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _same_dtype(*pairs):
+    codes = {c for _, c in pairs if c is not None}
+    if len(codes) != 1:
+        raise TypeError("x and all weights must share one dtype")
+    return codes.pop()
+
+
+class Oracle:
+    """The oracle's steps, bound to one compiled copy of moe_oracle.c."""
+
+    def __init__(self, path: str):
+        lib = ctypes.CDLL(path)
+        P, I, D, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_double, ctypes.c_size_t
+        sigs = {
+            "oracle_gate_scores": ([I, I, I, I, I, D, I, P, P, P, P, P, P, P], None),
+            "oracle_topk": ([I, I, I, I, P, P, P], None),
+            "oracle_capacity": ([I, I, I, D, I], I),
+            "oracle_dispatch": ([I, I, I, I, P, P, P], None),
+            "oracle_expert": ([I, I, I, P, S, P, S, P, S, P, S, P, S, P], None),
+            "oracle_combine_tokens": ([I, I, I, I, P, I, P, P, P, P, P, P, P, P, P], None),
+        }
+        for name, (args, res) in sigs.items():
+            fn = getattr(lib, name)
+            fn.argtypes, fn.restype = args, res
+        self.lib = lib
+        self.path = path
+
+    def gate_scores(self, gate, x, w_gate=None, w_noise=None, eps=None, proj=None, emb=None, temperature=1.0):
+        """Step 1: selection scores [T, E] in float64."""
+        g = _GATE_CODES[gate]
+        xs = _raw(x)
+        wg, wn, pj, em = _raw(w_gate), _raw(w_noise), _raw(proj), _raw(emb)
+        dt = _same_dtype(xs, wg, wn, pj, em)
+        T, d = xs[0].shape
+        if g == GATE_COSINE:
+            p, E = pj[0].shape[0], em[0].shape[0]
+        else:
+            p, E = 0, wg[0].shape[0]
+        ep = None
+        if g == GATE_NOISY:
+            ep = eps.detach().cpu().numpy() if hasattr(eps, "detach") else eps
+            ep = np.ascontiguousarray(ep, dtype=np.float32)
+            assert ep.shape == (T, E)
+        out = np.empty((T, E), dtype=np.float64)
+        self.lib.oracle_gate_scores(g, T, d, E, p, float(temperature), dt, _ptr(xs[0]), _ptr(wg[0]),
+                                    _ptr(wn[0]), _ptr(ep), _ptr(pj[0]), _ptr(em[0]), _ptr(out))
+        return out
+
+    def topk(self, scores, k, norm):
+        """Step 2: (idx int32 [T, k] best first, gate float64 [T, k])."""
+        s = np.ascontiguousarray(scores, dtype=np.float64)
+        T, E = s.shape
+        idx = np.empty((T, k), dtype=np.int32)
+        gate = np.empty((T, k), dtype=np.float64)
+        self.lib.oracle_topk(T, E, k, _NORM_CODES[norm], _ptr(s), _ptr(idx), _ptr(gate))
+        return idx, gate
+
+    def capacity(self, T, E, k, capacity_factor, capacity=-1):
+        """Step 3a: the per-expert capacity C."""
+        return int(self.lib.oracle_capacity(T, E, k, float(capacity_factor), int(capacity)))
+
+    def dispatch(self, idx, E, C):
+        """Step 3b: (slot int32 [T, k] or -1 if dropped, count int32 [E] before the limit)."""
+        idx = np.ascontiguousarray(idx, dtype=np.int32)
+        T, k = idx.shape
+        slot = np.empty((T, k), dtype=np.int32)
+        count = np.empty((E,), dtype=np.int32)
+        self.lib.oracle_dispatch(T, E, k, int(C), _ptr(idx), _ptr(slot), _ptr(count))
+        return slot, count
+
+    def expert(self, x_row, w1_e, b1_e, w2_e, b2_e):
+        """Step 4 for one token and one expert: float64 [d].  w1_e [h, d], w2_e [d, h]."""
+        xs, a1, c1, a2, c2 = _raw(x_row), _raw(w1_e), _raw(b1_e), _raw(w2_e), _raw(b2_e)
+        dt = _same_dtype(xs, a1, c1, a2, c2)
+        h, d = a1[0].shape
+        y = np.empty((d,), dtype=np.float64)
+        self.lib.oracle_expert(d, h, dt, _ptr(xs[0]), 0, _ptr(a1[0]), 0, _ptr(c1[0]), 0, _ptr(a2[0]), 0,
+                               _ptr(c2[0]), 0, _ptr(y))
+        return y
+
+    def combine_tokens(self, tokens, x, idx, gate, slot, w1, b1, w2, b2):
+        """Steps 4+5 for the listed tokens: float64 [len(tokens), d]."""
+        xs, a1, c1, a2, c2 = _raw(x), _raw(w1), _raw(b1), _raw(w2), _raw(b2)
+        dt = _same_dtype(xs, a1, c1, a2, c2)
+        E, h, d = a1[0].shape
+        toks = np.ascontiguousarray(tokens, dtype=np.int32)
+        idx = np.ascontiguousarray(idx, dtype=np.int32)
+        gate = np.ascontiguousarray(gate, dtype=np.float64)
+        slot = np.ascontiguousarray(slot, dtype=np.int32)
+        k = idx.shape[1]
+        out = np.empty((len(toks), d), dtype=np.float64)
+        self.lib.oracle_combine_tokens(d, h, k, dt, _ptr(toks), len(toks), _ptr(xs[0]), _ptr(idx),
+                                       _ptr(gate), _ptr(slot), _ptr(a1[0]), _ptr(c1[0]), _ptr(a2[0]),
+                                       _ptr(c2[0]), _ptr(out))
+        return out
+
+    def route(self, gate, k, norm, x, w_gate=None, w_noise=None, eps=None, proj=None, emb=None,
+              temperature=1.0):
+        """Steps 1+2: (scores, idx, gate)."""
+        s = self.gate_scores(gate, x, w_gate, w_noise, eps, proj, emb, temperature)
+        idx, g = self.topk(s, k, norm)
+        return s, idx, g
+
+    def forward(self, spec, t, tokens=None):
+        """Whole layer.  ``spec``: mapping with gate, norm, k, E, capacity_factor, capacity,
+        temperature; ``t``: mapping of tensors x, w_gate, w_noise, eps, proj, emb, w1, b1, w2, b2
+        (absent -> None).  Returns a dict with scores, idx, gate, C, slot, count, tokens and out
+        ([len(tokens), d])."""
+        s, idx, g = self.route(spec["gate"], spec["k"], spec["norm"], t.get("x"), t.get("w_gate"),
+                               t.get("w_noise"), t.get("eps"), t.get("proj"), t.get("emb"),
+                               spec.get("temperature", 1.0))
+        T = s.shape[0]
+        C = self.capacity(T, spec["E"], spec["k"], spec.get("capacity_factor", 1.0), spec.get("capacity", -1))
+        slot, count = self.dispatch(idx, spec["E"], C)
+        if tokens is None:
+            tokens = np.arange(T, dtype=np.int32)
+        out = self.combine_tokens(tokens, t.get("x"), idx, g, slot, t.get("w1"), t.get("b1"), t.get("w2"),
+                                  t.get("b2"))
+        return dict(scores=s, idx=idx, gate=g, C=C, slot=slot, count=count, tokens=np.asarray(tokens), out=out)
+
+
+_lock = threading.Lock()
+_default = None
+
+
+def default() -> Oracle:
+    """The oracle compiled from moe_oracle.c (built on first use)."""
+    global _default
+    with _lock:
+        if _default is None:
+            _default = Oracle(build())
+    return _default
+
+
+def gate_scores(*a, **kw):
+    return default().gate_scores(*a, **kw)
+
+
+def topk(*a, **kw):
+    return default().topk(*a, **kw)
+
+
+def capacity(*a, **kw):
+    return default().capacity(*a, **kw)
+
+
+def dispatch(*a, **kw):
+    return default().dispatch(*a, **kw)
+
+
+def expert(*a, **kw):
+    return default().expert(*a, **kw)
+
+
+def combine_tokens(*a, **kw):
+    return default().combine_tokens(*a, **kw)
+
+
+def route(*a, **kw):
+    return default().route(*a, **kw)
+
+
+def forward(*a, **kw):
+    return default().forward(*a, **kw)

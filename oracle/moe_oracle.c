@@ -1,0 +1,218 @@
+/*
+ * moe_oracle.c -- plain, slow, single-threaded fp64 reference of the sparse MoE layer forward pass.
+ *
+ * TEST INFRASTRUCTURE.  Only the tests, the smoke check and the benchmark's CPU-baseline leg use it.
+ * It shares no code, header, table or constant with the CUDA library and includes nothing from it.
+ *
+ * Every value is read from the caller's fp32 or bf16 buffers and widened exactly to double; all
+ * arithmetic is double precision, in loops, with no BLAS, threads, SIMD intrinsics or reordering
+ * beyond what each function's definition states.
+ *
+ * The steps follow the pages in order:
+ *   1. gate scores   -- "MoE sparse-compute acceleration" section 2.1 (NoisyTopKGating: clean and noise
+ *                       linear maps without bias, noise scaled by softplus); intelliparadigm section
+ *                       2.1 ("a single linear layer followed by Softmax"); Tutel guide, gate types
+ *                       top / cosine_top.  The cosine form cos(x P, e_j) / temperature is the reading
+ *                       the workload definition fixes, since the pages give no formula for it.
+ *   2. top-k + gates -- NoisyTopKGating: topk of the logits, softmax over the k selected; the top-1
+ *                       MOELayer of "Does the PyTorch-CUDA-v2.6 image support MoE": softmax over all
+ *                       experts, the max weight multiplies the output.
+ *   3. dispatch      -- intelliparadigm section 3.1 (group tokens by chosen expert); Tutel guide
+ *                       capacity_factor (1.2 allows 120 % of an expert's share); overflow dropped.
+ *   4. expert FFN    -- CANN MOELayer example: Linear(d, 4d) -> GELU -> Linear(4d, d).
+ *   5. combine       -- "MoE on a single card" section 1.2: Output = sum_i g_i(x) E_i(x).
+ *
+ * Build: gcc -O2 -ffp-contract=off -fPIC -shared moe_oracle.c -lm  (oracle/__init__.py does this).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define OR_F32 0
+#define OR_BF16 1
+
+#define GATE_SOFTMAX 0
+#define GATE_NOISY 1
+#define GATE_COSINE 2
+
+#define NORM_ALL 0
+#define NORM_TOPK 1
+
+/* Exact widening of element i of a fp32 or bf16 buffer.  A bf16 value is the upper half of the
+ * fp32 with the same sign, exponent and leading 7 mantissa bits. */
+static double elem(const void *base, size_t i, int dtype)
+{
+    if (dtype == OR_BF16) {
+        uint32_t bits = (uint32_t)((const uint16_t *)base)[i] << 16;
+        float f;
+        memcpy(&f, &bits, sizeof f);
+        return (double)f;
+    }
+    return (double)((const float *)base)[i];
+}
+
+/* sum_i a[i] * b[i], i = 0..n-1, accumulated left to right in double. */
+static double dot_rows(const void *a, size_t a_off, const void *b, size_t b_off, int n, int dtype)
+{
+    double s = 0.0;
+    for (int i = 0; i < n; ++i)
+        s += elem(a, a_off + (size_t)i, dtype) * elem(b, b_off + (size_t)i, dtype);
+    return s;
+}
+
+static double softplus(double z) { return log1p(exp(z)); }
+
+static double gelu_erf(double z) { return 0.5 * z * (1.0 + erf(z / sqrt(2.0))); }
+
+/* ---- step 1: selection scores s[t][e] ------------------------------------------------------------
+ * SOFTMAX: s = x . W_g[e]
+ * NOISY:   s = x . W_g[e] + eps[t][e] * softplus(x . W_n[e])
+ * COSINE:  u = P x (u_j = x . P[j], j < p);  s = (u . emb[e]) / (max(|u|,1e-12) max(|emb[e]|,1e-12)) / temp
+ */
+void oracle_gate_scores(int gate_type, int T, int d, int E, int p, double temperature, int dtype,
+                        const void *x, const void *w_gate, const void *w_noise, const float *eps,
+                        const void *proj, const void *emb, double *scores)
+{
+    double *u = NULL;
+    if (gate_type == GATE_COSINE)
+        u = (double *)malloc(sizeof(double) * (size_t)(p > 0 ? p : 1));
+    for (int t = 0; t < T; ++t) {
+        size_t xo = (size_t)t * (size_t)d;
+        if (gate_type == GATE_COSINE) {
+            double nu2 = 0.0;
+            for (int j = 0; j < p; ++j) {
+                u[j] = dot_rows(x, xo, proj, (size_t)j * (size_t)d, d, dtype);
+                nu2 += u[j] * u[j];
+            }
+            double nu = sqrt(nu2);
+            if (nu < 1e-12) nu = 1e-12;
+            for (int e = 0; e < E; ++e) {
+                double num = 0.0, ne2 = 0.0;
+                for (int j = 0; j < p; ++j) {
+                    double ej = elem(emb, (size_t)e * (size_t)p + (size_t)j, dtype);
+                    num += u[j] * ej;
+                    ne2 += ej * ej;
+                }
+                double ne = sqrt(ne2);
+                if (ne < 1e-12) ne = 1e-12;
+                scores[(size_t)t * E + e] = num / (nu * ne) / temperature;
+            }
+        } else {
+            for (int e = 0; e < E; ++e) {
+                double s = dot_rows(x, xo, w_gate, (size_t)e * (size_t)d, d, dtype);
+                if (gate_type == GATE_NOISY) {
+                    double noise = dot_rows(x, xo, w_noise, (size_t)e * (size_t)d, d, dtype);
+                    s += (double)eps[(size_t)t * E + e] * softplus(noise);
+                }
+                scores[(size_t)t * E + e] = s;
+            }
+        }
+    }
+    free(u);
+}
+
+/* ---- step 2: top-k by score, ties to the lower expert id, and the gate weights -------------------
+ * k rounds of argmax over the experts not yet chosen; a later expert replaces the running best only
+ * if its score is strictly greater, so equal scores keep the lower id.  With m the best score:
+ *   NORM_ALL:  g_j = exp(s_j - m) / sum_{all e} exp(s_e - m)
+ *   NORM_TOPK: g_j = exp(s_j - m) / sum_{chosen e} exp(s_e - m)
+ */
+void oracle_topk(int T, int E, int k, int norm, const double *scores, int32_t *idx, double *gate)
+{
+    char *taken = (char *)malloc((size_t)(E > 0 ? E : 1));
+    for (int t = 0; t < T; ++t) {
+        const double *s = scores + (size_t)t * E;
+        memset(taken, 0, (size_t)E);
+        for (int j = 0; j < k; ++j) {
+            int best = -1;
+            for (int e = 0; e < E; ++e) {
+                if (taken[e]) continue;
+                if (best < 0 || s[e] > s[best]) best = e;
+            }
+            taken[best] = 1;
+            idx[(size_t)t * k + j] = best;
+        }
+        double m = s[idx[(size_t)t * k]];
+        double den = 0.0;
+        if (norm == NORM_ALL) {
+            for (int e = 0; e < E; ++e) den += exp(s[e] - m);
+        } else {
+            for (int j = 0; j < k; ++j) den += exp(s[idx[(size_t)t * k + j]] - m);
+        }
+        for (int j = 0; j < k; ++j)
+            gate[(size_t)t * k + j] = exp(s[idx[(size_t)t * k + j]] - m) / den;
+    }
+    free(taken);
+}
+
+/* ---- step 3: capacity ----------------------------------------------------------------------------
+ * C = ceil(capacity_factor * T * k / E), the product and quotient evaluated in double, left to right;
+ * an explicit capacity >= 0 overrides it. */
+int oracle_capacity(int T, int E, int k, double capacity_factor, int capacity)
+{
+    if (capacity >= 0) return capacity;
+    return (int)ceil(capacity_factor * (double)T * (double)k / (double)E);
+}
+
+/* Walk the pairs in token order (t = 0..T-1, then rank j = 0..k-1).  Each pair takes the next free
+ * position of its expert's queue; the pair is kept if that position is < C, else dropped (slot -1).
+ * count[e] is the number of pairs routed to e before the limit. */
+void oracle_dispatch(int T, int E, int k, int C, const int32_t *idx, int32_t *slot, int32_t *count)
+{
+    for (int e = 0; e < E; ++e) count[e] = 0;
+    for (int t = 0; t < T; ++t) {
+        for (int j = 0; j < k; ++j) {
+            int e = idx[(size_t)t * k + j];
+            int pos = count[e]++;
+            slot[(size_t)t * k + j] = pos < C ? pos : -1;
+        }
+    }
+}
+
+/* ---- step 4: one expert on one token ------------------------------------------------------------
+ * y = W2 GELU(W1 x + b1) + b2, W1 [h, d], W2 [d, h] (rows = output features).  b1 / b2 may be NULL. */
+void oracle_expert(int d, int h, int dtype, const void *x, size_t x_off, const void *w1,
+                   size_t w1_off, const void *b1, size_t b1_off, const void *w2, size_t w2_off,
+                   const void *b2, size_t b2_off, double *y)
+{
+    double *a = (double *)malloc(sizeof(double) * (size_t)h);
+    for (int n = 0; n < h; ++n) {
+        double z = dot_rows(x, x_off, w1, w1_off + (size_t)n * (size_t)d, d, dtype);
+        if (b1) z += elem(b1, b1_off + (size_t)n, dtype);
+        a[n] = gelu_erf(z);
+    }
+    for (int n = 0; n < d; ++n) {
+        double z = 0.0;
+        for (int i = 0; i < h; ++i)
+            z += a[i] * elem(w2, w2_off + (size_t)n * (size_t)h + (size_t)i, dtype);
+        if (b2) z += elem(b2, b2_off + (size_t)n, dtype);
+        y[n] = z;
+    }
+    free(a);
+}
+
+/* ---- step 5: combine, for a list of tokens -------------------------------------------------------
+ * out[i] = sum over ranks j of token tokens[i] with slot >= 0 of gate[t][j] * expert_{idx[t][j]}(x_t);
+ * a token whose pairs were all dropped gets 0.  out is [ntok, d]. */
+void oracle_combine_tokens(int d, int h, int k, int dtype, const int32_t *tokens, int ntok,
+                           const void *x, const int32_t *idx, const double *gate,
+                           const int32_t *slot, const void *w1, const void *b1, const void *w2,
+                           const void *b2, double *out)
+{
+    double *y = (double *)malloc(sizeof(double) * (size_t)d);
+    for (int i = 0; i < ntok; ++i) {
+        int t = tokens[i];
+        double *o = out + (size_t)i * (size_t)d;
+        for (int n = 0; n < d; ++n) o[n] = 0.0;
+        for (int j = 0; j < k; ++j) {
+            if (slot[(size_t)t * k + j] < 0) continue;
+            size_t e = (size_t)idx[(size_t)t * k + j];
+            oracle_expert(d, h, dtype, x, (size_t)t * (size_t)d, w1, e * (size_t)h * (size_t)d, b1,
+                          e * (size_t)h, w2, e * (size_t)d * (size_t)h, b2, e * (size_t)d, y);
+            double g = gate[(size_t)t * k + j];
+            for (int n = 0; n < d; ++n) o[n] += g * y[n];
+        }
+    }
+    free(y);
+}

@@ -1,0 +1,304 @@
+"""Pins of the fp64 oracle against facts that do not come from the oracle itself.
+
+Each ``pin_*`` function takes an ``oracle.Oracle`` and raises AssertionError if the oracle disagrees
+with: a hand-worked case (tests/golden/hand_worked.json), a library routine applied to a special case
+(torch / numpy / scipy in float64), an invariant the definition implies, or a second, dense
+formulation of the whole layer (``dense_layer`` below: every expert on every token, masked).
+
+They are run against the real oracle (test_oracle_pins.py) and against deliberately broken copies of
+its source (test_oracle_mutants.py), where at least one pin must fail for every planted mistake.
+"""
+from __future__ import annotations
+
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import torch
+import torch.nn.functional as F
+
+from mixture_experts_sparse_03_b300.inputs import make_inputs, small_workload
+
+GOLDEN = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "hand_worked.json")))
+
+
+def _t(a, dtype=torch.float32):
+    return torch.tensor(a, dtype=dtype)
+
+
+def _f64(t):
+    return None if t is None else t.detach().cpu().to(torch.float64)
+
+
+# ---------------------------------------------------------------- a second formulation of the layer
+def dense_layer(wl, t):
+    """The whole layer written differently from the oracle: scores by matrix products, top-k by a
+    stable sort, capacity by a cumulative count per expert, every expert evaluated on every token with
+    torch's own Linear and exact GELU, and the result masked.  float64 throughout."""
+    X = _f64(t["x"])
+    T = X.shape[0]
+    if wl.gate == "softmax":
+        S = X @ _f64(t["w_gate"]).T
+    elif wl.gate == "noisy":
+        S = X @ _f64(t["w_gate"]).T + t["eps"].to(torch.float64) * torch.from_numpy(
+            np.logaddexp(0.0, (X @ _f64(t["w_noise"]).T).numpy()))
+    else:
+        U = X @ _f64(t["proj"]).T
+        S = F.cosine_similarity(U[:, None, :], _f64(t["emb"])[None, :, :], dim=-1, eps=1e-12) / wl.temperature
+    S = S.numpy()
+    E, k = wl.E, wl.k
+    # stable sort on -score keeps the lower expert id first among equal scores
+    order = np.argsort(-S, axis=1, kind="stable")[:, :k].astype(np.int32)
+    if wl.norm == "all":
+        P = torch.softmax(torch.from_numpy(S), dim=1).numpy()
+        gate = np.take_along_axis(P, order, axis=1)
+    else:
+        chosen = np.take_along_axis(S, order, axis=1)
+        gate = torch.softmax(torch.from_numpy(chosen), dim=1).numpy()
+    C = wl.capacity if wl.capacity >= 0 else math.ceil(wl.capacity_factor * T * k / E)
+    # position of pair (t, j) in its expert's queue = pairs of earlier tokens with that expert
+    onehot = np.zeros((T, E), dtype=np.int64)
+    for j in range(k):
+        onehot[np.arange(T), order[:, j]] += 1
+    before = np.cumsum(onehot, axis=0) - onehot
+    pos = np.take_along_axis(before, order, axis=1)
+    slot = np.where(pos < C, pos, -1).astype(np.int32)
+    count = onehot.sum(axis=0).astype(np.int32)
+    W1, W2 = _f64(t["w1"]), _f64(t["w2"])
+    b1 = _f64(t["b1"]) if t.get("b1") is not None else torch.zeros(E, W1.shape[1], dtype=torch.float64)
+    b2 = _f64(t["b2"]) if t.get("b2") is not None else torch.zeros(E, W2.shape[1], dtype=torch.float64)
+    Y = torch.stack([F.linear(F.gelu(F.linear(X, W1[e], b1[e]), approximate="none"), W2[e], b2[e])
+                     for e in range(E)])  # [E, T, d]
+    out = torch.zeros_like(X)
+    for j in range(k):
+        keep = torch.from_numpy(slot[:, j] >= 0)
+        ye = Y[torch.from_numpy(order[:, j]).long(), torch.arange(T)]
+        out += torch.where(keep[:, None], torch.from_numpy(gate[:, j])[:, None] * ye, torch.zeros_like(ye))
+    return dict(scores=S, idx=order, gate=gate, C=C, slot=slot, count=count, out=out.numpy())
+
+
+# ------------------------------------------------------------------------------------------- pins
+def pin_softmax_gate_hand(o):
+    g = GOLDEN["softmax_gate"]
+    s, idx, gate = o.route("softmax", 2, "topk", _t(g["x"]), _t(g["w_gate"]))
+    assert np.array_equal(s, np.array(g["scores"]))
+    assert np.array_equal(idx, np.array(g["top2_idx"]))
+    assert np.allclose(gate, np.array(g["top2_gate"]), rtol=1e-15, atol=0)
+    # the same data in bf16 (every value is exact in bf16)
+    s2 = o.gate_scores("softmax", _t(g["x"], torch.bfloat16), _t(g["w_gate"], torch.bfloat16))
+    assert np.array_equal(s2, s)
+
+
+def pin_full_softmax_top1_hand(o):
+    g = GOLDEN["full_softmax_top1"]
+    idx, gate = o.topk(np.array(g["scores"]), 1, "all")
+    assert np.array_equal(idx, np.array(g["idx"]))
+    assert abs(gate[0, 0] - 0.75) < 1e-15
+
+
+def pin_cosine_gate_hand(o):
+    g = GOLDEN["cosine_gate"]
+    s = o.gate_scores("cosine", _t(g["x"]), proj=_t(g["proj"]), emb=_t(g["emb"]), temperature=g["temperature"])
+    want = np.array(g["cosines"]) / g["temperature"]
+    assert np.allclose(s, want, rtol=1e-14, atol=1e-14)
+
+
+def pin_noisy_gate_hand(o):
+    g = GOLDEN["noisy_gate_zero_noise_weights"]
+    s = o.gate_scores("noisy", _t(g["x"]), _t(g["w_gate"]), _t(g["w_noise"]), eps=np.array(g["eps"], np.float32))
+    assert np.allclose(s, np.array(g["scores"]), rtol=1e-15, atol=0)
+
+
+def pin_capacity_values(o):
+    for c in GOLDEN["capacity"]["cases"]:
+        assert o.capacity(c["T"], c["E"], c["k"], c["cf"], c["capacity"]) == c["C"], c
+
+
+def pin_dispatch_hand(o):
+    for c in GOLDEN["dispatch"]["cases"]:
+        slot, count = o.dispatch(np.array(c["idx"], np.int32), c["E"], c["C"])
+        assert np.array_equal(slot, np.array(c["slot"])), (slot, c)
+        assert np.array_equal(count, np.array(c["count"])), (count, c)
+
+
+def pin_gelu_normal_cdf(o):
+    """Identity weights make the expert return GELU(x) itself; GELU(z) = z Phi(z) with Phi from a table."""
+    g = GOLDEN["gelu_normal_cdf"]
+    z = np.array(g["z"])
+    n = len(z)
+    I = torch.eye(n, dtype=torch.float32)
+    y = o.expert(_t(z.tolist()), I, None, I, None)
+    assert np.allclose(y, z * np.array(g["phi"]), rtol=1e-14, atol=1e-300)
+    big = o.expert(_t([10.0, -10.0]), torch.eye(2), None, torch.eye(2), None)
+    assert abs(big[0] - 10.0) < 1e-20 and abs(big[1]) < 1e-20
+
+
+def pin_topk_bruteforce(o):
+    """Every k on small E, against a stable sort by (-score, id); scores quantised to force ties."""
+    rng = np.random.default_rng(5)
+    for E in range(1, 7):
+        S = np.round(rng.normal(size=(40, E)) * 2) / 2  # many exact ties
+        for k in range(1, E + 1):
+            for norm in ("all", "topk"):
+                idx, gate = o.topk(S, k, norm)
+                want = np.array([sorted(range(E), key=lambda e: (-S[t, e], e))[:k] for t in range(40)])
+                assert np.array_equal(idx, want), (E, k)
+                assert np.all(gate > 0)
+                if norm == "topk" or k == E:
+                    assert np.allclose(gate.sum(1), 1.0, rtol=0, atol=1e-12)
+                if norm == "all":
+                    full = torch.softmax(torch.from_numpy(S), dim=1).numpy()
+                    assert np.allclose(gate, np.take_along_axis(full, want, axis=1), rtol=1e-13, atol=0)
+
+
+def pin_duplicate_rows_tie(o):
+    """Experts with identical gate rows tie exactly: the lower id is chosen first."""
+    x = torch.randn(16, 8, generator=torch.Generator().manual_seed(2)).to(torch.bfloat16)
+    w = torch.randn(3, 8, generator=torch.Generator().manual_seed(3)).to(torch.bfloat16)
+    w = torch.stack([w[0], w[1], w[1], w[2], w[0]])  # 1 == 2 and 0 == 4
+    s, idx, _ = o.route("softmax", 5, "topk", x, w)
+    for t in range(16):
+        r = list(idx[t])
+        assert r.index(1) < r.index(2) and r.index(0) < r.index(4)
+        assert s[t, 1] == s[t, 2] and s[t, 0] == s[t, 4]
+
+
+def pin_noisy_reductions(o):
+    """eps = 0 gives the clean logits; W_n = 0 adds exactly eps ln 2; random case vs numpy logaddexp."""
+    g = torch.Generator().manual_seed(7)
+    x = torch.randn(12, 16, generator=g).to(torch.bfloat16)
+    wg = (torch.randn(5, 16, generator=g) / 4).to(torch.bfloat16)
+    wn = (torch.randn(5, 16, generator=g) / 4).to(torch.bfloat16)
+    eps = torch.randn(12, 5, generator=g)
+    clean = o.gate_scores("softmax", x, wg)
+    assert np.array_equal(o.gate_scores("noisy", x, wg, wn, eps=torch.zeros(12, 5)), clean)
+    s0 = o.gate_scores("noisy", x, wg, torch.zeros_like(wn), eps=eps)
+    assert np.allclose(s0, clean + eps.double().numpy() * math.log(2.0), rtol=1e-15, atol=1e-15)
+    s = o.gate_scores("noisy", x, wg, wn, eps=eps)
+    want = clean + eps.double().numpy() * np.logaddexp(0.0, (_f64(x) @ _f64(wn).T).numpy())
+    assert np.allclose(s, want, rtol=1e-13, atol=1e-14)
+
+
+def pin_cosine_invariants(o):
+    """Scaling P and the embeddings by powers of two changes nothing (exactly); random case vs torch's
+    cosine_similarity; orthogonal and opposite embeddings give 0 and -1/temperature."""
+    g = torch.Generator().manual_seed(9)
+    x = torch.randn(10, 32, generator=g).to(torch.bfloat16)
+    P = (torch.randn(8, 32, generator=g) / 6).to(torch.bfloat16)
+    em = (torch.randn(6, 8, generator=g) / 3).to(torch.bfloat16)
+    s = o.gate_scores("cosine", x, proj=P, emb=em, temperature=0.07)
+    s2 = o.gate_scores("cosine", x, proj=P * 2, emb=em * 4, temperature=0.07)
+    assert np.array_equal(s, s2)
+    U = _f64(x) @ _f64(P).T
+    want = F.cosine_similarity(U[:, None, :], _f64(em)[None], dim=-1).numpy() / 0.07
+    assert np.allclose(s, want, rtol=1e-12, atol=1e-12)
+    assert np.all(np.abs(s) <= 1 / 0.07 + 1e-12)
+
+
+def pin_dispatch_properties(o):
+    """Random routings: counts are the routing histogram; each expert keeps exactly its first C tokens
+    in token order, with slots 0..kept-1 in that order; kept + dropped = T k; reversing the token order
+    keeps each expert's last C tokens instead."""
+    rng = np.random.default_rng(3)
+    for (T, E, k, C) in [(50, 4, 1, 9), (64, 6, 2, 15), (33, 5, 3, 20), (20, 3, 3, 20), (40, 8, 2, 1)]:
+        idx = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+        slot, count = o.dispatch(idx, E, C)
+        assert np.array_equal(count, np.bincount(idx.ravel(), minlength=E))
+        assert (slot >= 0).sum() + (slot < 0).sum() == T * k
+        for e in range(E):
+            toks = np.nonzero((idx == e).any(1))[0]  # ascending token order
+            kept = toks[:C]
+            got = [(t, slot[t][list(idx[t]).index(e)]) for t in toks]
+            assert [t for t, s_ in got if s_ >= 0] == list(kept)
+            assert [s_ for t, s_ in got if s_ >= 0] == list(range(len(kept)))
+        rslot, _ = o.dispatch(idx[::-1].copy(), E, C)
+        for e in range(E):
+            toks = np.nonzero((idx == e).any(1))[0]
+            want_kept = set(toks[::-1][:C])
+            got_kept = {T - 1 - r for r in range(T) for j in range(k) if idx[::-1][r][j] == e and rslot[r][j] >= 0}
+            assert got_kept == want_kept
+
+
+def pin_expert_vs_torch(o):
+    g = torch.Generator().manual_seed(4)
+    for dt in (torch.float32, torch.bfloat16):
+        x = torch.randn(24, generator=g).to(dt)
+        w1 = (torch.randn(40, 24, generator=g) / 5).to(dt)
+        b1 = torch.randn(40, generator=g).to(dt)
+        w2 = (torch.randn(24, 40, generator=g) / 6).to(dt)
+        b2 = torch.randn(24, generator=g).to(dt)
+        y = o.expert(x, w1, b1, w2, b2)
+        want = F.linear(F.gelu(F.linear(_f64(x), _f64(w1), _f64(b1)), approximate="none"), _f64(w2), _f64(b2))
+        assert np.allclose(y, want.numpy(), rtol=1e-13, atol=1e-13)
+        y0 = o.expert(x, w1, None, w2, None)
+        want0 = F.linear(F.gelu(F.linear(_f64(x), _f64(w1)), approximate="none"), _f64(w2))
+        assert np.allclose(y0, want0.numpy(), rtol=1e-13, atol=1e-13)
+
+
+def pin_single_expert_is_dense_ffn(o):
+    """E = 1, k = 1, capacity >= T: the layer is the dense Linear-GELU-Linear (gate weight 1)."""
+    wl = small_workload(T=9, d=16, h=24, E=1, k=1, norm="all", capacity_factor=1.0, dtype="f32", bias="normal")
+    t = make_inputs(wl)
+    r = o.forward(wl.spec(), t)
+    want = F.linear(F.gelu(F.linear(_f64(t["x"]), _f64(t["w1"][0]), _f64(t["b1"][0])), approximate="none"),
+                    _f64(t["w2"][0]), _f64(t["b2"][0]))
+    assert np.allclose(r["gate"], 1.0, rtol=0, atol=1e-15)
+    assert np.allclose(r["out"], want.numpy(), rtol=1e-13, atol=1e-13)
+
+
+def pin_naive_top1_layer(o):
+    """The top-1 layer as the 'PyTorch-CUDA-v2.6' page writes it (gate Linear without bias here,
+    softmax, max -> weight and index, each expert on its masked tokens, output times the weight), in
+    torch float64, equals the oracle with a capacity that drops nothing."""
+    wl = small_workload(T=40, d=16, h=32, E=4, k=1, norm="all", capacity=40, dtype="f32", bias="normal")
+    t = make_inputs(wl)
+    X = _f64(t["x"])
+    weights = torch.softmax(X @ _f64(t["w_gate"]).T, dim=-1)
+    top1_w, top1_i = weights.max(dim=-1)
+    final = torch.zeros_like(X)
+    for i in range(wl.E):
+        mask = top1_i == i
+        if mask.any():
+            final[mask] = F.linear(F.gelu(F.linear(X[mask], _f64(t["w1"][i]), _f64(t["b1"][i])), approximate="none"),
+                                   _f64(t["w2"][i]), _f64(t["b2"][i]))
+    final = final * top1_w.unsqueeze(-1)
+    r = o.forward(wl.spec(), t)
+    assert np.allclose(r["out"], final.numpy(), rtol=1e-12, atol=1e-13)
+
+
+def pin_layer_vs_dense_formulation(o):
+    """Whole layer on small workloads of every gate type, both dtypes, several k, with and without
+    drops, against ``dense_layer``."""
+    cases = [
+        small_workload(T=37, d=16, h=32, E=4, k=1, norm="all", dtype="f32", capacity_factor=1.0),
+        small_workload(T=41, d=32, h=16, E=5, k=2, dtype="bf16", capacity_factor=0.8),
+        small_workload(T=30, d=16, h=16, E=6, k=3, dtype="bf16", capacity_factor=2.0, bias="none"),
+        small_workload(T=33, d=16, h=32, E=5, k=2, gate="noisy", dtype="bf16", capacity_factor=0.9),
+        small_workload(T=29, d=32, h=16, E=4, k=2, gate="cosine", cos_dim=8, dtype="bf16", capacity_factor=1.0,
+                       x_dist="clusters"),
+        small_workload(T=25, d=16, h=16, E=3, k=3, dtype="f32", capacity=25, norm="all"),
+    ]
+    for wl in cases:
+        t = make_inputs(wl)
+        r = o.forward(wl.spec(), t)
+        ref = dense_layer(wl, t)
+        assert r["C"] == ref["C"]
+        assert np.allclose(r["scores"], ref["scores"], rtol=1e-12, atol=1e-12), wl
+        assert np.array_equal(r["idx"], ref["idx"]), wl
+        assert np.allclose(r["gate"], ref["gate"], rtol=1e-12, atol=1e-15), wl
+        assert np.array_equal(r["slot"], ref["slot"]), wl
+        assert np.array_equal(r["count"], ref["count"]), wl
+        scale = np.abs(ref["out"]).max()
+        assert np.allclose(r["out"], ref["out"], rtol=1e-11, atol=1e-12 * scale), wl
+
+
+def pin_drops_zero_output(o):
+    """A token whose pairs are all dropped outputs exactly 0; with C = 0 every token does."""
+    wl = small_workload(T=20, d=16, h=16, E=2, k=1, capacity=0, dtype="f32")
+    r = o.forward(wl.spec(), make_inputs(wl))
+    assert np.all(r["slot"] == -1) and np.all(r["out"] == 0.0)
+
+
+ALL_PINS = [v for k_, v in sorted(globals().items()) if k_.startswith("pin_") and callable(v)]

@@ -1,0 +1,56 @@
+"""Plant plausible mistakes in copies of the oracle's C source (on the CPU, in a temp directory) and
+check that at least one pin catches each: a dropped term, a wrong sign, a wrong index, a transposed
+operand, a flipped tie rule, an off-by-one.  The real oracle is untouched."""
+import os
+
+import pytest
+
+import oracle
+from tests.oracle_pins import ALL_PINS
+
+# (name, text in moe_oracle.c, replacement)
+MUTANTS = [
+    ("noisy_sign", "s += (double)eps[(size_t)t * E + e] * softplus(noise);",
+     "s -= (double)eps[(size_t)t * E + e] * softplus(noise);"),
+    ("softplus_drops_log1p", "return log1p(exp(z));", "return exp(z);"),
+    ("gelu_missing_sqrt2", "erf(z / sqrt(2.0))", "erf(z)"),
+    ("tie_to_higher_id", "if (best < 0 || s[e] > s[best]) best = e;", "if (best < 0 || s[e] >= s[best]) best = e;"),
+    ("topk_norm_over_all", "if (norm == NORM_ALL) {", "if (1) {"),
+    ("all_norm_over_topk", "for (int e = 0; e < E; ++e) den += exp(s[e] - m);",
+     "for (int e = 0; e < k; ++e) den += exp(s[idx[(size_t)t * k + e]] - m);"),
+    ("capacity_floor", "return (int)ceil(", "return (int)floor("),
+    ("keep_one_too_many", "slot[(size_t)t * k + j] = pos < C ? pos : -1;", "slot[(size_t)t * k + j] = pos <= C ? pos : -1;"),
+    ("rank_major_slots", "    for (int t = 0; t < T; ++t) {\n        for (int j = 0; j < k; ++j) {\n            int e = idx",
+     "    for (int j = 0; j < k; ++j) {\n        for (int t = 0; t < T; ++t) {\n            int e = idx"),
+    ("count_only_kept", "int pos = count[e]++;", "int pos = count[e]; if (pos < C) count[e]++;"),
+    ("cosine_no_emb_norm", "if (ne < 1e-12) ne = 1e-12;", "ne = 1.0;"),
+    ("cosine_times_temperature", "num / (nu * ne) / temperature", "num / (nu * ne) * temperature"),
+    ("cosine_emb_transposed", "elem(emb, (size_t)e * (size_t)p + (size_t)j, dtype)",
+     "elem(emb, (size_t)j * (size_t)E + (size_t)e, dtype)"),
+    ("dot_off_by_one", "for (int i = 0; i < n; ++i)\n        s += elem(a", "for (int i = 0; i < n - 1; ++i)\n        s += elem(a"),
+    ("gate_reads_token0", "double s = dot_rows(x, xo, w_gate", "double s = dot_rows(x, 0, w_gate"),
+    ("b1_dropped", "if (b1) z += elem(b1,", "if (0) z += elem(b1,"),
+    ("b2_dropped", "if (b2) z += elem(b2,", "if (0) z += elem(b2,"),
+    ("w2_transposed", "elem(w2, w2_off + (size_t)n * (size_t)h + (size_t)i, dtype)",
+     "elem(w2, w2_off + (size_t)i * (size_t)d + (size_t)n, dtype)"),
+    ("combine_drops_gate", "o[n] += g * y[n];", "o[n] += y[n];"),
+    ("combine_keeps_dropped", "if (slot[(size_t)t * k + j] < 0) continue;", ""),
+    ("bf16_widening_wrong_half", "uint32_t bits = (uint32_t)((const uint16_t *)base)[i] << 16;",
+     "uint32_t bits = (uint32_t)((const uint16_t *)base)[i] << 15;"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(name, old, new, tmp_path):
+    src = open(oracle.SOURCE).read()
+    assert src.count(old) == 1, "mutation site of %s not found exactly once" % name
+    path = os.path.join(tmp_path, "mutant.c")
+    open(path, "w").write(src.replace(old, new))
+    o = oracle.Oracle(oracle.compile_source(path, os.path.join(tmp_path, "mutant.so")))
+    caught = []
+    for pin in ALL_PINS:
+        try:
+            pin(o)
+        except AssertionError:
+            caught.append(pin.__name__)
+    assert caught, "no pin catches the planted mistake %s" % name
