@@ -1,0 +1,422 @@
+"""Benchmark of the sparse MoE layer forward pass on B300 (one JSON line on rank 0).
+
+A step is one moe_forward (gate -> top-k -> capacity dispatch -> grouped Linear-GELU-Linear -> combine)
+over one batch of synthetic tokens already resident in HBM, replayed from a CUDA graph.  Between timed
+steps a 256 MiB buffer is written to flush the 126 MB L2.  Each step is timed with CUDA events on the
+launching stream; `value` = tokens processed by all ranks / the slowest rank's summed step time.
+
+  --impl ours (default)   the CUDA library through its C ABI
+  --impl reference        the fp64 CPU oracle on the host cores (bounded samples; rank 0 only)
+
+With torchrun (--gpus N > 1) every rank runs an independent replica of the layer on its own GPU
+(the layer's one-GPU path has no exchange step); the ranks only meet for a barrier and the max-time
+reduction.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from mixture_experts_sparse_03_b300.inputs import WORKLOADS, make_inputs  # noqa: E402
+
+METRIC = "MoE layer fwd tokens/s on 1 B300; % of bf16 TC peak or HBM roofline"
+UNIT = "tokens/s"
+DEFAULT_WORKLOAD = "bf16_e8_k2"
+FLUSH_BYTES = 256 << 20
+KERNELS_FUSED = ["gate_topk", "dispatch_scan", "dispatch_assign_gather", "expert_up_gelu", "expert_down_combine"]
+KERNELS_UNFUSED = ["gate_topk", "dispatch_scan", "dispatch_assign_gather", "expert_up_gelu", "expert_down",
+                   "combine_gather"]
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-graph", action="store_true", help="time eager launches instead of a CUDA graph")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm=d["hbm_gbs"], bf16=d["bf16_tflops"], bf16_sustained=d["bf16_tflops_sustained"],
+                    source="measured")
+    return dict(hbm=6400.0, bf16=1800.0, bf16_sustained=1400.0, source="fallback")
+
+
+def layer_work(wl, kept_pairs: int, experts_used: int):
+    """Algorithmic work of one forward: FLOPs of the kept (token, expert) pairs through both expert
+    GEMMs plus the gate GEMM, and the expert-weight bytes the used experts occupy."""
+    esize = 2 if wl.dtype == "bf16" else 4
+    gemm = 2.0 * kept_pairs * wl.d * wl.h  # one of the two expert GEMMs
+    if wl.gate == "softmax":
+        gate = 2.0 * wl.T * wl.d * wl.E
+    elif wl.gate == "noisy":
+        gate = 4.0 * wl.T * wl.d * wl.E
+    else:
+        gate = 2.0 * wl.T * wl.d * wl.cos_dim + 2.0 * wl.T * wl.cos_dim * wl.E
+    wbytes = experts_used * 2 * wl.d * wl.h * esize
+    return gemm, gate, wbytes
+
+
+# ------------------------------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.out = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            sel = ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
+        except Exception:
+            sel = []
+        self.cmd = ["nvidia-smi", *sel, "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits", "-lms", "100"]
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------------- CPU oracle
+def cpu_oracle_sample(wl, tc, tg, seconds: float):
+    """Time the oracle (as it stands, single-threaded C, fp64) on a bounded sample of the workload:
+    routing and dispatch of every token, then the expert FFN and combine for a prefix of tokens sized
+    to about `seconds` of CPU work.  Returns (tokens/s, description, cores used)."""
+    import oracle
+
+    t0 = time.perf_counter()
+    scores = oracle.gate_scores(wl.gate, tc["x"], tc["w_gate"], tc["w_noise"], tc["eps"], tc["proj"], tc["emb"],
+                                wl.temperature)
+    idx, gate = oracle.topk(scores, wl.k, wl.norm)
+    C = oracle.capacity(wl.T, wl.E, wl.k, wl.capacity_factor, wl.capacity)
+    slot, _ = oracle.dispatch(idx, wl.E, C)
+    t_route = time.perf_counter() - t0
+    w = {n: (tc[n] if tc.get(n) is not None else (tg[n].cpu() if tg.get(n) is not None else None))
+         for n in ("w1", "b1", "w2", "b2")}
+    # calibrate on 2 tokens, then size the sample
+    t1 = time.perf_counter()
+    oracle.combine_tokens(np.arange(2, dtype=np.int32), tc["x"], idx, gate, slot, w["w1"], w["b1"], w["w2"], w["b2"])
+    per_tok = max((time.perf_counter() - t1) / 2, 1e-6)
+    n = int(min(wl.T, max(2, (seconds - t_route) / per_tok)))
+    t2 = time.perf_counter()
+    oracle.combine_tokens(np.arange(n, dtype=np.int32), tc["x"], idx, gate, slot, w["w1"], w["b1"], w["w2"], w["b2"])
+    t_ffn = time.perf_counter() - t2
+    per_token = t_route / wl.T + t_ffn / n
+    desc = ("routing + capacity dispatch of all %d tokens (%.2f s) and expert FFN + combine of the first %d tokens "
+            "(%.2f s); tokens/s = 1 / (route_time/T + ffn_time/n)" % (wl.T, t_route, n, t_ffn))
+    return 1.0 / per_token, desc, 1, t_route + t_ffn
+
+
+def run_reference(args, rank):
+    wl = WORKLOADS[args.workload]
+    if rank != 0:
+        return
+    tc = make_inputs(wl, device="cpu", expert_device="cpu") if wl.expert_weight_bytes() <= (4 << 30) else None
+    if tc is None:
+        print(json.dumps({"impl": "reference", "unavailable": "expert weights of this workload exceed the host "
+                          "sample budget"}))
+        return
+    per_step = max(1.0, args.cpu_seconds / max(1, args.steps + args.warmup))
+    vals, descs, total = [], [], 0.0
+    for i in range(args.warmup + args.steps):
+        v, desc, cores, dt = cpu_oracle_sample(wl, tc, {}, per_step)
+        if i >= args.warmup:
+            vals.append(v)
+            descs.append(desc)
+            total += dt
+    value = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(vals),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "T": wl.T, "d": wl.d, "h": wl.h, "E": wl.E, "k": wl.k, "gate": wl.gate},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": descs[-1]},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------------------- our path
+def source_sha():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "mixture_experts_sparse_03_b300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it was taken on the
+    current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "%s_%s.md" % (kernel, workload))
+    if not os.path.exists(p):
+        return None
+    txt = open(p).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    s = re.search(r"source_sha256:\s*([0-9a-f]+)", txt)
+    if not m or not s or s.group(1) != source_sha():
+        return None
+    return float(m.group(1))
+
+
+def run_ours(args, rank, world, local):
+    from mixture_experts_sparse_03_b300 import binding as b
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+    wl = WORKLOADS[args.workload]
+    cfg = b.config(wl)
+    tg = make_inputs(wl, device=dev, expert_device="cuda" if wl.expert_weight_bytes() > (1 << 30) else "cpu")
+    ws = b.workspace(cfg, dev)
+    out = torch.empty((wl.T, wl.d), dtype=torch.float32, device=dev)
+    count = torch.empty((wl.E,), dtype=torch.int32, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    launches_per_step = b.moe_forward_launches(cfg)
+
+    def step():
+        b.check(b.moe_forward(cfg, tg["x"], tg.get("w_gate"), tg.get("w_noise"), tg.get("eps"), tg.get("proj"),
+                              tg.get("emb"), tg["w1"], tg.get("b1"), tg["w2"], tg.get("b2"), out, count, ws,
+                              ws.numel(), stream), "moe_forward")
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            step()
+    stream.synchronize()
+    st, info = b.moe_device_status(ws, ws.numel(), stream)
+    b.check(st, "device status after warm-up")
+    C = b.moe_capacity(cfg)
+    cnt = count.cpu().numpy()
+    kept = int(np.minimum(cnt, min(C, wl.T)).sum())
+    used = int((np.minimum(cnt, C) > 0).sum())
+    gemm_flops, gate_flops, wbytes = layer_work(wl, kept, used)
+
+    graph = None
+    if not args.no_graph:
+        try:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                step()
+            with torch.cuda.stream(stream):
+                graph.replay()
+            stream.synchronize()
+        except Exception as e:  # report eager timing instead
+            print("graph capture failed (%s); timing eager launches" % e, file=sys.stderr)
+            graph = None
+
+    def run_step():
+        if graph is not None:
+            graph.replay()
+        else:
+            step()
+
+    # ---- timed region: K steps, L2 flushed before each, events around each step
+    K = args.steps
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            flush.fill_(1)
+            run_step()
+    stream.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        for i in range(K):
+            flush.fill_(i & 0xFF)
+            evs[i][0].record(stream)
+            run_step()
+            evs[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    times = [a.elapsed_time(z) for a, z in evs]  # ms
+    total_ms = sum(times)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    value = world * K * wl.T / (total_ms / 1e3)
+    ms_per_step = total_ms / K
+
+    # ---- per-kernel durations (eager, trace events between the library's launches)
+    names = KERNELS_FUSED if launches_per_step == 5 else KERNELS_UNFUSED
+    per = {n: [] for n in names}
+    tev = [torch.cuda.Event(enable_timing=True) for _ in range(launches_per_step + 1)]
+    for e in tev:  # torch creates the CUDA event at its first record; the library needs real handles
+        e.record(stream)
+    stream.synchronize()
+    with torch.cuda.stream(stream):
+        for i in range(max(5, min(K, 20))):
+            flush.fill_(1)
+            keep = b.moe_trace_events(tev, len(tev))
+            step()
+            b.moe_trace_events(None, 0)
+            stream.synchronize()
+            if b.moe_trace_count() != len(tev):
+                raise RuntimeError("trace hook recorded %d of %d events" % (b.moe_trace_count(), len(tev)))
+            for j, n in enumerate(names):
+                per[n].append(tev[j].elapsed_time(tev[j + 1]))
+            del keep
+    kern_ms = {n: statistics.median(v) for n, v in per.items()}
+    dominant = max(kern_ms, key=kern_ms.get)
+    pk = peaks()
+    if dominant.startswith("expert_"):
+        achieved = gemm_flops / (kern_ms[dominant] * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": pk["bf16"], "unit": "TFLOP/s",
+                "frac": achieved / pk["bf16"]}
+    else:
+        roof = {"bound": "hbm", "achieved": None, "peak": pk["hbm"], "unit": "GB/s", "frac": None}
+    kernel_file = {"expert_up_gelu": "gemm_tc_up", "expert_down_combine": "gemm_tc_down",
+                   "expert_down": "gemm_tc_down"}.get(dominant, dominant)
+    roof.update({"traffic": recorded_traffic(kernel_file, wl.name), "kernel": dominant,
+                 "peak_source": pk["source"] + " (burst)", "kernel_ms": kern_ms[dominant],
+                 "layer_tflops": (2 * gemm_flops + gate_flops) / (ms_per_step * 1e-3) / 1e12})
+    if wl.dtype != "bf16":
+        roof["note"] = "fp32 CUDA-core path; bf16 tensor peak shown for reference only"
+
+    # ---- end to end through the C ABI with host buffers (pinned), copies inside the timed region
+    x_host = tg["x"].cpu().pin_memory()
+    eps_host = tg["eps"].cpu().pin_memory() if tg.get("eps") is not None else None
+    out_host = torch.empty((wl.T, wl.d), dtype=torch.float32).pin_memory()
+    x_dev = torch.empty_like(tg["x"])
+    eps_dev = torch.empty_like(tg["eps"]) if eps_host is not None else None
+    h2d = x_host.numel() * x_host.element_size() + (eps_host.numel() * 4 if eps_host is not None else 0)
+    d2h = out_host.numel() * 4
+
+    def e2e_step():
+        x_dev.copy_(x_host, non_blocking=True)
+        if eps_dev is not None:
+            eps_dev.copy_(eps_host, non_blocking=True)
+        b.check(b.moe_forward(cfg, x_dev, tg.get("w_gate"), tg.get("w_noise"), eps_dev, tg.get("proj"), tg.get("emb"),
+                              tg["w1"], tg.get("b1"), tg["w2"], tg.get("b2"), out, None, ws, ws.numel(), stream),
+                "moe_forward")
+        out_host.copy_(out, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            e2e_step()
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e_ms = 0.0
+        for i in range(K):
+            flush.fill_(1)
+            e0.record(stream)
+            e2e_step()
+            e1.record(stream)
+            e1.synchronize()
+            e_ms += e0.elapsed_time(e1)
+    e2e_value = world * K * wl.T / (e_ms / 1e3)
+    if world > 1:
+        t = torch.tensor([e_ms], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_value = world * K * wl.T / (float(t.item()) / 1e3)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        tc = {n: (v.cpu() if v is not None else None) for n, v in tg.items()}
+        v, desc, cores, _ = cpu_oracle_sample(wl, tc, {}, args.cpu_seconds)
+        cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc,
+               "host_cores": os.cpu_count()}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+            "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": wl.dtype, "data": "synthetic (seeded; shapes and distributions of the workload)",
+            "config": {"workload": wl.name, "T": wl.T, "d_model": wl.d, "d_hidden": wl.h, "experts": wl.E,
+                       "top_k": wl.k, "gate": wl.gate, "capacity": C, "kept_pairs": kept,
+                       "parallelism": "replicas" if world > 1 else "single",
+                       "l2": "flushed between steps (256 MiB write)", "graph": graph is not None,
+                       "step_ms_median": statistics.median(times), "kernel_ms": kern_ms},
+            "roofline": roof,
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches_per_step * K,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py --impl ours needs a CUDA device")
+    run_ours(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -43,6 +43,12 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -58,8 +64,8 @@ typedef int32_t moe_status;
 #define MOE_ERR_DEVICE_TIMEOUT  6 /* a kernel's bounded barrier wait ran out (see moe_device_status)  */
 
 /* ---- enums ----------------------------------------------------------------------------------- */
-/* Gate types.  SOFTMAX: s = x W_g^T ("single linear layer + Softmax", intelliparadigm section 2.1;
- * Tutel top.py).  NOISY: s = x W_g^T + eps * softplus(x W_n^T) ("MoE sparse-compute acceleration",
+/* Gate types.  SOFTMAX: s = x W_g^T (one linear layer and a softmax, "How sparse activation improves
+ * efficiency", section 2.1; Tutel top.py).  NOISY: s = x W_g^T + eps * softplus(x W_n^T) ("MoE sparse-compute acceleration",
  * section 2.1, NoisyTopKGating; eps is supplied by the caller as an fp32 [T, E] tensor).  COSINE:
  * s_e = cos(x P^T, emb_e) / cos_temperature (Tutel cosine_top; the projection P and the expert
  * embeddings emb are inputs). */
@@ -68,7 +74,7 @@ typedef int32_t moe_status;
 #define MOE_GATE_COSINE  2
 
 /* Gate normalisation.  ALL: g = full softmax over all E scores, not renormalised (the top-1 layer of
- * "Does the PyTorch-CUDA-v2.6 image support MoE", which multiplies by the max softmax weight).
+ * "PyTorch-CUDA-v2.6 and MoE", which multiplies by the max softmax weight).
  * TOPK: softmax over the k selected scores (NoisyTopKGating's F.softmax(top_k_logits)). */
 #define MOE_GATE_NORM_ALL  0
 #define MOE_GATE_NORM_TOPK 1
@@ -88,7 +94,7 @@ typedef struct moe_config {
     double  capacity_factor;        /* > 0, used when capacity < 0                                   */
     int32_t gate_type;              /* MOE_GATE_*                                                    */
     int32_t gate_norm;              /* MOE_GATE_NORM_*                                               */
-    int32_t cos_dim;                /* cosine gate: projection width p, multiple of 4, 4..1024       */
+    int32_t cos_dim;                /* cosine gate: projection width p, multiple of 8, 8..1024       */
     int32_t dtype;                  /* MOE_F32 or MOE_BF16                                           */
     double  cos_temperature;        /* cosine gate: scores are divided by this (> 0)                 */
     int32_t flags;                  /* MOE_FLAG_* bits, 0 for the default path                       */
@@ -103,18 +109,19 @@ typedef struct moe_config {
 
 /* ---- sizes ------------------------------------------------------------------------------------ */
 /* Per-expert capacity C the dispatch step enforces, or -1 if the config is invalid. */
-int32_t moe_capacity(const moe_config* cfg);
+MOE_API int32_t moe_capacity(const moe_config* cfg);
 
 /* Upper bound on the number of dispatched rows: each expert's kept rows are padded to a multiple of
  * 128, so rows <= min(T*k + 127*E, E*roundup(C,128)).  x_dispatched / row_token / row_gate /
  * y_dispatched passed to moe_dispatch / moe_expert_ffn / moe_combine need this many rows.
  * Returns -1 if the config is invalid. */
-int64_t moe_dispatch_rows(const moe_config* cfg);
+MOE_API int64_t moe_dispatch_rows(const moe_config* cfg);
 
 /* Bytes of device workspace that every entry point below accepts (one size for all of them).
- * Returns 0 if the config is invalid.  The workspace needs no initialisation and may be reused by
- * consecutive calls on one stream; calls running concurrently need separate workspaces. */
-size_t moe_workspace_size(const moe_config* cfg);
+ * Returns 0 if the config is invalid.  The workspace must be 256-byte aligned (cudaMalloc memory is);
+ * it needs no initialisation and may be reused by consecutive calls on one stream; calls running
+ * concurrently need separate workspaces. */
+MOE_API size_t moe_workspace_size(const moe_config* cfg);
 
 /* ---- step 1+2: routing ------------------------------------------------------------------------ */
 /* Gate logits, scores, per-token top-k and gate weights.
@@ -130,14 +137,14 @@ size_t moe_workspace_size(const moe_config* cfg);
  * scores of a token are closer than the fp32 error bound of that token, the contenders are recomputed
  * with a doubled-precision (float-float) dot product, so the chosen set and its order equal those of
  * exact arithmetic except for differences below about 1e-12 of the score scale. */
-moe_status moe_route(const moe_config* cfg, const void* x, const void* w_gate, const void* w_noise,
+MOE_API moe_status moe_route(const moe_config* cfg, const void* x, const void* w_gate, const void* w_noise,
                      const float* noise_eps, const void* proj, const void* expert_emb,
                      int32_t* topk_idx, float* topk_gate, void* stream);
 
 /* ---- step 3: capacity-limited dispatch -------------------------------------------------------- */
-/* Groups the (token, expert) pairs by expert ("first group the samples by their chosen expert, then
- * run one batched matmul per group", intelliparadigm section 3.1) under a per-expert capacity C
- * (Tutel capacity_factor; CANN MOELayer capacity_factor).  Slots are handed out in token order (for
+/* Groups the (token, expert) pairs by expert, ahead of one batched matmul per group ("How sparse
+ * activation improves efficiency", section 3.1), under a per-expert capacity C (capacity_factor of the
+ * "Tutel MoE guide" and of CANN's MOELayer in "MoE sparse-compute acceleration", section 3.2).  Slots are handed out in token order (for
  * one expert, token t precedes token t+1; a token never picks an expert twice); a pair whose slot is
  * >= C is dropped.  Outputs:
  *   slot          [T, k] int32   slot of each pair in its expert's queue, -1 if dropped
@@ -149,7 +156,7 @@ moe_status moe_route(const moe_config* cfg, const void* x, const void* w_gate, c
  *   row_gate      [rows] fp32    gate weight of each dispatched row, 0 for padding rows
  *   x_dispatched  [rows, d]      copy of x[row_token[r]] for every real row (padding rows untouched)
  * rows = moe_dispatch_rows(cfg).  Deterministic: no result depends on thread scheduling. */
-moe_status moe_dispatch(const moe_config* cfg, const void* x, const int32_t* topk_idx,
+MOE_API moe_status moe_dispatch(const moe_config* cfg, const void* x, const int32_t* topk_idx,
                         const float* topk_gate, int32_t* slot, int32_t* expert_count,
                         int32_t* expert_offset, int32_t* row_token, float* row_gate,
                         void* x_dispatched, void* workspace, size_t workspace_bytes, void* stream);
@@ -165,7 +172,7 @@ moe_status moe_dispatch(const moe_config* cfg, const void* x, const int32_t* top
  *                         token with none).  With top_k <= 2 the result is bitwise deterministic;
  *                         with top_k > 2 the order of the fp32 additions may vary between runs.
  * The hidden activations (bf16 for MOE_BF16, fp32 for MOE_F32) live in the workspace. */
-moe_status moe_expert_ffn(const moe_config* cfg, const void* x_dispatched,
+MOE_API moe_status moe_expert_ffn(const moe_config* cfg, const void* x_dispatched,
                           const int32_t* expert_offset, const int32_t* row_token,
                           const float* row_gate, const void* w1, const void* b1, const void* w2,
                           const void* b2, float* y_dispatched, float* out, void* workspace,
@@ -174,9 +181,9 @@ moe_status moe_expert_ffn(const moe_config* cfg, const void* x_dispatched,
 /* ---- step 5 (unfused): combine ----------------------------------------------------------------- */
 /* out[t] = sum over j < k with slot[t,j] >= 0 of topk_gate[t,j] * y_dispatched[off[e] + slot[t,j]],
  * e = topk_idx[t,j], summed in rank order j = 0..k-1 (deterministic); 0 for a token whose pairs were
- * all dropped ("Output = sum_i g_i(x) E_i(x)", MoE on a single card, section 1.2).  out [T, d] fp32 is
+ * all dropped (Output = sum_i g_i(x) E_i(x), "MoE on a single card", section 1.2).  out [T, d] fp32 is
  * overwritten. */
-moe_status moe_combine(const moe_config* cfg, const float* y_dispatched, const int32_t* slot,
+MOE_API moe_status moe_combine(const moe_config* cfg, const float* y_dispatched, const int32_t* slot,
                        const int32_t* expert_offset, const int32_t* topk_idx,
                        const float* topk_gate, float* out, void* stream);
 
@@ -185,7 +192,7 @@ moe_status moe_combine(const moe_config* cfg, const float* y_dispatched, const i
  * intermediate in the workspace.  out [T, d] fp32 is overwritten.  expert_count (may be NULL)
  * receives the per-expert pre-capacity counts.  The fused combine is used when top_k <= 2 and the
  * gather combine otherwise, so the output is bitwise deterministic for every k. */
-moe_status moe_forward(const moe_config* cfg, const void* x, const void* w_gate,
+MOE_API moe_status moe_forward(const moe_config* cfg, const void* x, const void* w_gate,
                        const void* w_noise, const float* noise_eps, const void* proj,
                        const void* expert_emb, const void* w1, const void* b1, const void* w2,
                        const void* b2, float* out, int32_t* expert_count, void* workspace,
@@ -195,7 +202,7 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const void* w_gate,
 /* Synchronises `stream`, reads and clears the error word at the start of `workspace` and returns
  * MOE_OK, MOE_ERR_DEVICE_CHECK or MOE_ERR_DEVICE_TIMEOUT.  If `info` is not NULL it receives a code
  * saying which kernel recorded the error (0 if none). */
-moe_status moe_device_status(void* workspace, size_t workspace_bytes, int32_t* info, void* stream);
+MOE_API moe_status moe_device_status(void* workspace, size_t workspace_bytes, int32_t* info, void* stream);
 
 /* Profiling hook.  With events != NULL (an array of `capacity` cudaEvent_t, each passed as void*),
  * the library records events[0] on the launch stream before the first kernel it launches after this
@@ -203,14 +210,14 @@ moe_status moe_device_status(void* workspace, size_t workspace_bytes, int32_t* i
  * thus use n + 1 events and kernel i ran between events[i] and events[i+1].  moe_trace_count()
  * returns how many events have been recorded.  events == NULL turns the hook off.  Not thread-safe;
  * meant for benchmarks. */
-void    moe_trace_events(void** events, int32_t capacity);
-int32_t moe_trace_count(void);
+MOE_API void    moe_trace_events(void** events, int32_t capacity);
+MOE_API int32_t moe_trace_count(void);
 
 /* Number of kernels moe_forward launches for this config (for launch accounting), -1 if invalid. */
-int32_t moe_forward_launches(const moe_config* cfg);
+MOE_API int32_t moe_forward_launches(const moe_config* cfg);
 
 /* Human-readable name of a status code (static storage). */
-const char* moe_status_string(moe_status status);
+MOE_API const char* moe_status_string(moe_status status);
 
 #ifdef __cplusplus
 }

@@ -1,0 +1,384 @@
+// api.cu -- the C ABI of libmoe_b300 (declared in include/moe_b300.h): argument validation, workspace
+// planning, the launch sequence of the layer and the profiling hook.  Every argument is checked on the
+// host before anything is enqueued; a failed check returns a status and launches nothing.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include <algorithm>
+
+#include "kernels.h"
+#include "moe_b300.h"
+
+namespace moe {
+size_t gate_smem_bytes(int gate, int E, int p);
+}
+
+namespace {
+
+using namespace moe;
+
+constexpr size_t kAlign = 256;
+constexpr int kMaxSmem = 227 * 1024;
+
+size_t up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Plan {
+    int T, d, h, E, k, C, Ceff, p, nblk, gate, norm, bf16, esize, fused;
+    int64_t rows;
+    size_t o_err, o_idx, o_gate, o_slot, o_hist, o_count, o_off, o_rtok, o_rgate, o_xd, o_h, o_y, total;
+};
+
+moe_status make_plan(const moe_config* c, Plan* pl) {
+    if (c == nullptr) return MOE_ERR_INVALID_ARG;
+    Plan P{};
+    P.T = c->tokens;
+    P.d = c->model_dim;
+    P.h = c->hidden_size_per_expert;
+    P.E = c->num_experts;
+    P.k = c->top_k;
+    P.gate = c->gate_type;
+    P.norm = c->gate_norm;
+    P.bf16 = c->dtype == MOE_BF16;
+    P.esize = P.bf16 ? 2 : 4;
+    if (P.T < 0 || P.d < 64 || P.d % 64 || P.h < 64 || P.h % 64) return MOE_ERR_INVALID_ARG;
+    if (P.d > (1 << 16) || P.h > (1 << 16)) return MOE_ERR_UNSUPPORTED;
+    if (P.E < 1 || P.E > kMaxExperts || P.k < 1 || P.k > P.E || P.k > kMaxTopK) return MOE_ERR_INVALID_ARG;
+    if (c->dtype != MOE_F32 && c->dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+    if (P.gate < MOE_GATE_SOFTMAX || P.gate > MOE_GATE_COSINE) return MOE_ERR_INVALID_ARG;
+    if (P.norm != MOE_GATE_NORM_ALL && P.norm != MOE_GATE_NORM_TOPK) return MOE_ERR_INVALID_ARG;
+    if (c->flags & ~(MOE_FLAG_SIMT_FFN | MOE_FLAG_UNFUSED_COMBINE)) return MOE_ERR_INVALID_ARG;
+    if (c->reserved != 0) return MOE_ERR_INVALID_ARG;
+    if (P.gate == MOE_GATE_NOISY && P.E > 512) return MOE_ERR_UNSUPPORTED;
+    P.p = 0;
+    if (P.gate == MOE_GATE_COSINE) {
+        P.p = c->cos_dim;
+        if (P.p < 8 || P.p > 1024 || P.p % 8) return MOE_ERR_INVALID_ARG;
+        if (!(c->cos_temperature > 0.0) || !isfinite(c->cos_temperature)) return MOE_ERR_INVALID_ARG;
+    }
+    if (c->capacity >= 0) {
+        P.C = c->capacity;
+    } else {
+        if (!(c->capacity_factor > 0.0) || !isfinite(c->capacity_factor)) return MOE_ERR_INVALID_ARG;
+        const double v = ceil(c->capacity_factor * (double)P.T * (double)P.k / (double)P.E);
+        if (!(v >= 0.0) || v > 2147483647.0) return MOE_ERR_INVALID_ARG;
+        P.C = (int)v;
+    }
+    if (gate_smem_bytes(P.gate, P.E, P.p) > (size_t)kMaxSmem) return MOE_ERR_UNSUPPORTED;
+    P.Ceff = std::min(P.C, P.T);  // a token takes an expert at most once, so C >= T drops nothing
+    const int64_t cpad = ((int64_t)P.Ceff + kRowAlign - 1) / kRowAlign * kRowAlign;
+    P.rows = std::min<int64_t>((int64_t)P.T * P.k + (int64_t)(kRowAlign - 1) * P.E, (int64_t)P.E * cpad);
+    if (P.rows > (int64_t)1 << 30) return MOE_ERR_UNSUPPORTED;
+    P.nblk = (P.T + kTokensPerBlock - 1) / kTokensPerBlock;
+    P.fused = P.k <= 2 && !(c->flags & MOE_FLAG_UNFUSED_COMBINE);
+    size_t o = 0;
+    auto take = [&](size_t bytes) { size_t r = o; o = up(o + bytes); return r; };
+    const size_t tk = (size_t)P.T * P.k;
+    P.o_err = take(16);
+    P.o_idx = take(4 * tk);
+    P.o_gate = take(4 * tk);
+    P.o_slot = take(4 * tk);
+    P.o_hist = take(4 * (size_t)P.nblk * P.E);
+    P.o_count = take(4 * (size_t)P.E);
+    P.o_off = take(4 * (size_t)(P.E + 1));
+    P.o_rtok = take(4 * (size_t)P.rows);
+    P.o_rgate = take(4 * (size_t)P.rows);
+    P.o_xd = take((size_t)P.rows * P.d * P.esize);
+    P.o_h = take((size_t)P.rows * P.h * P.esize);
+    P.o_y = take((size_t)P.rows * P.d * 4);
+    P.total = o;
+    *pl = P;
+    return MOE_OK;
+}
+
+moe_status check_ws(const Plan& P, void* ws, size_t bytes) {
+    if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) || bytes < P.total) return MOE_ERR_WORKSPACE;
+    return MOE_OK;
+}
+
+template <typename Tp>
+Tp* at(void* ws, size_t off) { return reinterpret_cast<Tp*>(static_cast<char*>(ws) + off); }
+
+// ---- profiling hook -------------------------------------------------------------------------------
+void** g_events = nullptr;
+int g_capacity = 0;
+int g_recorded = 0;
+
+// A failed record (e.g. an event that was never created) turns the hook off and clears the error, so
+// tracing can never change the status of a launch; moe_trace_count() then shows the shortfall.
+void trace_record(int i, cudaStream_t s) {
+    if (cudaEventRecord(static_cast<cudaEvent_t>(g_events[i]), s) != cudaSuccess) {
+        cudaGetLastError();
+        g_events = nullptr;
+        return;
+    }
+    g_recorded = i + 1;
+}
+void trace_pre(cudaStream_t s) {
+    if (g_events != nullptr && g_recorded == 0 && g_capacity > 0) trace_record(0, s);
+}
+void trace_post(cudaStream_t s) {
+    if (g_events != nullptr && g_recorded > 0 && g_recorded < g_capacity) trace_record(g_recorded, s);
+}
+
+// wrap one kernel launch: trace events around it, CUDA errors mapped to a status
+template <typename F>
+moe_status launch(cudaStream_t s, F&& f) {
+    trace_pre(s);
+    cudaError_t e = f();
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    trace_post(s);
+    return MOE_OK;
+}
+#define MOE_TRY(expr)                      \
+    do {                                   \
+        moe_status st_ = (expr);           \
+        if (st_ != MOE_OK) return st_;     \
+    } while (0)
+
+moe_status check_route_args(const Plan& P, const void* x, const void* w_gate, const void* w_noise,
+                            const float* eps, const void* proj, const void* emb, const void* idx, const void* gate) {
+    if (!x || !idx || !gate || !aligned16(x) || !aligned16(idx) || !aligned16(gate)) return MOE_ERR_INVALID_ARG;
+    if (P.gate == MOE_GATE_COSINE) {
+        if (!proj || !emb || !aligned16(proj) || !aligned16(emb)) return MOE_ERR_INVALID_ARG;
+    } else {
+        if (!w_gate || !aligned16(w_gate)) return MOE_ERR_INVALID_ARG;
+        if (P.gate == MOE_GATE_NOISY && (!w_noise || !eps || !aligned16(w_noise) || !aligned16(eps)))
+            return MOE_ERR_INVALID_ARG;
+    }
+    return MOE_OK;
+}
+
+GateParams gate_params(const Plan& P, const moe_config* c, const void* x, const void* w_gate, const void* w_noise,
+                       const float* eps, const void* proj, const void* emb, int32_t* idx, float* gate) {
+    GateParams g{};
+    g.x = x;
+    g.w_gate = w_gate;
+    g.w_noise = w_noise;
+    g.eps = eps;
+    g.proj = proj;
+    g.emb = emb;
+    g.T = P.T;
+    g.d = P.d;
+    g.E = P.E;
+    g.k = P.k;
+    g.p = P.p;
+    g.gate = P.gate;
+    g.norm = P.norm;
+    g.bf16 = P.bf16;
+    g.temp = P.gate == MOE_GATE_COSINE ? c->cos_temperature : 1.0;
+    g.inv_temp = (float)(1.0 / g.temp);
+    g.topk_idx = idx;
+    g.topk_gate = gate;
+    return g;
+}
+
+FfnParams ffn_params(const Plan& P, int mode, const void* A, const void* W, const void* bias, const int* off,
+                     const int* rtok, const float* rgate, void* C, float* out, int* err) {
+    FfnParams f{};
+    f.A = A;
+    f.W = W;
+    f.bias = bias;
+    f.offset = off;
+    f.row_token = rtok;
+    f.row_gate = rgate;
+    f.C = C;
+    f.out = out;
+    f.E = P.E;
+    f.K = mode == 0 ? P.d : P.h;
+    f.N = mode == 0 ? P.h : P.d;
+    f.bf16 = P.bf16;
+    f.mode = mode;
+    f.rows_cap = P.rows;
+    f.err = err;
+    return f;
+}
+
+moe_status run_ffn(const Plan& P, const moe_config* c, const FfnParams& f, cudaStream_t s) {
+    const bool tc = P.bf16 && !(c->flags & MOE_FLAG_SIMT_FFN);
+    return launch(s, [&] { return tc ? launch_ffn_tc(f, s) : launch_ffn_simt(f, s); });
+}
+
+// expert FFN + (fused or separate) combine, shared by moe_expert_ffn and moe_forward
+moe_status ffn_and_combine(const Plan& P, const moe_config* c, const void* xd, const int* off, const int* rtok,
+                           const float* rgate, const void* w1, const void* b1, const void* w2, const void* b2,
+                           float* y, float* out, bool fused, void* ws, cudaStream_t s) {
+    int* err = at<int>(ws, P.o_err);
+    void* hbuf = at<void>(ws, P.o_h);
+    MOE_TRY(run_ffn(P, c, ffn_params(P, 0, xd, w1, b1, off, rtok, rgate, hbuf, nullptr, err), s));
+    if (fused) return run_ffn(P, c, ffn_params(P, 2, hbuf, w2, b2, off, rtok, rgate, nullptr, out, err), s);
+    return run_ffn(P, c, ffn_params(P, 1, hbuf, w2, b2, off, rtok, rgate, y, nullptr, err), s);
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t moe_capacity(const moe_config* cfg) {
+    Plan P;
+    return make_plan(cfg, &P) == MOE_OK ? P.C : -1;
+}
+
+int64_t moe_dispatch_rows(const moe_config* cfg) {
+    Plan P;
+    return make_plan(cfg, &P) == MOE_OK ? P.rows : -1;
+}
+
+size_t moe_workspace_size(const moe_config* cfg) {
+    Plan P;
+    return make_plan(cfg, &P) == MOE_OK ? P.total : 0;
+}
+
+int32_t moe_forward_launches(const moe_config* cfg) {
+    Plan P;
+    if (make_plan(cfg, &P) != MOE_OK) return -1;
+    if (P.T == 0) return 0;
+    return P.fused ? 5 : 6;
+}
+
+moe_status moe_route(const moe_config* cfg, const void* x, const void* w_gate, const void* w_noise,
+                     const float* noise_eps, const void* proj, const void* expert_emb, int32_t* topk_idx,
+                     float* topk_gate, void* stream) {
+    Plan P;
+    MOE_TRY(make_plan(cfg, &P));
+    if (P.T == 0) return MOE_OK;
+    MOE_TRY(check_route_args(P, x, w_gate, w_noise, noise_eps, proj, expert_emb, topk_idx, topk_gate));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    GateParams g = gate_params(P, cfg, x, w_gate, w_noise, noise_eps, proj, expert_emb, topk_idx, topk_gate);
+    return launch(s, [&] { return launch_gate(g, s); });
+}
+
+moe_status moe_dispatch(const moe_config* cfg, const void* x, const int32_t* topk_idx, const float* topk_gate,
+                        int32_t* slot, int32_t* expert_count, int32_t* expert_offset, int32_t* row_token,
+                        float* row_gate, void* x_dispatched, void* workspace, size_t workspace_bytes, void* stream) {
+    Plan P;
+    MOE_TRY(make_plan(cfg, &P));
+    if (P.T == 0) return MOE_OK;
+    MOE_TRY(check_ws(P, workspace, workspace_bytes));
+    const void* ptrs[] = {x, topk_idx, topk_gate, slot, expert_count, expert_offset, row_token, row_gate, x_dispatched};
+    for (const void* q : ptrs)
+        if (!q || !aligned16(q)) return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int* err = at<int>(workspace, P.o_err);
+    int* hist = at<int>(workspace, P.o_hist);
+    if (cudaMemsetAsync(err, 0, 8, s) != cudaSuccess) return MOE_ERR_CUDA;
+    MOE_TRY(launch(s, [&] { return launch_dispatch_count(topk_idx, P.T, P.k, P.E, hist, err, s); }));
+    MOE_TRY(launch(s, [&] {
+        return launch_dispatch_scan(hist, P.T, P.k, P.E, P.Ceff, expert_count, expert_offset, row_token, row_gate, s);
+    }));
+    return launch(s, [&] {
+        return launch_dispatch_assign(x, P.bf16, topk_idx, topk_gate, hist, expert_offset, P.T, P.k, P.E, P.d, P.Ceff,
+                                      slot, row_token, row_gate, x_dispatched, nullptr, err, s);
+    });
+}
+
+moe_status moe_expert_ffn(const moe_config* cfg, const void* x_dispatched, const int32_t* expert_offset,
+                          const int32_t* row_token, const float* row_gate, const void* w1, const void* b1,
+                          const void* w2, const void* b2, float* y_dispatched, float* out, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+    Plan P;
+    MOE_TRY(make_plan(cfg, &P));
+    if (P.T == 0) return MOE_OK;
+    MOE_TRY(check_ws(P, workspace, workspace_bytes));
+    const void* ptrs[] = {x_dispatched, expert_offset, row_token, row_gate, w1, w2};
+    for (const void* q : ptrs)
+        if (!q || !aligned16(q)) return MOE_ERR_INVALID_ARG;
+    if ((b1 && !aligned16(b1)) || (b2 && !aligned16(b2))) return MOE_ERR_INVALID_ARG;
+    const bool fused = y_dispatched == nullptr;
+    if (fused ? (!out || !aligned16(out)) : !aligned16(y_dispatched)) return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(at<int>(workspace, P.o_err), 0, 8, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (fused) MOE_TRY(launch(s, [&] { return launch_zero(out, (size_t)P.T * P.d, s); }));
+    return ffn_and_combine(P, cfg, x_dispatched, expert_offset, row_token, row_gate, w1, b1, w2, b2, y_dispatched,
+                           out, fused, workspace, s);
+}
+
+moe_status moe_combine(const moe_config* cfg, const float* y_dispatched, const int32_t* slot,
+                       const int32_t* expert_offset, const int32_t* topk_idx, const float* topk_gate, float* out,
+                       void* stream) {
+    Plan P;
+    MOE_TRY(make_plan(cfg, &P));
+    if (P.T == 0) return MOE_OK;
+    const void* ptrs[] = {y_dispatched, slot, expert_offset, topk_idx, topk_gate, out};
+    for (const void* q : ptrs)
+        if (!q || !aligned16(q)) return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return launch(s, [&] {
+        return launch_combine(y_dispatched, slot, expert_offset, topk_idx, topk_gate, P.T, P.k, P.d, out, s);
+    });
+}
+
+moe_status moe_forward(const moe_config* cfg, const void* x, const void* w_gate, const void* w_noise,
+                       const float* noise_eps, const void* proj, const void* expert_emb, const void* w1,
+                       const void* b1, const void* w2, const void* b2, float* out, int32_t* expert_count,
+                       void* workspace, size_t workspace_bytes, void* stream) {
+    Plan P;
+    MOE_TRY(make_plan(cfg, &P));
+    if (P.T == 0) return MOE_OK;
+    MOE_TRY(check_ws(P, workspace, workspace_bytes));
+    int32_t* idx = at<int32_t>(workspace, P.o_idx);
+    float* gate = at<float>(workspace, P.o_gate);
+    MOE_TRY(check_route_args(P, x, w_gate, w_noise, noise_eps, proj, expert_emb, idx, gate));
+    if (!w1 || !w2 || !out || !aligned16(w1) || !aligned16(w2) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
+    if ((b1 && !aligned16(b1)) || (b2 && !aligned16(b2)) || (expert_count && !aligned16(expert_count)))
+        return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int* err = at<int>(workspace, P.o_err);
+    int* hist = at<int>(workspace, P.o_hist);
+    int* count = expert_count ? expert_count : at<int>(workspace, P.o_count);
+    int* off = at<int>(workspace, P.o_off);
+    int* slot = at<int>(workspace, P.o_slot);
+    int* rtok = at<int>(workspace, P.o_rtok);
+    float* rgate = at<float>(workspace, P.o_rgate);
+    void* xd = at<void>(workspace, P.o_xd);
+    float* y = at<float>(workspace, P.o_y);
+    if (cudaMemsetAsync(err, 0, 8, s) != cudaSuccess) return MOE_ERR_CUDA;
+    GateParams g = gate_params(P, cfg, x, w_gate, w_noise, noise_eps, proj, expert_emb, idx, gate);
+    g.blk_hist = hist;
+    g.err = err;
+    MOE_TRY(launch(s, [&] { return launch_gate(g, s); }));
+    MOE_TRY(launch(s, [&] { return launch_dispatch_scan(hist, P.T, P.k, P.E, P.Ceff, count, off, rtok, rgate, s); }));
+    MOE_TRY(launch(s, [&] {
+        return launch_dispatch_assign(x, P.bf16, idx, gate, hist, off, P.T, P.k, P.E, P.d, P.Ceff, slot, rtok, rgate,
+                                      xd, P.fused ? out : nullptr, err, s);
+    }));
+    MOE_TRY(ffn_and_combine(P, cfg, xd, off, rtok, rgate, w1, b1, w2, b2, y, out, P.fused != 0, workspace, s));
+    if (!P.fused) MOE_TRY(launch(s, [&] { return launch_combine(y, slot, off, idx, gate, P.T, P.k, P.d, out, s); }));
+    return MOE_OK;
+}
+
+moe_status moe_device_status(void* workspace, size_t workspace_bytes, int32_t* info, void* stream) {
+    if (workspace == nullptr || workspace_bytes < 16) return MOE_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int32_t w[2] = {0, 0};
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaMemcpy(w, workspace, sizeof w, cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaMemset(workspace, 0, sizeof w) != cudaSuccess) return MOE_ERR_CUDA;
+    if (info) *info = w[1];
+    if (w[0] == 0) return MOE_OK;
+    return w[0] == MOE_ERR_DEVICE_TIMEOUT ? MOE_ERR_DEVICE_TIMEOUT : MOE_ERR_DEVICE_CHECK;
+}
+
+void moe_trace_events(void** events, int32_t capacity) {
+    g_events = capacity > 0 ? events : nullptr;
+    g_capacity = capacity > 0 ? capacity : 0;
+    g_recorded = 0;
+}
+
+int32_t moe_trace_count(void) { return g_recorded; }
+
+const char* moe_status_string(moe_status status) {
+    switch (status) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_INVALID_ARG: return "invalid argument";
+        case MOE_ERR_UNSUPPORTED: return "unsupported configuration";
+        case MOE_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+        case MOE_ERR_CUDA: return "CUDA runtime error";
+        case MOE_ERR_DEVICE_CHECK: return "device-side check failed";
+        case MOE_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+        default: return "unknown status";
+    }
+}
+
+}  // extern "C"

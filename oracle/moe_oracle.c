@@ -10,15 +10,16 @@
  *
  * The steps follow the pages in order:
  *   1. gate scores   -- "MoE sparse-compute acceleration" section 2.1 (NoisyTopKGating: clean and noise
- *                       linear maps without bias, noise scaled by softplus); intelliparadigm section
- *                       2.1 ("a single linear layer followed by Softmax"); Tutel guide, gate types
- *                       top / cosine_top.  The cosine form cos(x P, e_j) / temperature is the reading
+ *                       linear maps without bias, noise scaled by softplus); "How sparse activation
+ *                       improves efficiency" section 2.1 (one linear layer and a softmax); "Tutel MoE
+ *                       guide", gate types top / cosine_top.  The cosine form cos(x P, e_j) / temperature is the reading
  *                       the workload definition fixes, since the pages give no formula for it.
  *   2. top-k + gates -- NoisyTopKGating: topk of the logits, softmax over the k selected; the top-1
- *                       MOELayer of "Does the PyTorch-CUDA-v2.6 image support MoE": softmax over all
+ *                       MOELayer of "PyTorch-CUDA-v2.6 and MoE": softmax over all
  *                       experts, the max weight multiplies the output.
- *   3. dispatch      -- intelliparadigm section 3.1 (group tokens by chosen expert); Tutel guide
- *                       capacity_factor (1.2 allows 120 % of an expert's share); overflow dropped.
+ *   3. dispatch      -- "How sparse activation improves efficiency" section 3.1 (group tokens by
+ *                       chosen expert); "Tutel MoE guide" capacity_factor (1.2 admits 20 % above an
+ *                       even share); overflow dropped.
  *   4. expert FFN    -- CANN MOELayer example: Linear(d, 4d) -> GELU -> Linear(4d, d).
  *   5. combine       -- "MoE on a single card" section 1.2: Output = sum_i g_i(x) E_i(x).
  *

@@ -1,0 +1,140 @@
+"""The C ABI without a GPU: the library loads, exports every function include/moe_b300.h declares,
+its struct layout matches the C compiler's, and host-side validation and sizing behave as documented
+(no call here launches a kernel)."""
+import ctypes
+import math
+import os
+import subprocess
+
+import pytest
+
+import oracle
+from mixture_experts_sparse_03_b300 import binding as b
+from mixture_experts_sparse_03_b300.inputs import WORKLOADS, small_workload
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_exports_every_declared_function():
+    names = b.declared_functions()
+    assert len(names) >= 13
+    lib = ctypes.CDLL(b.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    for n in ("moe_route", "moe_dispatch", "moe_expert_ffn", "moe_combine", "moe_forward"):
+        assert n in names
+
+
+def test_config_layout_matches_c(tmp_path):
+    src = os.path.join(tmp_path, "layout.c")
+    open(src, "w").write(
+        '#include <stdio.h>\n#include <stddef.h>\n#include "moe_b300.h"\n'
+        'int main(void){printf("%zu %zu %zu %zu %zu %zu\\n", sizeof(moe_config), offsetof(moe_config, capacity),'
+        ' offsetof(moe_config, capacity_factor), offsetof(moe_config, cos_dim), offsetof(moe_config, cos_temperature),'
+        ' offsetof(moe_config, reserved)); return 0;}\n')
+    exe = os.path.join(tmp_path, "layout")
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), "-o", exe, src], check=True)
+    got = [int(v) for v in subprocess.run([exe], capture_output=True, text=True, check=True).stdout.split()]
+    C = b.MoEConfig
+    assert got == [ctypes.sizeof(C), C.capacity.offset, C.capacity_factor.offset, C.cos_dim.offset,
+                   C.cos_temperature.offset, C.reserved.offset]
+
+
+@pytest.mark.parametrize("name", list(WORKLOADS))
+def test_capacity_matches_oracle(name):
+    wl = WORKLOADS[name]
+    c = b.config(wl)
+    assert b.moe_capacity(c) == oracle.capacity(wl.T, wl.E, wl.k, wl.capacity_factor, wl.capacity)
+
+
+def test_capacity_values_and_rows_bound():
+    want = {"tiny_fp32": 77, "bf16_e8_k2": 1229, "bf16_noisy_e64": 768, "bf16_cosine_skew": 615, "bf16_decode_e256": 64}
+    for name, C in want.items():
+        wl = WORKLOADS[name]
+        c = b.config(wl)
+        assert b.moe_capacity(c) == C
+        Ceff = min(C, wl.T)
+        rows = min(wl.T * wl.k + 127 * wl.E, wl.E * math.ceil(Ceff / 128) * 128)
+        assert b.moe_dispatch_rows(c) == rows
+        assert b.moe_workspace_size(c) > rows * wl.d * (2 if wl.dtype == "bf16" else 4)
+
+
+def _bad(**kw):
+    c = b.config(small_workload())
+    for k_, v in kw.items():
+        setattr(c, k_, v)
+    return c
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("model_dim", 96, 1), ("model_dim", 0, 1), ("hidden_size_per_expert", 100, 1), ("num_experts", 0, 1),
+    ("num_experts", 2000, 1), ("top_k", 0, 1), ("top_k", 6, 1), ("top_k", 17, 1), ("tokens", -1, 1),
+    ("gate_type", 3, 1), ("gate_norm", 2, 1), ("dtype", 2, 1), ("flags", 64, 1), ("reserved", 1, 1),
+    ("capacity_factor", 0.0, 1), ("capacity_factor", float("nan"), 1), ("capacity_factor", float("inf"), 1),
+])
+def test_invalid_config_rejected(field, value, status):
+    c = _bad(**{field: value})
+    assert b.moe_workspace_size(c) == 0
+    assert b.moe_capacity(c) == -1
+    assert b.lib.moe_route(ctypes.byref(c), None, None, None, None, None, None, None, None, None) == status
+
+
+def test_cosine_and_noisy_limits():
+    wl = small_workload(gate="cosine", cos_dim=12)
+    assert b.moe_workspace_size(b.config(wl)) == 0  # cos_dim must be a multiple of 8
+    c = b.config(small_workload(gate="cosine", cos_dim=16))
+    c.cos_temperature = 0.0
+    assert b.moe_workspace_size(c) == 0
+    c = b.config(small_workload(gate="noisy", E=600, k=2))
+    assert b.lib.moe_route(ctypes.byref(c), None, None, None, None, None, None, None, None, None) == 2
+
+
+def test_null_and_misaligned_pointers_rejected_before_launch():
+    c = b.config(small_workload())
+    lib = b.lib
+    P = 0x10000
+    # missing x / outputs
+    assert lib.moe_route(ctypes.byref(c), None, P, None, None, None, None, P, P, None) == 1
+    assert lib.moe_route(ctypes.byref(c), P, P, None, None, None, None, None, P, None) == 1
+    # misaligned
+    assert lib.moe_route(ctypes.byref(c), P + 2, P, None, None, None, None, P, P, None) == 1
+    # noisy needs w_noise and eps
+    cn = b.config(small_workload(gate="noisy"))
+    assert lib.moe_route(ctypes.byref(cn), P, P, None, None, None, None, P, P, None) == 1
+    # cosine needs proj and emb
+    cc = b.config(small_workload(gate="cosine", cos_dim=16))
+    assert lib.moe_route(ctypes.byref(cc), P, P, None, None, None, None, P, P, None) == 1
+    # workspace missing / too small / misaligned
+    n = b.moe_workspace_size(c)
+    args = [P] * 9
+    assert lib.moe_dispatch(ctypes.byref(c), *args, None, n, None) == 3
+    assert lib.moe_dispatch(ctypes.byref(c), *args, 0x100000, n - 1, None) == 3
+    assert lib.moe_dispatch(ctypes.byref(c), *args, 0x100010, n, None) == 3
+    assert lib.moe_forward(ctypes.byref(c), P, P, None, None, None, None, P, None, P, None, P, None, None, n, None) == 3
+    assert lib.moe_forward(ctypes.byref(c), P, P, None, None, None, None, None, None, P, None, P, None, 0x100000, n,
+                           None) == 1
+
+
+def test_empty_input_is_a_no_op():
+    c = b.config(small_workload(), tokens=0)
+    assert b.moe_capacity(c) == 0
+    assert b.moe_dispatch_rows(c) == 0
+    assert b.moe_forward_launches(c) == 0
+    lib = b.lib
+    assert lib.moe_route(ctypes.byref(c), None, None, None, None, None, None, None, None, None) == 0
+    assert lib.moe_dispatch(ctypes.byref(c), *([None] * 10), 0, None) == 0
+    assert lib.moe_expert_ffn(ctypes.byref(c), *([None] * 11), 0, None) == 0
+    assert lib.moe_combine(ctypes.byref(c), *([None] * 7)) == 0
+    assert lib.moe_forward(ctypes.byref(c), *([None] * 13), 0, None) == 0
+
+
+def test_launch_counts():
+    assert b.moe_forward_launches(b.config(small_workload(k=2))) == 5
+    assert b.moe_forward_launches(b.config(small_workload(k=3))) == 6
+    assert b.moe_forward_launches(b.config(small_workload(k=2), flags=b.FLAG_UNFUSED_COMBINE)) == 6
+
+
+def test_status_strings():
+    for s in range(7):
+        assert b.moe_status_string(s) != "unknown status"
+    assert b.moe_status_string(99) == "unknown status"

@@ -1,0 +1,125 @@
+"""GPU parity of the CUDA path against the fp64 oracle, through the C ABI.
+
+Small workloads (several tiles and a ragged tail, every gate type, both dtypes, k from 1 to 4, with
+and without drops) compare every token; the five full-size workloads compare routing and dispatch on
+every token and the layer output on sampled tokens, in the launch configuration the benchmark uses."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from mixture_experts_sparse_03_b300 import binding as b
+from mixture_experts_sparse_03_b300.inputs import WORKLOADS, small_workload
+from tests import parity as P
+
+pytestmark = pytest.mark.gpu
+
+SMALL = [
+    small_workload(T=97, d=64, h=128, E=5, k=2, capacity_factor=1.0),
+    small_workload(T=300, d=128, h=256, E=8, k=2, capacity_factor=0.7),          # drops
+    small_workload(T=257, d=64, h=320, E=3, k=1, norm="all", capacity_factor=1.3),  # h not a multiple of 256
+    small_workload(T=200, d=192, h=192, E=6, k=3, capacity_factor=1.0),          # k > 2: gather combine
+    small_workload(T=150, d=64, h=128, E=16, k=4, capacity=150, bias="none"),     # dropless
+    small_workload(T=129, d=128, h=128, E=12, k=2, gate="noisy", capacity_factor=1.1),
+    small_workload(T=180, d=128, h=256, E=10, k=2, gate="cosine", cos_dim=64, capacity_factor=1.0,
+                   x_dist="clusters"),
+    small_workload(T=75, d=64, h=64, E=4, k=1, norm="all", dtype="f32", capacity_factor=1.2, bias="zero"),
+    small_workload(T=211, d=128, h=128, E=7, k=2, dtype="f32", capacity_factor=0.9),
+    small_workload(T=64, d=64, h=128, E=40, k=3, gate="noisy", dtype="f32", capacity_factor=1.5),
+    small_workload(T=1, d=64, h=64, E=2, k=1, capacity_factor=1.0),
+    small_workload(T=33, d=64, h=64, E=1, k=1, norm="all", capacity_factor=1.0),  # one expert: dense FFN
+]
+
+
+def _id(wl):
+    return "%s_%s_T%d_d%d_h%d_E%d_k%d" % (wl.gate, wl.dtype, wl.T, wl.d, wl.h, wl.E, wl.k)
+
+
+def _full_check(wl, flags=0):
+    tc, tg = P.inputs(wl)
+    g = P.run_steps(wl, tg, flags)
+    scores, nties, ndiff = P.check_routing(wl, tc, g)
+    C, slot = P.check_dispatch(wl, tc["x"], g)
+    toks = np.arange(wl.T, dtype=np.int32)
+    ref = P.oracle_out(wl, tc, tg, scores, g["idx"], slot, toks)
+    P.check_output(wl, g["out"], ref, toks)
+    out, count = P.run_forward(wl, tg, flags)
+    assert np.array_equal(count, g["count"])
+    P.check_output(wl, out, ref, toks)
+    return out
+
+
+@pytest.mark.parametrize("wl", SMALL, ids=_id)
+def test_small_parity(wl):
+    _full_check(wl)
+
+
+@pytest.mark.parametrize("wl", [SMALL[0], SMALL[3], SMALL[5], SMALL[6]], ids=_id)
+def test_small_parity_simt_ffn(wl):
+    """The CUDA-core FFN path of a bf16 layer agrees with the oracle too."""
+    _full_check(wl, flags=b.FLAG_SIMT_FFN)
+
+
+def test_unfused_combine_matches_fused():
+    wl = SMALL[1]
+    _, tg = P.inputs(wl)
+    fused, _ = P.run_forward(wl, tg)
+    unfused, _ = P.run_forward(wl, tg, flags=b.FLAG_UNFUSED_COMBINE)
+    assert np.allclose(fused, unfused, rtol=1e-6, atol=1e-6)
+
+
+def test_deterministic():
+    for wl in (SMALL[1], SMALL[3]):
+        _, tg = P.inputs(wl)
+        a, _ = P.run_forward(wl, tg)
+        b2, _ = P.run_forward(wl, tg)
+        assert np.array_equal(a.view(np.int32), b2.view(np.int32))
+
+
+def test_exact_ties_go_to_lower_expert():
+    wl = small_workload(T=64, d=64, h=64, E=6, k=3, capacity=64)
+    tc, tg = P.inputs(wl)
+    wg = tc["w_gate"].clone()
+    wg[3] = wg[1]
+    wg[5] = wg[0]
+    tc["w_gate"] = wg
+    tg["w_gate"] = wg.cuda()
+    g = P.run_steps(wl, tg)
+    P.check_routing(wl, tc, g)
+    for t in range(wl.T):
+        r = list(g["idx"][t])
+        if 1 in r and 3 in r:
+            assert r.index(1) < r.index(3)
+        if 0 in r and 5 in r:
+            assert r.index(0) < r.index(5)
+
+
+def test_all_dropped_outputs_zero():
+    wl = small_workload(T=50, d=64, h=64, E=4, k=2, capacity=0)
+    _, tg = P.inputs(wl)
+    out, count = P.run_forward(wl, tg)
+    assert np.all(out == 0.0) and count.sum() == 100
+
+
+def test_heavy_drops_and_bias():
+    wl = small_workload(T=400, d=64, h=128, E=4, k=2, capacity_factor=0.25, bias="normal")
+    _full_check(wl)
+
+
+@pytest.mark.parametrize("name", ["tiny_fp32", "bf16_e8_k2", "bf16_cosine_skew", "bf16_noisy_e64", "bf16_decode_e256"])
+def test_full_size_workload(name):
+    """Full sizes, launch configuration of the benchmark: routing and dispatch on every token, the
+    output on sampled tokens (all tokens for the tiny layer)."""
+    wl = WORKLOADS[name]
+    tc, tg = P.inputs(wl)
+    g = P.run_steps(wl, tg)
+    scores, nties, ndiff = P.check_routing(wl, tc, g)
+    C, slot = P.check_dispatch(wl, tc["x"], g)
+    n = {"tiny_fp32": wl.T, "bf16_e8_k2": 48, "bf16_cosine_skew": 48, "bf16_noisy_e64": 10, "bf16_decode_e256": 6}[name]
+    toks = P.sample_tokens(wl.T, n, seed=wl.seed)
+    ref = P.oracle_out(wl, tc, tg, scores, g["idx"], slot, toks)
+    P.check_output(wl, g["out"], ref, toks)
+    out, count = P.run_forward(wl, tg)
+    assert np.array_equal(count, g["count"])
+    P.check_output(wl, out, ref, toks)
+    print("%s: near-tie tokens %d, routing differences %d, drops %d" % (name, nties, ndiff, int((slot < 0).sum())))
