@@ -36,9 +36,8 @@ METRIC = "MoE layer fwd tokens/s on 1 B300; % of bf16 TC peak or HBM roofline"
 UNIT = "tokens/s"
 DEFAULT_WORKLOAD = "bf16_e8_k2"
 FLUSH_BYTES = 256 << 20
-KERNELS_FUSED = ["gate_topk", "dispatch_scan", "dispatch_assign_gather", "expert_up_gelu", "expert_down_combine"]
-KERNELS_UNFUSED = ["gate_topk", "dispatch_scan", "dispatch_assign_gather", "expert_up_gelu", "expert_down",
-                   "combine_gather"]
+KERNELS_FUSED = ["gate_topk_scan", "dispatch_assign_gather", "expert_up_gelu", "expert_down_combine"]
+KERNELS_UNFUSED = ["gate_topk_scan", "dispatch_assign_gather", "expert_up_gelu", "expert_down", "combine_gather"]
 
 
 def parse():
@@ -307,7 +306,7 @@ def run_ours(args, rank, world, local):
     ms_per_step = total_ms / K
 
     # ---- per-kernel durations (eager, trace events between the library's launches)
-    names = KERNELS_FUSED if launches_per_step == 5 else KERNELS_UNFUSED
+    names = KERNELS_FUSED if launches_per_step == 4 else KERNELS_UNFUSED
     per = {n: [] for n in names}
     tev = [torch.cuda.Event(enable_timing=True) for _ in range(launches_per_step + 1)]
     for e in tev:  # torch creates the CUDA event at its first record; the library needs real handles
@@ -318,10 +317,11 @@ def run_ours(args, rank, world, local):
             flush.fill_(1)
             keep = b.moe_trace_events(tev, len(tev))
             step()
+            recorded = b.moe_trace_count()
             b.moe_trace_events(None, 0)
             stream.synchronize()
-            if b.moe_trace_count() != len(tev):
-                raise RuntimeError("trace hook recorded %d of %d events" % (b.moe_trace_count(), len(tev)))
+            if recorded != len(tev):
+                raise RuntimeError("trace hook recorded %d of %d events" % (recorded, len(tev)))
             for j, n in enumerate(names):
                 per[n].append(tev[j].elapsed_time(tev[j + 1]))
             del keep

@@ -208,8 +208,8 @@ MOE_API moe_status moe_device_status(void* workspace, size_t workspace_bytes, in
  * the library records events[0] on the launch stream before the first kernel it launches after this
  * call, and events[i] right after the i-th such kernel, until `capacity` events are used; n kernels
  * thus use n + 1 events and kernel i ran between events[i] and events[i+1].  moe_trace_count()
- * returns how many events have been recorded.  events == NULL turns the hook off.  Not thread-safe;
- * meant for benchmarks. */
+ * returns how many events the current (or, once turned off, the last) trace recorded.  events == NULL
+ * turns the hook off.  Not thread-safe; meant for benchmarks. */
 MOE_API void    moe_trace_events(void** events, int32_t capacity);
 MOE_API int32_t moe_trace_count(void);
 

@@ -10,10 +10,6 @@
 #include "kernels.h"
 #include "moe_b300.h"
 
-namespace moe {
-size_t gate_smem_bytes(int gate, int E, int p);
-}
-
 namespace {
 
 using namespace moe;
@@ -65,7 +61,7 @@ moe_status make_plan(const moe_config* c, Plan* pl) {
         if (!(v >= 0.0) || v > 2147483647.0) return MOE_ERR_INVALID_ARG;
         P.C = (int)v;
     }
-    if (gate_smem_bytes(P.gate, P.E, P.p) > (size_t)kMaxSmem) return MOE_ERR_UNSUPPORTED;
+    if (gate_smem_bytes(P.gate, P.E, P.p, P.d) > (size_t)kMaxSmem) return MOE_ERR_UNSUPPORTED;
     P.Ceff = std::min(P.C, P.T);  // a token takes an expert at most once, so C >= T drops nothing
     const int64_t cpad = ((int64_t)P.Ceff + kRowAlign - 1) / kRowAlign * kRowAlign;
     P.rows = std::min<int64_t>((int64_t)P.T * P.k + (int64_t)(kRowAlign - 1) * P.E, (int64_t)P.E * cpad);
@@ -234,7 +230,7 @@ int32_t moe_forward_launches(const moe_config* cfg) {
     Plan P;
     if (make_plan(cfg, &P) != MOE_OK) return -1;
     if (P.T == 0) return 0;
-    return P.fused ? 5 : 6;
+    return P.fused ? 4 : 5;
 }
 
 moe_status moe_route(const moe_config* cfg, const void* x, const void* w_gate, const void* w_noise,
@@ -333,12 +329,18 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const void* w_gate,
     float* rgate = at<float>(workspace, P.o_rgate);
     void* xd = at<void>(workspace, P.o_xd);
     float* y = at<float>(workspace, P.o_y);
-    if (cudaMemsetAsync(err, 0, 8, s) != cudaSuccess) return MOE_ERR_CUDA;
+    // error word, its info and the gate's block ticket start at zero
+    if (cudaMemsetAsync(err, 0, 16, s) != cudaSuccess) return MOE_ERR_CUDA;
     GateParams g = gate_params(P, cfg, x, w_gate, w_noise, noise_eps, proj, expert_emb, idx, gate);
     g.blk_hist = hist;
     g.err = err;
+    g.ticket = err + 2;
+    g.C = P.Ceff;
+    g.count = count;
+    g.offset = off;
+    g.row_token = rtok;
+    g.row_gate = rgate;
     MOE_TRY(launch(s, [&] { return launch_gate(g, s); }));
-    MOE_TRY(launch(s, [&] { return launch_dispatch_scan(hist, P.T, P.k, P.E, P.Ceff, count, off, rtok, rgate, s); }));
     MOE_TRY(launch(s, [&] {
         return launch_dispatch_assign(x, P.bf16, idx, gate, hist, off, P.T, P.k, P.E, P.d, P.Ceff, slot, rtok, rgate,
                                       xd, P.fused ? out : nullptr, err, s);
@@ -361,8 +363,13 @@ moe_status moe_device_status(void* workspace, size_t workspace_bytes, int32_t* i
 }
 
 void moe_trace_events(void** events, int32_t capacity) {
-    g_events = capacity > 0 ? events : nullptr;
-    g_capacity = capacity > 0 ? capacity : 0;
+    if (events == nullptr || capacity <= 0) {  // off; the count of the last trace stays readable
+        g_events = nullptr;
+        g_capacity = 0;
+        return;
+    }
+    g_events = events;
+    g_capacity = capacity;
     g_recorded = 0;
 }
 

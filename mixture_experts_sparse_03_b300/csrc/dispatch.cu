@@ -6,7 +6,8 @@
 // acceleration", section 3.2), with overflow pairs dropped.
 // Slot of pair (t, e) = number of pairs of earlier tokens routed to e; kept iff slot < C.
 //
-// Three steps over blocks of 32 tokens (the gate kernel's blocks, so it can produce step 1 itself):
+// Three steps over blocks of 32 tokens (the gate kernel's blocks, so within moe_forward the gate
+// produces step 1 and its last block runs step 2, see scan.cuh):
 //   count   per-block expert histogram                          blk_hist[b][e]
 //   scan    per expert: exclusive prefix over blocks (in place), total count, kept = min(count, C),
 //           padded segment offsets off[e] = sum_{e'<e} roundup(kept[e'], 128), padding rows marked
@@ -17,6 +18,7 @@
 // No step depends on scheduling order, so the result is deterministic.
 #include "common.cuh"
 #include "kernels.h"
+#include "scan.cuh"
 
 namespace moe {
 
@@ -46,83 +48,20 @@ __global__ void __launch_bounds__(256) count_kernel(const int* __restrict__ topk
     for (int e = threadIdx.x; e < E; e += blockDim.x) blk_hist[(size_t)blockIdx.x * E + e] = hist[e];
 }
 
-// one block of 1024 threads; `tpe` threads per expert split the blocks into contiguous ranges
-__global__ void __launch_bounds__(1024) scan_kernel(int* __restrict__ blk_hist, int nblk, int E, int C, int tpe,
+// one block of 1024 threads
+__global__ void __launch_bounds__(1024) scan_kernel(int* __restrict__ blk_hist, int nblk, int E, int C,
                                                     int* __restrict__ count, int* __restrict__ offset,
                                                     int* __restrict__ row_token, float* __restrict__ row_gate) {
     __shared__ int part[1024];
     __shared__ int padded[kMaxExperts + 1];
-    __shared__ int keptv[kMaxExperts];
-    const int tid = threadIdx.x;
-    const int e = tid / tpe, sub = tid % tpe;
-    const bool active = e < E;
-    const int per = (nblk + tpe - 1) / tpe;
-    const int b0 = min(nblk, sub * per), b1 = min(nblk, b0 + per);
-    int s = 0;
-    if (active)
-        for (int b = b0; b < b1; ++b) s += blk_hist[(size_t)b * E + e];
-    part[tid] = s;
-    __syncthreads();
-    int prefix = 0;
-    if (active)
-        for (int q = 0; q < sub; ++q) prefix += part[e * tpe + q];
-    if (active) {
-        int run = prefix;
-        for (int b = b0; b < b1; ++b) {
-            int c = blk_hist[(size_t)b * E + e];
-            blk_hist[(size_t)b * E + e] = run;
-            run += c;
-        }
-        if (sub == tpe - 1) {
-            count[e] = run;
-            int kept = min(run, C);
-            keptv[e] = kept;
-            padded[e] = (kept + kRowAlign - 1) / kRowAlign * kRowAlign;
-        }
-    }
-    __syncthreads();
-    {  // exclusive scan of the padded sizes over E <= 1024 values: warp scans, then warp totals
-        __shared__ int wsum[32];
-        const int lane = tid & 31, warp = tid >> 5;
-        const int v = tid < E ? padded[tid] : 0;
-        int inc = v;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            int o = __shfl_up_sync(0xffffffffu, inc, off);
-            if (lane >= off) inc += o;
-        }
-        if (lane == 31) wsum[warp] = inc;
-        __syncthreads();
-        if (warp == 0) {
-            int w = wsum[lane];
-            int winc = w;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                int o = __shfl_up_sync(0xffffffffu, winc, off);
-                if (lane >= off) winc += o;
-            }
-            wsum[lane] = winc - w;  // exclusive prefix of the warp totals
-        }
-        __syncthreads();
-        const int excl = wsum[warp] + inc - v;
-        __syncthreads();
-        if (tid < E) padded[tid] = excl;
-        if (tid == E - 1) padded[E] = excl + v;
-    }
-    __syncthreads();
-    for (int q = tid; q <= E; q += blockDim.x) offset[q] = padded[q];
-    // mark the padding rows of each expert's segment (the expert's tpe threads share the work)
-    if (active) {
-        const int r0 = padded[e] + keptv[e], r1 = padded[e + 1];
-        for (int r = r0 + sub; r < r1; r += tpe) {
-            row_token[r] = -1;
-            row_gate[r] = 0.f;
-        }
-    }
+    __shared__ int kept[kMaxExperts];
+    __shared__ int wsum[33];
+    ScanSmem sm{part, padded, kept, wsum};
+    scan_experts(blk_hist, nblk, E, C, count, offset, row_token, row_gate, sm);
 }
 
 template <typename T>
-__global__ void __launch_bounds__(256) assign_kernel(const T* __restrict__ x, const int* __restrict__ topk_idx,
+__global__ void __launch_bounds__(1024) assign_kernel(const T* __restrict__ x, const int* __restrict__ topk_idx,
                                                      const float* __restrict__ topk_gate,
                                                      const int* __restrict__ blk_base, const int* __restrict__ offset,
                                                      int T_, int k, int E, int d, int C, int* __restrict__ slot,
@@ -166,7 +105,7 @@ __global__ void __launch_bounds__(256) assign_kernel(const T* __restrict__ x, co
         }
     }
     __syncthreads();
-    // row gather, 16 bytes per lane per step
+    // row gather, 16 bytes per lane per step, four loads in flight per lane
     constexpr int V = 16 / sizeof(T);
     const int nv = d / V;
     for (int p = warp; p < npairs; p += blockDim.x / 32) {
@@ -174,7 +113,15 @@ __global__ void __launch_bounds__(256) assign_kernel(const T* __restrict__ x, co
         if (r < 0) continue;
         const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)(t0 + p / k) * d);
         uint4* dst = reinterpret_cast<uint4*>(xd + (size_t)r * d);
-        for (int i = lane; i < nv; i += 32) dst[i] = src[i];
+        for (int i0 = lane; i0 < nv; i0 += 4 * 32) {
+            uint4 v[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (i0 + j * 32 < nv) v[j] = __ldg(src + i0 + j * 32);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (i0 + j * 32 < nv) dst[i0 + j * 32] = v[j];
+        }
     }
     if (out_zero != nullptr) {
         const int n4 = d / 4;
@@ -199,9 +146,7 @@ cudaError_t launch_dispatch_scan(int* blk_hist, int T, int k, int E, int C, int*
     (void)k;
     if (T <= 0) return cudaSuccess;
     const int nblk = (T + kBT - 1) / kBT;
-    int tpe = 1;
-    while (tpe * 2 * E <= 1024 && tpe * 2 <= nblk) tpe *= 2;
-    scan_kernel<<<1, 1024, 0, s>>>(blk_hist, nblk, E, C, tpe, count, offset, row_token, row_gate);
+    scan_kernel<<<1, 1024, 0, s>>>(blk_hist, nblk, E, C, count, offset, row_token, row_gate);
     return cudaGetLastError();
 }
 
@@ -212,11 +157,11 @@ cudaError_t launch_dispatch_assign(const void* x, int bf16, const int* topk_idx,
     if (T <= 0) return cudaSuccess;
     const int blocks = (T + kBT - 1) / kBT;
     if (bf16)
-        assign_kernel<bf16_t><<<blocks, 256, 0, s>>>(static_cast<const bf16_t*>(x), topk_idx, topk_gate, blk_hist,
+        assign_kernel<bf16_t><<<blocks, 1024, 0, s>>>(static_cast<const bf16_t*>(x), topk_idx, topk_gate, blk_hist,
                                                      offset, T, k, E, d, C, slot, row_token, row_gate,
                                                      static_cast<bf16_t*>(x_dispatched), out_to_zero, err);
     else
-        assign_kernel<float><<<blocks, 256, 0, s>>>(static_cast<const float*>(x), topk_idx, topk_gate, blk_hist,
+        assign_kernel<float><<<blocks, 1024, 0, s>>>(static_cast<const float*>(x), topk_idx, topk_gate, blk_hist,
                                                     offset, T, k, E, d, C, slot, row_token, row_gate,
                                                     static_cast<float*>(x_dispatched), out_to_zero, err);
     return cudaGetLastError();

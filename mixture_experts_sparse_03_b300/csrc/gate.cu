@@ -8,11 +8,14 @@
 // card" (section 3.3) recommends fusing the gate with the expert selection in one CUDA kernel; this is
 // that kernel.
 //
-// One block = 32 tokens, 256 threads, three phases:
+// One block = 32 tokens, three phases:
 //  1. logits [32, N] into shared memory (N = E, 2E for the noisy gate, cos_dim for the cosine gate).
-//     Products are summed in fp32 over chunks of 32, and the chunk sums are added with TwoSum
-//     compensation, so each logit's error is at most 31 u sum|x_i w_i| + u |logit| <= 33 u |x| |w|
-//     (u = 2^-24; Cauchy-Schwarz), a bound the kernel evaluates per token from the row norms.
+//     Small gates (N <= 16, N * d <= 16384: the weight fits in shared memory) use 512 threads, one warp
+//     per token (two per warp in turn), the weight staged once per block; larger gates use 256 threads
+//     and a tiled SIMT GEMM over 32-wide reduction chunks.  Either way products are summed in fp32
+//     over chunks of at most 32, and the chunk sums are added with TwoSum compensation, so each
+//     logit's error is at most 31 u sum|x_i w_i| + u |logit| <= 33 u |x| |w| (u = 2^-24;
+//     Cauchy-Schwarz), a bound the kernel evaluates per token from the row norms.
 //  2. one warp per token: scores, top-(k+1) by warp-shuffle argmax (ties -> lower expert id), and a
 //     bound on the fp32 score error.  If two of the top-k scores, or the k-th and (k+1)-th, lie within
 //     twice that bound, the token is queued for re-scoring; otherwise its choice is provably the
@@ -21,21 +24,21 @@
 //     within twice the bound of the k-th best) with float-float dot products (TwoProduct/TwoSum,
 //     about 48 bits) and picks the top-k of those by the exact scores.
 // The gate weights use the fp32 scores (they are continuous in the scores; only the choice is
-// discrete).  Optionally the block also writes the expert histogram of its 32 tokens, which is the
-// first step of the dispatch.
+// discrete).  Optionally the block also writes the expert histogram of its 32 tokens (the first step
+// of the dispatch), and the last block to finish runs the dispatch scan over all histograms.
 #include <float.h>
 #include <math.h>
 
 #include "common.cuh"
 #include "kernels.h"
+#include "scan.cuh"
 
 namespace moe {
 
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
 constexpr int kBT = kTokensPerBlock;   // 32 tokens per block
+constexpr int kSmallElems = 16384;     // N * d at or below which the weight is staged whole
 constexpr int kKC = 32;                // reduction chunk
 constexpr int kXSS = kBT + 1;          // shared stride of the transposed x tile
 constexpr int kMaxCand = 64;           // contenders re-scored per token
@@ -46,13 +49,15 @@ struct Layout {
     int N;       // logits per token
     int BN;      // logits per pass
     int stage;   // cosine: expert embeddings staged (transposed) in shared memory
-    size_t logits, xs, ws, wn2, xn2, sc, embs, embn, selv, seli, rl_tok, rl_n, rl_m, rl_den, rl_cand,
-        rl_sc, fidx, hist, ex, uex, nref, total;
+    size_t logits, xs, ws, wst, wn2, xn2, sc, embs, embn, selv, seli, rl_tok, rl_n, rl_m, rl_den, rl_cand,
+        rl_sc, fidx, hist, ex, uex, nref, scan_part, scan_padded, scan_kept, scan_wsum, total;
 };
 
 __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-__host__ __device__ inline Layout make_layout(int gate, int E, int p, int BN, int stage) {
+__host__ __device__ inline Layout make_layout(int gate, int E, int p, int d, int BN, int stage, bool small,
+                                              int nthreads) {
+    const int nwarps = nthreads / 32;
     Layout L;
     L.N = gate == kGateSoftmax ? E : gate == kGateNoisy ? 2 * E : p;
     L.BN = BN;
@@ -60,15 +65,16 @@ __host__ __device__ inline Layout make_layout(int gate, int E, int p, int BN, in
     size_t o = 0;
     auto take = [&](size_t bytes, size_t al) { o = align_up(o, al); size_t r = o; o += bytes; return r; };
     L.logits = take(sizeof(float) * kBT * L.N, 16);
-    L.xs = take(sizeof(float) * kKC * kXSS, 16);
-    L.ws = take(sizeof(float) * kKC * (BN + 1), 16);
+    L.xs = take(small ? 0 : sizeof(float) * kKC * kXSS, 16);
+    L.ws = take(small ? 0 : sizeof(float) * kKC * (BN + 1), 16);
+    L.wst = take(small ? sizeof(float) * (size_t)L.N * d : 0, 16);
     L.wn2 = take(sizeof(float) * L.N, 16);
     L.xn2 = take(sizeof(float) * kBT, 16);
-    L.sc = take(sizeof(float) * kWarps * E, 16);
+    L.sc = take(sizeof(float) * nwarps * E, 16);
     L.embs = take(stage ? sizeof(float) * E * p : 0, 16);
     L.embn = take(gate == kGateCosine ? sizeof(float) * E : 0, 16);
-    L.selv = take(sizeof(float) * kWarps * (kMaxTopK + 1), 16);
-    L.seli = take(sizeof(int) * kWarps * (kMaxTopK + 1), 16);
+    L.selv = take(sizeof(float) * nwarps * (kMaxTopK + 1), 16);
+    L.seli = take(sizeof(int) * nwarps * (kMaxTopK + 1), 16);
     L.rl_tok = take(sizeof(int) * kBT, 16);
     L.rl_n = take(sizeof(int) * kBT, 16);
     L.rl_m = take(sizeof(float) * kBT, 16);
@@ -80,6 +86,10 @@ __host__ __device__ inline Layout make_layout(int gate, int E, int p, int BN, in
     L.ex = take(sizeof(double) * kMaxCand, 16);
     L.uex = take(gate == kGateCosine ? sizeof(double) * p : 0, 16);
     L.nref = take(sizeof(int) * 4, 16);
+    L.scan_part = take(sizeof(int) * nthreads, 16);
+    L.scan_padded = take(sizeof(int) * (E + 1), 16);
+    L.scan_kept = take(sizeof(int) * E, 16);
+    L.scan_wsum = take(sizeof(int) * 33, 16);
     L.total = align_up(o, 16);
     return L;
 }
@@ -117,16 +127,19 @@ __device__ __forceinline__ double warp_dot_ff(const T* a, const T* b, int d, int
     return (double)hi + (double)lo;
 }
 
-template <typename T, int GATE, int TM, int TN, int TX>
-__global__ void __launch_bounds__(kThreads) gate_kernel(const GateParams P, const int stage) {
-    constexpr int TY = kThreads / TX;
+template <typename T, int GATE, int TM, int TN, int TX, bool SMALL>
+__global__ void __launch_bounds__(SMALL ? 512 : 256) gate_kernel(const GateParams P, const int stage) {
+    constexpr int NT = SMALL ? 512 : 256;
+    constexpr int NW = NT / 32;
+    constexpr int TY = 256 / TX;
     constexpr int BN = TN * TX;
-    static_assert(TM * TY == kBT, "a block covers 32 tokens");
+    static_assert(SMALL || TM * TY == kBT, "a block covers 32 tokens");
     extern __shared__ __align__(16) unsigned char smem[];
-    const Layout L = make_layout(GATE, P.E, P.p, BN, stage);
+    const Layout L = make_layout(GATE, P.E, P.p, P.d, BN, stage, SMALL, NT);
     float* logits = reinterpret_cast<float*>(smem + L.logits);
     float* xs = reinterpret_cast<float*>(smem + L.xs);
     float* ws = reinterpret_cast<float*>(smem + L.ws);
+    float* wst = reinterpret_cast<float*>(smem + L.wst);
     float* wn2 = reinterpret_cast<float*>(smem + L.wn2);
     float* xn2 = reinterpret_cast<float*>(smem + L.xn2);
     float* scw = reinterpret_cast<float*>(smem + L.sc);
@@ -156,6 +169,79 @@ __global__ void __launch_bounds__(kThreads) gate_kernel(const GateParams P, cons
     if (tid == 0) nref[0] = 0;
 
     // ---------------------------------------------------------------- phase 1: logits [32, N]
+    if constexpr (SMALL) {
+        // stage the N weight rows (fp32) and their squared norms
+        for (int i = tid * 8; i < N * d; i += NT * 8) {
+            const int n = i / d, c = i % d;
+            float v[8];
+            load8(logit_row<T>(P, GATE, n) + c, v);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) wst[i + j] = v[j];
+        }
+        __syncthreads();
+        for (int n = warp; n < N; n += NW) {
+            float q = 0.f;
+            for (int c = lane; c < d; c += 32) q = fmaf(wst[n * d + c], wst[n * d + c], q);
+            q = warp_sum(q);
+            if (lane == 0) wn2[n] = q;
+        }
+        // one warp per token: lane owns the 8-element slices lane*8 + 256*j of the row
+        for (int tt = warp; tt < kBT; tt += NW) {
+            float hi[16], lo[16];
+#pragma unroll
+            for (int n = 0; n < 16; ++n) hi[n] = lo[n] = 0.f;
+            float sq = 0.f;
+            if (tt < ntok) {
+                const T* xr = x + (size_t)(tok0 + tt) * d;
+                for (int c0 = lane * 8; c0 < d; c0 += 4 * 256) {  // up to 4 slices = 32 products per chunk
+                    float xv[4][8];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int c = c0 + j * 256;
+                        if (c < d) load8(xr + c, xv[j]);
+                        else {
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) xv[j][q] = 0.f;
+                        }
+                    }
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) sq = fmaf(xv[j][q], xv[j][q], sq);
+#pragma unroll
+                    for (int n = 0; n < 16; ++n) {
+                        if (n >= N) break;
+                        float c = 0.f;
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const int col = c0 + j * 256;
+                            if (col < d) {
+                                const float4 w0 = *reinterpret_cast<const float4*>(wst + n * d + col);
+                                const float4 w1 = *reinterpret_cast<const float4*>(wst + n * d + col + 4);
+                                c = fmaf(xv[j][0], w0.x, c); c = fmaf(xv[j][1], w0.y, c);
+                                c = fmaf(xv[j][2], w0.z, c); c = fmaf(xv[j][3], w0.w, c);
+                                c = fmaf(xv[j][4], w1.x, c); c = fmaf(xv[j][5], w1.y, c);
+                                c = fmaf(xv[j][6], w1.z, c); c = fmaf(xv[j][7], w1.w, c);
+                            }
+                        }
+                        float s_, e_;
+                        two_sum(hi[n], c, s_, e_);
+                        hi[n] = s_;
+                        lo[n] += e_;
+                    }
+                }
+            }
+            // compensated butterfly: every lane ends with the full sums
+#pragma unroll
+            for (int n = 0; n < 16; ++n) {
+                if (n >= N) break;
+                ff_warp_sum(hi[n], lo[n]);
+                if (lane == n) logits[tt * N + n] = hi[n] + lo[n];
+            }
+            sq = warp_sum(sq);
+            if (lane == 0) xn2[tt] = sq;
+        }
+    } else {
     const int ty = tid / TX, tx = tid % TX;
     const int lrow = tid >> 2, lc8 = (tid & 3) * 8;  // loaders: 4 threads per row, 8 elements each
     const T* xrow = (tid < 4 * kBT && lrow < ntok) ? x + (size_t)(tok0 + lrow) * d : nullptr;
@@ -238,10 +324,11 @@ __global__ void __launch_bounds__(kThreads) gate_kernel(const GateParams P, cons
     sqx += __shfl_xor_sync(0xffffffffu, sqx, 1);
     sqx += __shfl_xor_sync(0xffffffffu, sqx, 2);
     if (tid < 4 * kBT && (tid & 3) == 0) xn2[lrow] = sqx;
+    }  // tiled phase 1
 
     if (GATE == kGateCosine) {  // expert embedding norms (and a transposed copy if it fits)
         const T* emb = static_cast<const T*>(P.emb);
-        for (int e = warp; e < E; e += kWarps) {
+        for (int e = warp; e < E; e += NW) {
             float s = 0.f;
             for (int j = lane * 8; j < P.p; j += 32 * 8) {
                 float v[8];
@@ -263,7 +350,7 @@ __global__ void __launch_bounds__(kThreads) gate_kernel(const GateParams P, cons
     float* selv = selv_all + warp * (kMaxTopK + 1);
     int* seli = seli_all + warp * (kMaxTopK + 1);
     const int ksel = min(k + 1, E);
-    for (int tt = warp; tt < ntok; tt += kWarps) {
+    for (int tt = warp; tt < ntok; tt += NW) {
         const int t = tok0 + tt;
         const float* Lr = logits + tt * N;
         const float xn = sqrtf(xn2[tt]);
@@ -398,13 +485,13 @@ __global__ void __launch_bounds__(kThreads) gate_kernel(const GateParams P, cons
         const int* cand = rl_cand + q * kMaxCand;
         if (GATE == kGateCosine) {
             const T* proj = static_cast<const T*>(P.proj);
-            for (int j = warp; j < P.p; j += kWarps) {
+            for (int j = warp; j < P.p; j += NW) {
                 double u = warp_dot_ff<T>(xr, proj + (size_t)j * d, d, lane);
                 if (lane == 0) uex[j] = u;
             }
             __syncthreads();
             const T* emb = static_cast<const T*>(P.emb);
-            for (int c = warp; c < nc; c += kWarps) {
+            for (int c = warp; c < nc; c += NW) {
                 const int e = cand[c];
                 double dot = 0.0, ne2 = 0.0, nu2 = 0.0;
                 for (int j = lane; j < P.p; j += 32) {
@@ -420,7 +507,7 @@ __global__ void __launch_bounds__(kThreads) gate_kernel(const GateParams P, cons
                 if (lane == 0) ex[c] = dot / (fmax(sqrt(nu2), 1e-12) * fmax(sqrt(ne2), 1e-12)) / P.temp;
             }
         } else {
-            for (int c = warp; c < nc; c += kWarps) {
+            for (int c = warp; c < nc; c += NW) {
                 const int e = cand[c];
                 double s = warp_dot_ff<T>(xr, logit_row<T>(P, GATE, e), d, lane);
                 if (GATE == kGateNoisy) {
@@ -461,38 +548,61 @@ __global__ void __launch_bounds__(kThreads) gate_kernel(const GateParams P, cons
 
     // ---------------------------------------------------------------- expert histogram of the block
     if (P.blk_hist != nullptr) {
-        for (int e = tid; e < E; e += kThreads) hist[e] = 0;
+        for (int e = tid; e < E; e += NT) hist[e] = 0;
         __syncthreads();
-        for (int i = tid; i < ntok * k; i += kThreads) atomicAdd(&hist[fidx[(i / k) * kMaxTopK + i % k]], 1);
+        for (int i = tid; i < ntok * k; i += NT) atomicAdd(&hist[fidx[(i / k) * kMaxTopK + i % k]], 1);
         __syncthreads();
-        for (int e = tid; e < E; e += kThreads) P.blk_hist[(size_t)blockIdx.x * E + e] = hist[e];
+        for (int e = tid; e < E; e += NT) P.blk_hist[(size_t)blockIdx.x * E + e] = hist[e];
+        if (P.ticket != nullptr) {  // the last block to finish runs the dispatch scan
+            __threadfence();
+            __syncthreads();
+            if (tid == 0) nref[1] = atomicAdd(P.ticket, 1);
+            __syncthreads();
+            if (nref[1] == (int)gridDim.x - 1) {
+                __threadfence();
+                ScanSmem sm;
+                sm.part = reinterpret_cast<int*>(smem + L.scan_part);
+                sm.padded = reinterpret_cast<int*>(smem + L.scan_padded);
+                sm.kept = reinterpret_cast<int*>(smem + L.scan_kept);
+                sm.wsum = reinterpret_cast<int*>(smem + L.scan_wsum);
+                scan_experts(P.blk_hist, gridDim.x, E, P.C, P.count, P.offset, P.row_token, P.row_gate, sm);
+                if (tid == 0) *P.ticket = 0;  // ready for the next call
+            }
+        }
     }
 }
 
-template <typename T, int GATE, int TM, int TN, int TX>
+bool use_small(int gate, int E, int p, int d) {
+    const int N = gate == kGateSoftmax ? E : gate == kGateNoisy ? 2 * E : p;
+    return N <= 16 && N * d <= kSmallElems;
+}
+
+template <typename T, int GATE, int TM, int TN, int TX, bool SMALL>
 cudaError_t launch_cfg(const GateParams& P, cudaStream_t s) {
     constexpr int BN = TN * TX;
-    Layout L0 = make_layout(GATE, P.E, P.p, BN, 0);
+    constexpr int NT = SMALL ? 512 : 256;
+    Layout L0 = make_layout(GATE, P.E, P.p, P.d, BN, 0, SMALL, NT);
     int stage = 0;
     if (GATE == kGateCosine) {
-        Layout L1 = make_layout(GATE, P.E, P.p, BN, 1);
+        Layout L1 = make_layout(GATE, P.E, P.p, P.d, BN, 1, SMALL, NT);
         if (L1.total <= 200 * 1024) { stage = 1; L0 = L1; }
     }
-    auto kern = gate_kernel<T, GATE, TM, TN, TX>;
+    auto kern = gate_kernel<T, GATE, TM, TN, TX, SMALL>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L0.total);
     if (e != cudaSuccess) return e;
     const int blocks = (P.T + kBT - 1) / kBT;
-    kern<<<blocks, kThreads, L0.total, s>>>(P, stage);
+    kern<<<blocks, NT, L0.total, s>>>(P, stage);
     return cudaGetLastError();
 }
 
 template <typename T, int GATE>
 cudaError_t launch_gate_t(const GateParams& P, cudaStream_t s) {
     const int N = GATE == kGateSoftmax ? P.E : GATE == kGateNoisy ? 2 * P.E : P.p;
-    if (N <= 8) return launch_cfg<T, GATE, 1, 1, 8>(P, s);
-    if (N <= 16) return launch_cfg<T, GATE, 1, 2, 8>(P, s);
-    if (N <= 32) return launch_cfg<T, GATE, 2, 2, 16>(P, s);
-    return launch_cfg<T, GATE, 2, 4, 16>(P, s);
+    if (use_small(GATE, P.E, P.p, P.d)) return launch_cfg<T, GATE, 1, 1, 8, true>(P, s);
+    if (N <= 8) return launch_cfg<T, GATE, 1, 1, 8, false>(P, s);
+    if (N <= 16) return launch_cfg<T, GATE, 1, 2, 8, false>(P, s);
+    if (N <= 32) return launch_cfg<T, GATE, 2, 2, 16, false>(P, s);
+    return launch_cfg<T, GATE, 2, 4, 16, false>(P, s);
 }
 
 template <typename T>
@@ -506,10 +616,11 @@ cudaError_t launch_gate_d(const GateParams& P, cudaStream_t s) {
 
 }  // namespace
 
-size_t gate_smem_bytes(int gate, int E, int p) {
+size_t gate_smem_bytes(int gate, int E, int p, int d) {
     const int N = gate == kGateSoftmax ? E : gate == kGateNoisy ? 2 * E : p;
-    const int BN = N <= 8 ? 8 : N <= 16 ? 16 : N <= 32 ? 32 : 64;
-    return make_layout(gate, E, p, BN, 0).total;
+    const bool small = use_small(gate, E, p, d);
+    const int BN = small ? 8 : N <= 8 ? 8 : N <= 16 ? 16 : N <= 32 ? 32 : 64;
+    return make_layout(gate, E, p, d, BN, 0, small, small ? 512 : 256).total;
 }
 
 cudaError_t launch_gate(const GateParams& P, cudaStream_t s) {

@@ -28,7 +28,15 @@ struct GateParams {
     float* topk_gate;       // [T, k]
     int* blk_hist;          // [ceil(T/32), E] per-block expert histogram, or nullptr
     int* err;               // error word or nullptr
+    // dispatch scan fused into the gate's last block (when ticket != nullptr; needs blk_hist)
+    int* ticket;            // zero-initialised counter of finished blocks (reset by the last block)
+    int C;                  // capacity
+    int* count;             // [E]
+    int* offset;            // [E+1]
+    int* row_token;         // padding rows get -1
+    float* row_gate;        // padding rows get 0
 };
+size_t gate_smem_bytes(int gate, int E, int p, int d);
 cudaError_t launch_gate(const GateParams& p, cudaStream_t s);
 
 // ---- dispatch ---------------------------------------------------------------------------------

@@ -129,9 +129,9 @@ def test_empty_input_is_a_no_op():
 
 
 def test_launch_counts():
-    assert b.moe_forward_launches(b.config(small_workload(k=2))) == 5
-    assert b.moe_forward_launches(b.config(small_workload(k=3))) == 6
-    assert b.moe_forward_launches(b.config(small_workload(k=2), flags=b.FLAG_UNFUSED_COMBINE)) == 6
+    assert b.moe_forward_launches(b.config(small_workload(k=2))) == 4
+    assert b.moe_forward_launches(b.config(small_workload(k=3))) == 5
+    assert b.moe_forward_launches(b.config(small_workload(k=2), flags=b.FLAG_UNFUSED_COMBINE)) == 5
 
 
 def test_status_strings():

@@ -94,6 +94,41 @@ def test_exact_ties_go_to_lower_expert():
             assert r.index(0) < r.index(5)
 
 
+def _ulp_step(w: torch.Tensor, up: bool) -> torch.Tensor:
+    """The next bf16 value above (or below) each element of a bf16 tensor."""
+    bits = w.view(torch.int16).to(torch.int32)
+    away = (bits >= 0) == up  # moving away from zero increments the magnitude bits
+    nb = torch.where(away, bits + 1, bits - 1)
+    return nb.to(torch.int16).view(torch.bfloat16)
+
+
+@pytest.mark.parametrize("gate", ["softmax", "noisy"])
+def test_near_ties_resolved_exactly(gate):
+    """Gate rows that differ from another row by one bf16 ulp in one element: their scores differ by
+    1e-7 to 1e-3, often inside the fp32 error bound, so the kernel must settle the order with its
+    float-float re-scoring.  The choice must equal the oracle's on every token."""
+    wl = small_workload(T=256, d=256, h=64, E=6, k=2, gate=gate, capacity=256)
+    tc, tg = P.inputs(wl)
+    wg = tc["w_gate"].clone()
+    wg[2] = wg[0]
+    wg[2, 5] = _ulp_step(wg[0, 5:6], True)[0]
+    wg[4] = wg[1]
+    wg[4, 17] = _ulp_step(wg[1, 17:18], False)[0]
+    tc["w_gate"] = wg
+    tg["w_gate"] = wg.cuda()
+    if gate == "noisy":
+        wn = tc["w_noise"].clone()
+        wn[2] = wn[0]
+        wn[4] = wn[1]
+        tc["w_noise"] = wn
+        tg["w_noise"] = wn.cuda()
+    g = P.run_steps(wl, tg)
+    scores, nties, ndiff = P.check_routing(wl, tc, g)
+    assert ndiff == 0
+    gaps = np.abs(scores[:, 2] - scores[:, 0])
+    assert gaps.max() > 0 and np.median(gaps) < 1e-3  # the pairs really are near ties
+
+
 def test_all_dropped_outputs_zero():
     wl = small_workload(T=50, d=64, h=64, E=4, k=2, capacity=0)
     _, tg = P.inputs(wl)
