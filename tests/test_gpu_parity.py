@@ -122,6 +122,12 @@ def test_near_ties_resolved_exactly(gate):
         wn[4] = wn[1]
         tc["w_noise"] = wn
         tg["w_noise"] = wn.cuda()
+        # the noise term of a copied row must match too, so its draws are copied as well
+        ep = tc["eps"].clone()
+        ep[:, 2] = ep[:, 0]
+        ep[:, 4] = ep[:, 1]
+        tc["eps"] = ep
+        tg["eps"] = ep.cuda()
     g = P.run_steps(wl, tg)
     scores, nties, ndiff = P.check_routing(wl, tc, g)
     assert ndiff == 0
