@@ -161,6 +161,33 @@ MOE_API moe_status moe_dispatch(const moe_config* cfg, const void* x, const int3
                         int32_t* expert_offset, int32_t* row_token, float* row_gate,
                         void* x_dispatched, void* workspace, size_t workspace_bytes, void* stream);
 
+/* ---- step 3 without a caller workspace ----------------------------------------------------------- */
+/* The pages have no counterpart to this entry point; it exists for callers that cannot allocate device
+ * memory: code running inside another framework's memory pool or a plugin host that hands out only the
+ * tensors it owns, and programs that must not allocate after start-up.  They still pass every input and
+ * output, but have no way to provide moe_dispatch's workspace.
+ *
+ * Same arguments, results and ordering guarantees as moe_dispatch, without `workspace` and
+ * `workspace_bytes`.  The scratch moe_dispatch keeps in the workspace (an error word and the per-block
+ * expert histogram of ceil(T/32) x E ints) lives instead in one fixed device array inside the library,
+ * 256 + 4 * MOE_DISPATCH_STATIC_MAX_HIST bytes (1 MiB), which every GPU that loads the library holds
+ * until the process exits.  The call allocates nothing (no cudaMalloc, no allocator of any library).
+ *  - Limit.  Configs with ceil(T/32) * E > MOE_DISPATCH_STATIC_MAX_HIST return MOE_ERR_UNSUPPORTED and
+ *    launch nothing (e.g. T = 16384 allows E <= 511; T = 65536 allows E <= 127).
+ *  - Set-up.  The first call on each device looks up the array's device address (cudaGetSymbolAddress)
+ *    with that device current; make that first call before any stream capture.
+ *  - Sharing.  Every call on a device uses the same array, which keeps the last call's contents (the
+ *    call clears what must start at zero).  Calls whose kernels overlap on the GPU (other streams, other
+ *    host threads) race on it and give wrong results: serialise them, e.g. on one stream.
+ *  - Errors.  Host-side checks return a status as moe_dispatch does.  Expert ids outside [0, E) in
+ *    topk_idx are treated as dropped (slot -1, not counted); the device error word of this variant is not
+ *    readable by the caller (moe_device_status needs a workspace). */
+#define MOE_DISPATCH_STATIC_MAX_HIST 262080
+MOE_API moe_status moe_dispatch_static_scratch(const moe_config* cfg, const void* x, const int32_t* topk_idx,
+                                       const float* topk_gate, int32_t* slot, int32_t* expert_count,
+                                       int32_t* expert_offset, int32_t* row_token, float* row_gate,
+                                       void* x_dispatched, void* stream);
+
 /* ---- steps 4+5: grouped expert FFN ------------------------------------------------------------ */
 /* For every real dispatched row r of expert e:  y_r = W2[e] GELU(W1[e] x_r + b1[e]) + b2[e], with
  * GELU(z) = z/2 (1 + erf(z / sqrt 2)) (the expert of CANN's MOELayer example: Linear(d, 4d), GELU,

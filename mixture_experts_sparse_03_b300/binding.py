@@ -69,6 +69,7 @@ def _load():
         "moe_forward_launches": ([C], I32),
         "moe_route": ([C, P, P, P, P, P, P, P, P, P], I32),
         "moe_dispatch": ([C, P, P, P, P, P, P, P, P, P, P, SZ, P], I32),
+        "moe_dispatch_static_scratch": ([C, P, P, P, P, P, P, P, P, P, P], I32),
         "moe_expert_ffn": ([C, P, P, P, P, P, P, P, P, P, P, P, SZ, P], I32),
         "moe_combine": ([C, P, P, P, P, P, P, P], I32),
         "moe_forward": ([C, P, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P], I32),
@@ -157,6 +158,13 @@ def moe_dispatch(cfg, x, topk_idx, topk_gate, slot, expert_count, expert_offset,
     return lib.moe_dispatch(ctypes.byref(cfg), ptr(x), ptr(topk_idx), ptr(topk_gate), ptr(slot), ptr(expert_count),
                             ptr(expert_offset), ptr(row_token), ptr(row_gate), ptr(x_dispatched), ptr(workspace),
                             workspace_bytes, stream_handle(stream))
+
+
+def moe_dispatch_static_scratch(cfg, x, topk_idx, topk_gate, slot, expert_count, expert_offset, row_token, row_gate,
+                                x_dispatched, stream=None) -> int:
+    return lib.moe_dispatch_static_scratch(ctypes.byref(cfg), ptr(x), ptr(topk_idx), ptr(topk_gate), ptr(slot),
+                                           ptr(expert_count), ptr(expert_offset), ptr(row_token), ptr(row_gate),
+                                           ptr(x_dispatched), stream_handle(stream))
 
 
 def moe_expert_ffn(cfg, x_dispatched, expert_offset, row_token, row_gate, w1, b1, w2, b2, y_dispatched, out,
