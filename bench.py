@@ -36,8 +36,17 @@ METRIC = "MoE layer fwd tokens/s on 1 B300; % of bf16 TC peak or HBM roofline"
 UNIT = "tokens/s"
 DEFAULT_WORKLOAD = "bf16_e8_k2"
 FLUSH_BYTES = 256 << 20
-KERNELS_FUSED = ["gate_topk_scan", "dispatch_assign_gather", "expert_up_gelu", "expert_down_combine"]
-KERNELS_UNFUSED = ["gate_topk_scan", "dispatch_assign_gather", "expert_up_gelu", "expert_down", "combine_gather"]
+RIDGE_ROWS = 268  # bf16: FLOP per expert-weight byte = rows per expert; ridge = peak FLOP/s / HBM B/s
+
+
+def kernel_names(wl, launches: int):
+    """Names of the kernels moe_forward launches, in launch order."""
+    names = (["gate_logits_gemm"] if wl.dtype == "bf16" else []) + ["gate_topk_scan", "dispatch_assign_gather",
+                                                                      "expert_up_gelu"]
+    names += ["expert_down_combine"] if wl.k <= 2 else ["expert_down", "combine_gather"]
+    if len(names) != launches:
+        raise RuntimeError("moe_forward launches %d kernels, expected %d" % (launches, len(names)))
+    return names
 
 
 def parse():
@@ -205,17 +214,21 @@ def source_sha():
 
 
 def recorded_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it was taken on the
-    current kernel sources (else None)."""
-    p = os.path.join(ROOT, "profiles", "%s_%s.md" % (kernel, workload))
-    if not os.path.exists(p):
+    """DRAM bytes per launch of `kernel` from the committed ncu summaries of `workload`, if they were
+    taken on the current kernel sources (else None).  A summary states
+    `source_sha256: <hash>` and `traffic_bytes_per_launch <kernel>: <bytes>`."""
+    pdir = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(pdir):
         return None
-    txt = open(p).read()
-    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt)
-    s = re.search(r"source_sha256:\s*([0-9a-f]+)", txt)
-    if not m or not s or s.group(1) != source_sha():
-        return None
-    return float(m.group(1))
+    for f in sorted(os.listdir(pdir)):
+        if not f.endswith(".md") or workload not in f:
+            continue
+        txt = open(os.path.join(pdir, f)).read()
+        m = re.search(r"traffic_bytes_per_launch %s:\s*([0-9.eE+]+)" % re.escape(kernel), txt)
+        s = re.search(r"source_sha256:\s*`?([0-9a-f]+)", txt)
+        if m and s and s.group(1) == source_sha():
+            return float(m.group(1))
+    return None
 
 
 def run_ours(args, rank, world, local):
@@ -306,7 +319,7 @@ def run_ours(args, rank, world, local):
     ms_per_step = total_ms / K
 
     # ---- per-kernel durations (eager, trace events between the library's launches)
-    names = KERNELS_FUSED if launches_per_step == 4 else KERNELS_UNFUSED
+    names = kernel_names(wl, launches_per_step)
     per = {n: [] for n in names}
     tev = [torch.cuda.Event(enable_timing=True) for _ in range(launches_per_step + 1)]
     for e in tev:  # torch creates the CUDA event at its first record; the library needs real handles
@@ -328,17 +341,22 @@ def run_ours(args, rank, world, local):
     kern_ms = {n: statistics.median(v) for n, v in per.items()}
     dominant = max(kern_ms, key=kern_ms.get)
     pk = peaks()
-    if dominant.startswith("expert_"):
+    hbm_bound = kept < RIDGE_ROWS * max(used, 1)  # few rows per expert: the weights' bytes bound the FFN
+    if dominant.startswith("expert_") and hbm_bound:
+        # one expert GEMM streams one of the two weight matrices of every used expert
+        achieved = (wbytes / 2) / (kern_ms[dominant] * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s",
+                "frac": achieved / pk["hbm"]}
+    elif dominant.startswith("expert_"):
         achieved = gemm_flops / (kern_ms[dominant] * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": pk["bf16"], "unit": "TFLOP/s",
                 "frac": achieved / pk["bf16"]}
     else:
         roof = {"bound": "hbm", "achieved": None, "peak": pk["hbm"], "unit": "GB/s", "frac": None}
-    kernel_file = {"expert_up_gelu": "gemm_tc_up", "expert_down_combine": "gemm_tc_down",
-                   "expert_down": "gemm_tc_down"}.get(dominant, dominant)
-    roof.update({"traffic": recorded_traffic(kernel_file, wl.name), "kernel": dominant,
+    roof.update({"traffic": recorded_traffic(dominant, wl.name), "kernel": dominant,
                  "peak_source": pk["source"] + " (burst)", "kernel_ms": kern_ms[dominant],
-                 "layer_tflops": (2 * gemm_flops + gate_flops) / (ms_per_step * 1e-3) / 1e12})
+                 "layer_tflops": (2 * gemm_flops + gate_flops) / (ms_per_step * 1e-3) / 1e12,
+                 "layer_weight_gbs": wbytes / (ms_per_step * 1e-3) / 1e9})
     if wl.dtype != "bf16":
         roof["note"] = "fp32 CUDA-core path; bf16 tensor peak shown for reference only"
 

@@ -133,13 +133,32 @@ MOE_API size_t moe_workspace_size(const moe_config* cfg);
  * Outputs:
  *   topk_idx   [T, k] int32          expert ids in rank order, best first; ties go to the lower id
  *   topk_gate  [T, k] fp32           gate weight of each chosen expert (see MOE_GATE_NORM_*)
- * Selection is made on the scores (before the softmax).  Scores are first computed in fp32; when two
- * scores of a token are closer than the fp32 error bound of that token, the contenders are recomputed
- * with a doubled-precision (float-float) dot product, so the chosen set and its order equal those of
- * exact arithmetic except for differences below about 1e-12 of the score scale. */
+ * Selection is made on the scores (before the softmax).  Scores are first computed in fp32 (for
+ * MOE_BF16 the logits come from the tensor cores, see moe_gate_logits; for MOE_F32 from CUDA-core FMA
+ * with compensated sums), each with an error bound; when two scores of a token are closer than twice
+ * that bound, the contenders are recomputed with a doubled-precision (float-float) dot product, so the
+ * chosen set and its order equal those of exact arithmetic except for differences below about 1e-12 of
+ * the score scale.  `workspace` (moe_workspace_size bytes) holds the partial logits. */
 MOE_API moe_status moe_route(const moe_config* cfg, const void* x, const void* w_gate, const void* w_noise,
                      const float* noise_eps, const void* proj, const void* expert_emb,
-                     int32_t* topk_idx, float* topk_gate, void* stream);
+                     int32_t* topk_idx, float* topk_gate, void* workspace, size_t workspace_bytes,
+                     void* stream);
+
+/* ---- step 1 alone: gate logits ---------------------------------------------------------------- */
+/* The gate GEMM of a MOE_BF16 layer on the tensor cores (tcgen05: exact bf16 products, fp32
+ * accumulation within each 64-wide block of d, blocks added in float-float on the CUDA cores):
+ *   SOFTMAX  logits [T, E]      = x W_g^T     (the single linear layer before the softmax, "How sparse
+ *                                              activation improves efficiency", section 2.1)
+ *   NOISY    logits [T, 2E]     = [x W_g^T, x W_n^T]  (clean and noise logits of NoisyTopKGating,
+ *                                              "MoE sparse-compute acceleration", section 2.1)
+ *   COSINE   logits [T, cos_dim] = x P^T      (the projection of Tutel's cosine_top)
+ * fp32, row-major, overwritten.  Error: |logit - exact| <= 32 * 2^-23 * sum_i |x_i w_i|, the bound
+ * moe_route assumes for this GEMM (21 * 2^-23 from the measured rounding of the tensor cores, with a
+ * margin).  noise_eps and expert_emb are not used.  MOE_F32 layers return MOE_ERR_UNSUPPORTED (their logits are computed inside
+ * moe_route's CUDA-core kernel). */
+MOE_API moe_status moe_gate_logits(const moe_config* cfg, const void* x, const void* w_gate, const void* w_noise,
+                           const void* proj, float* logits, void* workspace, size_t workspace_bytes,
+                           void* stream);
 
 /* ---- step 3: capacity-limited dispatch -------------------------------------------------------- */
 /* Groups the (token, expert) pairs by expert, ahead of one batched matmul per group ("How sparse

@@ -67,7 +67,8 @@ def _load():
         "moe_dispatch_rows": ([C], I64),
         "moe_workspace_size": ([C], SZ),
         "moe_forward_launches": ([C], I32),
-        "moe_route": ([C, P, P, P, P, P, P, P, P, P], I32),
+        "moe_route": ([C, P, P, P, P, P, P, P, P, P, SZ, P], I32),
+        "moe_gate_logits": ([C, P, P, P, P, P, P, SZ, P], I32),
         "moe_dispatch": ([C, P, P, P, P, P, P, P, P, P, P, SZ, P], I32),
         "moe_dispatch_static_scratch": ([C, P, P, P, P, P, P, P, P, P, P], I32),
         "moe_expert_ffn": ([C, P, P, P, P, P, P, P, P, P, P, P, SZ, P], I32),
@@ -148,9 +149,16 @@ def moe_forward_launches(cfg: MoEConfig) -> int:
     return lib.moe_forward_launches(ctypes.byref(cfg))
 
 
-def moe_route(cfg, x, w_gate, w_noise, noise_eps, proj, expert_emb, topk_idx, topk_gate, stream=None) -> int:
+def moe_route(cfg, x, w_gate, w_noise, noise_eps, proj, expert_emb, topk_idx, topk_gate, workspace, workspace_bytes,
+              stream=None) -> int:
     return lib.moe_route(ctypes.byref(cfg), ptr(x), ptr(w_gate), ptr(w_noise), ptr(noise_eps), ptr(proj),
-                         ptr(expert_emb), ptr(topk_idx), ptr(topk_gate), stream_handle(stream))
+                         ptr(expert_emb), ptr(topk_idx), ptr(topk_gate), ptr(workspace), workspace_bytes,
+                         stream_handle(stream))
+
+
+def moe_gate_logits(cfg, x, w_gate, w_noise, proj, logits, workspace, workspace_bytes, stream=None) -> int:
+    return lib.moe_gate_logits(ctypes.byref(cfg), ptr(x), ptr(w_gate), ptr(w_noise), ptr(proj), ptr(logits),
+                               ptr(workspace), workspace_bytes, stream_handle(stream))
 
 
 def moe_dispatch(cfg, x, topk_idx, topk_gate, slot, expert_count, expert_offset, row_token, row_gate, x_dispatched,

@@ -1,8 +1,9 @@
 // combine.cu -- gate-weighted combine back into token order, Output = sum_i g_i(x) E_i(x) (the layer
 // formula of "MoE on a single card", section 1.2), and a zero fill.
 //
-// One warp per token, 16-byte loads: out[t] = sum over ranks j = 0..k-1 (in that order) of the kept
-// pairs of gate[t, j] * y[off[e] + slot[t, j]]; a token with every pair dropped gets 0.
+// One thread per 4 consecutive outputs: out[t] = sum over ranks j = 0..k-1 (in that order) of the kept
+// pairs of gate[t, j] * y[off[e] + slot[t, j]], all k rows loaded before the sum; a token with every
+// pair dropped gets 0.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -14,30 +15,39 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
                                                       const int* __restrict__ offset, const int* __restrict__ topk_idx,
                                                       const float* __restrict__ topk_gate, int T, int k, int d,
                                                       float* __restrict__ out) {
-    const int lane = threadIdx.x & 31;
-    const int t = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
-    if (t >= T) return;
-    int rows[kMaxTopK];
-    float g[kMaxTopK];
-    for (int j = 0; j < k; ++j) {
-        const int s = slot[(size_t)t * k + j];
-        rows[j] = s >= 0 ? offset[topk_idx[(size_t)t * k + j]] + s : -1;
-        g[j] = topk_gate[(size_t)t * k + j];
-    }
     const int n4 = d / 4;
-    float4* o = reinterpret_cast<float4*>(out + (size_t)t * d);
-    for (int i = lane; i < n4; i += 32) {
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int j = 0; j < k; ++j) {
-            if (rows[j] < 0) continue;
-            const float4 v = reinterpret_cast<const float4*>(y + (size_t)rows[j] * d)[i];
-            acc.x = fmaf(g[j], v.x, acc.x);
-            acc.y = fmaf(g[j], v.y, acc.y);
-            acc.z = fmaf(g[j], v.z, acc.z);
-            acc.w = fmaf(g[j], v.w, acc.w);
+    const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (size_t)T * n4) return;
+    const int t = (int)(i / n4), c = (int)(i - (size_t)t * n4);
+    // all k rows' loads first, then the sum in rank order
+    float4 v[kMaxTopK];
+    float g[kMaxTopK];
+    unsigned kept = 0;
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) {
+        v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        g[j] = 0.f;
+        if (j < k) {
+            const int s = slot[(size_t)t * k + j];
+            if (s >= 0) {
+                const int r = offset[topk_idx[(size_t)t * k + j]] + s;
+                v[j] = reinterpret_cast<const float4*>(y + (size_t)r * d)[c];
+                g[j] = topk_gate[(size_t)t * k + j];
+                kept |= 1u << j;
+            }
         }
-        o[i] = acc;
     }
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) {
+        if ((kept >> j) & 1u) {
+            acc.x = fmaf(g[j], v[j].x, acc.x);
+            acc.y = fmaf(g[j], v[j].y, acc.y);
+            acc.z = fmaf(g[j], v[j].z, acc.z);
+            acc.w = fmaf(g[j], v[j].w, acc.w);
+        }
+    }
+    reinterpret_cast<float4*>(out + (size_t)t * d)[c] = acc;
 }
 
 __global__ void zero_kernel(float4* __restrict__ p, size_t n4) {
@@ -50,7 +60,8 @@ __global__ void zero_kernel(float4* __restrict__ p, size_t n4) {
 cudaError_t launch_combine(const float* y, const int* slot, const int* offset, const int* topk_idx,
                            const float* topk_gate, int T, int k, int d, float* out, cudaStream_t s) {
     if (T <= 0) return cudaSuccess;
-    combine_kernel<<<(T + 7) / 8, 256, 0, s>>>(y, slot, offset, topk_idx, topk_gate, T, k, d, out);
+    const size_t n = (size_t)T * (d / 4);
+    combine_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(y, slot, offset, topk_idx, topk_gate, T, k, d, out);
     return cudaGetLastError();
 }
 

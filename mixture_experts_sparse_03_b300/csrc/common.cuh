@@ -14,7 +14,7 @@ using bf16_t = uint16_t;  // raw bits of a bfloat16; converted with the helpers 
 enum : int { kErrCheck = 5, kErrTimeout = 6 };
 enum : int {
     kWhereGate = 1, kWhereDispatch = 2, kWhereFfnSimt = 3, kWhereGemmProducer = 4, kWhereGemmMma = 5,
-    kWhereGemmEpilogue = 6, kWhereCombine = 7
+    kWhereGemmEpilogue = 6, kWhereCombine = 7, kWhereGateGemm = 8
 };
 
 __device__ __forceinline__ void record_error(int* err, int code, int where) {
@@ -102,6 +102,12 @@ __device__ __forceinline__ double warp_sum_d(double v) {
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
     return v;
+}
+
+__device__ __forceinline__ unsigned lanemask_lt() {
+    unsigned m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
 }
 
 // GELU with the exact erf form: z/2 (1 + erf(z / sqrt 2))

@@ -79,11 +79,11 @@ moe_status moe_dispatch_static_scratch(const moe_config* cfg, const void* x, con
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // the error word must start at zero; the histogram is written in full before it is read
     if (cudaMemsetAsync(err, 0, 8, s) != cudaSuccess) return MOE_ERR_CUDA;
-    if (launch_dispatch_count(topk_idx, T, k, E, hist, err, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_dispatch_rank(topk_idx, T, k, E, hist, slot, err, s) != cudaSuccess) return MOE_ERR_CUDA;
     if (launch_dispatch_scan(hist, T, k, E, Ceff, expert_count, expert_offset, row_token, row_gate, s) != cudaSuccess)
         return MOE_ERR_CUDA;
-    if (launch_dispatch_assign(x, bf16, topk_idx, topk_gate, hist, expert_offset, T, k, E, d, Ceff, slot, row_token,
-                               row_gate, x_dispatched, nullptr, err, s) != cudaSuccess)
+    if (launch_dispatch_gather(x, bf16, topk_idx, topk_gate, hist, expert_offset, T, k, E, d, Ceff, slot, row_token,
+                               row_gate, x_dispatched, nullptr, s) != cudaSuccess)
         return MOE_ERR_CUDA;
     return MOE_OK;
 }

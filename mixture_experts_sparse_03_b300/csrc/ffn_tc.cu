@@ -20,13 +20,11 @@
 // Every mbarrier wait is bounded: on expiry the kernel records MOE_ERR_DEVICE_TIMEOUT in the error
 // word, all roles stop, the producer waits (bounded) for its copies in flight, the MMA warp waits for
 // its last MMAs, and the TMEM is freed before the CTA exits.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
 #include <mutex>
 
 #include "common.cuh"
 #include "kernels.h"
+#include "tc_ptx.cuh"
 
 namespace moe {
 
@@ -38,7 +36,6 @@ constexpr uint32_t kABytes = kBM * kBK * 2;           // 16 KiB
 constexpr uint32_t kBBytes = kBN * kBK * 2;           // 32 KiB
 constexpr uint32_t kStageBytes = kABytes + kBBytes;   // 48 KiB
 constexpr uint32_t kTmemCols = 2 * kBN;               // 512
-constexpr uint32_t kSpinLimit = 1u << 22;             // polls before a wait gives up (about a second)
 
 struct TcArgs {
     const int* offset;
@@ -51,92 +48,7 @@ struct TcArgs {
     int* err;
 };
 
-// ---- PTX wrappers ------------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.b32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-// bounded wait; false if it gave up or another role already gave up
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
-    for (uint32_t i = 0; i < kSpinLimit; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 255u) == 255u && *abort_flag) return false;
-        if (i > 1024u) __nanosleep(64);
-    }
-    return false;
-}
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-        "l"(map), "r"(bar), "r"(c0), "r"(c1)
-        : "memory");
-}
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1,
-                                            int c2) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
-        "l"(map), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
-        : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
-        : "memory");
-}
-// 32 lanes x 32 consecutive 32-bit columns: thread i of the warp gets lane (base lane + i), columns c..c+31
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
-          "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]),
-          "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
-          "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-// shared-memory matrix descriptor: K-major operand, 128-byte swizzle, 8-row groups 1024 bytes apart
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
-    uint64_t d = 0;
-    d |= (uint64_t)((addr & 0x3FFFFu) >> 4);         // start address
-    d |= (uint64_t)(16u >> 4) << 16;                 // leading byte offset (unused with this swizzle)
-    d |= (uint64_t)(1024u >> 4) << 32;               // stride byte offset: next 8-row group
-    d |= (uint64_t)1 << 46;                          // descriptor version
-    d |= (uint64_t)2 << 61;                          // 128-byte swizzle
-    return d;
-}
-// instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major, M x N
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
+using namespace tc;
 
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const TcArgs a) {
@@ -170,14 +82,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_holder)),
-                     "r"(kTmemCols)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        tmem_alloc(smem_u32(tmem_holder), kTmemCols);
     }
-    tc_fence_before();
+    fence_before();
     __syncthreads();
-    tc_fence_after();
+    fence_after();
     const uint32_t tmem_base = *tmem_holder;
 
     const int total_rows = s_off[a.E];
@@ -213,8 +122,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // let every copy this thread started land before the CTA's shared memory goes away
                 for (int s = 0; s < kStages; ++s)
                     if (issued[s]) {
-                        for (uint32_t i = 0; i < kSpinLimit && !mbar_try_wait(bar(FULL + s), issued_phase[s]); ++i)
-                            __nanosleep(64);
+                        mbar_wait_bounded(bar(FULL + s), issued_phase[s]);
                     }
             }
         }
@@ -229,29 +137,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int acc = local & 1;
                 const uint32_t acc_phase = (local >> 1) & 1;
                 if (!mbar_wait(bar(TEMPTY + acc), acc_phase ^ 1u, abort_flag)) { ok = false; break; }
-                tc_fence_after();
+                fence_after();
                 const uint32_t d_tmem = tmem_base + acc * kBN;
                 for (int kb = 0; kb < k_iters; ++kb) {
                     if (!mbar_wait(bar(FULL + stage), phase, abort_flag)) { ok = false; break; }
-                    tc_fence_after();
+                    fence_after();
                     const uint64_t ad = smem_desc_sw128(smem_u32(sA + stage * kABytes));
                     const uint64_t bd = smem_desc_sw128(smem_u32(sB + stage * kBBytes));
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk)
-                        tc_mma(d_tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc, (kb | kk) != 0);
+                        mma_bf16(d_tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc, (kb | kk) != 0);
                     any = true;
-                    tc_commit(bar(EMPTY + stage));
+                    commit(bar(EMPTY + stage));
                     if (++stage == kStages) { stage = 0; phase ^= 1u; }
                 }
-                if (ok) tc_commit(bar(TFULL + acc));
+                if (ok) commit(bar(TFULL + acc));
             }
             if (!ok) {
                 record_error(a.err, kErrTimeout, kWhereGemmMma);
                 *abort_flag = 1;
             }
             if (any) {  // all MMAs this thread issued have finished once LAST completes
-                tc_commit(bar(LAST));
-                for (uint32_t i = 0; i < kSpinLimit && !mbar_try_wait(bar(LAST), 0); ++i) __nanosleep(64);
+                commit(bar(LAST));
+                mbar_wait_bounded(bar(LAST), 0);
             }
         }
     } else {
@@ -270,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 break;
             }
-            tc_fence_after();
+            fence_after();
             const int m0 = (tile / n_tiles) * kBM, n0 = (tile % n_tiles) * kBN;
             const int e = expert_of_row(s_off, a.E, m0);
             const int r = m0 + row;
@@ -318,17 +226,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 }
             }
-            tc_fence_before();
+            fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(TEMPTY + acc));
         }
     }
-    tc_fence_before();
+    fence_before();
     __syncthreads();
-    tc_fence_after();
+    fence_after();
     if (warp == 1) {
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols)
-                     : "memory");
+        tmem_free(tmem_base, kTmemCols);
     }
 }
 
@@ -363,8 +270,9 @@ std::mutex g_map_mutex;
 MapEntry g_maps[64];
 int g_maps_used = 0, g_maps_next = 0;
 
-// bf16 tensor [d2][d1][d0] (d0 contiguous) tiled in boxes of 64 x b1 (x 1), 128-byte swizzle
-bool get_map(const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b1, CUtensorMap* out) {
+}  // namespace
+
+bool tma_map_bf16(const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b1, CUtensorMap* out) {
     const MapKey key{ptr, d0, d1, d2, b1};
     std::lock_guard<std::mutex> lock(g_map_mutex);
     for (int i = 0; i < g_maps_used; ++i)
@@ -390,7 +298,7 @@ bool get_map(const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b1
     return true;
 }
 
-int num_sms() {
+int device_sm_count() {
     static int n = 0;
     if (n == 0) {
         int dev = 0;
@@ -401,8 +309,6 @@ int num_sms() {
     return n;
 }
 
-}  // namespace
-
 size_t ffn_tc_smem_bytes(int E) {
     return 1024 + (size_t)kStages * kStageBytes + (2 * kStages + 5) * 8 + 16 + 4 * (size_t)(E + 1);
 }
@@ -411,8 +317,8 @@ cudaError_t launch_ffn_tc(const FfnParams& P, cudaStream_t s) {
     if (!P.bf16) return cudaErrorInvalidValue;
     if (P.rows_cap <= 0) return cudaSuccess;
     CUtensorMap ma, mb;
-    if (!get_map(P.A, (uint64_t)P.K, (uint64_t)P.rows_cap, 0, kBM, &ma)) return cudaErrorInvalidValue;
-    if (!get_map(P.W, (uint64_t)P.K, (uint64_t)P.N, (uint64_t)P.E, kBN, &mb)) return cudaErrorInvalidValue;
+    if (!tma_map_bf16(P.A, (uint64_t)P.K, (uint64_t)P.rows_cap, 0, kBM, &ma)) return cudaErrorInvalidValue;
+    if (!tma_map_bf16(P.W, (uint64_t)P.K, (uint64_t)P.N, (uint64_t)P.E, kBN, &mb)) return cudaErrorInvalidValue;
     TcArgs a;
     a.offset = P.offset;
     a.row_token = P.row_token;
@@ -429,7 +335,7 @@ cudaError_t launch_ffn_tc(const FfnParams& P, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int64_t max_tiles = (P.rows_cap / kBM) * (int64_t)((P.N + kBN - 1) / kBN);
-    int grid = num_sms();
+    int grid = device_sm_count();
     if (max_tiles < grid) grid = (int)(max_tiles > 0 ? max_tiles : 1);
     gemm_tc_kernel<<<grid, kThreads, smem, s>>>(ma, mb, a);
     return cudaGetLastError();

@@ -30,6 +30,7 @@
 #include <math.h>
 
 #include "common.cuh"
+#include "gate_common.cuh"
 #include "kernels.h"
 #include "scan.cuh"
 
@@ -37,13 +38,12 @@ namespace moe {
 
 namespace {
 
+using namespace gate;
+
 constexpr int kBT = kTokensPerBlock;   // 32 tokens per block
 constexpr int kSmallElems = 16384;     // N * d at or below which the weight is staged whole
 constexpr int kKC = 32;                // reduction chunk
 constexpr int kXSS = kBT + 1;          // shared stride of the transposed x tile
-constexpr int kMaxCand = 64;           // contenders re-scored per token
-constexpr float kU = 5.9604644775390625e-08f;  // 2^-24
-constexpr int kGateSoftmax = 0, kGateNoisy = 1, kGateCosine = 2;
 
 struct Layout {
     int N;       // logits per token
@@ -56,7 +56,7 @@ struct Layout {
 __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 __host__ __device__ inline Layout make_layout(int gate, int E, int p, int d, int BN, int stage, bool small,
-                                              int nthreads) {
+                                              int nthreads, bool pre = false) {
     const int nwarps = nthreads / 32;
     Layout L;
     L.N = gate == kGateSoftmax ? E : gate == kGateNoisy ? 2 * E : p;
@@ -94,46 +94,17 @@ __host__ __device__ inline Layout make_layout(int gate, int E, int p, int d, int
     return L;
 }
 
-__device__ __forceinline__ unsigned lanemask_lt() {
-    unsigned m;
-    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
-    return m;
-}
+// phase-1 variants: logits by the tiled SIMT GEMM or by the small-gate SIMT path
+constexpr int kPh1Tiled = 0, kPh1Small = 1;
 
-__device__ __forceinline__ float softplus_f(float z) {
-    // log(1 + e^z); the second form is the same function written to avoid overflow of e^z
-    return z > 20.0f ? z + log1pf(expf(-z)) : log1pf(expf(z));
-}
-
-template <typename T>
-__device__ __forceinline__ const T* logit_row(const GateParams& P, int gate, int n) {
-    if (gate == kGateCosine) return static_cast<const T*>(P.proj) + (size_t)n * P.d;
-    if (gate == kGateNoisy && n >= P.E) return static_cast<const T*>(P.w_noise) + (size_t)(n - P.E) * P.d;
-    return static_cast<const T*>(P.w_gate) + (size_t)n * P.d;
-}
-
-// float-float dot product of two length-d rows by one warp (lanes take 8-element slices)
-template <typename T>
-__device__ __forceinline__ double warp_dot_ff(const T* a, const T* b, int d, int lane) {
-    float hi = 0.f, lo = 0.f;
-    for (int i = lane * 8; i < d; i += 32 * 8) {
-        float va[8], vb[8];
-        load8(a + i, va);
-        load8(b + i, vb);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) ff_fma(hi, lo, va[j], vb[j]);
-    }
-    ff_warp_sum(hi, lo);
-    return (double)hi + (double)lo;
-}
-
-template <typename T, int GATE, int TM, int TN, int TX, bool SMALL>
-__global__ void __launch_bounds__(SMALL ? 512 : 256) gate_kernel(const GateParams P, const int stage) {
+template <typename T, int GATE, int TM, int TN, int TX, int PH1>
+__global__ void __launch_bounds__(PH1 == kPh1Small ? 512 : 256) gate_kernel(const GateParams P, const int stage) {
+    constexpr bool SMALL = PH1 == kPh1Small;
     constexpr int NT = SMALL ? 512 : 256;
     constexpr int NW = NT / 32;
     constexpr int TY = 256 / TX;
     constexpr int BN = TN * TX;
-    static_assert(SMALL || TM * TY == kBT, "a block covers 32 tokens");
+    static_assert(PH1 != kPh1Tiled || TM * TY == kBT, "a block covers 32 tokens");
     extern __shared__ __align__(16) unsigned char smem[];
     const Layout L = make_layout(GATE, P.E, P.p, P.d, BN, stage, SMALL, NT);
     float* logits = reinterpret_cast<float*>(smem + L.logits);
@@ -359,7 +330,7 @@ __global__ void __launch_bounds__(SMALL ? 512 : 256) gate_kernel(const GateParam
             for (int e = lane; e < E; e += 32) {
                 float s = Lr[e];
                 sc[e] = s;
-                dmax = fmaxf(dmax, 33.f * kU * xn * sqrtf(wn2[e]) + 4.f * kU * fabsf(s));
+                dmax = fmaxf(dmax, P.cb * xn * sqrtf(wn2[e]) + 4.f * kU * fabsf(s));
             }
         } else if (GATE == kGateNoisy) {
             for (int e = lane; e < E; e += 32) {
@@ -368,8 +339,8 @@ __global__ void __launch_bounds__(SMALL ? 512 : 256) gate_kernel(const GateParam
                 float sp = softplus_f(z);
                 float s = fmaf(ep, sp, c);
                 sc[e] = s;
-                float bc = 33.f * kU * xn * sqrtf(wn2[e]) + 4.f * kU * fabsf(c);
-                float bz = 33.f * kU * xn * sqrtf(wn2[E + e]) + 4.f * kU * fabsf(z);
+                float bc = P.cb * xn * sqrtf(wn2[e]) + 4.f * kU * fabsf(c);
+                float bz = P.cb * xn * sqrtf(wn2[E + e]) + 4.f * kU * fabsf(z);
                 dmax = fmaxf(dmax, bc + fabsf(ep) * (bz + 8.f * kU * (sp + 1.f)) + 4.f * kU * fabsf(s));
             }
         } else {
@@ -378,7 +349,7 @@ __global__ void __launch_bounds__(SMALL ? 512 : 256) gate_kernel(const GateParam
             for (int j = lane; j < p; j += 32) {
                 float u = Lr[j];
                 nu2 = fmaf(u, u, nu2);
-                float du = 33.f * kU * xn * sqrtf(wn2[j]) + 4.f * kU * fabsf(u);
+                float du = P.cb * xn * sqrtf(wn2[j]) + 4.f * kU * fabsf(u);
                 D2 = fmaf(du, du, D2);
             }
             nu2 = warp_sum(nu2);
@@ -546,20 +517,24 @@ __global__ void __launch_bounds__(SMALL ? 512 : 256) gate_kernel(const GateParam
         __syncthreads();
     }
 
-    // ---------------------------------------------------------------- expert histogram of the block
+    // ---------------------------------------------------------------- block ranks and expert histogram
     if (P.blk_hist != nullptr) {
         for (int e = tid; e < E; e += NT) hist[e] = 0;
         __syncthreads();
-        for (int i = tid; i < ntok * k; i += NT) atomicAdd(&hist[fidx[(i / k) * kMaxTopK + i % k]], 1);
+        if (warp == 0)
+            rank_pairs_warp([&](int i) { return fidx[(i / k) * kMaxTopK + i % k]; }, ntok * k, hist,
+                            P.slot + (size_t)tok0 * k, lane);
         __syncthreads();
         for (int e = tid; e < E; e += NT) P.blk_hist[(size_t)blockIdx.x * E + e] = hist[e];
         if (P.ticket != nullptr) {  // the last block to finish runs the dispatch scan
-            __threadfence();
-            __syncthreads();
-            if (tid == 0) nref[1] = atomicAdd(P.ticket, 1);
+            __syncthreads();  // the block's histogram is written; thread 0 publishes it with the ticket
+            if (tid == 0) {
+                __threadfence();
+                nref[1] = atomicAdd(P.ticket, 1);
+                __threadfence();
+            }
             __syncthreads();
             if (nref[1] == (int)gridDim.x - 1) {
-                __threadfence();
                 ScanSmem sm;
                 sm.part = reinterpret_cast<int*>(smem + L.scan_part);
                 sm.padded = reinterpret_cast<int*>(smem + L.scan_padded);
@@ -577,9 +552,10 @@ bool use_small(int gate, int E, int p, int d) {
     return N <= 16 && N * d <= kSmallElems;
 }
 
-template <typename T, int GATE, int TM, int TN, int TX, bool SMALL>
+template <typename T, int GATE, int TM, int TN, int TX, int PH1>
 cudaError_t launch_cfg(const GateParams& P, cudaStream_t s) {
     constexpr int BN = TN * TX;
+    constexpr bool SMALL = PH1 == kPh1Small;
     constexpr int NT = SMALL ? 512 : 256;
     Layout L0 = make_layout(GATE, P.E, P.p, P.d, BN, 0, SMALL, NT);
     int stage = 0;
@@ -587,7 +563,7 @@ cudaError_t launch_cfg(const GateParams& P, cudaStream_t s) {
         Layout L1 = make_layout(GATE, P.E, P.p, P.d, BN, 1, SMALL, NT);
         if (L1.total <= 200 * 1024) { stage = 1; L0 = L1; }
     }
-    auto kern = gate_kernel<T, GATE, TM, TN, TX, SMALL>;
+    auto kern = gate_kernel<T, GATE, TM, TN, TX, PH1>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L0.total);
     if (e != cudaSuccess) return e;
     const int blocks = (P.T + kBT - 1) / kBT;
@@ -598,11 +574,11 @@ cudaError_t launch_cfg(const GateParams& P, cudaStream_t s) {
 template <typename T, int GATE>
 cudaError_t launch_gate_t(const GateParams& P, cudaStream_t s) {
     const int N = GATE == kGateSoftmax ? P.E : GATE == kGateNoisy ? 2 * P.E : P.p;
-    if (use_small(GATE, P.E, P.p, P.d)) return launch_cfg<T, GATE, 1, 1, 8, true>(P, s);
-    if (N <= 8) return launch_cfg<T, GATE, 1, 1, 8, false>(P, s);
-    if (N <= 16) return launch_cfg<T, GATE, 1, 2, 8, false>(P, s);
-    if (N <= 32) return launch_cfg<T, GATE, 2, 2, 16, false>(P, s);
-    return launch_cfg<T, GATE, 2, 4, 16, false>(P, s);
+    if (use_small(GATE, P.E, P.p, P.d)) return launch_cfg<T, GATE, 1, 1, 8, kPh1Small>(P, s);
+    if (N <= 8) return launch_cfg<T, GATE, 1, 1, 8, kPh1Tiled>(P, s);
+    if (N <= 16) return launch_cfg<T, GATE, 1, 2, 8, kPh1Tiled>(P, s);
+    if (N <= 32) return launch_cfg<T, GATE, 2, 2, 16, kPh1Tiled>(P, s);
+    return launch_cfg<T, GATE, 2, 4, 16, kPh1Tiled>(P, s);
 }
 
 template <typename T>
@@ -625,6 +601,7 @@ size_t gate_smem_bytes(int gate, int E, int p, int d) {
 
 cudaError_t launch_gate(const GateParams& P, cudaStream_t s) {
     if (P.T <= 0) return cudaSuccess;
+    if (P.part != nullptr) return launch_gate_select(P, s);  // logits precomputed on the tensor cores
     return P.bf16 ? launch_gate_d<bf16_t>(P, s) : launch_gate_d<float>(P, s);
 }
 

@@ -27,6 +27,7 @@ struct GateParams {
     int* topk_idx;          // [T, k]
     float* topk_gate;       // [T, k]
     int* blk_hist;          // [ceil(T/32), E] per-block expert histogram, or nullptr
+    int* slot;              // [T, k] receives each pair's rank within its block (with blk_hist)
     int* err;               // error word or nullptr
     // dispatch scan fused into the gate's last block (when ticket != nullptr; needs blk_hist)
     int* ticket;            // zero-initialised counter of finished blocks (reset by the last block)
@@ -35,19 +36,50 @@ struct GateParams {
     int* offset;            // [E+1]
     int* row_token;         // padding rows get -1
     float* row_gate;        // padding rows get 0
+    // logits precomputed by the tensor-core GEMM (bf16 layers): partials [S][T][Np], summed in split
+    // order, with the squared norms of the x rows [S][T] and weight rows [S][Np]; nullptr -> the gate
+    // kernel computes the logits itself on CUDA cores
+    const float* part;
+    const float* xn2p;
+    const float* wn2p;
+    int S, Np;
+    float cb;               // logit error bound = cb * |x_t| * |w_n| (+ 4u |logit|)
 };
-size_t gate_smem_bytes(int gate, int E, int p, int d);
+size_t gate_smem_bytes(int gate, int E, int p, int d);  // CUDA-core gate (fp32 layers)
+size_t gate_select_smem_bytes(int gate, int E, int p);  // selection from precomputed logits
+cudaError_t launch_gate_select(const GateParams& p, cudaStream_t s);
+
+// ---- gate logits GEMM on the tensor cores (gate_tc.cu) ------------------------------------------
+constexpr int kGateMaxSplits = 8;
+constexpr int kPlanSms = 148;  // SM count the split-K plan (and so the workspace size) assumes
+struct GateGemmPlan {
+    int BN;        // logits per n-tile (multiple of 16, <= 256)
+    int nt0, nt1;  // n-tiles over the first / second weight tensor
+    int mt;        // 128-token tiles
+    int kb;        // 64-wide K blocks
+    int per;       // K blocks per split
+    int S;         // splits of K
+    int Np;        // logits per token (N0 + N1)
+    size_t smem;   // dynamic shared memory per CTA
+};
+GateGemmPlan gate_gemm_plan(int T, int d, int N0, int N1, int sms);
+// part [S][T][Np] (S = plan.S) receives the partial logits; xn2_part [S][T] and wn2_part [S][Np]
+// the partial squared norms (either may be nullptr to skip)
+cudaError_t launch_gate_gemm(const GateGemmPlan& g, const void* x, const void* w0, const void* w1, int T, int d,
+                             int N0, int N1, float* part, float* xn2_part, float* wn2_part, int* err,
+                             cudaStream_t s);
 cudaError_t launch_gate(const GateParams& p, cudaStream_t s);
 
 // ---- dispatch ---------------------------------------------------------------------------------
-cudaError_t launch_dispatch_count(const int* topk_idx, int T, int k, int E, int* blk_hist, int* err,
-                                  cudaStream_t s);
+cudaError_t launch_dispatch_rank(const int* topk_idx, int T, int k, int E, int* blk_hist, int* rank, int* err,
+                                 cudaStream_t s);
 cudaError_t launch_dispatch_scan(int* blk_hist, int T, int k, int E, int C, int* count, int* offset,
                                  int* row_token, float* row_gate, cudaStream_t s);
-cudaError_t launch_dispatch_assign(const void* x, int bf16, const int* topk_idx, const float* topk_gate,
-                                   const int* blk_hist, const int* offset, int T, int k, int E, int d, int C,
+// slot [T, k] holds the block ranks on entry (from the rank step or the gate kernel) and the slots on exit
+cudaError_t launch_dispatch_gather(const void* x, int bf16, const int* topk_idx, const float* topk_gate,
+                                   const int* blk_base, const int* offset, int T, int k, int E, int d, int C,
                                    int* slot, int* row_token, float* row_gate, void* x_dispatched,
-                                   float* out_to_zero, int* err, cudaStream_t s);
+                                   float* out_to_zero, cudaStream_t s);
 
 // ---- expert FFN -------------------------------------------------------------------------------
 // mode: 0 = up projection (+b1, GELU, store hidden), 1 = down projection to y (fp32),

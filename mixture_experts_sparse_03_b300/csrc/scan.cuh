@@ -1,6 +1,7 @@
-// scan.cuh -- the dispatch scan as a block-level device function, shared by the standalone scan
-// kernel and by the last block of the gate kernel (which runs it once every block has written its
-// histogram).
+// scan.cuh -- the block-level steps of the dispatch, shared by the dispatch kernels and the gate
+// kernels (which run them on their own block of tokens, and the scan in their last block):
+//   rank_pairs_warp  within-block token-order ranks of the (token, expert) pairs + block histogram
+//   scan_experts     per-expert prefix over the block histograms, counts, padded segment offsets
 //
 // Input: blk_hist[b][e] = pairs of token block b routed to expert e.  Output, in place: blk_hist[b][e]
 // = pairs of blocks before b routed to e (the first slot block b hands out for e); count[e] = total;
@@ -12,6 +13,28 @@
 
 namespace moe {
 
+// One warp numbers the block's pairs in token order (pair i belongs to token i / k, rank i % k): 32 pairs
+// at a time, __match_any_sync groups equal experts and each pair's rank among them is the number of
+// lower lanes in its group; a shared running count per expert carries the numbering across chunks.
+// `running` [E] must be zero on entry and holds the block's expert histogram on exit.  expert_of(i)
+// < 0 marks a pair that takes no slot (rank -1, not counted).
+template <typename F>
+__device__ __forceinline__ void rank_pairs_warp(F expert_of, int npairs, int* running, int* rank_out, int lane) {
+    for (int c0 = 0; c0 < npairs; c0 += 32) {
+        const int i = c0 + lane;
+        const bool valid = i < npairs;
+        const int e = valid ? expert_of(i) : -1;
+        const unsigned mask = __match_any_sync(0xffffffffu, e);
+        const int rank = __popc(mask & lanemask_lt());
+        const bool real = valid && e >= 0;
+        const int base = real ? running[e] : 0;
+        __syncwarp();
+        if (real && rank == 0) running[e] = base + __popc(mask);
+        __syncwarp();
+        if (valid) rank_out[i] = real ? base + rank : -1;
+    }
+}
+
 struct ScanSmem {
     int* part;     // [blockDim.x]
     int* padded;   // [E + 1]
@@ -21,29 +44,59 @@ struct ScanSmem {
 
 __device__ __forceinline__ void scan_experts(int* blk_hist, int nblk, int E, int C, int* count, int* offset,
                                              int* row_token, float* row_gate, const ScanSmem& sm) {
+    constexpr int R = 16;  // block rows a thread keeps in registers between reading and writing them
     const int NT = blockDim.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    int tpe = 1;  // threads per expert, each taking a contiguous range of blocks
-    while (tpe * 2 * E <= NT && tpe * 2 <= nblk) tpe *= 2;
-    const int groups = NT / tpe;
-    for (int e0 = 0; e0 < E; e0 += groups) {
-        const int e = e0 + tid / tpe, sub = tid % tpe;
-        const bool active = e < E;
-        const int per = (nblk + tpe - 1) / tpe;
-        const int b0 = min(nblk, sub * per), b1 = min(nblk, b0 + per);
+    // per chunk of up to NT experts: thread (g, e) owns expert e over the g-th run of `per` blocks, so
+    // a warp reads consecutive experts of one block row (coalesced), all of its rows in flight at once
+    for (int e0 = 0; e0 < E; e0 += NT) {
+        const int ne = min(NT, E - e0);
+        const int G = max(1, min(nblk, NT / ne));
+        const int per = (nblk + G - 1) / G;
+        const int g = tid / ne, e = e0 + tid % ne;
+        const bool active = g < G;
+        const int b0 = active ? min(nblk, g * per) : nblk, b1 = active ? min(nblk, b0 + per) : nblk;
+        int v[R];
         int s = 0;
-        if (active)
-            for (int b = b0; b < b1; ++b) s += __ldcg(blk_hist + (size_t)b * E + e);
+#pragma unroll
+        for (int j = 0; j < R; ++j) v[j] = b0 + j < b1 ? __ldcg(blk_hist + (size_t)(b0 + j) * E + e) : 0;
+#pragma unroll
+        for (int j = 0; j < R; ++j) s += v[j];
+        for (int i0 = b0 + R; i0 < b1; i0 += 8) {  // rows beyond the first R: summed now, re-read below
+            int w[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) w[j] = i0 + j < b1 ? __ldcg(blk_hist + (size_t)(i0 + j) * E + e) : 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) s += w[j];
+        }
         sm.part[tid] = s;
         __syncthreads();
+        // inclusive scan over the groups of each expert (Hillis-Steele, stride ne)
+        for (int off = 1; off < G; off <<= 1) {
+            const int add = (active && g >= off) ? sm.part[tid - off * ne] : 0;
+            __syncthreads();
+            sm.part[tid] += add;
+            __syncthreads();
+        }
         if (active) {
-            int run = 0;
-            for (int q = 0; q < sub; ++q) run += sm.part[tid - sub + q];
-            for (int b = b0; b < b1; ++b) {
-                const int c = __ldcg(blk_hist + (size_t)b * E + e);
-                blk_hist[(size_t)b * E + e] = run;
-                run += c;
+            int run = sm.part[tid] - s;  // blocks of this expert before b0
+#pragma unroll
+            for (int j = 0; j < R; ++j)
+                if (b0 + j < b1) {
+                    blk_hist[(size_t)(b0 + j) * E + e] = run;
+                    run += v[j];
+                }
+            for (int i0 = b0 + R; i0 < b1; i0 += 8) {
+                int w[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) w[j] = i0 + j < b1 ? __ldcg(blk_hist + (size_t)(i0 + j) * E + e) : 0;
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (i0 + j < b1) {
+                        blk_hist[(size_t)(i0 + j) * E + e] = run;
+                        run += w[j];
+                    }
             }
-            if (sub == tpe - 1) {
+            if (g == G - 1) {
                 count[e] = run;
                 const int kept = min(run, C);
                 sm.kept[e] = kept;
@@ -52,40 +105,26 @@ __device__ __forceinline__ void scan_experts(int* blk_hist, int nblk, int E, int
         }
         __syncthreads();
     }
-    // exclusive scan of the padded sizes, NT values at a time
-    int carry = 0;
-    for (int base = 0; base < E; base += NT) {
-        const int i = base + tid;
-        const int v = i < E ? sm.padded[i] : 0;
-        int inc = v;
+    // exclusive scan of the padded sizes by one warp: lane l takes experts [l*per, (l+1)*per)
+    if (warp == 0) {
+        const int per = (E + 31) / 32;
+        const int lo = min(E, lane * per), hi = min(E, lo + per);
+        int own = 0;
+        for (int i = lo; i < hi; ++i) own += sm.padded[i];
+        int inc = own;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
             const int o = __shfl_up_sync(0xffffffffu, inc, off);
             if (lane >= off) inc += o;
         }
-        if (lane == 31) sm.wsum[warp] = inc;
-        __syncthreads();
-        if (warp == 0) {
-            const int nw = NT / 32;
-            const int w = lane < nw ? sm.wsum[lane] : 0;
-            int winc = w;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const int o = __shfl_up_sync(0xffffffffu, winc, off);
-                if (lane >= off) winc += o;
-            }
-            if (lane < nw) sm.wsum[lane] = winc - w;  // exclusive prefix of the warp totals
-            if (lane == 31) sm.wsum[32] = winc;       // total of this chunk
+        int run = inc - own;
+        for (int i = lo; i < hi; ++i) {
+            const int pv = sm.padded[i];
+            sm.padded[i] = run;
+            run += pv;
         }
-        __syncthreads();
-        const int excl = carry + sm.wsum[warp] + inc - v;
-        const int total = sm.wsum[32];
-        __syncthreads();
-        if (i < E) sm.padded[i] = excl;
-        carry += total;
-        __syncthreads();
+        if (lane == 31) sm.padded[E] = inc;
     }
-    if (tid == 0) sm.padded[E] = carry;
     __syncthreads();
     for (int q = tid; q <= E; q += NT) offset[q] = sm.padded[q];
     for (int i = tid; i < E * kRowAlign; i += NT) {

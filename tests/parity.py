@@ -66,8 +66,8 @@ def run_steps(wl: Workload, tg: dict, flags: int = 0):
     ws = b.workspace(c, dev)
     idx = torch.full((T, k), -7, dtype=torch.int32, device=dev)
     gate = torch.full((T, k), float("nan"), dtype=torch.float32, device=dev)
-    b.check(b.moe_route(c, tg["x"], tg["w_gate"], tg["w_noise"], tg["eps"], tg["proj"], tg["emb"], idx, gate),
-            "moe_route")
+    b.check(b.moe_route(c, tg["x"], tg["w_gate"], tg["w_noise"], tg["eps"], tg["proj"], tg["emb"], idx, gate, ws,
+                        ws.numel()), "moe_route")
     slot = torch.full((T, k), -7, dtype=torch.int32, device=dev)
     count = torch.full((E,), -7, dtype=torch.int32, device=dev)
     off = torch.full((E + 1,), -7, dtype=torch.int32, device=dev)

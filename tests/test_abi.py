@@ -76,7 +76,7 @@ def test_invalid_config_rejected(field, value, status):
     c = _bad(**{field: value})
     assert b.moe_workspace_size(c) == 0
     assert b.moe_capacity(c) == -1
-    assert b.lib.moe_route(ctypes.byref(c), None, None, None, None, None, None, None, None, None) == status
+    assert b.lib.moe_route(ctypes.byref(c), None, None, None, None, None, None, None, None, None, 0, None) == status
 
 
 def test_cosine_and_noisy_limits():
@@ -86,26 +86,39 @@ def test_cosine_and_noisy_limits():
     c.cos_temperature = 0.0
     assert b.moe_workspace_size(c) == 0
     c = b.config(small_workload(gate="noisy", E=600, k=2))
-    assert b.lib.moe_route(ctypes.byref(c), None, None, None, None, None, None, None, None, None) == 2
+    assert b.lib.moe_route(ctypes.byref(c), None, None, None, None, None, None, None, None, None, 0, None) == 2
 
 
 def test_null_and_misaligned_pointers_rejected_before_launch():
     c = b.config(small_workload())
     lib = b.lib
     P = 0x10000
+    W = 0x100000
+    n = b.moe_workspace_size(c)
     # missing x / outputs
-    assert lib.moe_route(ctypes.byref(c), None, P, None, None, None, None, P, P, None) == 1
-    assert lib.moe_route(ctypes.byref(c), P, P, None, None, None, None, None, P, None) == 1
+    assert lib.moe_route(ctypes.byref(c), None, P, None, None, None, None, P, P, W, n, None) == 1
+    assert lib.moe_route(ctypes.byref(c), P, P, None, None, None, None, None, P, W, n, None) == 1
     # misaligned
-    assert lib.moe_route(ctypes.byref(c), P + 2, P, None, None, None, None, P, P, None) == 1
+    assert lib.moe_route(ctypes.byref(c), P + 2, P, None, None, None, None, P, P, W, n, None) == 1
     # noisy needs w_noise and eps
     cn = b.config(small_workload(gate="noisy"))
-    assert lib.moe_route(ctypes.byref(cn), P, P, None, None, None, None, P, P, None) == 1
+    nn = b.moe_workspace_size(cn)
+    assert lib.moe_route(ctypes.byref(cn), P, P, None, None, None, None, P, P, W, nn, None) == 1
     # cosine needs proj and emb
     cc = b.config(small_workload(gate="cosine", cos_dim=16))
-    assert lib.moe_route(ctypes.byref(cc), P, P, None, None, None, None, P, P, None) == 1
+    nc = b.moe_workspace_size(cc)
+    assert lib.moe_route(ctypes.byref(cc), P, P, None, None, None, None, P, P, W, nc, None) == 1
+    # the gate's partial logits live in the workspace
+    assert lib.moe_route(ctypes.byref(c), P, P, None, None, None, None, P, P, None, n, None) == 3
+    assert lib.moe_route(ctypes.byref(c), P, P, None, None, None, None, P, P, W, n - 1, None) == 3
+    # the logits GEMM alone: bf16 only, needs its weights
+    L = 0x20000
+    assert lib.moe_gate_logits(ctypes.byref(c), P, None, None, None, L, W, n, None) == 1
+    assert lib.moe_gate_logits(ctypes.byref(cn), P, P, None, None, L, W, nn, None) == 1
+    assert lib.moe_gate_logits(ctypes.byref(cc), P, P, None, None, L, W, nc, None) == 1
+    cf = b.config(small_workload(dtype="f32"))
+    assert lib.moe_gate_logits(ctypes.byref(cf), P, P, None, None, L, W, b.moe_workspace_size(cf), None) == 2
     # workspace missing / too small / misaligned
-    n = b.moe_workspace_size(c)
     args = [P] * 9
     assert lib.moe_dispatch(ctypes.byref(c), *args, None, n, None) == 3
     assert lib.moe_dispatch(ctypes.byref(c), *args, 0x100000, n - 1, None) == 3
@@ -121,7 +134,8 @@ def test_empty_input_is_a_no_op():
     assert b.moe_dispatch_rows(c) == 0
     assert b.moe_forward_launches(c) == 0
     lib = b.lib
-    assert lib.moe_route(ctypes.byref(c), None, None, None, None, None, None, None, None, None) == 0
+    assert lib.moe_route(ctypes.byref(c), None, None, None, None, None, None, None, None, None, 0, None) == 0
+    assert lib.moe_gate_logits(ctypes.byref(c), *([None] * 6), 0, None) == 0
     assert lib.moe_dispatch(ctypes.byref(c), *([None] * 10), 0, None) == 0
     assert lib.moe_expert_ffn(ctypes.byref(c), *([None] * 11), 0, None) == 0
     assert lib.moe_combine(ctypes.byref(c), *([None] * 7)) == 0
@@ -129,9 +143,13 @@ def test_empty_input_is_a_no_op():
 
 
 def test_launch_counts():
-    assert b.moe_forward_launches(b.config(small_workload(k=2))) == 4
-    assert b.moe_forward_launches(b.config(small_workload(k=3))) == 5
-    assert b.moe_forward_launches(b.config(small_workload(k=2), flags=b.FLAG_UNFUSED_COMBINE)) == 5
+    # bf16: logits GEMM, gate (+ dispatch scan), dispatch, up, down (+ combine when k > 2 or unfused)
+    assert b.moe_forward_launches(b.config(small_workload(k=2))) == 5
+    assert b.moe_forward_launches(b.config(small_workload(k=3))) == 6
+    assert b.moe_forward_launches(b.config(small_workload(k=2), flags=b.FLAG_UNFUSED_COMBINE)) == 6
+    # fp32: the gate computes its logits itself
+    assert b.moe_forward_launches(b.config(small_workload(k=2, dtype="f32"))) == 4
+    assert b.moe_forward_launches(b.config(small_workload(k=3, dtype="f32"))) == 5
 
 
 def test_status_strings():

@@ -164,3 +164,59 @@ def test_full_size_workload(name):
     assert np.array_equal(count, g["count"])
     P.check_output(wl, out, ref, toks)
     print("%s: near-tie tokens %d, routing differences %d, drops %d" % (name, nties, ndiff, int((slot < 0).sum())))
+
+
+def _logits_error_ratio(wl, tc, tg):
+    """max over logits of |GPU - exact| / (2^-23 sum_i |x_i w_i|) for moe_gate_logits."""
+    c = b.config(wl)
+    ws = b.workspace(c, "cuda")
+    rows = {"softmax": [tc["w_gate"]], "noisy": [tc["w_gate"], tc["w_noise"]], "cosine": [tc["proj"]]}[wl.gate]
+    N = sum(r.shape[0] for r in rows)
+    got = torch.full((wl.T, N), float("nan"), dtype=torch.float32, device="cuda")
+    b.check(b.moe_gate_logits(c, tg["x"], tg.get("w_gate"), tg.get("w_noise"), tg.get("proj"), got, ws, ws.numel()),
+            "moe_gate_logits")
+    got = got.cpu().numpy().astype(np.float64)
+    # the exact logits are the oracle's softmax-gate scores x W^T of each weight tensor
+    want = np.concatenate([oracle.gate_scores("softmax", tc["x"], w_gate=w) for w in rows], axis=1)
+    xa = np.abs(tc["x"].double().numpy())
+    wa = np.abs(torch.cat(rows).double().numpy())
+    scale = 2.0 ** -23 * (xa @ wa.T)
+    return np.max(np.abs(got - want) / np.maximum(scale, 1e-300))
+
+
+@pytest.mark.parametrize("gate,E,p,d,T", [("softmax", 8, 0, 1024, 300), ("noisy", 37, 0, 256, 200),
+                                          ("cosine", 10, 256, 512, 129), ("softmax", 256, 0, 7168, 64)])
+def test_gate_logits_within_assumed_tensor_core_bound(gate, E, p, d, T):
+    """The tensor-core logits GEMM against the exact products' sum: the routing step assumes
+    |error| <= 32 * 2^-23 * sum |x_i w_i| and re-scores near ties inside twice that, so the observed
+    error must sit well inside it (here: below a quarter of it)."""
+    wl = small_workload(T=T, d=d, h=64, E=E, k=2, gate=gate, cos_dim=p or 32, capacity_factor=1.0)
+    tc, tg = P.inputs(wl)
+    ratio = _logits_error_ratio(wl, tc, tg)
+    print("observed error / (2^-23 sum|x w|) = %.3e" % ratio)
+    assert ratio < 8.0
+
+
+def test_gate_logits_bound_under_cancellation():
+    """Rows built so that the products cancel: each weight row is +-x of one token with signs chosen
+    to keep the running sum near zero, the dot product is tiny next to sum |x_i w_i| and rounding in
+    the accumulator shows at full strength."""
+    wl = small_workload(T=128, d=1024, h=64, E=16, k=2, capacity_factor=1.0)
+    tc, tg = P.inputs(wl)
+    x = tc["x"].float()
+    scale = torch.exp2(torch.randint(-6, 7, x.shape, generator=torch.Generator().manual_seed(5)).float())
+    x = (x * scale).to(torch.bfloat16)
+    w = torch.empty((wl.E, wl.d), dtype=torch.bfloat16)
+    for e in range(wl.E):
+        xr = x[e].double()
+        run, signs = 0.0, []
+        for v in (xr * xr).tolist():
+            sg = -1.0 if run > 0 else 1.0
+            run += sg * v
+            signs.append(sg)
+        w[e] = (xr * torch.tensor(signs, dtype=torch.float64)).to(torch.bfloat16)
+    tc["x"], tc["w_gate"] = x, w
+    tg["x"], tg["w_gate"] = x.cuda(), w.cuda()
+    ratio = _logits_error_ratio(wl, tc, tg)
+    print("cancellation: observed error / (2^-23 sum|x w|) = %.3e" % ratio)
+    assert ratio < 8.0

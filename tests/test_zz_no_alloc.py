@@ -45,12 +45,12 @@ def _dispatch_outputs(c, x, rows, dev):
     )
 
 
-def _route(c, t, dev):
+def _route(c, t, ws, dev):
     T, k = c.tokens, c.top_k
     idx = torch.empty((T, k), dtype=torch.int32, device=dev)
     gate = torch.empty((T, k), dtype=torch.float32, device=dev)
     b.check(b.moe_route(c, t["x"], t.get("w_gate"), t.get("w_noise"), t.get("eps"), t.get("proj"), t.get("emb"),
-                        idx, gate), "moe_route")
+                        idx, gate, ws, ws.numel()), "moe_route")
     return idx, gate
 
 
@@ -65,8 +65,8 @@ def test_static_scratch_dispatch_matches_workspace_dispatch():
         tg = {n: (v.to(dev) if v is not None else None) for n, v in make_inputs(wl, device="cpu").items()}
         c = b.config(wl)
         rows = b.moe_dispatch_rows(c)
-        idx, gate = _route(c, tg, dev)
         ws = b.workspace(c, dev)
+        idx, gate = _route(c, tg, ws, dev)
         want = _dispatch_outputs(c, tg["x"], rows, dev)
         b.check(b.moe_dispatch(c, tg["x"], idx, gate, want["slot"], want["count"], want["off"], want["rtok"],
                                want["rgate"], want["xd"], ws, ws.numel()), "moe_dispatch")
