@@ -57,6 +57,8 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-graph", action="store_true", help="time eager launches instead of a CUDA graph")
+    ap.add_argument("--ffn", choices=["auto", "one-sm", "sm-pair"], default="auto",
+                    help="expert GEMMs on single SMs or on pairs of SMs (default: the library's choice)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
     return ap.parse_args()
@@ -241,7 +243,7 @@ def run_ours(args, rank, world, local):
 
         dist.init_process_group("nccl", device_id=dev)
     wl = WORKLOADS[args.workload]
-    cfg = b.config(wl)
+    cfg = b.config(wl, flags={"auto": 0, "one-sm": b.FLAG_FFN_ONE_SM, "sm-pair": b.FLAG_FFN_SM_PAIR}[args.ffn])
     tg = make_inputs(wl, device=dev, expert_device="cuda" if wl.expert_weight_bytes() > (1 << 30) else "cpu")
     ws = b.workspace(cfg, dev)
     out = torch.empty((wl.T, wl.d), dtype=torch.float32, device=dev)

@@ -106,6 +106,10 @@ typedef struct moe_config {
  * per-row expert outputs and combine them in a separate gather pass even when k <= 2. */
 #define MOE_FLAG_SIMT_FFN         1
 #define MOE_FLAG_UNFUSED_COMBINE  2
+/* The bf16 expert GEMMs run either on single SMs (128 x 256 tiles) or on pairs of SMs (256 x 256 tiles,
+ * tcgen05 cta_group::2); by default pairs are used when T * k / E >= 2048.  These flags force one. */
+#define MOE_FLAG_FFN_ONE_SM       4
+#define MOE_FLAG_FFN_SM_PAIR      8
 
 /* ---- sizes ------------------------------------------------------------------------------------ */
 /* Per-expert capacity C the dispatch step enforces, or -1 if the config is invalid. */

@@ -27,6 +27,8 @@ NORM = {"all": 0, "topk": 1}
 DTYPE = {"f32": 0, "bf16": 1}
 FLAG_SIMT_FFN = 1
 FLAG_UNFUSED_COMBINE = 2
+FLAG_FFN_ONE_SM = 4
+FLAG_FFN_SM_PAIR = 8
 
 
 class MoEConfig(ctypes.Structure):

@@ -23,6 +23,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 struct Plan {
     int T, d, h, E, k, C, Ceff, p, nblk, gate, norm, bf16, esize, fused;
     int N0, N1;         // gate logits from the first / second weight tensor
+    int pair;           // expert GEMMs on pairs of SMs
     GateGemmPlan gg;    // tensor-core logits GEMM (bf16 layers)
     int64_t rows;
     size_t o_err, o_idx, o_gate, o_slot, o_hist, o_count, o_off, o_rtok, o_rgate, o_xd, o_h, o_y, o_part, o_xn2,
@@ -38,6 +39,9 @@ struct Plan {
 // blocks in float-float, so the whole dot product errs by at most 21 * 2^-23 * sum |x_i w_i|; the
 // constant leaves a 1.5x margin.  Summing S fp32 split partials adds S * 2^-24 * sum |x_i w_i|.
 constexpr double kTcErr = 32.0;
+
+// expected rows per expert (T * k / E) from which the expert GEMMs run on pairs of SMs by default
+constexpr int kPairMinRows = 2048;
 
 moe_status make_plan(const moe_config* c, Plan* pl) {
     if (c == nullptr) return MOE_ERR_INVALID_ARG;
@@ -57,7 +61,9 @@ moe_status make_plan(const moe_config* c, Plan* pl) {
     if (c->dtype != MOE_F32 && c->dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
     if (P.gate < MOE_GATE_SOFTMAX || P.gate > MOE_GATE_COSINE) return MOE_ERR_INVALID_ARG;
     if (P.norm != MOE_GATE_NORM_ALL && P.norm != MOE_GATE_NORM_TOPK) return MOE_ERR_INVALID_ARG;
-    if (c->flags & ~(MOE_FLAG_SIMT_FFN | MOE_FLAG_UNFUSED_COMBINE)) return MOE_ERR_INVALID_ARG;
+    if (c->flags & ~(MOE_FLAG_SIMT_FFN | MOE_FLAG_UNFUSED_COMBINE | MOE_FLAG_FFN_ONE_SM | MOE_FLAG_FFN_SM_PAIR))
+        return MOE_ERR_INVALID_ARG;
+    if ((c->flags & MOE_FLAG_FFN_ONE_SM) && (c->flags & MOE_FLAG_FFN_SM_PAIR)) return MOE_ERR_INVALID_ARG;
     if (c->reserved != 0) return MOE_ERR_INVALID_ARG;
     if (P.gate == MOE_GATE_NOISY && P.E > 512) return MOE_ERR_UNSUPPORTED;
     P.p = 0;
@@ -85,6 +91,10 @@ moe_status make_plan(const moe_config* c, Plan* pl) {
     if (P.rows > (int64_t)1 << 30) return MOE_ERR_UNSUPPORTED;
     P.nblk = (P.T + kTokensPerBlock - 1) / kTokensPerBlock;
     P.fused = P.k <= 2 && !(c->flags & MOE_FLAG_UNFUSED_COMBINE);
+    // pairs of SMs pay off when experts get many rows: their 256-row tiles waste at most 128 rows per
+    // expert, against 2x the rows each weight byte serves
+    P.pair = (c->flags & MOE_FLAG_FFN_SM_PAIR) ||
+             (!(c->flags & MOE_FLAG_FFN_ONE_SM) && (int64_t)P.T * P.k >= (int64_t)kPairMinRows * P.E);
     size_t o = 0;
     auto take = [&](size_t bytes) { size_t r = o; o = up(o + bytes); return r; };
     const size_t tk = (size_t)P.T * P.k;
@@ -229,6 +239,7 @@ FfnParams ffn_params(const Plan& P, int mode, const void* A, const void* W, cons
     f.mode = mode;
     f.rows_cap = P.rows;
     f.err = err;
+    f.pair = P.pair;
     return f;
 }
 

@@ -12,11 +12,9 @@
 //   warp 1     allocates 512 TMEM columns (two 128 x 256 fp32 accumulators); one lane issues
 //              tcgen05.mma (M = 128, N = 256, K = 16, kind::f16) and tcgen05.commit to release smem
 //              stages and to hand finished accumulators to the epilogue
-//   warps 2-5  epilogue: tcgen05.ld of the accumulator (each warp its 32 TMEM lanes = 32 rows), then
-//              mode 0: + b1, GELU(erf), round to bf16, store the hidden row
-//              mode 1: + b2, store fp32 y
-//              mode 2: + b2, times the row's gate, fp32 atomic add into out[token] (fused combine)
-//              while the MMA warp fills the other accumulator
+//   warps 2-5  epilogue, one warp per TMEM lane quarter (32 rows): tcgen05.ld of the accumulator, then
+//              bias, GELU or gate scaling and the stores (see epilogue_cols), while the MMA warp fills
+//              the other accumulator
 // Every mbarrier wait is bounded: on expiry the kernel records MOE_ERR_DEVICE_TIMEOUT in the error
 // word, all roles stop, the producer waits (bounded) for its copies in flight, the MMA warp waits for
 // its last MMAs, and the TMEM is freed before the CTA exits.
@@ -31,7 +29,7 @@ namespace moe {
 namespace {
 
 constexpr int kBM = 128, kBN = 256, kBK = 64, kStages = 4;
-constexpr int kThreads = 192;
+constexpr int kThreads = 192;  // producer warp, MMA warp, 4 epilogue warps (one per TMEM lane quarter)
 constexpr uint32_t kABytes = kBM * kBK * 2;           // 16 KiB
 constexpr uint32_t kBBytes = kBN * kBK * 2;           // 32 KiB
 constexpr uint32_t kStageBytes = kABytes + kBBytes;   // 48 KiB
@@ -49,6 +47,56 @@ struct TcArgs {
 };
 
 using namespace tc;
+
+// Epilogue of columns [c_begin, c_end) of one accumulator row (TMEM lane = this thread's row r of the
+// tile, token tok, gate g), 32 at a time:
+//   mode 0: + b1, GELU(erf), round to bf16, store the hidden row
+//   mode 1: + b2, store fp32 y
+//   mode 2: + b2, times the row's gate, fp32 atomic add into out[tok] (fused combine)
+// All lanes of the warp call this (tcgen05.ld is warp-wide); rows with tok < 0 store nothing.
+__device__ __forceinline__ void epilogue_cols(const TcArgs& a, uint32_t taddr, int r, int tok, float g,
+                                              const bf16_t* bias, int n0, int c_begin, int c_end) {
+    for (int c0 = c_begin; c0 < c_end; c0 += 32) {
+        uint32_t v[32];
+        __syncwarp();
+        tmem_ld32(taddr + (uint32_t)c0, v);
+        const int n = n0 + c0;
+        if (tok < 0 || n >= a.N) continue;
+        float f[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
+        if (bias) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 8) {
+                float bb[8];
+                load8(bias + n + j, bb);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) f[j + i] += bb[i];
+            }
+        }
+        if (a.mode == 0) {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<bf16_t*>(a.C) + (size_t)r * a.N + n);
+#pragma unroll
+            for (int j = 0; j < 32; j += 8) {
+                uint4 w;
+                w.x = pack_bf16x2(gelu_erf(f[j + 0]), gelu_erf(f[j + 1]));
+                w.y = pack_bf16x2(gelu_erf(f[j + 2]), gelu_erf(f[j + 3]));
+                w.z = pack_bf16x2(gelu_erf(f[j + 4]), gelu_erf(f[j + 5]));
+                w.w = pack_bf16x2(gelu_erf(f[j + 6]), gelu_erf(f[j + 7]));
+                __stcs(dst + j / 8, w);  // streaming: the hidden rows should not push the weights out of L2
+            }
+        } else if (a.mode == 1) {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.C) + (size_t)r * a.N + n);
+#pragma unroll
+            for (int j = 0; j < 32; j += 4) __stcs(dst + j / 4, make_float4(f[j], f[j + 1], f[j + 2], f[j + 3]));
+        } else {
+            float4* dst = reinterpret_cast<float4*>(a.out + (size_t)tok * a.N + n);
+#pragma unroll
+            for (int j = 0; j < 32; j += 4)
+                atomicAdd(dst + j / 4, make_float4(g * f[j], g * f[j + 1], g * f[j + 2], g * f[j + 3]));
+        }
+    }
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const TcArgs a) {
@@ -185,47 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int tok = a.row_token[r];
             const float g = (a.mode == 2 && tok >= 0) ? a.row_gate[r] : 0.f;
             const bf16_t* bias = a.bias ? a.bias + (size_t)e * a.N : nullptr;
-            for (int c0 = 0; c0 < kBN; c0 += 32) {
-                uint32_t v[32];
-                __syncwarp();
-                tmem_ld32(tmem_base + lane_base + (uint32_t)(acc * kBN + c0), v);
-                const int n = n0 + c0;
-                if (tok >= 0 && n < a.N) {
-                float f[32];
-#pragma unroll
-                for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
-                if (bias) {
-#pragma unroll
-                    for (int j = 0; j < 32; j += 8) {
-                        float b[8];
-                        load8(bias + n + j, b);
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) f[j + i] += b[i];
-                    }
-                }
-                if (a.mode == 0) {
-                    uint4* dst = reinterpret_cast<uint4*>(static_cast<bf16_t*>(a.C) + (size_t)r * a.N + n);
-#pragma unroll
-                    for (int j = 0; j < 32; j += 8) {
-                        uint4 w;
-                        w.x = pack_bf16x2(gelu_erf(f[j + 0]), gelu_erf(f[j + 1]));
-                        w.y = pack_bf16x2(gelu_erf(f[j + 2]), gelu_erf(f[j + 3]));
-                        w.z = pack_bf16x2(gelu_erf(f[j + 4]), gelu_erf(f[j + 5]));
-                        w.w = pack_bf16x2(gelu_erf(f[j + 6]), gelu_erf(f[j + 7]));
-                        dst[j / 8] = w;
-                    }
-                } else if (a.mode == 1) {
-                    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.C) + (size_t)r * a.N + n);
-#pragma unroll
-                    for (int j = 0; j < 32; j += 4) dst[j / 4] = make_float4(f[j], f[j + 1], f[j + 2], f[j + 3]);
-                } else {
-                    float4* dst = reinterpret_cast<float4*>(a.out + (size_t)tok * a.N + n);
-#pragma unroll
-                    for (int j = 0; j < 32; j += 4)
-                        atomicAdd(dst + j / 4, make_float4(g * f[j], g * f[j + 1], g * f[j + 2], g * f[j + 3]));
-                }
-                }
-            }
+            epilogue_cols(a, tmem_base + lane_base + (uint32_t)(acc * kBN), r, tok, g, bias, n0, 0, kBN);
             fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(TEMPTY + acc));
@@ -237,6 +245,192 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) {
         tmem_free(tmem_base, kTmemCols);
     }
+}
+
+// ---- the same GEMM on pairs of SMs (cluster of 2, tcgen05 cta_group::2) -------------------------------
+// A pair computes a 256 x 256 tile: each CTA holds 128 rows of A and 128 of the 256 weight rows of B per
+// K block (32 KiB a stage, so 6 stages fit), one thread of the even CTA issues M = 256 MMAs that read
+// both CTAs' shared memory and write each CTA's 128 accumulator rows into its own TMEM.  Per SM this
+// halves the B bytes per FLOP against the single-SM tile, so the ring covers 1.5x the load latency.
+// Tiles start on expert segment boundaries: an expert with an odd number of 128-row blocks ends with a
+// tile whose upper half is discarded.  Barriers: FULL (even CTA, count 1: its producer expects both
+// CTAs' bytes, and both CTAs' copies complete on it), EMPTY and TFULL (both CTAs, by multicast commit),
+// TEMPTY (even CTA, count 8: four epilogue warps of each CTA).
+constexpr int k2Stages = 6;
+constexpr uint32_t k2HalfB = 128 * kBK * 2;            // 16 KiB: 128 of the 256 weight rows
+constexpr uint32_t k2StageBytes = kABytes + k2HalfB;   // 32 KiB per CTA
+
+__device__ __forceinline__ void pair_tile(const int* s_tp, const int* s_off, int E, int n_tiles, int tile, int& e,
+                                          int& m0, int& n0) {
+    const int mt = tile / n_tiles;
+    n0 = (tile % n_tiles) * kBN;
+    int lo = 0, hi = E;  // s_tp[lo] <= mt < s_tp[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (s_tp[mid] <= mt) lo = mid; else hi = mid;
+    }
+    e = lo;
+    m0 = s_off[e] + (mt - s_tp[e]) * 256;
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const TcArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint8_t* sA = base;
+    uint8_t* sB = base + k2Stages * kABytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sB + k2Stages * k2HalfB);
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * k2Stages + 5);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+    int* s_off = reinterpret_cast<int*>(tmem_holder + 4);
+    int* s_tp = s_off + (a.E + 1);  // first 256-row tile of each expert (prefix), E + 1 entries
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    auto bar = [&](int i) { return smem_u32(bars + i); };
+    const int FULL = 0, EMPTY = k2Stages, TFULL = 2 * k2Stages, TEMPTY = 2 * k2Stages + 2, LAST = 2 * k2Stages + 4;
+
+    for (int i = threadIdx.x; i <= a.E; i += kThreads) s_off[i] = a.offset[i];
+    if (threadIdx.x == 0) {
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
+        *abort_flag = 0;
+        for (int st = 0; st < k2Stages; ++st) {
+            mbar_init(bar(FULL + st), 1);
+            mbar_init(bar(EMPTY + st), 1);
+        }
+        for (int st = 0; st < 2; ++st) {
+            mbar_init(bar(TFULL + st), 1);
+            mbar_init(bar(TEMPTY + st), 8);
+        }
+        mbar_init(bar(LAST), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {  // tiles per expert: its rows (a multiple of 128) in blocks of 256
+        int acc = 0;
+        for (int e = 0; e < a.E; ++e) {
+            s_tp[e] = acc;
+            acc += (s_off[e + 1] - s_off[e] + 255) / 256;
+        }
+        s_tp[a.E] = acc;
+    }
+    if (warp == 1) tmem_alloc_pair(smem_u32(tmem_holder), kTmemCols);
+    fence_before();
+    __syncthreads();
+    cluster_sync();  // the peer's barriers are initialised before anyone arrives on them
+    fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    const int n_tiles = (a.N + kBN - 1) / kBN;
+    const int num_tiles = s_tp[a.E] * n_tiles;
+    const int k_iters = a.K / kBK;
+    const int pair_id = blockIdx.x >> 1, num_pairs = gridDim.x >> 1;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            const uint32_t full0 = mapa_shared(bar(FULL), 0);  // the even CTA's FULL barriers
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true, any = false;
+            for (int tile = pair_id; ok && tile < num_tiles; tile += num_pairs) {
+                int e, m0, n0;
+                pair_tile(s_tp, s_off, a.E, n_tiles, tile, e, m0, n0);
+                for (int kb = 0; kb < k_iters; ++kb) {
+                    if (!mbar_wait_cluster(bar(EMPTY + stage), phase ^ 1u, abort_flag)) { ok = false; break; }
+                    const uint32_t fb = full0 + 8u * (uint32_t)stage;
+                    // the even CTA expects both CTAs' bytes (its own arrive is CTA-local and cheap); the odd
+                    // CTA's copies may land first, taking the transaction count below zero for a while
+                    if (leader) mbar_expect_tx(bar(FULL + stage), 2 * k2StageBytes);
+                    tma_load_2d_pair(smem_u32(sA + stage * kABytes), &tmA, fb, kb * kBK, m0 + 128 * (int)rank);
+                    tma_load_3d_pair(smem_u32(sB + stage * k2HalfB), &tmB, fb, kb * kBK, n0 + 128 * (int)rank, e);
+                    any = true;
+                    if (++stage == k2Stages) { stage = 0; phase ^= 1u; }
+                }
+            }
+            if (!ok) {
+                record_error(a.err, kErrTimeout, kWhereGemmProducer);
+                *abort_flag = 1;
+                // copies in flight signal the even CTA's barriers, which this CTA cannot poll: give them
+                // time to land before the shared memory they write is released
+                if (any)
+                    for (int i = 0; i < 2000; ++i) __nanosleep(1000);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && leader) {
+            constexpr uint32_t idesc = idesc_bf16(256, kBN);
+            int stage = 0;
+            uint32_t phase = 0;
+            int local = 0;
+            bool ok = true, any = false;
+            for (int tile = pair_id; ok && tile < num_tiles; tile += num_pairs, ++local) {
+                const int acc = local & 1;
+                const uint32_t acc_phase = (local >> 1) & 1;
+                if (!mbar_wait_cluster(bar(TEMPTY + acc), acc_phase ^ 1u, abort_flag)) { ok = false; break; }
+                fence_after();
+                const uint32_t d_tmem = tmem_base + acc * kBN;
+                for (int kb = 0; kb < k_iters; ++kb) {
+                    if (!mbar_wait_cluster(bar(FULL + stage), phase, abort_flag)) { ok = false; break; }
+                    fence_after();
+                    const uint64_t ad = smem_desc_sw128(smem_u32(sA + stage * kABytes));
+                    const uint64_t bd = smem_desc_sw128(smem_u32(sB + stage * k2HalfB));
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk)
+                        mma_bf16_pair(d_tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc,
+                                      (kb | kk) != 0);
+                    any = true;
+                    commit_pair_mc(bar(EMPTY + stage), 3);
+                    if (++stage == k2Stages) { stage = 0; phase ^= 1u; }
+                }
+                if (ok) commit_pair_mc(bar(TFULL + acc), 3);
+            }
+            if (!ok) {
+                record_error(a.err, kErrTimeout, kWhereGemmMma);
+                *abort_flag = 1;
+            }
+            if (any) {  // every MMA issued above has finished once LAST completes
+                commit_pair_mc(bar(LAST), 1);
+                mbar_wait_bounded(bar(LAST), 0);
+            }
+        }
+    } else {
+        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        const int row = q * 32 + lane;
+        const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+        const uint32_t tempty0 = mapa_shared(bar(TEMPTY), 0);
+        int local = 0;
+        for (int tile = pair_id; tile < num_tiles; tile += num_pairs, ++local) {
+            const int acc = local & 1;
+            const uint32_t acc_phase = (local >> 1) & 1;
+            const bool ok = __all_sync(0xffffffffu, mbar_wait_cluster(bar(TFULL + acc), acc_phase, abort_flag));
+            if (!ok) {
+                if (lane == 0) {
+                    record_error(a.err, kErrTimeout, kWhereGemmEpilogue);
+                    *abort_flag = 1;
+                }
+                break;
+            }
+            fence_after();
+            int e, m0, n0;
+            pair_tile(s_tp, s_off, a.E, n_tiles, tile, e, m0, n0);
+            const int r = m0 + 128 * (int)rank + row;
+            const int tok = r < s_off[e + 1] ? a.row_token[r] : -1;  // beyond the segment: discarded
+            const float g = (a.mode == 2 && tok >= 0) ? a.row_gate[r] : 0.f;
+            const bf16_t* bias = a.bias ? a.bias + (size_t)e * a.N : nullptr;
+            epilogue_cols(a, tmem_base + lane_base + (uint32_t)(acc * kBN), r, tok, g, bias, n0, 0, kBN);
+            fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(tempty0 + 8u * (uint32_t)acc);
+        }
+    }
+    fence_before();
+    __syncthreads();
+    cluster_sync();  // both CTAs are done with the pair's TMEM and barriers
+    fence_after();
+    if (warp == 1) tmem_free_pair(tmem_base, kTmemCols);
 }
 
 // ---- host side ----------------------------------------------------------------------------------
@@ -298,6 +492,32 @@ bool tma_map_bf16(const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2, uint32
     return true;
 }
 
+// clusters of two of the pair kernel that can be resident at once (cached per shared-memory size)
+int pair_clusters(size_t smem) {
+    static size_t cached_smem = 0;
+    static int cached = 0;
+    if (cached_smem == smem && cached > 0) return cached;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * 74, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_pair_kernel, &cfg) != cudaSuccess || n <= 0) {
+        cudaGetLastError();
+        n = device_sm_count() / 2;
+    }
+    cached_smem = smem;
+    cached = n;
+    return n;
+}
+
 int device_sm_count() {
     static int n = 0;
     if (n == 0) {
@@ -311,6 +531,10 @@ int device_sm_count() {
 
 size_t ffn_tc_smem_bytes(int E) {
     return 1024 + (size_t)kStages * kStageBytes + (2 * kStages + 5) * 8 + 16 + 4 * (size_t)(E + 1);
+}
+
+size_t ffn_tc_pair_smem_bytes(int E) {
+    return 1024 + (size_t)k2Stages * k2StageBytes + (2 * k2Stages + 5) * 8 + 16 + 8 * (size_t)(E + 1);
 }
 
 cudaError_t launch_ffn_tc(const FfnParams& P, cudaStream_t s) {
@@ -331,6 +555,20 @@ cudaError_t launch_ffn_tc(const FfnParams& P, cudaStream_t s) {
     a.N = P.N;
     a.mode = P.mode;
     a.err = P.err;
+    if (P.pair) {
+        // pairs of SMs: B boxes of 128 weight rows (half of a 256-wide tile), grid = 2 x the clusters that fit
+        CUtensorMap mb2;
+        if (!tma_map_bf16(P.W, (uint64_t)P.K, (uint64_t)P.N, (uint64_t)P.E, 128, &mb2)) return cudaErrorInvalidValue;
+        const size_t smem2 = ffn_tc_pair_smem_bytes(P.E);
+        cudaError_t e2 =
+            cudaFuncSetAttribute(gemm_tc_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2);
+        if (e2 != cudaSuccess) return e2;
+        const int64_t max_tiles = (P.rows_cap / kBM + P.E) / 2 * (int64_t)((P.N + kBN - 1) / kBN) + 1;
+        int pairs = pair_clusters(smem2);
+        if (max_tiles < pairs) pairs = (int)max_tiles;
+        gemm_tc_pair_kernel<<<2 * pairs, kThreads, smem2, s>>>(ma, mb2, a);
+        return cudaGetLastError();
+    }
     const size_t smem = ffn_tc_smem_bytes(P.E);
     cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;

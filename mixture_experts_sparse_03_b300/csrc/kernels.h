@@ -94,6 +94,7 @@ struct FfnParams {
     void* C;                  // mode 0: hidden [rows, N] (dtype); mode 1: y [rows, N] fp32
     float* out;               // mode 2: [T, N] fp32
     int E, K, N, bf16, mode;
+    int pair;                 // tensor-core kernel on pairs of SMs (256 x 256 tiles)
     int64_t rows_cap;
     int* err;
 };

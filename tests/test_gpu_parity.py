@@ -220,3 +220,21 @@ def test_gate_logits_bound_under_cancellation():
     ratio = _logits_error_ratio(wl, tc, tg)
     print("cancellation: observed error / (2^-23 sum|x w|) = %.3e" % ratio)
     assert ratio < 8.0
+
+
+PAIR_CASES = [wl for wl in SMALL if wl.dtype == "bf16"] + [
+    small_workload(T=1500, d=128, h=512, E=3, k=2, capacity_factor=1.0),   # several 256-row tiles per expert
+    small_workload(T=700, d=256, h=256, E=5, k=1, capacity_factor=2.0, bias="none"),
+]
+
+
+@pytest.mark.parametrize("wl", PAIR_CASES, ids=_id)
+def test_expert_ffn_on_sm_pairs(wl):
+    """The expert GEMMs on pairs of SMs (tcgen05 cta_group::2, 256 x 256 tiles), forced on small layers
+    whose experts end in odd 128-row blocks (the upper half of their last tile is discarded)."""
+    _full_check(wl, flags=b.FLAG_FFN_SM_PAIR)
+
+
+def test_expert_ffn_single_sm_on_large_experts():
+    """The single-SM expert GEMMs, forced on a layer that would use pairs by default."""
+    _full_check(small_workload(T=2048, d=128, h=256, E=2, k=2, capacity_factor=1.0), flags=b.FLAG_FFN_ONE_SM)
