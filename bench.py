@@ -40,9 +40,14 @@ RIDGE_ROWS = 268  # bf16: FLOP per expert-weight byte = rows per expert; ridge =
 
 
 def kernel_names(wl, launches: int):
-    """Names of the kernels moe_forward launches, in launch order."""
-    names = (["gate_logits_gemm"] if wl.dtype == "bf16" else []) + ["gate_topk_scan", "dispatch_assign_gather",
-                                                                      "expert_up_gelu"]
+    """Names of the kernels moe_forward launches, in launch order (the softmax gate of a bf16 layer with
+    E <= 64 runs as one fused launch)."""
+    if wl.dtype == "bf16" and wl.gate == "softmax" and wl.E <= 64:
+        names = ["gate_fused_gemm_topk_scan", "dispatch_gather", "expert_up_gelu"]
+    elif wl.dtype == "bf16":
+        names = ["gate_logits_gemm", "gate_topk_scan", "dispatch_gather", "expert_up_gelu"]
+    else:
+        names = ["gate_topk_scan", "dispatch_gather", "expert_up_gelu"]
     names += ["expert_down_combine"] if wl.k <= 2 else ["expert_down", "combine_gather"]
     if len(names) != launches:
         raise RuntimeError("moe_forward launches %d kernels, expected %d" % (launches, len(names)))

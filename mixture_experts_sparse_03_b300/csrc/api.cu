@@ -84,7 +84,7 @@ moe_status make_plan(const moe_config* c, Plan* pl) {
     if (gsm > (size_t)kMaxSmem) return MOE_ERR_UNSUPPORTED;
     P.N0 = P.gate == MOE_GATE_COSINE ? P.p : P.E;
     P.N1 = P.gate == MOE_GATE_NOISY ? P.E : 0;
-    P.gg = gate_gemm_plan(P.T, P.d, P.N0, P.N1, kPlanSms);
+    P.gg = gate_gemm_plan(P.T, P.d, P.N0, P.N1, kPlanSms, P.gate == MOE_GATE_SOFTMAX);
     P.Ceff = std::min(P.C, P.T);  // a token takes an expert at most once, so C >= T drops nothing
     const int64_t cpad = ((int64_t)P.Ceff + kRowAlign - 1) / kRowAlign * kRowAlign;
     P.rows = std::min<int64_t>((int64_t)P.T * P.k + (int64_t)(kRowAlign - 1) * P.E, (int64_t)P.E * cpad);
@@ -209,16 +209,24 @@ moe_status gate_logits_tc(const Plan& P, GateParams& g, void* ws, cudaStream_t s
     float* part = at<float>(ws, P.o_part);
     float* xn2 = at<float>(ws, P.o_xn2);
     float* wn2 = at<float>(ws, P.o_wn2);
-    MOE_TRY(launch(s, [&] {
-        return launch_gate_gemm(P.gg, g.x, w0, w1, P.T, P.d, P.N0, P.N1, part, xn2, wn2, at<int>(ws, P.o_err), s);
-    }));
     g.part = part;
     g.xn2p = xn2;
     g.wn2p = wn2;
     g.S = P.gg.S;
     g.Np = P.gg.Np;
     g.cb = (float)(kTcErr * 1.1920928955078125e-07 + (P.gg.S + 1) * 5.9604644775390625e-08);
-    return MOE_OK;
+    return launch(s, [&] {
+        return launch_gate_gemm(P.gg, g.x, w0, w1, P.T, P.d, P.N0, P.N1, part, xn2, wn2, at<int>(ws, P.o_err), &g, s);
+    });
+}
+
+// the whole gate: the logits GEMM (bf16 layers) and the selection, or both fused into one launch
+moe_status run_gate(const Plan& P, GateParams& g, void* ws, cudaStream_t s) {
+    if (P.bf16) {
+        MOE_TRY(gate_logits_tc(P, g, ws, s));
+        if (P.gg.fused) return MOE_OK;
+    }
+    return launch(s, [&] { return launch_gate(g, s); });
 }
 
 FfnParams ffn_params(const Plan& P, int mode, const void* A, const void* W, const void* bias, const int* off,
@@ -282,7 +290,7 @@ int32_t moe_forward_launches(const moe_config* cfg) {
     Plan P;
     if (make_plan(cfg, &P) != MOE_OK) return -1;
     if (P.T == 0) return 0;
-    return (P.fused ? 4 : 5) + (P.bf16 ? 1 : 0);
+    return (P.fused ? 4 : 5) + (P.bf16 && !P.gg.fused ? 1 : 0);
 }
 
 moe_status moe_route(const moe_config* cfg, const void* x, const void* w_gate, const void* w_noise,
@@ -298,8 +306,7 @@ moe_status moe_route(const moe_config* cfg, const void* x, const void* w_gate, c
     if (cudaMemsetAsync(err, 0, 8, s) != cudaSuccess) return MOE_ERR_CUDA;
     GateParams g = gate_params(P, cfg, x, w_gate, w_noise, noise_eps, proj, expert_emb, topk_idx, topk_gate);
     g.err = err;
-    if (P.bf16) MOE_TRY(gate_logits_tc(P, g, workspace, s));
-    return launch(s, [&] { return launch_gate(g, s); });
+    return run_gate(P, g, workspace, s);
 }
 
 moe_status moe_gate_logits(const moe_config* cfg, const void* x, const void* w_gate, const void* w_noise,
@@ -316,9 +323,9 @@ moe_status moe_gate_logits(const moe_config* cfg, const void* x, const void* w_g
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     int* err = at<int>(workspace, P.o_err);
     if (cudaMemsetAsync(err, 0, 8, s) != cudaSuccess) return MOE_ERR_CUDA;
-    const GateGemmPlan one = gate_gemm_plan(P.T, P.d, P.N0, P.N1, 1);  // one split: the whole K in TMEM
+    const GateGemmPlan one = gate_gemm_plan(P.T, P.d, P.N0, P.N1, 1, false);  // one split, logits out
     return launch(s, [&] {
-        return launch_gate_gemm(one, x, w0, w1, P.T, P.d, P.N0, P.N1, logits, nullptr, nullptr, err, s);
+        return launch_gate_gemm(one, x, w0, w1, P.T, P.d, P.N0, P.N1, logits, nullptr, nullptr, err, nullptr, s);
     });
 }
 
@@ -409,7 +416,6 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const void* w_gate,
     // error word, its info and the gate's block ticket start at zero
     if (cudaMemsetAsync(err, 0, 16, s) != cudaSuccess) return MOE_ERR_CUDA;
     GateParams g = gate_params(P, cfg, x, w_gate, w_noise, noise_eps, proj, expert_emb, idx, gate);
-    if (P.bf16) MOE_TRY(gate_logits_tc(P, g, workspace, s));
     g.blk_hist = hist;
     g.slot = slot;
     g.err = err;
@@ -419,7 +425,7 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const void* w_gate,
     g.offset = off;
     g.row_token = rtok;
     g.row_gate = rgate;
-    MOE_TRY(launch(s, [&] { return launch_gate(g, s); }));
+    MOE_TRY(run_gate(P, g, workspace, s));
     MOE_TRY(launch(s, [&] {
         return launch_dispatch_gather(x, P.bf16, idx, gate, hist, off, P.T, P.k, P.E, P.d, P.Ceff, slot, rtok, rgate,
                                       xd, P.fused ? out : nullptr, s);

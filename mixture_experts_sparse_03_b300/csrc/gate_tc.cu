@@ -19,10 +19,15 @@
 // 64 products and the error bound does not grow with d), compute the squared norms of the x rows
 // (n-tile 0) and weight rows (m-tile 0) from the shared-memory tiles -- the selection kernel bounds
 // each logit's error by them -- and store the logits.
+// When one CTA holds every logit of its tokens (softmax gate, E <= 64) the selection runs in the same
+// epilogue (fused_select): scores, top-k, near-tie re-scoring, gates, the dispatch's pair ranks and
+// block histograms, and the dispatch scan in the last CTA -- the whole gate in one launch.
 // Every mbarrier wait is bounded; on expiry the kernel records MOE_ERR_DEVICE_TIMEOUT, waits (bounded)
 // for its own copies and MMAs, frees its TMEM and returns.
 #include "common.cuh"
+#include "gate_common.cuh"
 #include "kernels.h"
+#include "scan.cuh"
 #include "tc_ptx.cuh"
 
 namespace moe {
@@ -30,8 +35,13 @@ namespace moe {
 namespace {
 
 using namespace tc;
+using gate::kMaxCand;
+using gate::kU;
 
-constexpr int kGM = 128, kGK = 64, kGStages = 4, kGThreads = 192;
+constexpr int kGM = 128, kGK = 64;
+constexpr int kGMaxStages = 12;  // TMA ring depth: as many stages as fit (the CTAs are few and latency-bound)
+constexpr int kGThreads = 320;  // producer, MMA, 4 accumulation warps, 4 norm warps
+constexpr int kGChunks = 8;     // TMEM accumulators the MMAs rotate through
 constexpr int kGMaxBN = 64;  // logits per n-tile: the epilogue holds 64 float-float sums per row
 constexpr uint32_t kGABytes = kGM * kGK * 2;  // 16 KiB
 
@@ -42,7 +52,7 @@ struct GemmArgs {
     const bf16_t* x;   // [T, d]
     const bf16_t* w0;  // [N0, d]
     const bf16_t* w1;  // [N1, d] or nullptr
-    int T, d, N0, N1, Np, BN, nt0, per, kb;
+    int T, d, N0, N1, Np, BN, nt0, per, kb, stages;
     int* err;
 };
 
@@ -65,18 +75,170 @@ __device__ __forceinline__ float sumsq_tile_row(const uint8_t* row) {
     return ((s[0] + s[1]) + (s[2] + s[3])) + ((s[4] + s[5]) + (s[6] + s[7]));
 }
 
+// Fused selection smem (softmax gate, all logits in one n-tile): per row the top-(k+1) values and ids and
+// the chosen ids, per warp the row being re-scored and its contenders, the weight-row norms, per warp the
+// dispatch rank counters, and the dispatch scan's scratch.
+struct FusedSmem {
+    float selv[kGM][kMaxTopK + 1];
+    int seli[kGM][kMaxTopK + 1];
+    int fidx[kGM][kMaxTopK];
+    float xn2[kGM];
+    float wn2[kGMaxBN];
+    float wsc[4][kGMaxBN];
+    int cand[4][kMaxCand];
+    double ex[4][kMaxCand];
+    int running[4][kGMaxBN];
+    int part[kGThreads];
+    int padded[kGMaxBN + 1];
+    int kept[kGMaxBN];
+    int wsum[33];
+    int last;
+};
+
+// Selection in the epilogue of the logits GEMM when one CTA holds all of a token's logits (softmax gate,
+// E <= 64): the thread owning row r has its token's logits as float-float sums; it forms the error
+// bound, picks the top-(k+1) (ties -> lower id), writes ids and gates, or queues the token when two of
+// them lie within twice the bound; the warp then re-scores each queued token's contenders with
+// float-float dot products, and finally numbers its 32 tokens' pairs for the dispatch.
+template <int BNC>
+__device__ __forceinline__ void fused_select(const GateParams& P, FusedSmem& fs, const float (&hi)[BNC],
+                                             const float (&lo)[BNC], int m0, int r, int lane, int q) {
+    const int E = P.E, k = P.k, ksel = min(k + 1, E);
+    const int t = m0 + r;
+    const bool valid = t < P.T;
+    const float xn = sqrtf(fs.xn2[r]);
+    float L[BNC];
+#pragma unroll
+    for (int j = 0; j < BNC; ++j) L[j] = hi[j] + lo[j];
+    float dmax = 0.f;
+#pragma unroll
+    for (int j = 0; j < BNC; ++j)
+        if (j < E) dmax = fmaxf(dmax, P.cb * xn * sqrtf(fs.wn2[j]) + 4.f * kU * fabsf(L[j]));
+    dmax *= 1.0625f;
+    uint64_t taken = 0;
+    for (int s2 = 0; s2 < ksel; ++s2) {
+        float bv = -INFINITY;
+        int bi = -1;
+#pragma unroll
+        for (int j = 0; j < BNC; ++j)
+            if (j < E && !((taken >> j) & 1ull) && (bi < 0 || L[j] > bv)) { bv = L[j]; bi = j; }
+        taken |= 1ull << bi;
+        fs.selv[r][s2] = bv;
+        fs.seli[r][s2] = bi;
+    }
+    const float two_d = 2.f * dmax;
+    bool refine = false;
+    for (int s2 = 1; s2 < k; ++s2) refine |= !(fs.selv[r][s2 - 1] - fs.selv[r][s2] > two_d);
+    if (k < E) refine |= !(fs.selv[r][k - 1] - fs.selv[r][k] > two_d);
+    const float m = fs.selv[r][0];
+    float den_all = 0.f;
+    if (P.norm == 0) {
+#pragma unroll
+        for (int j = 0; j < BNC; ++j)
+            if (j < E) den_all += expf(L[j] - m);
+    }
+    if (valid && !refine) {
+        float den = den_all;
+        if (P.norm != 0) {
+            den = 0.f;
+            for (int s2 = 0; s2 < k; ++s2) den += expf(fs.selv[r][s2] - m);
+        }
+        for (int s2 = 0; s2 < k; ++s2) {
+            P.topk_idx[(size_t)t * k + s2] = fs.seli[r][s2];
+            P.topk_gate[(size_t)t * k + s2] = expf(fs.selv[r][s2] - m) / den;
+            fs.fidx[r][s2] = fs.seli[r][s2];
+        }
+    }
+    // the warp re-scores its queued rows one at a time
+    unsigned flagged = __ballot_sync(0xffffffffu, valid && refine);
+    while (flagged) {
+        const int src = __ffs(flagged) - 1;
+        flagged &= flagged - 1;
+        if (lane == src) {
+#pragma unroll
+            for (int j = 0; j < BNC; ++j)
+                if (j < E) fs.wsc[q][j] = L[j];
+        }
+        __syncwarp();
+        const int rs = q * 32 + src, ts = m0 + rs;
+        const float thr = __shfl_sync(0xffffffffu, fs.selv[r][k - 1] - two_d, src);
+        const float ms = __shfl_sync(0xffffffffu, m, src);
+        const float dens = __shfl_sync(0xffffffffu, den_all, src);
+        int cnt = 0;
+        for (int base = 0; base < E; base += 32) {
+            const int e = base + lane;
+            const bool pred = e < E && !(fs.wsc[q][e] < thr);
+            const unsigned mask = __ballot_sync(0xffffffffu, pred);
+            const int pos = cnt + __popc(mask & lanemask_lt());
+            if (pred && pos < kMaxCand) fs.cand[q][pos] = e;
+            cnt += __popc(mask);
+        }
+        cnt = min(cnt, kMaxCand);
+        __syncwarp();
+        const bf16_t* xr = static_cast<const bf16_t*>(P.x) + (size_t)ts * P.d;
+        for (int c = 0; c < cnt; ++c) {
+            const double v = gate::warp_dot_ff<bf16_t>(
+                xr, static_cast<const bf16_t*>(P.w_gate) + (size_t)fs.cand[q][c] * P.d, P.d, lane);
+            if (lane == 0) fs.ex[q][c] = v;
+        }
+        __syncwarp();
+        if (lane == 0) {
+            uint64_t used = 0;
+            int chosen[kMaxTopK];
+            for (int s2 = 0; s2 < k; ++s2) {
+                int best = -1;
+                for (int c = 0; c < cnt; ++c) {
+                    if ((used >> c) & 1ull) continue;
+                    if (best < 0 || fs.ex[q][c] > fs.ex[q][best] ||
+                        (fs.ex[q][c] == fs.ex[q][best] && fs.cand[q][c] < fs.cand[q][best]))
+                        best = c;
+                }
+                used |= 1ull << best;
+                chosen[s2] = fs.cand[q][best];
+            }
+            float den = dens;
+            if (P.norm != 0) {
+                den = 0.f;
+                for (int s2 = 0; s2 < k; ++s2) den += expf(fs.wsc[q][chosen[s2]] - ms);
+            }
+            for (int s2 = 0; s2 < k; ++s2) {
+                P.topk_idx[(size_t)ts * k + s2] = chosen[s2];
+                P.topk_gate[(size_t)ts * k + s2] = expf(fs.wsc[q][chosen[s2]] - ms) / den;
+                fs.fidx[rs][s2] = chosen[s2];
+            }
+        }
+        __syncwarp();
+    }
+    // the dispatch's first step on this warp's 32 tokens (one dispatch block): pair ranks, histogram
+    if (P.blk_hist != nullptr) {
+        const int t0 = m0 + q * 32;
+        const int ntok = min(32, P.T - t0);
+        if (ntok > 0) {
+            for (int e = lane; e < E; e += 32) fs.running[q][e] = 0;
+            __syncwarp();
+            rank_pairs_warp([&](int i) { return fs.fidx[q * 32 + i / k][i % k]; }, ntok * k, fs.running[q],
+                            P.slot + (size_t)t0 * k, lane);
+            __syncwarp();
+            for (int e = lane; e < E; e += 32) P.blk_hist[(size_t)(t0 / 32) * E + e] = fs.running[q][e];
+        }
+    }
+}
+
+template <bool FUSED, int BNC>
 __global__ void __launch_bounds__(kGThreads, 1)
     gate_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
-                     const __grid_constant__ CUtensorMap tmB1, const GemmArgs a) {
+                     const __grid_constant__ CUtensorMap tmB1, const GemmArgs a, const GateParams P) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t b_bytes = (uint32_t)a.BN * kGK * 2;
     const uint32_t stage_bytes = kGABytes + b_bytes;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(base + kGStages * stage_bytes);
-    // bars: full[kGStages], empty[kGStages], chunk_full[2], chunk_empty[2], last
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * kGStages + 5);
+    const int NS = a.stages;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(base + NS * stage_bytes);
+    // bars: full[NS], empty[NS], chunk_full[kGChunks], chunk_empty[kGChunks], last
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * NS + 2 * kGChunks + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
-    const int FULL = 0, EMPTY = kGStages, CFULL = 2 * kGStages, CEMPTY = 2 * kGStages + 2, LAST = 2 * kGStages + 4;
+    FusedSmem& fs = *reinterpret_cast<FusedSmem*>(tmem_holder + 4);
+    const int FULL = 0, EMPTY = NS, CFULL = 2 * NS, CEMPTY = 2 * NS + kGChunks, LAST = 2 * NS + 2 * kGChunks;
     auto bar = [&](int i) { return smem_u32(bars + i); };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -88,21 +250,22 @@ __global__ void __launch_bounds__(kGThreads, 1)
     const int m0 = mt * kGM;
     const int kb0 = split * a.per, kb1 = min(a.kb, kb0 + a.per);
     const int nkb = kb1 - kb0;
-    const bool x_norms = a.xn2_part != nullptr && nt == 0;
-    const bool w_norms = a.wn2_part != nullptr && mt == 0;
-    const bool readers = x_norms || w_norms;  // epilogue warps read the smem tiles too
+    const int ncols = min(a.BN, n_map - n_local);
+    const bool x_norms = FUSED || (a.xn2_part != nullptr && nt == 0);
+    const bool w_norms = FUSED || (a.wn2_part != nullptr && mt == 0);
+    const bool readers = x_norms || w_norms;  // the norm warps read the smem tiles too
     uint32_t tcols = 32;
-    while (tcols < 2u * (uint32_t)a.BN) tcols <<= 1;
+    while (tcols < (uint32_t)(kGChunks * a.BN)) tcols <<= 1;
 
     if (threadIdx.x == 0) {
         prefetch_tmap(&tmA);
         prefetch_tmap(second ? &tmB1 : &tmB0);
         *abort_flag = 0;
-        for (int s = 0; s < kGStages; ++s) {
+        for (int s = 0; s < NS; ++s) {
             mbar_init(bar(FULL + s), 1);
             mbar_init(bar(EMPTY + s), readers ? 5 : 1);
         }
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < kGChunks; ++s) {
             mbar_init(bar(CFULL + s), 1);
             mbar_init(bar(CEMPTY + s), 4);
         }
@@ -118,9 +281,9 @@ __global__ void __launch_bounds__(kGThreads, 1)
     if (warp == 0) {
         if (lane == 0) {
             const CUtensorMap* mb = second ? &tmB1 : &tmB0;
-            uint32_t issued_phase[kGStages];
-            bool issued[kGStages];
-            for (int s = 0; s < kGStages; ++s) { issued[s] = false; issued_phase[s] = 0; }
+            uint32_t issued_phase[kGMaxStages];
+            bool issued[kGMaxStages];
+            for (int s = 0; s < kGMaxStages; ++s) { issued[s] = false; issued_phase[s] = 0; }
             bool ok = true;
             int stage = 0;
             uint32_t phase = 0;
@@ -132,26 +295,27 @@ __global__ void __launch_bounds__(kGThreads, 1)
                 tma_load_2d(smem_u32(st + kGABytes), mb, bar(FULL + stage), kb * kGK, n_local);
                 issued[stage] = true;
                 issued_phase[stage] = phase;
-                if (++stage == kGStages) { stage = 0; phase ^= 1u; }
+                if (++stage == NS) { stage = 0; phase ^= 1u; }
             }
             if (!ok) {
                 record_error(a.err, kErrTimeout, kWhereGateGemm);
                 *abort_flag = 1;
-                for (int s = 0; s < kGStages; ++s)
+                for (int s = 0; s < NS; ++s)
                     if (issued[s]) mbar_wait_bounded(bar(FULL + s), issued_phase[s]);
             }
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            // each 64-wide K block goes to a fresh accumulator (two, alternating), which the epilogue
-            // adds into float-float sums: the tensor cores' rounding only ever spans 64 products
+            // each 64-wide K block goes to a fresh accumulator (kGChunks of them, in turn), which the
+            // accumulation warps add into float-float sums: the tensor cores' rounding only ever spans 64
+            // products, and the MMAs run up to kGChunks blocks ahead of the additions
             const uint32_t idesc = idesc_bf16(kGM, a.BN);
             bool ok = true, any = false;
             int stage = 0;
             uint32_t phase = 0;
             for (int i = 0; i < nkb; ++i) {
-                const int buf = i & 1;
-                if (!mbar_wait(bar(CEMPTY + buf), ((i >> 1) & 1) ^ 1u, abort_flag)) { ok = false; break; }
+                const int buf = i % kGChunks;
+                if (!mbar_wait(bar(CEMPTY + buf), ((i / kGChunks) & 1) ^ 1u, abort_flag)) { ok = false; break; }
                 if (!mbar_wait(bar(FULL + stage), phase, abort_flag)) { ok = false; break; }
                 fence_after();
                 uint8_t* st = base + stage * stage_bytes;
@@ -164,7 +328,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
                 any = true;
                 commit(bar(EMPTY + stage));
                 commit(bar(CFULL + buf));
-                if (++stage == kGStages) { stage = 0; phase ^= 1u; }
+                if (++stage == NS) { stage = 0; phase ^= 1u; }
             }
             if (!ok) {
                 record_error(a.err, kErrTimeout, kWhereGateGemm);
@@ -175,35 +339,51 @@ __global__ void __launch_bounds__(kGThreads, 1)
                 mbar_wait_bounded(bar(LAST), 0);
             }
         }
-    } else {
-        const int q = warp & 3;  // TMEM lane quarter this warp may access
-        const int r = q * 32 + lane;
-        const int et = threadIdx.x - 64;  // 0..127
-        const int ncols = min(a.BN, n_map - n_local);
-        float hi[64], lo[64];
-#pragma unroll
-        for (int j = 0; j < 64; ++j) hi[j] = lo[j] = 0.f;
+    } else if (warp >= 6) {
+        // norm warps: squared norms of the x rows and weight rows over this CTA's K range, from the tiles
+        const int nr = threadIdx.x - 192;  // 0..127
         float xs = 0.f, wsq = 0.f;
         bool ok = true;
         int stage = 0;
         uint32_t phase = 0;
-        for (int i = 0; i < nkb && ok; ++i) {
-            if (readers) {  // squared norms of this row of x and of this weight row, from the smem tiles
-                ok = __all_sync(0xffffffffu, mbar_wait(bar(FULL + stage), phase, abort_flag));
-                if (!ok) break;
-                const uint8_t* st = base + stage * stage_bytes;
-                if (x_norms) xs += sumsq_tile_row(st + r * 128);
-                if (w_norms && et < a.BN) wsq += sumsq_tile_row(st + kGABytes + et * 128);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(EMPTY + stage));
-                if (++stage == kGStages) { stage = 0; phase ^= 1u; }
+        for (int i = 0; i < nkb && readers; ++i) {
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(FULL + stage), phase, abort_flag));
+            if (!ok) break;
+            const uint8_t* st = base + stage * stage_bytes;
+            if (x_norms) xs += sumsq_tile_row(st + nr * 128);
+            if (w_norms && nr < a.BN) wsq += sumsq_tile_row(st + kGABytes + nr * 128);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(EMPTY + stage));
+            if (++stage == NS) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) {
+            if (lane == 0) {
+                record_error(a.err, kErrTimeout, kWhereGateGemm);
+                *abort_flag = 1;
             }
-            const int buf = i & 1;
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(CFULL + buf), (i >> 1) & 1, abort_flag));
+        } else if constexpr (!FUSED) {
+            if (x_norms && m0 + nr < a.T) a.xn2_part[(size_t)split * a.T + m0 + nr] = xs;
+            if (w_norms && nr < ncols) a.wn2_part[(size_t)split * a.Np + col0 + nr] = wsq;
+        } else {
+            fs.xn2[nr] = xs;
+            if (nr < ncols) fs.wn2[nr] = wsq;
+        }
+        if constexpr (FUSED) asm volatile("bar.sync 1, 256;" ::: "memory");  // norms ready for the selection
+    } else {
+        // accumulation warps: one per TMEM lane quarter (32 rows)
+        const int q = warp & 3;
+        const int r = q * 32 + lane;
+        float hi[BNC], lo[BNC];
+#pragma unroll
+        for (int j = 0; j < BNC; ++j) hi[j] = lo[j] = 0.f;
+        bool ok = true;
+        for (int i = 0; i < nkb && ok; ++i) {
+            const int buf = i % kGChunks;
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(CFULL + buf), (i / kGChunks) & 1, abort_flag));
             if (!ok) break;
             fence_after();
 #pragma unroll
-            for (int c0 = 0; c0 < 64; c0 += 16) {
+            for (int c0 = 0; c0 < BNC; c0 += 16) {
                 if (c0 < a.BN) {
                     uint32_t v[16];
                     tmem_ld16(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * a.BN + c0), v);
@@ -225,28 +405,49 @@ __global__ void __launch_bounds__(kGThreads, 1)
                 record_error(a.err, kErrTimeout, kWhereGateGemm);
                 *abort_flag = 1;
             }
-        } else {
+        }
+        if constexpr (!FUSED) {
             const int row = m0 + r;
-            if (row < a.T) {
+            if (ok && row < a.T) {
                 float* dst = a.part + ((size_t)split * a.T + row) * a.Np + col0;
 #pragma unroll
-                for (int j = 0; j < 64; ++j)
+                for (int j = 0; j < BNC; ++j)
                     if (j < ncols) dst[j] = hi[j] + lo[j];
-                if (x_norms) a.xn2_part[(size_t)split * a.T + row] = xs;
             }
-            if (w_norms && et < ncols) a.wn2_part[(size_t)split * a.Np + col0 + et] = wsq;
+        } else {
+            asm volatile("bar.sync 1, 256;" ::: "memory");  // the norm warps' results
+            if (ok) fused_select<BNC>(P, fs, hi, lo, m0, r, lane, q);
         }
     }
     fence_before();
     __syncthreads();
     fence_after();
     if (warp == 1) tmem_free(tmem_base, tcols);
+    if constexpr (FUSED) {
+        // the dispatch scan runs in the last CTA to finish its blocks' histograms
+        if (P.blk_hist != nullptr && P.ticket != nullptr) {
+            if (threadIdx.x == 0) {
+                __threadfence();
+                fs.last = atomicAdd(P.ticket, 1) == (int)gridDim.x - 1;
+                __threadfence();
+            }
+            __syncthreads();
+            if (fs.last) {
+                ScanSmem sm{fs.part, fs.padded, fs.kept, fs.wsum};
+                const int nblk = (P.T + kTokensPerBlock - 1) / kTokensPerBlock;
+                scan_experts(P.blk_hist, nblk, P.E, P.C, P.count, P.offset, P.row_token, P.row_gate, sm);
+                if (threadIdx.x == 0) *P.ticket = 0;  // ready for the next call
+            }
+        }
+    }
 }
 
 }  // namespace
 
-GateGemmPlan gate_gemm_plan(int T, int d, int N0, int N1, int sms) {
+GateGemmPlan gate_gemm_plan(int T, int d, int N0, int N1, int sms, bool fuse_select) {
     GateGemmPlan g{};
+    g.fused = fuse_select && N1 == 0 && N0 <= kGMaxBN;
+    if (g.fused) sms = 1;  // one split: the CTA holds every logit of its tokens
     const int nmax = N0 > N1 ? N0 : N1;
     g.BN = nmax >= kGMaxBN ? kGMaxBN : (nmax + 15) / 16 * 16;
     if (g.BN < 16) g.BN = 16;
@@ -262,13 +463,18 @@ GateGemmPlan gate_gemm_plan(int T, int d, int N0, int N1, int sms) {
     if (S < 1) S = 1;
     g.per = (g.kb + S - 1) / S;
     g.S = (g.kb + g.per - 1) / g.per;
-    g.smem = 1024 + (size_t)kGStages * (kGABytes + (size_t)g.BN * kGK * 2) + (2 * kGStages + 5) * 8 + 16;
+    const size_t stage_bytes = kGABytes + (size_t)g.BN * kGK * 2;
+    const size_t fixed = 1024 + 16 + (g.fused ? sizeof(FusedSmem) : 0) + (2 * kGChunks + 1) * 8;
+    g.stages = (int)((200 * 1024 - fixed) / (stage_bytes + 16));
+    if (g.stages > kGMaxStages) g.stages = kGMaxStages;
+    if (g.stages > g.per) g.stages = g.per < 2 ? 2 : g.per;
+    g.smem = fixed + (size_t)g.stages * (stage_bytes + 16);
     return g;
 }
 
 cudaError_t launch_gate_gemm(const GateGemmPlan& g, const void* x, const void* w0, const void* w1, int T, int d,
                              int N0, int N1, float* part, float* xn2_part, float* wn2_part, int* err,
-                             cudaStream_t s) {
+                             const GateParams* sel, cudaStream_t s) {
     if (T <= 0) return cudaSuccess;
     CUtensorMap ma, mb0, mb1;
     if (!tma_map_bf16(x, (uint64_t)d, (uint64_t)T, 0, kGM, &ma)) return cudaErrorInvalidValue;
@@ -294,11 +500,25 @@ cudaError_t launch_gate_gemm(const GateGemmPlan& g, const void* x, const void* w
     a.nt0 = g.nt0;
     a.per = g.per;
     a.kb = g.kb;
+    a.stages = g.stages;
     a.err = err;
-    cudaError_t e = cudaFuncSetAttribute(gate_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)g.smem);
-    if (e != cudaSuccess) return e;
     dim3 grid(g.mt, g.nt0 + g.nt1, g.S);
-    gate_gemm_kernel<<<grid, kGThreads, g.smem, s>>>(ma, mb0, mb1, a);
+    if (g.fused && sel == nullptr) return cudaErrorInvalidValue;
+    const GateParams none{};
+    auto go = [&](auto kern, const GateParams& p) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)g.smem);
+        if (e != cudaSuccess) return e;
+        kern<<<grid, kGThreads, g.smem, s>>>(ma, mb0, mb1, a, p);
+        return cudaSuccess;
+    };
+    cudaError_t e;
+    if (g.fused)
+        e = g.BN <= 16 ? go(gate_gemm_kernel<true, 16>, *sel)
+            : g.BN <= 32 ? go(gate_gemm_kernel<true, 32>, *sel) : go(gate_gemm_kernel<true, 64>, *sel);
+    else
+        e = g.BN <= 16 ? go(gate_gemm_kernel<false, 16>, none)
+            : g.BN <= 32 ? go(gate_gemm_kernel<false, 32>, none) : go(gate_gemm_kernel<false, 64>, none);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

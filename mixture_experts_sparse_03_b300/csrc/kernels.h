@@ -60,14 +60,17 @@ struct GateGemmPlan {
     int per;       // K blocks per split
     int S;         // splits of K
     int Np;        // logits per token (N0 + N1)
+    bool fused;    // selection fused into the GEMM's epilogue (no partials, no selection kernel)
+    int stages;    // TMA ring depth
     size_t smem;   // dynamic shared memory per CTA
 };
-GateGemmPlan gate_gemm_plan(int T, int d, int N0, int N1, int sms);
+GateGemmPlan gate_gemm_plan(int T, int d, int N0, int N1, int sms, bool fuse_select);
 // part [S][T][Np] (S = plan.S) receives the partial logits; xn2_part [S][T] and wn2_part [S][Np]
 // the partial squared norms (either may be nullptr to skip)
+// sel: the selection's parameters (ids, gates, dispatch outputs; cb set) when g.fused, else ignored
 cudaError_t launch_gate_gemm(const GateGemmPlan& g, const void* x, const void* w0, const void* w1, int T, int d,
                              int N0, int N1, float* part, float* xn2_part, float* wn2_part, int* err,
-                             cudaStream_t s);
+                             const GateParams* sel, cudaStream_t s);
 cudaError_t launch_gate(const GateParams& p, cudaStream_t s);
 
 // ---- dispatch ---------------------------------------------------------------------------------

@@ -143,10 +143,14 @@ def test_empty_input_is_a_no_op():
 
 
 def test_launch_counts():
-    # bf16: logits GEMM, gate (+ dispatch scan), dispatch, up, down (+ combine when k > 2 or unfused)
-    assert b.moe_forward_launches(b.config(small_workload(k=2))) == 5
-    assert b.moe_forward_launches(b.config(small_workload(k=3))) == 6
-    assert b.moe_forward_launches(b.config(small_workload(k=2), flags=b.FLAG_UNFUSED_COMBINE)) == 6
+    # bf16 softmax gate with E <= 64: one fused gate launch (logits, top-k, dispatch ranks and scan),
+    # dispatch gather, up, down (+ combine when k > 2 or unfused)
+    assert b.moe_forward_launches(b.config(small_workload(k=2))) == 4
+    assert b.moe_forward_launches(b.config(small_workload(k=3))) == 5
+    assert b.moe_forward_launches(b.config(small_workload(k=2), flags=b.FLAG_UNFUSED_COMBINE)) == 5
+    # other bf16 gates: logits GEMM and selection kernel
+    assert b.moe_forward_launches(b.config(small_workload(k=2, gate="noisy"))) == 5
+    assert b.moe_forward_launches(b.config(small_workload(k=2, E=65))) == 5
     # fp32: the gate computes its logits itself
     assert b.moe_forward_launches(b.config(small_workload(k=2, dtype="f32"))) == 4
     assert b.moe_forward_launches(b.config(small_workload(k=3, dtype="f32"))) == 5
