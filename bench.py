@@ -100,6 +100,24 @@ def layer_work(wl, kept_pairs: int, experts_used: int):
     return gemm, gate, wbytes
 
 
+# ----------------------------------------------------------------------------------- replicas (N > 1)
+def max_over_ranks(value: float, device=None) -> float:
+    """The largest `value` over all ranks of the default process group (the value itself when no group
+    is initialised).  Each rank runs an independent replica of the layer; the slowest one sets the time."""
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, steps: int, tokens: int, max_total_ms: float) -> float:
+    """Whole-job tokens/s: the tokens every rank processed over the slowest rank's summed step time."""
+    return world * steps * tokens / (max_total_ms / 1e3)
+
+
 # ------------------------------------------------------------------------------------------ clocks
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -317,12 +335,8 @@ def run_ours(args, rank, world, local):
         torch.distributed.barrier()
     clocks = sampler.stop()
     times = [a.elapsed_time(z) for a, z in evs]  # ms
-    total_ms = sum(times)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
-    value = world * K * wl.T / (total_ms / 1e3)
+    total_ms = max_over_ranks(sum(times), dev)
+    value = job_throughput(world, K, wl.T, total_ms)
     ms_per_step = total_ms / K
 
     # ---- per-kernel durations (eager, trace events between the library's launches)
@@ -398,11 +412,7 @@ def run_ours(args, rank, world, local):
             e1.record(stream)
             e1.synchronize()
             e_ms += e0.elapsed_time(e1)
-    e2e_value = world * K * wl.T / (e_ms / 1e3)
-    if world > 1:
-        t = torch.tensor([e_ms], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_value = world * K * wl.T / (float(t.item()) / 1e3)
+    e2e_value = job_throughput(world, K, wl.T, max_over_ranks(e_ms, dev))
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
