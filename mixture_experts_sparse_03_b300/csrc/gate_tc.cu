@@ -376,29 +376,58 @@ __global__ void __launch_bounds__(kGThreads, 1)
         float hi[BNC], lo[BNC];
 #pragma unroll
         for (int j = 0; j < BNC; ++j) hi[j] = lo[j] = 0.f;
+        // G = 64 / BNC accumulators per round: their TMEM loads are in flight together, then added
+        constexpr int G = 64 / BNC;
         bool ok = true;
-        for (int i = 0; i < nkb && ok; ++i) {
-            const int buf = i % kGChunks;
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(CFULL + buf), (i / kGChunks) & 1, abort_flag));
+        for (int i0 = 0; i0 < nkb && ok; i0 += G) {
+            const int ng = min(G, nkb - i0);
+            for (int j = 0; j < ng && ok; ++j)
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(CFULL + (i0 + j) % kGChunks), ((i0 + j) / kGChunks) & 1,
+                                                       abort_flag));
             if (!ok) break;
             fence_after();
+            if constexpr (BNC == 64) {  // one accumulator per round, loaded 16 columns at a time
+                const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)((i0 % kGChunks) * a.BN);
 #pragma unroll
-            for (int c0 = 0; c0 < BNC; c0 += 16) {
-                if (c0 < a.BN) {
-                    uint32_t v[16];
-                    tmem_ld16(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * a.BN + c0), v);
+                for (int c0 = 0; c0 < 64; c0 += 16) {
+                    if (c0 < a.BN) {
+                        uint32_t v[16];
+                        tmem_ld16(tb + (uint32_t)c0, v);
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        float s_, e_;
-                        two_sum(hi[c0 + j], __uint_as_float(v[j]), s_, e_);
-                        hi[c0 + j] = s_;
-                        lo[c0 + j] += e_;
+                        for (int c = 0; c < 16; ++c) {
+                            float s_, e_;
+                            two_sum(hi[c0 + c], __uint_as_float(v[c]), s_, e_);
+                            hi[c0 + c] = s_;
+                            lo[c0 + c] += e_;
+                        }
                     }
                 }
+            } else {
+            uint32_t v[G][BNC];
+#pragma unroll
+            for (int j = 0; j < G; ++j)
+#pragma unroll
+                for (int c0 = 0; c0 < BNC; c0 += 16)
+                    if (j < ng && c0 < a.BN)
+                        tmem_ld16_async(tmem_base + ((uint32_t)(q * 32) << 16) +
+                                            (uint32_t)(((i0 + j) % kGChunks) * a.BN + c0),
+                                        *reinterpret_cast<uint32_t(*)[16]>(&v[j][c0]));
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < G; ++j)
+#pragma unroll
+                for (int c = 0; c < BNC; ++c)
+                    if (j < ng && c < a.BN) {  // blocks added in K order
+                        float s_, e_;
+                        two_sum(hi[c], __uint_as_float(v[j][c]), s_, e_);
+                        hi[c] = s_;
+                        lo[c] += e_;
+                    }
             }
             fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(CEMPTY + buf));
+            if (lane == 0)
+                for (int j = 0; j < ng; ++j) mbar_arrive(bar(CEMPTY + (i0 + j) % kGChunks));
         }
         if (!ok) {
             if (lane == 0) {
