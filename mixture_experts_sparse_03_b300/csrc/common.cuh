@@ -110,8 +110,23 @@ __device__ __forceinline__ unsigned lanemask_lt() {
     return m;
 }
 
-// GELU with the exact erf form: z/2 (1 + erf(z / sqrt 2))
-__device__ __forceinline__ float gelu_erf(float z) { return 0.5f * z * (1.0f + erff(z * 0.70710678118654752f)); }
+// GELU with the erf form, z/2 (1 + erf(z / sqrt 2)) (the exact GELU, not the tanh approximation).
+// erf comes from Abramowitz & Stegun, Handbook of Mathematical Functions, formula 7.1.26: for x >= 0,
+// 1 - erf(x) = t (a1 + t (a2 + t (a3 + t (a4 + t a5)))) e^(-x^2), t = 1 / (1 + p x), |error| <= 1.5e-7.
+// With Q = 1 - erf(|z| / sqrt 2), 1 + erf(z / sqrt 2) is 2 - Q for z >= 0 and Q for z < 0, so the
+// negative side keeps its small values without cancellation.  The hidden activations are rounded to
+// bf16 (relative step 2^-8) right after, far above this error.
+__device__ __forceinline__ float gelu_erf(float z) {
+    const float x = fabsf(z) * 0.70710678118654752f;
+    float t;  // 1 / (1 + p x) with the hardware's approximate reciprocal (relative error ~2^-23)
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(t) : "f"(fmaf(0.3275911f, x, 1.0f)));
+    float p = fmaf(t, 1.061405429f, -1.453152027f);
+    p = fmaf(t, p, 1.421413741f);
+    p = fmaf(t, p, -0.284496736f);
+    p = fmaf(t, p, 0.254829592f);
+    const float q = p * t * __expf(-x * x);
+    return 0.5f * z * (z >= 0.0f ? 2.0f - q : q);
+}
 
 // expert owning dispatched row r: the e with off[e] <= r < off[e+1] (off ascending, E+1 entries)
 __device__ __forceinline__ int expert_of_row(const int* off, int E, int r) {

@@ -238,3 +238,31 @@ def test_expert_ffn_on_sm_pairs(wl):
 def test_expert_ffn_single_sm_on_large_experts():
     """The single-SM expert GEMMs, forced on a layer that would use pairs by default."""
     _full_check(small_workload(T=2048, d=128, h=256, E=2, k=2, capacity_factor=1.0), flags=b.FLAG_FFN_ONE_SM)
+
+
+def test_gelu_against_exact_erf():
+    """The expert's GELU (erf via Abramowitz & Stegun 7.1.26 in the GEMM epilogue) against the exact
+    erf GELU: a one-expert layer with x = 0, W1 = 0, b1 = z and W2 = I outputs bf16(GELU(z)) for every
+    token, which must equal the exact value rounded to bf16 within one bf16 step (ties of the
+    rounding), and lie within half a step plus 1e-6 of the exact value."""
+    d = 2048
+    wl = small_workload(T=64, d=d, h=d, E=1, k=1, norm="topk", capacity=64, bias="zero")
+    tc, tg = P.inputs(wl)
+    z = torch.linspace(-9.0, 9.0, d, dtype=torch.float64).to(torch.bfloat16)
+    tg["x"] = torch.zeros_like(tg["x"])
+    tg["w1"] = torch.zeros_like(tg["w1"])
+    tg["b1"] = z.reshape(1, d).cuda()
+    tg["w2"] = torch.eye(d, dtype=torch.bfloat16).reshape(1, d, d).cuda()
+    tg["b2"] = torch.zeros_like(tg["b2"])
+    out, _ = P.run_forward(wl, tg)
+    zz = z.double()
+    exact = (torch.nn.functional.gelu(zz, approximate="none")).numpy()
+    want = torch.from_numpy(exact).to(torch.bfloat16).double().numpy()
+    got = out[0]
+    assert np.all(out == got[None, :])  # every token the same
+    step = np.abs(np.spacing(want.astype(np.float32))) * 2 ** 16  # one bf16 step at each value
+    step = np.maximum(step, 2.0 ** -133)
+    assert np.all(np.abs(got - want) <= step + 1e-6)
+    assert np.all(np.abs(got - exact) <= 0.5 * step + 1e-6)
+    big = np.abs(exact) > 1e-3  # where the value is not lost in the absolute error bound
+    assert np.mean(got[big] == want[big]) > 0.99  # rounds like the exact value almost everywhere
