@@ -15,6 +15,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
                                                       const int* __restrict__ offset, const int* __restrict__ topk_idx,
                                                       const float* __restrict__ topk_gate, int T, int k, int d,
                                                       float* __restrict__ out) {
+    pdl_wait();
+    pdl_trigger();
     const int n4 = d / 4;
     const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= (size_t)T * n4) return;
@@ -51,6 +53,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
 }
 
 __global__ void zero_kernel(float4* __restrict__ p, size_t n4) {
+    pdl_wait();
+    pdl_trigger();
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x)
         p[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
@@ -61,8 +65,8 @@ cudaError_t launch_combine(const float* y, const int* slot, const int* offset, c
                            const float* topk_gate, int T, int k, int d, float* out, cudaStream_t s) {
     if (T <= 0) return cudaSuccess;
     const size_t n = (size_t)T * (d / 4);
-    combine_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(y, slot, offset, topk_idx, topk_gate, T, k, d, out);
-    return cudaGetLastError();
+    return launch_pdl(combine_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s, y, slot, offset, topk_idx,
+                      topk_gate, T, k, d, out);
 }
 
 cudaError_t launch_zero(float* p, size_t n, cudaStream_t s) {
@@ -70,8 +74,7 @@ cudaError_t launch_zero(float* p, size_t n, cudaStream_t s) {
     const size_t n4 = n / 4;  // n is a multiple of 4 (d is a multiple of 64)
     unsigned blocks = (unsigned)((n4 + 255) / 256);
     if (blocks > 148u * 16u) blocks = 148u * 16u;
-    zero_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<float4*>(p), n4);
-    return cudaGetLastError();
+    return launch_pdl(zero_kernel, dim3(blocks), dim3(256), 0, s, reinterpret_cast<float4*>(p), n4);
 }
 
 }  // namespace moe

@@ -17,6 +17,30 @@ enum : int {
     kWhereGemmEpilogue = 6, kWhereCombine = 7, kWhereGateGemm = 8
 };
 
+// ---- programmatic dependent launch ------------------------------------------------------------------
+// Every kernel is launched so that the next one in the stream may start (prologue: barriers, TMEM,
+// descriptor prefetch) while this one finishes.  A kernel calls pdl_wait() before it touches global
+// memory (it returns once the preceding grids have completed and their writes are visible), then
+// pdl_trigger() to let its own successor launch.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 __device__ __forceinline__ void record_error(int* err, int code, int where) {
     if (err != nullptr && atomicCAS(err, 0, code) == 0) atomicExch(err + 1, where);
 }

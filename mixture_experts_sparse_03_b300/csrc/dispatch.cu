@@ -31,6 +31,8 @@ __global__ void __launch_bounds__(256) rank_kernel(const int* __restrict__ topk_
                                                    int* __restrict__ blk_hist, int* __restrict__ rank, int* err) {
     __shared__ int running[kMaxExperts];
     __shared__ int ids[kBT * kMaxTopK];
+    pdl_wait();
+    pdl_trigger();
     const int t0 = blockIdx.x * kBT;
     const int n = min(kBT, T - t0) * k;
     for (int e = threadIdx.x; e < E; e += blockDim.x) running[e] = 0;
@@ -55,6 +57,8 @@ __global__ void __launch_bounds__(1024) scan_kernel(int* __restrict__ blk_hist, 
     __shared__ int padded[kMaxExperts + 1];
     __shared__ int kept[kMaxExperts];
     __shared__ int wsum[33];
+    pdl_wait();
+    pdl_trigger();
     ScanSmem sm{part, padded, kept, wsum};
     scan_experts(blk_hist, nblk, E, C, count, offset, row_token, row_gate, sm);
 }
@@ -65,6 +69,8 @@ __global__ void __launch_bounds__(32 * kGatherWarps) gather_kernel(
     const int* __restrict__ blk_base, const int* __restrict__ offset, int T_, int k, int E, int d, int C,
     int* __restrict__ slot, int* __restrict__ row_token, float* __restrict__ row_gate, T* __restrict__ xd,
     float* __restrict__ out_zero) {
+    pdl_wait();
+    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const long npairs = (long)T_ * k;
     const long p = (long)blockIdx.x * kGatherWarps + (threadIdx.x >> 5);
@@ -115,8 +121,7 @@ __global__ void __launch_bounds__(32 * kGatherWarps) gather_kernel(
 cudaError_t launch_dispatch_rank(const int* topk_idx, int T, int k, int E, int* blk_hist, int* rank, int* err,
                                  cudaStream_t s) {
     if (T <= 0) return cudaSuccess;
-    rank_kernel<<<(T + kBT - 1) / kBT, 256, 0, s>>>(topk_idx, T, k, E, blk_hist, rank, err);
-    return cudaGetLastError();
+    return launch_pdl(rank_kernel, dim3((T + kBT - 1) / kBT), dim3(256), 0, s, topk_idx, T, k, E, blk_hist, rank, err);
 }
 
 cudaError_t launch_dispatch_scan(int* blk_hist, int T, int k, int E, int C, int* count, int* offset,
@@ -124,8 +129,7 @@ cudaError_t launch_dispatch_scan(int* blk_hist, int T, int k, int E, int C, int*
     (void)k;
     if (T <= 0) return cudaSuccess;
     const int nblk = (T + kBT - 1) / kBT;
-    scan_kernel<<<1, 1024, 0, s>>>(blk_hist, nblk, E, C, count, offset, row_token, row_gate);
-    return cudaGetLastError();
+    return launch_pdl(scan_kernel, dim3(1), dim3(1024), 0, s, blk_hist, nblk, E, C, count, offset, row_token, row_gate);
 }
 
 cudaError_t launch_dispatch_gather(const void* x, int bf16, const int* topk_idx, const float* topk_gate,
@@ -136,14 +140,12 @@ cudaError_t launch_dispatch_gather(const void* x, int bf16, const int* topk_idx,
     const long npairs = (long)T * k;
     const unsigned blocks = (unsigned)((npairs + kGatherWarps - 1) / kGatherWarps);
     if (bf16)
-        gather_kernel<bf16_t><<<blocks, 32 * kGatherWarps, 0, s>>>(
-            static_cast<const bf16_t*>(x), topk_idx, topk_gate, blk_base, offset, T, k, E, d, C, slot, row_token,
-            row_gate, static_cast<bf16_t*>(x_dispatched), out_to_zero);
-    else
-        gather_kernel<float><<<blocks, 32 * kGatherWarps, 0, s>>>(
-            static_cast<const float*>(x), topk_idx, topk_gate, blk_base, offset, T, k, E, d, C, slot, row_token,
-            row_gate, static_cast<float*>(x_dispatched), out_to_zero);
-    return cudaGetLastError();
+        return launch_pdl(gather_kernel<bf16_t>, dim3(blocks), dim3(32 * kGatherWarps), 0, s,
+                          static_cast<const bf16_t*>(x), topk_idx, topk_gate, blk_base, offset, T, k, E, d, C, slot,
+                          row_token, row_gate, static_cast<bf16_t*>(x_dispatched), out_to_zero);
+    return launch_pdl(gather_kernel<float>, dim3(blocks), dim3(32 * kGatherWarps), 0, s,
+                      static_cast<const float*>(x), topk_idx, topk_gate, blk_base, offset, T, k, E, d, C, slot,
+                      row_token, row_gate, static_cast<float*>(x_dispatched), out_to_zero);
 }
 
 }  // namespace moe

@@ -21,6 +21,8 @@ template <typename T>
 __global__ void __launch_bounds__(256) ffn_simt_kernel(const FfnParams P) {
     __shared__ __align__(16) float As[kKC * kSS];
     __shared__ __align__(16) float Bs[kKC * kSS];
+    pdl_wait();
+    pdl_trigger();
     const int tid = threadIdx.x;
     const int r0 = blockIdx.x * kTile;
     const int total = P.offset[P.E];
@@ -90,8 +92,9 @@ __global__ void __launch_bounds__(256) ffn_simt_kernel(const FfnParams P) {
 cudaError_t launch_ffn_simt(const FfnParams& P, cudaStream_t s) {
     if (P.rows_cap <= 0) return cudaSuccess;
     dim3 grid((unsigned)((P.rows_cap + kTile - 1) / kTile), (unsigned)((P.N + kTile - 1) / kTile));
-    if (P.bf16) ffn_simt_kernel<bf16_t><<<grid, 256, 0, s>>>(P);
-    else ffn_simt_kernel<float><<<grid, 256, 0, s>>>(P);
+    cudaError_t e = P.bf16 ? launch_pdl(ffn_simt_kernel<bf16_t>, grid, dim3(256), 0, s, P)
+                           : launch_pdl(ffn_simt_kernel<float>, grid, dim3(256), 0, s, P);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

@@ -115,8 +115,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto bar = [&](int i) { return smem_u32(bars + i); };
     const int FULL = 0, EMPTY = kStages, TFULL = 2 * kStages, TEMPTY = 2 * kStages + 2, LAST = 2 * kStages + 4;
 
-    for (int i = threadIdx.x; i <= a.E; i += kThreads) s_off[i] = a.offset[i];
     if (threadIdx.x == 0) {
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
         *abort_flag = 0;
         for (int s = 0; s < kStages; ++s) {
             mbar_init(bar(FULL + s), 1);
@@ -132,6 +133,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_holder), kTmemCols);
     }
+    pdl_wait();  // the set-up above overlaps the previous kernel; its outputs are read from here on
+    pdl_trigger();
+    for (int i = threadIdx.x; i <= a.E; i += kThreads) s_off[i] = a.offset[i];
     fence_before();
     __syncthreads();
     fence_after();
@@ -292,7 +296,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     auto bar = [&](int i) { return smem_u32(bars + i); };
     const int FULL = 0, EMPTY = k2Stages, TFULL = 2 * k2Stages, TEMPTY = 2 * k2Stages + 2, LAST = 2 * k2Stages + 4;
 
-    for (int i = threadIdx.x; i <= a.E; i += kThreads) s_off[i] = a.offset[i];
     if (threadIdx.x == 0) {
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmB);
@@ -308,6 +311,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         mbar_init(bar(LAST), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    pdl_wait();  // the set-up above overlaps the previous kernel; its outputs are read from here on
+    pdl_trigger();
+    for (int i = threadIdx.x; i <= a.E; i += kThreads) s_off[i] = a.offset[i];
     __syncthreads();
     if (threadIdx.x == 0) {  // tiles per expert: its rows (a multiple of 128) in blocks of 256
         int acc = 0;
@@ -566,8 +572,7 @@ cudaError_t launch_ffn_tc(const FfnParams& P, cudaStream_t s) {
         const int64_t max_tiles = (P.rows_cap / kBM + P.E) / 2 * (int64_t)((P.N + kBN - 1) / kBN) + 1;
         int pairs = pair_clusters(smem2);
         if (max_tiles < pairs) pairs = (int)max_tiles;
-        gemm_tc_pair_kernel<<<2 * pairs, kThreads, smem2, s>>>(ma, mb2, a);
-        return cudaGetLastError();
+            return launch_pdl(gemm_tc_pair_kernel, dim3(2 * pairs), dim3(kThreads), smem2, s, ma, mb2, a);
     }
     const size_t smem = ffn_tc_smem_bytes(P.E);
     cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -575,8 +580,7 @@ cudaError_t launch_ffn_tc(const FfnParams& P, cudaStream_t s) {
     const int64_t max_tiles = (P.rows_cap / kBM) * (int64_t)((P.N + kBN - 1) / kBN);
     int grid = device_sm_count();
     if (max_tiles < grid) grid = (int)(max_tiles > 0 ? max_tiles : 1);
-    gemm_tc_kernel<<<grid, kThreads, smem, s>>>(ma, mb, a);
-    return cudaGetLastError();
+    return launch_pdl(gemm_tc_kernel, dim3(grid), dim3(kThreads), smem, s, ma, mb, a);
 }
 
 }  // namespace moe

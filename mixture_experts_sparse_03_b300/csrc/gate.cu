@@ -99,6 +99,8 @@ constexpr int kPh1Tiled = 0, kPh1Small = 1;
 
 template <typename T, int GATE, int TM, int TN, int TX, int PH1>
 __global__ void __launch_bounds__(PH1 == kPh1Small ? 512 : 256) gate_kernel(const GateParams P, const int stage) {
+    pdl_wait();
+    pdl_trigger();
     constexpr bool SMALL = PH1 == kPh1Small;
     constexpr int NT = SMALL ? 512 : 256;
     constexpr int NW = NT / 32;
@@ -567,8 +569,7 @@ cudaError_t launch_cfg(const GateParams& P, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L0.total);
     if (e != cudaSuccess) return e;
     const int blocks = (P.T + kBT - 1) / kBT;
-    kern<<<blocks, NT, L0.total, s>>>(P, stage);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(blocks), dim3(NT), L0.total, s, P, stage);
 }
 
 template <typename T, int GATE>

@@ -70,6 +70,8 @@ __host__ __device__ inline SelLayout sel_layout(int gate, int E, int p, int stag
 
 template <typename T, int GATE>
 __global__ void __launch_bounds__(kSelThreads) gate_select_kernel(const GateParams P, const int stage) {
+    pdl_wait();
+    pdl_trigger();
     extern __shared__ __align__(16) unsigned char smem[];
     const SelLayout L = sel_layout(GATE, P.E, P.p, stage);
     float* logits = reinterpret_cast<float*>(smem + L.logits);
@@ -401,8 +403,7 @@ cudaError_t launch_sel(const GateParams& P, cudaStream_t s) {
     auto kern = gate_select_kernel<T, GATE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.total);
     if (e != cudaSuccess) return e;
-    kern<<<(P.T + kBT - 1) / kBT, kSelThreads, L.total, s>>>(P, stage);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3((P.T + kBT - 1) / kBT), dim3(kSelThreads), L.total, s, P, stage);
 }
 
 }  // namespace

@@ -277,6 +277,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
     __syncthreads();
     fence_after();
     const uint32_t tmem_base = *tmem_holder;
+    pdl_wait();  // the set-up above overlaps the previous kernel; its outputs are read below
+    pdl_trigger();
 
     if (warp == 0) {
         if (lane == 0) {
@@ -537,8 +539,7 @@ cudaError_t launch_gate_gemm(const GateGemmPlan& g, const void* x, const void* w
     auto go = [&](auto kern, const GateParams& p) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)g.smem);
         if (e != cudaSuccess) return e;
-        kern<<<grid, kGThreads, g.smem, s>>>(ma, mb0, mb1, a, p);
-        return cudaSuccess;
+        return launch_pdl(kern, grid, dim3(kGThreads), g.smem, s, ma, mb0, mb1, a, p);
     };
     cudaError_t e;
     if (g.fused)
