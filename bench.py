@@ -45,7 +45,8 @@ def kernel_names(wl, launches: int):
     if wl.dtype == "bf16" and wl.gate == "softmax" and wl.E <= 64:
         names = ["gate_fused_gemm_topk_scan", "dispatch_gather", "expert_up_gelu"]
     elif wl.dtype == "bf16":
-        names = ["gate_logits_gemm", "gate_topk_scan", "dispatch_gather", "expert_up_gelu"]
+        names = ["gate_logits_gemm", "gate_topk"] + (["gate_cos_fold"] if wl.gate == "cosine" else [])
+        names += ["gate_rescore", "dispatch_rank_scan", "dispatch_gather", "expert_up_gelu"]
     else:
         names = ["gate_topk_scan", "dispatch_gather", "expert_up_gelu"]
     names += ["expert_down_combine"] if wl.k <= 2 else ["expert_down", "combine_gather"]
@@ -360,22 +361,35 @@ def run_ours(args, rank, world, local):
                 per[n].append(tev[j].elapsed_time(tev[j + 1]))
             del keep
     kern_ms = {n: statistics.median(v) for n, v in per.items()}
-    dominant = max(kern_ms, key=kern_ms.get)
+    # the dominant kernel is the one whose launches take the most time in a step; the expert GEMM kernel
+    # runs twice (up-projection with GELU, down-projection), with equal work per launch
+    gemm_names = [n for n in names if n.startswith("expert_")]
+    gemm_launch_ms = sum(kern_ms[n] for n in gemm_names) / len(gemm_names)
+    rest = {n: v for n, v in kern_ms.items() if n not in gemm_names}
+    top_rest = max(rest, key=rest.get)
+    gemm_dominant = sum(kern_ms[n] for n in gemm_names) >= rest[top_rest]
     pk = peaks()
     hbm_bound = kept < RIDGE_ROWS * max(used, 1)  # few rows per expert: the weights' bytes bound the FFN
-    if dominant.startswith("expert_") and hbm_bound:
+    if gemm_dominant and hbm_bound:
         # one expert GEMM streams one of the two weight matrices of every used expert
-        achieved = (wbytes / 2) / (kern_ms[dominant] * 1e-3) / 1e9
+        achieved = (wbytes / 2) / (gemm_launch_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s",
                 "frac": achieved / pk["hbm"]}
-    elif dominant.startswith("expert_"):
-        achieved = gemm_flops / (kern_ms[dominant] * 1e-3) / 1e12
+    elif gemm_dominant:
+        achieved = gemm_flops / (gemm_launch_ms * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": pk["bf16"], "unit": "TFLOP/s",
                 "frac": achieved / pk["bf16"]}
     else:
         roof = {"bound": "hbm", "achieved": None, "peak": pk["hbm"], "unit": "GB/s", "frac": None}
-    roof.update({"traffic": recorded_traffic(dominant, wl.name), "kernel": dominant,
-                 "peak_source": pk["source"] + " (burst)", "kernel_ms": kern_ms[dominant],
+    if gemm_dominant:
+        dominant = "expert_gemm (%s)" % " + ".join(gemm_names)
+        tr = [recorded_traffic(n, wl.name) for n in gemm_names]
+        traffic = sum(tr) / len(tr) if all(v is not None for v in tr) else None
+        dom_ms = gemm_launch_ms
+    else:
+        dominant, traffic, dom_ms = top_rest, recorded_traffic(top_rest, wl.name), rest[top_rest]
+    roof.update({"traffic": traffic, "kernel": dominant,
+                 "peak_source": pk["source"] + " (burst)", "kernel_ms": dom_ms,
                  "layer_tflops": (2 * gemm_flops + gate_flops) / (ms_per_step * 1e-3) / 1e12,
                  "layer_weight_gbs": wbytes / (ms_per_step * 1e-3) / 1e9})
     if wl.dtype != "bf16":

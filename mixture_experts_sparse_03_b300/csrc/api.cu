@@ -27,7 +27,8 @@ struct Plan {
     GateGemmPlan gg;    // tensor-core logits GEMM (bf16 layers)
     int64_t rows;
     size_t o_err, o_idx, o_gate, o_slot, o_hist, o_count, o_off, o_rtok, o_rgate, o_xd, o_h, o_y, o_part, o_xn2,
-        o_wn2, total;
+        o_wn2, o_rq, o_cosv, total;
+    size_t hdr_bytes;  // error word, its info, tickets and the cosine gate's expert flags: zeroed per call
 };
 
 // Bound on the error of the tensor-core logits: |logit - exact| <= kTcErr * 2^-23 * sum_i |x_i w_i|.
@@ -98,7 +99,9 @@ moe_status make_plan(const moe_config* c, Plan* pl) {
     size_t o = 0;
     auto take = [&](size_t bytes) { size_t r = o; o = up(o + bytes); return r; };
     const size_t tk = (size_t)P.T * P.k;
-    P.o_err = take(16);
+    const bool cos_tc = P.bf16 && P.gate == MOE_GATE_COSINE;  // cosine gates never take the fused path
+    P.hdr_bytes = 16 + (cos_tc ? 4 * (size_t)P.E : 0);
+    P.o_err = take(P.hdr_bytes);
     P.o_idx = take(4 * tk);
     P.o_gate = take(4 * tk);
     P.o_slot = take(4 * tk);
@@ -114,6 +117,8 @@ moe_status make_plan(const moe_config* c, Plan* pl) {
     P.o_part = take(P.bf16 ? 4 * (size_t)P.gg.S * P.T * np : 0);
     P.o_xn2 = take(P.bf16 ? 4 * (size_t)P.gg.S * P.T : 0);
     P.o_wn2 = take(P.bf16 ? 4 * (size_t)P.gg.S * np : 0);
+    P.o_rq = take(P.bf16 && !P.gg.fused ? 4 * (size_t)P.T * kRescoreInts : 0);
+    P.o_cosv = take(cos_tc ? 8 * (size_t)P.E * P.d : 0);
     P.total = o;
     *pl = P;
     return MOE_OK;
@@ -220,13 +225,33 @@ moe_status gate_logits_tc(const Plan& P, GateParams& g, void* ws, cudaStream_t s
     });
 }
 
-// the whole gate: the logits GEMM (bf16 layers) and the selection, or both fused into one launch
+// the whole gate (and, with g.blk_hist set, the dispatch's rank step and scan):
+//   bf16, softmax, E <= 64: one fused launch;
+//   other bf16 gates: logits GEMM, selection (tokens with near ties queued), for the cosine gate the fold
+//   v_e = P^T e_e of the contending experts, grid-wide re-scoring of the queue, then the rank step with
+//   the scan in its last block;
+//   fp32: the CUDA-core gate kernel, which does all of it
 moe_status run_gate(const Plan& P, GateParams& g, void* ws, cudaStream_t s) {
-    if (P.bf16) {
-        MOE_TRY(gate_logits_tc(P, g, ws, s));
-        if (P.gg.fused) return MOE_OK;
+    if (!P.bf16) return launch(s, [&] { return launch_gate(g, s); });
+    MOE_TRY(gate_logits_tc(P, g, ws, s));
+    if (P.gg.fused) return MOE_OK;
+    GateParams sel = g;
+    sel.blk_hist = nullptr;
+    sel.ticket = nullptr;
+    sel.rq_count = at<int>(ws, P.o_err) + 3;  // zeroed with the error word
+    sel.rq = at<int>(ws, P.o_rq);
+    if (P.gate == MOE_GATE_COSINE) {
+        sel.need = at<int>(ws, P.o_err) + 4;  // zeroed with the error word
+        sel.cosv = at<float2>(ws, P.o_cosv);
     }
-    return launch(s, [&] { return launch_gate(g, s); });
+    MOE_TRY(launch(s, [&] { return launch_gate(sel, s); }));
+    if (P.gate == MOE_GATE_COSINE) MOE_TRY(launch(s, [&] { return launch_gate_cos_fold(sel, s); }));
+    MOE_TRY(launch(s, [&] { return launch_gate_rescore(sel, s); }));
+    if (g.blk_hist == nullptr) return MOE_OK;
+    return launch(s, [&] {
+        return launch_dispatch_rank(g.topk_idx, P.T, P.k, P.E, g.blk_hist, g.slot, g.err, g.ticket, g.C, g.count,
+                                    g.offset, g.row_token, g.row_gate, s);
+    });
 }
 
 FfnParams ffn_params(const Plan& P, int mode, const void* A, const void* W, const void* bias, const int* off,
@@ -290,7 +315,8 @@ int32_t moe_forward_launches(const moe_config* cfg) {
     Plan P;
     if (make_plan(cfg, &P) != MOE_OK) return -1;
     if (P.T == 0) return 0;
-    return (P.fused ? 4 : 5) + (P.bf16 && !P.gg.fused ? 1 : 0);
+    const int gate_extra = P.bf16 && !P.gg.fused ? 3 + (P.gate == MOE_GATE_COSINE ? 1 : 0) : 0;
+    return (P.fused ? 4 : 5) + gate_extra;
 }
 
 moe_status moe_route(const moe_config* cfg, const void* x, const void* w_gate, const void* w_noise,
@@ -303,7 +329,7 @@ moe_status moe_route(const moe_config* cfg, const void* x, const void* w_gate, c
     MOE_TRY(check_route_args(P, x, w_gate, w_noise, noise_eps, proj, expert_emb, topk_idx, topk_gate));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     int* err = at<int>(workspace, P.o_err);
-    if (cudaMemsetAsync(err, 0, 8, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaMemsetAsync(err, 0, P.hdr_bytes, s) != cudaSuccess) return MOE_ERR_CUDA;
     GateParams g = gate_params(P, cfg, x, w_gate, w_noise, noise_eps, proj, expert_emb, topk_idx, topk_gate);
     g.err = err;
     return run_gate(P, g, workspace, s);
@@ -342,10 +368,11 @@ moe_status moe_dispatch(const moe_config* cfg, const void* x, const int32_t* top
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     int* err = at<int>(workspace, P.o_err);
     int* hist = at<int>(workspace, P.o_hist);
-    if (cudaMemsetAsync(err, 0, 8, s) != cudaSuccess) return MOE_ERR_CUDA;
-    MOE_TRY(launch(s, [&] { return launch_dispatch_rank(topk_idx, P.T, P.k, P.E, hist, slot, err, s); }));
+    // error word, its info and the rank step's CTA ticket start at zero
+    if (cudaMemsetAsync(err, 0, 16, s) != cudaSuccess) return MOE_ERR_CUDA;
     MOE_TRY(launch(s, [&] {
-        return launch_dispatch_scan(hist, P.T, P.k, P.E, P.Ceff, expert_count, expert_offset, row_token, row_gate, s);
+        return launch_dispatch_rank(topk_idx, P.T, P.k, P.E, hist, slot, err, err + 2, P.Ceff, expert_count,
+                                    expert_offset, row_token, row_gate, s);
     }));
     return launch(s, [&] {
         return launch_dispatch_gather(x, P.bf16, topk_idx, topk_gate, hist, expert_offset, P.T, P.k, P.E, P.d, P.Ceff,
@@ -413,8 +440,8 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const void* w_gate,
     float* rgate = at<float>(workspace, P.o_rgate);
     void* xd = at<void>(workspace, P.o_xd);
     float* y = at<float>(workspace, P.o_y);
-    // error word, its info and the gate's block ticket start at zero
-    if (cudaMemsetAsync(err, 0, 16, s) != cudaSuccess) return MOE_ERR_CUDA;
+    // error word, its info, the block tickets and the cosine gate's expert flags start at zero
+    if (cudaMemsetAsync(err, 0, P.hdr_bytes, s) != cudaSuccess) return MOE_ERR_CUDA;
     GateParams g = gate_params(P, cfg, x, w_gate, w_noise, noise_eps, proj, expert_emb, idx, gate);
     g.blk_hist = hist;
     g.slot = slot;

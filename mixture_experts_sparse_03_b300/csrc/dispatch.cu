@@ -6,10 +6,11 @@
 // acceleration", section 3.2), with overflow pairs dropped.
 // Slot of pair (t, e) = number of pairs of earlier tokens routed to e; kept iff slot < C.
 //
-// Three steps over blocks of 32 tokens (the gate kernels' blocks: within moe_forward the gate kernel
-// does step 1 on its own tokens and its last block runs step 2, see scan.cuh):
-//   rank    per block: each pair's rank among the block's pairs of the same expert, in token order
-//           (kept in `slot` until the gather), and the block's expert histogram blk_hist[b][e]
+// Three steps over blocks of 32 tokens (the gate kernels' blocks: the fp32 gate kernel and the fused
+// bf16 gate do step 1 on their own tokens and run step 2 in their last block, see scan.cuh):
+//   rank    a warp per block, 32 blocks per CTA: each pair's rank among the block's pairs of the same
+//           expert, in token order (kept in `slot` until the gather), and the block's expert histogram
+//           blk_hist[b][e]; the last CTA to finish runs the scan
 //   scan    per expert: exclusive prefix over blocks (in place), total count, kept = min(count, C),
 //           padded segment offsets off[e] = sum_{e'<e} roundup(kept[e'], 128), padding rows marked
 //   gather  one warp per pair: slot = prefix[b][e] + rank, kept iff slot < C, row = off[e] + slot;
@@ -26,41 +27,56 @@ namespace {
 
 constexpr int kBT = kTokensPerBlock;
 constexpr int kGatherWarps = 8;  // warps (pairs) per gather block
+constexpr int kRankWarps = 32;   // token blocks per rank CTA, a warp each
 
-__global__ void __launch_bounds__(256) rank_kernel(const int* __restrict__ topk_idx, int T, int k, int E,
-                                                   int* __restrict__ blk_hist, int* __restrict__ rank, int* err) {
-    __shared__ int running[kMaxExperts];
-    __shared__ int ids[kBT * kMaxTopK];
-    pdl_wait();
-    pdl_trigger();
-    const int t0 = blockIdx.x * kBT;
-    const int n = min(kBT, T - t0) * k;
-    for (int e = threadIdx.x; e < E; e += blockDim.x) running[e] = 0;
-    for (int i = threadIdx.x; i < n; i += blockDim.x) {
-        const int e = topk_idx[(size_t)t0 * k + i];
-        const bool ok = e >= 0 && e < E;
-        if (!ok) record_error(err, kErrCheck, kWhereDispatch);
-        ids[i] = ok ? e : -2;  // an out-of-range id takes no slot
-    }
-    __syncthreads();
-    if (threadIdx.x < 32)
-        rank_pairs_warp([&](int i) { return ids[i]; }, n, running, rank + (size_t)t0 * k, threadIdx.x);
-    __syncthreads();
-    for (int e = threadIdx.x; e < E; e += blockDim.x) blk_hist[(size_t)blockIdx.x * E + e] = running[e];
-}
-
-// one block of 1024 threads
-__global__ void __launch_bounds__(1024) scan_kernel(int* __restrict__ blk_hist, int nblk, int E, int C,
-                                                    int* __restrict__ count, int* __restrict__ offset,
-                                                    int* __restrict__ row_token, float* __restrict__ row_gate) {
-    __shared__ int part[1024];
+__global__ void __launch_bounds__(32 * kRankWarps) rank_kernel(const int* __restrict__ topk_idx, int T, int k,
+                                                              int E, int* __restrict__ blk_hist,
+                                                              int* __restrict__ rank, int* err, int* ticket, int C,
+                                                              int* count, int* offset, int* row_token,
+                                                              float* row_gate) {
+    extern __shared__ int running_all[];  // [kRankWarps][E]
+    __shared__ int part[32 * kRankWarps];
     __shared__ int padded[kMaxExperts + 1];
     __shared__ int kept[kMaxExperts];
     __shared__ int wsum[33];
+    __shared__ int last;
     pdl_wait();
     pdl_trigger();
-    ScanSmem sm{part, padded, kept, wsum};
-    scan_experts(blk_hist, nblk, E, C, count, offset, row_token, row_gate, sm);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nblk = (T + kBT - 1) / kBT;
+    const int b = blockIdx.x * kRankWarps + warp;
+    if (b < nblk) {
+        int* running = running_all + (size_t)warp * E;
+        for (int e = lane; e < E; e += 32) running[e] = 0;
+        __syncwarp();
+        const int t0 = b * kBT;
+        const int* ids = topk_idx + (size_t)t0 * k;
+        bool bad = false;
+        rank_pairs_warp(
+            [&](int i) {
+                const int e = ids[i];
+                const bool ok = e >= 0 && e < E;
+                bad |= !ok;
+                return ok ? e : -2;  // an out-of-range id takes no slot
+            },
+            min(kBT, T - t0) * k, running, rank + (size_t)t0 * k, lane);
+        if (bad) record_error(err, kErrCheck, kWhereDispatch);
+        __syncwarp();
+        for (int e = lane; e < E; e += 32) blk_hist[(size_t)b * E + e] = running[e];
+    }
+    // the last CTA to finish runs the scan over every block's histogram
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        last = atomicAdd(ticket, 1) == (int)gridDim.x - 1;
+        __threadfence();
+    }
+    __syncthreads();
+    if (last) {
+        ScanSmem sm{part, padded, kept, wsum};
+        scan_experts(blk_hist, nblk, E, C, count, offset, row_token, row_gate, sm);
+        if (threadIdx.x == 0) *ticket = 0;  // ready for the next call
+    }
 }
 
 template <typename T>
@@ -119,17 +135,17 @@ __global__ void __launch_bounds__(32 * kGatherWarps) gather_kernel(
 }  // namespace
 
 cudaError_t launch_dispatch_rank(const int* topk_idx, int T, int k, int E, int* blk_hist, int* rank, int* err,
+                                 int* ticket, int C, int* count, int* offset, int* row_token, float* row_gate,
                                  cudaStream_t s) {
     if (T <= 0) return cudaSuccess;
-    return launch_pdl(rank_kernel, dim3((T + kBT - 1) / kBT), dim3(256), 0, s, topk_idx, T, k, E, blk_hist, rank, err);
-}
-
-cudaError_t launch_dispatch_scan(int* blk_hist, int T, int k, int E, int C, int* count, int* offset,
-                                 int* row_token, float* row_gate, cudaStream_t s) {
-    (void)k;
-    if (T <= 0) return cudaSuccess;
     const int nblk = (T + kBT - 1) / kBT;
-    return launch_pdl(scan_kernel, dim3(1), dim3(1024), 0, s, blk_hist, nblk, E, C, count, offset, row_token, row_gate);
+    const size_t smem = sizeof(int) * (size_t)kRankWarps * E;
+    if (smem > 48 * 1024) {
+        const cudaError_t e = cudaFuncSetAttribute(rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    return launch_pdl(rank_kernel, dim3((nblk + kRankWarps - 1) / kRankWarps), dim3(32 * kRankWarps), smem, s,
+                      topk_idx, T, k, E, blk_hist, rank, err, ticket, C, count, offset, row_token, row_gate);
 }
 
 cudaError_t launch_dispatch_gather(const void* x, int bf16, const int* topk_idx, const float* topk_gate,

@@ -77,10 +77,11 @@ moe_status moe_dispatch_static_scratch(const moe_config* cfg, const void* x, con
     const int Ceff = C < T ? C : T;
     const int bf16 = cfg->dtype == MOE_BF16;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // the error word must start at zero; the histogram is written in full before it is read
-    if (cudaMemsetAsync(err, 0, 8, s) != cudaSuccess) return MOE_ERR_CUDA;
-    if (launch_dispatch_rank(topk_idx, T, k, E, hist, slot, err, s) != cudaSuccess) return MOE_ERR_CUDA;
-    if (launch_dispatch_scan(hist, T, k, E, Ceff, expert_count, expert_offset, row_token, row_gate, s) != cudaSuccess)
+    // the error word and the rank step's CTA ticket must start at zero; the histogram is written in full
+    // before it is read
+    if (cudaMemsetAsync(err, 0, 16, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_dispatch_rank(topk_idx, T, k, E, hist, slot, err, err + 2, Ceff, expert_count, expert_offset,
+                             row_token, row_gate, s) != cudaSuccess)
         return MOE_ERR_CUDA;
     if (launch_dispatch_gather(x, bf16, topk_idx, topk_gate, hist, expert_offset, T, k, E, d, Ceff, slot, row_token,
                                row_gate, x_dispatched, nullptr, s) != cudaSuccess)

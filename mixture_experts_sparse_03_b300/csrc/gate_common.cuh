@@ -7,7 +7,7 @@
 namespace moe {
 namespace gate {
 
-constexpr int kMaxCand = 64;                   // contenders re-scored per token
+constexpr int kMaxCand = kMaxCandidates;       // contenders re-scored per token
 constexpr float kU = 5.9604644775390625e-08f;  // 2^-24
 constexpr int kGateSoftmax = 0, kGateNoisy = 1, kGateCosine = 2;
 

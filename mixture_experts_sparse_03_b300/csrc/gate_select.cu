@@ -1,17 +1,22 @@
 // gate_select.cu -- scores, per-token top-k and gate weights from the tensor-core logits (bf16 layers).
 //
 // The logits come from gate_tc.cu as fp32 partial sums over splits of d, with the squared norms of the
-// x rows and weight rows.  One warp per token, 32 tokens (one dispatch block) per CTA:
-//   1. the warp sums its token's partials in split order, forms the scores -- softmax gate: the logit;
-//      noisy gate: clean + eps * softplus(noise) (NoisyTopKGating, "MoE sparse-compute acceleration",
-//      section 2.1); cosine gate: cos(u, e_j) / temperature with u = x P^T (Tutel's cosine_top) -- and
-//      a bound on each score's error from the tensor-core accumulation bound cb |x| |w|;
-//   2. picks the top-(k+1) by warp-shuffle argmax (ties -> lower expert id);
-//   3. if two of them lie within twice the bound, queues the token; the CTA then re-scores each queued
-//      token's contenders with float-float dot products (about 48 bits), a warp per contender (the
-//      cosine gate first recomputes all of u, a warp per component), and picks by those scores;
-//   4. writes ids and gate weights (softmax over the k chosen scores, or the full softmax for top-1
-//      layers), the CTA's expert histogram, and the last CTA to finish runs the dispatch scan.
+// x rows and weight rows.  Three kernels:
+//   select   one warp per token, 32 tokens per CTA: sums the token's partials in split order and forms
+//            the scores -- softmax gate: the logit; noisy gate: clean + eps * softplus(noise)
+//            (NoisyTopKGating, "MoE sparse-compute acceleration", section 2.1); cosine gate:
+//            cos(u, e_j) / temperature with u = x P^T (Tutel's cosine_top) -- with a bound on each
+//            score's error from the tensor-core accumulation bound cb |x| |w|, and picks the top-(k+1)
+//            by warp-shuffle argmax (ties -> lower expert id).  If two of them lie within twice the
+//            bound, the token goes to a global queue with its contenders (every expert within twice the
+//            bound of the k-th best); otherwise it gets its ids and gate weights here.
+//   fold     cosine gate only: v_e = P^T e_e in float-float for every expert that contends somewhere.
+//            u . e_e = x . v_e, and |u| and the temperature are common to all experts, so x . v_e / |e_e|
+//            orders the experts exactly as cos(u, e_e) / temperature does.
+//   rescore  every SM works through the queue, a token per CTA and a warp per contender: float-float
+//            dot products (about 48 bits) give the contenders' scores, and the k best of those win.
+// The gate weights always come from the fp32 scores (softmax over the k chosen, or over all E for top-1
+// layers); the re-scoring only decides which experts are chosen.
 #include <float.h>
 #include <math.h>
 
@@ -19,6 +24,7 @@
 #include "gate_common.cuh"
 #include "kernels.h"
 #include "scan.cuh"
+#include "tc_ptx.cuh"
 
 namespace moe {
 
@@ -31,8 +37,7 @@ constexpr int kSelThreads = 32 * kBT;
 constexpr int kSel = kMaxTopK + 1;
 
 struct SelLayout {
-    size_t logits, sc, wn2, embs, embn, selv, seli, cand, candn, exs, fidx, hist, queue, nq, uex, cm, cden,
-        scan_part, scan_padded, scan_kept, scan_wsum, total;
+    size_t logits, sc, wn2, embs, embn, selv, seli, cand, total;
 };
 
 __host__ __device__ inline size_t al16(size_t v) { return (v + 15) / 16 * 16; }
@@ -51,19 +56,6 @@ __host__ __device__ inline SelLayout sel_layout(int gate, int E, int p, int stag
     L.selv = take(4 * kBT * kSel, 16);
     L.seli = take(4 * kBT * kSel, 16);
     L.cand = take(4 * kBT * kMaxCand, 16);
-    L.candn = take(4 * kBT, 16);
-    L.exs = take(8 * kBT * kMaxCand, 16);
-    L.fidx = take(4 * kBT * kMaxTopK, 16);
-    L.hist = take(4 * (size_t)E, 16);
-    L.queue = take(4 * kBT, 16);
-    L.nq = take(16, 16);
-    L.uex = take(cos ? 8 * (size_t)p : 0, 16);
-    L.cm = take(4 * kBT, 16);
-    L.cden = take(4 * kBT, 16);
-    L.scan_part = take(4 * kSelThreads, 16);
-    L.scan_padded = take(4 * (size_t)(E + 1), 16);
-    L.scan_kept = take(4 * (size_t)E, 16);
-    L.scan_wsum = take(4 * 33, 16);
     L.total = al16(o);
     return L;
 }
@@ -82,24 +74,13 @@ __global__ void __launch_bounds__(kSelThreads) gate_select_kernel(const GatePara
     float* selv_all = reinterpret_cast<float*>(smem + L.selv);
     int* seli_all = reinterpret_cast<int*>(smem + L.seli);
     int* cand_all = reinterpret_cast<int*>(smem + L.cand);
-    int* candn = reinterpret_cast<int*>(smem + L.candn);
-    double* exs_all = reinterpret_cast<double*>(smem + L.exs);
-    int* fidx = reinterpret_cast<int*>(smem + L.fidx);
-    int* hist = reinterpret_cast<int*>(smem + L.hist);
-    int* queue = reinterpret_cast<int*>(smem + L.queue);
-    int* nq = reinterpret_cast<int*>(smem + L.nq);
-    double* uex = reinterpret_cast<double*>(smem + L.uex);
-    float* cm = reinterpret_cast<float*>(smem + L.cm);
-    float* cden = reinterpret_cast<float*>(smem + L.cden);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int tok0 = blockIdx.x * kBT;
     const int ntok = min(kBT, P.T - tok0);
     const int E = P.E, k = P.k, d = P.d;
     const int N = GATE == kGateSoftmax ? E : GATE == kGateNoisy ? 2 * E : P.p;
-    const T* x = static_cast<const T*>(P.x);
 
-    if (tid == 0) nq[0] = 0;
     // ---- CTA: weight-row squared norms (sum of the split partials); cosine: embedding norms
     for (int n = tid; n < N; n += kSelThreads) {
         float q = 0.f;
@@ -258,7 +239,6 @@ __global__ void __launch_bounds__(kSelThreads) gate_select_kernel(const GatePara
             if (lane < k) {
                 P.topk_idx[(size_t)t * k + lane] = seli[lane];
                 P.topk_gate[(size_t)t * k + lane] = expf(selv[lane] - m) / den;
-                fidx[tt * kMaxTopK + lane] = seli[lane];
             }
         } else {
             // contenders: every expert whose score is within twice the bound of the k-th best
@@ -277,118 +257,202 @@ __global__ void __launch_bounds__(kSelThreads) gate_select_kernel(const GatePara
                 cnt = kMaxCand;
             }
             __syncwarp();
-            if (lane == 0) {  // the CTA re-scores its queued tokens together below
-                const int q = atomicAdd(nq, 1);
-                queue[q] = tt;
-                candn[tt] = cnt;
-                cm[tt] = m;
-                cden[tt] = den_all;
+            // the queue entry: token, contenders, the fp32 maximum score and softmax denominator, the
+            // contenders' ids and fp32 scores
+            int q = 0;
+            if (lane == 0) q = atomicAdd(P.rq_count, 1);
+            q = __shfl_sync(0xffffffffu, q, 0);
+            int* ent = P.rq + (size_t)q * kRescoreInts;
+            if (lane == 0) {
+                ent[0] = t;
+                ent[1] = cnt;
+                ent[2] = __float_as_int(m);
+                ent[3] = __float_as_int(den_all);
+            }
+            for (int c = lane; c < cnt; c += 32) {
+                ent[4 + c] = cand[c];
+                ent[4 + kMaxCand + c] = __float_as_int(sc[cand[c]]);
+                if (GATE == kGateCosine) P.need[cand[c]] = 1;
             }
         }
     }
-    __syncthreads();
+}
 
-    // ---- exact re-scoring of the queued tokens, one at a time by the whole CTA: a warp per contender
-    // (softmax / noisy), or first a warp per component of u = x P^T and then per contender (cosine)
-    {
-        const int nqueued = nq[0];
-        for (int qi = 0; qi < nqueued; ++qi) {
-            const int tq = queue[qi], tg = tok0 + tq, nc = candn[tq];
-            const int* cnd = cand_all + tq * kMaxCand;
-            double* ex = exs_all + tq * kMaxCand;
-            const T* xr = x + (size_t)tg * d;
-            if (GATE == kGateCosine) {
-                const T* proj = static_cast<const T*>(P.proj);
-                for (int j = warp; j < P.p; j += kBT) {
-                    const double u = warp_dot_ff<T>(xr, proj + (size_t)j * d, d, lane);
-                    if (lane == 0) uex[j] = u;
-                }
-                __syncthreads();
-                const T* emb = static_cast<const T*>(P.emb);
-                for (int c = warp; c < nc; c += kBT) {
-                    const int e = cnd[c];
-                    double dot = 0.0, ne2 = 0.0, nu2 = 0.0;
-                    for (int j = lane; j < P.p; j += 32) {
-                        const double uj = uex[j];
-                        const double ej = (double)load1(emb + (size_t)e * P.p + j);
-                        dot = fma(uj, ej, dot);
-                        ne2 = fma(ej, ej, ne2);
-                        nu2 = fma(uj, uj, nu2);
-                    }
-                    dot = warp_sum_d(dot);
-                    ne2 = warp_sum_d(ne2);
-                    nu2 = warp_sum_d(nu2);
-                    if (lane == 0) ex[c] = dot / (fmax(sqrt(nu2), 1e-12) * fmax(sqrt(ne2), 1e-12)) / P.temp;
-                }
+// ---- fold: v_e[i] = sum_j P[j][i] e_e[j] for the flagged experts, float-float (hi, lo) per entry.
+// A CTA covers kFoldCols columns of P for a group of 32 experts: it stages the column strip of P and
+// the group's embeddings (transposed, fp32) in shared memory a chunk of kFoldChunk rows at a time, and
+// thread (column c, expert lane) accumulates over j in two interleaved float-float chains.
+constexpr int kFoldCols = 8;
+constexpr int kFoldChunk = 256;
+constexpr int kFoldThreads = 32 * kFoldCols;
+
+template <typename T>
+__global__ void __launch_bounds__(kFoldThreads) gate_cos_fold_kernel(const GateParams P) {
+    __shared__ float ps[kFoldChunk][kFoldCols];
+    __shared__ float es[kFoldChunk][33];
+    pdl_wait();
+    pdl_trigger();
+    const int tid = threadIdx.x, lane = tid & 31, c = tid >> 5;
+    const int E = P.E, d = P.d, p = P.p;
+    const int i0 = blockIdx.x * kFoldCols, e0 = blockIdx.y * 32;
+    const int e = e0 + lane;
+    const bool mine = e < E && P.need[e] != 0;
+    if (__syncthreads_or(mine) == 0) return;  // no expert of the group contends anywhere
+    const T* proj = static_cast<const T*>(P.proj);
+    const T* emb = static_cast<const T*>(P.emb);
+    float hi[2] = {0.f, 0.f}, lo[2] = {0.f, 0.f};
+    for (int j0 = 0; j0 < p; j0 += kFoldChunk) {
+        const int nj = min(kFoldChunk, p - j0);
+        __syncthreads();
+        for (int q = tid; q < nj * kFoldCols; q += kFoldThreads) {
+            const int j = q / kFoldCols, cc = q % kFoldCols;
+            ps[j][cc] = i0 + cc < d ? load1(proj + (size_t)(j0 + j) * d + i0 + cc) : 0.f;
+        }
+        for (int q = tid; q < nj * 32; q += kFoldThreads) {
+            const int ee = q / nj, j = q % nj;
+            es[j][ee] = e0 + ee < E ? load1(emb + (size_t)(e0 + ee) * p + j0 + j) : 0.f;
+        }
+        __syncthreads();
+#pragma unroll 4
+        for (int j = 0; j < nj; j += 2) {  // p is a multiple of 8
+            ff_fma(hi[0], lo[0], ps[j][c], es[j][lane]);
+            ff_fma(hi[1], lo[1], ps[j + 1][c], es[j + 1][lane]);
+        }
+    }
+    ff_add(hi[0], lo[0], hi[1], lo[1]);
+    if (mine && i0 + c < d) P.cosv[(size_t)e * d + i0 + c] = make_float2(hi[0], lo[0]);
+}
+
+// x . v_e by one warp, float-float: x_i * hi_i exactly (TwoProduct), x_i * lo_i in fp32 (its error is
+// below 2^-48 |x_i v_i|); lanes take 8-element slices
+template <typename T>
+__device__ __forceinline__ double warp_dot_folded(const T* x, const float2* v, int d, int lane) {
+    float hi[2] = {0.f, 0.f}, lo[2] = {0.f, 0.f};
+    for (int i0 = lane * 8; i0 < d; i0 += 2 * 32 * 8) {
+        float xa[2][8];
+        float4 va[2][4];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int i = i0 + u * 32 * 8;
+            if (i < d) {
+                load8(x + i, xa[u]);
+                const float4* vp = reinterpret_cast<const float4*>(v + i);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) va[u][q] = vp[q];
             } else {
-                for (int c = warp; c < nc; c += kBT) {
-                    const int e = cnd[c];
-                    double sv = warp_dot_ff<T>(xr, logit_row<T>(P, GATE, e), d, lane);
-                    if (GATE == kGateNoisy) {
-                        const double z = warp_dot_ff<T>(xr, logit_row<T>(P, GATE, E + e), d, lane);
-                        sv += (double)P.eps[(size_t)tg * E + e] * log1p(exp(z));
-                    }
-                    if (lane == 0) ex[c] = sv;
-                }
+#pragma unroll
+                for (int q = 0; q < 8; ++q) xa[u][q] = 0.f;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) va[u][q] = make_float4(0.f, 0.f, 0.f, 0.f);
             }
-            __syncthreads();
-            if (tid == 0) {
-                const float* sc = GATE == kGateCosine ? scs + (size_t)tq * E : logits + (size_t)tq * N;
-                uint64_t used = 0;
-                int chosen[kMaxTopK];
-                for (int r = 0; r < k; ++r) {
-                    int best = -1;
-                    for (int c = 0; c < nc; ++c) {
-                        if ((used >> c) & 1ull) continue;
-                        if (best < 0 || ex[c] > ex[best] || (ex[c] == ex[best] && cnd[c] < cnd[best])) best = c;
-                    }
-                    used |= 1ull << best;
-                    chosen[r] = cnd[best];
-                }
-                const float m = cm[tq];
-                float den = cden[tq];
-                if (P.norm != 0) {
-                    den = 0.f;
-                    for (int r = 0; r < k; ++r) den += expf(sc[chosen[r]] - m);
-                }
-                for (int r = 0; r < k; ++r) {
-                    P.topk_idx[(size_t)tg * k + r] = chosen[r];
-                    P.topk_gate[(size_t)tg * k + r] = expf(sc[chosen[r]] - m) / den;
-                    fidx[tq * kMaxTopK + r] = chosen[r];
-                }
-            }
-            __syncthreads();
         }
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                ff_fma(hi[u], lo[u], xa[u][2 * q], va[u][q].x);
+                lo[u] = fmaf(xa[u][2 * q], va[u][q].y, lo[u]);
+                ff_fma(hi[u], lo[u], xa[u][2 * q + 1], va[u][q].z);
+                lo[u] = fmaf(xa[u][2 * q + 1], va[u][q].w, lo[u]);
+            }
     }
+    ff_add(hi[0], lo[0], hi[1], lo[1]);
+    ff_warp_sum(hi[0], lo[0]);
+    return (double)hi[0] + (double)lo[0];
+}
 
-    // ---- the dispatch's first step on the CTA's tokens (pair ranks in token order, expert histogram);
-    // the last CTA to finish runs the dispatch scan
-    if (P.blk_hist != nullptr) {
-        for (int e = tid; e < E; e += kSelThreads) hist[e] = 0;
+// ---- rescore: CTA q takes queue entries q, q + gridDim.x, ...; warps take the entry's contenders
+template <typename T, int GATE, int NW>
+__global__ void __launch_bounds__(32 * NW) gate_rescore_kernel(const GateParams P) {
+    __shared__ int cnd[kMaxCand];
+    __shared__ float csc[kMaxCand];
+    __shared__ double ex[kMaxCand];
+    __shared__ int hdr[4];
+    __shared__ int chosen[kMaxTopK];
+    pdl_wait();
+    pdl_trigger();
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int E = P.E, k = P.k, d = P.d;
+    const int nq = *P.rq_count;
+    for (int q = blockIdx.x; q < nq; q += gridDim.x) {
+        const int* ent = P.rq + (size_t)q * kRescoreInts;
+        if (tid < 4) hdr[tid] = ent[tid];
         __syncthreads();
-        if (warp == 0)
-            rank_pairs_warp([&](int i) { return fidx[(i / k) * kMaxTopK + i % k]; }, ntok * k, hist,
-                            P.slot + (size_t)tok0 * k, lane);
+        const int nc = hdr[1];
+        for (int c = tid; c < nc; c += 32 * NW) {
+            cnd[c] = ent[4 + c];
+            csc[c] = __int_as_float(ent[4 + kMaxCand + c]);
+        }
         __syncthreads();
-        for (int e = tid; e < E; e += kSelThreads) P.blk_hist[(size_t)blockIdx.x * E + e] = hist[e];
-        if (P.ticket != nullptr) {
-            __syncthreads();  // the block's histogram is written; thread 0 publishes it with the ticket
-            if (tid == 0) {
-                __threadfence();
-                nq[1] = atomicAdd(P.ticket, 1);
-                __threadfence();
+        const int t = hdr[0];
+        const T* xr = static_cast<const T*>(P.x) + (size_t)t * d;
+        for (int c = warp; c < nc; c += NW) {
+            const int e = cnd[c];
+            double sv;
+            if (GATE == kGateCosine) {
+                const T* er = static_cast<const T*>(P.emb) + (size_t)e * P.p;
+                double ne2 = 0.0;
+                for (int j = lane; j < P.p; j += 32) {
+                    const double v = (double)load1(er + j);
+                    ne2 = fma(v, v, ne2);
+                }
+                ne2 = warp_sum_d(ne2);
+                sv = warp_dot_folded<T>(xr, P.cosv + (size_t)e * d, d, lane) / fmax(sqrt(ne2), 1e-12);
+            } else {
+                sv = warp_dot_ff<T>(xr, logit_row<T>(P, GATE, e), d, lane);
+                if (GATE == kGateNoisy) {
+                    const double z = warp_dot_ff<T>(xr, logit_row<T>(P, GATE, E + e), d, lane);
+                    sv += (double)P.eps[(size_t)t * E + e] * log1p(exp(z));
+                }
             }
-            __syncthreads();
-            if (nq[1] == (int)gridDim.x - 1) {
-                ScanSmem sm;
-                sm.part = reinterpret_cast<int*>(smem + L.scan_part);
-                sm.padded = reinterpret_cast<int*>(smem + L.scan_padded);
-                sm.kept = reinterpret_cast<int*>(smem + L.scan_kept);
-                sm.wsum = reinterpret_cast<int*>(smem + L.scan_wsum);
-                scan_experts(P.blk_hist, gridDim.x, E, P.C, P.count, P.offset, P.row_token, P.row_gate, sm);
-                if (tid == 0) *P.ticket = 0;  // ready for the next call
+            if (lane == 0) ex[c] = sv;
+        }
+        __syncthreads();
+        if (warp == 0) {
+            // k rounds of a warp argmax over the contenders (a lane holds contenders lane and lane + 32);
+            // equal scores go to the lower expert id
+            bool used0 = lane >= nc, used1 = lane + 32 >= nc;
+            for (int r = 0; r < k; ++r) {
+                double bv = -INFINITY;
+                int bid = INT_MAX, bc = -1;
+                if (!used0) { bv = ex[lane]; bid = cnd[lane]; bc = lane; }
+                if (!used1 && (bc < 0 || ex[lane + 32] > bv || (ex[lane + 32] == bv && cnd[lane + 32] < bid))) {
+                    bv = ex[lane + 32];
+                    bid = cnd[lane + 32];
+                    bc = lane + 32;
+                }
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) {
+                    const double ov = __shfl_xor_sync(0xffffffffu, bv, off);
+                    const int oid = __shfl_xor_sync(0xffffffffu, bid, off);
+                    const int oc = __shfl_xor_sync(0xffffffffu, bc, off);
+                    if (oc >= 0 && (bc < 0 || ov > bv || (ov == bv && oid < bid))) {
+                        bv = ov;
+                        bid = oid;
+                        bc = oc;
+                    }
+                }
+                if (bc < 0) {  // fewer than k contenders: only a NaN score leaves the top k out
+                    if (lane == 0) record_error(P.err, kErrCheck, kWhereGate);
+                    bc = 0;
+                }
+                if (bc == lane) used0 = true;
+                if (bc == lane + 32) used1 = true;
+                if (lane == 0) chosen[r] = bc;
+            }
+            __syncwarp();
+            const float m = __int_as_float(hdr[2]);
+            float den = __int_as_float(hdr[3]);
+            if (P.norm != 0) {
+                den = 0.f;
+                for (int r = 0; r < k; ++r) den += expf(csc[chosen[r]] - m);
+            }
+            if (lane < k) {
+                P.topk_idx[(size_t)t * k + lane] = cnd[chosen[lane]];
+                P.topk_gate[(size_t)t * k + lane] = expf(csc[chosen[lane]] - m) / den;
             }
         }
+        __syncthreads();
     }
 }
 
@@ -409,6 +473,35 @@ cudaError_t launch_sel(const GateParams& P, cudaStream_t s) {
 }  // namespace
 
 size_t gate_select_smem_bytes(int gate, int E, int p) { return sel_layout(gate, E, p, 0).total; }
+
+cudaError_t launch_gate_rescore(const GateParams& P, cudaStream_t s) {
+    if (P.T <= 0) return cudaSuccess;
+    if (!P.bf16 || P.rq_count == nullptr) return cudaErrorInvalidValue;
+    // eight warps per CTA and four CTAs per SM: queued tokens mostly have k + 1 contenders.  Many experts
+    // make long contender lists more likely: there sixteen warps and two CTAs per SM.
+    const int sms = device_sm_count();
+    if (P.E >= 128) {
+        const dim3 grid((unsigned)(2 * sms));
+        switch (P.gate) {
+            case kGateSoftmax: return launch_pdl(gate_rescore_kernel<bf16_t, kGateSoftmax, 16>, grid, dim3(512), 0, s, P);
+            case kGateNoisy: return launch_pdl(gate_rescore_kernel<bf16_t, kGateNoisy, 16>, grid, dim3(512), 0, s, P);
+            default: return launch_pdl(gate_rescore_kernel<bf16_t, kGateCosine, 16>, grid, dim3(512), 0, s, P);
+        }
+    }
+    const dim3 grid((unsigned)(4 * sms));
+    switch (P.gate) {
+        case kGateSoftmax: return launch_pdl(gate_rescore_kernel<bf16_t, kGateSoftmax, 8>, grid, dim3(256), 0, s, P);
+        case kGateNoisy: return launch_pdl(gate_rescore_kernel<bf16_t, kGateNoisy, 8>, grid, dim3(256), 0, s, P);
+        default: return launch_pdl(gate_rescore_kernel<bf16_t, kGateCosine, 8>, grid, dim3(256), 0, s, P);
+    }
+}
+
+cudaError_t launch_gate_cos_fold(const GateParams& P, cudaStream_t s) {
+    if (P.T <= 0) return cudaSuccess;
+    if (!P.bf16 || P.gate != kGateCosine || P.need == nullptr || P.cosv == nullptr) return cudaErrorInvalidValue;
+    const dim3 grid((unsigned)((P.d + kFoldCols - 1) / kFoldCols), (unsigned)((P.E + 31) / 32));
+    return launch_pdl(gate_cos_fold_kernel<bf16_t>, grid, dim3(kFoldThreads), 0, s, P);
+}
 
 cudaError_t launch_gate_select(const GateParams& P, cudaStream_t s) {
     if (P.T <= 0) return cudaSuccess;

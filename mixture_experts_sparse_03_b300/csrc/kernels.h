@@ -44,10 +44,20 @@ struct GateParams {
     const float* wn2p;
     int S, Np;
     float cb;               // logit error bound = cb * |x_t| * |w_n| (+ 4u |logit|)
+    // re-scoring of near ties (selection from precomputed logits): tokens with near ties go to a global
+    // queue of kRescoreInts-int entries that the rescore kernel works through with every SM
+    int* rq_count;          // zero-initialised entry counter
+    int* rq;                // [T][kRescoreInts]
+    int* need;              // cosine: [E] zero-initialised flags, set for experts that contend somewhere
+    float2* cosv;           // cosine: [E][d] v_e = P^T e_e as float-float (hi, lo), flagged experts only
 };
+constexpr int kMaxCandidates = 64;                          // contenders re-scored per token
+constexpr int kRescoreInts = 4 + 2 * kMaxCandidates;       // token, count, m, den, ids, fp32 scores
 size_t gate_smem_bytes(int gate, int E, int p, int d);  // CUDA-core gate (fp32 layers)
 size_t gate_select_smem_bytes(int gate, int E, int p);  // selection from precomputed logits
 cudaError_t launch_gate_select(const GateParams& p, cudaStream_t s);
+cudaError_t launch_gate_cos_fold(const GateParams& p, cudaStream_t s);  // cosine: p.cosv for p.need
+cudaError_t launch_gate_rescore(const GateParams& p, cudaStream_t s);   // works through p.rq
 
 // ---- gate logits GEMM on the tensor cores (gate_tc.cu) ------------------------------------------
 constexpr int kGateMaxSplits = 8;
@@ -74,10 +84,12 @@ cudaError_t launch_gate_gemm(const GateGemmPlan& g, const void* x, const void* w
 cudaError_t launch_gate(const GateParams& p, cudaStream_t s);
 
 // ---- dispatch ---------------------------------------------------------------------------------
+// rank step over all tokens; the last CTA to finish (counted on `ticket`, a zero-initialised int that
+// it resets) runs the scan: count[E], offset[E+1] and the padding rows of row_token / row_gate, with
+// capacity C
 cudaError_t launch_dispatch_rank(const int* topk_idx, int T, int k, int E, int* blk_hist, int* rank, int* err,
+                                 int* ticket, int C, int* count, int* offset, int* row_token, float* row_gate,
                                  cudaStream_t s);
-cudaError_t launch_dispatch_scan(int* blk_hist, int T, int k, int E, int C, int* count, int* offset,
-                                 int* row_token, float* row_gate, cudaStream_t s);
 // slot [T, k] holds the block ranks on entry (from the rank step or the gate kernel) and the slots on exit
 cudaError_t launch_dispatch_gather(const void* x, int bf16, const int* topk_idx, const float* topk_gate,
                                    const int* blk_base, const int* offset, int T, int k, int E, int d, int C,

@@ -148,9 +148,11 @@ def test_launch_counts():
     assert b.moe_forward_launches(b.config(small_workload(k=2))) == 4
     assert b.moe_forward_launches(b.config(small_workload(k=3))) == 5
     assert b.moe_forward_launches(b.config(small_workload(k=2), flags=b.FLAG_UNFUSED_COMBINE)) == 5
-    # other bf16 gates: logits GEMM and selection kernel
-    assert b.moe_forward_launches(b.config(small_workload(k=2, gate="noisy"))) == 5
-    assert b.moe_forward_launches(b.config(small_workload(k=2, E=65))) == 5
+    # other bf16 gates: logits GEMM, selection, grid-wide re-scoring, rank step with the scan
+    assert b.moe_forward_launches(b.config(small_workload(k=2, gate="noisy"))) == 7
+    assert b.moe_forward_launches(b.config(small_workload(k=2, E=65))) == 7
+    # the cosine gate adds the fold of the projection into the expert embeddings
+    assert b.moe_forward_launches(b.config(small_workload(k=2, gate="cosine"))) == 8
     # fp32: the gate computes its logits itself
     assert b.moe_forward_launches(b.config(small_workload(k=2, dtype="f32"))) == 4
     assert b.moe_forward_launches(b.config(small_workload(k=3, dtype="f32"))) == 5

@@ -102,20 +102,24 @@ def _ulp_step(w: torch.Tensor, up: bool) -> torch.Tensor:
     return nb.to(torch.int16).view(torch.bfloat16)
 
 
-@pytest.mark.parametrize("gate", ["softmax", "noisy"])
-def test_near_ties_resolved_exactly(gate):
-    """Gate rows that differ from another row by one bf16 ulp in one element: their scores differ by
-    1e-7 to 1e-3, often inside the fp32 error bound, so the kernel must settle the order with its
-    float-float re-scoring.  The choice must equal the oracle's on every token."""
-    wl = small_workload(T=256, d=256, h=64, E=6, k=2, gate=gate, capacity=256)
+@pytest.mark.parametrize("gate,E", [("softmax", 6), ("softmax", 72), ("noisy", 6), ("cosine", 6)])
+def test_near_ties_resolved_exactly(gate, E):
+    """Gate rows (cosine gate: expert embeddings) that differ from another row by one bf16 ulp in one
+    element: their scores differ by 1e-7 to 1e-3, often inside the fp32 error bound, so the kernel must
+    settle the order with its float-float re-scoring (inside the fused gate for softmax with E <= 64,
+    else the grid-wide re-scoring kernel).  The choice must equal the oracle's on every token."""
+    wl = small_workload(T=256, d=256, h=64, E=E, k=2, gate=gate, capacity=256,
+                        cos_dim=64 if gate == "cosine" else 32)
     tc, tg = P.inputs(wl)
-    wg = tc["w_gate"].clone()
+    name = "emb" if gate == "cosine" else "w_gate"
+    col = (5, 17) if gate != "cosine" else (5, 40)
+    wg = tc[name].clone()
     wg[2] = wg[0]
-    wg[2, 5] = _ulp_step(wg[0, 5:6], True)[0]
+    wg[2, col[0]] = _ulp_step(wg[0, col[0]:col[0] + 1], True)[0]
     wg[4] = wg[1]
-    wg[4, 17] = _ulp_step(wg[1, 17:18], False)[0]
-    tc["w_gate"] = wg
-    tg["w_gate"] = wg.cuda()
+    wg[4, col[1]] = _ulp_step(wg[1, col[1]:col[1] + 1], False)[0]
+    tc[name] = wg
+    tg[name] = wg.cuda()
     if gate == "noisy":
         wn = tc["w_noise"].clone()
         wn[2] = wn[0]
