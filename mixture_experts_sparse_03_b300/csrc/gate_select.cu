@@ -304,13 +304,28 @@ __global__ void __launch_bounds__(kFoldThreads) gate_cos_fold_kernel(const GateP
     for (int j0 = 0; j0 < p; j0 += kFoldChunk) {
         const int nj = min(kFoldChunk, p - j0);
         __syncthreads();
-        for (int q = tid; q < nj * kFoldCols; q += kFoldThreads) {
-            const int j = q / kFoldCols, cc = q % kFoldCols;
-            ps[j][cc] = i0 + cc < d ? load1(proj + (size_t)(j0 + j) * d + i0 + cc) : 0.f;
+        // a row of the strip is one 16-byte load (d and i0 are multiples of 8), and so are eight
+        // consecutive entries of an embedding (p and j0 are multiples of 8)
+#pragma unroll 2
+        for (int j = tid; j < nj; j += kFoldThreads) {
+            float v[8];
+            load8(proj + (size_t)(j0 + j) * d + i0, v);
+#pragma unroll
+            for (int cc = 0; cc < kFoldCols; ++cc) ps[j][cc] = v[cc];
         }
-        for (int q = tid; q < nj * 32; q += kFoldThreads) {
-            const int ee = q / nj, j = q % nj;
-            es[j][ee] = e0 + ee < E ? load1(emb + (size_t)(e0 + ee) * p + j0 + j) : 0.f;
+        const int nv = nj / 8;
+#pragma unroll 4
+        for (int q = tid; q < 32 * nv; q += kFoldThreads) {
+            const int ee = q / nv, j = (q % nv) * 8;
+            float v[8];
+            if (e0 + ee < E) {
+                load8(emb + (size_t)(e0 + ee) * p + j0 + j, v);
+            } else {
+#pragma unroll
+                for (int u = 0; u < 8; ++u) v[u] = 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) es[j + u][ee] = v[u];
         }
         __syncthreads();
 #pragma unroll 4
@@ -320,7 +335,7 @@ __global__ void __launch_bounds__(kFoldThreads) gate_cos_fold_kernel(const GateP
         }
     }
     ff_add(hi[0], lo[0], hi[1], lo[1]);
-    if (mine && i0 + c < d) P.cosv[(size_t)e * d + i0 + c] = make_float2(hi[0], lo[0]);
+    if (mine) P.cosv[(size_t)e * d + i0 + c] = make_float2(hi[0], lo[0]);
 }
 
 // x . v_e by one warp, float-float: x_i * hi_i exactly (TwoProduct), x_i * lo_i in fp32 (its error is
@@ -499,7 +514,7 @@ cudaError_t launch_gate_rescore(const GateParams& P, cudaStream_t s) {
 cudaError_t launch_gate_cos_fold(const GateParams& P, cudaStream_t s) {
     if (P.T <= 0) return cudaSuccess;
     if (!P.bf16 || P.gate != kGateCosine || P.need == nullptr || P.cosv == nullptr) return cudaErrorInvalidValue;
-    const dim3 grid((unsigned)((P.d + kFoldCols - 1) / kFoldCols), (unsigned)((P.E + 31) / 32));
+    const dim3 grid((unsigned)(P.d / kFoldCols), (unsigned)((P.E + 31) / 32));  // d is a multiple of 8
     return launch_pdl(gate_cos_fold_kernel<bf16_t>, grid, dim3(kFoldThreads), 0, s, P);
 }
 

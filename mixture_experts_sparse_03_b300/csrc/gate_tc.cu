@@ -19,9 +19,11 @@
 // 64 products and the error bound does not grow with d), compute the squared norms of the x rows
 // (n-tile 0) and weight rows (m-tile 0) from the shared-memory tiles -- the selection kernel bounds
 // each logit's error by them -- and store the logits.
-// When one CTA holds every logit of its tokens (softmax gate, E <= 64) the selection runs in the same
-// epilogue (fused_select): scores, top-k, near-tie re-scoring, gates, the dispatch's pair ranks and
-// block histograms, and the dispatch scan in the last CTA -- the whole gate in one launch.
+// When one CTA can hold every logit of its tokens (softmax gate, E <= 64) the selection runs in the same
+// launch: a cluster of up to four CTAs per 128-token tile splits K, the CTAs add their float-float
+// partials through distributed shared memory, and each selects its share of the rows, a warp per token
+// (select_row): top-k, near-tie re-scoring, gates; then the dispatch's pair ranks and block histograms,
+// and the dispatch scan in the last CTA -- the whole gate in one launch.
 // Every mbarrier wait is bounded; on expiry the kernel records MOE_ERR_DEVICE_TIMEOUT, waits (bounded)
 // for its own copies and MMAs, frees its TMEM and returns.
 #include "common.cuh"
@@ -37,6 +39,7 @@ namespace {
 using namespace tc;
 using gate::kMaxCand;
 using gate::kU;
+using gate::order_key;
 
 constexpr int kGM = 128, kGK = 64;
 constexpr int kGMaxStages = 12;  // TMA ring depth: as many stages as fit (the CTAs are few and latency-bound)
@@ -44,6 +47,11 @@ constexpr int kGThreads = 320;  // producer, MMA, 4 accumulation warps, 4 norm w
 constexpr int kGChunks = 8;     // TMEM accumulators the MMAs rotate through
 constexpr int kGMaxBN = 64;  // logits per n-tile: the epilogue holds 64 float-float sums per row
 constexpr uint32_t kGABytes = kGM * kGK * 2;  // 16 KiB
+constexpr int kGMaxCluster = 4;  // fused gate: CTAs splitting K per token tile (at most one per row quarter)
+
+// fused gate: each CTA's float-float partial logits (hi [BN][128], lo [BN][128], column-major so that a
+// warp reads 32 consecutive rows), x-row norms [128] and weight-row norms [kGMaxBN] over its K range
+__host__ __device__ constexpr size_t red_bytes(int BN) { return (size_t)(2 * BN * kGM + kGM + kGMaxBN) * 4; }
 
 struct GemmArgs {
     float* part;       // [S][T][Np]
@@ -57,12 +65,14 @@ struct GemmArgs {
 };
 
 // sum of squares of the 64 bf16 of one 128-byte row of a swizzled tile (the swizzle only permutes the
-// row's 16-byte chunks, so the sum is over the same elements)
-__device__ __forceinline__ float sumsq_tile_row(const uint8_t* row) {
+// row's 16-byte chunks, so the sum is over the same elements).  Row r reads its chunks starting at chunk
+// r mod 8: rows are 128 bytes apart, so in the same chunk order eight consecutive rows would hit the same
+// four banks; rotated, each group of eight lanes covers all 32 banks.
+__device__ __forceinline__ float sumsq_tile_row(const uint8_t* row, int r) {
     float s[8];
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
-        const uint4 u = *reinterpret_cast<const uint4*>(row + c * 16);
+        const uint4 u = *reinterpret_cast<const uint4*>(row + ((c + r) & 7) * 16);
         const uint32_t w[4] = {u.x, u.y, u.z, u.w};
         s[c] = 0.f;
 #pragma unroll
@@ -75,18 +85,20 @@ __device__ __forceinline__ float sumsq_tile_row(const uint8_t* row) {
     return ((s[0] + s[1]) + (s[2] + s[3])) + ((s[4] + s[5]) + (s[6] + s[7]));
 }
 
-// Fused selection smem (softmax gate, all logits in one n-tile): per row the top-(k+1) values and ids and
-// the chosen ids, per warp the row being re-scored and its contenders, the weight-row norms, per warp the
-// dispatch rank counters, and the dispatch scan's scratch.
+constexpr int kGWarps = kGThreads / 32;
+constexpr int kLgStride = kGMaxBN + 1;  // row stride of the logits staged for the selection
+
+// Fused selection smem (softmax gate, all logits of a token in one CTA): per row the top-(k+1) values
+// and ids and the chosen ids, the rows' x norms and the weight-row norms, per warp the contenders of a
+// re-scored row, per row quarter the dispatch rank counters, and the dispatch scan's scratch.
 struct FusedSmem {
     float selv[kGM][kMaxTopK + 1];
     int seli[kGM][kMaxTopK + 1];
     int fidx[kGM][kMaxTopK];
     float xn2[kGM];
     float wn2[kGMaxBN];
-    float wsc[4][kGMaxBN];
-    int cand[4][kMaxCand];
-    double ex[4][kMaxCand];
+    int cand[kGWarps][kMaxCand];
+    double ex[kGWarps][kMaxCand];
     int running[4][kGMaxBN];
     int part[kGThreads];
     int padded[kGMaxBN + 1];
@@ -95,132 +107,115 @@ struct FusedSmem {
     int last;
 };
 
-// Selection in the epilogue of the logits GEMM when one CTA holds all of a token's logits (softmax gate,
-// E <= 64): the thread owning row r has its token's logits as float-float sums; it forms the error
-// bound, picks the top-(k+1) (ties -> lower id), writes ids and gates, or queues the token when two of
-// them lie within twice the bound; the warp then re-scores each queued token's contenders with
-// float-float dot products, and finally numbers its 32 tokens' pairs for the dispatch.
-template <int BNC>
-__device__ __forceinline__ void fused_select(const GateParams& P, FusedSmem& fs, const float (&hi)[BNC],
-                                             const float (&lo)[BNC], int m0, int r, int lane, int q) {
+// Selection of one token by one warp from its fp32 logits lrow[0..E) (E <= 64; lane l holds experts l
+// and l + 32): the error bound of each logit from the tensor-core accumulation bound cb |x| |w_e|, the
+// top-(k+1) by warp reductions over order keys (ties -> lower expert id), then the ids and gates, or --
+// when two of the top-(k+1) lie within twice the bound -- float-float re-scoring of every expert within
+// twice the bound of the k-th best, a warp dot product per contender, and the k best of those.
+__device__ __forceinline__ void select_row(const GateParams& P, FusedSmem& fs, const float* lrow, int rr, int t,
+                                           int w, int lane) {
     const int E = P.E, k = P.k, ksel = min(k + 1, E);
-    const int t = m0 + r;
-    const bool valid = t < P.T;
-    const float xn = sqrtf(fs.xn2[r]);
-    float L[BNC];
-#pragma unroll
-    for (int j = 0; j < BNC; ++j) L[j] = hi[j] + lo[j];
-    float dmax = 0.f;
-#pragma unroll
-    for (int j = 0; j < BNC; ++j)
-        if (j < E) dmax = fmaxf(dmax, P.cb * xn * sqrtf(fs.wn2[j]) + 4.f * kU * fabsf(L[j]));
-    dmax *= 1.0625f;
-    uint64_t taken = 0;
+    const bool h0 = lane < E, h1 = lane + 32 < E;
+    const float v0 = h0 ? lrow[lane] : 0.f, v1 = h1 ? lrow[lane + 32] : 0.f;
+    const float xn = sqrtf(fs.xn2[rr]);
+    float dm = 0.f;
+    if (h0) dm = P.cb * xn * sqrtf(fs.wn2[lane]) + 4.f * kU * fabsf(v0);
+    if (h1) dm = fmaxf(dm, P.cb * xn * sqrtf(fs.wn2[lane + 32]) + 4.f * kU * fabsf(v1));
+    const float two_d = 2.f * (warp_max(dm) * 1.0625f);
+    const uint32_t key0 = order_key(v0), key1 = order_key(v1);
+    bool t0 = !h0, t1 = !h1;  // taken (or absent)
     for (int s2 = 0; s2 < ksel; ++s2) {
-        float bv = -INFINITY;
-        int bi = -1;
-#pragma unroll
-        for (int j = 0; j < BNC; ++j)
-            if (j < E && !((taken >> j) & 1ull) && (bi < 0 || L[j] > bv)) { bv = L[j]; bi = j; }
-        taken |= 1ull << bi;
-        fs.selv[r][s2] = bv;
-        fs.seli[r][s2] = bi;
+        // the lane's best untaken expert (its lower id wins a tie), then the warp's
+        const bool use1 = !t1 && (t0 || key1 > key0);
+        const bool has = !t0 || !t1;
+        const uint32_t bk = use1 ? key1 : key0;
+        const uint32_t wk = __reduce_max_sync(0xffffffffu, has ? bk : 0u);
+        const int wi = (int)__reduce_min_sync(0xffffffffu, has && bk == wk ? (uint32_t)(use1 ? lane + 32 : lane) : 0xffffffffu);
+        if (wi == lane) t0 = true;
+        if (wi == lane + 32) t1 = true;
+        const float wv = __shfl_sync(0xffffffffu, wi < 32 ? v0 : v1, wi & 31);
+        if (lane == 0) {
+            fs.selv[rr][s2] = wv;
+            fs.seli[rr][s2] = wi;
+        }
     }
-    const float two_d = 2.f * dmax;
+    __syncwarp();
     bool refine = false;
-    for (int s2 = 1; s2 < k; ++s2) refine |= !(fs.selv[r][s2 - 1] - fs.selv[r][s2] > two_d);
-    if (k < E) refine |= !(fs.selv[r][k - 1] - fs.selv[r][k] > two_d);
-    const float m = fs.selv[r][0];
+    for (int s2 = 1; s2 < k; ++s2) refine |= !(fs.selv[rr][s2 - 1] - fs.selv[rr][s2] > two_d);
+    if (k < E) refine |= !(fs.selv[rr][k - 1] - fs.selv[rr][k] > two_d);
+    const float m = fs.selv[rr][0];
     float den_all = 0.f;
-    if (P.norm == 0) {
-#pragma unroll
-        for (int j = 0; j < BNC; ++j)
-            if (j < E) den_all += expf(L[j] - m);
-    }
-    if (valid && !refine) {
+    if (P.norm == 0) den_all = warp_sum((h0 ? expf(v0 - m) : 0.f) + (h1 ? expf(v1 - m) : 0.f));
+    if (!refine) {
         float den = den_all;
         if (P.norm != 0) {
             den = 0.f;
-            for (int s2 = 0; s2 < k; ++s2) den += expf(fs.selv[r][s2] - m);
+            for (int s2 = 0; s2 < k; ++s2) den += expf(fs.selv[rr][s2] - m);
         }
-        for (int s2 = 0; s2 < k; ++s2) {
-            P.topk_idx[(size_t)t * k + s2] = fs.seli[r][s2];
-            P.topk_gate[(size_t)t * k + s2] = expf(fs.selv[r][s2] - m) / den;
-            fs.fidx[r][s2] = fs.seli[r][s2];
+        if (lane < k) {
+            P.topk_idx[(size_t)t * k + lane] = fs.seli[rr][lane];
+            P.topk_gate[(size_t)t * k + lane] = expf(fs.selv[rr][lane] - m) / den;
+            fs.fidx[rr][lane] = fs.seli[rr][lane];
         }
+        return;
     }
-    // the warp re-scores its queued rows one at a time
-    unsigned flagged = __ballot_sync(0xffffffffu, valid && refine);
-    while (flagged) {
-        const int src = __ffs(flagged) - 1;
-        flagged &= flagged - 1;
-        if (lane == src) {
+    // contenders, in expert order
+    const float thr = fs.selv[rr][k - 1] - two_d;
+    const bool c0 = h0 && !(v0 < thr), c1 = h1 && !(v1 < thr);
+    const unsigned m0b = __ballot_sync(0xffffffffu, c0), m1b = __ballot_sync(0xffffffffu, c1);
+    const int n0 = __popc(m0b), cnt = n0 + __popc(m1b);  // at most 64 = kMaxCand
+    if (c0) fs.cand[w][__popc(m0b & lanemask_lt())] = lane;
+    if (c1) fs.cand[w][n0 + __popc(m1b & lanemask_lt())] = lane + 32;
+    __syncwarp();
+    const bf16_t* xr = static_cast<const bf16_t*>(P.x) + (size_t)t * P.d;
+    for (int c = 0; c < cnt; ++c) {
+        const double v = gate::warp_dot_ff<bf16_t>(
+            xr, static_cast<const bf16_t*>(P.w_gate) + (size_t)fs.cand[w][c] * P.d, P.d, lane);
+        if (lane == 0) fs.ex[w][c] = v;
+    }
+    __syncwarp();
+    // k rounds of a warp argmax over the contenders' exact scores (equal scores -> lower expert id)
+    bool u0 = lane >= cnt, u1 = lane + 32 >= cnt;
+    for (int s2 = 0; s2 < k; ++s2) {
+        double bv = -INFINITY;
+        int bid = INT_MAX, bc = -1;
+        if (!u0) { bv = fs.ex[w][lane]; bid = fs.cand[w][lane]; bc = lane; }
+        if (!u1 && (bc < 0 || fs.ex[w][lane + 32] > bv)) {
+            bv = fs.ex[w][lane + 32];
+            bid = fs.cand[w][lane + 32];
+            bc = lane + 32;
+        }
 #pragma unroll
-            for (int j = 0; j < BNC; ++j)
-                if (j < E) fs.wsc[q][j] = L[j];
-        }
-        __syncwarp();
-        const int rs = q * 32 + src, ts = m0 + rs;
-        const float thr = __shfl_sync(0xffffffffu, fs.selv[r][k - 1] - two_d, src);
-        const float ms = __shfl_sync(0xffffffffu, m, src);
-        const float dens = __shfl_sync(0xffffffffu, den_all, src);
-        int cnt = 0;
-        for (int base = 0; base < E; base += 32) {
-            const int e = base + lane;
-            const bool pred = e < E && !(fs.wsc[q][e] < thr);
-            const unsigned mask = __ballot_sync(0xffffffffu, pred);
-            const int pos = cnt + __popc(mask & lanemask_lt());
-            if (pred && pos < kMaxCand) fs.cand[q][pos] = e;
-            cnt += __popc(mask);
-        }
-        cnt = min(cnt, kMaxCand);
-        __syncwarp();
-        const bf16_t* xr = static_cast<const bf16_t*>(P.x) + (size_t)ts * P.d;
-        for (int c = 0; c < cnt; ++c) {
-            const double v = gate::warp_dot_ff<bf16_t>(
-                xr, static_cast<const bf16_t*>(P.w_gate) + (size_t)fs.cand[q][c] * P.d, P.d, lane);
-            if (lane == 0) fs.ex[q][c] = v;
-        }
-        __syncwarp();
-        if (lane == 0) {
-            uint64_t used = 0;
-            int chosen[kMaxTopK];
-            for (int s2 = 0; s2 < k; ++s2) {
-                int best = -1;
-                for (int c = 0; c < cnt; ++c) {
-                    if ((used >> c) & 1ull) continue;
-                    if (best < 0 || fs.ex[q][c] > fs.ex[q][best] ||
-                        (fs.ex[q][c] == fs.ex[q][best] && fs.cand[q][c] < fs.cand[q][best]))
-                        best = c;
-                }
-                used |= 1ull << best;
-                chosen[s2] = fs.cand[q][best];
-            }
-            float den = dens;
-            if (P.norm != 0) {
-                den = 0.f;
-                for (int s2 = 0; s2 < k; ++s2) den += expf(fs.wsc[q][chosen[s2]] - ms);
-            }
-            for (int s2 = 0; s2 < k; ++s2) {
-                P.topk_idx[(size_t)ts * k + s2] = chosen[s2];
-                P.topk_gate[(size_t)ts * k + s2] = expf(fs.wsc[q][chosen[s2]] - ms) / den;
-                fs.fidx[rs][s2] = chosen[s2];
+        for (int off = 16; off > 0; off >>= 1) {
+            const double ov = __shfl_xor_sync(0xffffffffu, bv, off);
+            const int oid = __shfl_xor_sync(0xffffffffu, bid, off);
+            const int oc = __shfl_xor_sync(0xffffffffu, bc, off);
+            if (oc >= 0 && (bc < 0 || ov > bv || (ov == bv && oid < bid))) {
+                bv = ov;
+                bid = oid;
+                bc = oc;
             }
         }
-        __syncwarp();
+        if (bc < 0) {  // fewer than k contenders: only a NaN logit leaves the top k out
+            if (lane == 0) record_error(P.err, kErrCheck, kWhereGateGemm);
+            bc = 0;
+            bid = fs.cand[w][0];
+        }
+        if (bc == lane) u0 = true;
+        if (bc == lane + 32) u1 = true;
+        if (lane == 0) fs.fidx[rr][s2] = bid;
     }
-    // the dispatch's first step on this warp's 32 tokens (one dispatch block): pair ranks, histogram
-    if (P.blk_hist != nullptr) {
-        const int t0 = m0 + q * 32;
-        const int ntok = min(32, P.T - t0);
-        if (ntok > 0) {
-            for (int e = lane; e < E; e += 32) fs.running[q][e] = 0;
-            __syncwarp();
-            rank_pairs_warp([&](int i) { return fs.fidx[q * 32 + i / k][i % k]; }, ntok * k, fs.running[q],
-                            P.slot + (size_t)t0 * k, lane);
-            __syncwarp();
-            for (int e = lane; e < E; e += 32) P.blk_hist[(size_t)(t0 / 32) * E + e] = fs.running[q][e];
-        }
+    __syncwarp();
+    // gates from the fp32 logits of the chosen experts
+    float den = den_all;
+    if (P.norm != 0) {
+        den = 0.f;
+        for (int s2 = 0; s2 < k; ++s2) den += expf(lrow[fs.fidx[rr][s2]] - m);
+    }
+    if (lane < k) {
+        const int e = fs.fidx[rr][lane];
+        P.topk_idx[(size_t)t * k + lane] = e;
+        P.topk_gate[(size_t)t * k + lane] = expf(lrow[e] - m) / den;
     }
 }
 
@@ -238,11 +233,16 @@ __global__ void __launch_bounds__(kGThreads, 1)
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * NS + 2 * kGChunks + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
     FusedSmem& fs = *reinterpret_cast<FusedSmem*>(tmem_holder + 4);
+    float* red = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(&fs) + sizeof(FusedSmem));  // fused only
     const int FULL = 0, EMPTY = NS, CFULL = 2 * NS, CEMPTY = 2 * NS + kGChunks, LAST = 2 * NS + 2 * kGChunks;
     auto bar = [&](int i) { return smem_u32(bars + i); };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int mt = blockIdx.x, nt = blockIdx.y, split = blockIdx.z;
+    // fused: grid (cs, m-tiles) in clusters of cs CTAs, CTA `split` of a cluster taking the split-th range
+    // of K blocks of the cluster's token tile; otherwise grid (m-tiles, n-tiles, splits)
+    const int mt = FUSED ? blockIdx.y : blockIdx.x, nt = FUSED ? 0 : blockIdx.y;
+    const int split = FUSED ? blockIdx.x : blockIdx.z;
+    const int cs = FUSED ? (int)gridDim.x : 1;
     const bool second = nt >= a.nt0;                        // tile of w_noise (noisy gate)
     const int n_local = (second ? nt - a.nt0 : nt) * a.BN;  // first weight row of the tile
     const int n_map = second ? a.N1 : a.N0;                 // rows of that weight tensor
@@ -280,6 +280,9 @@ __global__ void __launch_bounds__(kGThreads, 1)
     pdl_wait();  // the set-up above overlaps the previous kernel; its outputs are read below
     pdl_trigger();
 
+    float hi[BNC], lo[BNC];  // accumulation warps: the float-float logits of row r
+#pragma unroll
+    for (int j = 0; j < BNC; ++j) hi[j] = lo[j] = 0.f;
     if (warp == 0) {
         if (lane == 0) {
             const CUtensorMap* mb = second ? &tmB1 : &tmB0;
@@ -352,8 +355,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
             ok = __all_sync(0xffffffffu, mbar_wait(bar(FULL + stage), phase, abort_flag));
             if (!ok) break;
             const uint8_t* st = base + stage * stage_bytes;
-            if (x_norms) xs += sumsq_tile_row(st + nr * 128);
-            if (w_norms && nr < a.BN) wsq += sumsq_tile_row(st + kGABytes + nr * 128);
+            if (x_norms) xs += sumsq_tile_row(st + nr * 128, nr);
+            if (w_norms && nr < a.BN) wsq += sumsq_tile_row(st + kGABytes + nr * 128, nr);
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(EMPTY + stage));
             if (++stage == NS) { stage = 0; phase ^= 1u; }
@@ -367,17 +370,13 @@ __global__ void __launch_bounds__(kGThreads, 1)
             if (x_norms && m0 + nr < a.T) a.xn2_part[(size_t)split * a.T + m0 + nr] = xs;
             if (w_norms && nr < ncols) a.wn2_part[(size_t)split * a.Np + col0 + nr] = wsq;
         } else {
-            fs.xn2[nr] = xs;
-            if (nr < ncols) fs.wn2[nr] = wsq;
+            red[2 * a.BN * kGM + nr] = xs;
+            if (nr < kGMaxBN) red[2 * a.BN * kGM + kGM + nr] = nr < ncols ? wsq : 0.f;
         }
-        if constexpr (FUSED) asm volatile("bar.sync 1, 256;" ::: "memory");  // norms ready for the selection
     } else {
         // accumulation warps: one per TMEM lane quarter (32 rows)
         const int q = warp & 3;
         const int r = q * 32 + lane;
-        float hi[BNC], lo[BNC];
-#pragma unroll
-        for (int j = 0; j < BNC; ++j) hi[j] = lo[j] = 0.f;
         // G = 64 / BNC accumulators per round: their TMEM loads are in flight together, then added
         constexpr int G = 64 / BNC;
         bool ok = true;
@@ -446,8 +445,12 @@ __global__ void __launch_bounds__(kGThreads, 1)
                     if (j < ncols) dst[j] = hi[j] + lo[j];
             }
         } else {
-            asm volatile("bar.sync 1, 256;" ::: "memory");  // the norm warps' results
-            if (ok) fused_select<BNC>(P, fs, hi, lo, m0, r, lane, q);
+#pragma unroll
+            for (int j = 0; j < BNC; ++j)
+                if (j < a.BN) {
+                    red[j * kGM + r] = hi[j];
+                    red[(a.BN + j) * kGM + r] = lo[j];
+                }
         }
     }
     fence_before();
@@ -455,11 +458,67 @@ __global__ void __launch_bounds__(kGThreads, 1)
     fence_after();
     if (warp == 1) tmem_free(tmem_base, tcols);
     if constexpr (FUSED) {
+        if (cs > 1) cluster_sync();  // every CTA's partials (written before the barrier above) are visible
+        // the CTA that selects row quarter q (q = split, split + cs, ...) adds the cluster's partials into
+        // the quarter's accumulation warp: its own first, then the others in rank order (a fixed order), and
+        // stages the logits in the stage ring, which the finished K loop no longer uses
+        float* lg = reinterpret_cast<float*>(base);  // [kGM][kLgStride]
+        const int q = warp & 3;
+        if (warp >= 2 && warp < 6 && q % cs == split) {
+            const int r = q * 32 + lane;
+            float xs = red[2 * a.BN * kGM + r];
+#pragma unroll
+            for (int c = 0; c < kGMaxCluster; ++c) {
+                if (c >= cs) break;
+                if (c == split) continue;
+                // generic pointers into another CTA's shared memory: plain loads the compiler can batch
+                const float* rr = static_cast<const float*>(__cluster_map_shared_rank(red, (unsigned)c));
+#pragma unroll
+                for (int j = 0; j < BNC; ++j)
+                    if (j < a.BN) ff_add(hi[j], lo[j], rr[j * kGM + r], rr[(a.BN + j) * kGM + r]);
+                xs += rr[2 * a.BN * kGM + r];
+            }
+#pragma unroll
+            for (int j = 0; j < BNC; ++j)
+                if (j < a.BN) lg[r * kLgStride + j] = hi[j] + lo[j];
+            fs.xn2[r] = xs;
+            if (q == split) {  // the first quarter's warp also sums the weight-row norms
+                for (int j = lane; j < kGMaxBN; j += 32) {
+                    float w = 0.f;
+                    for (int c = 0; c < cs; ++c)
+                        w += static_cast<const float*>(__cluster_map_shared_rank(red, (unsigned)c))[2 * a.BN * kGM + kGM + j];
+                    fs.wn2[j] = w;
+                }
+            }
+        }
+        if (cs > 1) cluster_arrive();  // done reading the other CTAs' shared memory
+        __syncthreads();
+        // selection: a warp per row of the CTA's quarters
+        const int nown = (4 - split + cs - 1) / cs;  // quarters this CTA selects
+        for (int i = warp; i < 32 * nown; i += kGWarps) {
+            const int rr = (split + cs * (i >> 5)) * 32 + (i & 31);
+            if (m0 + rr < P.T) select_row(P, fs, lg + rr * kLgStride, rr, m0 + rr, warp, lane);
+        }
+        __syncthreads();
+        // the dispatch's first step, a warp per 32-token block: pair ranks in token order, block histogram
+        if (P.blk_hist != nullptr && warp < nown) {
+            const int qq = split + cs * warp;
+            const int t0 = m0 + qq * 32, ntok = min(32, P.T - t0), E = P.E, k = P.k;
+            if (ntok > 0) {
+                for (int e = lane; e < E; e += 32) fs.running[warp][e] = 0;
+                __syncwarp();
+                rank_pairs_warp([&](int i) { return fs.fidx[qq * 32 + i / k][i % k]; }, ntok * k, fs.running[warp],
+                                P.slot + (size_t)t0 * k, lane);
+                __syncwarp();
+                for (int e = lane; e < E; e += 32) P.blk_hist[(size_t)(t0 / 32) * E + e] = fs.running[warp][e];
+            }
+        }
+        __syncthreads();
         // the dispatch scan runs in the last CTA to finish its blocks' histograms
         if (P.blk_hist != nullptr && P.ticket != nullptr) {
             if (threadIdx.x == 0) {
                 __threadfence();
-                fs.last = atomicAdd(P.ticket, 1) == (int)gridDim.x - 1;
+                fs.last = atomicAdd(P.ticket, 1) == (int)(gridDim.x * gridDim.y) - 1;
                 __threadfence();
             }
             __syncthreads();
@@ -470,6 +529,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
                 if (threadIdx.x == 0) *P.ticket = 0;  // ready for the next call
             }
         }
+        if (cs > 1) cluster_wait();  // no CTA leaves while another may still read its shared memory
     }
 }
 
@@ -478,7 +538,15 @@ __global__ void __launch_bounds__(kGThreads, 1)
 GateGemmPlan gate_gemm_plan(int T, int d, int N0, int N1, int sms, bool fuse_select) {
     GateGemmPlan g{};
     g.fused = fuse_select && N1 == 0 && N0 <= kGMaxBN;
-    if (g.fused) sms = 1;  // one split: the CTA holds every logit of its tokens
+    g.cs = 1;
+    if (g.fused) {
+        // a cluster of cs CTAs per token tile splits K; their float-float partials meet in shared memory,
+        // so the selecting CTA still sees every logit of its tokens.  As many as keep one wave.
+        const long mtiles = (T + kGM - 1) / kGM;
+        for (int c = kGMaxCluster; c > 1; c >>= 1)
+            if (c <= d / kGK && mtiles * c <= sms) { g.cs = c; break; }
+        sms = 1;  // no split-K partials in global memory
+    }
     const int nmax = N0 > N1 ? N0 : N1;
     g.BN = nmax >= kGMaxBN ? kGMaxBN : (nmax + 15) / 16 * 16;
     if (g.BN < 16) g.BN = 16;
@@ -492,13 +560,15 @@ GateGemmPlan gate_gemm_plan(int T, int d, int N0, int N1, int sms, bool fuse_sel
     if (S > kGateMaxSplits) S = kGateMaxSplits;
     if (S > g.kb) S = g.kb;
     if (S < 1) S = 1;
-    g.per = (g.kb + S - 1) / S;
-    g.S = (g.kb + g.per - 1) / g.per;
+    g.per = (g.kb + S * g.cs - 1) / (S * g.cs);
+    g.S = g.fused ? 1 : (g.kb + g.per - 1) / g.per;
     const size_t stage_bytes = kGABytes + (size_t)g.BN * kGK * 2;
-    const size_t fixed = 1024 + 16 + (g.fused ? sizeof(FusedSmem) : 0) + (2 * kGChunks + 1) * 8;
+    const size_t fixed = 1024 + 16 + (g.fused ? sizeof(FusedSmem) + red_bytes(g.BN) : 0) + (2 * kGChunks + 1) * 8;
     g.stages = (int)((200 * 1024 - fixed) / (stage_bytes + 16));
     if (g.stages > kGMaxStages) g.stages = kGMaxStages;
     if (g.stages > g.per) g.stages = g.per < 2 ? 2 : g.per;
+    // the fused selection stages the tile's logits in the stage ring once the K loop is done
+    while (g.fused && (size_t)g.stages * stage_bytes < (size_t)kGM * kLgStride * 4) ++g.stages;
     g.smem = fixed + (size_t)g.stages * (stage_bytes + 16);
     return g;
 }
@@ -533,13 +603,28 @@ cudaError_t launch_gate_gemm(const GateGemmPlan& g, const void* x, const void* w
     a.kb = g.kb;
     a.stages = g.stages;
     a.err = err;
-    dim3 grid(g.mt, g.nt0 + g.nt1, g.S);
+    const dim3 grid = g.fused ? dim3(g.cs, g.mt, 1) : dim3(g.mt, g.nt0 + g.nt1, g.S);
     if (g.fused && sel == nullptr) return cudaErrorInvalidValue;
     const GateParams none{};
     auto go = [&](auto kern, const GateParams& p) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)g.smem);
         if (e != cudaSuccess) return e;
-        return launch_pdl(kern, grid, dim3(kGThreads), g.smem, s, ma, mb0, mb1, a, p);
+        if (!g.fused || g.cs == 1) return launch_pdl(kern, grid, dim3(kGThreads), g.smem, s, ma, mb0, mb1, a, p);
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = grid;
+        cfg.blockDim = dim3(kGThreads);
+        cfg.dynamicSmemBytes = g.smem;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[2];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = (unsigned)g.cs;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 2;
+        return cudaLaunchKernelEx(&cfg, kern, ma, mb0, mb1, a, p);
     };
     cudaError_t e;
     if (g.fused)

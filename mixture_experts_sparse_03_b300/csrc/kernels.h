@@ -71,6 +71,7 @@ struct GateGemmPlan {
     int S;         // splits of K
     int Np;        // logits per token (N0 + N1)
     bool fused;    // selection fused into the GEMM's epilogue (no partials, no selection kernel)
+    int cs;        // fused: CTAs per 128-token tile, a cluster splitting K (partials added in shared memory)
     int stages;    // TMA ring depth
     size_t smem;   // dynamic shared memory per CTA
 };

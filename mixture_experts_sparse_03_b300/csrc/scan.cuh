@@ -42,20 +42,50 @@ struct ScanSmem {
     int* wsum;     // [33]
 };
 
+// The block's global stores all come after its last barrier when E <= blockDim.x (one chunk of experts):
+// a barrier that follows stores to global memory costs the block a round trip to L2.
 __device__ __forceinline__ void scan_experts(int* blk_hist, int nblk, int E, int C, int* count, int* offset,
                                              int* row_token, float* row_gate, const ScanSmem& sm) {
     constexpr int R = 16;  // block rows a thread keeps in registers between reading and writing them
     const int NT = blockDim.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const bool one_chunk = E <= NT;
+    int v[R];
+    int e = 0, b0 = 0, b1 = 0, run0 = 0;
+    bool active = false, last_group = false;
+    // thread (g, e) writes the exclusive prefixes of expert e over blocks [b0, b1) (v: the first R counts)
+    auto write_back = [&]() {
+        int run = run0;
+#pragma unroll
+        for (int j = 0; j < R; ++j)
+            if (b0 + j < b1) {
+                blk_hist[(size_t)(b0 + j) * E + e] = run;
+                run += v[j];
+            }
+        for (int i0 = b0 + R; i0 < b1; i0 += 8) {
+            int w[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) w[j] = i0 + j < b1 ? __ldcg(blk_hist + (size_t)(i0 + j) * E + e) : 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (i0 + j < b1) {
+                    blk_hist[(size_t)(i0 + j) * E + e] = run;
+                    run += w[j];
+                }
+        }
+        if (last_group) count[e] = run;
+    };
     // per chunk of up to NT experts: thread (g, e) owns expert e over the g-th run of `per` blocks, so
     // a warp reads consecutive experts of one block row (coalesced), all of its rows in flight at once
     for (int e0 = 0; e0 < E; e0 += NT) {
         const int ne = min(NT, E - e0);
         const int G = max(1, min(nblk, NT / ne));
         const int per = (nblk + G - 1) / G;
-        const int g = tid / ne, e = e0 + tid % ne;
-        const bool active = g < G;
-        const int b0 = active ? min(nblk, g * per) : nblk, b1 = active ? min(nblk, b0 + per) : nblk;
-        int v[R];
+        const int g = tid / ne;
+        e = e0 + tid % ne;
+        active = g < G;
+        last_group = g == G - 1;
+        b0 = active ? min(nblk, g * per) : nblk;
+        b1 = active ? min(nblk, b0 + per) : nblk;
         int s = 0;
 #pragma unroll
         for (int j = 0; j < R; ++j) v[j] = b0 + j < b1 ? __ldcg(blk_hist + (size_t)(b0 + j) * E + e) : 0;
@@ -78,30 +108,13 @@ __device__ __forceinline__ void scan_experts(int* blk_hist, int nblk, int E, int
             __syncthreads();
         }
         if (active) {
-            int run = sm.part[tid] - s;  // blocks of this expert before b0
-#pragma unroll
-            for (int j = 0; j < R; ++j)
-                if (b0 + j < b1) {
-                    blk_hist[(size_t)(b0 + j) * E + e] = run;
-                    run += v[j];
-                }
-            for (int i0 = b0 + R; i0 < b1; i0 += 8) {
-                int w[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) w[j] = i0 + j < b1 ? __ldcg(blk_hist + (size_t)(i0 + j) * E + e) : 0;
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    if (i0 + j < b1) {
-                        blk_hist[(size_t)(i0 + j) * E + e] = run;
-                        run += w[j];
-                    }
-            }
-            if (g == G - 1) {
-                count[e] = run;
-                const int kept = min(run, C);
+            run0 = sm.part[tid] - s;  // blocks of this expert before b0
+            if (last_group) {
+                const int kept = min(sm.part[tid], C);
                 sm.kept[e] = kept;
                 sm.padded[e] = (kept + kRowAlign - 1) / kRowAlign * kRowAlign;
             }
+            if (!one_chunk) write_back();  // the registers serve the next chunk
         }
         __syncthreads();
     }
@@ -126,11 +139,13 @@ __device__ __forceinline__ void scan_experts(int* blk_hist, int nblk, int E, int
         if (lane == 31) sm.padded[E] = inc;
     }
     __syncthreads();
+    // global stores only from here on
+    if (one_chunk && active) write_back();
     for (int q = tid; q <= E; q += NT) offset[q] = sm.padded[q];
     for (int i = tid; i < E * kRowAlign; i += NT) {
-        const int e = i / kRowAlign;
-        const int r = sm.padded[e] + sm.kept[e] + i % kRowAlign;
-        if (r < sm.padded[e + 1]) {
+        const int ee = i / kRowAlign;
+        const int r = sm.padded[ee] + sm.kept[ee] + i % kRowAlign;
+        if (r < sm.padded[ee + 1]) {
             row_token[r] = -1;
             row_gate[r] = 0.f;
         }
