@@ -74,5 +74,35 @@ __device__ __forceinline__ double warp_dot_ff(const T* a, const T* b, int d, int
     return (double)hi[0] + (double)lo[0];
 }
 
+// float-float dot products of one length-d row a with up to four rows b[0..nb) by one warp: the loads of
+// all rows' slices are in flight together (one round of memory latency for all of them, not nb rounds)
+template <typename T>
+__device__ __forceinline__ void warp_dot_ff4(const T* a, const T* const (&b)[4], int nb, int d, int lane,
+                                             double (&out)[4]) {
+    float hi[4] = {0.f, 0.f, 0.f, 0.f}, lo[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int i = lane * 8; i < d; i += 32 * 8) {
+        float va[8], vb[4][8];
+        load8(a + i, va);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            if (u < nb) {
+                load8(b[u] + i, vb[u]);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) vb[u][j] = 0.f;
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+#pragma unroll
+            for (int u = 0; u < 4; ++u) ff_acc<T>(hi[u], lo[u], va[j], vb[u][j]);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        ff_warp_sum(hi[u], lo[u]);
+        out[u] = (double)hi[u] + (double)lo[u];
+    }
+}
+
 }  // namespace gate
 }  // namespace moe

@@ -168,10 +168,16 @@ __device__ __forceinline__ void select_row(const GateParams& P, FusedSmem& fs, c
     if (c1) fs.cand[w][n0 + __popc(m1b & lanemask_lt())] = lane + 32;
     __syncwarp();
     const bf16_t* xr = static_cast<const bf16_t*>(P.x) + (size_t)t * P.d;
-    for (int c = 0; c < cnt; ++c) {
-        const double v = gate::warp_dot_ff<bf16_t>(
-            xr, static_cast<const bf16_t*>(P.w_gate) + (size_t)fs.cand[w][c] * P.d, P.d, lane);
-        if (lane == 0) fs.ex[w][c] = v;
+    for (int c0 = 0; c0 < cnt; c0 += 4) {  // four contenders per pass, their loads in flight together
+        const int nb = min(4, cnt - c0);
+        const bf16_t* rows[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            rows[u] = static_cast<const bf16_t*>(P.w_gate) + (size_t)fs.cand[w][c0 + min(u, nb - 1)] * P.d;
+        double v[4];
+        gate::warp_dot_ff4<bf16_t>(xr, rows, nb, P.d, lane, v);
+        if (lane == 0)
+            for (int u = 0; u < nb; ++u) fs.ex[w][c0 + u] = v[u];
     }
     __syncwarp();
     // k rounds of a warp argmax over the contenders' exact scores (equal scores -> lower expert id)
@@ -467,17 +473,31 @@ __global__ void __launch_bounds__(kGThreads, 1)
         if (warp >= 2 && warp < 6 && q % cs == split) {
             const int r = q * 32 + lane;
             float xs = red[2 * a.BN * kGM + r];
+            // generic pointers into the other CTAs' shared memory (rank order): plain loads the compiler can
+            // issue together
+            const int np = cs - 1;  // peer u is CTA u, or u + 1 from this CTA's rank on
+            const float* rp[kGMaxCluster - 1];
 #pragma unroll
-            for (int c = 0; c < kGMaxCluster; ++c) {
-                if (c >= cs) break;
-                if (c == split) continue;
-                // generic pointers into another CTA's shared memory: plain loads the compiler can batch
-                const float* rr = static_cast<const float*>(__cluster_map_shared_rank(red, (unsigned)c));
+            for (int u = 0; u < kGMaxCluster - 1; ++u)
+                rp[u] = static_cast<const float*>(
+                    __cluster_map_shared_rank(red, (unsigned)min(u < split ? u : u + 1, cs - 1)));
 #pragma unroll
-                for (int j = 0; j < BNC; ++j)
-                    if (j < a.BN) ff_add(hi[j], lo[j], rr[j * kGM + r], rr[(a.BN + j) * kGM + r]);
-                xs += rr[2 * a.BN * kGM + r];
-            }
+            for (int j = 0; j < BNC; ++j)
+                if (j < a.BN) {
+                    float ph[kGMaxCluster - 1], pl[kGMaxCluster - 1];
+#pragma unroll
+                    for (int u = 0; u < kGMaxCluster - 1; ++u)
+                        if (u < np) {
+                            ph[u] = rp[u][j * kGM + r];
+                            pl[u] = rp[u][(a.BN + j) * kGM + r];
+                        }
+#pragma unroll
+                    for (int u = 0; u < kGMaxCluster - 1; ++u)
+                        if (u < np) ff_add(hi[j], lo[j], ph[u], pl[u]);
+                }
+#pragma unroll
+            for (int u = 0; u < kGMaxCluster - 1; ++u)
+                if (u < np) xs += rp[u][2 * a.BN * kGM + r];
 #pragma unroll
             for (int j = 0; j < BNC; ++j)
                 if (j < a.BN) lg[r * kLgStride + j] = hi[j] + lo[j];
