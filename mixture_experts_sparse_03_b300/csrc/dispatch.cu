@@ -92,6 +92,15 @@ __global__ void __launch_bounds__(32 * kGatherWarps) gather_kernel(
     const long p = (long)blockIdx.x * kGatherWarps + (threadIdx.x >> 5);
     if (p < npairs) {
         const int t = (int)(p / k);
+        constexpr int V = 16 / sizeof(T);
+        const int nv = d / V;
+        const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * d);
+        // the token's row is known before its routing: its first 8 x 32 16-byte pieces are loaded while
+        // the pair's expert, rank and block prefix are still on their way
+        uint4 v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (lane + j * 32 < nv) v[j] = __ldg(src + lane + j * 32);
         const int e = topk_idx[p];
         const int rk = slot[p];  // the block rank, replaced by the slot below
         int s = -1, r = -1;
@@ -109,18 +118,18 @@ __global__ void __launch_bounds__(32 * kGatherWarps) gather_kernel(
             }
         }
         if (r >= 0) {
-            constexpr int V = 16 / sizeof(T);
-            const int nv = d / V;
-            const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * d);
             uint4* dst = reinterpret_cast<uint4*>(xd + (size_t)r * d);
-            for (int i0 = lane; i0 < nv; i0 += 8 * 32) {
-                uint4 v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (lane + j * 32 < nv) dst[lane + j * 32] = v[j];
+            for (int i0 = lane + 8 * 32; i0 < nv; i0 += 8 * 32) {  // rows longer than 4 KiB
+                uint4 w[8];
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
-                    if (i0 + j * 32 < nv) v[j] = __ldg(src + i0 + j * 32);
+                    if (i0 + j * 32 < nv) w[j] = __ldg(src + i0 + j * 32);
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
-                    if (i0 + j * 32 < nv) dst[i0 + j * 32] = v[j];
+                    if (i0 + j * 32 < nv) dst[i0 + j * 32] = w[j];
             }
         }
     }

@@ -51,7 +51,7 @@ __host__ __device__ inline SelLayout sel_layout(int gate, int E, int p, int stag
     L.logits = take(4 * (size_t)kBT * N, 16);
     L.sc = take(cos ? 4 * (size_t)kBT * E : 0, 16);
     L.wn2 = take(4 * (size_t)N, 16);
-    L.embs = take(stage ? 4 * (size_t)p * E : 0, 16);
+    L.embs = take(stage ? 4 * (size_t)p * (E + 1) : 0, 16);
     L.embn = take(cos ? 4 * (size_t)E : 0, 16);
     L.selv = take(4 * kBT * kSel, 16);
     L.seli = take(4 * kBT * kSel, 16);
@@ -101,14 +101,18 @@ __global__ void __launch_bounds__(kSelThreads) gate_select_kernel(const GatePara
                 float v[8];
                 load8(emb + (size_t)e * P.p + j, v);
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    s = fmaf(v[q], v[q], s);
-                    if (stage) embs[(j + q) * E + e] = v[q];
-                }
+                for (int q = 0; q < 8; ++q) s = fmaf(v[q], v[q], s);
             }
             s = warp_sum(s);
             if (lane == 0) embn[e] = sqrtf(s);
         }
+        // the embeddings transposed into shared memory, rows padded to E + 1 so that neither these
+        // stores (consecutive threads: consecutive j) nor the score loop's loads (lanes: experts) conflict
+        if (stage)
+            for (int i = tid; i < P.p * E; i += kSelThreads) {
+                const int e = i / P.p, j = i - e * P.p;
+                embs[j * (E + 1) + e] = load1(emb + (size_t)e * P.p + j);
+            }
     }
     __syncthreads();
 
@@ -187,11 +191,28 @@ __global__ void __launch_bounds__(kSelThreads) gate_select_kernel(const GatePara
             const T* emb = static_cast<const T*>(P.emb);
             for (int e = lane; e < E; e += 32) {
                 float dot = 0.f;
+                // four interleaved partial sums (p is a multiple of 8): u is read four components at a
+                // time (one broadcast 16-byte load) and the four FMA chains overlap; the error stays
+                // within the (2p + 8) u bound of a p-term dot product
+                float d4[4] = {0.f, 0.f, 0.f, 0.f};
                 if (stage) {
-                    for (int j = 0; j < p; ++j) dot = fmaf(Lr[j], embs[j * E + e], dot);
+#pragma unroll 2
+                    for (int j = 0; j < p; j += 4) {
+                        const float4 u4 = *reinterpret_cast<const float4*>(Lr + j);
+                        d4[0] = fmaf(u4.x, embs[(j + 0) * (E + 1) + e], d4[0]);
+                        d4[1] = fmaf(u4.y, embs[(j + 1) * (E + 1) + e], d4[1]);
+                        d4[2] = fmaf(u4.z, embs[(j + 2) * (E + 1) + e], d4[2]);
+                        d4[3] = fmaf(u4.w, embs[(j + 3) * (E + 1) + e], d4[3]);
+                    }
                 } else {
-                    for (int j = 0; j < p; ++j) dot = fmaf(Lr[j], load1(emb + (size_t)e * p + j), dot);
+                    for (int j = 0; j < p; j += 8) {
+                        float ev[8];
+                        load8(emb + (size_t)e * p + j, ev);
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) d4[q & 3] = fmaf(Lr[j + q], ev[q], d4[q & 3]);
+                    }
                 }
+                dot = (d4[0] + d4[1]) + (d4[2] + d4[3]);
                 const float s = dot / (nuc * fmaxf(embn[e], 1e-12f)) * P.inv_temp;
                 sc[e] = s;
                 dmax = fmaxf(dmax, rel * P.inv_temp + 4.f * kU * fabsf(s));
