@@ -43,7 +43,10 @@ def kernel_names(wl, launches: int):
     """Names of the kernels moe_forward launches, in launch order (the softmax gate of a bf16 layer with
     E <= 64 runs as one fused launch)."""
     if wl.dtype == "bf16" and wl.gate == "softmax" and wl.E <= 64:
-        names = ["gate_fused_gemm_topk_scan", "dispatch_gather", "expert_up_gelu"]
+        if -(-wl.T // 32) * wl.E <= 2048:  # a small histogram: the gather scans it (per CTA)
+            names = ["gate_fused_gemm_topk", "dispatch_scan_gather", "expert_up_gelu"]
+        else:
+            names = ["gate_fused_gemm_topk_scan", "dispatch_gather", "expert_up_gelu"]
     elif wl.dtype == "bf16":
         names = ["gate_logits_gemm", "gate_topk"] + (["gate_cos_fold"] if wl.gate == "cosine" else [])
         names += ["gate_rescore", "dispatch_rank_scan", "dispatch_gather", "expert_up_gelu"]

@@ -375,7 +375,8 @@ moe_status moe_dispatch(const moe_config* cfg, const void* x, const int32_t* top
                                     expert_offset, row_token, row_gate, s);
     }));
     return launch(s, [&] {
-        return launch_dispatch_gather(x, P.bf16, topk_idx, topk_gate, hist, expert_offset, P.T, P.k, P.E, P.d, P.Ceff,
+        return launch_dispatch_gather(x, P.bf16, topk_idx, topk_gate, hist, expert_offset, nullptr, false, P.T, P.k,
+                                      P.E, P.d, P.Ceff,
                                       slot, row_token, row_gate, x_dispatched, nullptr, s);
     });
 }
@@ -446,7 +447,10 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const void* w_gate,
     g.blk_hist = hist;
     g.slot = slot;
     g.err = err;
-    g.ticket = err + 2;
+    // a small histogram (fused softmax gate) is scanned by the gather itself, every CTA for its own
+    // blocks: the gate then skips its ticket and last-CTA scan
+    const bool gather_scan = P.bf16 && P.gg.fused && P.E <= kGatherScanMaxE && (int64_t)P.nblk * P.E <= kGatherScanMaxHist;
+    g.ticket = gather_scan ? nullptr : err + 2;
     g.C = P.Ceff;
     g.count = count;
     g.offset = off;
@@ -454,7 +458,8 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const void* w_gate,
     g.row_gate = rgate;
     MOE_TRY(run_gate(P, g, workspace, s));
     MOE_TRY(launch(s, [&] {
-        return launch_dispatch_gather(x, P.bf16, idx, gate, hist, off, P.T, P.k, P.E, P.d, P.Ceff, slot, rtok, rgate,
+        return launch_dispatch_gather(x, P.bf16, idx, gate, hist, off, count, gather_scan, P.T, P.k, P.E, P.d, P.Ceff,
+                                      slot, rtok, rgate,
                                       xd, P.fused ? out : nullptr, s);
     }));
     MOE_TRY(ffn_and_combine(P, cfg, xd, off, rtok, rgate, w1, b1, w2, b2, y, out, P.fused != 0, workspace, s));

@@ -7,7 +7,9 @@
 // Slot of pair (t, e) = number of pairs of earlier tokens routed to e; kept iff slot < C.
 //
 // Three steps over blocks of 32 tokens (the gate kernels' blocks: the fp32 gate kernel and the fused
-// bf16 gate do step 1 on their own tokens and run step 2 in their last block, see scan.cuh):
+// bf16 gate do step 1 on their own tokens and run step 2 in their last block, see scan.cuh; when the
+// histogram is small -- the fused gate's usual case -- every gather CTA does step 2's work for its own
+// blocks instead, and the gate skips it):
 //   rank    a warp per block, 32 blocks per CTA: each pair's rank among the block's pairs of the same
 //           expert, in token order (kept in `slot` until the gather), and the block's expert histogram
 //           blk_hist[b][e]; the last CTA to finish runs the scan
@@ -28,6 +30,7 @@ namespace {
 constexpr int kBT = kTokensPerBlock;
 constexpr int kGatherWarps = 8;  // warps (pairs) per gather block
 constexpr int kRankWarps = 32;   // token blocks per rank CTA, a warp each
+static_assert(kGatherWarps <= kBT, "a gather CTA's pairs span at most two token blocks");
 
 __global__ void __launch_bounds__(32 * kRankWarps) rank_kernel(const int* __restrict__ topk_idx, int T, int k,
                                                               int E, int* __restrict__ blk_hist,
@@ -79,35 +82,112 @@ __global__ void __launch_bounds__(32 * kRankWarps) rank_kernel(const int* __rest
     }
 }
 
-template <typename T>
+// SCAN: blk_hist holds each block's raw expert histogram and every CTA derives what it needs itself
+// (E <= kGatherScanMaxE): the prefix of its one or two token blocks, the expert totals and the padded
+// segment offsets; CTA 0 writes count and offset, CTA c writes the padding rows of experts c, c + grid,
+// ...  Otherwise blk_hist holds the scanned prefixes and offset the segment offsets.
+template <typename T, bool SCAN>
 __global__ void __launch_bounds__(32 * kGatherWarps) gather_kernel(
     const T* __restrict__ x, const int* __restrict__ topk_idx, const float* __restrict__ topk_gate,
-    const int* __restrict__ blk_base, const int* __restrict__ offset, int T_, int k, int E, int d, int C,
-    int* __restrict__ slot, int* __restrict__ row_token, float* __restrict__ row_gate, T* __restrict__ xd,
-    float* __restrict__ out_zero) {
+    const int* __restrict__ blk_hist, int* __restrict__ offset, int* __restrict__ count, int T_, int k, int E,
+    int d, int C, int* __restrict__ slot, int* __restrict__ row_token, float* __restrict__ row_gate,
+    T* __restrict__ xd, float* __restrict__ out_zero) {
+    __shared__ int s_pre[2][kGatherScanMaxE];  // prefix of blocks b_lo and b_lo + 1
+    __shared__ int s_off[kGatherScanMaxE + 1];
+    __shared__ int s_kept[kGatherScanMaxE];
+    __shared__ int s_part[3][32 * kGatherWarps];
     pdl_wait();
     pdl_trigger();
-    const int lane = threadIdx.x & 31;
+    const int lane = threadIdx.x & 31, tid = threadIdx.x;
     const long npairs = (long)T_ * k;
     const long p = (long)blockIdx.x * kGatherWarps + (threadIdx.x >> 5);
+    const int t = p < npairs ? (int)(p / k) : 0;
+    constexpr int V = 16 / sizeof(T);
+    const int nv = d / V;
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * d);
+    // the token's row is known before its routing: its first 8 x 32 16-byte pieces are loaded while the
+    // pair's expert, rank and block prefix are still on their way
+    uint4 v[8];
     if (p < npairs) {
-        const int t = (int)(p / k);
-        constexpr int V = 16 / sizeof(T);
-        const int nv = d / V;
-        const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * d);
-        // the token's row is known before its routing: its first 8 x 32 16-byte pieces are loaded while
-        // the pair's expert, rank and block prefix are still on their way
-        uint4 v[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j)
             if (lane + j * 32 < nv) v[j] = __ldg(src + lane + j * 32);
+    }
+    const int b_lo = (int)(((long)blockIdx.x * kGatherWarps / k) / kBT);
+    if constexpr (SCAN) {
+        // thread (g, e) sums rows g, g + G, ... of the histogram: those before b_lo, row b_lo, and all
+        const int nblk = (T_ + kBT - 1) / kBT;
+        const int G = (32 * kGatherWarps) / E, g = tid / E, e = tid - g * E;
+        int lo = 0, mid = 0, tot = 0;
+        if (g < G) {
+            for (int b = g; b < nblk; b += G) {
+                const int c = blk_hist[(size_t)b * E + e];
+                tot += c;
+                lo += b < b_lo ? c : 0;
+                mid += b == b_lo ? c : 0;
+            }
+        }
+        s_part[0][tid] = lo;
+        s_part[1][tid] = mid;
+        s_part[2][tid] = tot;
+        __syncthreads();
+        if (tid < E) {
+            int a = 0, m = 0, n = 0;
+            for (int gg = 0; gg < G; ++gg) {
+                a += s_part[0][gg * E + tid];
+                m += s_part[1][gg * E + tid];
+                n += s_part[2][gg * E + tid];
+            }
+            s_pre[0][tid] = a;
+            s_pre[1][tid] = a + m;
+            const int kept = min(n, C);
+            s_kept[tid] = kept;
+            s_off[tid] = (kept + kRowAlign - 1) / kRowAlign * kRowAlign;  // padded size, scanned below
+            if (blockIdx.x == 0 && count != nullptr) count[tid] = n;
+        }
+        __syncthreads();
+        if (tid < 32) {  // exclusive scan of the padded sizes (E <= 64: two per lane)
+            const int i0 = 2 * lane, i1 = 2 * lane + 1;
+            const int a0 = i0 < E ? s_off[i0] : 0, a1 = i1 < E ? s_off[i1] : 0;
+            int inc = a0 + a1;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int u = __shfl_up_sync(0xffffffffu, inc, o);
+                if (lane >= o) inc += u;
+            }
+            const int ex = inc - a0 - a1;
+            __syncwarp();
+            if (i0 < E) s_off[i0] = ex;
+            if (i1 < E) s_off[i1] = ex + a0;
+            if (lane == 31) s_off[E] = inc;
+        }
+        __syncthreads();
+        if (blockIdx.x == 0)
+            for (int q = tid; q <= E; q += 32 * kGatherWarps) offset[q] = s_off[q];
+        for (int c = blockIdx.x; c < E; c += gridDim.x)  // padding rows of expert c
+            for (int i = tid; i < kRowAlign; i += 32 * kGatherWarps) {
+                const int r = s_off[c] + s_kept[c] + i;
+                if (r < s_off[c + 1]) {
+                    row_token[r] = -1;
+                    row_gate[r] = 0.f;
+                }
+            }
+    }
+    if (p < npairs) {
         const int e = topk_idx[p];
         const int rk = slot[p];  // the block rank, replaced by the slot below
         int s = -1, r = -1;
         if (rk >= 0 && e >= 0 && e < E) {
-            s = blk_base[(size_t)(t / kBT) * E + e] + rk;
-            if (s < C) r = offset[e] + s;
-            else s = -1;
+            const int b = t / kBT;
+            if constexpr (SCAN) {
+                s = s_pre[b - b_lo][e] + rk;  // a CTA's 8 pairs span at most two token blocks
+                if (s < C) r = s_off[e] + s;
+                else s = -1;
+            } else {
+                s = blk_hist[(size_t)b * E + e] + rk;
+                if (s < C) r = offset[e] + s;
+                else s = -1;
+            }
         }
         __syncwarp();
         if (lane == 0) {
@@ -158,19 +238,30 @@ cudaError_t launch_dispatch_rank(const int* topk_idx, int T, int k, int E, int* 
 }
 
 cudaError_t launch_dispatch_gather(const void* x, int bf16, const int* topk_idx, const float* topk_gate,
-                                   const int* blk_base, const int* offset, int T, int k, int E, int d, int C,
-                                   int* slot, int* row_token, float* row_gate, void* x_dispatched,
+                                   const int* blk_hist, int* offset, int* count, bool scan, int T, int k, int E,
+                                   int d, int C, int* slot, int* row_token, float* row_gate, void* x_dispatched,
                                    float* out_to_zero, cudaStream_t s) {
     if (T <= 0) return cudaSuccess;
+    if (scan && E > kGatherScanMaxE) return cudaErrorInvalidValue;
     const long npairs = (long)T * k;
     const unsigned blocks = (unsigned)((npairs + kGatherWarps - 1) / kGatherWarps);
-    if (bf16)
-        return launch_pdl(gather_kernel<bf16_t>, dim3(blocks), dim3(32 * kGatherWarps), 0, s,
-                          static_cast<const bf16_t*>(x), topk_idx, topk_gate, blk_base, offset, T, k, E, d, C, slot,
-                          row_token, row_gate, static_cast<bf16_t*>(x_dispatched), out_to_zero);
-    return launch_pdl(gather_kernel<float>, dim3(blocks), dim3(32 * kGatherWarps), 0, s,
-                      static_cast<const float*>(x), topk_idx, topk_gate, blk_base, offset, T, k, E, d, C, slot,
-                      row_token, row_gate, static_cast<float*>(x_dispatched), out_to_zero);
+    const dim3 grid(blocks), block(32 * kGatherWarps);
+    if (bf16) {
+        auto xp = static_cast<const bf16_t*>(x);
+        auto xo = static_cast<bf16_t*>(x_dispatched);
+        if (scan)
+            return launch_pdl(gather_kernel<bf16_t, true>, grid, block, 0, s, xp, topk_idx, topk_gate, blk_hist,
+                              offset, count, T, k, E, d, C, slot, row_token, row_gate, xo, out_to_zero);
+        return launch_pdl(gather_kernel<bf16_t, false>, grid, block, 0, s, xp, topk_idx, topk_gate, blk_hist, offset,
+                          count, T, k, E, d, C, slot, row_token, row_gate, xo, out_to_zero);
+    }
+    auto xp = static_cast<const float*>(x);
+    auto xo = static_cast<float*>(x_dispatched);
+    if (scan)
+        return launch_pdl(gather_kernel<float, true>, grid, block, 0, s, xp, topk_idx, topk_gate, blk_hist, offset,
+                          count, T, k, E, d, C, slot, row_token, row_gate, xo, out_to_zero);
+    return launch_pdl(gather_kernel<float, false>, grid, block, 0, s, xp, topk_idx, topk_gate, blk_hist, offset,
+                      count, T, k, E, d, C, slot, row_token, row_gate, xo, out_to_zero);
 }
 
 }  // namespace moe

@@ -83,7 +83,8 @@ moe_status moe_dispatch_static_scratch(const moe_config* cfg, const void* x, con
     if (launch_dispatch_rank(topk_idx, T, k, E, hist, slot, err, err + 2, Ceff, expert_count, expert_offset,
                              row_token, row_gate, s) != cudaSuccess)
         return MOE_ERR_CUDA;
-    if (launch_dispatch_gather(x, bf16, topk_idx, topk_gate, hist, expert_offset, T, k, E, d, Ceff, slot, row_token,
+    if (launch_dispatch_gather(x, bf16, topk_idx, topk_gate, hist, expert_offset, nullptr, false, T, k, E, d, Ceff,
+                               slot, row_token,
                                row_gate, x_dispatched, nullptr, s) != cudaSuccess)
         return MOE_ERR_CUDA;
     return MOE_OK;

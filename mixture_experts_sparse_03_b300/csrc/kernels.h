@@ -92,9 +92,14 @@ cudaError_t launch_dispatch_rank(const int* topk_idx, int T, int k, int E, int* 
                                  int* ticket, int C, int* count, int* offset, int* row_token, float* row_gate,
                                  cudaStream_t s);
 // slot [T, k] holds the block ranks on entry (from the rank step or the gate kernel) and the slots on exit
+// scan = false: blk_hist holds the scanned block prefixes and offset the segment offsets (from the rank
+// step's scan); scan = true (E <= kGatherScanMaxE): blk_hist holds the raw block histograms and the
+// gather does the scan's work itself -- it writes count (if not null), offset and the padding rows
+constexpr int kGatherScanMaxE = 64;
+constexpr int kGatherScanMaxHist = 2048;  // ints of histogram every gather CTA reads
 cudaError_t launch_dispatch_gather(const void* x, int bf16, const int* topk_idx, const float* topk_gate,
-                                   const int* blk_base, const int* offset, int T, int k, int E, int d, int C,
-                                   int* slot, int* row_token, float* row_gate, void* x_dispatched,
+                                   const int* blk_hist, int* offset, int* count, bool scan, int T, int k, int E,
+                                   int d, int C, int* slot, int* row_token, float* row_gate, void* x_dispatched,
                                    float* out_to_zero, cudaStream_t s);
 
 // ---- expert FFN -------------------------------------------------------------------------------
