@@ -108,10 +108,15 @@ __global__ void __launch_bounds__(32 * kGatherWarps) gather_kernel(
     // the token's row is known before its routing: its first 8 x 32 16-byte pieces are loaded while the
     // pair's expert, rank and block prefix are still on their way
     uint4 v[8];
+    int e = -1, rk = -1;
+    float gv = 0.f;
     if (p < npairs) {
 #pragma unroll
         for (int j = 0; j < 8; ++j)
             if (lane + j * 32 < nv) v[j] = __ldg(src + lane + j * 32);
+        e = topk_idx[p];
+        rk = slot[p];  // the block rank, replaced by the slot below
+        gv = topk_gate[p];
     }
     const int b_lo = (int)(((long)blockIdx.x * kGatherWarps / k) / kBT);
     if constexpr (SCAN) {
@@ -174,8 +179,6 @@ __global__ void __launch_bounds__(32 * kGatherWarps) gather_kernel(
             }
     }
     if (p < npairs) {
-        const int e = topk_idx[p];
-        const int rk = slot[p];  // the block rank, replaced by the slot below
         int s = -1, r = -1;
         if (rk >= 0 && e >= 0 && e < E) {
             const int b = t / kBT;
@@ -194,7 +197,7 @@ __global__ void __launch_bounds__(32 * kGatherWarps) gather_kernel(
             slot[p] = s;
             if (r >= 0) {
                 row_token[r] = t;
-                row_gate[r] = topk_gate[p];
+                row_gate[r] = gv;
             }
         }
         if (r >= 0) {
