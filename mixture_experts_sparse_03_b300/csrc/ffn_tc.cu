@@ -35,6 +35,12 @@ constexpr uint32_t kBBytes = kBN * kBK * 2;           // 32 KiB
 constexpr uint32_t kStageBytes = kABytes + kBBytes;   // 48 KiB
 constexpr uint32_t kTmemCols = 2 * kBN;               // 512
 
+// the epilogue warps' bias buffers follow the ints that start at s_off, 16-byte aligned
+__device__ __forceinline__ void* smem_bias_base(int* s_off, int nints) {
+    return reinterpret_cast<void*>((reinterpret_cast<uintptr_t>(s_off + nints) + 15) & ~uintptr_t(15));
+}
+constexpr size_t kBiasSmem = 4 * kBN * sizeof(float) + 16;  // 4 epilogue warps x kBN floats, + alignment
+
 struct TcArgs {
     const int* offset;
     const int* row_token;
@@ -55,7 +61,7 @@ using namespace tc;
 //   mode 2: + b2, times the row's gate, fp32 atomic add into out[tok] (fused combine)
 // All lanes of the warp call this (tcgen05.ld is warp-wide); rows with tok < 0 store nothing.
 __device__ __forceinline__ void epilogue_cols(const TcArgs& a, uint32_t taddr, int r, int tok, float g,
-                                              const bf16_t* bias, int n0, int c_begin, int c_end) {
+                                              const float* sbias, int n0, int c_begin, int c_end) {
     for (int c0 = c_begin; c0 < c_end; c0 += 32) {
         uint32_t v[32];
         __syncwarp();
@@ -65,13 +71,14 @@ __device__ __forceinline__ void epilogue_cols(const TcArgs& a, uint32_t taddr, i
         float f[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
-        if (bias) {
+        if (sbias) {  // the tile's bias slice, staged in shared memory (all lanes read the same words)
 #pragma unroll
-            for (int j = 0; j < 32; j += 8) {
-                float bb[8];
-                load8(bias + n + j, bb);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) f[j + i] += bb[i];
+            for (int j = 0; j < 32; j += 4) {
+                const float4 bb = *reinterpret_cast<const float4*>(sbias + c0 + j);
+                f[j] += bb.x;
+                f[j + 1] += bb.y;
+                f[j + 2] += bb.z;
+                f[j + 3] += bb.w;
             }
         }
         if (a.mode == 0) {
@@ -98,6 +105,25 @@ __device__ __forceinline__ void epilogue_cols(const TcArgs& a, uint32_t taddr, i
     }
 }
 
+// One warp stages the bias slice of a tile (kBN columns from n0 of expert e's bias) as fp32 in its own
+// shared-memory buffer: eight columns per lane, one 16-byte load each (N is a multiple of 64).
+__device__ __forceinline__ const float* stage_bias(const TcArgs& a, float* wbias, int e, int n0, int lane) {
+    if (a.bias == nullptr) return nullptr;
+    const int n = n0 + lane * 8;
+    float bb[8];
+    if (n < a.N) {
+        load8(a.bias + (size_t)e * a.N + n, bb);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) bb[i] = 0.f;
+    }
+    __syncwarp();  // the previous tile's reads of the buffer are done
+    *reinterpret_cast<float4*>(wbias + lane * 8) = make_float4(bb[0], bb[1], bb[2], bb[3]);
+    *reinterpret_cast<float4*>(wbias + lane * 8 + 4) = make_float4(bb[4], bb[5], bb[6], bb[7]);
+    __syncwarp();
+    return wbias;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const TcArgs a) {
     extern __shared__ uint8_t smem_raw[];
@@ -110,6 +136,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 5);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
     int* s_off = reinterpret_cast<int*>(tmem_holder + 4);
+    float* s_bias = reinterpret_cast<float*>(smem_bias_base(s_off, a.E + 1));  // [4 warps][kBN]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     auto bar = [&](int i) { return smem_u32(bars + i); };
@@ -222,6 +249,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
             const int acc = local & 1;
             const uint32_t acc_phase = (local >> 1) & 1;
+            // the tile's rows, tokens, gates and bias are fetched while its accumulator is still being filled
+            const int m0 = (tile / n_tiles) * kBM, n0 = (tile % n_tiles) * kBN;
+            const int e = expert_of_row(s_off, a.E, m0);
+            const int r = m0 + row;
+            const int tok = a.row_token[r];
+            const float g = (a.mode == 2 && tok >= 0) ? a.row_gate[r] : 0.f;
+            const float* sb = stage_bias(a, s_bias + q * kBN, e, n0, lane);
             const bool ok = __all_sync(0xffffffffu, mbar_wait(bar(TFULL + acc), acc_phase, abort_flag));
             if (!ok) {
                 if (lane == 0) {
@@ -231,13 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             fence_after();
-            const int m0 = (tile / n_tiles) * kBM, n0 = (tile % n_tiles) * kBN;
-            const int e = expert_of_row(s_off, a.E, m0);
-            const int r = m0 + row;
-            const int tok = a.row_token[r];
-            const float g = (a.mode == 2 && tok >= 0) ? a.row_gate[r] : 0.f;
-            const bf16_t* bias = a.bias ? a.bias + (size_t)e * a.N : nullptr;
-            epilogue_cols(a, tmem_base + lane_base + (uint32_t)(acc * kBN), r, tok, g, bias, n0, 0, kBN);
+            epilogue_cols(a, tmem_base + lane_base + (uint32_t)(acc * kBN), r, tok, g, sb, n0, 0, kBN);
             fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(TEMPTY + acc));
@@ -289,6 +317,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
     int* s_off = reinterpret_cast<int*>(tmem_holder + 4);
     int* s_tp = s_off + (a.E + 1);  // first 256-row tile of each expert (prefix), E + 1 entries
+    float* s_bias = reinterpret_cast<float*>(smem_bias_base(s_off, 2 * (a.E + 1)));  // [4 warps][kBN]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();
@@ -411,6 +440,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int tile = pair_id; tile < num_tiles; tile += num_pairs, ++local) {
             const int acc = local & 1;
             const uint32_t acc_phase = (local >> 1) & 1;
+            // the tile's rows, tokens, gates and bias are fetched while its accumulator is still being filled
+            int e, m0, n0;
+            pair_tile(s_tp, s_off, a.E, n_tiles, tile, e, m0, n0);
+            const int r = m0 + 128 * (int)rank + row;
+            const int tok = r < s_off[e + 1] ? a.row_token[r] : -1;  // beyond the segment: discarded
+            const float g = (a.mode == 2 && tok >= 0) ? a.row_gate[r] : 0.f;
+            const float* sb = stage_bias(a, s_bias + q * kBN, e, n0, lane);
             const bool ok = __all_sync(0xffffffffu, mbar_wait_cluster(bar(TFULL + acc), acc_phase, abort_flag));
             if (!ok) {
                 if (lane == 0) {
@@ -420,13 +456,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 break;
             }
             fence_after();
-            int e, m0, n0;
-            pair_tile(s_tp, s_off, a.E, n_tiles, tile, e, m0, n0);
-            const int r = m0 + 128 * (int)rank + row;
-            const int tok = r < s_off[e + 1] ? a.row_token[r] : -1;  // beyond the segment: discarded
-            const float g = (a.mode == 2 && tok >= 0) ? a.row_gate[r] : 0.f;
-            const bf16_t* bias = a.bias ? a.bias + (size_t)e * a.N : nullptr;
-            epilogue_cols(a, tmem_base + lane_base + (uint32_t)(acc * kBN), r, tok, g, bias, n0, 0, kBN);
+            epilogue_cols(a, tmem_base + lane_base + (uint32_t)(acc * kBN), r, tok, g, sb, n0, 0, kBN);
             fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(tempty0 + 8u * (uint32_t)acc);
@@ -536,11 +566,11 @@ int device_sm_count() {
 }
 
 size_t ffn_tc_smem_bytes(int E) {
-    return 1024 + (size_t)kStages * kStageBytes + (2 * kStages + 5) * 8 + 16 + 4 * (size_t)(E + 1);
+    return 1024 + (size_t)kStages * kStageBytes + (2 * kStages + 5) * 8 + 16 + 4 * (size_t)(E + 1) + kBiasSmem;
 }
 
 size_t ffn_tc_pair_smem_bytes(int E) {
-    return 1024 + (size_t)k2Stages * k2StageBytes + (2 * k2Stages + 5) * 8 + 16 + 8 * (size_t)(E + 1);
+    return 1024 + (size_t)k2Stages * k2StageBytes + (2 * k2Stages + 5) * 8 + 16 + 8 * (size_t)(E + 1) + kBiasSmem;
 }
 
 cudaError_t launch_ffn_tc(const FfnParams& P, cudaStream_t s) {
