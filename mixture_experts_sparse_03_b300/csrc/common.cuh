@@ -41,13 +41,6 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
     return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
-// out[0..4) += (a, b, c, d), each element atomically, no value returned (a reduction, so the issuing
-// warp never waits for it); p must be 16-byte aligned
-__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
-    asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
-                 : "memory");
-}
-
 __device__ __forceinline__ void record_error(int* err, int code, int where) {
     if (err != nullptr && atomicCAS(err, 0, code) == 0) atomicExch(err + 1, where);
 }

@@ -97,9 +97,10 @@ __device__ __forceinline__ void epilogue_cols(const TcArgs& a, uint32_t taddr, i
 #pragma unroll
             for (int j = 0; j < 32; j += 4) __stcs(dst + j / 4, make_float4(f[j], f[j + 1], f[j + 2], f[j + 3]));
         } else {
-            float* dst = a.out + (size_t)tok * a.N + n;
+            float4* dst = reinterpret_cast<float4*>(a.out + (size_t)tok * a.N + n);
 #pragma unroll
-            for (int j = 0; j < 32; j += 4) red_add_v4(dst + j, g * f[j], g * f[j + 1], g * f[j + 2], g * f[j + 3]);
+            for (int j = 0; j < 32; j += 4)
+                atomicAdd(dst + j / 4, make_float4(g * f[j], g * f[j + 1], g * f[j + 2], g * f[j + 3]));
         }
     }
 }
