@@ -28,6 +28,10 @@ SMALL = [
     small_workload(T=64, d=64, h=128, E=40, k=3, gate="noisy", dtype="f32", capacity_factor=1.5),
     small_workload(T=1, d=64, h=64, E=2, k=1, capacity_factor=1.0),
     small_workload(T=33, d=64, h=64, E=1, k=1, norm="all", capacity_factor=1.0),  # one expert: dense FFN
+    # fused softmax gate with 32- and 64-wide logit tiles (clusters of 4 and 2 CTAs over K)
+    small_workload(T=300, d=256, h=128, E=24, k=2, capacity_factor=1.0),
+    small_workload(T=200, d=192, h=128, E=48, k=2, norm="all", capacity_factor=1.1),
+    small_workload(T=520, d=128, h=128, E=64, k=4, capacity_factor=0.8),        # 64 experts, k > 2, drops
 ]
 
 
