@@ -106,14 +106,15 @@ def _ulp_step(w: torch.Tensor, up: bool) -> torch.Tensor:
     return nb.to(torch.int16).view(torch.bfloat16)
 
 
-@pytest.mark.parametrize("gate,E", [("softmax", 6), ("softmax", 72), ("noisy", 6), ("cosine", 6)])
-def test_near_ties_resolved_exactly(gate, E):
+@pytest.mark.parametrize("gate,E,p", [("softmax", 6, 0), ("softmax", 72, 0), ("noisy", 6, 0), ("cosine", 6, 64),
+                                       ("cosine", 40, 512)])
+def test_near_ties_resolved_exactly(gate, E, p):
     """Gate rows (cosine gate: expert embeddings) that differ from another row by one bf16 ulp in one
     element: their scores differ by 1e-7 to 1e-3, often inside the fp32 error bound, so the kernel must
     settle the order with its float-float re-scoring (inside the fused gate for softmax with E <= 64,
-    else the grid-wide re-scoring kernel).  The choice must equal the oracle's on every token."""
-    wl = small_workload(T=256, d=256, h=64, E=E, k=2, gate=gate, capacity=256,
-                        cos_dim=64 if gate == "cosine" else 32)
+    else the grid-wide re-scoring kernel; for the cosine gate through v_e = P^T e_e, folded in chunks of
+    256 components when p = 512).  The choice must equal the oracle's on every token."""
+    wl = small_workload(T=256, d=256, h=64, E=E, k=2, gate=gate, capacity=256, cos_dim=p or 32)
     tc, tg = P.inputs(wl)
     name = "emb" if gate == "cosine" else "w_gate"
     col = (5, 17) if gate != "cosine" else (5, 40)
