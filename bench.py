@@ -364,6 +364,41 @@ def run_ours(args, rank, world, local):
                 per[n].append(tev[j].elapsed_time(tev[j + 1]))
             del keep
     kern_ms = {n: statistics.median(v) for n, v in per.items()}
+
+    # ---- router statistics (moe_router_stats) on this workload's routing and dispatch: event-timed calls
+    T_, k_, E_ = wl.T, wl.k, wl.E
+    r_idx = torch.empty((T_, k_), dtype=torch.int32, device=dev)
+    r_gate = torch.empty((T_, k_), dtype=torch.float32, device=dev)
+    r_slot = torch.empty((T_, k_), dtype=torch.int32, device=dev)
+    rows_ = max(b.moe_dispatch_rows(cfg), 1)
+    r_cnt = torch.empty((E_,), dtype=torch.int32, device=dev)
+    r_off = torch.empty((E_ + 1,), dtype=torch.int32, device=dev)
+    r_rtok = torch.empty((rows_,), dtype=torch.int32, device=dev)
+    r_rgate = torch.empty((rows_,), dtype=torch.float32, device=dev)
+    r_xd = torch.empty((rows_, wl.d), dtype=tg["x"].dtype, device=dev)
+    r_imp = torch.empty((E_,), dtype=torch.float32, device=dev)
+    r_loss = torch.empty((2,), dtype=torch.float32, device=dev)
+    r_drop = torch.empty((1,), dtype=torch.int64, device=dev)
+    b.check(b.moe_route(cfg, tg["x"], tg.get("w_gate"), tg.get("w_noise"), tg.get("eps"), tg.get("proj"),
+                        tg.get("emb"), r_idx, r_gate, ws, ws.numel(), stream), "moe_route")
+    b.check(b.moe_dispatch(cfg, tg["x"], r_idx, r_gate, r_slot, r_cnt, r_off, r_rtok, r_rgate, r_xd, ws, ws.numel(),
+                           stream), "moe_dispatch")
+    rs_us = []
+    with torch.cuda.stream(stream):
+        for i in range(13):
+            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a0.record(stream)
+            b.check(b.moe_router_stats(cfg, r_idx, r_gate, r_slot, r_imp, r_loss, r_drop, ws, ws.numel(), stream),
+                    "moe_router_stats")
+            a1.record(stream)
+            a1.synchronize()
+            if i >= 3:
+                rs_us.append(a0.elapsed_time(a1) * 1000.0)
+    rs_bytes = T_ * k_ * 12 + E_ * 4 + 16  # ids, gates, slots in; importance, losses, drops out
+    router_stats = {"us": statistics.median(rs_us), "bytes": rs_bytes, "bound": "latency",
+                    "importance_loss": float(r_loss[0]), "load_balance_loss": float(r_loss[1]),
+                    "dropped": int(r_drop[0])}
+    del r_xd
     # the dominant kernel is the one whose launches take the most time in a step; the expert GEMM kernel
     # runs twice (up-projection with GELU, down-projection), with equal work per launch
     gemm_names = [n for n in names if n.startswith("expert_")]
@@ -478,6 +513,7 @@ def run_ours(args, rank, world, local):
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "pipelined": "2 buffer sets; H2D, compute and D2H on three streams"},
             "gpu_launches": launches_per_step * K,
+            "router_stats": router_stats,
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)

@@ -237,6 +237,27 @@ MOE_API moe_status moe_combine(const moe_config* cfg, const float* y_dispatched,
                        const int32_t* expert_offset, const int32_t* topk_idx,
                        const float* topk_gate, float* out, void* stream);
 
+/* ---- router statistics ------------------------------------------------------------------------- */
+/* Statistics of one routing, for monitoring expert load and for the auxiliary losses the pages add:
+ *   importance[e]   = sum over tokens of the gate the token gives expert e (0 where e is not among
+ *                     its top k): the column sums of the dense gate matrix ("MoE sparse-compute
+ *                     acceleration", section 4.1); utilisation = importance / T
+ *   losses[0]       = expert_importance_loss = 0.1 * std(importance), std with E - 1 in the
+ *                     denominator (section 4.1; NaN when E = 1)
+ *   losses[1]       = load_balance_loss = sum_e (mean_e importance - importance[e])^2 ("MoE
+ *                     architecture: breaking the single-card compute bottleneck", load balancing)
+ *   *dropped        = pairs the capacity limit refused (slot < 0), if slot and dropped are not NULL
+ * topk_idx [T, k] int32 and topk_gate [T, k] fp32 as moe_route writes them (gates in [0, 1]); slot
+ * [T, k] as moe_dispatch / moe_forward write it, or NULL.  importance [E] fp32 and losses [2] fp32 are
+ * device buffers, dropped a device int64 or NULL.  Each gate is added as a multiple of 2^-32 (rounded
+ * to nearest) in 64-bit integers, so the sums are exact and independent of the order the GPU adds them
+ * in: importance[e] is within (pairs of e) * 2^-33 of the exact sum before its rounding to fp32, and
+ * the losses are computed in fp64 from those sums.  An expert id outside [0, E) or a gate outside
+ * [0, 1] records MOE_ERR_DEVICE_CHECK and is skipped.  Uses the workspace (moe_workspace_size). */
+MOE_API moe_status moe_router_stats(const moe_config* cfg, const int32_t* topk_idx, const float* topk_gate,
+                            const int32_t* slot, float* importance, float* losses, int64_t* dropped,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
 /* ---- whole layer ------------------------------------------------------------------------------ */
 /* moe_route -> moe_dispatch -> moe_expert_ffn (+ fused or separate combine) on `stream`, with every
  * intermediate in the workspace.  out [T, d] fp32 is overwritten.  expert_count (may be NULL)

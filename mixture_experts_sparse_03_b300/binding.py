@@ -75,6 +75,7 @@ def _load():
         "moe_dispatch_static_scratch": ([C, P, P, P, P, P, P, P, P, P, P], I32),
         "moe_expert_ffn": ([C, P, P, P, P, P, P, P, P, P, P, P, SZ, P], I32),
         "moe_combine": ([C, P, P, P, P, P, P, P], I32),
+        "moe_router_stats": ([C, P, P, P, P, P, P, P, SZ, P], I32),
         "moe_forward": ([C, P, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P], I32),
         "moe_device_status": ([P, SZ, ctypes.POINTER(I32), P], I32),
         "moe_trace_events": ([ctypes.POINTER(P), I32], None),
@@ -187,6 +188,12 @@ def moe_expert_ffn(cfg, x_dispatched, expert_offset, row_token, row_gate, w1, b1
 def moe_combine(cfg, y_dispatched, slot, expert_offset, topk_idx, topk_gate, out, stream=None) -> int:
     return lib.moe_combine(ctypes.byref(cfg), ptr(y_dispatched), ptr(slot), ptr(expert_offset), ptr(topk_idx),
                            ptr(topk_gate), ptr(out), stream_handle(stream))
+
+
+def moe_router_stats(cfg, topk_idx, topk_gate, slot, importance, losses, dropped, workspace, workspace_bytes,
+                     stream=None) -> int:
+    return lib.moe_router_stats(ctypes.byref(cfg), ptr(topk_idx), ptr(topk_gate), ptr(slot), ptr(importance),
+                                ptr(losses), ptr(dropped), ptr(workspace), workspace_bytes, stream_handle(stream))
 
 
 def moe_forward(cfg, x, w_gate, w_noise, noise_eps, proj, expert_emb, w1, b1, w2, b2, out, expert_count, workspace,

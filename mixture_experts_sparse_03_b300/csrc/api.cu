@@ -27,7 +27,7 @@ struct Plan {
     GateGemmPlan gg;    // tensor-core logits GEMM (bf16 layers)
     int64_t rows;
     size_t o_err, o_idx, o_gate, o_slot, o_hist, o_count, o_off, o_rtok, o_rgate, o_xd, o_h, o_y, o_part, o_xn2,
-        o_wn2, o_rq, o_cosv, total;
+        o_wn2, o_rq, o_cosv, o_stats, total;
     size_t hdr_bytes;  // error word, its info, tickets and the cosine gate's expert flags: zeroed per call
 };
 
@@ -119,6 +119,7 @@ moe_status make_plan(const moe_config* c, Plan* pl) {
     P.o_wn2 = take(P.bf16 ? 4 * (size_t)P.gg.S * np : 0);
     P.o_rq = take(P.bf16 && !P.gg.fused ? 4 * (size_t)P.T * kRescoreInts : 0);
     P.o_cosv = take(cos_tc ? 8 * (size_t)P.E * P.d : 0);
+    P.o_stats = take(8 * (size_t)(P.E + 1) + 16);  // router statistics: expert sums, drop count, ticket
     P.total = o;
     *pl = P;
     return MOE_OK;
@@ -465,6 +466,27 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const void* w_gate,
     MOE_TRY(ffn_and_combine(P, cfg, xd, off, rtok, rgate, w1, b1, w2, b2, y, out, P.fused != 0, workspace, s));
     if (!P.fused) MOE_TRY(launch(s, [&] { return launch_combine(y, slot, off, idx, gate, P.T, P.k, P.d, out, s); }));
     return MOE_OK;
+}
+
+moe_status moe_router_stats(const moe_config* cfg, const int32_t* topk_idx, const float* topk_gate,
+                            const int32_t* slot, float* importance, float* losses, int64_t* dropped,
+                            void* workspace, size_t workspace_bytes, void* stream) {
+    Plan P;
+    MOE_TRY(make_plan(cfg, &P));
+    MOE_TRY(check_ws(P, workspace, workspace_bytes));
+    if (!importance || !losses || !aligned16(importance) || !aligned16(losses)) return MOE_ERR_INVALID_ARG;
+    if (P.T > 0 && (!topk_idx || !topk_gate || !aligned16(topk_idx) || !aligned16(topk_gate)))
+        return MOE_ERR_INVALID_ARG;
+    if ((slot && !aligned16(slot)) || (dropped && (reinterpret_cast<uintptr_t>(dropped) & 7))) return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int* err = at<int>(workspace, P.o_err);
+    void* scratch = at<void>(workspace, P.o_stats);
+    if (cudaMemsetAsync(err, 0, 16, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaMemsetAsync(scratch, 0, 8 * (size_t)(P.E + 1) + 16, s) != cudaSuccess) return MOE_ERR_CUDA;
+    return launch(s, [&] {
+        return launch_router_stats(topk_idx, topk_gate, slot, P.T, P.k, P.E, scratch, err, importance, losses,
+                                   reinterpret_cast<long long*>(dropped), s);
+    });
 }
 
 moe_status moe_device_status(void* workspace, size_t workspace_bytes, int32_t* info, void* stream) {

@@ -14,7 +14,7 @@ using bf16_t = uint16_t;  // raw bits of a bfloat16; converted with the helpers 
 enum : int { kErrCheck = 5, kErrTimeout = 6 };
 enum : int {
     kWhereGate = 1, kWhereDispatch = 2, kWhereFfnSimt = 3, kWhereGemmProducer = 4, kWhereGemmMma = 5,
-    kWhereGemmEpilogue = 6, kWhereCombine = 7, kWhereGateGemm = 8
+    kWhereGemmEpilogue = 6, kWhereCombine = 7, kWhereGateGemm = 8, kWhereRouterStats = 9
 };
 
 // ---- programmatic dependent launch ------------------------------------------------------------------

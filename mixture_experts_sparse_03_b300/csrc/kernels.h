@@ -123,6 +123,10 @@ cudaError_t launch_ffn_simt(const FfnParams& p, cudaStream_t s);
 cudaError_t launch_ffn_tc(const FfnParams& p, cudaStream_t s);  // bf16 only; tcgen05 + TMA
 
 // ---- combine / misc ---------------------------------------------------------------------------
+// router statistics: scratch holds E + 1 uint64 and an int, zero on entry (router_stats.cu)
+cudaError_t launch_router_stats(const int* topk_idx, const float* topk_gate, const int* slot, int T, int k, int E,
+                                void* scratch, int* err, float* importance, float* losses, long long* dropped,
+                                cudaStream_t s);
 cudaError_t launch_combine(const float* y, const int* slot, const int* offset, const int* topk_idx,
                            const float* topk_gate, int T, int k, int d, float* out, cudaStream_t s);
 cudaError_t launch_zero(float* p, size_t n, cudaStream_t s);

@@ -92,6 +92,7 @@ class Oracle:
             "oracle_dispatch": ([I, I, I, I, P, P, P], None),
             "oracle_expert": ([I, I, I, P, S, P, S, P, S, P, S, P, S, P], None),
             "oracle_combine_tokens": ([I, I, I, I, P, I, P, P, P, P, P, P, P, P, P], None),
+            "oracle_router_stats": ([I, I, I, P, P, P, P, P, P, P], None),
         }
         for name, (args, res) in sigs.items():
             fn = getattr(lib, name)
@@ -168,6 +169,19 @@ class Oracle:
                                        _ptr(c2[0]), _ptr(out))
         return out
 
+    def router_stats(self, idx, gate, E, slot=None):
+        """Router statistics: (importance float64 [E], expert_importance_loss, load_balance_loss, dropped)."""
+        idx = np.ascontiguousarray(idx, dtype=np.int32)
+        gate = np.ascontiguousarray(gate, dtype=np.float64)
+        T, k = idx.shape
+        imp = np.empty((E,), dtype=np.float64)
+        il, lb = ctypes.c_double(), ctypes.c_double()
+        dropped = ctypes.c_int64()
+        sl = None if slot is None else np.ascontiguousarray(slot, dtype=np.int32)
+        self.lib.oracle_router_stats(T, E, k, _ptr(idx), _ptr(gate), _ptr(sl) if sl is not None else None,
+                                     _ptr(imp), ctypes.byref(il), ctypes.byref(lb), ctypes.byref(dropped))
+        return imp, il.value, lb.value, int(dropped.value)
+
     def route(self, gate, k, norm, x, w_gate=None, w_noise=None, eps=None, proj=None, emb=None,
               temperature=1.0):
         """Steps 1+2: (scores, idx, gate)."""
@@ -228,6 +242,10 @@ def expert(*a, **kw):
 
 def combine_tokens(*a, **kw):
     return default().combine_tokens(*a, **kw)
+
+
+def router_stats(*a, **kw):
+    return default().router_stats(*a, **kw)
 
 
 def route(*a, **kw):

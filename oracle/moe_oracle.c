@@ -217,3 +217,32 @@ void oracle_combine_tokens(int d, int h, int k, int dtype, const int32_t *tokens
     }
     free(y);
 }
+
+/* ---- router statistics -----------------------------------------------------------------------------
+ * "MoE sparse-compute acceleration" section 4.1: the importance of expert e is the column sum of the
+ * dense gate matrix, sum over tokens of the gate the token gives e (0 where e is not among its top k);
+ * expert_importance_loss = 0.1 * std(importance) with torch.std's default (n - 1 in the denominator,
+ * NaN for a single expert).  "MoE architecture: breaking the single-card compute bottleneck", load
+ * balancing: load_balance_loss = sum_e (mean_load - load_e)^2 with load_e the same column sums.  The
+ * dropped pairs are those the capacity limit refused (slot -1).  Sums in token order, then rank. */
+void oracle_router_stats(int T, int E, int k, const int32_t *idx, const double *gate, const int32_t *slot,
+                         double *importance, double *importance_loss, double *load_balance_loss,
+                         int64_t *dropped)
+{
+    for (int e = 0; e < E; ++e) importance[e] = 0.0;
+    int64_t drops = 0;
+    for (int t = 0; t < T; ++t)
+        for (int j = 0; j < k; ++j) {
+            size_t i = (size_t)t * (size_t)k + (size_t)j;
+            importance[idx[i]] += gate[i];
+            if (slot && slot[i] < 0) ++drops;
+        }
+    double mean = 0.0;
+    for (int e = 0; e < E; ++e) mean += importance[e];
+    mean /= (double)E;
+    double ss = 0.0;
+    for (int e = 0; e < E; ++e) ss += (mean - importance[e]) * (mean - importance[e]);
+    *load_balance_loss = ss;
+    *importance_loss = E > 1 ? 0.1 * sqrt(ss / (double)(E - 1)) : NAN;
+    *dropped = drops;
+}

@@ -301,4 +301,40 @@ def pin_drops_zero_output(o):
     assert np.all(r["slot"] == -1) and np.all(r["out"] == 0.0)
 
 
+def pin_router_stats_hand(o):
+    """Router statistics worked by hand from their definitions: three tokens, top-2 over three experts.
+    Importance = gate column sums: e0 = 0.6 + 0.9 = 1.5, e1 = 0.4 + 0.5 = 0.9, e2 = 0.5 + 0.1 = 0.6;
+    mean 1.0, so load_balance_loss = 0.25 + 0.01 + 0.16 = 0.42 and expert_importance_loss =
+    0.1 * sqrt(0.42 / (3 - 1)); one pair has slot -1."""
+    idx = np.array([[0, 1], [1, 2], [0, 2]], dtype=np.int32)
+    gate = np.array([[0.6, 0.4], [0.5, 0.5], [0.9, 0.1]])
+    slot = np.array([[0, 0], [1, -1], [1, 0]], dtype=np.int32)
+    imp, il, lb, dropped = o.router_stats(idx, gate, 3, slot)
+    assert np.allclose(imp, [1.5, 0.9, 0.6], rtol=0, atol=1e-15)
+    assert abs(lb - 0.42) < 1e-15 and abs(il - 0.1 * (0.21 ** 0.5)) < 1e-15
+    assert dropped == 1
+
+
+def pin_router_stats_invariants(o):
+    """Balanced routing gives zero losses; relabelling the experts permutes the importance and leaves the
+    losses alone; importance sums to the gates' total; one expert has no standard deviation (NaN)."""
+    T, k, E = 40, 2, 4
+    idx = np.array([[(2 * t) % E, (2 * t + 1) % E] for t in range(T)], dtype=np.int32)
+    gate = np.full((T, k), 0.5)
+    imp, il, lb, dropped = o.router_stats(idx, gate, E)
+    assert np.allclose(imp, T * k * 0.5 / E) and il == 0.0 and lb == 0.0 and dropped == 0
+    rng = np.random.default_rng(5)
+    idx2 = rng.integers(0, E, size=(T, k)).astype(np.int32)
+    idx2[:, 1] = (idx2[:, 0] + 1 + rng.integers(0, E - 1, size=T)) % E
+    g2 = rng.random((T, k))
+    imp2, il2, lb2, _ = o.router_stats(idx2, g2, E)
+    perm = np.array([2, 0, 3, 1], dtype=np.int32)  # expert e becomes perm[e]
+    imp3, il3, lb3, _ = o.router_stats(perm[idx2], g2, E)
+    assert np.allclose(imp3[perm], imp2, rtol=1e-14) and abs(il3 - il2) < 1e-14 and abs(lb3 - lb2) < 1e-12
+    assert abs(imp2.sum() - g2.sum()) < 1e-12
+    assert abs(lb2 - (E - 1) * (il2 / 0.1) ** 2) < 1e-10
+    _, il1, lb1, _ = o.router_stats(np.zeros((T, 1), dtype=np.int32), np.ones((T, 1)), 1)
+    assert np.isnan(il1) and lb1 == 0.0
+
+
 ALL_PINS = [v for k_, v in sorted(globals().items()) if k_.startswith("pin_") and callable(v)]

@@ -162,3 +162,19 @@ def test_status_strings():
     for s in range(7):
         assert b.moe_status_string(s) != "unknown status"
     assert b.moe_status_string(99) == "unknown status"
+
+
+def test_router_stats_host_validation():
+    """moe_router_stats refuses a short workspace, missing outputs and a misaligned drop counter on the
+    host, before any CUDA call (the pointers below are never dereferenced)."""
+    c = b.config(small_workload(k=2))
+    nbytes = b.lib.moe_workspace_size(ctypes.byref(c))
+    fake = ctypes.c_void_p(1 << 20)
+    st = b.lib.moe_router_stats(ctypes.byref(c), fake, fake, None, fake, fake, None, fake, 0, None)
+    assert st == 3  # MOE_ERR_WORKSPACE
+    st = b.lib.moe_router_stats(ctypes.byref(c), fake, fake, None, None, fake, None, fake, nbytes, None)
+    assert st == 1  # importance missing
+    st = b.lib.moe_router_stats(ctypes.byref(c), fake, fake, None, fake, fake, ctypes.c_void_p((1 << 20) + 4), fake,
+                                nbytes, None)
+    assert st == 1  # dropped not 8-byte aligned
+

@@ -35,6 +35,9 @@ MUTANTS = [
      "elem(w2, w2_off + (size_t)i * (size_t)d + (size_t)n, dtype)"),
     ("combine_drops_gate", "o[n] += g * y[n];", "o[n] += y[n];"),
     ("combine_keeps_dropped", "if (slot[(size_t)t * k + j] < 0) continue;", ""),
+    ("std_over_n", "0.1 * sqrt(ss / (double)(E - 1))", "0.1 * sqrt(ss / (double)E)"),
+    ("importance_counts_pairs", "importance[idx[i]] += gate[i];", "importance[idx[i]] += 1.0;"),
+    ("drops_counts_kept", "if (slot && slot[i] < 0) ++drops;", "if (slot && slot[i] >= 0) ++drops;"),
     ("bf16_widening_wrong_half", "uint32_t bits = (uint32_t)((const uint16_t *)base)[i] << 16;",
      "uint32_t bits = (uint32_t)((const uint16_t *)base)[i] << 15;"),
 ]
