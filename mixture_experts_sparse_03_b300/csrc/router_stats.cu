@@ -7,9 +7,9 @@
 // ("MoE architecture: breaking the single-card compute bottleneck", load balancing).
 //
 // One grid-stride pass over the (token, rank) pairs: each gate, rounded to a multiple of 2^-32, is
-// added to its expert's 64-bit integer accumulator, so the sums are exact and do not depend on the
-// order of the atomic adds (the result is the same on every run); each warp counts its dropped pairs
-// with a ballot.  The last block to finish (ticket) converts the sums and computes the two losses in
+// added to its expert's 64-bit integer accumulator in shared memory, and each block adds its nonzero
+// accumulators to the global ones once, so the sums are exact and do not depend on the order of the
+// atomic adds (the result is the same on every run); each warp counts its dropped pairs with a ballot.  The last block to finish (ticket) converts the sums and computes the two losses in
 // fp64, a thread per expert and a block reduction in a fixed order.
 #include "common.cuh"
 #include "kernels.h"
@@ -39,9 +39,12 @@ __global__ void __launch_bounds__(kStatsThreads) router_stats_kernel(
     float* importance, float* losses, long long* dropped) {
     __shared__ double red[kStatsThreads / 32];
     __shared__ int last;
+    extern __shared__ unsigned long long s_acc[];  // [E]
     pdl_wait();
     pdl_trigger();
     const int lane = threadIdx.x & 31;
+    for (int e = threadIdx.x; e < E; e += kStatsThreads) s_acc[e] = 0ull;
+    __syncthreads();
     unsigned long long nd = 0;
     for (long long p = (long long)blockIdx.x * kStatsThreads + threadIdx.x; p - lane < npairs;
          p += (long long)gridDim.x * kStatsThreads) {
@@ -52,12 +55,15 @@ __global__ void __launch_bounds__(kStatsThreads) router_stats_kernel(
             if (e < 0 || e >= E || !(g >= 0.f && g <= 1.f)) {
                 record_error(err, kErrCheck, kWhereRouterStats);
             } else {
-                atomicAdd(acc + e, (unsigned long long)llrint((double)g * kFix));
+                atomicAdd(s_acc + e, (unsigned long long)llrint((double)g * kFix));
             }
         }
         if (slot != nullptr) nd += __popc(__ballot_sync(0xffffffffu, in && slot[p] < 0));
     }
     if (slot != nullptr && lane == 0 && nd != 0) atomicAdd(drops, nd);
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += kStatsThreads)
+        if (s_acc[e] != 0ull) atomicAdd(acc + e, s_acc[e]);
     // the last block to finish turns the sums into the statistics
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -98,7 +104,8 @@ cudaError_t launch_router_stats(const int* topk_idx, const float* topk_gate, con
     const long long cap = 4LL * device_sm_count();
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    return launch_pdl(router_stats_kernel, dim3((unsigned)blocks), dim3(kStatsThreads), 0, s, topk_idx, topk_gate,
+    return launch_pdl(router_stats_kernel, dim3((unsigned)blocks), dim3(kStatsThreads), sizeof(unsigned long long) * E, s,
+                      topk_idx, topk_gate,
                       slot, npairs, E, acc, acc + E, ticket, err, importance, losses, dropped);
 }
 
