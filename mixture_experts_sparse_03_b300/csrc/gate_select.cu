@@ -78,7 +78,7 @@ __global__ void __launch_bounds__(kSelThreads) gate_select_kernel(const GatePara
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int tok0 = blockIdx.x * kBT;
     const int ntok = min(kBT, P.T - tok0);
-    const int E = P.E, k = P.k, d = P.d;
+    const int E = P.E, k = P.k;
     const int N = GATE == kGateSoftmax ? E : GATE == kGateNoisy ? 2 * E : P.p;
 
     // ---- CTA: weight-row squared norms (sum of the split partials); cosine: embedding norms
