@@ -5,6 +5,12 @@ over one batch of synthetic tokens already resident in HBM, replayed from a CUDA
 steps a 256 MiB buffer is written to flush the 126 MB L2.  Each step is timed with CUDA events on the
 launching stream; `value` = tokens processed by all ranks / the slowest rank's summed step time.
 
+The default workload is the largest layer that fits one GPU (noisy top-2 gating over 64 experts,
+T = 16384, d = 2048, h = 8192).  Per-kernel durations come from a second graph of the same step whose
+launches are separated by event-record nodes (the library's trace hook under stream capture), so they
+hold no host launch gaps.  The other four workloads are measured the same way (graph-timed step and
+per-kernel split, no end-to-end leg) and reported under "workloads" unless --only is given.
+
   --impl ours (default)   the CUDA library through its C ABI
   --impl reference        the fp64 CPU oracle on the host cores (bounded samples; rank 0 only)
 
@@ -30,11 +36,11 @@ import torch
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from mixture_experts_sparse_03_b300.inputs import WORKLOADS, make_inputs  # noqa: E402
+from mixture_experts_sparse_03_b300.inputs import WORKLOAD_ORDER, WORKLOADS, make_inputs  # noqa: E402
 
 METRIC = "MoE layer fwd tokens/s on 1 B300; % of bf16 TC peak or HBM roofline"
 UNIT = "tokens/s"
-DEFAULT_WORKLOAD = "bf16_e8_k2"
+DEFAULT_WORKLOAD = "bf16_noisy_e64"
 FLUSH_BYTES = 256 << 20
 RIDGE_ROWS = 268  # bf16: FLOP per expert-weight byte = rows per expert; ridge = peak FLOP/s / HBM B/s
 
@@ -69,7 +75,8 @@ def parse():
     ap.add_argument("--ffn", choices=["auto", "one-sm", "sm-pair"], default="auto",
                     help="expert GEMMs on single SMs or on pairs of SMs (default: the library's choice)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
+    ap.add_argument("--only", action="store_true", help="measure the chosen workload only (no 'workloads' key)")
     return ap.parse_args()
 
 
@@ -175,48 +182,103 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------------------------- CPU oracle
-def cpu_oracle_sample(wl, tc, tg, seconds: float):
-    """Time the oracle (as it stands, single-threaded C, fp64) on a bounded sample of the workload:
-    routing and dispatch of every token, then the expert FFN and combine for a prefix of tokens sized
-    to about `seconds` of CPU work.  Returns (tokens/s, description, cores used)."""
+def cpu_model() -> str:
+    """The host CPU's model name (from /proc/cpuinfo)."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+class OneCore:
+    """Pin the calling thread to one host core for the length of the block (the oracle is single-threaded
+    C called from this thread), then restore the previous affinity mask."""
+
+    def __init__(self):
+        self.old = None
+        self.core = None
+
+    def __enter__(self):
+        try:
+            self.old = os.sched_getaffinity(0)
+            self.core = min(self.old)
+            os.sched_setaffinity(0, {self.core})
+        except (AttributeError, OSError):
+            self.old, self.core = None, None
+        return self
+
+    def __exit__(self, *exc):
+        if self.old is not None:
+            os.sched_setaffinity(0, self.old)
+        return False
+
+
+def oracle_prefix(wl, tc, n: int):
+    """The oracle's whole layer (scores, top-k, capacity dispatch, expert FFN, combine) on the first n
+    tokens of the workload.  Slots are assigned in token order, so a prefix's slots and outputs are
+    exactly the full layer's for those tokens (the capacity is the full workload's)."""
     import oracle
 
-    t0 = time.perf_counter()
-    scores = oracle.gate_scores(wl.gate, tc["x"], tc["w_gate"], tc["w_noise"], tc["eps"], tc["proj"], tc["emb"],
-                                wl.temperature)
+    sl = (lambda t: None if t is None else t[:n])
+    scores = oracle.gate_scores(wl.gate, tc["x"][:n], tc["w_gate"], tc["w_noise"], sl(tc["eps"]), tc["proj"],
+                                tc["emb"], wl.temperature)
     idx, gate = oracle.topk(scores, wl.k, wl.norm)
     C = oracle.capacity(wl.T, wl.E, wl.k, wl.capacity_factor, wl.capacity)
     slot, _ = oracle.dispatch(idx, wl.E, C)
-    t_route = time.perf_counter() - t0
-    w = {n: (tc[n] if tc.get(n) is not None else (tg[n].cpu() if tg.get(n) is not None else None))
-         for n in ("w1", "b1", "w2", "b2")}
-    # calibrate on 2 tokens, then size the sample
-    t1 = time.perf_counter()
-    oracle.combine_tokens(np.arange(2, dtype=np.int32), tc["x"], idx, gate, slot, w["w1"], w["b1"], w["w2"], w["b2"])
-    per_tok = max((time.perf_counter() - t1) / 2, 1e-6)
-    n = int(min(wl.T, max(2, (seconds - t_route) / per_tok)))
-    t2 = time.perf_counter()
-    oracle.combine_tokens(np.arange(n, dtype=np.int32), tc["x"], idx, gate, slot, w["w1"], w["b1"], w["w2"], w["b2"])
-    t_ffn = time.perf_counter() - t2
-    per_token = t_route / wl.T + t_ffn / n
-    desc = ("routing + capacity dispatch of all %d tokens (%.2f s) and expert FFN + combine of the first %d tokens "
-            "(%.2f s); tokens/s = 1 / (route_time/T + ffn_time/n)" % (wl.T, t_route, n, t_ffn))
-    return 1.0 / per_token, desc, 1, t_route + t_ffn
+    return oracle.combine_tokens(np.arange(n, dtype=np.int32), tc["x"], idx, gate, slot, tc["w1"], tc["b1"],
+                                 tc["w2"], tc["b2"])
+
+
+def cpu_oracle_sample(wl, tc, seconds: float):
+    """Time the oracle (as it stands: single-threaded C, fp64) on one host core over a bounded sample
+    of the workload: the whole layer for the first n tokens, n sized to about `seconds` of CPU work from
+    a 2-token calibration.  Returns (tokens/s, description, cores used, seconds spent, core)."""
+    with OneCore() as pin:
+        t0 = time.perf_counter()
+        oracle_prefix(wl, tc, 2)
+        per_tok = max((time.perf_counter() - t0) / 2, 1e-6)
+        n = int(min(wl.T, max(2, seconds / per_tok)))
+        t1 = time.perf_counter()
+        oracle_prefix(wl, tc, n)
+        dt = time.perf_counter() - t1
+    desc = ("the whole layer (gate scores, top-k, capacity dispatch with the full workload's capacity, "
+            "expert FFN, combine) for the first %d of %d tokens in %.2f s on one core; tokens/s = n / time"
+            % (n, wl.T, dt))
+    return n / dt, desc, 1, dt, pin.core
+
+
+def host_inputs(wl):
+    """The workload's tensors on the host, with the same values the GPU arm uses (expert weights larger
+    than 1 GiB are drawn by the seeded CUDA generator when a GPU is present, then copied back)."""
+    big = wl.expert_weight_bytes() > (1 << 30)
+    if big and not torch.cuda.is_available():
+        return None
+    t = make_inputs(wl, device="cpu", expert_device="cuda" if big else "cpu")
+    return {n: (v.cpu() if v is not None else None) for n, v in t.items()}
 
 
 def run_reference(args, rank):
     wl = WORKLOADS[args.workload]
     if rank != 0:
         return
-    tc = make_inputs(wl, device="cpu", expert_device="cpu") if wl.expert_weight_bytes() <= (4 << 30) else None
-    if tc is None:
+    if wl.expert_weight_bytes() > (4 << 30):
         print(json.dumps({"impl": "reference", "unavailable": "expert weights of this workload exceed the host "
-                          "sample budget"}))
+                          "sample budget (4 GiB)"}))
         return
-    per_step = max(1.0, args.cpu_seconds / max(1, args.steps + args.warmup))
-    vals, descs, total = [], [], 0.0
+    tc = host_inputs(wl)
+    if tc is None:
+        print(json.dumps({"impl": "reference", "unavailable": "this workload's expert weights are drawn by the "
+                          "CUDA generator and no GPU is present"}))
+        return
+    # each step is a bounded sample sized so that warm-up + steps take about two minutes in all
+    per_step = min(10.0, max(0.3, 120.0 / max(1, args.steps + args.warmup)))
+    vals, descs, total, core = [], [], 0.0, None
     for i in range(args.warmup + args.steps):
-        v, desc, cores, dt = cpu_oracle_sample(wl, tc, {}, per_step)
+        v, desc, cores, dt, core = cpu_oracle_sample(wl, tc, per_step)
         if i >= args.warmup:
             vals.append(v)
             descs.append(desc)
@@ -226,8 +288,10 @@ def run_reference(args, rank):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(vals),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": wl.name, "T": wl.T, "d": wl.d, "h": wl.h, "E": wl.E, "k": wl.k, "gate": wl.gate},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": descs[-1]},
+        "config": {"workload": wl.name, "T": wl.T, "d_model": wl.d, "d_hidden": wl.h, "experts": wl.E,
+                   "top_k": wl.k, "gate": wl.gate},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": descs[-1],
+                         "pinned_core": core, "host_cores": os.cpu_count(), "cpu_model": cpu_model()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -263,8 +327,8 @@ def recorded_traffic(kernel: str, workload: str):
         m = re.search(r"traffic_bytes_per_launch %s:\s*([0-9.eE+]+)" % re.escape(kernel), txt)
         if not m:
             continue
-        k = re.search(r"kernel_source_sha256 (\S+):\s*`?([0-9a-f]+)", txt)
-        if k and file_sha(k.group(1)) == k.group(2):
+        ks = re.findall(r"kernel_source_sha256 (\S+):\s*`?([0-9a-f]+)", txt)
+        if ks and all(file_sha(name) == h for name, h in ks):
             return float(m.group(1))
         s = re.search(r"source_sha256:\s*`?([0-9a-f]+)", txt)
         if s and s.group(1) == source_sha():
@@ -272,60 +336,104 @@ def recorded_traffic(kernel: str, workload: str):
     return None
 
 
-def run_ours(args, rank, world, local):
-    from mixture_experts_sparse_03_b300 import binding as b
+def roofline(wl, kern_ms, names, kept, used):
+    """Roofline of the dominant kernel (the one whose launches take the largest share of a step).  The
+    expert GEMM kernel runs twice per step (up-projection with GELU, down-projection) with equal work
+    per launch; for it, achieved = algorithmic work of one launch / its mean launch duration."""
+    gemm_flops, gate_flops, wbytes = layer_work(wl, kept, used)
+    gemm_names = [n for n in names if n.startswith("expert_")]
+    gemm_launch_ms = sum(kern_ms[n] for n in gemm_names) / len(gemm_names)
+    rest = {n: v for n, v in kern_ms.items() if n not in gemm_names}
+    top_rest = max(rest, key=rest.get)
+    gemm_dominant = sum(kern_ms[n] for n in gemm_names) >= rest[top_rest]
+    pk = peaks()
+    hbm_bound = kept < RIDGE_ROWS * max(used, 1)  # few rows per expert: the weights' bytes bound the FFN
+    if gemm_dominant and hbm_bound:
+        # one expert GEMM streams one of the two weight matrices of every used expert
+        achieved = (wbytes / 2) / (gemm_launch_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s",
+                "frac": achieved / pk["hbm"], "algorithmic_per_launch": wbytes / 2}
+    elif gemm_dominant:
+        achieved = gemm_flops / (gemm_launch_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": pk["bf16"], "unit": "TFLOP/s",
+                "frac": achieved / pk["bf16"], "frac_of_sustained": achieved / pk["bf16_sustained"],
+                "algorithmic_per_launch": gemm_flops}
+    else:
+        roof = {"bound": "hbm", "achieved": None, "peak": pk["hbm"], "unit": "GB/s", "frac": None}
+    if gemm_dominant:
+        dominant = "expert_gemm (%s)" % " + ".join(gemm_names)
+        tr = [recorded_traffic(n, wl.name) for n in gemm_names]
+        traffic = sum(tr) / len(tr) if all(v is not None for v in tr) else None
+        dom_ms = gemm_launch_ms
+    else:
+        dominant, traffic, dom_ms = top_rest, recorded_traffic(top_rest, wl.name), rest[top_rest]
+    roof.update({"traffic": traffic, "kernel": dominant, "peak_source": pk["source"] + " (burst)",
+                 "kernel_ms": dom_ms})
+    if wl.dtype != "bf16":
+        roof["note"] = "fp32 CUDA-core path; bf16 tensor peak shown for reference only"
+    return roof, gemm_flops, gate_flops, wbytes
 
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    if world > 1:
-        import torch.distributed as dist
 
-        dist.init_process_group("nccl", device_id=dev)
-    wl = WORKLOADS[args.workload]
-    cfg = b.config(wl, flags={"auto": 0, "one-sm": b.FLAG_FFN_ONE_SM, "sm-pair": b.FLAG_FFN_SM_PAIR}[args.ffn])
-    tg = make_inputs(wl, device=dev, expert_device="cuda" if wl.expert_weight_bytes() > (1 << 30) else "cpu")
-    ws = b.workspace(cfg, dev)
-    out = torch.empty((wl.T, wl.d), dtype=torch.float32, device=dev)
-    count = torch.empty((wl.E,), dtype=torch.int32, device=dev)
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    stream = torch.cuda.Stream(device=dev)
-    launches_per_step = b.moe_forward_launches(cfg)
+class Layer:
+    """One workload's inputs, workspace and output on the device, and its moe_forward step."""
 
-    def step():
-        b.check(b.moe_forward(cfg, tg["x"], tg.get("w_gate"), tg.get("w_noise"), tg.get("eps"), tg.get("proj"),
-                              tg.get("emb"), tg["w1"], tg.get("b1"), tg["w2"], tg.get("b2"), out, count, ws,
-                              ws.numel(), stream), "moe_forward")
+    def __init__(self, wl, dev, stream, ffn="auto"):
+        from mixture_experts_sparse_03_b300 import binding as b
 
+        self.b, self.wl, self.dev, self.stream = b, wl, dev, stream
+        self.cfg = b.config(wl, flags={"auto": 0, "one-sm": b.FLAG_FFN_ONE_SM, "sm-pair": b.FLAG_FFN_SM_PAIR}[ffn])
+        self.tg = make_inputs(wl, device=dev,
+                              expert_device="cuda" if wl.expert_weight_bytes() > (1 << 30) else "cpu")
+        self.ws = b.workspace(self.cfg, dev)
+        self.out = torch.empty((wl.T, wl.d), dtype=torch.float32, device=dev)
+        self.count = torch.empty((wl.E,), dtype=torch.int32, device=dev)
+        self.launches = b.moe_forward_launches(self.cfg)
+        self.names = kernel_names(wl, self.launches)
+
+    def step(self, x=None, eps=None, out=None, count="default"):
+        b, t = self.b, self.tg
+        b.check(b.moe_forward(self.cfg, t["x"] if x is None else x, t.get("w_gate"), t.get("w_noise"),
+                              t.get("eps") if eps is None else eps, t.get("proj"), t.get("emb"), t["w1"],
+                              t.get("b1"), t["w2"], t.get("b2"), self.out if out is None else out,
+                              self.count if count == "default" else count, self.ws, self.ws.numel(), self.stream),
+                "moe_forward")
+
+    def capture(self, traced_events=None):
+        """A CUDA graph of one step; with events, the library's trace hook puts an event-record node
+        before the first launch and after every launch."""
+        b = self.b
+        g = torch.cuda.CUDAGraph()
+        keep = None
+        with torch.cuda.graph(g, stream=self.stream):
+            if traced_events is not None:
+                keep = b.moe_trace_events(traced_events, len(traced_events))
+            self.step()
+            if traced_events is not None:
+                recorded = b.moe_trace_count()
+                b.moe_trace_events(None, 0)
+        if traced_events is not None and recorded != len(traced_events):
+            raise RuntimeError("trace hook recorded %d of %d events" % (recorded, len(traced_events)))
+        del keep
+        return g
+
+
+def measure(wl, args, dev, stream, flush, world):
+    """Graph-timed steps and the per-kernel split of one workload.  Returns (result dict, Layer)."""
+    L = Layer(wl, dev, stream, args.ffn)
+    b = L.b
     with torch.cuda.stream(stream):
         for _ in range(max(3, args.warmup)):
-            step()
+            L.step()
     stream.synchronize()
-    st, info = b.moe_device_status(ws, ws.numel(), stream)
+    st, info = b.moe_device_status(L.ws, L.ws.numel(), stream)
     b.check(st, "device status after warm-up")
-    C = b.moe_capacity(cfg)
-    cnt = count.cpu().numpy()
+    C = b.moe_capacity(L.cfg)
+    cnt = L.count.cpu().numpy()
     kept = int(np.minimum(cnt, min(C, wl.T)).sum())
     used = int((np.minimum(cnt, C) > 0).sum())
-    gemm_flops, gate_flops, wbytes = layer_work(wl, kept, used)
 
-    graph = None
-    if not args.no_graph:
-        try:
-            graph = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(graph, stream=stream):
-                step()
-            with torch.cuda.stream(stream):
-                graph.replay()
-            stream.synchronize()
-        except Exception as e:  # report eager timing instead
-            print("graph capture failed (%s); timing eager launches" % e, file=sys.stderr)
-            graph = None
-
-    def run_step():
-        if graph is not None:
-            graph.replay()
-        else:
-            step()
+    graph = None if args.no_graph else L.capture()
+    run_step = graph.replay if graph is not None else L.step
 
     # ---- timed region: K steps, L2 flushed before each, events around each step
     K = args.steps
@@ -335,7 +443,7 @@ def run_ours(args, rank, world, local):
             flush.fill_(1)
             run_step()
     stream.synchronize()
-    sampler = ClockSampler(local)
+    sampler = ClockSampler(dev.index)
     sampler.start()
     if world > 1:
         torch.distributed.barrier()
@@ -352,37 +460,46 @@ def run_ours(args, rank, world, local):
     clocks = sampler.stop()
     times = [a.elapsed_time(z) for a, z in evs]  # ms
     total_ms = max_over_ranks(sum(times), dev)
-    value = job_throughput(world, K, wl.T, total_ms)
-    ms_per_step = total_ms / K
 
-    # ---- per-kernel durations (eager, trace events between the library's launches)
-    names = kernel_names(wl, launches_per_step)
-    per = {n: [] for n in names}
-    tev = [torch.cuda.Event(enable_timing=True) for _ in range(launches_per_step + 1)]
+    # ---- per-kernel durations: a graph of the same step with event-record nodes between its launches
+    tev = [torch.cuda.Event(enable_timing=True) for _ in range(L.launches + 1)]
     for e in tev:  # torch creates the CUDA event at its first record; the library needs real handles
         e.record(stream)
     stream.synchronize()
+    per = {n: [] for n in L.names}
+    traced_steps = []
+    tgraph = L.capture(tev)
     with torch.cuda.stream(stream):
         for i in range(max(5, min(K, 20))):
             flush.fill_(1)
-            keep = b.moe_trace_events(tev, len(tev))
-            step()
-            recorded = b.moe_trace_count()
-            b.moe_trace_events(None, 0)
+            tgraph.replay()
             stream.synchronize()
-            if recorded != len(tev):
-                raise RuntimeError("trace hook recorded %d of %d events" % (recorded, len(tev)))
-            for j, n in enumerate(names):
+            for j, n in enumerate(L.names):
                 per[n].append(tev[j].elapsed_time(tev[j + 1]))
-            del keep
+            traced_steps.append(tev[0].elapsed_time(tev[-1]))
+    del tgraph
     kern_ms = {n: statistics.median(v) for n, v in per.items()}
+    roof, gemm_flops, gate_flops, wbytes = roofline(wl, kern_ms, L.names, kept, used)
+    ms_per_step = total_ms / K
+    roof.update({"layer_tflops": (2 * gemm_flops + gate_flops) / (ms_per_step * 1e-3) / 1e12,
+                 "layer_weight_gbs": wbytes / (ms_per_step * 1e-3) / 1e9})
+    res = {"value": job_throughput(world, K, wl.T, total_ms), "ms_per_step": ms_per_step,
+           "step_ms_median": statistics.median(times), "traced_step_ms_median": statistics.median(traced_steps),
+           "kernel_ms": kern_ms, "capacity": C, "kept_pairs": kept, "experts_used": used,
+           "graph": graph is not None, "roofline": roof, "clocks": clocks, "gpu_launches": L.launches * K}
+    del graph
+    return res, L
 
-    # ---- router statistics (moe_router_stats) on this workload's routing and dispatch: event-timed calls
+
+def router_stats_timing(L, stream):
+    """moe_router_stats on the layer's routing and dispatch: 20 calls captured in one CUDA graph, the
+    replay event-timed, per call."""
+    b, wl, dev, tg = L.b, L.wl, L.dev, L.tg
     T_, k_, E_ = wl.T, wl.k, wl.E
     r_idx = torch.empty((T_, k_), dtype=torch.int32, device=dev)
     r_gate = torch.empty((T_, k_), dtype=torch.float32, device=dev)
     r_slot = torch.empty((T_, k_), dtype=torch.int32, device=dev)
-    rows_ = max(b.moe_dispatch_rows(cfg), 1)
+    rows_ = max(b.moe_dispatch_rows(L.cfg), 1)
     r_cnt = torch.empty((E_,), dtype=torch.int32, device=dev)
     r_off = torch.empty((E_ + 1,), dtype=torch.int32, device=dev)
     r_rtok = torch.empty((rows_,), dtype=torch.int32, device=dev)
@@ -391,77 +508,57 @@ def run_ours(args, rank, world, local):
     r_imp = torch.empty((E_,), dtype=torch.float32, device=dev)
     r_loss = torch.empty((2,), dtype=torch.float32, device=dev)
     r_drop = torch.empty((1,), dtype=torch.int64, device=dev)
-    b.check(b.moe_route(cfg, tg["x"], tg.get("w_gate"), tg.get("w_noise"), tg.get("eps"), tg.get("proj"),
-                        tg.get("emb"), r_idx, r_gate, ws, ws.numel(), stream), "moe_route")
-    b.check(b.moe_dispatch(cfg, tg["x"], r_idx, r_gate, r_slot, r_cnt, r_off, r_rtok, r_rgate, r_xd, ws, ws.numel(),
-                           stream), "moe_dispatch")
-    rs_us = []
+    ws = L.ws
     with torch.cuda.stream(stream):
-        for i in range(6):  # batches of 20 back-to-back calls (as a training loop issues them), per call
+        b.check(b.moe_route(L.cfg, tg["x"], tg.get("w_gate"), tg.get("w_noise"), tg.get("eps"), tg.get("proj"),
+                            tg.get("emb"), r_idx, r_gate, ws, ws.numel(), stream), "moe_route")
+        b.check(b.moe_dispatch(L.cfg, tg["x"], r_idx, r_gate, r_slot, r_cnt, r_off, r_rtok, r_rgate, r_xd, ws,
+                               ws.numel(), stream), "moe_dispatch")
+
+    def call():
+        b.check(b.moe_router_stats(L.cfg, r_idx, r_gate, r_slot, r_imp, r_loss, r_drop, ws, ws.numel(), stream),
+                "moe_router_stats")
+
+    with torch.cuda.stream(stream):
+        call()
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(20):
+            call()
+    us = []
+    with torch.cuda.stream(stream):
+        for i in range(6):
             a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a0.record(stream)
-            for _ in range(20):
-                b.check(b.moe_router_stats(cfg, r_idx, r_gate, r_slot, r_imp, r_loss, r_drop, ws, ws.numel(),
-                                           stream), "moe_router_stats")
+            g.replay()
             a1.record(stream)
             a1.synchronize()
             if i >= 1:
-                rs_us.append(a0.elapsed_time(a1) * 1000.0 / 20)
+                us.append(a0.elapsed_time(a1) * 1000.0 / 20)
     rs_bytes = T_ * k_ * 12 + E_ * 4 + 16  # ids, gates, slots in; importance, losses, drops out
-    router_stats = {"us": statistics.median(rs_us), "bytes": rs_bytes, "bound": "latency",
-                    "importance_loss": float(r_loss[0]), "load_balance_loss": float(r_loss[1]),
-                    "dropped": int(r_drop[0])}
-    del r_xd
-    # the dominant kernel is the one whose launches take the most time in a step; the expert GEMM kernel
-    # runs twice (up-projection with GELU, down-projection), with equal work per launch
-    gemm_names = [n for n in names if n.startswith("expert_")]
-    gemm_launch_ms = sum(kern_ms[n] for n in gemm_names) / len(gemm_names)
-    rest = {n: v for n, v in kern_ms.items() if n not in gemm_names}
-    top_rest = max(rest, key=rest.get)
-    gemm_dominant = sum(kern_ms[n] for n in gemm_names) >= rest[top_rest]
-    pk = peaks()
-    hbm_bound = kept < RIDGE_ROWS * max(used, 1)  # few rows per expert: the weights' bytes bound the FFN
-    if gemm_dominant and hbm_bound:
-        # one expert GEMM streams one of the two weight matrices of every used expert
-        achieved = (wbytes / 2) / (gemm_launch_ms * 1e-3) / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s",
-                "frac": achieved / pk["hbm"]}
-    elif gemm_dominant:
-        achieved = gemm_flops / (gemm_launch_ms * 1e-3) / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": pk["bf16"], "unit": "TFLOP/s",
-                "frac": achieved / pk["bf16"]}
-    else:
-        roof = {"bound": "hbm", "achieved": None, "peak": pk["hbm"], "unit": "GB/s", "frac": None}
-    if gemm_dominant:
-        dominant = "expert_gemm (%s)" % " + ".join(gemm_names)
-        tr = [recorded_traffic(n, wl.name) for n in gemm_names]
-        traffic = sum(tr) / len(tr) if all(v is not None for v in tr) else None
-        dom_ms = gemm_launch_ms
-    else:
-        dominant, traffic, dom_ms = top_rest, recorded_traffic(top_rest, wl.name), rest[top_rest]
-    roof.update({"traffic": traffic, "kernel": dominant,
-                 "peak_source": pk["source"] + " (burst)", "kernel_ms": dom_ms,
-                 "layer_tflops": (2 * gemm_flops + gate_flops) / (ms_per_step * 1e-3) / 1e12,
-                 "layer_weight_gbs": wbytes / (ms_per_step * 1e-3) / 1e9})
-    if wl.dtype != "bf16":
-        roof["note"] = "fp32 CUDA-core path; bf16 tensor peak shown for reference only"
+    return {"us": statistics.median(us), "bytes": rs_bytes, "bound": "latency", "timing": "20 calls in one graph",
+            "importance_loss": float(r_loss[0]), "load_balance_loss": float(r_loss[1]), "dropped": int(r_drop[0])}
 
-    # ---- end to end through the C ABI with host buffers (pinned), copies inside the timed region.  Steps
-    # are pipelined the way a serving loop would run them: step i's host-to-device copy (its own stream),
-    # its moe_forward (after an L2 flush, on the compute stream) and its device-to-host copy of `out`
-    # (a third stream) overlap the neighbouring steps' work; two device buffer sets alternate.
+
+def e2e_timing(L, flush, K, world):
+    """End to end through the C ABI with pinned host buffers: every step copies x (and eps) in, flushes
+    L2, runs moe_forward and copies `out` back.  Steps are pipelined the way a serving loop runs them:
+    step i's host-to-device copy (its own stream), its moe_forward (compute stream) and its
+    device-to-host copy of `out` (a third stream) overlap the neighbouring steps' work; two device
+    buffer sets alternate.  Returns (tokens/s, h2d bytes per step, d2h bytes per step)."""
+    wl, dev, stream, tg = L.wl, L.dev, L.stream, L.tg
     x_host = tg["x"].cpu().pin_memory()
     eps_host = tg["eps"].cpu().pin_memory() if tg.get("eps") is not None else None
     out_host = [torch.empty((wl.T, wl.d), dtype=torch.float32).pin_memory() for _ in range(2)]
     x_dev = [torch.empty_like(tg["x"]) for _ in range(2)]
     eps_dev = [torch.empty_like(tg["eps"]) for _ in range(2)] if eps_host is not None else [None, None]
-    out_dev = [out, torch.empty_like(out)]
+    out_dev = [L.out, torch.empty_like(L.out)]
     h2d = x_host.numel() * x_host.element_size() + (eps_host.numel() * 4 if eps_host is not None else 0)
     d2h = out_host[0].numel() * 4
     s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
 
-    def e2e_run(n):
-        """n pipelined steps; returns the events bracketing them"""
+    def run(n):
         ev_in = [torch.cuda.Event() for _ in range(n)]
         ev_fw = [torch.cuda.Event() for _ in range(n)]
         ev_out = [torch.cuda.Event() for _ in range(n)]
@@ -483,9 +580,7 @@ def run_ours(args, rank, world, local):
                 if i >= 2:
                     stream.wait_event(ev_out[i - 2])  # out[j] has been read back
                 flush.fill_(i & 0xFF)
-                b.check(b.moe_forward(cfg, x_dev[j], tg.get("w_gate"), tg.get("w_noise"), eps_dev[j], tg.get("proj"),
-                                      tg.get("emb"), tg["w1"], tg.get("b1"), tg["w2"], tg.get("b2"), out_dev[j], None,
-                                      ws, ws.numel(), stream), "moe_forward")
+                L.step(x=x_dev[j], eps=eps_dev[j], out=out_dev[j], count=None)
                 ev_fw[i].record(stream)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(ev_fw[i])
@@ -496,38 +591,80 @@ def run_ours(args, rank, world, local):
         end.record(stream)
         return start, end
 
-    e2e_run(3)
+    run(3)
     torch.cuda.synchronize(dev)
-    start, end = e2e_run(K)
+    start, end = run(K)
     end.synchronize()
     e_ms = start.elapsed_time(end)
-    e2e_value = job_throughput(world, K, wl.T, max_over_ranks(e_ms, dev))
     torch.cuda.synchronize(dev)
+    return job_throughput(world, K, wl.T, max_over_ranks(e_ms, dev)), h2d, d2h
+
+
+def config_of(wl, res, world):
+    return {"workload": wl.name, "T": wl.T, "d_model": wl.d, "d_hidden": wl.h, "experts": wl.E, "top_k": wl.k,
+            "gate": wl.gate, "capacity": res["capacity"], "kept_pairs": res["kept_pairs"],
+            "experts_used": res["experts_used"], "parallelism": "replicas" if world > 1 else "single",
+            "l2": "flushed between steps (256 MiB write)", "graph": res["graph"],
+            "step_ms_median": res["step_ms_median"], "traced_step_ms_median": res["traced_step_ms_median"],
+            "kernel_ms": res["kernel_ms"],
+            "kernel_timing": "graph replay with event-record nodes between launches (no host gaps); their "
+                             "sum is traced_step_ms, which lacks the overlap of programmatic dependent "
+                             "launch that the timed step has"}
+
+
+def run_ours(args, rank, world, local):
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+    wl = WORKLOADS[args.workload]
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    res, L = measure(wl, args, dev, stream, flush, world)
+    router_stats = router_stats_timing(L, stream)
+    e2e_value, h2d, d2h = e2e_timing(L, flush, args.steps, world)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        tc = {n: (v.cpu() if v is not None else None) for n, v in tg.items()}
-        v, desc, cores, _ = cpu_oracle_sample(wl, tc, {}, args.cpu_seconds)
-        cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc,
-               "host_cores": os.cpu_count()}
+        tc = {n: (v.cpu() if v is not None else None) for n, v in L.tg.items()}
+        v, desc, cores, _, core = cpu_oracle_sample(wl, tc, args.cpu_seconds)
+        cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc, "pinned_core": core,
+               "host_cores": os.cpu_count(), "cpu_model": cpu_model()}
+        del tc
+    del L
+    torch.cuda.empty_cache()
+
+    others = {}
+    if not args.only:
+        for name in WORKLOAD_ORDER:
+            if name == wl.name:
+                continue
+            o_args = argparse.Namespace(**{**vars(args), "steps": min(args.steps, 20), "warmup": 3})
+            r, Lo = measure(WORKLOADS[name], o_args, dev, stream, flush, world)
+            del Lo
+            torch.cuda.empty_cache()
+            others[name] = {"tokens_per_s": r["value"], "ms_per_step": r["ms_per_step"],
+                            "config": config_of(WORKLOADS[name], r, world), "roofline": r["roofline"],
+                            "clocks": r["clocks"], "steps": o_args.steps}
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
-            "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": wl.dtype, "data": "synthetic (seeded; shapes and distributions of the workload)",
-            "config": {"workload": wl.name, "T": wl.T, "d_model": wl.d, "d_hidden": wl.h, "experts": wl.E,
-                       "top_k": wl.k, "gate": wl.gate, "capacity": C, "kept_pairs": kept,
-                       "parallelism": "replicas" if world > 1 else "single",
-                       "l2": "flushed between steps (256 MiB write)", "graph": graph is not None,
-                       "step_ms_median": statistics.median(times), "kernel_ms": kern_ms},
-            "roofline": roof,
+            "metric": METRIC, "value": res["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": res["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": wl.dtype,
+            "data": "synthetic (seeded; shapes and distributions of the workload)",
+            "config": config_of(wl, res, world),
+            "roofline": res["roofline"],
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "pipelined": "2 buffer sets; H2D, compute and D2H on three streams"},
-            "gpu_launches": launches_per_step * K,
+            "gpu_launches": res["gpu_launches"],
             "router_stats": router_stats,
-            "clocks": clocks,
+            "clocks": res["clocks"],
+            "workloads": others,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

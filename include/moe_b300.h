@@ -198,7 +198,10 @@ MOE_API moe_status moe_dispatch(const moe_config* cfg, const void* x, const int3
  *  - Limit.  Configs with ceil(T/32) * E > MOE_DISPATCH_STATIC_MAX_HIST return MOE_ERR_UNSUPPORTED and
  *    launch nothing (e.g. T = 16384 allows E <= 511; T = 65536 allows E <= 127).
  *  - Set-up.  The first call on each device looks up the array's device address (cudaGetSymbolAddress)
- *    with that device current; make that first call before any stream capture.
+ *    with that device current; make that first call before any stream capture.  The address is kept
+ *    per device and context: after a device reset (cudaDeviceReset) the next call looks it up again,
+ *    and should likewise come before any stream capture.
+ *  - Config errors.  A config moe_dispatch rejects is rejected with the same status.
  *  - Sharing.  Every call on a device uses the same array, which keeps the last call's contents (the
  *    call clears what must start at zero).  Calls whose kernels overlap on the GPU (other streams, other
  *    host threads) race on it and give wrong results: serialise them, e.g. on one stream.
@@ -280,7 +283,11 @@ MOE_API moe_status moe_device_status(void* workspace, size_t workspace_bytes, in
  * call, and events[i] right after the i-th such kernel, until `capacity` events are used; n kernels
  * thus use n + 1 events and kernel i ran between events[i] and events[i+1].  moe_trace_count()
  * returns how many events the current (or, once turned off, the last) trace recorded.  events == NULL
- * turns the hook off.  Not thread-safe; meant for benchmarks. */
+ * turns the hook off.  Events are recorded with cudaEventRecordExternal, so a call made while `stream`
+ * is being captured puts event-record nodes into the graph and every replay of that graph times its
+ * kernels with no host gaps between them.  Not thread-safe; meant for benchmarks.
+ * Every compute entry point also opens an NVTX range named after itself for the length of the call
+ * (a no-op unless a profiler is attached). */
 MOE_API void    moe_trace_events(void** events, int32_t capacity);
 MOE_API int32_t moe_trace_count(void);
 

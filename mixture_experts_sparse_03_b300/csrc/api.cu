@@ -3,6 +3,7 @@
 // host before anything is enqueued; a failed check returns a status and launches nothing.
 #include <cuda_runtime.h>
 #include <math.h>
+#include <nvtx3/nvToolsExt.h>
 #include <stdint.h>
 
 #include <algorithm>
@@ -139,9 +140,11 @@ int g_capacity = 0;
 int g_recorded = 0;
 
 // A failed record (e.g. an event that was never created) turns the hook off and clears the error, so
-// tracing can never change the status of a launch; moe_trace_count() then shows the shortfall.
+// tracing can never change the status of a launch; moe_trace_count() then shows the shortfall.  The
+// records are external: under stream capture each becomes an event-record node of the graph, so a
+// replayed graph times its kernels without host gaps between them.
 void trace_record(int i, cudaStream_t s) {
-    if (cudaEventRecord(static_cast<cudaEvent_t>(g_events[i]), s) != cudaSuccess) {
+    if (cudaEventRecordWithFlags(static_cast<cudaEvent_t>(g_events[i]), s, cudaEventRecordExternal) != cudaSuccess) {
         cudaGetLastError();
         g_events = nullptr;
         return;
@@ -164,6 +167,14 @@ moe_status launch(cudaStream_t s, F&& f) {
     trace_post(s);
     return MOE_OK;
 }
+// One NVTX range per C-ABI call (visible to nsys / ncu's NVTX filters; a no-op without a tool attached).
+struct NvtxRange {
+    explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange&) = delete;
+    NvtxRange& operator=(const NvtxRange&) = delete;
+};
+
 #define MOE_TRY(expr)                      \
     do {                                   \
         moe_status st_ = (expr);           \
@@ -295,6 +306,13 @@ moe_status ffn_and_combine(const Plan& P, const moe_config* c, const void* xd, c
 
 }  // namespace
 
+namespace moe {
+int32_t config_status(const void* cfg) {
+    Plan P;
+    return make_plan(static_cast<const moe_config*>(cfg), &P);
+}
+}  // namespace moe
+
 extern "C" {
 
 int32_t moe_capacity(const moe_config* cfg) {
@@ -323,6 +341,7 @@ int32_t moe_forward_launches(const moe_config* cfg) {
 moe_status moe_route(const moe_config* cfg, const void* x, const void* w_gate, const void* w_noise,
                      const float* noise_eps, const void* proj, const void* expert_emb, int32_t* topk_idx,
                      float* topk_gate, void* workspace, size_t workspace_bytes, void* stream) {
+    NvtxRange nvtx_("moe_route");
     Plan P;
     MOE_TRY(make_plan(cfg, &P));
     if (P.T == 0) return MOE_OK;
@@ -338,6 +357,7 @@ moe_status moe_route(const moe_config* cfg, const void* x, const void* w_gate, c
 
 moe_status moe_gate_logits(const moe_config* cfg, const void* x, const void* w_gate, const void* w_noise,
                            const void* proj, float* logits, void* workspace, size_t workspace_bytes, void* stream) {
+    NvtxRange nvtx_("moe_gate_logits");
     Plan P;
     MOE_TRY(make_plan(cfg, &P));
     if (!P.bf16) return MOE_ERR_UNSUPPORTED;
@@ -359,6 +379,7 @@ moe_status moe_gate_logits(const moe_config* cfg, const void* x, const void* w_g
 moe_status moe_dispatch(const moe_config* cfg, const void* x, const int32_t* topk_idx, const float* topk_gate,
                         int32_t* slot, int32_t* expert_count, int32_t* expert_offset, int32_t* row_token,
                         float* row_gate, void* x_dispatched, void* workspace, size_t workspace_bytes, void* stream) {
+    NvtxRange nvtx_("moe_dispatch");
     Plan P;
     MOE_TRY(make_plan(cfg, &P));
     if (P.T == 0) return MOE_OK;
@@ -386,6 +407,7 @@ moe_status moe_expert_ffn(const moe_config* cfg, const void* x_dispatched, const
                           const int32_t* row_token, const float* row_gate, const void* w1, const void* b1,
                           const void* w2, const void* b2, float* y_dispatched, float* out, void* workspace,
                           size_t workspace_bytes, void* stream) {
+    NvtxRange nvtx_("moe_expert_ffn");
     Plan P;
     MOE_TRY(make_plan(cfg, &P));
     if (P.T == 0) return MOE_OK;
@@ -406,6 +428,7 @@ moe_status moe_expert_ffn(const moe_config* cfg, const void* x_dispatched, const
 moe_status moe_combine(const moe_config* cfg, const float* y_dispatched, const int32_t* slot,
                        const int32_t* expert_offset, const int32_t* topk_idx, const float* topk_gate, float* out,
                        void* stream) {
+    NvtxRange nvtx_("moe_combine");
     Plan P;
     MOE_TRY(make_plan(cfg, &P));
     if (P.T == 0) return MOE_OK;
@@ -422,6 +445,7 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const void* w_gate,
                        const float* noise_eps, const void* proj, const void* expert_emb, const void* w1,
                        const void* b1, const void* w2, const void* b2, float* out, int32_t* expert_count,
                        void* workspace, size_t workspace_bytes, void* stream) {
+    NvtxRange nvtx_("moe_forward");
     Plan P;
     MOE_TRY(make_plan(cfg, &P));
     if (P.T == 0) return MOE_OK;
@@ -471,6 +495,7 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const void* w_gate,
 moe_status moe_router_stats(const moe_config* cfg, const int32_t* topk_idx, const float* topk_gate,
                             const int32_t* slot, float* importance, float* losses, int64_t* dropped,
                             void* workspace, size_t workspace_bytes, void* stream) {
+    NvtxRange nvtx_("moe_router_stats");
     Plan P;
     MOE_TRY(make_plan(cfg, &P));
     MOE_TRY(check_ws(P, workspace, workspace_bytes));

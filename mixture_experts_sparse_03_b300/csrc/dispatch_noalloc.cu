@@ -7,6 +7,7 @@
 // and callers that must not allocate after start-up (no cudaMalloc, no allocator call on the hot
 // path).  moe_dispatch_static_scratch keeps that scratch in a fixed array compiled into the library
 // instead, and otherwise runs exactly the kernels moe_dispatch runs.
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -28,24 +29,62 @@ static __device__ __align__(256) int32_t g_dispatch_scratch[kScratchInts];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mutex;
-int32_t* g_scratch_ptr[kMaxDevices] = {};
+struct ScratchAddr {
+    unsigned long long ctx_id;  // the context the address belongs to (0: none looked up yet)
+    int32_t* ptr;
+};
+ScratchAddr g_scratch[kMaxDevices] = {};
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// Unique id of the calling thread's current context (0 if there is none or the driver cannot say).
+// Context ids are never reused within a process, so a device reset, which destroys the primary
+// context and the module holding the array, changes the id and forces a fresh look-up.
+unsigned long long current_context_id() {
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    static bool resolved = false;
+    if (!resolved) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<CtxGetIdFn>(p);
+        cudaGetLastError();
+        resolved = true;
+    }
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current == nullptr || get_id == nullptr || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+    if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
 
 // Device address of g_dispatch_scratch on the current device.  On the host the symbol names a host
-// stand-in, so its address must be looked up once per device, with that device current.
+// stand-in, so its device address is looked up with cudaGetSymbolAddress, with the device current:
+// once per device and context (the first call on a device, and the first after a device reset).
 moe_status scratch_for_current_device(int32_t** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_UNSUPPORTED;
     std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (g_scratch_ptr[dev] == nullptr) {
+    unsigned long long id = current_context_id();
+    if (id == 0 || g_scratch[dev].ctx_id != id) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_dispatch_scratch) != cudaSuccess || p == nullptr) {
             cudaGetLastError();
             return MOE_ERR_CUDA;
         }
-        g_scratch_ptr[dev] = static_cast<int32_t*>(p);
+        // the look-up makes the device's primary context current if nothing was; key the address by it
+        if (id == 0) id = current_context_id();
+        g_scratch[dev] = ScratchAddr{id, static_cast<int32_t*>(p)};  // id 0: look up again next call
     }
-    *out = g_scratch_ptr[dev];
+    *out = g_scratch[dev].ptr;
     return MOE_OK;
 }
 
@@ -59,9 +98,11 @@ moe_status moe_dispatch_static_scratch(const moe_config* cfg, const void* x, con
                                        const float* topk_gate, int32_t* slot, int32_t* expert_count,
                                        int32_t* expert_offset, int32_t* row_token, float* row_gate,
                                        void* x_dispatched, void* stream) {
-    // sizes and capacity exactly as moe_dispatch derives them (moe_capacity validates the config)
+    // the config is validated by the same planner as moe_dispatch's, with the same status; sizes and
+    // capacity exactly as moe_dispatch derives them
+    const moe_status plan = config_status(cfg);
+    if (plan != MOE_OK) return plan;
     const int32_t C = moe_capacity(cfg);
-    if (C < 0) return MOE_ERR_INVALID_ARG;
     const int T = cfg->tokens, k = cfg->top_k, E = cfg->num_experts, d = cfg->model_dim;
     if (T == 0) return MOE_OK;
     const int64_t nblk = ((int64_t)T + kTokensPerBlock - 1) / kTokensPerBlock;

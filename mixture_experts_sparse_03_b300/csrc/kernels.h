@@ -131,4 +131,9 @@ cudaError_t launch_combine(const float* y, const int* slot, const int* offset, c
                            const float* topk_gate, int T, int k, int d, float* out, cudaStream_t s);
 cudaError_t launch_zero(float* p, size_t n, cudaStream_t s);
 
+// ---- configuration ------------------------------------------------------------------------------
+// The status the library's own planner gives a config (MOE_OK, MOE_ERR_INVALID_ARG or
+// MOE_ERR_UNSUPPORTED), so that every entry point reports a bad config the same way.
+int32_t config_status(const void* cfg);
+
 }  // namespace moe

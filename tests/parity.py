@@ -171,3 +171,24 @@ def sample_tokens(T: int, n: int, seed: int = 0) -> np.ndarray:
         return np.arange(T, dtype=np.int32)
     rng = np.random.default_rng(seed)
     return np.sort(rng.choice(T, size=n, replace=False)).astype(np.int32)
+
+
+def segment_edge_tokens(idx: np.ndarray, slot: np.ndarray, E: int, C: int) -> np.ndarray:
+    """Tokens that own the rows at the edges of every expert's segment of the dispatched rows: slots 0,
+    127, 128 (either side of the first 128-row tile boundary) and the last kept slot (the expert's
+    last, usually partial, tile).  Checking their outputs reaches every expert's tile edges."""
+    T, k = idx.shape
+    counts = np.zeros(E, np.int64)
+    np.add.at(counts, idx[slot >= 0], 1)
+    kept = np.minimum(counts, C)
+    want = {}
+    for e in range(E):
+        for sl in (0, 127, 128, int(kept[e]) - 1):
+            if 0 <= sl < kept[e]:
+                want[(e, sl)] = None
+    toks = set()
+    t_idx, j_idx = np.nonzero(slot >= 0)
+    for t, j in zip(t_idx.tolist(), j_idx.tolist()):
+        if (int(idx[t, j]), int(slot[t, j])) in want:
+            toks.add(t)
+    return np.array(sorted(toks), dtype=np.int32)

@@ -178,3 +178,14 @@ def test_router_stats_host_validation():
                                 nbytes, None)
     assert st == 1  # dropped not 8-byte aligned
 
+
+
+@pytest.mark.parametrize("field,value,status", [("model_dim", 1 << 17, 2), ("hidden_size_per_expert", 1 << 17, 2),
+                                                ("model_dim", 96, 1), ("top_k", 0, 1)])
+def test_static_scratch_dispatch_rejects_configs_like_moe_dispatch(field, value, status):
+    """The dispatch without a caller workspace validates the config with the same planner as
+    moe_dispatch and returns the same status (unsupported sizes included), before any CUDA call."""
+    c = _bad(**{field: value})
+    nulls = [None] * 9
+    assert b.lib.moe_dispatch(ctypes.byref(c), *nulls, None, 0, None) == status
+    assert b.lib.moe_dispatch_static_scratch(ctypes.byref(c), *nulls, None) == status

@@ -165,14 +165,19 @@ def test_full_size_workload(name):
     g = P.run_steps(wl, tg)
     scores, nties, ndiff = P.check_routing(wl, tc, g)
     C, slot = P.check_dispatch(wl, tc["x"], g)
-    n = {"tiny_fp32": wl.T, "bf16_e8_k2": 48, "bf16_cosine_skew": 48, "bf16_noisy_e64": 10, "bf16_decode_e256": 6}[name]
-    toks = P.sample_tokens(wl.T, n, seed=wl.seed)
+    # random tokens plus the owners of every expert segment's edge rows (first row, either side of the
+    # first 128-row tile boundary, last kept row), so that every expert's last partial tile is checked
+    n = {"tiny_fp32": wl.T, "bf16_e8_k2": 64, "bf16_cosine_skew": 64, "bf16_noisy_e64": 128,
+         "bf16_decode_e256": wl.T}[name]
+    edges = P.segment_edge_tokens(g["idx"], slot, wl.E, C)
+    toks = np.union1d(P.sample_tokens(wl.T, n, seed=wl.seed), edges).astype(np.int32)
     ref = P.oracle_out(wl, tc, tg, scores, g["idx"], slot, toks)
     P.check_output(wl, g["out"], ref, toks)
     out, count = P.run_forward(wl, tg)
     assert np.array_equal(count, g["count"])
     P.check_output(wl, out, ref, toks)
-    print("%s: near-tie tokens %d, routing differences %d, drops %d" % (name, nties, ndiff, int((slot < 0).sum())))
+    print("%s: near-tie tokens %d, routing differences %d, drops %d, output checked on %d tokens (%d edge owners)"
+          % (name, nties, ndiff, int((slot < 0).sum()), len(toks), len(edges)))
 
 
 def _logits_error_ratio(wl, tc, tg):
