@@ -48,14 +48,19 @@ RIDGE_ROWS = 268  # bf16: FLOP per expert-weight byte = rows per expert; ridge =
 def kernel_names(wl, launches: int):
     """Names of the kernels moe_forward launches, in launch order (the softmax gate of a bf16 layer with
     E <= 64 runs as one fused launch)."""
+    rank = getattr(wl, "priority", "token") == "rank"  # slots in rank order: a separate rank kernel
     if wl.dtype == "bf16" and wl.gate == "softmax" and wl.E <= 64:
-        if -(-wl.T // 32) * wl.E <= 2048:  # a small histogram: the gather scans it (per CTA)
+        if rank:
+            names = ["gate_fused_gemm_topk", "dispatch_rank_scan", "dispatch_gather", "expert_up_gelu"]
+        elif -(-wl.T // 32) * wl.E <= 2048:  # a small histogram: the gather scans it (per CTA)
             names = ["gate_fused_gemm_topk", "dispatch_scan_gather", "expert_up_gelu"]
         else:
             names = ["gate_fused_gemm_topk_scan", "dispatch_gather", "expert_up_gelu"]
     elif wl.dtype == "bf16":
         names = ["gate_logits_gemm", "gate_topk"] + (["gate_cos_fold"] if wl.gate == "cosine" else [])
         names += ["gate_rescore", "dispatch_rank_scan", "dispatch_gather", "expert_up_gelu"]
+    elif rank:
+        names = ["gate_topk", "dispatch_rank_scan", "dispatch_gather", "expert_up_gelu"]
     else:
         names = ["gate_topk_scan", "dispatch_gather", "expert_up_gelu"]
     names += ["expert_down_combine"] if wl.k <= 2 else ["expert_down", "combine_gather"]
@@ -77,6 +82,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
     ap.add_argument("--only", action="store_true", help="measure the chosen workload only (no 'workloads' key)")
+    ap.add_argument("--experts", type=int, default=0,
+                    help="profiling aid: the chosen workload with this many experts and T scaled to keep the rows "
+                         "per expert (the same per-expert GEMM shapes on a smaller device footprint); implies --only")
     return ap.parse_args()
 
 
@@ -130,6 +138,73 @@ def job_throughput(world: int, steps: int, tokens: int, max_total_ms: float) -> 
 
 
 # ------------------------------------------------------------------------------------------ clocks
+class NvmlSampler:
+    """Reads the SM clock, power and clock-event reasons through NVML every few milliseconds on a host
+    thread (read-only queries), so that a timed region of tens of milliseconds still gets many samples."""
+
+    REASONS = (("hw_slowdown", "nvmlClocksEventReasonHwSlowdown"),
+               ("hw_thermal_slowdown", "nvmlClocksEventReasonHwThermalSlowdown"),
+               ("sw_thermal_slowdown", "nvmlClocksEventReasonSwThermalSlowdown"),
+               ("sw_power_cap", "nvmlClocksEventReasonSwPowerCap"))
+
+    def __init__(self, device_index: int, period_s: float = 0.002):
+        import threading
+
+        self.period = period_s
+        self.samples = []
+        self.stop_flag = threading.Event()
+        self.thread = None
+        self.nv = None
+        try:
+            import pynvml as nv
+
+            nv.nvmlInit()
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+            self.h = nv.nvmlDeviceGetHandleByUUID(uuid.encode())
+            self.nv = nv
+        except Exception:
+            self.nv = None
+
+    def _run(self):
+        nv = self.nv
+        while not self.stop_flag.is_set():
+            try:
+                sm = nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM)
+                pw = nv.nvmlDeviceGetPowerUsage(self.h) / 1000.0
+                rs = nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+                self.samples.append((sm, pw, rs))
+            except Exception:
+                return
+            time.sleep(self.period)
+
+    def start(self):
+        import threading
+
+        if self.nv is None:
+            return
+        self.thread = threading.Thread(target=self._run, daemon=True)
+        self.thread.start()
+
+    def stop(self):
+        if self.thread is None:
+            return None
+        self.stop_flag.set()
+        self.thread.join(timeout=2)
+        if not self.samples:
+            return None
+        nv = self.nv
+        sm = [s[0] for s in self.samples]
+        reasons = sorted({n for n, attr in self.REASONS for s in self.samples if s[2] & getattr(nv, attr, 0)})
+        try:
+            mx = nv.nvmlDeviceGetMaxClockInfo(self.h, nv.NVML_CLOCK_SM)
+        except Exception:
+            mx = max(sm)
+        return {"sm_mhz": statistics.median(sm), "sm_mhz_min": min(sm), "sm_max_mhz": mx,
+                "power_w_max": max(s[1] for s in self.samples), "reasons": reasons, "samples": len(sm),
+                "period_ms": self.period * 1e3}
+
+
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -219,8 +294,9 @@ class OneCore:
 
 def oracle_prefix(wl, tc, n: int):
     """The oracle's whole layer (scores, top-k, capacity dispatch, expert FFN, combine) on the first n
-    tokens of the workload.  Slots are assigned in token order, so a prefix's slots and outputs are
-    exactly the full layer's for those tokens (the capacity is the full workload's)."""
+    tokens of the workload, with the full workload's capacity.  With slots in token order a prefix's
+    slots and outputs are exactly the full layer's for those tokens; in rank order they are a sample of
+    the same work."""
     import oracle
 
     sl = (lambda t: None if t is None else t[:n])
@@ -228,7 +304,7 @@ def oracle_prefix(wl, tc, n: int):
                                 tc["emb"], wl.temperature)
     idx, gate = oracle.topk(scores, wl.k, wl.norm)
     C = oracle.capacity(wl.T, wl.E, wl.k, wl.capacity_factor, wl.capacity)
-    slot, _ = oracle.dispatch(idx, wl.E, C)
+    slot, _ = oracle.dispatch(idx, wl.E, C, wl.priority)
     return oracle.combine_tokens(np.arange(n, dtype=np.int32), tc["x"], idx, gate, slot, tc["w1"], tc["b1"],
                                  tc["w2"], tc["b2"])
 
@@ -445,6 +521,8 @@ def measure(wl, args, dev, stream, flush, world):
     stream.synchronize()
     sampler = ClockSampler(dev.index)
     sampler.start()
+    fine = NvmlSampler(dev.index)
+    fine.start()
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
@@ -458,6 +536,11 @@ def measure(wl, args, dev, stream, flush, world):
     if world > 1:
         torch.distributed.barrier()
     clocks = sampler.stop()
+    nvml = fine.stop()
+    if clocks is not None and nvml is not None:
+        clocks["nvml_2ms"] = nvml
+    elif nvml is not None:
+        clocks = dict(nvml, source="nvml")
     times = [a.elapsed_time(z) for a, z in evs]  # ms
     total_ms = max_over_ranks(sum(times), dev)
 
@@ -612,6 +695,18 @@ def config_of(wl, res, world):
                              "launch that the timed step has"}
 
 
+def scaled_workload(wl, experts: int):
+    """The workload with `experts` experts and its token count scaled by experts / E (same expected rows
+    per expert, same capacity when the capacity comes from the capacity factor)."""
+    if not experts or experts == wl.E:
+        return wl
+    if wl.T * experts % wl.E or experts < wl.k:
+        raise SystemExit("--experts %d does not scale T = %d evenly (E = %d, k = %d)" % (experts, wl.T, wl.E, wl.k))
+    T = wl.T * experts // wl.E
+    return wl.with_(name="%s_E%d" % (wl.name, experts), E=experts, T=T,
+                    capacity=(T if wl.capacity == wl.T else wl.capacity))
+
+
 def run_ours(args, rank, world, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
@@ -619,7 +714,9 @@ def run_ours(args, rank, world, local):
         import torch.distributed as dist
 
         dist.init_process_group("nccl", device_id=dev)
-    wl = WORKLOADS[args.workload]
+    wl = scaled_workload(WORKLOADS[args.workload], args.experts)
+    if args.experts:
+        args.only = True
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream(device=dev)
 

@@ -110,6 +110,13 @@ typedef struct moe_config {
  * tcgen05 cta_group::2); by default pairs are used when T * k / E >= 2048.  These flags force one. */
 #define MOE_FLAG_FFN_ONE_SM       4
 #define MOE_FLAG_FFN_SM_PAIR      8
+/* Capacity priority.  By default slots are handed out in token order (token t's pairs before token
+ * t + 1's; the workloads' "capacity slots in token order").  MOE_FLAG_RANK_MAJOR hands them out in rank
+ * order instead: every token's first choice, in token order, then every token's second choice, ... --
+ * the other reading of the "Tutel MoE guide"'s capacity_factor rule, under which a token's lower-ranked
+ * choices never take a slot from another token's first choice.  It changes which pairs overflow, not
+ * how a kept pair is computed.  Applies to moe_forward, moe_dispatch and moe_dispatch_static_scratch. */
+#define MOE_FLAG_RANK_MAJOR      16
 
 /* ---- sizes ------------------------------------------------------------------------------------ */
 /* Per-expert capacity C the dispatch step enforces, or -1 if the config is invalid. */
@@ -167,9 +174,10 @@ MOE_API moe_status moe_gate_logits(const moe_config* cfg, const void* x, const v
 /* ---- step 3: capacity-limited dispatch -------------------------------------------------------- */
 /* Groups the (token, expert) pairs by expert, ahead of one batched matmul per group ("How sparse
  * activation improves efficiency", section 3.1), under a per-expert capacity C (capacity_factor of the
- * "Tutel MoE guide" and of CANN's MOELayer in "MoE sparse-compute acceleration", section 3.2).  Slots are handed out in token order (for
- * one expert, token t precedes token t+1; a token never picks an expert twice); a pair whose slot is
- * >= C is dropped.  Outputs:
+ * "Tutel MoE guide" and of CANN's MOELayer in "MoE sparse-compute acceleration", section 3.2).  Slots
+ * are handed out in token order (for one expert, token t precedes token t+1; a token never picks an
+ * expert twice), or in rank order with MOE_FLAG_RANK_MAJOR; a pair whose slot is >= C is dropped.
+ * Outputs:
  *   slot          [T, k] int32   slot of each pair in its expert's queue, -1 if dropped
  *   expert_count  [E]    int32   pairs routed to each expert before the capacity limit
  *   expert_offset [E+1]  int32   first dispatched row of each expert; expert e owns rows
@@ -196,7 +204,8 @@ MOE_API moe_status moe_dispatch(const moe_config* cfg, const void* x, const int3
  * 256 + 4 * MOE_DISPATCH_STATIC_MAX_HIST bytes (1 MiB), which every GPU that loads the library holds
  * until the process exits.  The call allocates nothing (no cudaMalloc, no allocator of any library).
  *  - Limit.  Configs with ceil(T/32) * E > MOE_DISPATCH_STATIC_MAX_HIST return MOE_ERR_UNSUPPORTED and
- *    launch nothing (e.g. T = 16384 allows E <= 511; T = 65536 allows E <= 127).
+ *    launch nothing (e.g. T = 16384 allows E <= 511; T = 65536 allows E <= 127).  With
+ *    MOE_FLAG_RANK_MAJOR the histogram has ceil(T*k/32) rows instead of ceil(T/32).
  *  - Set-up.  The first call on each device looks up the array's device address (cudaGetSymbolAddress)
  *    with that device current; make that first call before any stream capture.  The address is kept
  *    per device and context: after a device reset (cudaDeviceReset) the next call looks it up again,
@@ -271,6 +280,32 @@ MOE_API moe_status moe_forward(const moe_config* cfg, const void* x, const void*
                        const void* expert_emb, const void* w1, const void* b1, const void* w2,
                        const void* b2, float* out, int32_t* expert_count, void* workspace,
                        size_t workspace_bytes, void* stream);
+
+/* ---- block-FP8 expert weights --------------------------------------------------------------------- */
+/* The same FFN step and whole layer with the expert weights stored as block FP8 ("MoE architecture:
+ * breaking the single-card compute bottleneck", section 1.3: FP8 weights shrink the model; the Block FP8
+ * rows of the "Tutel MoE guide" throughput table).  Reading taken (the pages fix no format):
+ *   w1_q [E, h, d], w2_q [E, d, h]   uint8 FP8 E4M3 codes (sign, 4 exponent bits with bias 7, 3 mantissa
+ *                                     bits; exponent field 0 is subnormal; 0x7F / 0xFF are NaN)
+ *   w1_scale [E, h/128, d/128], w2_scale [E, d/128, h/128]  fp32, one scale per 128 x 128 block
+ * and the layer computes with the dequantised weights  code value * scale  (everything else as in
+ * moe_expert_ffn / moe_forward: bf16 activations, fp32 accumulation).  The kernel widens the codes to bf16
+ * in shared memory (exact when the scales are powers of two, else the product is rounded to bf16) and
+ * streams one byte per weight from HBM.  Requires dtype MOE_BF16, d and h multiples of 128 and no
+ * MOE_FLAG_SIMT_FFN (else MOE_ERR_UNSUPPORTED); scales must be 4-byte aligned; the expert GEMMs run on
+ * single SMs whatever MOE_FLAG_FFN_SM_PAIR says.  Workspace, outputs and errors as the bf16 calls. */
+MOE_API moe_status moe_expert_ffn_fp8(const moe_config* cfg, const void* x_dispatched,
+                              const int32_t* expert_offset, const int32_t* row_token, const float* row_gate,
+                              const uint8_t* w1_q, const float* w1_scale, const void* b1,
+                              const uint8_t* w2_q, const float* w2_scale, const void* b2,
+                              float* y_dispatched, float* out, void* workspace, size_t workspace_bytes,
+                              void* stream);
+MOE_API moe_status moe_forward_fp8(const moe_config* cfg, const void* x, const void* w_gate,
+                           const void* w_noise, const float* noise_eps, const void* proj,
+                           const void* expert_emb, const uint8_t* w1_q, const float* w1_scale,
+                           const void* b1, const uint8_t* w2_q, const float* w2_scale, const void* b2,
+                           float* out, int32_t* expert_count, void* workspace, size_t workspace_bytes,
+                           void* stream);
 
 /* ---- diagnostics ------------------------------------------------------------------------------ */
 /* Synchronises `stream`, reads and clears the error word at the start of `workspace` and returns

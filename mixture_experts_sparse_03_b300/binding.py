@@ -16,7 +16,8 @@ import torch
 from .inputs import Workload
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libmoe_b300.so")
+# MOE_B300_LIB names another build of the same library (e.g. one compiled with different tuning macros)
+LIB_PATH = os.environ.get("MOE_B300_LIB") or os.path.join(_HERE, "libmoe_b300.so")
 HEADER = os.path.join(os.path.dirname(_HERE), "include", "moe_b300.h")
 
 MOE_OK = 0
@@ -29,6 +30,7 @@ FLAG_SIMT_FFN = 1
 FLAG_UNFUSED_COMBINE = 2
 FLAG_FFN_ONE_SM = 4
 FLAG_FFN_SM_PAIR = 8
+FLAG_RANK_MAJOR = 16
 
 
 class MoEConfig(ctypes.Structure):
@@ -77,6 +79,8 @@ def _load():
         "moe_combine": ([C, P, P, P, P, P, P, P], I32),
         "moe_router_stats": ([C, P, P, P, P, P, P, P, SZ, P], I32),
         "moe_forward": ([C, P, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P], I32),
+        "moe_expert_ffn_fp8": ([C, P, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P], I32),
+        "moe_forward_fp8": ([C, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P], I32),
         "moe_device_status": ([P, SZ, ctypes.POINTER(I32), P], I32),
         "moe_trace_events": ([ctypes.POINTER(P), I32], None),
         "moe_trace_count": ([], I32),
@@ -111,7 +115,7 @@ def config(wl: Workload, flags: int = 0, tokens: int | None = None) -> MoEConfig
     c.cos_dim = wl.cos_dim
     c.dtype = DTYPE[wl.dtype]
     c.cos_temperature = wl.temperature
-    c.flags = flags
+    c.flags = flags | (FLAG_RANK_MAJOR if wl.priority == "rank" else 0)
     c.reserved = 0
     return c
 
@@ -203,6 +207,20 @@ def moe_forward(cfg, x, w_gate, w_noise, noise_eps, proj, expert_emb, w1, b1, w2
                            ptr(workspace), workspace_bytes, stream_handle(stream))
 
 
+def moe_expert_ffn_fp8(cfg, x_dispatched, expert_offset, row_token, row_gate, w1_q, w1_scale, b1, w2_q, w2_scale,
+                       b2, y_dispatched, out, workspace, workspace_bytes, stream=None) -> int:
+    return lib.moe_expert_ffn_fp8(ctypes.byref(cfg), ptr(x_dispatched), ptr(expert_offset), ptr(row_token),
+                                  ptr(row_gate), ptr(w1_q), ptr(w1_scale), ptr(b1), ptr(w2_q), ptr(w2_scale), ptr(b2),
+                                  ptr(y_dispatched), ptr(out), ptr(workspace), workspace_bytes, stream_handle(stream))
+
+
+def moe_forward_fp8(cfg, x, w_gate, w_noise, noise_eps, proj, expert_emb, w1_q, w1_scale, b1, w2_q, w2_scale, b2,
+                    out, expert_count, workspace, workspace_bytes, stream=None) -> int:
+    return lib.moe_forward_fp8(ctypes.byref(cfg), ptr(x), ptr(w_gate), ptr(w_noise), ptr(noise_eps), ptr(proj),
+                               ptr(expert_emb), ptr(w1_q), ptr(w1_scale), ptr(b1), ptr(w2_q), ptr(w2_scale), ptr(b2),
+                               ptr(out), ptr(expert_count), ptr(workspace), workspace_bytes, stream_handle(stream))
+
+
 def moe_device_status(workspace, workspace_bytes, stream=None):
     info = ctypes.c_int32(0)
     st = lib.moe_device_status(ptr(workspace), workspace_bytes, ctypes.byref(info), stream_handle(stream))
@@ -242,6 +260,11 @@ def forward(cfg: MoEConfig, t: dict, out=None, expert_count=None, ws=None, strea
         out = torch.empty((cfg.tokens, cfg.model_dim), dtype=torch.float32, device=x.device)
     if ws is None:
         ws = workspace(cfg, x.device)
+    if t.get("w1_scale") is not None:  # block-FP8 expert weights
+        check(moe_forward_fp8(cfg, x, t.get("w_gate"), t.get("w_noise"), t.get("eps"), t.get("proj"), t.get("emb"),
+                              t["w1"], t["w1_scale"], t.get("b1"), t["w2"], t["w2_scale"], t.get("b2"), out,
+                              expert_count, ws, ws.numel(), stream), "moe_forward_fp8")
+        return out
     check(moe_forward(cfg, x, t.get("w_gate"), t.get("w_noise"), t.get("eps"), t.get("proj"), t.get("emb"), t["w1"],
                       t.get("b1"), t["w2"], t.get("b2"), out, expert_count, ws, ws.numel(), stream), "moe_forward")
     return out

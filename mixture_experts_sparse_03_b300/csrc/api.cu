@@ -23,6 +23,8 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 struct Plan {
     int T, d, h, E, k, C, Ceff, p, nblk, gate, norm, bf16, esize, fused;
+    int rank_major;     // capacity slots in (rank, token) order
+    int nblk_hist;      // blocks of the dispatch histogram: of 32 tokens, or of 32 (rank, token) pairs
     int N0, N1;         // gate logits from the first / second weight tensor
     int pair;           // expert GEMMs on pairs of SMs
     GateGemmPlan gg;    // tensor-core logits GEMM (bf16 layers)
@@ -63,7 +65,8 @@ moe_status make_plan(const moe_config* c, Plan* pl) {
     if (c->dtype != MOE_F32 && c->dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
     if (P.gate < MOE_GATE_SOFTMAX || P.gate > MOE_GATE_COSINE) return MOE_ERR_INVALID_ARG;
     if (P.norm != MOE_GATE_NORM_ALL && P.norm != MOE_GATE_NORM_TOPK) return MOE_ERR_INVALID_ARG;
-    if (c->flags & ~(MOE_FLAG_SIMT_FFN | MOE_FLAG_UNFUSED_COMBINE | MOE_FLAG_FFN_ONE_SM | MOE_FLAG_FFN_SM_PAIR))
+    if (c->flags & ~(MOE_FLAG_SIMT_FFN | MOE_FLAG_UNFUSED_COMBINE | MOE_FLAG_FFN_ONE_SM | MOE_FLAG_FFN_SM_PAIR |
+                     MOE_FLAG_RANK_MAJOR))
         return MOE_ERR_INVALID_ARG;
     if ((c->flags & MOE_FLAG_FFN_ONE_SM) && (c->flags & MOE_FLAG_FFN_SM_PAIR)) return MOE_ERR_INVALID_ARG;
     if (c->reserved != 0) return MOE_ERR_INVALID_ARG;
@@ -92,6 +95,8 @@ moe_status make_plan(const moe_config* c, Plan* pl) {
     P.rows = std::min<int64_t>((int64_t)P.T * P.k + (int64_t)(kRowAlign - 1) * P.E, (int64_t)P.E * cpad);
     if (P.rows > (int64_t)1 << 30) return MOE_ERR_UNSUPPORTED;
     P.nblk = (P.T + kTokensPerBlock - 1) / kTokensPerBlock;
+    P.rank_major = (c->flags & MOE_FLAG_RANK_MAJOR) != 0;
+    P.nblk_hist = dispatch_hist_blocks(P.T, P.k, P.rank_major);
     P.fused = P.k <= 2 && !(c->flags & MOE_FLAG_UNFUSED_COMBINE);
     // pairs of SMs pay off when experts get many rows: their 256-row tiles waste at most 128 rows per
     // expert, against 2x the rows each weight byte serves
@@ -106,7 +111,7 @@ moe_status make_plan(const moe_config* c, Plan* pl) {
     P.o_idx = take(4 * tk);
     P.o_gate = take(4 * tk);
     P.o_slot = take(4 * tk);
-    P.o_hist = take(4 * (size_t)P.nblk * P.E);
+    P.o_hist = take(4 * (size_t)P.nblk_hist * P.E);
     P.o_count = take(4 * (size_t)P.E);
     P.o_off = take(4 * (size_t)(P.E + 1));
     P.o_rtok = take(4 * (size_t)P.rows);
@@ -262,15 +267,19 @@ moe_status run_gate(const Plan& P, GateParams& g, void* ws, cudaStream_t s) {
     if (g.blk_hist == nullptr) return MOE_OK;
     return launch(s, [&] {
         return launch_dispatch_rank(g.topk_idx, P.T, P.k, P.E, g.blk_hist, g.slot, g.err, g.ticket, g.C, g.count,
-                                    g.offset, g.row_token, g.row_gate, s);
+                                    g.offset, g.row_token, g.row_gate, P.rank_major, s);
     });
 }
 
-FfnParams ffn_params(const Plan& P, int mode, const void* A, const void* W, const void* bias, const int* off,
-                     const int* rtok, const float* rgate, void* C, float* out, int* err) {
+// the gate kernel itself ranks the pairs (in token order) and scans: the fused bf16 gate and the fp32 gate
+bool gate_ranks_in_kernel(const Plan& P) { return !P.bf16 || P.gg.fused; }
+
+FfnParams ffn_params(const Plan& P, int mode, const void* A, const void* W, const float* w_scale, const void* bias,
+                     const int* off, const int* rtok, const float* rgate, void* C, float* out, int* err) {
     FfnParams f{};
     f.A = A;
     f.W = W;
+    f.w_scale = w_scale;
     f.bias = bias;
     f.offset = off;
     f.row_token = rtok;
@@ -284,7 +293,7 @@ FfnParams ffn_params(const Plan& P, int mode, const void* A, const void* W, cons
     f.mode = mode;
     f.rows_cap = P.rows;
     f.err = err;
-    f.pair = P.pair;
+    f.pair = w_scale ? 0 : P.pair;  // block-FP8 weights run on single SMs
     return f;
 }
 
@@ -293,15 +302,115 @@ moe_status run_ffn(const Plan& P, const moe_config* c, const FfnParams& f, cudaS
     return launch(s, [&] { return tc ? launch_ffn_tc(f, s) : launch_ffn_simt(f, s); });
 }
 
-// expert FFN + (fused or separate) combine, shared by moe_expert_ffn and moe_forward
+// expert FFN + (fused or separate) combine, shared by moe_expert_ffn(_fp8) and moe_forward(_fp8); s1 / s2
+// are the block scales of FP8 weights (nullptr: bf16 / fp32 weights)
 moe_status ffn_and_combine(const Plan& P, const moe_config* c, const void* xd, const int* off, const int* rtok,
-                           const float* rgate, const void* w1, const void* b1, const void* w2, const void* b2,
-                           float* y, float* out, bool fused, void* ws, cudaStream_t s) {
+                           const float* rgate, const void* w1, const float* s1, const void* b1, const void* w2,
+                           const float* s2, const void* b2, float* y, float* out, bool fused, void* ws,
+                           cudaStream_t s) {
     int* err = at<int>(ws, P.o_err);
     void* hbuf = at<void>(ws, P.o_h);
-    MOE_TRY(run_ffn(P, c, ffn_params(P, 0, xd, w1, b1, off, rtok, rgate, hbuf, nullptr, err), s));
-    if (fused) return run_ffn(P, c, ffn_params(P, 2, hbuf, w2, b2, off, rtok, rgate, nullptr, out, err), s);
-    return run_ffn(P, c, ffn_params(P, 1, hbuf, w2, b2, off, rtok, rgate, y, nullptr, err), s);
+    MOE_TRY(run_ffn(P, c, ffn_params(P, 0, xd, w1, s1, b1, off, rtok, rgate, hbuf, nullptr, err), s));
+    if (fused) return run_ffn(P, c, ffn_params(P, 2, hbuf, w2, s2, b2, off, rtok, rgate, nullptr, out, err), s);
+    return run_ffn(P, c, ffn_params(P, 1, hbuf, w2, s2, b2, off, rtok, rgate, y, nullptr, err), s);
+}
+
+// block-FP8 weights: bf16 activations on the tensor cores, d and h multiples of the 128-wide scale blocks
+moe_status check_fp8_weights(const Plan& P, const moe_config* c, const void* w1, const float* s1, const void* w2,
+                             const float* s2) {
+    if (!P.bf16 || (c->flags & MOE_FLAG_SIMT_FFN)) return MOE_ERR_UNSUPPORTED;
+    if (P.d % 128 || P.h % 128) return MOE_ERR_UNSUPPORTED;
+    if (!w1 || !w2 || !s1 || !s2 || !aligned16(w1) || !aligned16(w2)) return MOE_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(s1) & 3) || (reinterpret_cast<uintptr_t>(s2) & 3)) return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+}
+
+}  // namespace
+
+namespace {
+
+moe_status expert_ffn_impl(const moe_config* cfg, const void* x_dispatched, const int32_t* expert_offset,
+                           const int32_t* row_token, const float* row_gate, const void* w1, const float* s1,
+                           const void* b1, const void* w2, const float* s2, const void* b2, float* y_dispatched,
+                           float* out, void* workspace, size_t workspace_bytes, void* stream) {
+    Plan P;
+    MOE_TRY(make_plan(cfg, &P));
+    if (s1 || s2) MOE_TRY(check_fp8_weights(P, cfg, w1, s1, w2, s2));
+    if (P.T == 0) return MOE_OK;
+    MOE_TRY(check_ws(P, workspace, workspace_bytes));
+    const void* ptrs[] = {x_dispatched, expert_offset, row_token, row_gate, w1, w2};
+    for (const void* q : ptrs)
+        if (!q || !aligned16(q)) return MOE_ERR_INVALID_ARG;
+    if ((b1 && !aligned16(b1)) || (b2 && !aligned16(b2))) return MOE_ERR_INVALID_ARG;
+    const bool fused = y_dispatched == nullptr;
+    if (fused ? (!out || !aligned16(out)) : !aligned16(y_dispatched)) return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(at<int>(workspace, P.o_err), 0, 8, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (fused) MOE_TRY(launch(s, [&] { return launch_zero(out, (size_t)P.T * P.d, s); }));
+    return ffn_and_combine(P, cfg, x_dispatched, expert_offset, row_token, row_gate, w1, s1, b1, w2, s2, b2,
+                           y_dispatched, out, fused, workspace, s);
+}
+}  // namespace
+
+namespace {
+
+moe_status forward_impl(const moe_config* cfg, const void* x, const void* w_gate, const void* w_noise,
+                        const float* noise_eps, const void* proj, const void* expert_emb, const void* w1,
+                        const float* s1, const void* b1, const void* w2, const float* s2, const void* b2, float* out,
+                        int32_t* expert_count, void* workspace, size_t workspace_bytes, void* stream) {
+    Plan P;
+    MOE_TRY(make_plan(cfg, &P));
+    if (s1 || s2) MOE_TRY(check_fp8_weights(P, cfg, w1, s1, w2, s2));
+    if (P.T == 0) return MOE_OK;
+    MOE_TRY(check_ws(P, workspace, workspace_bytes));
+    int32_t* idx = at<int32_t>(workspace, P.o_idx);
+    float* gate = at<float>(workspace, P.o_gate);
+    MOE_TRY(check_route_args(P, x, w_gate, w_noise, noise_eps, proj, expert_emb, idx, gate));
+    if (!w1 || !w2 || !out || !aligned16(w1) || !aligned16(w2) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
+    if ((b1 && !aligned16(b1)) || (b2 && !aligned16(b2)) || (expert_count && !aligned16(expert_count)))
+        return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int* err = at<int>(workspace, P.o_err);
+    int* hist = at<int>(workspace, P.o_hist);
+    int* count = expert_count ? expert_count : at<int>(workspace, P.o_count);
+    int* off = at<int>(workspace, P.o_off);
+    int* slot = at<int>(workspace, P.o_slot);
+    int* rtok = at<int>(workspace, P.o_rtok);
+    float* rgate = at<float>(workspace, P.o_rgate);
+    void* xd = at<void>(workspace, P.o_xd);
+    float* y = at<float>(workspace, P.o_y);
+    // error word, its info, the block tickets and the cosine gate's expert flags start at zero
+    if (cudaMemsetAsync(err, 0, P.hdr_bytes, s) != cudaSuccess) return MOE_ERR_CUDA;
+    GateParams g = gate_params(P, cfg, x, w_gate, w_noise, noise_eps, proj, expert_emb, idx, gate);
+    // with rank priority a gate kernel that ranks in token order leaves the ranking to the rank kernel
+    const bool rank_after_gate = P.rank_major && gate_ranks_in_kernel(P);
+    g.blk_hist = rank_after_gate ? nullptr : hist;
+    g.slot = slot;
+    g.err = err;
+    // a small histogram (fused softmax gate) is scanned by the gather itself, every CTA for its own
+    // blocks: the gate then skips its ticket and last-CTA scan
+    const bool gather_scan = !P.rank_major && P.bf16 && P.gg.fused && P.E <= kGatherScanMaxE &&
+                             (int64_t)P.nblk * P.E <= kGatherScanMaxHist;
+    g.ticket = gather_scan ? nullptr : err + 2;
+    g.C = P.Ceff;
+    g.count = count;
+    g.offset = off;
+    g.row_token = rtok;
+    g.row_gate = rgate;
+    MOE_TRY(run_gate(P, g, workspace, s));
+    if (rank_after_gate)
+        MOE_TRY(launch(s, [&] {
+            return launch_dispatch_rank(idx, P.T, P.k, P.E, hist, slot, err, err + 2, P.Ceff, count, off, rtok, rgate,
+                                        1, s);
+        }));
+    MOE_TRY(launch(s, [&] {
+        return launch_dispatch_gather(x, P.bf16, idx, gate, hist, off, count, gather_scan, P.T, P.k, P.E, P.d, P.Ceff,
+                                      slot, rtok, rgate,
+                                      xd, P.fused ? out : nullptr, P.rank_major, s);
+    }));
+    MOE_TRY(ffn_and_combine(P, cfg, xd, off, rtok, rgate, w1, s1, b1, w2, s2, b2, y, out, P.fused != 0, workspace, s));
+    if (!P.fused) MOE_TRY(launch(s, [&] { return launch_combine(y, slot, off, idx, gate, P.T, P.k, P.d, out, s); }));
+    return MOE_OK;
 }
 
 }  // namespace
@@ -335,7 +444,8 @@ int32_t moe_forward_launches(const moe_config* cfg) {
     if (make_plan(cfg, &P) != MOE_OK) return -1;
     if (P.T == 0) return 0;
     const int gate_extra = P.bf16 && !P.gg.fused ? 3 + (P.gate == MOE_GATE_COSINE ? 1 : 0) : 0;
-    return (P.fused ? 4 : 5) + gate_extra;
+    const int rank_extra = P.rank_major && gate_ranks_in_kernel(P) ? 1 : 0;  // a separate rank kernel
+    return (P.fused ? 4 : 5) + gate_extra + rank_extra;
 }
 
 moe_status moe_route(const moe_config* cfg, const void* x, const void* w_gate, const void* w_noise,
@@ -394,35 +504,34 @@ moe_status moe_dispatch(const moe_config* cfg, const void* x, const int32_t* top
     if (cudaMemsetAsync(err, 0, 16, s) != cudaSuccess) return MOE_ERR_CUDA;
     MOE_TRY(launch(s, [&] {
         return launch_dispatch_rank(topk_idx, P.T, P.k, P.E, hist, slot, err, err + 2, P.Ceff, expert_count,
-                                    expert_offset, row_token, row_gate, s);
+                                    expert_offset, row_token, row_gate, P.rank_major, s);
     }));
     return launch(s, [&] {
         return launch_dispatch_gather(x, P.bf16, topk_idx, topk_gate, hist, expert_offset, nullptr, false, P.T, P.k,
                                       P.E, P.d, P.Ceff,
-                                      slot, row_token, row_gate, x_dispatched, nullptr, s);
+                                      slot, row_token, row_gate, x_dispatched, nullptr, P.rank_major, s);
     });
 }
+
 
 moe_status moe_expert_ffn(const moe_config* cfg, const void* x_dispatched, const int32_t* expert_offset,
                           const int32_t* row_token, const float* row_gate, const void* w1, const void* b1,
                           const void* w2, const void* b2, float* y_dispatched, float* out, void* workspace,
                           size_t workspace_bytes, void* stream) {
     NvtxRange nvtx_("moe_expert_ffn");
-    Plan P;
-    MOE_TRY(make_plan(cfg, &P));
-    if (P.T == 0) return MOE_OK;
-    MOE_TRY(check_ws(P, workspace, workspace_bytes));
-    const void* ptrs[] = {x_dispatched, expert_offset, row_token, row_gate, w1, w2};
-    for (const void* q : ptrs)
-        if (!q || !aligned16(q)) return MOE_ERR_INVALID_ARG;
-    if ((b1 && !aligned16(b1)) || (b2 && !aligned16(b2))) return MOE_ERR_INVALID_ARG;
-    const bool fused = y_dispatched == nullptr;
-    if (fused ? (!out || !aligned16(out)) : !aligned16(y_dispatched)) return MOE_ERR_INVALID_ARG;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (cudaMemsetAsync(at<int>(workspace, P.o_err), 0, 8, s) != cudaSuccess) return MOE_ERR_CUDA;
-    if (fused) MOE_TRY(launch(s, [&] { return launch_zero(out, (size_t)P.T * P.d, s); }));
-    return ffn_and_combine(P, cfg, x_dispatched, expert_offset, row_token, row_gate, w1, b1, w2, b2, y_dispatched,
-                           out, fused, workspace, s);
+    return expert_ffn_impl(cfg, x_dispatched, expert_offset, row_token, row_gate, w1, nullptr, b1, w2, nullptr, b2,
+                           y_dispatched, out, workspace, workspace_bytes, stream);
+}
+
+moe_status moe_expert_ffn_fp8(const moe_config* cfg, const void* x_dispatched, const int32_t* expert_offset,
+                              const int32_t* row_token, const float* row_gate, const uint8_t* w1_q,
+                              const float* w1_scale, const void* b1, const uint8_t* w2_q, const float* w2_scale,
+                              const void* b2, float* y_dispatched, float* out, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+    NvtxRange nvtx_("moe_expert_ffn_fp8");
+    if (!w1_scale || !w2_scale) return MOE_ERR_INVALID_ARG;
+    return expert_ffn_impl(cfg, x_dispatched, expert_offset, row_token, row_gate, w1_q, w1_scale, b1, w2_q, w2_scale,
+                           b2, y_dispatched, out, workspace, workspace_bytes, stream);
 }
 
 moe_status moe_combine(const moe_config* cfg, const float* y_dispatched, const int32_t* slot,
@@ -441,55 +550,25 @@ moe_status moe_combine(const moe_config* cfg, const float* y_dispatched, const i
     });
 }
 
+
 moe_status moe_forward(const moe_config* cfg, const void* x, const void* w_gate, const void* w_noise,
                        const float* noise_eps, const void* proj, const void* expert_emb, const void* w1,
                        const void* b1, const void* w2, const void* b2, float* out, int32_t* expert_count,
                        void* workspace, size_t workspace_bytes, void* stream) {
     NvtxRange nvtx_("moe_forward");
-    Plan P;
-    MOE_TRY(make_plan(cfg, &P));
-    if (P.T == 0) return MOE_OK;
-    MOE_TRY(check_ws(P, workspace, workspace_bytes));
-    int32_t* idx = at<int32_t>(workspace, P.o_idx);
-    float* gate = at<float>(workspace, P.o_gate);
-    MOE_TRY(check_route_args(P, x, w_gate, w_noise, noise_eps, proj, expert_emb, idx, gate));
-    if (!w1 || !w2 || !out || !aligned16(w1) || !aligned16(w2) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
-    if ((b1 && !aligned16(b1)) || (b2 && !aligned16(b2)) || (expert_count && !aligned16(expert_count)))
-        return MOE_ERR_INVALID_ARG;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    int* err = at<int>(workspace, P.o_err);
-    int* hist = at<int>(workspace, P.o_hist);
-    int* count = expert_count ? expert_count : at<int>(workspace, P.o_count);
-    int* off = at<int>(workspace, P.o_off);
-    int* slot = at<int>(workspace, P.o_slot);
-    int* rtok = at<int>(workspace, P.o_rtok);
-    float* rgate = at<float>(workspace, P.o_rgate);
-    void* xd = at<void>(workspace, P.o_xd);
-    float* y = at<float>(workspace, P.o_y);
-    // error word, its info, the block tickets and the cosine gate's expert flags start at zero
-    if (cudaMemsetAsync(err, 0, P.hdr_bytes, s) != cudaSuccess) return MOE_ERR_CUDA;
-    GateParams g = gate_params(P, cfg, x, w_gate, w_noise, noise_eps, proj, expert_emb, idx, gate);
-    g.blk_hist = hist;
-    g.slot = slot;
-    g.err = err;
-    // a small histogram (fused softmax gate) is scanned by the gather itself, every CTA for its own
-    // blocks: the gate then skips its ticket and last-CTA scan
-    const bool gather_scan = P.bf16 && P.gg.fused && P.E <= kGatherScanMaxE && (int64_t)P.nblk * P.E <= kGatherScanMaxHist;
-    g.ticket = gather_scan ? nullptr : err + 2;
-    g.C = P.Ceff;
-    g.count = count;
-    g.offset = off;
-    g.row_token = rtok;
-    g.row_gate = rgate;
-    MOE_TRY(run_gate(P, g, workspace, s));
-    MOE_TRY(launch(s, [&] {
-        return launch_dispatch_gather(x, P.bf16, idx, gate, hist, off, count, gather_scan, P.T, P.k, P.E, P.d, P.Ceff,
-                                      slot, rtok, rgate,
-                                      xd, P.fused ? out : nullptr, s);
-    }));
-    MOE_TRY(ffn_and_combine(P, cfg, xd, off, rtok, rgate, w1, b1, w2, b2, y, out, P.fused != 0, workspace, s));
-    if (!P.fused) MOE_TRY(launch(s, [&] { return launch_combine(y, slot, off, idx, gate, P.T, P.k, P.d, out, s); }));
-    return MOE_OK;
+    return forward_impl(cfg, x, w_gate, w_noise, noise_eps, proj, expert_emb, w1, nullptr, b1, w2, nullptr, b2, out,
+                        expert_count, workspace, workspace_bytes, stream);
+}
+
+moe_status moe_forward_fp8(const moe_config* cfg, const void* x, const void* w_gate, const void* w_noise,
+                           const float* noise_eps, const void* proj, const void* expert_emb, const uint8_t* w1_q,
+                           const float* w1_scale, const void* b1, const uint8_t* w2_q, const float* w2_scale,
+                           const void* b2, float* out, int32_t* expert_count, void* workspace, size_t workspace_bytes,
+                           void* stream) {
+    NvtxRange nvtx_("moe_forward_fp8");
+    if (!w1_scale || !w2_scale) return MOE_ERR_INVALID_ARG;
+    return forward_impl(cfg, x, w_gate, w_noise, noise_eps, proj, expert_emb, w1_q, w1_scale, b1, w2_q, w2_scale, b2,
+                        out, expert_count, workspace, workspace_bytes, stream);
 }
 
 moe_status moe_router_stats(const moe_config* cfg, const int32_t* topk_idx, const float* topk_gate,

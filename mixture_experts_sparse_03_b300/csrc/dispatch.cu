@@ -18,6 +18,9 @@
 //   gather  one warp per pair: slot = prefix[b][e] + rank, kept iff slot < C, row = off[e] + slot;
 //           the row of x is copied with 16-byte loads, eight in flight per lane; the same grid also
 //           zeroes the output when the combine is fused into the expert GEMM
+// With rank priority (every token's first choice before any second choice) the rank and gather steps
+// walk the pairs in (rank, token) order instead: virtual item v = j * T + t stands for pair (t, j), and
+// the blocks are 32 consecutive virtual items, so the same rank / scan / gather machinery numbers them.
 // No step depends on scheduling order, so the result is deterministic.
 #include "common.cuh"
 #include "kernels.h"
@@ -36,7 +39,7 @@ __global__ void __launch_bounds__(32 * kRankWarps) rank_kernel(const int* __rest
                                                               int E, int* __restrict__ blk_hist,
                                                               int* __restrict__ rank, int* err, int* ticket, int C,
                                                               int* count, int* offset, int* row_token,
-                                                              float* row_gate) {
+                                                              float* row_gate, int rank_major) {
     extern __shared__ int running_all[];  // [kRankWarps][E]
     __shared__ int part[32 * kRankWarps];
     __shared__ int padded[kMaxExperts + 1];
@@ -46,23 +49,30 @@ __global__ void __launch_bounds__(32 * kRankWarps) rank_kernel(const int* __rest
     pdl_wait();
     pdl_trigger();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int nblk = (T + kBT - 1) / kBT;
+    const int nblk = rank_major ? (int)(((long)T * k + kBT - 1) / kBT) : (T + kBT - 1) / kBT;
     const int b = blockIdx.x * kRankWarps + warp;
     if (b < nblk) {
         int* running = running_all + (size_t)warp * E;
         for (int e = lane; e < E; e += 32) running[e] = 0;
         __syncwarp();
-        const int t0 = b * kBT;
-        const int* ids = topk_idx + (size_t)t0 * k;
         bool bad = false;
-        rank_pairs_warp(
-            [&](int i) {
-                const int e = ids[i];
-                const bool ok = e >= 0 && e < E;
-                bad |= !ok;
-                return ok ? e : -2;  // an out-of-range id takes no slot
-            },
-            min(kBT, T - t0) * k, running, rank + (size_t)t0 * k, lane);
+        auto checked = [&](int e) {
+            const bool ok = e >= 0 && e < E;
+            bad |= !ok;
+            return ok ? e : -2;  // an out-of-range id takes no slot
+        };
+        if (rank_major) {  // 32 virtual items v = j * T + t, item i of the block is pair (t, j)
+            const long v0 = (long)b * kBT;
+            auto pair_of = [&](int i) { const long v = v0 + i; return (v % T) * k + v / T; };
+            rank_pairs_warp_to([&](int i) { return checked(topk_idx[pair_of(i)]); },
+                               (int)min((long)kBT, (long)T * k - v0), running,
+                               [&](int i, int r) { rank[pair_of(i)] = r; }, lane);
+        } else {
+            const int t0 = b * kBT;
+            const int* ids = topk_idx + (size_t)t0 * k;
+            rank_pairs_warp([&](int i) { return checked(ids[i]); }, min(kBT, T - t0) * k, running,
+                            rank + (size_t)t0 * k, lane);
+        }
         if (bad) record_error(err, kErrCheck, kWhereDispatch);
         __syncwarp();
         for (int e = lane; e < E; e += 32) blk_hist[(size_t)b * E + e] = running[e];
@@ -91,7 +101,7 @@ __global__ void __launch_bounds__(32 * kGatherWarps) gather_kernel(
     const T* __restrict__ x, const int* __restrict__ topk_idx, const float* __restrict__ topk_gate,
     const int* __restrict__ blk_hist, int* __restrict__ offset, int* __restrict__ count, int T_, int k, int E,
     int d, int C, int* __restrict__ slot, int* __restrict__ row_token, float* __restrict__ row_gate,
-    T* __restrict__ xd, float* __restrict__ out_zero) {
+    T* __restrict__ xd, float* __restrict__ out_zero, int rank_major) {
     __shared__ int s_pre[2][kGatherScanMaxE];  // prefix of blocks b_lo and b_lo + 1
     __shared__ int s_off[kGatherScanMaxE + 1];
     __shared__ int s_kept[kGatherScanMaxE];
@@ -187,7 +197,9 @@ __global__ void __launch_bounds__(32 * kGatherWarps) gather_kernel(
                 if (s < C) r = s_off[e] + s;
                 else s = -1;
             } else {
-                s = blk_hist[(size_t)b * E + e] + rk;
+                // rank priority: the pair's block in (rank, token) order
+                const int bb = rank_major ? (int)(((long)(p % k) * T_ + t) / kBT) : b;
+                s = blk_hist[(size_t)bb * E + e] + rk;
                 if (s < C) r = offset[e] + s;
                 else s = -1;
             }
@@ -228,24 +240,25 @@ __global__ void __launch_bounds__(32 * kGatherWarps) gather_kernel(
 
 cudaError_t launch_dispatch_rank(const int* topk_idx, int T, int k, int E, int* blk_hist, int* rank, int* err,
                                  int* ticket, int C, int* count, int* offset, int* row_token, float* row_gate,
-                                 cudaStream_t s) {
+                                 int rank_major, cudaStream_t s) {
     if (T <= 0) return cudaSuccess;
-    const int nblk = (T + kBT - 1) / kBT;
+    const int nblk = rank_major ? (int)(((long)T * k + kBT - 1) / kBT) : (T + kBT - 1) / kBT;
     const size_t smem = sizeof(int) * (size_t)kRankWarps * E;
     if (smem > 48 * 1024) {
         const cudaError_t e = cudaFuncSetAttribute(rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }
     return launch_pdl(rank_kernel, dim3((nblk + kRankWarps - 1) / kRankWarps), dim3(32 * kRankWarps), smem, s,
-                      topk_idx, T, k, E, blk_hist, rank, err, ticket, C, count, offset, row_token, row_gate);
+                      topk_idx, T, k, E, blk_hist, rank, err, ticket, C, count, offset, row_token, row_gate,
+                      rank_major);
 }
 
 cudaError_t launch_dispatch_gather(const void* x, int bf16, const int* topk_idx, const float* topk_gate,
                                    const int* blk_hist, int* offset, int* count, bool scan, int T, int k, int E,
                                    int d, int C, int* slot, int* row_token, float* row_gate, void* x_dispatched,
-                                   float* out_to_zero, cudaStream_t s) {
+                                   float* out_to_zero, int rank_major, cudaStream_t s) {
     if (T <= 0) return cudaSuccess;
-    if (scan && E > kGatherScanMaxE) return cudaErrorInvalidValue;
+    if (scan && (E > kGatherScanMaxE || rank_major)) return cudaErrorInvalidValue;
     const long npairs = (long)T * k;
     const unsigned blocks = (unsigned)((npairs + kGatherWarps - 1) / kGatherWarps);
     const dim3 grid(blocks), block(32 * kGatherWarps);
@@ -254,17 +267,17 @@ cudaError_t launch_dispatch_gather(const void* x, int bf16, const int* topk_idx,
         auto xo = static_cast<bf16_t*>(x_dispatched);
         if (scan)
             return launch_pdl(gather_kernel<bf16_t, true>, grid, block, 0, s, xp, topk_idx, topk_gate, blk_hist,
-                              offset, count, T, k, E, d, C, slot, row_token, row_gate, xo, out_to_zero);
+                              offset, count, T, k, E, d, C, slot, row_token, row_gate, xo, out_to_zero, rank_major);
         return launch_pdl(gather_kernel<bf16_t, false>, grid, block, 0, s, xp, topk_idx, topk_gate, blk_hist, offset,
-                          count, T, k, E, d, C, slot, row_token, row_gate, xo, out_to_zero);
+                          count, T, k, E, d, C, slot, row_token, row_gate, xo, out_to_zero, rank_major);
     }
     auto xp = static_cast<const float*>(x);
     auto xo = static_cast<float*>(x_dispatched);
     if (scan)
         return launch_pdl(gather_kernel<float, true>, grid, block, 0, s, xp, topk_idx, topk_gate, blk_hist, offset,
-                          count, T, k, E, d, C, slot, row_token, row_gate, xo, out_to_zero);
+                          count, T, k, E, d, C, slot, row_token, row_gate, xo, out_to_zero, rank_major);
     return launch_pdl(gather_kernel<float, false>, grid, block, 0, s, xp, topk_idx, topk_gate, blk_hist, offset,
-                      count, T, k, E, d, C, slot, row_token, row_gate, xo, out_to_zero);
+                      count, T, k, E, d, C, slot, row_token, row_gate, xo, out_to_zero, rank_major);
 }
 
 }  // namespace moe

@@ -105,7 +105,8 @@ moe_status moe_dispatch_static_scratch(const moe_config* cfg, const void* x, con
     const int32_t C = moe_capacity(cfg);
     const int T = cfg->tokens, k = cfg->top_k, E = cfg->num_experts, d = cfg->model_dim;
     if (T == 0) return MOE_OK;
-    const int64_t nblk = ((int64_t)T + kTokensPerBlock - 1) / kTokensPerBlock;
+    const int rank_major = (cfg->flags & MOE_FLAG_RANK_MAJOR) != 0;
+    const int64_t nblk = dispatch_hist_blocks(T, k, rank_major);
     if (nblk * E > (int64_t)MOE_DISPATCH_STATIC_MAX_HIST) return MOE_ERR_UNSUPPORTED;
     const void* ptrs[] = {x, topk_idx, topk_gate, slot, expert_count, expert_offset, row_token, row_gate, x_dispatched};
     for (const void* q : ptrs)
@@ -122,11 +123,11 @@ moe_status moe_dispatch_static_scratch(const moe_config* cfg, const void* x, con
     // before it is read
     if (cudaMemsetAsync(err, 0, 16, s) != cudaSuccess) return MOE_ERR_CUDA;
     if (launch_dispatch_rank(topk_idx, T, k, E, hist, slot, err, err + 2, Ceff, expert_count, expert_offset,
-                             row_token, row_gate, s) != cudaSuccess)
+                             row_token, row_gate, rank_major, s) != cudaSuccess)
         return MOE_ERR_CUDA;
     if (launch_dispatch_gather(x, bf16, topk_idx, topk_gate, hist, expert_offset, nullptr, false, T, k, E, d, Ceff,
                                slot, row_token,
-                               row_gate, x_dispatched, nullptr, s) != cudaSuccess)
+                               row_gate, x_dispatched, nullptr, rank_major, s) != cudaSuccess)
         return MOE_ERR_CUDA;
     return MOE_OK;
 }

@@ -18,6 +18,9 @@
 // Every mbarrier wait is bounded: on expiry the kernel records MOE_ERR_DEVICE_TIMEOUT in the error
 // word, all roles stop, the producer waits (bounded) for its copies in flight, the MMA warp waits for
 // its last MMAs, and the TMEM is freed before the CTA exits.
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
 #include <mutex>
 
 #include "common.cuh"
@@ -50,6 +53,7 @@ struct TcArgs {
     float* out;
     int E, K, N, mode;
     int* err;
+    const float* scale;  // block-FP8 weights: fp32 scale per 128 x 128 block, [E, N/128, K/128]
 };
 
 using namespace tc;
@@ -469,6 +473,245 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (warp == 1) tmem_free_pair(tmem_base, kTmemCols);
 }
 
+// ---- the single-SM GEMM with block-FP8 weights ----------------------------------------------------
+// The expert weight arrives as FP8 E4M3 codes ([E, N, K], one byte each) with one fp32 scale per 128 x 128
+// block ([E, N/128, K/128]).  The producer loads each stage's 256 x 64 codes by TMA (no swizzle: 64-byte
+// rows) next to the bf16 A tile; eight converter warps turn them into bf16 (code value x scale, exact for
+// power-of-two scales), written in the 128-byte-swizzled K-major layout the MMA reads, into one of two
+// bf16 B buffers, and signal it; the MMAs (kind::f16) and the epilogue are those of gemm_tc_kernel.  HBM
+// carries one byte per weight.  Barriers: FULL / EMPTY (staging ring), BREADY (count: the converter
+// warps) / BEMPTY (bf16 buffers, freed by the MMA's commit), TFULL / TEMPTY (accumulators), LAST.
+constexpr int kF8Stages = 4;
+constexpr int kF8Bufs = 2;
+constexpr uint32_t kB8Bytes = kBN * kBK;                 // 16 KiB of codes per stage
+constexpr uint32_t kF8StageBytes = kABytes + kB8Bytes;   // 32 KiB
+constexpr int kF8ConvWarps = 8;
+constexpr int kF8Threads = kThreads + 32 * kF8ConvWarps;  // 448
+constexpr int kF8Block = 128;                            // scale block edge
+
+// 16 E4M3 codes (one row's K block of 16) times `scale` -> 16 bf16 in two 16-byte chunks
+__device__ __forceinline__ void e4m3x16_to_bf16(const uint4 v, float scale, uint4& lo, uint4& hi) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+            const __half2_raw hr =
+                __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w[i] >> (16 * hf)), __NV_E4M3);
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+            o[2 * i + hf] = pack_bf16x2(f.x * scale, f.y * scale);
+        }
+    }
+    lo = make_uint4(o[0], o[1], o[2], o[3]);
+    hi = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+__global__ void __launch_bounds__(kF8Threads, 1)
+    gemm_fp8w_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB8,
+                     const TcArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint8_t* sStage = base;                                  // [stage]: A (bf16) then the B codes
+    uint8_t* sBb = base + kF8Stages * kF8StageBytes;         // [buffer]: bf16 B, 128-byte swizzle
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sBb + kF8Bufs * kBBytes);
+    constexpr int FULL = 0, EMPTY = kF8Stages, BREADY = 2 * kF8Stages, BEMPTY = 2 * kF8Stages + kF8Bufs,
+                  TFULL = 2 * kF8Stages + 2 * kF8Bufs, TEMPTY = TFULL + 2, LAST = TFULL + 4, NBARS = TFULL + 5;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + NBARS);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+    int* s_off = reinterpret_cast<int*>(tmem_holder + 4);
+    float* s_bias = reinterpret_cast<float*>(smem_bias_base(s_off, a.E + 1));
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    auto bar = [&](int i) { return smem_u32(bars + i); };
+
+    if (threadIdx.x == 0) {
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB8);
+        *abort_flag = 0;
+        for (int i = 0; i < kF8Stages; ++i) {
+            mbar_init(bar(FULL + i), 1);
+            mbar_init(bar(EMPTY + i), 1);
+        }
+        for (int i = 0; i < kF8Bufs; ++i) {
+            mbar_init(bar(BREADY + i), kF8ConvWarps);
+            mbar_init(bar(BEMPTY + i), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(TFULL + i), 1);
+            mbar_init(bar(TEMPTY + i), 4);
+        }
+        mbar_init(bar(LAST), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) tmem_alloc(smem_u32(tmem_holder), kTmemCols);
+    pdl_wait();
+    pdl_trigger();
+    for (int i = threadIdx.x; i <= a.E; i += kF8Threads) s_off[i] = a.offset[i];
+    fence_before();
+    __syncthreads();
+    fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    const int total_rows = s_off[a.E];
+    const int m_tiles = total_rows / kBM;
+    const int n_tiles = (a.N + kBN - 1) / kBN;
+    const int num_tiles = m_tiles * n_tiles;
+    const int k_iters = a.K / kBK;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t issued_phase[kF8Stages];
+            bool issued[kF8Stages];
+            for (int i = 0; i < kF8Stages; ++i) { issued[i] = false; issued_phase[i] = 0; }
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+                const int m0 = (tile / n_tiles) * kBM, n0 = (tile % n_tiles) * kBN;
+                const int e = expert_of_row(s_off, a.E, m0);
+                for (int kb = 0; kb < k_iters; ++kb) {
+                    if (!mbar_wait(bar(EMPTY + stage), phase ^ 1u, abort_flag)) { ok = false; break; }
+                    mbar_expect_tx(bar(FULL + stage), kF8StageBytes);
+                    uint8_t* st = sStage + stage * kF8StageBytes;
+                    tma_load_2d(smem_u32(st), &tmA, bar(FULL + stage), kb * kBK, m0);
+                    tma_load_3d(smem_u32(st + kABytes), &tmB8, bar(FULL + stage), kb * kBK, n0, e);
+                    issued[stage] = true;
+                    issued_phase[stage] = phase;
+                    if (++stage == kF8Stages) { stage = 0; phase ^= 1u; }
+                }
+            }
+            if (!ok) {
+                record_error(a.err, kErrTimeout, kWhereGemmProducer);
+                *abort_flag = 1;
+                for (int i = 0; i < kF8Stages; ++i)
+                    if (issued[i]) mbar_wait_bounded(bar(FULL + i), issued_phase[i]);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16(kBM, kBN);
+            int stage = 0, buf = 0;
+            uint32_t phase = 0, bphase = 0;
+            int local = 0;
+            bool ok = true, any = false;
+            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x, ++local) {
+                const int acc = local & 1;
+                const uint32_t acc_phase = (local >> 1) & 1;
+                if (!mbar_wait(bar(TEMPTY + acc), acc_phase ^ 1u, abort_flag)) { ok = false; break; }
+                fence_after();
+                const uint32_t d_tmem = tmem_base + acc * kBN;
+                for (int kb = 0; kb < k_iters; ++kb) {
+                    if (!mbar_wait(bar(FULL + stage), phase, abort_flag) ||
+                        !mbar_wait(bar(BREADY + buf), bphase, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    fence_after();
+                    const uint64_t ad = smem_desc_sw128(smem_u32(sStage + stage * kF8StageBytes));
+                    const uint64_t bd = smem_desc_sw128(smem_u32(sBb + buf * kBBytes));
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk)
+                        mma_bf16(d_tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc, (kb | kk) != 0);
+                    any = true;
+                    commit(bar(EMPTY + stage));
+                    commit(bar(BEMPTY + buf));
+                    if (++stage == kF8Stages) { stage = 0; phase ^= 1u; }
+                    if (++buf == kF8Bufs) { buf = 0; bphase ^= 1u; }
+                }
+                if (ok) commit(bar(TFULL + acc));
+            }
+            if (!ok) {
+                record_error(a.err, kErrTimeout, kWhereGemmMma);
+                *abort_flag = 1;
+            }
+            if (any) {
+                commit(bar(LAST));
+                mbar_wait_bounded(bar(LAST), 0);
+            }
+        }
+    } else if (warp < kThreads / 32) {
+        const int q = warp & 3;
+        const int row = q * 32 + lane;
+        const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+        int local = 0;
+        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
+            const int acc = local & 1;
+            const uint32_t acc_phase = (local >> 1) & 1;
+            const int m0 = (tile / n_tiles) * kBM, n0 = (tile % n_tiles) * kBN;
+            const int e = expert_of_row(s_off, a.E, m0);
+            const int r = m0 + row;
+            const int tok = a.row_token[r];
+            const float g = (a.mode == 2 && tok >= 0) ? a.row_gate[r] : 0.f;
+            const float* sb = stage_bias(a, s_bias + q * kBN, e, n0, lane);
+            const bool ok = __all_sync(0xffffffffu, mbar_wait(bar(TFULL + acc), acc_phase, abort_flag));
+            if (!ok) {
+                if (lane == 0) {
+                    record_error(a.err, kErrTimeout, kWhereGemmEpilogue);
+                    *abort_flag = 1;
+                }
+                break;
+            }
+            fence_after();
+            epilogue_cols(a, tmem_base + lane_base + (uint32_t)(acc * kBN), r, tok, g, sb, n0, 0, kBN);
+            fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(TEMPTY + acc));
+        }
+    } else {
+        // converter warps: thread ct handles 16-byte pieces ct, ct + 256, ct + 512, ct + 768 of the
+        // stage's 256 x 64 codes (row = piece / 4, K bytes 16 * (piece % 4) ..), rows 64 apart
+        const int ct = threadIdx.x - kThreads;
+        const int r0 = ct >> 2, j = ct & 3;
+        const int nbn = a.N / kF8Block, nbk = a.K / kF8Block;
+        int stage = 0, buf = 0;
+        uint32_t phase = 0, bphase = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+            const int m0 = (tile / n_tiles) * kBM, n0 = (tile % n_tiles) * kBN;
+            const int e = expert_of_row(s_off, a.E, m0);
+            for (int kb = 0; kb < k_iters; ++kb) {
+                // the two 128-row scale blocks of this stage's 256 weight rows (rows past N are zero codes)
+                const int nb0 = n0 / kF8Block, kbs = (kb * kBK) / kF8Block;
+                const float* sp = a.scale + ((size_t)e * nbn) * nbk + kbs;
+                const float sc0 = nb0 < nbn ? __ldg(sp + (size_t)nb0 * nbk) : 0.f;
+                const float sc1 = nb0 + 1 < nbn ? __ldg(sp + (size_t)(nb0 + 1) * nbk) : 0.f;
+                const bool got = mbar_wait(bar(FULL + stage), phase, abort_flag) &&
+                                 mbar_wait(bar(BEMPTY + buf), bphase ^ 1u, abort_flag);
+                if (!__all_sync(0xffffffffu, got)) {
+                    ok = false;
+                    break;
+                }
+                const uint8_t* src = sStage + stage * kF8StageBytes + kABytes;
+                uint8_t* dst = sBb + buf * kBBytes;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int r = r0 + 64 * i;
+                    const uint4 v = *reinterpret_cast<const uint4*>(src + r * kBK + j * 16);
+                    uint4 lo, hi;
+                    e4m3x16_to_bf16(v, i < 2 ? sc0 : sc1, lo, hi);
+                    uint8_t* drow = dst + (r >> 3) * 1024 + (r & 7) * 128;
+                    *reinterpret_cast<uint4*>(drow + (((2 * j) ^ (r & 7)) << 4)) = lo;
+                    *reinterpret_cast<uint4*>(drow + (((2 * j + 1) ^ (r & 7)) << 4)) = hi;
+                }
+                fence_proxy_async_smem();  // the MMA reads these bytes through the async proxy
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(BREADY + buf));
+                if (++stage == kF8Stages) { stage = 0; phase ^= 1u; }
+                if (++buf == kF8Bufs) { buf = 0; bphase ^= 1u; }
+            }
+        }
+        if (!ok && lane == 0) {
+            record_error(a.err, kErrTimeout, kWhereGemmProducer);
+            *abort_flag = 1;
+        }
+    }
+    fence_before();
+    __syncthreads();
+    fence_after();
+    if (warp == 1) tmem_free(tmem_base, kTmemCols);
+}
+
 // ---- host side ----------------------------------------------------------------------------------
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -488,8 +731,9 @@ struct MapKey {
     const void* ptr;
     uint64_t d0, d1, d2;
     uint32_t b1;
+    uint32_t kind;  // 0: bf16, 128-byte swizzle; 1: bytes, no swizzle
     bool operator==(const MapKey& o) const {
-        return ptr == o.ptr && d0 == o.d0 && d1 == o.d1 && d2 == o.d2 && b1 == o.b1;
+        return ptr == o.ptr && d0 == o.d0 && d1 == o.d1 && d2 == o.d2 && b1 == o.b1 && kind == o.kind;
     }
 };
 struct MapEntry {
@@ -502,8 +746,10 @@ int g_maps_used = 0, g_maps_next = 0;
 
 }  // namespace
 
-bool tma_map_bf16(const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b1, CUtensorMap* out) {
-    const MapKey key{ptr, d0, d1, d2, b1};
+namespace {
+bool tma_map_kind(const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b1, uint32_t kind,
+                  CUtensorMap* out) {
+    const MapKey key{ptr, d0, d1, d2, b1, kind};
     std::lock_guard<std::mutex> lock(g_map_mutex);
     for (int i = 0; i < g_maps_used; ++i)
         if (g_maps[i].key == key) { *out = g_maps[i].map; return true; }
@@ -511,13 +757,15 @@ bool tma_map_bf16(const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2, uint32
     if (!fn) return false;
     CUtensorMap m;
     const cuuint32_t rank = d2 > 0 ? 3 : 2;
+    const uint64_t es_bytes = kind == 0 ? 2 : 1;
     cuuint64_t dims[3] = {d0, d1, d2};
-    cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
-    cuuint32_t box[3] = {(cuuint32_t)kBK, b1, 1};
+    cuuint64_t strides[2] = {d0 * es_bytes, d0 * d1 * es_bytes};
+    cuuint32_t box[3] = {(cuuint32_t)kBK, b1, 1};  // 64 elements of K: 128 bytes (bf16) or 64 (codes)
     cuuint32_t es[3] = {1, 1, 1};
-    CUresult r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), dims, strides, box, es,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = fn(&m, kind == 0 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, rank,
+                    const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    kind == 0 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return false;
     MapEntry& slot = g_maps[g_maps_next];
     slot.key = key;
@@ -526,6 +774,11 @@ bool tma_map_bf16(const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2, uint32
     if (g_maps_used < 64) ++g_maps_used;
     *out = m;
     return true;
+}
+}  // namespace
+
+bool tma_map_bf16(const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b1, CUtensorMap* out) {
+    return tma_map_kind(ptr, d0, d1, d2, b1, 0, out);
 }
 
 // clusters of two of the pair kernel that can be resident at once (cached per shared-memory size)
@@ -573,11 +826,29 @@ size_t ffn_tc_pair_smem_bytes(int E) {
     return 1024 + (size_t)k2Stages * k2StageBytes + (2 * k2Stages + 5) * 8 + 16 + 8 * (size_t)(E + 1) + kBiasSmem;
 }
 
+size_t ffn_fp8_smem_bytes(int E) {
+    return 1024 + (size_t)kF8Stages * kF8StageBytes + (size_t)kF8Bufs * kBBytes +
+           (2 * kF8Stages + 2 * kF8Bufs + 5) * 8 + 16 + 4 * (size_t)(E + 1) + kBiasSmem;
+}
+
 cudaError_t launch_ffn_tc(const FfnParams& P, cudaStream_t s) {
     if (!P.bf16) return cudaErrorInvalidValue;
     if (P.rows_cap <= 0) return cudaSuccess;
     CUtensorMap ma, mb;
     if (!tma_map_bf16(P.A, (uint64_t)P.K, (uint64_t)P.rows_cap, 0, kBM, &ma)) return cudaErrorInvalidValue;
+    if (P.w_scale != nullptr) {  // block-FP8 weights: byte codes, single-SM tiles
+        if (P.K % kF8Block || P.N % kF8Block) return cudaErrorInvalidValue;
+        if (!tma_map_kind(P.W, (uint64_t)P.K, (uint64_t)P.N, (uint64_t)P.E, kBN, 1, &mb)) return cudaErrorInvalidValue;
+        TcArgs a8{P.offset, P.row_token, P.row_gate, static_cast<const bf16_t*>(P.bias), P.C, P.out,
+                  P.E, P.K, P.N, P.mode, P.err, P.w_scale};
+        const size_t smem8 = ffn_fp8_smem_bytes(P.E);
+        cudaError_t e8 = cudaFuncSetAttribute(gemm_fp8w_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem8);
+        if (e8 != cudaSuccess) return e8;
+        const int64_t tiles8 = (P.rows_cap / kBM) * (int64_t)((P.N + kBN - 1) / kBN);
+        int grid8 = device_sm_count();
+        if (tiles8 < grid8) grid8 = (int)(tiles8 > 0 ? tiles8 : 1);
+        return launch_pdl(gemm_fp8w_kernel, dim3(grid8), dim3(kF8Threads), smem8, s, ma, mb, a8);
+    }
     if (!tma_map_bf16(P.W, (uint64_t)P.K, (uint64_t)P.N, (uint64_t)P.E, kBN, &mb)) return cudaErrorInvalidValue;
     TcArgs a;
     a.offset = P.offset;
@@ -591,6 +862,7 @@ cudaError_t launch_ffn_tc(const FfnParams& P, cudaStream_t s) {
     a.N = P.N;
     a.mode = P.mode;
     a.err = P.err;
+    a.scale = nullptr;
     if (P.pair) {
         // pairs of SMs: B boxes of 128 weight rows (half of a 256-wide tile), grid = 2 x the clusters that fit
         CUtensorMap mb2;

@@ -88,19 +88,24 @@ cudaError_t launch_gate(const GateParams& p, cudaStream_t s);
 // rank step over all tokens; the last CTA to finish (counted on `ticket`, a zero-initialised int that
 // it resets) runs the scan: count[E], offset[E+1] and the padding rows of row_token / row_gate, with
 // capacity C
+// rank_major: pairs numbered in (rank, token) order, blocks of 32 such pairs (blk_hist [ceil(T k/32), E])
 cudaError_t launch_dispatch_rank(const int* topk_idx, int T, int k, int E, int* blk_hist, int* rank, int* err,
                                  int* ticket, int C, int* count, int* offset, int* row_token, float* row_gate,
-                                 cudaStream_t s);
+                                 int rank_major, cudaStream_t s);
+inline int dispatch_hist_blocks(int T, int k, int rank_major) {
+    return rank_major ? (int)(((long)T * k + kTokensPerBlock - 1) / kTokensPerBlock)
+                      : (T + kTokensPerBlock - 1) / kTokensPerBlock;
+}
 // slot [T, k] holds the block ranks on entry (from the rank step or the gate kernel) and the slots on exit
 // scan = false: blk_hist holds the scanned block prefixes and offset the segment offsets (from the rank
-// step's scan); scan = true (E <= kGatherScanMaxE): blk_hist holds the raw block histograms and the
+// step's scan, in (rank, token) order when rank_major); scan = true (token order only) (E <= kGatherScanMaxE): blk_hist holds the raw block histograms and the
 // gather does the scan's work itself -- it writes count (if not null), offset and the padding rows
 constexpr int kGatherScanMaxE = 64;
 constexpr int kGatherScanMaxHist = 2048;  // ints of histogram every gather CTA reads
 cudaError_t launch_dispatch_gather(const void* x, int bf16, const int* topk_idx, const float* topk_gate,
                                    const int* blk_hist, int* offset, int* count, bool scan, int T, int k, int E,
                                    int d, int C, int* slot, int* row_token, float* row_gate, void* x_dispatched,
-                                   float* out_to_zero, cudaStream_t s);
+                                   float* out_to_zero, int rank_major, cudaStream_t s);
 
 // ---- expert FFN -------------------------------------------------------------------------------
 // mode: 0 = up projection (+b1, GELU, store hidden), 1 = down projection to y (fp32),
@@ -118,7 +123,9 @@ struct FfnParams {
     int pair;                 // tensor-core kernel on pairs of SMs (256 x 256 tiles)
     int64_t rows_cap;
     int* err;
+    const float* w_scale;     // block-FP8 weights: W holds E4M3 codes, w_scale [E, N/128, K/128]; else nullptr
 };
+size_t ffn_fp8_smem_bytes(int E);
 cudaError_t launch_ffn_simt(const FfnParams& p, cudaStream_t s);
 cudaError_t launch_ffn_tc(const FfnParams& p, cudaStream_t s);  // bf16 only; tcgen05 + TMA
 

@@ -18,8 +18,9 @@ namespace moe {
 // lower lanes in its group; a shared running count per expert carries the numbering across chunks.
 // `running` [E] must be zero on entry and holds the block's expert histogram on exit.  expert_of(i)
 // < 0 marks a pair that takes no slot (rank -1, not counted).
-template <typename F>
-__device__ __forceinline__ void rank_pairs_warp(F expert_of, int npairs, int* running, int* rank_out, int lane) {
+// store_rank(i, r) receives pair i's rank (-1 for a pair that takes no slot).
+template <typename F, typename S>
+__device__ __forceinline__ void rank_pairs_warp_to(F expert_of, int npairs, int* running, S store_rank, int lane) {
     for (int c0 = 0; c0 < npairs; c0 += 32) {
         const int i = c0 + lane;
         const bool valid = i < npairs;
@@ -31,8 +32,12 @@ __device__ __forceinline__ void rank_pairs_warp(F expert_of, int npairs, int* ru
         __syncwarp();
         if (real && rank == 0) running[e] = base + __popc(mask);
         __syncwarp();
-        if (valid) rank_out[i] = real ? base + rank : -1;
+        if (valid) store_rank(i, real ? base + rank : -1);
     }
+}
+template <typename F>
+__device__ __forceinline__ void rank_pairs_warp(F expert_of, int npairs, int* running, int* rank_out, int lane) {
+    rank_pairs_warp_to(expert_of, npairs, running, [&](int i, int r) { rank_out[i] = r; }, lane);
 }
 
 struct ScanSmem {

@@ -28,9 +28,10 @@ _LIB_PATH = os.path.join(_HERE, "_moe_oracle.so")
 
 GATE_SOFTMAX, GATE_NOISY, GATE_COSINE = 0, 1, 2
 NORM_ALL, NORM_TOPK = 0, 1
-F32, BF16 = 0, 1
+F32, BF16, F64 = 0, 1, 2
 _GATE_CODES = {"softmax": GATE_SOFTMAX, "noisy": GATE_NOISY, "cosine": GATE_COSINE}
 _NORM_CODES = {"all": NORM_ALL, "topk": NORM_TOPK}
+_PRIORITY_CODES = {"token": 0, "rank": 1}
 
 
 def compile_source(src: str, out: str) -> str:
@@ -65,7 +66,9 @@ def _raw(t):
     a = np.ascontiguousarray(t)
     if a.dtype == np.float32:
         return a, F32
-    raise TypeError("oracle numpy arrays must be float32 (pass bf16 as a torch tensor), got %s" % a.dtype)
+    if a.dtype == np.float64:  # dequantised weights
+        return a, F64
+    raise TypeError("oracle numpy arrays must be float32 or float64 (pass bf16 as a torch tensor), got %s" % a.dtype)
 
 
 def _ptr(a):
@@ -79,6 +82,16 @@ def _same_dtype(*pairs):
     return codes.pop()
 
 
+def _x_and_weight_dtypes(xs, b1, b2, w1, w2):
+    """(dtype of x and the biases, dtype of the two weight tensors): the same, or float64 weights
+    (dequantised block-FP8) with any x dtype."""
+    dt = _same_dtype(xs, b1, b2)
+    wdt = _same_dtype(w1, w2)
+    if wdt != dt and wdt != F64:
+        raise TypeError("x and all weights must share one dtype")
+    return dt, wdt
+
+
 class Oracle:
     """The oracle's steps, bound to one compiled copy of moe_oracle.c."""
 
@@ -89,9 +102,10 @@ class Oracle:
             "oracle_gate_scores": ([I, I, I, I, I, D, I, P, P, P, P, P, P, P], None),
             "oracle_topk": ([I, I, I, I, P, P, P], None),
             "oracle_capacity": ([I, I, I, D, I], I),
-            "oracle_dispatch": ([I, I, I, I, P, P, P], None),
-            "oracle_expert": ([I, I, I, P, S, P, S, P, S, P, S, P, S, P], None),
-            "oracle_combine_tokens": ([I, I, I, I, P, I, P, P, P, P, P, P, P, P, P], None),
+            "oracle_dispatch": ([I, I, I, I, I, P, P, P], None),
+            "oracle_expert": ([I, I, I, I, P, S, P, S, P, S, P, S, P, S, P], None),
+            "oracle_combine_tokens": ([I, I, I, I, I, P, I, P, P, P, P, P, P, P, P, P], None),
+            "oracle_dequant_block_fp8": ([I, I, I, P, P, P], None),
             "oracle_router_stats": ([I, I, I, P, P, P, P, P, P, P], None),
         }
         for name, (args, res) in sigs.items():
@@ -134,29 +148,31 @@ class Oracle:
         """Step 3a: the per-expert capacity C."""
         return int(self.lib.oracle_capacity(T, E, k, float(capacity_factor), int(capacity)))
 
-    def dispatch(self, idx, E, C):
-        """Step 3b: (slot int32 [T, k] or -1 if dropped, count int32 [E] before the limit)."""
+    def dispatch(self, idx, E, C, priority="token"):
+        """Step 3b: (slot int32 [T, k] or -1 if dropped, count int32 [E] before the limit).  priority:
+        "token" (slots in token order) or "rank" (every token's first choice before any second choice)."""
         idx = np.ascontiguousarray(idx, dtype=np.int32)
         T, k = idx.shape
         slot = np.empty((T, k), dtype=np.int32)
         count = np.empty((E,), dtype=np.int32)
-        self.lib.oracle_dispatch(T, E, k, int(C), _ptr(idx), _ptr(slot), _ptr(count))
+        self.lib.oracle_dispatch(T, E, k, int(C), _PRIORITY_CODES[priority], _ptr(idx), _ptr(slot), _ptr(count))
         return slot, count
 
     def expert(self, x_row, w1_e, b1_e, w2_e, b2_e):
-        """Step 4 for one token and one expert: float64 [d].  w1_e [h, d], w2_e [d, h]."""
+        """Step 4 for one token and one expert: float64 [d].  w1_e [h, d], w2_e [d, h]; the weights may
+        be float64 (dequantised) while x and the biases keep their own dtype."""
         xs, a1, c1, a2, c2 = _raw(x_row), _raw(w1_e), _raw(b1_e), _raw(w2_e), _raw(b2_e)
-        dt = _same_dtype(xs, a1, c1, a2, c2)
+        dt, wdt = _x_and_weight_dtypes(xs, c1, c2, a1, a2)
         h, d = a1[0].shape
         y = np.empty((d,), dtype=np.float64)
-        self.lib.oracle_expert(d, h, dt, _ptr(xs[0]), 0, _ptr(a1[0]), 0, _ptr(c1[0]), 0, _ptr(a2[0]), 0,
+        self.lib.oracle_expert(d, h, dt, wdt, _ptr(xs[0]), 0, _ptr(a1[0]), 0, _ptr(c1[0]), 0, _ptr(a2[0]), 0,
                                _ptr(c2[0]), 0, _ptr(y))
         return y
 
     def combine_tokens(self, tokens, x, idx, gate, slot, w1, b1, w2, b2):
         """Steps 4+5 for the listed tokens: float64 [len(tokens), d]."""
         xs, a1, c1, a2, c2 = _raw(x), _raw(w1), _raw(b1), _raw(w2), _raw(b2)
-        dt = _same_dtype(xs, a1, c1, a2, c2)
+        dt, wdt = _x_and_weight_dtypes(xs, c1, c2, a1, a2)
         E, h, d = a1[0].shape
         toks = np.ascontiguousarray(tokens, dtype=np.int32)
         idx = np.ascontiguousarray(idx, dtype=np.int32)
@@ -164,10 +180,32 @@ class Oracle:
         slot = np.ascontiguousarray(slot, dtype=np.int32)
         k = idx.shape[1]
         out = np.empty((len(toks), d), dtype=np.float64)
-        self.lib.oracle_combine_tokens(d, h, k, dt, _ptr(toks), len(toks), _ptr(xs[0]), _ptr(idx),
+        self.lib.oracle_combine_tokens(d, h, k, dt, wdt, _ptr(toks), len(toks), _ptr(xs[0]), _ptr(idx),
                                        _ptr(gate), _ptr(slot), _ptr(a1[0]), _ptr(c1[0]), _ptr(a2[0]),
                                        _ptr(c2[0]), _ptr(out))
         return out
+
+    def dequant_block_fp8(self, q, scale, block=128):
+        """Block-FP8 weights to float64: q holds E4M3 codes [..., rows, cols] (uint8 numpy array or a
+        torch float8_e4m3fn / uint8 tensor), scale fp32 [..., ceil(rows/block), ceil(cols/block)]."""
+        if hasattr(q, "detach"):
+            import torch
+
+            q = q.detach().cpu().contiguous()
+            q = q.view(torch.uint8).numpy() if q.dtype != torch.uint8 else q.numpy()
+        if hasattr(scale, "detach"):
+            scale = scale.detach().cpu().numpy()
+        q = np.ascontiguousarray(q, dtype=np.uint8)
+        scale = np.ascontiguousarray(scale, dtype=np.float32)
+        rows, cols = q.shape[-2:]
+        lead = q.shape[:-2]
+        qq = q.reshape((-1, rows, cols))
+        ss = scale.reshape((qq.shape[0],) + scale.shape[-2:])
+        assert ss.shape[1:] == (-(-rows // block), -(-cols // block)), (ss.shape, rows, cols, block)
+        out = np.empty(qq.shape, dtype=np.float64)
+        for i in range(qq.shape[0]):
+            self.lib.oracle_dequant_block_fp8(rows, cols, block, _ptr(qq[i]), _ptr(ss[i]), _ptr(out[i]))
+        return out.reshape(lead + (rows, cols))
 
     def router_stats(self, idx, gate, E, slot=None):
         """Router statistics: (importance float64 [E], expert_importance_loss, load_balance_loss, dropped)."""
@@ -191,7 +229,7 @@ class Oracle:
 
     def forward(self, spec, t, tokens=None):
         """Whole layer.  ``spec``: mapping with gate, norm, k, E, capacity_factor, capacity,
-        temperature; ``t``: mapping of tensors x, w_gate, w_noise, eps, proj, emb, w1, b1, w2, b2
+        temperature and optionally priority ("token" or "rank"); ``t``: mapping of tensors x, w_gate, w_noise, eps, proj, emb, w1, b1, w2, b2
         (absent -> None).  Returns a dict with scores, idx, gate, C, slot, count, tokens and out
         ([len(tokens), d])."""
         s, idx, g = self.route(spec["gate"], spec["k"], spec["norm"], t.get("x"), t.get("w_gate"),
@@ -199,7 +237,7 @@ class Oracle:
                                spec.get("temperature", 1.0))
         T = s.shape[0]
         C = self.capacity(T, spec["E"], spec["k"], spec.get("capacity_factor", 1.0), spec.get("capacity", -1))
-        slot, count = self.dispatch(idx, spec["E"], C)
+        slot, count = self.dispatch(idx, spec["E"], C, spec.get("priority", "token"))
         if tokens is None:
             tokens = np.arange(T, dtype=np.int32)
         out = self.combine_tokens(tokens, t.get("x"), idx, g, slot, t.get("w1"), t.get("b1"), t.get("w2"),
@@ -246,6 +284,10 @@ def combine_tokens(*a, **kw):
 
 def router_stats(*a, **kw):
     return default().router_stats(*a, **kw)
+
+
+def dequant_block_fp8(*a, **kw):
+    return default().dequant_block_fp8(*a, **kw)
 
 
 def route(*a, **kw):

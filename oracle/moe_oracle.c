@@ -32,6 +32,7 @@
 
 #define OR_F32 0
 #define OR_BF16 1
+#define OR_F64 2
 
 #define GATE_SOFTMAX 0
 #define GATE_NOISY 1
@@ -40,10 +41,11 @@
 #define NORM_ALL 0
 #define NORM_TOPK 1
 
-/* Exact widening of element i of a fp32 or bf16 buffer.  A bf16 value is the upper half of the
+/* Exact widening of element i of a fp32, bf16 or fp64 buffer.  A bf16 value is the upper half of the
  * fp32 with the same sign, exponent and leading 7 mantissa bits. */
 static double elem(const void *base, size_t i, int dtype)
 {
+    if (dtype == OR_F64) return ((const double *)base)[i];
     if (dtype == OR_BF16) {
         uint32_t bits = (uint32_t)((const uint16_t *)base)[i] << 16;
         float f;
@@ -53,12 +55,12 @@ static double elem(const void *base, size_t i, int dtype)
     return (double)((const float *)base)[i];
 }
 
-/* sum_i a[i] * b[i], i = 0..n-1, accumulated left to right in double. */
-static double dot_rows(const void *a, size_t a_off, const void *b, size_t b_off, int n, int dtype)
+/* sum_i a[i] * b[i], i = 0..n-1, accumulated left to right in double (a and b of element types adt, bdt). */
+static double dot_rows(const void *a, size_t a_off, int adt, const void *b, size_t b_off, int bdt, int n)
 {
     double s = 0.0;
     for (int i = 0; i < n; ++i)
-        s += elem(a, a_off + (size_t)i, dtype) * elem(b, b_off + (size_t)i, dtype);
+        s += elem(a, a_off + (size_t)i, adt) * elem(b, b_off + (size_t)i, bdt);
     return s;
 }
 
@@ -83,7 +85,7 @@ void oracle_gate_scores(int gate_type, int T, int d, int E, int p, double temper
         if (gate_type == GATE_COSINE) {
             double nu2 = 0.0;
             for (int j = 0; j < p; ++j) {
-                u[j] = dot_rows(x, xo, proj, (size_t)j * (size_t)d, d, dtype);
+                u[j] = dot_rows(x, xo, dtype, proj, (size_t)j * (size_t)d, dtype, d);
                 nu2 += u[j] * u[j];
             }
             double nu = sqrt(nu2);
@@ -101,9 +103,9 @@ void oracle_gate_scores(int gate_type, int T, int d, int E, int p, double temper
             }
         } else {
             for (int e = 0; e < E; ++e) {
-                double s = dot_rows(x, xo, w_gate, (size_t)e * (size_t)d, d, dtype);
+                double s = dot_rows(x, xo, dtype, w_gate, (size_t)e * (size_t)d, dtype, d);
                 if (gate_type == GATE_NOISY) {
-                    double noise = dot_rows(x, xo, w_noise, (size_t)e * (size_t)d, d, dtype);
+                    double noise = dot_rows(x, xo, dtype, w_noise, (size_t)e * (size_t)d, dtype, d);
                     s += (double)eps[(size_t)t * E + e] * softplus(noise);
                 }
                 scores[(size_t)t * E + e] = s;
@@ -156,12 +158,29 @@ int oracle_capacity(int T, int E, int k, double capacity_factor, int capacity)
     return (int)ceil(capacity_factor * (double)T * (double)k / (double)E);
 }
 
-/* Walk the pairs in token order (t = 0..T-1, then rank j = 0..k-1).  Each pair takes the next free
- * position of its expert's queue; the pair is kept if that position is < C, else dropped (slot -1).
- * count[e] is the number of pairs routed to e before the limit. */
-void oracle_dispatch(int T, int E, int k, int C, const int32_t *idx, int32_t *slot, int32_t *count)
+/* Walk the pairs in priority order.  Each pair takes the next free position of its expert's queue; the
+ * pair is kept if that position is < C, else dropped (slot -1).  count[e] is the number of pairs routed
+ * to e before the limit.
+ *   PRIORITY_TOKEN: token order (t = 0..T-1, then rank j = 0..k-1) -- the workloads' "capacity slots in
+ *                   token order";
+ *   PRIORITY_RANK:  rank order (every token's first choice, in token order, then every second choice,
+ *                   ...) -- the other reading of the "Tutel MoE guide"'s capacity_factor rule, where a
+ *                   token's lower-ranked choices never push out another token's first choice. */
+#define PRIORITY_TOKEN 0
+#define PRIORITY_RANK 1
+void oracle_dispatch(int T, int E, int k, int C, int priority, const int32_t *idx, int32_t *slot,
+                     int32_t *count)
 {
     for (int e = 0; e < E; ++e) count[e] = 0;
+    if (priority == PRIORITY_RANK) {
+        for (int r = 0; r < k; ++r)
+            for (int tok = 0; tok < T; ++tok) {
+                const size_t i = (size_t)tok * k + r;
+                const int q = count[idx[i]]++;
+                slot[i] = q < C ? q : -1;
+            }
+        return;
+    }
     for (int t = 0; t < T; ++t) {
         for (int j = 0; j < k; ++j) {
             int e = idx[(size_t)t * k + j];
@@ -172,31 +191,61 @@ void oracle_dispatch(int T, int E, int k, int C, const int32_t *idx, int32_t *sl
 }
 
 /* ---- step 4: one expert on one token ------------------------------------------------------------
- * y = W2 GELU(W1 x + b1) + b2, W1 [h, d], W2 [d, h] (rows = output features).  b1 / b2 may be NULL. */
-void oracle_expert(int d, int h, int dtype, const void *x, size_t x_off, const void *w1,
+ * y = W2 GELU(W1 x + b1) + b2, W1 [h, d], W2 [d, h] (rows = output features).  b1 / b2 may be NULL.
+ * x and the biases have element type `dtype`, the weights `wdtype` (fp64 for dequantised weights). */
+void oracle_expert(int d, int h, int dtype, int wdtype, const void *x, size_t x_off, const void *w1,
                    size_t w1_off, const void *b1, size_t b1_off, const void *w2, size_t w2_off,
                    const void *b2, size_t b2_off, double *y)
 {
     double *a = (double *)malloc(sizeof(double) * (size_t)h);
     for (int n = 0; n < h; ++n) {
-        double z = dot_rows(x, x_off, w1, w1_off + (size_t)n * (size_t)d, d, dtype);
+        double z = dot_rows(x, x_off, dtype, w1, w1_off + (size_t)n * (size_t)d, wdtype, d);
         if (b1) z += elem(b1, b1_off + (size_t)n, dtype);
         a[n] = gelu_erf(z);
     }
     for (int n = 0; n < d; ++n) {
         double z = 0.0;
         for (int i = 0; i < h; ++i)
-            z += a[i] * elem(w2, w2_off + (size_t)n * (size_t)h + (size_t)i, dtype);
+            z += a[i] * elem(w2, w2_off + (size_t)n * (size_t)h + (size_t)i, wdtype);
         if (b2) z += elem(b2, b2_off + (size_t)n, dtype);
         y[n] = z;
     }
     free(a);
 }
 
+/* ---- block-FP8 expert weights -----------------------------------------------------------------------
+ * "MoE architecture: breaking the single-card compute bottleneck", section 1.3 (FP8 weights shrink the
+ * model) and the Block FP8 rows of the "Tutel MoE guide" throughput table.  The pages fix no format;
+ * the reading taken: each weight matrix [rows, cols] is stored as FP8 E4M3 codes plus one fp32 scale
+ * per block x block tile, and the layer computes with the dequantised weight  code value * scale.
+ * An E4M3 code is sign (bit 7), exponent field E (bits 6..3, bias 7) and mantissa field M (bits 2..0):
+ * E > 0: (1 + M/8) * 2^(E-7);  E = 0: (M/8) * 2^-6 (subnormal);  E = 15 and M = 7 is NaN. */
+static double e4m3_value(uint8_t code)
+{
+    const int sign = code >> 7, ex = (code >> 3) & 15, man = code & 7;
+    double mag;
+    if (ex == 15 && man == 7) return NAN;
+    if (ex == 0)
+        mag = ldexp((double)man / 8.0, -6);
+    else
+        mag = ldexp(1.0 + (double)man / 8.0, ex - 7);
+    return sign ? -mag : mag;
+}
+
+/* out[r][c] = e4m3(q[r][c]) * scale[r / block][c / block]; scale is [ceil(rows/block), ceil(cols/block)]. */
+void oracle_dequant_block_fp8(int rows, int cols, int block, const uint8_t *q, const float *scale, double *out)
+{
+    const int sc = (cols + block - 1) / block;
+    for (int r = 0; r < rows; ++r)
+        for (int c = 0; c < cols; ++c)
+            out[(size_t)r * cols + c] =
+                e4m3_value(q[(size_t)r * cols + c]) * (double)scale[(size_t)(r / block) * sc + (c / block)];
+}
+
 /* ---- step 5: combine, for a list of tokens -------------------------------------------------------
  * out[i] = sum over ranks j of token tokens[i] with slot >= 0 of gate[t][j] * expert_{idx[t][j]}(x_t);
  * a token whose pairs were all dropped gets 0.  out is [ntok, d]. */
-void oracle_combine_tokens(int d, int h, int k, int dtype, const int32_t *tokens, int ntok,
+void oracle_combine_tokens(int d, int h, int k, int dtype, int wdtype, const int32_t *tokens, int ntok,
                            const void *x, const int32_t *idx, const double *gate,
                            const int32_t *slot, const void *w1, const void *b1, const void *w2,
                            const void *b2, double *out)
@@ -209,7 +258,7 @@ void oracle_combine_tokens(int d, int h, int k, int dtype, const int32_t *tokens
         for (int j = 0; j < k; ++j) {
             if (slot[(size_t)t * k + j] < 0) continue;
             size_t e = (size_t)idx[(size_t)t * k + j];
-            oracle_expert(d, h, dtype, x, (size_t)t * (size_t)d, w1, e * (size_t)h * (size_t)d, b1,
+            oracle_expert(d, h, dtype, wdtype, x, (size_t)t * (size_t)d, w1, e * (size_t)h * (size_t)d, b1,
                           e * (size_t)h, w2, e * (size_t)d * (size_t)h, b2, e * (size_t)d, y);
             double g = gate[(size_t)t * k + j];
             for (int n = 0; n < d; ++n) o[n] += g * y[n];

@@ -123,6 +123,87 @@ def pin_dispatch_hand(o):
         assert np.array_equal(count, np.array(c["count"])), (count, c)
 
 
+def pin_dispatch_rank_priority_hand(o):
+    """Hand-worked rank-priority dispatch; the same routings in token order differ as worked out too."""
+    for c in GOLDEN["dispatch_rank_priority"]["cases"]:
+        idx = np.array(c["idx"], np.int32)
+        slot, count = o.dispatch(idx, c["E"], c["C"], priority="rank")
+        assert np.array_equal(slot, np.array(c["slot"])), (slot, c)
+        assert np.array_equal(count, np.array(c["count"])), (count, c)
+        tslot, _ = o.dispatch(idx, c["E"], c["C"])
+        assert np.array_equal(tslot, np.array(c["token_order_slot"])), (tslot, c)
+
+
+def pin_dispatch_rank_priority_properties(o):
+    """Random routings in rank priority: with k = 1 it is token order; each expert keeps exactly the first
+    C of its pairs ordered by (rank, token) with slots 0..kept-1 in that order, so every kept pair of a
+    lower rank has a lower slot than every pair of a higher rank; counts are the routing histogram."""
+    rng = np.random.default_rng(7)
+    for (T, E, k, C) in [(50, 4, 1, 9), (64, 6, 2, 15), (33, 5, 3, 20), (40, 8, 2, 1), (30, 4, 4, 30)]:
+        idx = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+        slot, count = o.dispatch(idx, E, C, priority="rank")
+        assert np.array_equal(count, np.bincount(idx.ravel(), minlength=E))
+        if k == 1:
+            assert np.array_equal(slot, o.dispatch(idx, E, C)[0])
+        for e in range(E):
+            order = sorted((j, t) for t in range(T) for j in range(k) if idx[t, j] == e)
+            got = [slot[t, j] for j, t in order]
+            n = min(C, len(order))
+            assert got == list(range(n)) + [-1] * (len(order) - n)
+
+
+def pin_fp8_codes_hand(o):
+    """Hand-decoded E4M3 codes (normal, subnormal, signed, zero) and a hand-worked block-scaled matrix."""
+    g = GOLDEN["fp8_e4m3_codes"]
+    q = np.array([g["codes"]], np.uint8)
+    got = o.dequant_block_fp8(q, np.ones((1, 1), np.float32), block=128)[0]
+    assert np.array_equal(got, np.array(g["values"])), got
+    assert np.array_equal(np.signbit(got), np.signbit(np.array(g["values"])))
+    b = GOLDEN["fp8_block_scale"]
+    got = o.dequant_block_fp8(np.array(b["codes"], np.uint8), np.array(b["scale"], np.float32), block=b["block"])
+    assert np.array_equal(got, np.array(b["values"])), got
+
+
+def pin_fp8_dequant_vs_torch(o):
+    """Every non-NaN E4M3 code against torch's float8_e4m3fn conversion (a library routine), and random
+    block-scaled matrices (ragged edge blocks, power-of-two and other scales) against numpy."""
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], np.uint8)
+    want = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = o.dequant_block_fp8(codes.reshape(1, -1), np.ones((1, 1), np.float32), block=256)[0]
+    assert np.array_equal(got, want)
+    assert np.isnan(o.dequant_block_fp8(np.array([[0x7F, 0xFF]], np.uint8), np.ones((1, 1), np.float32))).all()
+    rng = np.random.default_rng(11)
+    for rows, cols, blk in [(5, 7, 2), (130, 260, 128), (64, 64, 32)]:
+        q = rng.choice(codes, size=(rows, cols)).astype(np.uint8)
+        sc = (np.exp2(rng.integers(-12, 4, size=(-(-rows // blk), -(-cols // blk)))) *
+              rng.choice([1.0, 1.25, -0.75], size=(-(-rows // blk), -(-cols // blk)))).astype(np.float32)
+        val = torch.from_numpy(q).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+        full = np.repeat(np.repeat(sc.astype(np.float64), blk, 0), blk, 1)[:rows, :cols]
+        assert np.array_equal(o.dequant_block_fp8(q, sc, block=blk), val * full)
+
+
+def pin_fp8_expert_with_dequantised_weights(o):
+    """The expert on float64 (dequantised) weights with a bf16 token: against torch fp64 Linear-GELU-Linear
+    on the same values, and against the same expert with the weights given as bf16 when they are
+    exactly representable in bf16 (E4M3 values times power-of-two scales)."""
+    rng = np.random.default_rng(12)
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], np.uint8)
+    d, h = 24, 40
+    x = torch.randn(d, generator=torch.Generator().manual_seed(13)).to(torch.bfloat16)
+    w1 = o.dequant_block_fp8(rng.choice(codes, size=(h, d)).astype(np.uint8),
+                             np.exp2(rng.integers(-9, -5, size=(1, 1))).astype(np.float32), block=128)
+    w2 = o.dequant_block_fp8(rng.choice(codes, size=(d, h)).astype(np.uint8),
+                             np.exp2(rng.integers(-9, -5, size=(1, 1))).astype(np.float32), block=128)
+    b1 = torch.randn(h, generator=torch.Generator().manual_seed(14)).to(torch.bfloat16)
+    b2 = torch.randn(d, generator=torch.Generator().manual_seed(15)).to(torch.bfloat16)
+    y = o.expert(x, w1, b1, w2, b2)
+    xt, t1, t2 = x.double(), torch.from_numpy(w1), torch.from_numpy(w2)
+    want = F.linear(F.gelu(F.linear(xt, t1, b1.double()), approximate="none"), t2, b2.double()).numpy()
+    assert np.allclose(y, want, rtol=1e-12, atol=1e-12)
+    yb = o.expert(x, torch.from_numpy(w1).to(torch.bfloat16), b1, torch.from_numpy(w2).to(torch.bfloat16), b2)
+    assert np.array_equal(y, yb)
+
+
 def pin_gelu_normal_cdf(o):
     """Identity weights make the expert return GELU(x) itself; GELU(z) = z Phi(z) with Phi from a table."""
     g = GOLDEN["gelu_normal_cdf"]

@@ -117,7 +117,7 @@ def check_routing(wl, tc, g, scores=None):
 def check_dispatch(wl, tc_x, g):
     """Dispatch outputs vs the oracle's dispatch run on the GPU's own routing; bit-exact."""
     C = oracle.capacity(wl.T, wl.E, wl.k, wl.capacity_factor, wl.capacity)
-    oslot, ocount = oracle.dispatch(g["idx"], wl.E, C)
+    oslot, ocount = oracle.dispatch(g["idx"], wl.E, C, wl.priority)
     assert np.array_equal(g["slot"], oslot)
     assert np.array_equal(g["count"], ocount)
     kept = np.minimum(ocount, C)

@@ -32,11 +32,21 @@ SMALL = [
     small_workload(T=300, d=256, h=128, E=24, k=2, capacity_factor=1.0),
     small_workload(T=200, d=192, h=128, E=48, k=2, norm="all", capacity_factor=1.1),
     small_workload(T=520, d=128, h=128, E=64, k=4, capacity_factor=0.8),        # 64 experts, k > 2, drops
+    # capacity slots in rank order (first choices first), with drops: the fused softmax gate, the
+    # unfused noisy and cosine gates, the fp32 gate, and k > 2
+    small_workload(T=300, d=128, h=256, E=8, k=2, capacity_factor=0.7, priority="rank"),
+    small_workload(T=129, d=128, h=128, E=12, k=2, gate="noisy", capacity_factor=0.8, priority="rank"),
+    small_workload(T=180, d=128, h=256, E=10, k=2, gate="cosine", cos_dim=64, capacity_factor=0.9,
+                   x_dist="clusters", priority="rank"),
+    small_workload(T=211, d=128, h=128, E=7, k=2, dtype="f32", capacity_factor=0.6, priority="rank"),
+    small_workload(T=200, d=192, h=192, E=6, k=3, capacity_factor=0.8, priority="rank"),
+    small_workload(T=2000, d=128, h=128, E=16, k=4, capacity_factor=0.9, priority="rank"),  # 250 pair blocks
 ]
 
 
 def _id(wl):
-    return "%s_%s_T%d_d%d_h%d_E%d_k%d" % (wl.gate, wl.dtype, wl.T, wl.d, wl.h, wl.E, wl.k)
+    return "%s_%s_T%d_d%d_h%d_E%d_k%d%s" % (wl.gate, wl.dtype, wl.T, wl.d, wl.h, wl.E, wl.k,
+                                           "_rank" if wl.priority == "rank" else "")
 
 
 def _full_check(wl, flags=0):
@@ -156,7 +166,20 @@ def test_heavy_drops_and_bias():
     _full_check(wl)
 
 
-@pytest.mark.parametrize("name", ["tiny_fp32", "bf16_e8_k2", "bf16_cosine_skew", "bf16_noisy_e64", "bf16_decode_e256"])
+def test_rank_priority_differs_from_token_order():
+    """With drops, rank order keeps a different set of pairs than token order (the flag reaches the
+    kernels): every first choice that fits is kept before any second choice."""
+    wl = small_workload(T=300, d=128, h=256, E=8, k=2, capacity_factor=0.7, priority="rank")
+    _, tg = P.inputs(wl)
+    g_rank = P.run_steps(wl, tg)
+    g_tok = P.run_steps(wl.with_(priority="token"), tg)
+    assert np.array_equal(g_rank["idx"], g_tok["idx"])
+    assert not np.array_equal(g_rank["slot"], g_tok["slot"])
+    assert (g_rank["slot"][:, 0] >= 0).sum() >= (g_tok["slot"][:, 0] >= 0).sum()
+
+
+@pytest.mark.parametrize("name", ["tiny_fp32", "bf16_e8_k2", "bf16_cosine_skew", "bf16_noisy_e64", "bf16_decode_e256",
+                                  "bf16_recsys_e8"])
 def test_full_size_workload(name):
     """Full sizes, launch configuration of the benchmark: routing and dispatch on every token, the
     output on sampled tokens (all tokens for the tiny layer)."""
@@ -168,7 +191,7 @@ def test_full_size_workload(name):
     # random tokens plus the owners of every expert segment's edge rows (first row, either side of the
     # first 128-row tile boundary, last kept row), so that every expert's last partial tile is checked
     n = {"tiny_fp32": wl.T, "bf16_e8_k2": 64, "bf16_cosine_skew": 64, "bf16_noisy_e64": 128,
-         "bf16_decode_e256": wl.T}[name]
+         "bf16_decode_e256": wl.T, "bf16_recsys_e8": 512}[name]
     edges = P.segment_edge_tokens(g["idx"], slot, wl.E, C)
     toks = np.union1d(P.sample_tokens(wl.T, n, seed=wl.seed), edges).astype(np.int32)
     ref = P.oracle_out(wl, tc, tg, scores, g["idx"], slot, toks)

@@ -23,16 +23,26 @@ MUTANTS = [
     ("rank_major_slots", "    for (int t = 0; t < T; ++t) {\n        for (int j = 0; j < k; ++j) {\n            int e = idx",
      "    for (int j = 0; j < k; ++j) {\n        for (int t = 0; t < T; ++t) {\n            int e = idx"),
     ("count_only_kept", "int pos = count[e]++;", "int pos = count[e]; if (pos < C) count[e]++;"),
+    ("rank_priority_in_token_order", "        for (int r = 0; r < k; ++r)\n            for (int tok = 0; tok < T; ++tok) {",
+     "        for (int tok = 0; tok < T; ++tok)\n            for (int r = 0; r < k; ++r) {"),
+    ("rank_priority_keeps_one_too_many", "slot[i] = q < C ? q : -1;", "slot[i] = q <= C ? q : -1;"),
+    ("rank_priority_ignored", "if (priority == PRIORITY_RANK) {", "if (0) {"),
     ("cosine_no_emb_norm", "if (ne < 1e-12) ne = 1e-12;", "ne = 1.0;"),
     ("cosine_times_temperature", "num / (nu * ne) / temperature", "num / (nu * ne) * temperature"),
     ("cosine_emb_transposed", "elem(emb, (size_t)e * (size_t)p + (size_t)j, dtype)",
      "elem(emb, (size_t)j * (size_t)E + (size_t)e, dtype)"),
     ("dot_off_by_one", "for (int i = 0; i < n; ++i)\n        s += elem(a", "for (int i = 0; i < n - 1; ++i)\n        s += elem(a"),
-    ("gate_reads_token0", "double s = dot_rows(x, xo, w_gate", "double s = dot_rows(x, 0, w_gate"),
+    ("gate_reads_token0", "double s = dot_rows(x, xo, dtype, w_gate", "double s = dot_rows(x, 0, dtype, w_gate"),
     ("b1_dropped", "if (b1) z += elem(b1,", "if (0) z += elem(b1,"),
     ("b2_dropped", "if (b2) z += elem(b2,", "if (0) z += elem(b2,"),
-    ("w2_transposed", "elem(w2, w2_off + (size_t)n * (size_t)h + (size_t)i, dtype)",
-     "elem(w2, w2_off + (size_t)i * (size_t)d + (size_t)n, dtype)"),
+    ("w2_transposed", "elem(w2, w2_off + (size_t)n * (size_t)h + (size_t)i, wdtype)",
+     "elem(w2, w2_off + (size_t)i * (size_t)d + (size_t)n, wdtype)"),
+    ("w1_reads_x_dtype", "w1_off + (size_t)n * (size_t)d, wdtype, d);", "w1_off + (size_t)n * (size_t)d, dtype, d);"),
+    ("fp8_exponent_bias_8", "mag = ldexp(1.0 + (double)man / 8.0, ex - 7);", "mag = ldexp(1.0 + (double)man / 8.0, ex - 8);"),
+    ("fp8_subnormal_as_normal", "mag = ldexp((double)man / 8.0, -6);", "mag = ldexp(1.0 + (double)man / 8.0, -7);"),
+    ("fp8_sign_dropped", "return sign ? -mag : mag;", "return mag;"),
+    ("fp8_scale_block_transposed", "scale[(size_t)(r / block) * sc + (c / block)]",
+     "scale[(size_t)(c / block) * sc + (r / block)]"),
     ("combine_drops_gate", "o[n] += g * y[n];", "o[n] += y[n];"),
     ("combine_keeps_dropped", "if (slot[(size_t)t * k + j] < 0) continue;", ""),
     ("std_over_n", "0.1 * sqrt(ss / (double)(E - 1))", "0.1 * sqrt(ss / (double)E)"),

@@ -60,6 +60,7 @@ def test_static_scratch_dispatch_matches_workspace_dispatch():
     cases = [
         small_workload(T=1000, d=128, h=64, E=6, k=2, capacity_factor=1.0),          # drops, ragged last block
         small_workload(T=777, d=192, h=64, E=37, k=3, gate="noisy", capacity_factor=0.8),
+        small_workload(T=500, d=128, h=64, E=9, k=2, capacity_factor=0.8, priority="rank"),  # slots in rank order
     ]
     for i, wl in enumerate(cases):  # two calls in a row: the second reuses the array the first left dirty
         tg = {n: (v.to(dev) if v is not None else None) for n, v in make_inputs(wl, device="cpu").items()}
