@@ -107,7 +107,6 @@ def peaks():
 def layer_work(wl, kept_pairs: int, experts_used: int):
     """Algorithmic work of one forward: FLOPs of the kept (token, expert) pairs through both expert
     GEMMs plus the gate GEMM, and the expert-weight bytes the used experts occupy."""
-    esize = 2 if wl.dtype == "bf16" else 4
     gemm = 2.0 * kept_pairs * wl.d * wl.h  # one of the two expert GEMMs
     if wl.gate == "softmax":
         gate = 2.0 * wl.T * wl.d * wl.E
@@ -115,7 +114,7 @@ def layer_work(wl, kept_pairs: int, experts_used: int):
         gate = 4.0 * wl.T * wl.d * wl.E
     else:
         gate = 2.0 * wl.T * wl.d * wl.cos_dim + 2.0 * wl.T * wl.cos_dim * wl.E
-    wbytes = experts_used * 2 * wl.d * wl.h * esize
+    wbytes = experts_used * (wl.expert_weight_bytes() // wl.E)  # both matrices (block-FP8: codes + scales)
     return gemm, gate, wbytes
 
 
@@ -468,11 +467,18 @@ class Layer:
 
     def step(self, x=None, eps=None, out=None, count="default"):
         b, t = self.b, self.tg
-        b.check(b.moe_forward(self.cfg, t["x"] if x is None else x, t.get("w_gate"), t.get("w_noise"),
-                              t.get("eps") if eps is None else eps, t.get("proj"), t.get("emb"), t["w1"],
-                              t.get("b1"), t["w2"], t.get("b2"), self.out if out is None else out,
-                              self.count if count == "default" else count, self.ws, self.ws.numel(), self.stream),
-                "moe_forward")
+        xx = t["x"] if x is None else x
+        ee = t.get("eps") if eps is None else eps
+        oo = self.out if out is None else out
+        cc = self.count if count == "default" else count
+        if t.get("w1_scale") is not None:  # block-FP8 expert weights
+            b.check(b.moe_forward_fp8(self.cfg, xx, t.get("w_gate"), t.get("w_noise"), ee, t.get("proj"), t.get("emb"),
+                                      t["w1"], t["w1_scale"], t.get("b1"), t["w2"], t["w2_scale"], t.get("b2"), oo, cc,
+                                      self.ws, self.ws.numel(), self.stream), "moe_forward_fp8")
+            return
+        b.check(b.moe_forward(self.cfg, xx, t.get("w_gate"), t.get("w_noise"), ee, t.get("proj"), t.get("emb"),
+                              t["w1"], t.get("b1"), t["w2"], t.get("b2"), oo, cc, self.ws, self.ws.numel(),
+                              self.stream), "moe_forward")
 
     def capture(self, traced_events=None):
         """A CUDA graph of one step; with events, the library's trace hook puts an event-record node

@@ -54,6 +54,7 @@ struct TcArgs {
     int E, K, N, mode;
     int* err;
     const float* scale;  // block-FP8 weights: fp32 scale per 128 x 128 block, [E, N/128, K/128]
+    int stages;          // SM-pair kernel: depth of its TMA ring
 };
 
 using namespace tc;
@@ -292,7 +293,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // tile whose upper half is discarded.  Barriers: FULL (even CTA, count 1: its producer expects both
 // CTAs' bytes, and both CTAs' copies complete on it), EMPTY and TFULL (both CTAs, by multicast commit),
 // TEMPTY (even CTA, count 8: four epilogue warps of each CTA).
-constexpr int k2Stages = 6;
+constexpr int k2Stages = 6;       // with a bias (its staging buffers take 4 KiB)
+constexpr int k2StagesNoBias = 7;  // without one: 224 KiB of ring
 constexpr uint32_t k2HalfB = 128 * kBK * 2;            // 16 KiB: 128 of the 256 weight rows
 constexpr uint32_t k2StageBytes = kABytes + k2HalfB;   // 32 KiB per CTA
 
@@ -315,9 +317,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t* sA = base;
-    uint8_t* sB = base + k2Stages * kABytes;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sB + k2Stages * k2HalfB);
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * k2Stages + 5);
+    const int NS = a.stages;
+    uint8_t* sB = base + NS * kABytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sB + NS * k2HalfB);
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * NS + 5);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
     int* s_off = reinterpret_cast<int*>(tmem_holder + 4);
     int* s_tp = s_off + (a.E + 1);  // first 256-row tile of each expert (prefix), E + 1 entries
@@ -327,13 +330,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t rank = cluster_ctarank();
     const bool leader = rank == 0;
     auto bar = [&](int i) { return smem_u32(bars + i); };
-    const int FULL = 0, EMPTY = k2Stages, TFULL = 2 * k2Stages, TEMPTY = 2 * k2Stages + 2, LAST = 2 * k2Stages + 4;
+    const int FULL = 0, EMPTY = NS, TFULL = 2 * NS, TEMPTY = 2 * NS + 2, LAST = 2 * NS + 4;
 
     if (threadIdx.x == 0) {
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmB);
         *abort_flag = 0;
-        for (int st = 0; st < k2Stages; ++st) {
+        for (int st = 0; st < NS; ++st) {
             mbar_init(bar(FULL + st), 1);
             mbar_init(bar(EMPTY + st), 1);
         }
@@ -386,7 +389,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     tma_load_2d_pair(smem_u32(sA + stage * kABytes), &tmA, fb, kb * kBK, m0 + 128 * (int)rank);
                     tma_load_3d_pair(smem_u32(sB + stage * k2HalfB), &tmB, fb, kb * kBK, n0 + 128 * (int)rank, e);
                     any = true;
-                    if (++stage == k2Stages) { stage = 0; phase ^= 1u; }
+                    if (++stage == NS) { stage = 0; phase ^= 1u; }
                 }
             }
             if (!ok) {
@@ -422,7 +425,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                       (kb | kk) != 0);
                     any = true;
                     commit_pair_mc(bar(EMPTY + stage), 3);
-                    if (++stage == k2Stages) { stage = 0; phase ^= 1u; }
+                    if (++stage == NS) { stage = 0; phase ^= 1u; }
                 }
                 if (ok) commit_pair_mc(bar(TFULL + acc), 3);
             }
@@ -822,8 +825,13 @@ size_t ffn_tc_smem_bytes(int E) {
     return 1024 + (size_t)kStages * kStageBytes + (2 * kStages + 5) * 8 + 16 + 4 * (size_t)(E + 1) + kBiasSmem;
 }
 
-size_t ffn_tc_pair_smem_bytes(int E) {
-    return 1024 + (size_t)k2Stages * k2StageBytes + (2 * k2Stages + 5) * 8 + 16 + 8 * (size_t)(E + 1) + kBiasSmem;
+size_t ffn_tc_pair_smem_bytes(int E, bool bias, int ns) {
+    return 1024 + (size_t)ns * k2StageBytes + (2 * ns + 5) * 8 + 16 + 8 * (size_t)(E + 1) + (bias ? kBiasSmem : 0);
+}
+
+// the SM-pair kernel's ring depth: one stage more when there is no bias to stage and it fits
+int pair_stages(int E, bool bias) {
+    return !bias && ffn_tc_pair_smem_bytes(E, false, k2StagesNoBias) <= 227 * 1024 ? k2StagesNoBias : k2Stages;
 }
 
 size_t ffn_fp8_smem_bytes(int E) {
@@ -840,7 +848,7 @@ cudaError_t launch_ffn_tc(const FfnParams& P, cudaStream_t s) {
         if (P.K % kF8Block || P.N % kF8Block) return cudaErrorInvalidValue;
         if (!tma_map_kind(P.W, (uint64_t)P.K, (uint64_t)P.N, (uint64_t)P.E, kBN, 1, &mb)) return cudaErrorInvalidValue;
         TcArgs a8{P.offset, P.row_token, P.row_gate, static_cast<const bf16_t*>(P.bias), P.C, P.out,
-                  P.E, P.K, P.N, P.mode, P.err, P.w_scale};
+                  P.E, P.K, P.N, P.mode, P.err, P.w_scale, kF8Stages};
         const size_t smem8 = ffn_fp8_smem_bytes(P.E);
         cudaError_t e8 = cudaFuncSetAttribute(gemm_fp8w_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem8);
         if (e8 != cudaSuccess) return e8;
@@ -863,11 +871,13 @@ cudaError_t launch_ffn_tc(const FfnParams& P, cudaStream_t s) {
     a.mode = P.mode;
     a.err = P.err;
     a.scale = nullptr;
+    a.stages = kStages;
     if (P.pair) {
         // pairs of SMs: B boxes of 128 weight rows (half of a 256-wide tile), grid = 2 x the clusters that fit
         CUtensorMap mb2;
         if (!tma_map_bf16(P.W, (uint64_t)P.K, (uint64_t)P.N, (uint64_t)P.E, 128, &mb2)) return cudaErrorInvalidValue;
-        const size_t smem2 = ffn_tc_pair_smem_bytes(P.E);
+        a.stages = pair_stages(P.E, P.bias != nullptr);
+        const size_t smem2 = ffn_tc_pair_smem_bytes(P.E, P.bias != nullptr, a.stages);
         cudaError_t e2 =
             cudaFuncSetAttribute(gemm_tc_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2);
         if (e2 != cudaSuccess) return e2;

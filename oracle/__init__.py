@@ -106,6 +106,7 @@ class Oracle:
             "oracle_expert": ([I, I, I, I, P, S, P, S, P, S, P, S, P, S, P], None),
             "oracle_combine_tokens": ([I, I, I, I, I, P, I, P, P, P, P, P, P, P, P, P], None),
             "oracle_dequant_block_fp8": ([I, I, I, P, P, P], None),
+            "oracle_backward": ([I, I, I, I, I, I, I, I, I, I] + [P] * 16, None),
             "oracle_router_stats": ([I, I, I, P, P, P, P, P, P, P], None),
         }
         for name, (args, res) in sigs.items():
@@ -207,6 +208,35 @@ class Oracle:
             self.lib.oracle_dequant_block_fp8(rows, cols, block, _ptr(qq[i]), _ptr(ss[i]), _ptr(out[i]))
         return out.reshape(lead + (rows, cols))
 
+    def backward(self, spec, t, dout):
+        """Gradients of sum(dout * out) for the whole layer (softmax or noisy gate): a dict with dx [T, d],
+        dw_gate [E, d], dw_noise [E, d] (noisy gate), dw1 [E, h, d], db1 [E, h], dw2 [E, d, h], db2 [E, d],
+        all float64.  ``spec`` and ``t`` as for forward(); dout [T, d]."""
+        gate = _GATE_CODES[spec["gate"]]
+        if gate == GATE_COSINE:
+            raise NotImplementedError("the oracle's backward covers the softmax and noisy gates")
+        xs, wg, wn, a1, c1, a2, c2 = (_raw(t.get(n)) for n in ("x", "w_gate", "w_noise", "w1", "b1", "w2", "b2"))
+        dt = _same_dtype(xs, wg, wn, a1, c1, a2, c2)
+        T, d = xs[0].shape
+        E, h, _ = a1[0].shape
+        k = spec["k"]
+        C = self.capacity(T, E, k, spec.get("capacity_factor", 1.0), spec.get("capacity", -1))
+        ep = None
+        if gate == GATE_NOISY:
+            ep = t["eps"].detach().cpu().numpy() if hasattr(t["eps"], "detach") else t["eps"]
+            ep = np.ascontiguousarray(ep, dtype=np.float32)
+        go = dout.detach().cpu().numpy() if hasattr(dout, "detach") else dout
+        go = np.ascontiguousarray(go, dtype=np.float64)
+        out = dict(dx=np.empty((T, d)), dw_gate=np.empty((E, d)), dw1=np.empty((E, h, d)), db1=np.empty((E, h)),
+                   dw2=np.empty((E, d, h)), db2=np.empty((E, d)))
+        out["dw_noise"] = np.empty((E, d)) if gate == GATE_NOISY else None
+        self.lib.oracle_backward(gate, _NORM_CODES[spec["norm"]], T, d, h, E, k, C,
+                                 _PRIORITY_CODES[spec.get("priority", "token")], dt, _ptr(xs[0]), _ptr(wg[0]),
+                                 _ptr(wn[0]), _ptr(ep), _ptr(a1[0]), _ptr(c1[0]), _ptr(a2[0]), _ptr(c2[0]), _ptr(go),
+                                 _ptr(out["dx"]), _ptr(out["dw_gate"]), _ptr(out["dw_noise"]), _ptr(out["dw1"]),
+                                 _ptr(out["db1"]), _ptr(out["dw2"]), _ptr(out["db2"]))
+        return out
+
     def router_stats(self, idx, gate, E, slot=None):
         """Router statistics: (importance float64 [E], expert_importance_loss, load_balance_loss, dropped)."""
         idx = np.ascontiguousarray(idx, dtype=np.int32)
@@ -288,6 +318,10 @@ def router_stats(*a, **kw):
 
 def dequant_block_fp8(*a, **kw):
     return default().dequant_block_fp8(*a, **kw)
+
+
+def backward(*a, **kw):
+    return default().backward(*a, **kw)
 
 
 def route(*a, **kw):

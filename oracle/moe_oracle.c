@@ -295,3 +295,130 @@ void oracle_router_stats(int T, int E, int k, const int32_t *idx, const double *
     *importance_loss = E > 1 ? 0.1 * sqrt(ss / (double)(E - 1)) : NAN;
     *dropped = drops;
 }
+
+/* ---- backward of the layer ------------------------------------------------------------------------
+ * "MoE sparse-compute acceleration", section 2.1: only the top-k paths carry gradients (the sparse gate
+ * matrix is zero elsewhere, so nothing flows to the other experts or through the choice itself).  Given
+ * dout = dL/dout [T, d] (fp64), the layer is recomputed (scores, top-k, gates, capacity dispatch) and for
+ * every kept pair (t, e, gate g), with z = W1[e] x_t + b1[e], a = GELU(z), y = W2[e] a + b2[e]:
+ *   dg = dout_t . y          dy = g dout_t         dW2[e] += dy a^T     db2[e] += dy
+ *   da = W2[e]^T dy          dz = da * GELU'(z)    dW1[e] += dz x_t^T   db1[e] += dz     dx_t += W1[e]^T dz
+ * with GELU'(z) = Phi(z) + z phi(z); a dropped pair has dg = 0.  The gates' gradient reaches the scores:
+ *   NORM_TOPK (softmax over the k chosen scores): ds_{e_j} = g_j (dg_j - sum_j' g_j' dg_j'), 0 elsewhere;
+ *   NORM_ALL (the chosen entries of the softmax over all E): ds_e = sum_j dg_j g_j ([e = e_j] - p_e).
+ * and the scores' reaches the gate weights and x:
+ *   SOFTMAX: s = x W_g^T                       dW_g[e] += ds_e x_t,  dx_t += sum_e ds_e W_g[e]
+ *   NOISY:   s = x W_g^T + eps softplus(x W_n^T)  additionally dn_e = ds_e eps_e sigmoid(x . W_n[e]):
+ *            dW_n[e] += dn_e x_t,  dx_t += sum_e dn_e W_n[e]
+ * (softplus' = sigmoid).  The cosine gate's backward is not part of this oracle.  Outputs are written
+ * (not accumulated); dw_noise may be NULL for the softmax gate, db1 / db2 are written even without biases. */
+static double gelu_grad(double z)
+{
+    const double pi = 3.14159265358979323846;
+    return 0.5 * (1.0 + erf(z * sqrt(0.5))) + z * exp(-0.5 * z * z) / sqrt(2.0 * pi);
+}
+
+static double sigmoid(double z) { return 1.0 / (1.0 + exp(-z)); }
+
+void oracle_backward(int gate_type, int norm, int T, int d, int h, int E, int k, int C, int priority, int dtype,
+                     const void *x, const void *w_gate, const void *w_noise, const float *eps, const void *w1,
+                     const void *b1, const void *w2, const void *b2, const double *dout, double *dx,
+                     double *dw_gate, double *dw_noise, double *dw1, double *db1, double *dw2, double *db2)
+{
+    double *scores = (double *)malloc(sizeof(double) * (size_t)T * E);
+    int32_t *idx = (int32_t *)malloc(sizeof(int32_t) * (size_t)T * k);
+    double *gate = (double *)malloc(sizeof(double) * (size_t)T * k);
+    int32_t *slot = (int32_t *)malloc(sizeof(int32_t) * (size_t)T * k);
+    int32_t *count = (int32_t *)malloc(sizeof(int32_t) * (size_t)E);
+    double *z = (double *)malloc(sizeof(double) * (size_t)h);
+    double *a = (double *)malloc(sizeof(double) * (size_t)h);
+    double *da = (double *)malloc(sizeof(double) * (size_t)h);
+    double *dg = (double *)malloc(sizeof(double) * (size_t)k);
+    double *ds = (double *)malloc(sizeof(double) * (size_t)E);
+    double *p = (double *)malloc(sizeof(double) * (size_t)E);
+    oracle_gate_scores(gate_type, T, d, E, 0, 1.0, dtype, x, w_gate, w_noise, eps, NULL, NULL, scores);
+    oracle_topk(T, E, k, norm, scores, idx, gate);
+    oracle_dispatch(T, E, k, C, priority, idx, slot, count);
+    memset(dx, 0, sizeof(double) * (size_t)T * d);
+    memset(dw_gate, 0, sizeof(double) * (size_t)E * d);
+    if (dw_noise) memset(dw_noise, 0, sizeof(double) * (size_t)E * d);
+    memset(dw1, 0, sizeof(double) * (size_t)E * h * d);
+    memset(db1, 0, sizeof(double) * (size_t)E * h);
+    memset(dw2, 0, sizeof(double) * (size_t)E * d * h);
+    memset(db2, 0, sizeof(double) * (size_t)E * d);
+    for (int t = 0; t < T; ++t) {
+        const size_t xo = (size_t)t * d;
+        const double *go = dout + xo;
+        double *gx = dx + xo;
+        /* the experts */
+        for (int j = 0; j < k; ++j) {
+            const size_t i = (size_t)t * k + j;
+            dg[j] = 0.0;
+            if (slot[i] < 0) continue;
+            const size_t e = (size_t)idx[i];
+            const double g = gate[i];
+            for (int n = 0; n < h; ++n) {
+                z[n] = dot_rows(x, xo, dtype, w1, (e * h + n) * (size_t)d, dtype, d);
+                if (b1) z[n] += elem(b1, e * h + n, dtype);
+                a[n] = gelu_erf(z[n]);
+                da[n] = 0.0;
+            }
+            for (int m = 0; m < d; ++m) {
+                double y = 0.0;
+                for (int n = 0; n < h; ++n) y += a[n] * elem(w2, (e * d + m) * (size_t)h + n, dtype);
+                if (b2) y += elem(b2, e * d + m, dtype);
+                dg[j] += go[m] * y;
+                const double dy = g * go[m];
+                db2[e * d + m] += dy;
+                for (int n = 0; n < h; ++n) {
+                    dw2[(e * d + m) * (size_t)h + n] += dy * a[n];
+                    da[n] += elem(w2, (e * d + m) * (size_t)h + n, dtype) * dy;
+                }
+            }
+            for (int n = 0; n < h; ++n) {
+                const double dz = da[n] * gelu_grad(z[n]);
+                db1[e * h + n] += dz;
+                for (int m = 0; m < d; ++m) {
+                    dw1[(e * h + n) * (size_t)d + m] += dz * elem(x, xo + m, dtype);
+                    gx[m] += elem(w1, (e * h + n) * (size_t)d + m, dtype) * dz;
+                }
+            }
+        }
+        /* the gates -> the scores */
+        for (int e = 0; e < E; ++e) ds[e] = 0.0;
+        if (norm == NORM_TOPK) {
+            double sum = 0.0;
+            for (int j = 0; j < k; ++j) sum += gate[(size_t)t * k + j] * dg[j];
+            for (int j = 0; j < k; ++j) ds[idx[(size_t)t * k + j]] = gate[(size_t)t * k + j] * (dg[j] - sum);
+        } else {
+            const double *s = scores + (size_t)t * E;
+            double m = s[0], den = 0.0;
+            for (int e = 1; e < E; ++e) if (s[e] > m) m = s[e];
+            for (int e = 0; e < E; ++e) p[e] = exp(s[e] - m);
+            for (int e = 0; e < E; ++e) den += p[e];
+            for (int e = 0; e < E; ++e) p[e] /= den;
+            for (int j = 0; j < k; ++j) {
+                const double gj = gate[(size_t)t * k + j];
+                for (int e = 0; e < E; ++e) ds[e] += dg[j] * gj * ((e == idx[(size_t)t * k + j] ? 1.0 : 0.0) - p[e]);
+            }
+        }
+        /* the scores -> the gate weights and x */
+        for (int e = 0; e < E; ++e) {
+            if (ds[e] == 0.0) continue;
+            for (int m = 0; m < d; ++m) {
+                dw_gate[(size_t)e * d + m] += ds[e] * elem(x, xo + m, dtype);
+                gx[m] += ds[e] * elem(w_gate, (size_t)e * d + m, dtype);
+            }
+            if (gate_type == GATE_NOISY) {
+                const double nl = dot_rows(x, xo, dtype, w_noise, (size_t)e * d, dtype, d);
+                const double dn = ds[e] * (double)eps[(size_t)t * E + e] * sigmoid(nl);
+                for (int m = 0; m < d; ++m) {
+                    dw_noise[(size_t)e * d + m] += dn * elem(x, xo + m, dtype);
+                    gx[m] += dn * elem(w_noise, (size_t)e * d + m, dtype);
+                }
+            }
+        }
+    }
+    free(scores); free(idx); free(gate); free(slot); free(count);
+    free(z); free(a); free(da); free(dg); free(ds); free(p);
+}

@@ -204,6 +204,61 @@ def pin_fp8_expert_with_dequantised_weights(o):
     assert np.array_equal(y, yb)
 
 
+def _fd_layer(seed, gate, E=4):
+    g = torch.Generator().manual_seed(seed)
+    T, d, h = 6, 8, 12
+    t = {"x": torch.randn(T, d, generator=g), "w_gate": torch.randn(E, d, generator=g) * 0.6,
+         "w1": torch.randn(E, h, d, generator=g) * 0.4, "b1": torch.randn(E, h, generator=g) * 0.3,
+         "w2": torch.randn(E, d, h, generator=g) * 0.3, "b2": torch.randn(E, d, generator=g) * 0.3}
+    if gate == "noisy":
+        t["w_noise"] = torch.randn(E, d, generator=g) * 0.6
+        t["eps"] = torch.randn(T, E, generator=g)
+    dout = torch.randn(T, d, generator=g, dtype=torch.float64)
+    return t, dout
+
+
+def pin_backward_finite_differences(o):
+    """The backward against central differences of the oracle's own forward (loss = sum(dout * out)) on tiny
+    fp32 layers: every gradient tensor (x, both gate weights, both expert weights and biases) at sampled
+    entries, for the softmax and noisy gates, both gate normalisations, with and without capacity drops,
+    token and rank priority.  The step is a power of two, each perturbed value is exact in fp32, and the
+    routing must not change under the step (else the case would not be differentiable there)."""
+    cases = [("softmax", "topk", 2, 6, "token", 21), ("softmax", "all", 1, 6, "token", 22),
+             ("noisy", "topk", 2, 2, "token", 23), ("softmax", "topk", 3, 3, "rank", 24), ("noisy", "topk", 1, 2, "token", 25)]
+    rng = np.random.default_rng(9)
+    dropped_somewhere = False
+    for gate, norm, k, cap, prio, seed in cases:
+        t, dout = _fd_layer(seed, gate)
+        spec = dict(gate=gate, norm=norm, k=k, E=4, capacity=cap, capacity_factor=1.0, temperature=1.0,
+                    priority=prio)
+        grads = o.backward(spec, t, dout)
+        base = o.forward(spec, t)
+        dropped_somewhere = dropped_somewhere or bool((base["slot"] < 0).any())
+
+        def loss(tt):
+            f = o.forward(spec, tt)
+            assert np.array_equal(f["idx"], base["idx"]) and np.array_equal(f["slot"], base["slot"])
+            return float((f["out"] * dout.numpy()).sum())
+
+        names = [("x", "dx"), ("w_gate", "dw_gate"), ("w1", "dw1"), ("b1", "db1"), ("w2", "dw2"), ("b2", "db2")]
+        if gate == "noisy":
+            names.append(("w_noise", "dw_noise"))
+        for name, key in names:
+            flat = t[name].reshape(-1)
+            for i in rng.choice(flat.numel(), size=6, replace=False):
+                step = 2.0 ** -12
+                plus, minus = dict(t), dict(t)
+                vp, vm = t[name].clone(), t[name].clone()
+                vp.view(-1)[i] += step
+                vm.view(-1)[i] -= step
+                plus[name], minus[name] = vp, vm
+                width = float(vp.view(-1)[i]) - float(vm.view(-1)[i])
+                fd = (loss(plus) - loss(minus)) / width
+                an = grads[key].reshape(-1)[i]
+                assert abs(fd - an) <= 1e-6 * max(1.0, abs(an)), (gate, norm, name, int(i), fd, an)
+    assert dropped_somewhere  # the capacity cases do drop pairs
+
+
 def pin_gelu_normal_cdf(o):
     """Identity weights make the expert return GELU(x) itself; GELU(z) = z Phi(z) with Phi from a table."""
     g = GOLDEN["gelu_normal_cdf"]

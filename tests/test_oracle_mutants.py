@@ -38,6 +38,15 @@ MUTANTS = [
     ("w2_transposed", "elem(w2, w2_off + (size_t)n * (size_t)h + (size_t)i, wdtype)",
      "elem(w2, w2_off + (size_t)i * (size_t)d + (size_t)n, wdtype)"),
     ("w1_reads_x_dtype", "w1_off + (size_t)n * (size_t)d, wdtype, d);", "w1_off + (size_t)n * (size_t)d, dtype, d);"),
+    ("gelu_grad_drops_density", " + z * exp(-0.5 * z * z) / sqrt(2.0 * pi);", ";"),
+    ("topk_gate_grad_sign", "gate[(size_t)t * k + j] * (dg[j] - sum);", "gate[(size_t)t * k + j] * (sum - dg[j]);"),
+    ("dropped_pair_gets_gradient", "            dg[j] = 0.0;\n            if (slot[i] < 0) continue;",
+     "            dg[j] = 0.0;"),
+    ("noisy_grad_without_eps", "ds[e] * (double)eps[(size_t)t * E + e] * sigmoid(nl)", "ds[e] * sigmoid(nl)"),
+    ("dw2_from_preactivation", "dw2[(e * d + m) * (size_t)h + n] += dy * a[n];", "dw2[(e * d + m) * (size_t)h + n] += dy * z[n];"),
+    ("all_norm_grad_drops_softmax", "((e == idx[(size_t)t * k + j] ? 1.0 : 0.0) - p[e])",
+     "(e == idx[(size_t)t * k + j] ? 1.0 : 0.0)"),
+    ("dx_misses_gate_path", "gx[m] += ds[e] * elem(w_gate,", "gx[m] += 0.0 * elem(w_gate,"),
     ("fp8_exponent_bias_8", "mag = ldexp(1.0 + (double)man / 8.0, ex - 7);", "mag = ldexp(1.0 + (double)man / 8.0, ex - 8);"),
     ("fp8_subnormal_as_normal", "mag = ldexp((double)man / 8.0, -6);", "mag = ldexp(1.0 + (double)man / 8.0, -7);"),
     ("fp8_sign_dropped", "return sign ? -mag : mag;", "return mag;"),
