@@ -154,27 +154,41 @@ class NvmlSampler:
         self.stop_flag = threading.Event()
         self.thread = None
         self.nv = None
+        self.error = None
         try:
             import pynvml as nv
 
             nv.nvmlInit()
             uuid = str(torch.cuda.get_device_properties(device_index).uuid)
             uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
-            self.h = nv.nvmlDeviceGetHandleByUUID(uuid.encode())
+            try:
+                self.h = nv.nvmlDeviceGetHandleByUUID(uuid)
+            except Exception:  # noqa: BLE001 -- fall back to the index NVML and CUDA usually share
+                self.h = nv.nvmlDeviceGetHandleByIndex(device_index)
             self.nv = nv
-        except Exception:
+        except Exception as e:  # noqa: BLE001
+            self.error = "init: %s" % e
             self.nv = None
 
     def _run(self):
         nv = self.nv
+        reasons_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(nv, "nvmlDeviceGetCurrentClocksThrottleReasons", None)
         while not self.stop_flag.is_set():
             try:
                 sm = nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM)
-                pw = nv.nvmlDeviceGetPowerUsage(self.h) / 1000.0
-                rs = nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
-                self.samples.append((sm, pw, rs))
-            except Exception:
+            except Exception as e:  # noqa: BLE001 -- reported, never fatal
+                self.error = "clock: %s" % e
                 return
+            try:
+                pw = nv.nvmlDeviceGetPowerUsage(self.h) / 1000.0
+            except Exception:  # noqa: BLE001
+                pw = float("nan")
+            try:
+                rs = reasons_fn(self.h) if reasons_fn else 0
+            except Exception:  # noqa: BLE001
+                rs = 0
+            self.samples.append((sm, pw, rs))
             time.sleep(self.period)
 
     def start(self):
@@ -187,11 +201,11 @@ class NvmlSampler:
 
     def stop(self):
         if self.thread is None:
-            return None
+            return {"error": self.error} if self.error else None
         self.stop_flag.set()
         self.thread.join(timeout=2)
         if not self.samples:
-            return None
+            return {"error": self.error or "no samples"}
         nv = self.nv
         sm = [s[0] for s in self.samples]
         reasons = sorted({n for n, attr in self.REASONS for s in self.samples if s[2] & getattr(nv, attr, 0)})
@@ -202,6 +216,8 @@ class NvmlSampler:
         return {"sm_mhz": statistics.median(sm), "sm_mhz_min": min(sm), "sm_max_mhz": mx,
                 "power_w_max": max(s[1] for s in self.samples), "reasons": reasons, "samples": len(sm),
                 "period_ms": self.period * 1e3}
+
+
 
 
 class ClockSampler:

@@ -281,6 +281,29 @@ MOE_API moe_status moe_forward(const moe_config* cfg, const void* x, const void*
                        const void* b2, float* out, int32_t* expert_count, void* workspace,
                        size_t workspace_bytes, void* stream);
 
+/* ---- backward --------------------------------------------------------------------------------- */
+/* Gradients of the layer for a loss L with dL/dout = dout [T, d] fp32 ("MoE sparse-compute acceleration",
+ * section 2.1: only the top-k paths carry gradients -- the sparse gate matrix is zero elsewhere, so nothing
+ * flows to unchosen experts, through the choice itself, or through dropped pairs):
+ *   dx [T, d], dw_gate [E, d], dw_noise [E, d] (noisy gate; may be NULL for softmax), dw1 [E, h, d],
+ *   dw2 [E, d, h], db1 [E, h] and db2 [E, d] (each may be NULL), all fp32 and overwritten.
+ * For every kept pair (t, e, gate g) with z = W1[e] x_t + b1[e], y = W2[e] GELU(z) + b2[e]:
+ *   dg = dout_t . y;  dW2[e] += g dout_t GELU(z)^T;  dz = (W2[e]^T g dout_t) * GELU'(z);  dW1[e] += dz x_t^T;
+ *   dx_t += W1[e]^T dz;  and through the gates (softmax over the k chosen scores, or over all E for
+ *   MOE_GATE_NORM_ALL) to the scores, W_g (and for the noisy gate, through eps softplus(x W_n^T), to W_n)
+ *   and x.  The call recomputes the forward (routing, dispatch, the expert FFN keeping Z = W1 x + b1 in
+ *   bf16) and runs the backward GEMMs on the tensor cores: the data gradients grouped by expert over the
+ *   dispatched rows (with transposed copies of W1 and W2), the weight gradients contracting over each
+ *   expert's rows.  Intermediate gradients (dY = g dout per row, dZ, the scores' gradient) are rounded to
+ *   bf16 for the GEMMs; dx is accumulated with fp32 atomics (not bitwise reproducible).
+ * Supported: bf16 layers with the softmax or noisy gate (else MOE_ERR_UNSUPPORTED, also for
+ * MOE_FLAG_SIMT_FFN).  workspace: moe_backward_workspace_size(cfg) bytes (it includes the forward's). */
+MOE_API size_t moe_backward_workspace_size(const moe_config* cfg);
+MOE_API moe_status moe_backward(const moe_config* cfg, const void* x, const void* w_gate, const void* w_noise,
+                        const float* noise_eps, const void* w1, const void* b1, const void* w2, const void* b2,
+                        const float* dout, float* dx, float* dw_gate, float* dw_noise, float* dw1, float* db1,
+                        float* dw2, float* db2, void* workspace, size_t workspace_bytes, void* stream);
+
 /* ---- block-FP8 expert weights --------------------------------------------------------------------- */
 /* The same FFN step and whole layer with the expert weights stored as block FP8 ("MoE architecture:
  * breaking the single-card compute bottleneck", section 1.3: FP8 weights shrink the model; the Block FP8

@@ -80,6 +80,8 @@ def _load():
         "moe_router_stats": ([C, P, P, P, P, P, P, P, SZ, P], I32),
         "moe_forward": ([C, P, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P], I32),
         "moe_expert_ffn_fp8": ([C, P, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P], I32),
+        "moe_backward_workspace_size": ([C], SZ),
+        "moe_backward": ([C] + [P] * 17 + [SZ, P], I32),
         "moe_forward_fp8": ([C, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P], I32),
         "moe_device_status": ([P, SZ, ctypes.POINTER(I32), P], I32),
         "moe_trace_events": ([ctypes.POINTER(P), I32], None),
@@ -219,6 +221,17 @@ def moe_forward_fp8(cfg, x, w_gate, w_noise, noise_eps, proj, expert_emb, w1_q, 
     return lib.moe_forward_fp8(ctypes.byref(cfg), ptr(x), ptr(w_gate), ptr(w_noise), ptr(noise_eps), ptr(proj),
                                ptr(expert_emb), ptr(w1_q), ptr(w1_scale), ptr(b1), ptr(w2_q), ptr(w2_scale), ptr(b2),
                                ptr(out), ptr(expert_count), ptr(workspace), workspace_bytes, stream_handle(stream))
+
+
+def moe_backward_workspace_size(cfg: MoEConfig) -> int:
+    return lib.moe_backward_workspace_size(ctypes.byref(cfg))
+
+
+def moe_backward(cfg, x, w_gate, w_noise, noise_eps, w1, b1, w2, b2, dout, dx, dw_gate, dw_noise, dw1, db1, dw2, db2,
+                 workspace, workspace_bytes, stream=None) -> int:
+    return lib.moe_backward(ctypes.byref(cfg), ptr(x), ptr(w_gate), ptr(w_noise), ptr(noise_eps), ptr(w1), ptr(b1),
+                            ptr(w2), ptr(b2), ptr(dout), ptr(dx), ptr(dw_gate), ptr(dw_noise), ptr(dw1), ptr(db1),
+                            ptr(dw2), ptr(db2), ptr(workspace), workspace_bytes, stream_handle(stream))
 
 
 def moe_device_status(workspace, workspace_bytes, stream=None):

@@ -293,7 +293,7 @@ FfnParams ffn_params(const Plan& P, int mode, const void* A, const void* W, cons
     f.mode = mode;
     f.rows_cap = P.rows;
     f.err = err;
-    f.pair = w_scale ? 0 : P.pair;  // block-FP8 weights run on single SMs
+    f.pair = (w_scale || mode >= 3) ? 0 : P.pair;  // block-FP8 weights and the backward run on single SMs
     return f;
 }
 
@@ -354,33 +354,20 @@ moe_status expert_ffn_impl(const moe_config* cfg, const void* x_dispatched, cons
 
 namespace {
 
-moe_status forward_impl(const moe_config* cfg, const void* x, const void* w_gate, const void* w_noise,
-                        const float* noise_eps, const void* proj, const void* expert_emb, const void* w1,
-                        const float* s1, const void* b1, const void* w2, const float* s2, const void* b2, float* out,
-                        int32_t* expert_count, void* workspace, size_t workspace_bytes, void* stream) {
-    Plan P;
-    MOE_TRY(make_plan(cfg, &P));
-    if (s1 || s2) MOE_TRY(check_fp8_weights(P, cfg, w1, s1, w2, s2));
-    if (P.T == 0) return MOE_OK;
-    MOE_TRY(check_ws(P, workspace, workspace_bytes));
+// gate, dispatch ranks and scan, row gather of moe_forward, intermediates in the workspace (the error
+// header must be zeroed first); `zero` [T, d] is cleared by the gather when not null
+moe_status route_and_dispatch(const Plan& P, const moe_config* cfg, const void* x, const void* w_gate,
+                              const void* w_noise, const float* noise_eps, const void* proj, const void* expert_emb,
+                              int* count, float* zero, void* workspace, cudaStream_t s) {
     int32_t* idx = at<int32_t>(workspace, P.o_idx);
     float* gate = at<float>(workspace, P.o_gate);
-    MOE_TRY(check_route_args(P, x, w_gate, w_noise, noise_eps, proj, expert_emb, idx, gate));
-    if (!w1 || !w2 || !out || !aligned16(w1) || !aligned16(w2) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
-    if ((b1 && !aligned16(b1)) || (b2 && !aligned16(b2)) || (expert_count && !aligned16(expert_count)))
-        return MOE_ERR_INVALID_ARG;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
     int* err = at<int>(workspace, P.o_err);
     int* hist = at<int>(workspace, P.o_hist);
-    int* count = expert_count ? expert_count : at<int>(workspace, P.o_count);
     int* off = at<int>(workspace, P.o_off);
     int* slot = at<int>(workspace, P.o_slot);
     int* rtok = at<int>(workspace, P.o_rtok);
     float* rgate = at<float>(workspace, P.o_rgate);
     void* xd = at<void>(workspace, P.o_xd);
-    float* y = at<float>(workspace, P.o_y);
-    // error word, its info, the block tickets and the cosine gate's expert flags start at zero
-    if (cudaMemsetAsync(err, 0, P.hdr_bytes, s) != cudaSuccess) return MOE_ERR_CUDA;
     GateParams g = gate_params(P, cfg, x, w_gate, w_noise, noise_eps, proj, expert_emb, idx, gate);
     // with rank priority a gate kernel that ranks in token order leaves the ranking to the rank kernel
     const bool rank_after_gate = P.rank_major && gate_ranks_in_kernel(P);
@@ -403,13 +390,195 @@ moe_status forward_impl(const moe_config* cfg, const void* x, const void* w_gate
             return launch_dispatch_rank(idx, P.T, P.k, P.E, hist, slot, err, err + 2, P.Ceff, count, off, rtok, rgate,
                                         1, s);
         }));
-    MOE_TRY(launch(s, [&] {
+    return launch(s, [&] {
         return launch_dispatch_gather(x, P.bf16, idx, gate, hist, off, count, gather_scan, P.T, P.k, P.E, P.d, P.Ceff,
-                                      slot, rtok, rgate,
-                                      xd, P.fused ? out : nullptr, P.rank_major, s);
-    }));
+                                      slot, rtok, rgate, xd, zero, P.rank_major, s);
+    });
+}
+
+moe_status forward_impl(const moe_config* cfg, const void* x, const void* w_gate, const void* w_noise,
+                        const float* noise_eps, const void* proj, const void* expert_emb, const void* w1,
+                        const float* s1, const void* b1, const void* w2, const float* s2, const void* b2, float* out,
+                        int32_t* expert_count, void* workspace, size_t workspace_bytes, void* stream) {
+    Plan P;
+    MOE_TRY(make_plan(cfg, &P));
+    if (s1 || s2) MOE_TRY(check_fp8_weights(P, cfg, w1, s1, w2, s2));
+    if (P.T == 0) return MOE_OK;
+    MOE_TRY(check_ws(P, workspace, workspace_bytes));
+    int32_t* idx = at<int32_t>(workspace, P.o_idx);
+    float* gate = at<float>(workspace, P.o_gate);
+    MOE_TRY(check_route_args(P, x, w_gate, w_noise, noise_eps, proj, expert_emb, idx, gate));
+    if (!w1 || !w2 || !out || !aligned16(w1) || !aligned16(w2) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
+    if ((b1 && !aligned16(b1)) || (b2 && !aligned16(b2)) || (expert_count && !aligned16(expert_count)))
+        return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int* err = at<int>(workspace, P.o_err);
+    int* count = expert_count ? expert_count : at<int>(workspace, P.o_count);
+    int* off = at<int>(workspace, P.o_off);
+    int* slot = at<int>(workspace, P.o_slot);
+    int* rtok = at<int>(workspace, P.o_rtok);
+    float* rgate = at<float>(workspace, P.o_rgate);
+    void* xd = at<void>(workspace, P.o_xd);
+    float* y = at<float>(workspace, P.o_y);
+    // error word, its info, the block tickets and the cosine gate's expert flags start at zero
+    if (cudaMemsetAsync(err, 0, P.hdr_bytes, s) != cudaSuccess) return MOE_ERR_CUDA;
+    MOE_TRY(route_and_dispatch(P, cfg, x, w_gate, w_noise, noise_eps, proj, expert_emb, count, P.fused ? out : nullptr,
+                               workspace, s));
     MOE_TRY(ffn_and_combine(P, cfg, xd, off, rtok, rgate, w1, s1, b1, w2, s2, b2, y, out, P.fused != 0, workspace, s));
     if (!P.fused) MOE_TRY(launch(s, [&] { return launch_combine(y, slot, off, idx, gate, P.T, P.k, P.d, out, s); }));
+    return MOE_OK;
+}
+
+// ---- backward: its workspace after the forward's ------------------------------------------------------
+struct BwdPlan {
+    int Rp, Tp, Np, NpP;  // rows rounded to 64, tokens to 128, gate logits per token (and rounded to 64)
+    size_t o_z, o_dy, o_dz, o_xdT, o_hT, o_dyT, o_dzT, o_w1T, o_w2T, o_logits, o_dS, o_dST, o_xT, o_wcatT, o_dwcat,
+        o_rows, o_off2, total;
+};
+
+moe_status make_bwd_plan(const Plan& P, const moe_config* c, BwdPlan* B) {
+    if (!P.bf16 || P.gate == MOE_GATE_COSINE || (c->flags & MOE_FLAG_SIMT_FFN)) return MOE_ERR_UNSUPPORTED;
+    BwdPlan b{};
+    b.Rp = (int)((P.rows + 63) / 64 * 64);
+    b.Tp = (P.T + 127) / 128 * 128;
+    b.Np = P.gate == MOE_GATE_NOISY ? 2 * P.E : P.E;
+    b.NpP = (b.Np + 63) / 64 * 64;
+    size_t o = P.total;
+    auto take = [&](size_t bytes) { size_t r = o; o = up(o + bytes); return r; };
+    const size_t R = (size_t)P.rows;
+    b.o_z = take(R * P.h * 2);
+    b.o_dy = take(R * P.d * 2);
+    b.o_dz = take(R * P.h * 2);
+    b.o_xdT = take((size_t)P.d * b.Rp * 2);
+    b.o_hT = take((size_t)P.h * b.Rp * 2);
+    b.o_dyT = take((size_t)P.d * b.Rp * 2);
+    b.o_dzT = take((size_t)P.h * b.Rp * 2);
+    b.o_w1T = take((size_t)P.E * P.d * P.h * 2);
+    b.o_w2T = take((size_t)P.E * P.h * P.d * 2);
+    b.o_logits = take((size_t)P.T * b.Np * 4);
+    b.o_dS = take((size_t)b.Tp * b.NpP * 2);
+    b.o_dST = take((size_t)b.NpP * b.Tp * 2);
+    b.o_xT = take((size_t)P.d * b.Tp * 2);
+    b.o_wcatT = take((size_t)P.d * b.NpP * 2);
+    b.o_dwcat = take((size_t)b.Np * P.d * 4);
+    b.o_rows = take((size_t)b.Tp * 4);
+    b.o_off2 = take(8);
+    b.total = o;
+    *B = b;
+    return MOE_OK;
+}
+
+moe_status backward_impl(const moe_config* cfg, const void* x, const void* w_gate, const void* w_noise,
+                         const float* noise_eps, const void* w1, const void* b1, const void* w2, const void* b2,
+                         const float* dout, float* dx, float* dw_gate, float* dw_noise, float* dw1, float* db1,
+                         float* dw2, float* db2, void* ws, size_t ws_bytes, cudaStream_t s) {
+    Plan P;
+    MOE_TRY(make_plan(cfg, &P));
+    BwdPlan B;
+    MOE_TRY(make_bwd_plan(P, cfg, &B));
+    if (P.T == 0) return MOE_OK;
+    if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) || ws_bytes < B.total) return MOE_ERR_WORKSPACE;
+    int32_t* idx = at<int32_t>(ws, P.o_idx);
+    float* gate = at<float>(ws, P.o_gate);
+    MOE_TRY(check_route_args(P, x, w_gate, w_noise, noise_eps, nullptr, nullptr, idx, gate));
+    const void* need[] = {w1, w2, dout, dx, dw_gate, dw1, dw2};
+    for (const void* q : need)
+        if (!q || !aligned16(q)) return MOE_ERR_INVALID_ARG;
+    if (P.gate == MOE_GATE_NOISY && (!dw_noise || !aligned16(dw_noise))) return MOE_ERR_INVALID_ARG;
+    const void* opt[] = {b1, b2, db1, db2};
+    for (const void* q : opt)
+        if (q && !aligned16(q)) return MOE_ERR_INVALID_ARG;
+    int* err = at<int>(ws, P.o_err);
+    int* off = at<int>(ws, P.o_off);
+    int* slot = at<int>(ws, P.o_slot);
+    int* rtok = at<int>(ws, P.o_rtok);
+    float* rgate = at<float>(ws, P.o_rgate);
+    void* xd = at<void>(ws, P.o_xd);
+    void* hb = at<void>(ws, P.o_h);
+    float* y = at<float>(ws, P.o_y);
+    const int T = P.T, d = P.d, h = P.h, E = P.E, R = (int)P.rows;
+    if (cudaMemsetAsync(err, 0, P.hdr_bytes, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaMemsetAsync(dx, 0, (size_t)T * d * 4, s) != cudaSuccess) return MOE_ERR_CUDA;
+    // 1. the forward again: routing and dispatch, Z and H = GELU(Z), y per dispatched row, and the gate logits
+    MOE_TRY(route_and_dispatch(P, cfg, x, w_gate, w_noise, noise_eps, nullptr, nullptr, at<int>(ws, P.o_count),
+                               nullptr, ws, s));
+    FfnParams up = ffn_params(P, 4, xd, w1, nullptr, b1, off, rtok, rgate, hb, nullptr, err);
+    up.aux = at<void>(ws, B.o_z);
+    MOE_TRY(run_ffn(P, cfg, up, s));
+    MOE_TRY(run_ffn(P, cfg, ffn_params(P, 1, hb, w2, nullptr, b2, off, rtok, rgate, y, nullptr, err), s));
+    const GateGemmPlan one = gate_gemm_plan(T, d, P.N0, P.N1, 1, false);
+    float* logits = at<float>(ws, B.o_logits);
+    MOE_TRY(launch(s, [&] {
+        return launch_gate_gemm(one, x, w_gate, P.gate == MOE_GATE_NOISY ? w_noise : nullptr, T, d, P.N0, P.N1,
+                                logits, nullptr, nullptr, err, nullptr, s);
+    }));
+    // 2. dY = gate * dout per row; the gates' and scores' gradient per token
+    void* dy = at<void>(ws, B.o_dy);
+    void* dS = at<void>(ws, B.o_dS);
+    MOE_TRY(launch(s, [&] { return launch_bwd_dy(dout, rtok, rgate, R, d, dy, s); }));
+    MOE_TRY(launch(s, [&] {
+        return launch_bwd_gate(dout, y, idx, gate, slot, off, logits, noise_eps, T, B.Tp, d, E, P.k,
+                               P.gate == MOE_GATE_NOISY, P.norm == MOE_GATE_NORM_ALL, B.NpP, dS, s);
+    }));
+    // 3. data gradients through the experts: dZ = (dY W2) * GELU'(Z), dx += dZ W1 (scattered to tokens)
+    void* w1T = at<void>(ws, B.o_w1T);
+    void* w2T = at<void>(ws, B.o_w2T);
+    void* dz = at<void>(ws, B.o_dz);
+    MOE_TRY(launch(s, [&] { return launch_transpose(w2, w2T, E, d, h, d, nullptr, s); }));
+    MOE_TRY(launch(s, [&] { return launch_transpose(w1, w1T, E, h, d, h, nullptr, s); }));
+    FfnParams da{};
+    da.A = dy; da.W = w2T; da.offset = off; da.row_token = rtok; da.row_gate = rgate; da.C = dz;
+    da.aux = at<void>(ws, B.o_z); da.E = E; da.K = d; da.N = h; da.bf16 = 1; da.mode = 3; da.rows_cap = P.rows;
+    da.err = err;
+    MOE_TRY(run_ffn(P, cfg, da, s));
+    FfnParams dxe{};
+    dxe.A = dz; dxe.W = w1T; dxe.offset = off; dxe.row_token = rtok; dxe.row_gate = rgate; dxe.out = dx;
+    dxe.E = E; dxe.K = h; dxe.N = d; dxe.bf16 = 1; dxe.mode = 5; dxe.rows_cap = P.rows; dxe.err = err;
+    MOE_TRY(run_ffn(P, cfg, dxe, s));
+    // 4. data gradient through the gate: dx += dS [W_g ; W_n]
+    int* rows_id = at<int>(ws, B.o_rows);
+    int* off2 = at<int>(ws, B.o_off2);
+    void* wcatT = at<void>(ws, B.o_wcatT);
+    MOE_TRY(launch(s, [&] { return launch_iota_rows(rows_id, T, B.Tp, off2, s); }));
+    MOE_TRY(launch(s, [&] {
+        return launch_gate_weights_t(w_gate, P.gate == MOE_GATE_NOISY ? w_noise : nullptr, E, d, B.NpP, wcatT, s);
+    }));
+    FfnParams dxg{};
+    dxg.A = dS; dxg.W = wcatT; dxg.offset = off2; dxg.row_token = rows_id; dxg.out = dx;
+    dxg.E = 1; dxg.K = B.NpP; dxg.N = d; dxg.bf16 = 1; dxg.mode = 5; dxg.rows_cap = B.Tp; dxg.err = err;
+    MOE_TRY(run_ffn(P, cfg, dxg, s));
+    // 5. weight gradients, contracting over each expert's rows: dW2 = dY^T H, dW1 = dZ^T X_d
+    void* xdT = at<void>(ws, B.o_xdT);
+    void* hT = at<void>(ws, B.o_hT);
+    void* dyT = at<void>(ws, B.o_dyT);
+    void* dzT = at<void>(ws, B.o_dzT);
+    MOE_TRY(launch(s, [&] { return launch_transpose(dy, dyT, 1, R, d, B.Rp, rtok, s); }));
+    MOE_TRY(launch(s, [&] { return launch_transpose(hb, hT, 1, R, h, B.Rp, rtok, s); }));
+    MOE_TRY(launch(s, [&] { return launch_transpose(dz, dzT, 1, R, h, B.Rp, rtok, s); }));
+    MOE_TRY(launch(s, [&] { return launch_transpose(xd, xdT, 1, R, d, B.Rp, rtok, s); }));
+    MOE_TRY(launch(s, [&] {
+        return launch_wgrad_tc(WgradParams{dyT, hT, off, dw2, E, d, h, (int64_t)B.Rp, err}, s);
+    }));
+    MOE_TRY(launch(s, [&] {
+        return launch_wgrad_tc(WgradParams{dzT, xdT, off, dw1, E, h, d, (int64_t)B.Rp, err}, s);
+    }));
+    // 6. gate weight gradients: [dW_g ; dW_n] = dS^T x, contracting over the tokens
+    void* dST = at<void>(ws, B.o_dST);
+    void* xT = at<void>(ws, B.o_xT);
+    float* dwcat = at<float>(ws, B.o_dwcat);
+    MOE_TRY(launch(s, [&] { return launch_transpose(dS, dST, 1, B.Tp, B.NpP, B.Tp, nullptr, s); }));
+    MOE_TRY(launch(s, [&] { return launch_transpose(x, xT, 1, T, d, B.Tp, nullptr, s); }));
+    MOE_TRY(launch(s, [&] {
+        return launch_wgrad_tc(WgradParams{dST, xT, off2, dwcat, 1, B.Np, d, (int64_t)B.Tp, err}, s);
+    }));
+    if (cudaMemcpyAsync(dw_gate, dwcat, (size_t)E * d * 4, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (P.gate == MOE_GATE_NOISY &&
+        cudaMemcpyAsync(dw_noise, dwcat + (size_t)E * d, (size_t)E * d * 4, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    // 7. bias gradients: column sums over each expert's rows
+    if (db2) MOE_TRY(launch(s, [&] { return launch_segment_colsum(dy, off, rtok, E, d, db2, s); }));
+    if (db1) MOE_TRY(launch(s, [&] { return launch_segment_colsum(dz, off, rtok, E, h, db1, s); }));
     return MOE_OK;
 }
 
@@ -569,6 +738,22 @@ moe_status moe_forward_fp8(const moe_config* cfg, const void* x, const void* w_g
     if (!w1_scale || !w2_scale) return MOE_ERR_INVALID_ARG;
     return forward_impl(cfg, x, w_gate, w_noise, noise_eps, proj, expert_emb, w1_q, w1_scale, b1, w2_q, w2_scale, b2,
                         out, expert_count, workspace, workspace_bytes, stream);
+}
+
+size_t moe_backward_workspace_size(const moe_config* cfg) {
+    Plan P;
+    BwdPlan B;
+    if (make_plan(cfg, &P) != MOE_OK || make_bwd_plan(P, cfg, &B) != MOE_OK) return 0;
+    return B.total;
+}
+
+moe_status moe_backward(const moe_config* cfg, const void* x, const void* w_gate, const void* w_noise,
+                        const float* noise_eps, const void* w1, const void* b1, const void* w2, const void* b2,
+                        const float* dout, float* dx, float* dw_gate, float* dw_noise, float* dw1, float* db1,
+                        float* dw2, float* db2, void* workspace, size_t workspace_bytes, void* stream) {
+    NvtxRange nvtx_("moe_backward");
+    return backward_impl(cfg, x, w_gate, w_noise, noise_eps, w1, b1, w2, b2, dout, dx, dw_gate, dw_noise, dw1, db1,
+                         dw2, db2, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
 }
 
 moe_status moe_router_stats(const moe_config* cfg, const int32_t* topk_idx, const float* topk_gate,

@@ -152,6 +152,21 @@ __device__ __forceinline__ float gelu_erf(float z) {
     return 0.5f * z * (z >= 0.0f ? 2.0f - q : q);
 }
 
+// GELU'(z) = Phi(z) + z phi(z) (the derivative of the erf-form GELU), with Phi from the same
+// Abramowitz & Stegun 7.1.26 erf as gelu_erf; phi(z) = e^(-z^2/2) / sqrt(2 pi) reuses its exponential.
+__device__ __forceinline__ float gelu_grad(float z) {
+    const float x = fabsf(z) * 0.70710678118654752f;
+    float t;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(t) : "f"(fmaf(0.3275911f, x, 1.0f)));
+    float p = fmaf(t, 1.061405429f, -1.453152027f);
+    p = fmaf(t, p, 1.421413741f);
+    p = fmaf(t, p, -0.284496736f);
+    p = fmaf(t, p, 0.254829592f);
+    const float ex = __expf(-x * x);  // e^(-z^2 / 2)
+    const float q = p * t * ex;
+    return 0.5f * (z >= 0.0f ? 2.0f - q : q) + z * ex * 0.3989422804014327f;
+}
+
 // expert owning dispatched row r: the e with off[e] <= r < off[e+1] (off ascending, E+1 entries)
 __device__ __forceinline__ int expert_of_row(const int* off, int E, int r) {
     int lo = 0, hi = E;  // invariant: off[lo] <= r < off[hi]

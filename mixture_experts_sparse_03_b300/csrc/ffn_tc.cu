@@ -55,6 +55,8 @@ struct TcArgs {
     int* err;
     const float* scale;  // block-FP8 weights: fp32 scale per 128 x 128 block, [E, N/128, K/128]
     int stages;          // SM-pair kernel: depth of its TMA ring
+    bf16_t* aux;         // modes 3 / 4: the pre-activations Z [rows, N] (read / written)
+    int M;               // weight-gradient kernel: rows of each expert's output [M, N]
 };
 
 using namespace tc;
@@ -64,7 +66,12 @@ using namespace tc;
 //   mode 0: + b1, GELU(erf), round to bf16, store the hidden row
 //   mode 1: + b2, store fp32 y
 //   mode 2: + b2, times the row's gate, fp32 atomic add into out[tok] (fused combine)
+//   mode 3: (backward) times GELU'(Z[r]) with the saved pre-activations, store bf16 dZ
+//   mode 4: + b1, store bf16 Z and bf16 GELU(Z) (the forward that the backward recomputes)
+//   mode 5: (backward) fp32 atomic add into out[tok] (gate 1, no bias: the gather-reduce of dx)
 // All lanes of the warp call this (tcgen05.ld is warp-wide); rows with tok < 0 store nothing.
+// kBwd: the backward's modes (3 - 5) are compiled in; the forward kernels leave them out (registers)
+template <bool kBwd = false>
 __device__ __forceinline__ void epilogue_cols(const TcArgs& a, uint32_t taddr, int r, int tok, float g,
                                               const float* sbias, int n0, int c_begin, int c_end) {
     for (int c0 = c_begin; c0 < c_end; c0 += 32) {
@@ -101,6 +108,38 @@ __device__ __forceinline__ void epilogue_cols(const TcArgs& a, uint32_t taddr, i
             float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.C) + (size_t)r * a.N + n);
 #pragma unroll
             for (int j = 0; j < 32; j += 4) __stcs(dst + j / 4, make_float4(f[j], f[j + 1], f[j + 2], f[j + 3]));
+        } else if (kBwd && a.mode == 3) {
+            const uint4* zs = reinterpret_cast<const uint4*>(a.aux + (size_t)r * a.N + n);
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<bf16_t*>(a.C) + (size_t)r * a.N + n);
+#pragma unroll
+            for (int j = 0; j < 32; j += 8) {
+                const uint4 zz = __ldg(zs + j / 8);
+                const uint32_t zw[4] = {zz.x, zz.y, zz.z, zz.w};
+                uint32_t o[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    o[i] = pack_bf16x2(f[j + 2 * i] * gelu_grad(bf16_lo(zw[i])),
+                                       f[j + 2 * i + 1] * gelu_grad(bf16_hi(zw[i])));
+                dst[j / 8] = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+        } else if (kBwd && a.mode == 4) {
+            uint4* zd = reinterpret_cast<uint4*>(a.aux + (size_t)r * a.N + n);
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<bf16_t*>(a.C) + (size_t)r * a.N + n);
+#pragma unroll
+            for (int j = 0; j < 32; j += 8) {
+                uint32_t zw[4], hw[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    zw[i] = pack_bf16x2(f[j + 2 * i], f[j + 2 * i + 1]);
+                    hw[i] = pack_bf16x2(gelu_erf(f[j + 2 * i]), gelu_erf(f[j + 2 * i + 1]));
+                }
+                zd[j / 8] = make_uint4(zw[0], zw[1], zw[2], zw[3]);
+                dst[j / 8] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            }
+        } else if (kBwd && a.mode == 5) {
+            float4* dst = reinterpret_cast<float4*>(a.out + (size_t)tok * a.N + n);
+#pragma unroll
+            for (int j = 0; j < 32; j += 4) atomicAdd(dst + j / 4, make_float4(f[j], f[j + 1], f[j + 2], f[j + 3]));
         } else {
             float4* dst = reinterpret_cast<float4*>(a.out + (size_t)tok * a.N + n);
 #pragma unroll
@@ -129,6 +168,7 @@ __device__ __forceinline__ const float* stage_bias(const TcArgs& a, float* wbias
     return wbias;
 }
 
+template <bool kBwd>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const TcArgs a) {
     extern __shared__ uint8_t smem_raw[];
@@ -270,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             fence_after();
-            epilogue_cols(a, tmem_base + lane_base + (uint32_t)(acc * kBN), r, tok, g, sb, n0, 0, kBN);
+            epilogue_cols<kBwd>(a, tmem_base + lane_base + (uint32_t)(acc * kBN), r, tok, g, sb, n0, 0, kBN);
             fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(TEMPTY + acc));
@@ -474,6 +514,171 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     cluster_sync();  // both CTAs are done with the pair's TMEM and barriers
     fence_after();
     if (warp == 1) tmem_free_pair(tmem_base, kTmemCols);
+}
+
+// ---- weight gradients: GEMMs grouped along K ------------------------------------------------------------
+// dW[e] [M, N] = sum over the dispatched rows r of expert e of A[r][m] B[r][n], i.e. the contraction runs over
+// the expert's own row segment [off[e], off[e+1]).  Both operands arrive transposed, K-major: At [M, rows]
+// and Bt [N, rows] (2-D maps), so the MMAs are those of gemm_tc_kernel; padding rows are zero in both.
+// Tiles (e, m-tile, n-tile) are dealt to one CTA per SM; a tile of an expert without rows stores zeros.
+// The epilogue stores fp32 rows m < M of dW[e] (mode 1 of epilogue_cols on the row e * M + m).
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                      const TcArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint8_t* sA = base;
+    uint8_t* sB = base + kStages * kABytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sB + kStages * kBBytes);
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 5);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+    int* s_off = reinterpret_cast<int*>(tmem_holder + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    auto bar = [&](int i) { return smem_u32(bars + i); };
+    const int FULL = 0, EMPTY = kStages, TFULL = 2 * kStages, TEMPTY = 2 * kStages + 2, LAST = 2 * kStages + 4;
+
+    if (threadIdx.x == 0) {
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
+        *abort_flag = 0;
+        for (int st = 0; st < kStages; ++st) {
+            mbar_init(bar(FULL + st), 1);
+            mbar_init(bar(EMPTY + st), 1);
+        }
+        for (int st = 0; st < 2; ++st) {
+            mbar_init(bar(TFULL + st), 1);
+            mbar_init(bar(TEMPTY + st), 4);
+        }
+        mbar_init(bar(LAST), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) tmem_alloc(smem_u32(tmem_holder), kTmemCols);
+    pdl_wait();
+    pdl_trigger();
+    for (int i = threadIdx.x; i <= a.E; i += kThreads) s_off[i] = a.offset[i];
+    fence_before();
+    __syncthreads();
+    fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    const int m_tiles = (a.M + kBM - 1) / kBM;
+    const int n_tiles = (a.N + kBN - 1) / kBN;
+    const int per_e = m_tiles * n_tiles;
+    const int num_tiles = a.E * per_e;
+    auto decode = [&](int tile, int& e, int& m0, int& n0, int& k0, int& nk) {
+        e = tile / per_e;
+        const int rem = tile - e * per_e;
+        m0 = (rem / n_tiles) * kBM;
+        n0 = (rem % n_tiles) * kBN;
+        k0 = s_off[e];
+        nk = (s_off[e + 1] - k0) / kBK;
+    };
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t issued_phase[kStages];
+            bool issued[kStages];
+            for (int st = 0; st < kStages; ++st) { issued[st] = false; issued_phase[st] = 0; }
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+                int e, m0, n0, k0, nk;
+                decode(tile, e, m0, n0, k0, nk);
+                for (int kb = 0; kb < nk; ++kb) {
+                    if (!mbar_wait(bar(EMPTY + stage), phase ^ 1u, abort_flag)) { ok = false; break; }
+                    mbar_expect_tx(bar(FULL + stage), kStageBytes);
+                    tma_load_2d(smem_u32(sA + stage * kABytes), &tmA, bar(FULL + stage), k0 + kb * kBK, m0);
+                    tma_load_2d(smem_u32(sB + stage * kBBytes), &tmB, bar(FULL + stage), k0 + kb * kBK, n0);
+                    issued[stage] = true;
+                    issued_phase[stage] = phase;
+                    if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                }
+            }
+            if (!ok) {
+                record_error(a.err, kErrTimeout, kWhereGemmProducer);
+                *abort_flag = 1;
+                for (int st = 0; st < kStages; ++st)
+                    if (issued[st]) mbar_wait_bounded(bar(FULL + st), issued_phase[st]);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16(kBM, kBN);
+            int stage = 0;
+            uint32_t phase = 0;
+            int local = 0;
+            bool ok = true, any = false;
+            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x, ++local) {
+                int e, m0, n0, k0, nk;
+                decode(tile, e, m0, n0, k0, nk);
+                const int acc = local & 1;
+                const uint32_t acc_phase = (local >> 1) & 1;
+                if (!mbar_wait(bar(TEMPTY + acc), acc_phase ^ 1u, abort_flag)) { ok = false; break; }
+                fence_after();
+                const uint32_t d_tmem = tmem_base + acc * kBN;
+                for (int kb = 0; kb < nk; ++kb) {
+                    if (!mbar_wait(bar(FULL + stage), phase, abort_flag)) { ok = false; break; }
+                    fence_after();
+                    const uint64_t ad = smem_desc_sw128(smem_u32(sA + stage * kABytes));
+                    const uint64_t bd = smem_desc_sw128(smem_u32(sB + stage * kBBytes));
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk)
+                        mma_bf16(d_tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc, (kb | kk) != 0);
+                    any = true;
+                    commit(bar(EMPTY + stage));
+                    if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+                if (nk > 0) commit(bar(TFULL + acc));
+                else mbar_arrive(bar(TFULL + acc));  // nothing to wait for: the epilogue stores zeros
+            }
+            if (!ok) {
+                record_error(a.err, kErrTimeout, kWhereGemmMma);
+                *abort_flag = 1;
+            }
+            if (any) {
+                commit(bar(LAST));
+                mbar_wait_bounded(bar(LAST), 0);
+            }
+        }
+    } else {
+        const int q = warp & 3;
+        const int row = q * 32 + lane;
+        const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+        int local = 0;
+        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
+            int e, m0, n0, k0, nk;
+            decode(tile, e, m0, n0, k0, nk);
+            const int acc = local & 1;
+            const uint32_t acc_phase = (local >> 1) & 1;
+            const int m = m0 + row;
+            const bool ok = __all_sync(0xffffffffu, mbar_wait(bar(TFULL + acc), acc_phase, abort_flag));
+            if (!ok) {
+                if (lane == 0) {
+                    record_error(a.err, kErrTimeout, kWhereGemmEpilogue);
+                    *abort_flag = 1;
+                }
+                break;
+            }
+            fence_after();
+            if (nk > 0) {
+                epilogue_cols(a, tmem_base + lane_base + (uint32_t)(acc * kBN), e * a.M + m, m < a.M ? 0 : -1, 0.f,
+                              nullptr, n0, 0, kBN);
+            } else if (m < a.M) {  // an expert without rows: its gradient is zero
+                float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.C) + ((size_t)e * a.M + m) * a.N + n0);
+                for (int c = 0; c < kBN && n0 + c < a.N; c += 4) dst[c / 4] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(TEMPTY + acc));
+        }
+    }
+    fence_before();
+    __syncthreads();
+    fence_after();
+    if (warp == 1) tmem_free(tmem_base, kTmemCols);
 }
 
 // ---- the single-SM GEMM with block-FP8 weights ----------------------------------------------------
@@ -834,6 +1039,29 @@ int pair_stages(int E, bool bias) {
     return !bias && ffn_tc_pair_smem_bytes(E, false, k2StagesNoBias) <= 227 * 1024 ? k2StagesNoBias : k2Stages;
 }
 
+cudaError_t launch_wgrad_tc(const WgradParams& P, cudaStream_t s) {
+    if (P.M <= 0 || P.N <= 0 || P.E <= 0) return cudaSuccess;
+    CUtensorMap ma, mb;
+    if (!tma_map_bf16(P.At, (uint64_t)P.rows, (uint64_t)P.M, 0, kBM, &ma)) return cudaErrorInvalidValue;
+    if (!tma_map_bf16(P.Bt, (uint64_t)P.rows, (uint64_t)P.N, 0, kBN, &mb)) return cudaErrorInvalidValue;
+    TcArgs a{};
+    a.offset = P.offset;
+    a.C = P.dW;
+    a.E = P.E;
+    a.K = 0;
+    a.N = P.N;
+    a.M = P.M;
+    a.mode = 1;
+    a.err = P.err;
+    const size_t smem = 1024 + (size_t)kStages * kStageBytes + (2 * kStages + 5) * 8 + 16 + 4 * (size_t)(P.E + 1);
+    cudaError_t e = cudaFuncSetAttribute(gemm_wgrad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const int64_t tiles = (int64_t)P.E * ((P.M + kBM - 1) / kBM) * ((P.N + kBN - 1) / kBN);
+    int grid = device_sm_count();
+    if (tiles < grid) grid = (int)tiles;
+    return launch_pdl(gemm_wgrad_kernel, dim3(grid), dim3(kThreads), smem, s, ma, mb, a);
+}
+
 size_t ffn_fp8_smem_bytes(int E) {
     return 1024 + (size_t)kF8Stages * kF8StageBytes + (size_t)kF8Bufs * kBBytes +
            (2 * kF8Stages + 2 * kF8Bufs + 5) * 8 + 16 + 4 * (size_t)(E + 1) + kBiasSmem;
@@ -848,7 +1076,7 @@ cudaError_t launch_ffn_tc(const FfnParams& P, cudaStream_t s) {
         if (P.K % kF8Block || P.N % kF8Block) return cudaErrorInvalidValue;
         if (!tma_map_kind(P.W, (uint64_t)P.K, (uint64_t)P.N, (uint64_t)P.E, kBN, 1, &mb)) return cudaErrorInvalidValue;
         TcArgs a8{P.offset, P.row_token, P.row_gate, static_cast<const bf16_t*>(P.bias), P.C, P.out,
-                  P.E, P.K, P.N, P.mode, P.err, P.w_scale, kF8Stages};
+                  P.E, P.K, P.N, P.mode, P.err, P.w_scale, kF8Stages, static_cast<bf16_t*>(P.aux), 0};
         const size_t smem8 = ffn_fp8_smem_bytes(P.E);
         cudaError_t e8 = cudaFuncSetAttribute(gemm_fp8w_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem8);
         if (e8 != cudaSuccess) return e8;
@@ -872,6 +1100,8 @@ cudaError_t launch_ffn_tc(const FfnParams& P, cudaStream_t s) {
     a.err = P.err;
     a.scale = nullptr;
     a.stages = kStages;
+    a.aux = static_cast<bf16_t*>(P.aux);
+    a.M = 0;
     if (P.pair) {
         // pairs of SMs: B boxes of 128 weight rows (half of a 256-wide tile), grid = 2 x the clusters that fit
         CUtensorMap mb2;
@@ -887,12 +1117,14 @@ cudaError_t launch_ffn_tc(const FfnParams& P, cudaStream_t s) {
             return launch_pdl(gemm_tc_pair_kernel, dim3(2 * pairs), dim3(kThreads), smem2, s, ma, mb2, a);
     }
     const size_t smem = ffn_tc_smem_bytes(P.E);
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    const bool bwd = P.mode >= 3;
+    auto kern = bwd ? gemm_tc_kernel<true> : gemm_tc_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int64_t max_tiles = (P.rows_cap / kBM) * (int64_t)((P.N + kBN - 1) / kBN);
     int grid = device_sm_count();
     if (max_tiles < grid) grid = (int)(max_tiles > 0 ? max_tiles : 1);
-    return launch_pdl(gemm_tc_kernel, dim3(grid), dim3(kThreads), smem, s, ma, mb, a);
+    return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, s, ma, mb, a);
 }
 
 }  // namespace moe

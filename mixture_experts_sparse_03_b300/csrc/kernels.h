@@ -109,7 +109,9 @@ cudaError_t launch_dispatch_gather(const void* x, int bf16, const int* topk_idx,
 
 // ---- expert FFN -------------------------------------------------------------------------------
 // mode: 0 = up projection (+b1, GELU, store hidden), 1 = down projection to y (fp32),
-//       2 = down projection with the combine fused (atomic fp32 add of gate * y into out)
+//       2 = down projection with the combine fused (atomic fp32 add of gate * y into out),
+//       3 = (backward) times GELU'(aux) into bf16, 4 = up projection storing Z (aux) and GELU(Z),
+//       5 = (backward) atomic fp32 add into out[row_token] with gate 1
 struct FfnParams {
     const void* A;            // [rows, K] dispatched activations (x_dispatched or hidden)
     const void* W;            // [E, N, K]
@@ -124,8 +126,21 @@ struct FfnParams {
     int64_t rows_cap;
     int* err;
     const float* w_scale;     // block-FP8 weights: W holds E4M3 codes, w_scale [E, N/128, K/128]; else nullptr
+    void* aux;                // modes 3 / 4 (backward): pre-activations Z [rows, N] bf16
 };
 size_t ffn_fp8_smem_bytes(int E);
+// weight gradients grouped along K (ffn_tc.cu): dW[e] [M, N] fp32 = sum over the rows r of expert e
+// (offset[e] <= r < offset[e+1], multiples of 128) of At[m][r] Bt[n][r]; At [M, rows], Bt [N, rows] bf16
+struct WgradParams {
+    const void* At;
+    const void* Bt;
+    const int* offset;  // [E+1]
+    float* dW;          // [E, M, N]
+    int E, M, N;
+    int64_t rows;       // columns of At and Bt (a multiple of 64)
+    int* err;
+};
+cudaError_t launch_wgrad_tc(const WgradParams& p, cudaStream_t s);
 cudaError_t launch_ffn_simt(const FfnParams& p, cudaStream_t s);
 cudaError_t launch_ffn_tc(const FfnParams& p, cudaStream_t s);  // bf16 only; tcgen05 + TMA
 
@@ -137,6 +152,25 @@ cudaError_t launch_router_stats(const int* topk_idx, const float* topk_gate, con
 cudaError_t launch_combine(const float* y, const int* slot, const int* offset, const int* topk_idx,
                            const float* topk_gate, int T, int k, int d, float* out, cudaStream_t s);
 cudaError_t launch_zero(float* p, size_t n, cudaStream_t s);
+
+// ---- backward (bwd.cu) ------------------------------------------------------------------------------
+// dst[b][c][r] = src[b][r][c] (bf16) for r < R, zero where row_mask[r] < 0 (if given) and for R <= r < Rp
+cudaError_t launch_transpose(const void* src, void* dst, int B, int R, int C, int Rp, const int* row_mask,
+                             cudaStream_t s);
+// dY[r] = row_gate[r] * dout[row_token[r]] in bf16 (zero for padding rows)
+cudaError_t launch_bwd_dy(const float* dout, const int* row_token, const float* row_gate, int rows, int d, void* dY,
+                          cudaStream_t s);
+// per token: the gates' and scores' gradient, dS [Tp, Np] bf16 = [ds | dn (noisy) | 0]
+cudaError_t launch_bwd_gate(const float* dout, const float* y, const int* topk_idx, const float* topk_gate,
+                            const int* slot, const int* offset, const float* logits, const float* eps, int T, int Tp,
+                            int d, int E, int k, int noisy, int norm_all, int Np, void* dS, cudaStream_t s);
+// db[e][c] = column sums of src [rows, C] (bf16) over expert e's real rows (row_token >= 0)
+cudaError_t launch_segment_colsum(const void* src, const int* offset, const int* row_token, int E, int C, float* db,
+                                  cudaStream_t s);
+// out [d][Np] = [W_g ; W_n ; 0]^T
+cudaError_t launch_gate_weights_t(const void* wg, const void* wn, int E, int d, int Np, void* out, cudaStream_t s);
+// rows[i] = i for i < T, -1 up to Tp; off2 = {0, Tp}
+cudaError_t launch_iota_rows(int* rows, int T, int Tp, int* off2, cudaStream_t s);
 
 // ---- configuration ------------------------------------------------------------------------------
 // The status the library's own planner gives a config (MOE_OK, MOE_ERR_INVALID_ARG or
