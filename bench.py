@@ -137,89 +137,6 @@ def job_throughput(world: int, steps: int, tokens: int, max_total_ms: float) -> 
 
 
 # ------------------------------------------------------------------------------------------ clocks
-class NvmlSampler:
-    """Reads the SM clock, power and clock-event reasons through NVML every few milliseconds on a host
-    thread (read-only queries), so that a timed region of tens of milliseconds still gets many samples."""
-
-    REASONS = (("hw_slowdown", "nvmlClocksEventReasonHwSlowdown"),
-               ("hw_thermal_slowdown", "nvmlClocksEventReasonHwThermalSlowdown"),
-               ("sw_thermal_slowdown", "nvmlClocksEventReasonSwThermalSlowdown"),
-               ("sw_power_cap", "nvmlClocksEventReasonSwPowerCap"))
-
-    def __init__(self, device_index: int, period_s: float = 0.002):
-        import threading
-
-        self.period = period_s
-        self.samples = []
-        self.stop_flag = threading.Event()
-        self.thread = None
-        self.nv = None
-        self.error = None
-        try:
-            import pynvml as nv
-
-            nv.nvmlInit()
-            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
-            uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
-            try:
-                self.h = nv.nvmlDeviceGetHandleByUUID(uuid)
-            except Exception:  # noqa: BLE001 -- fall back to the index NVML and CUDA usually share
-                self.h = nv.nvmlDeviceGetHandleByIndex(device_index)
-            self.nv = nv
-        except Exception as e:  # noqa: BLE001
-            self.error = "init: %s" % e
-            self.nv = None
-
-    def _run(self):
-        nv = self.nv
-        reasons_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
-            getattr(nv, "nvmlDeviceGetCurrentClocksThrottleReasons", None)
-        while not self.stop_flag.is_set():
-            try:
-                sm = nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM)
-            except Exception as e:  # noqa: BLE001 -- reported, never fatal
-                self.error = "clock: %s" % e
-                return
-            try:
-                pw = nv.nvmlDeviceGetPowerUsage(self.h) / 1000.0
-            except Exception:  # noqa: BLE001
-                pw = float("nan")
-            try:
-                rs = reasons_fn(self.h) if reasons_fn else 0
-            except Exception:  # noqa: BLE001
-                rs = 0
-            self.samples.append((sm, pw, rs))
-            time.sleep(self.period)
-
-    def start(self):
-        import threading
-
-        if self.nv is None:
-            return
-        self.thread = threading.Thread(target=self._run, daemon=True)
-        self.thread.start()
-
-    def stop(self):
-        if self.thread is None:
-            return {"error": self.error} if self.error else None
-        self.stop_flag.set()
-        self.thread.join(timeout=2)
-        if not self.samples:
-            return {"error": self.error or "no samples"}
-        nv = self.nv
-        sm = [s[0] for s in self.samples]
-        reasons = sorted({n for n, attr in self.REASONS for s in self.samples if s[2] & getattr(nv, attr, 0)})
-        try:
-            mx = nv.nvmlDeviceGetMaxClockInfo(self.h, nv.NVML_CLOCK_SM)
-        except Exception:
-            mx = max(sm)
-        return {"sm_mhz": statistics.median(sm), "sm_mhz_min": min(sm), "sm_max_mhz": mx,
-                "power_w_max": max(s[1] for s in self.samples), "reasons": reasons, "samples": len(sm),
-                "period_ms": self.period * 1e3}
-
-
-
-
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -233,7 +150,8 @@ class ClockSampler:
             sel = ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
         except Exception:
             sel = []
-        self.cmd = ["nvidia-smi", *sel, "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits", "-lms", "100"]
+        # a 20 ms period: a timed region of a few tens of milliseconds still gets a handful of samples
+        self.cmd = ["nvidia-smi", *sel, "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits", "-lms", "20"]
 
     def start(self):
         try:
@@ -543,8 +461,6 @@ def measure(wl, args, dev, stream, flush, world):
     stream.synchronize()
     sampler = ClockSampler(dev.index)
     sampler.start()
-    fine = NvmlSampler(dev.index)
-    fine.start()
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
@@ -558,11 +474,6 @@ def measure(wl, args, dev, stream, flush, world):
     if world > 1:
         torch.distributed.barrier()
     clocks = sampler.stop()
-    nvml = fine.stop()
-    if clocks is not None and nvml is not None:
-        clocks["nvml_2ms"] = nvml
-    elif nvml is not None:
-        clocks = dict(nvml, source="nvml")
     times = [a.elapsed_time(z) for a, z in evs]  # ms
     total_ms = max_over_ranks(sum(times), dev)
 

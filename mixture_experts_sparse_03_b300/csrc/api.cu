@@ -287,8 +287,9 @@ FfnParams ffn_params(const Plan& P, int mode, const void* A, const void* W, cons
     f.C = C;
     f.out = out;
     f.E = P.E;
-    f.K = mode == 0 ? P.d : P.h;
-    f.N = mode == 0 ? P.h : P.d;
+    const bool up_proj = mode == 0 || mode == 4;  // x_d [rows, d] -> [rows, h]
+    f.K = up_proj ? P.d : P.h;
+    f.N = up_proj ? P.h : P.d;
     f.bf16 = P.bf16;
     f.mode = mode;
     f.rows_cap = P.rows;

@@ -24,6 +24,8 @@ CASES = [
     small_workload(T=200, d=192, h=128, E=8, k=2, gate="noisy", capacity_factor=0.7, bias="none"),
     small_workload(T=150, d=128, h=128, E=5, k=3, capacity_factor=0.8, priority="rank", bias="normal"),
     small_workload(T=512, d=256, h=512, E=8, k=2, gate="noisy", capacity_factor=1.2, bias="normal"),
+    # several 128-row tiles per expert and several 256-wide column tiles in every GEMM
+    small_workload(T=1024, d=256, h=1024, E=4, k=2, capacity_factor=1.1, bias="none"),
 ]
 
 
