@@ -507,6 +507,90 @@ def measure(wl, args, dev, stream, flush, world):
     return res, L
 
 
+BWD_TAIL = ["fwd_up_keep_z", "fwd_down_y", "logits_gemm", "bwd_dy", "bwd_gate_grad", "transpose_w2", "transpose_w1",
+            "bwd_dz_gemm", "bwd_dx_gemm", "iota_rows", "gate_weights_t", "bwd_dx_gate_gemm", "transpose_dy",
+            "transpose_h", "transpose_dz", "transpose_xd", "wgrad_w2", "wgrad_w1", "transpose_ds", "transpose_x",
+            "wgrad_gate", "colsum_db2", "colsum_db1"]
+
+
+def backward_timing(L, flush, steps):
+    """moe_backward (forward recomputed, then every gradient) on the layer's inputs with a seeded dout:
+    graph-replayed calls, L2 flushed before each, event-timed; the per-kernel split from a graph with
+    event-record nodes.  Reports ms per call and the tensor-core work of its expert GEMMs (six of them:
+    the recomputed up and down projections, dZ, dX and the two weight gradients, each 2 kept-pairs d h)."""
+    b, wl, dev, stream, tg = L.b, L.wl, L.dev, L.stream, L.tg
+    n = b.moe_backward_workspace_size(L.cfg)
+    if n == 0 or tg.get("w1_scale") is not None:
+        return None
+    ws = torch.empty(n, dtype=torch.uint8, device=dev)
+    T, d, h, E = wl.T, wl.d, wl.h, wl.E
+    gen = torch.Generator(device="cpu").manual_seed(wl.seed + 7)
+    dout = torch.randn(T, d, generator=gen).to(dev)
+    z = lambda *sh: torch.empty(sh, dtype=torch.float32, device=dev)  # noqa: E731
+    g = dict(dx=z(T, d), dw_gate=z(E, d), dw_noise=z(E, d) if wl.gate == "noisy" else None, dw1=z(E, h, d),
+             db1=z(E, h), dw2=z(E, d, h), db2=z(E, d))
+
+    def call():
+        b.check(b.moe_backward(L.cfg, tg["x"], tg.get("w_gate"), tg.get("w_noise"), tg.get("eps"), tg["w1"], tg.get("b1"),
+                               tg["w2"], tg.get("b2"), dout, g["dx"], g["dw_gate"], g["dw_noise"], g["dw1"], g["db1"],
+                               g["dw2"], g["db2"], ws, n, stream), "moe_backward")
+
+    with torch.cuda.stream(stream):
+        call()
+    stream.synchronize()
+    cap = [torch.cuda.Event(enable_timing=True) for _ in range(64)]
+    for e in cap:
+        e.record(stream)
+    stream.synchronize()
+    with torch.cuda.stream(stream):
+        keep = b.moe_trace_events(cap, len(cap))
+        call()
+        launches = b.moe_trace_count() - 1
+        b.moe_trace_events(None, 0)
+    stream.synchronize()
+    del keep
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        call()
+    times = []
+    with torch.cuda.stream(stream):
+        for i in range(3 + steps):
+            flush.fill_(1)
+            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a0.record(stream)
+            graph.replay()
+            a1.record(stream)
+            a1.synchronize()
+            if i >= 3:
+                times.append(a0.elapsed_time(a1))
+    st, info = b.moe_device_status(ws, n, stream)
+    b.check(st, "device status after moe_backward")
+    tev = cap[:launches + 1]
+    tgraph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(tgraph, stream=stream):
+        keep = b.moe_trace_events(tev, len(tev))
+        call()
+        b.moe_trace_events(None, 0)
+    per = [[] for _ in range(launches)]
+    with torch.cuda.stream(stream):
+        for i in range(5):
+            flush.fill_(1)
+            tgraph.replay()
+            stream.synchronize()
+            for j in range(launches):
+                per[j].append(tev[j].elapsed_time(tev[j + 1]))
+    route = launches - len(BWD_TAIL)
+    names = L.names[:route] + BWD_TAIL if route >= 0 else ["k%d" % j for j in range(launches)]
+    kern = {names[j]: statistics.median(per[j]) for j in range(launches)}
+    C = b.moe_capacity(L.cfg)
+    kept = int(np.minimum(L.count.cpu().numpy(), min(C, wl.T)).sum())
+    flops = 6 * 2.0 * kept * d * h
+    ms = statistics.median(times)
+    return {"ms_per_call": ms, "launches": launches, "expert_gemm_tflop": flops / 1e12,
+            "tflops_whole_call": flops / (ms * 1e-3) / 1e12, "kernel_ms": kern,
+            "timing": "CUDA graph replay, L2 flushed before each call; kernel_ms from event-record nodes"}
+
+
 def router_stats_timing(L, stream):
     """moe_router_stats on the layer's routing and dispatch: 20 calls captured in one CUDA graph, the
     replay event-timed, per call."""
@@ -655,6 +739,7 @@ def run_ours(args, rank, world, local):
 
     res, L = measure(wl, args, dev, stream, flush, world)
     router_stats = router_stats_timing(L, stream)
+    backward = backward_timing(L, flush, min(args.steps, 10))
     e2e_value, h2d, d2h = e2e_timing(L, flush, args.steps, world)
 
     cpu = None
@@ -693,6 +778,7 @@ def run_ours(args, rank, world, local):
                     "pipelined": "2 buffer sets; H2D, compute and D2H on three streams"},
             "gpu_launches": res["gpu_launches"],
             "router_stats": router_stats,
+            "backward": backward,
             "clocks": res["clocks"],
             "workloads": others,
         }

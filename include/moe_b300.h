@@ -117,6 +117,11 @@ typedef struct moe_config {
  * choices never take a slot from another token's first choice.  It changes which pairs overflow, not
  * how a kept pair is computed.  Applies to moe_forward, moe_dispatch and moe_dispatch_static_scratch. */
 #define MOE_FLAG_RANK_MAJOR      16
+/* Router statistics fused into the forward: with MOE_FLAG_ROUTER_STATS, moe_forward / moe_forward_fp8
+ * also compute what moe_router_stats computes (expert importance, the importance and load-balance losses,
+ * the dropped pairs) inside their dispatch kernel -- no extra kernel launch -- and keep them in the
+ * workspace until the next call; moe_router_stats_result() copies them out. */
+#define MOE_FLAG_ROUTER_STATS    32
 
 /* ---- sizes ------------------------------------------------------------------------------------ */
 /* Per-expert capacity C the dispatch step enforces, or -1 if the config is invalid. */
@@ -269,6 +274,13 @@ MOE_API moe_status moe_combine(const moe_config* cfg, const float* y_dispatched,
 MOE_API moe_status moe_router_stats(const moe_config* cfg, const int32_t* topk_idx, const float* topk_gate,
                             const int32_t* slot, float* importance, float* losses, int64_t* dropped,
                             void* workspace, size_t workspace_bytes, void* stream);
+
+/* The statistics of the last moe_forward / moe_forward_fp8 made with MOE_FLAG_ROUTER_STATS on this
+ * workspace (same definitions and exact fixed-point sums as moe_router_stats): enqueues device-to-device
+ * copies on `stream` into importance [E] fp32, losses [2] fp32 (importance loss, load-balance loss) and
+ * dropped (int64); any of the three may be NULL.  MOE_ERR_INVALID_ARG if cfg lacks the flag. */
+MOE_API moe_status moe_router_stats_result(const moe_config* cfg, const void* workspace, size_t workspace_bytes,
+                                   float* importance, float* losses, int64_t* dropped, void* stream);
 
 /* ---- whole layer ------------------------------------------------------------------------------ */
 /* moe_route -> moe_dispatch -> moe_expert_ffn (+ fused or separate combine) on `stream`, with every

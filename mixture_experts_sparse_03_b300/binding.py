@@ -31,6 +31,7 @@ FLAG_UNFUSED_COMBINE = 2
 FLAG_FFN_ONE_SM = 4
 FLAG_FFN_SM_PAIR = 8
 FLAG_RANK_MAJOR = 16
+FLAG_ROUTER_STATS = 32
 
 
 class MoEConfig(ctypes.Structure):
@@ -81,6 +82,7 @@ def _load():
         "moe_forward": ([C, P, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P], I32),
         "moe_expert_ffn_fp8": ([C, P, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P], I32),
         "moe_backward_workspace_size": ([C], SZ),
+        "moe_router_stats_result": ([C, P, SZ, P, P, P, P], I32),
         "moe_backward": ([C] + [P] * 17 + [SZ, P], I32),
         "moe_forward_fp8": ([C, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P], I32),
         "moe_device_status": ([P, SZ, ctypes.POINTER(I32), P], I32),
@@ -221,6 +223,11 @@ def moe_forward_fp8(cfg, x, w_gate, w_noise, noise_eps, proj, expert_emb, w1_q, 
     return lib.moe_forward_fp8(ctypes.byref(cfg), ptr(x), ptr(w_gate), ptr(w_noise), ptr(noise_eps), ptr(proj),
                                ptr(expert_emb), ptr(w1_q), ptr(w1_scale), ptr(b1), ptr(w2_q), ptr(w2_scale), ptr(b2),
                                ptr(out), ptr(expert_count), ptr(workspace), workspace_bytes, stream_handle(stream))
+
+
+def moe_router_stats_result(cfg, workspace, workspace_bytes, importance, losses, dropped, stream=None) -> int:
+    return lib.moe_router_stats_result(ctypes.byref(cfg), ptr(workspace), workspace_bytes, ptr(importance), ptr(losses),
+                                       ptr(dropped), stream_handle(stream))
 
 
 def moe_backward_workspace_size(cfg: MoEConfig) -> int:

@@ -24,13 +24,15 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 struct Plan {
     int T, d, h, E, k, C, Ceff, p, nblk, gate, norm, bf16, esize, fused;
     int rank_major;     // capacity slots in (rank, token) order
+    int stats;          // router statistics fused into the forward's gather
+    size_t o_fstats;    // their accumulators (in the zeroed header) and o_fstats_out their results
     int nblk_hist;      // blocks of the dispatch histogram: of 32 tokens, or of 32 (rank, token) pairs
     int N0, N1;         // gate logits from the first / second weight tensor
     int pair;           // expert GEMMs on pairs of SMs
     GateGemmPlan gg;    // tensor-core logits GEMM (bf16 layers)
     int64_t rows;
     size_t o_err, o_idx, o_gate, o_slot, o_hist, o_count, o_off, o_rtok, o_rgate, o_xd, o_h, o_y, o_part, o_xn2,
-        o_wn2, o_rq, o_cosv, o_stats, total;
+        o_wn2, o_rq, o_cosv, o_stats, o_fstats_out, total;
     size_t hdr_bytes;  // error word, its info, tickets and the cosine gate's expert flags: zeroed per call
 };
 
@@ -66,7 +68,7 @@ moe_status make_plan(const moe_config* c, Plan* pl) {
     if (P.gate < MOE_GATE_SOFTMAX || P.gate > MOE_GATE_COSINE) return MOE_ERR_INVALID_ARG;
     if (P.norm != MOE_GATE_NORM_ALL && P.norm != MOE_GATE_NORM_TOPK) return MOE_ERR_INVALID_ARG;
     if (c->flags & ~(MOE_FLAG_SIMT_FFN | MOE_FLAG_UNFUSED_COMBINE | MOE_FLAG_FFN_ONE_SM | MOE_FLAG_FFN_SM_PAIR |
-                     MOE_FLAG_RANK_MAJOR))
+                     MOE_FLAG_RANK_MAJOR | MOE_FLAG_ROUTER_STATS))
         return MOE_ERR_INVALID_ARG;
     if ((c->flags & MOE_FLAG_FFN_ONE_SM) && (c->flags & MOE_FLAG_FFN_SM_PAIR)) return MOE_ERR_INVALID_ARG;
     if (c->reserved != 0) return MOE_ERR_INVALID_ARG;
@@ -106,8 +108,13 @@ moe_status make_plan(const moe_config* c, Plan* pl) {
     auto take = [&](size_t bytes) { size_t r = o; o = up(o + bytes); return r; };
     const size_t tk = (size_t)P.T * P.k;
     const bool cos_tc = P.bf16 && P.gate == MOE_GATE_COSINE;  // cosine gates never take the fused path
-    P.hdr_bytes = 16 + (cos_tc ? 4 * (size_t)P.E : 0);
+    P.stats = (c->flags & MOE_FLAG_ROUTER_STATS) != 0;
+    const size_t cos_flags = cos_tc ? 4 * (size_t)P.E : 0;
+    // the fused statistics' accumulators (E + 1 uint64) and ticket sit in the header, zeroed per call
+    const size_t fstats_at = (16 + cos_flags + 7) / 8 * 8;
+    P.hdr_bytes = P.stats ? fstats_at + 8 * (size_t)(P.E + 1) + 8 : 16 + cos_flags;
     P.o_err = take(P.hdr_bytes);
+    P.o_fstats = P.o_err + fstats_at;
     P.o_idx = take(4 * tk);
     P.o_gate = take(4 * tk);
     P.o_slot = take(4 * tk);
@@ -126,6 +133,7 @@ moe_status make_plan(const moe_config* c, Plan* pl) {
     P.o_rq = take(P.bf16 && !P.gg.fused ? 4 * (size_t)P.T * kRescoreInts : 0);
     P.o_cosv = take(cos_tc ? 8 * (size_t)P.E * P.d : 0);
     P.o_stats = take(8 * (size_t)(P.E + 1) + 16);  // router statistics: expert sums, drop count, ticket
+    P.o_fstats_out = take(P.stats ? 4 * (size_t)P.E + 16 : 0);  // fused statistics: importance, losses, drops
     P.total = o;
     *pl = P;
     return MOE_OK;
@@ -359,7 +367,7 @@ namespace {
 // header must be zeroed first); `zero` [T, d] is cleared by the gather when not null
 moe_status route_and_dispatch(const Plan& P, const moe_config* cfg, const void* x, const void* w_gate,
                               const void* w_noise, const float* noise_eps, const void* proj, const void* expert_emb,
-                              int* count, float* zero, void* workspace, cudaStream_t s) {
+                              int* count, float* zero, void* workspace, cudaStream_t s, bool with_stats = true) {
     int32_t* idx = at<int32_t>(workspace, P.o_idx);
     float* gate = at<float>(workspace, P.o_gate);
     int* err = at<int>(workspace, P.o_err);
@@ -391,9 +399,17 @@ moe_status route_and_dispatch(const Plan& P, const moe_config* cfg, const void* 
             return launch_dispatch_rank(idx, P.T, P.k, P.E, hist, slot, err, err + 2, P.Ceff, count, off, rtok, rgate,
                                         1, s);
         }));
+    GatherStats st{};
+    if (P.stats && with_stats) {
+        st.acc = at<unsigned long long>(workspace, P.o_fstats);
+        st.ticket = reinterpret_cast<int*>(st.acc + P.E + 1);
+        st.importance = at<float>(workspace, P.o_fstats_out);
+        st.losses = st.importance + P.E;
+        st.dropped = reinterpret_cast<long long*>(at<char>(workspace, P.o_fstats_out) + 4 * (size_t)P.E + 8);
+    }
     return launch(s, [&] {
         return launch_dispatch_gather(x, P.bf16, idx, gate, hist, off, count, gather_scan, P.T, P.k, P.E, P.d, P.Ceff,
-                                      slot, rtok, rgate, xd, zero, P.rank_major, s);
+                                      slot, rtok, rgate, xd, zero, P.rank_major, st, s);
     });
 }
 
@@ -502,7 +518,7 @@ moe_status backward_impl(const moe_config* cfg, const void* x, const void* w_gat
     if (cudaMemsetAsync(dx, 0, (size_t)T * d * 4, s) != cudaSuccess) return MOE_ERR_CUDA;
     // 1. the forward again: routing and dispatch, Z and H = GELU(Z), y per dispatched row, and the gate logits
     MOE_TRY(route_and_dispatch(P, cfg, x, w_gate, w_noise, noise_eps, nullptr, nullptr, at<int>(ws, P.o_count),
-                               nullptr, ws, s));
+                               nullptr, ws, s, false));
     FfnParams up = ffn_params(P, 4, xd, w1, nullptr, b1, off, rtok, rgate, hb, nullptr, err);
     up.aux = at<void>(ws, B.o_z);
     MOE_TRY(run_ffn(P, cfg, up, s));
@@ -679,7 +695,7 @@ moe_status moe_dispatch(const moe_config* cfg, const void* x, const int32_t* top
     return launch(s, [&] {
         return launch_dispatch_gather(x, P.bf16, topk_idx, topk_gate, hist, expert_offset, nullptr, false, P.T, P.k,
                                       P.E, P.d, P.Ceff,
-                                      slot, row_token, row_gate, x_dispatched, nullptr, P.rank_major, s);
+                                      slot, row_token, row_gate, x_dispatched, nullptr, P.rank_major, GatherStats{}, s);
     });
 }
 
@@ -777,6 +793,23 @@ moe_status moe_router_stats(const moe_config* cfg, const int32_t* topk_idx, cons
         return launch_router_stats(topk_idx, topk_gate, slot, P.T, P.k, P.E, scratch, err, importance, losses,
                                    reinterpret_cast<long long*>(dropped), s);
     });
+}
+
+moe_status moe_router_stats_result(const moe_config* cfg, const void* workspace, size_t workspace_bytes,
+                                   float* importance, float* losses, int64_t* dropped, void* stream) {
+    Plan P;
+    MOE_TRY(make_plan(cfg, &P));
+    if (!P.stats) return MOE_ERR_INVALID_ARG;
+    MOE_TRY(check_ws(P, const_cast<void*>(workspace), workspace_bytes));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const char* res = static_cast<const char*>(workspace) + P.o_fstats_out;
+    if (importance && cudaMemcpyAsync(importance, res, 4 * (size_t)P.E, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (losses && cudaMemcpyAsync(losses, res + 4 * (size_t)P.E, 8, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (dropped && cudaMemcpyAsync(dropped, res + 4 * (size_t)P.E + 8, 8, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return MOE_OK;
 }
 
 moe_status moe_device_status(void* workspace, size_t workspace_bytes, int32_t* info, void* stream) {

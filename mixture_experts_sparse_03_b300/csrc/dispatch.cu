@@ -92,6 +92,74 @@ __global__ void __launch_bounds__(32 * kRankWarps) rank_kernel(const int* __rest
     }
 }
 
+// Router statistics fused into the gather (moe_forward with MOE_FLAG_ROUTER_STATS): each CTA adds its
+// pairs' gates -- every top-k gate, kept or dropped -- to the experts' 64-bit fixed-point sums (a gate is
+// a multiple of 2^-32 after rounding, so the sums are exact and independent of the order of the adds)
+// and its dropped pairs to a counter; the last CTA to finish (ticket) turns the sums into the importance
+// and the two losses, in fp64 in a fixed order, and resets the accumulators for the next call.
+__device__ __forceinline__ double block_sum_d256(double v, double* red) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    v = warp_sum_d(v);
+    __syncthreads();
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    double s = 0.0;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) s += red[w];
+    return s;
+}
+
+__device__ void fused_router_stats(const GatherStats& st, int E, int warp, int lane, int e, float gv, bool counted,
+                                   bool dropped) {
+    constexpr double kFix = 4294967296.0;  // 2^32
+    __shared__ int s_e[kGatherWarps];
+    __shared__ unsigned long long s_g[kGatherWarps];
+    __shared__ int s_drop[kGatherWarps];
+    __shared__ int s_last;
+    __shared__ double s_red[kGatherWarps];
+    if (lane == 0) {
+        s_e[warp] = counted ? e : -1;
+        s_g[warp] = counted ? (unsigned long long)llrint((double)gv * kFix) : 0ull;
+        s_drop[warp] = dropped ? 1 : 0;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int nd = 0;
+        for (int w = 0; w < kGatherWarps; ++w) {
+            nd += s_drop[w];
+            if (s_e[w] < 0) continue;
+            unsigned long long sum = s_g[w];
+            for (int v = w + 1; v < kGatherWarps; ++v)  // the CTA's pairs of the same expert, one add
+                if (s_e[v] == s_e[w]) { sum += s_g[v]; s_e[v] = -1; }
+            atomicAdd(st.acc + s_e[w], sum);
+        }
+        if (nd) atomicAdd(st.acc + E, (unsigned long long)nd);
+        __threadfence();
+        s_last = atomicAdd(st.ticket, 1) == (int)gridDim.x - 1;
+        __threadfence();
+    }
+    __syncthreads();
+    if (!s_last) return;
+    double s = 0.0;
+    for (int i = threadIdx.x; i < E; i += blockDim.x) s += (double)__ldcg(st.acc + i) / kFix;
+    const double mean = block_sum_d256(s, s_red) / (double)E;
+    double ss = 0.0;
+    for (int i = threadIdx.x; i < E; i += blockDim.x) {
+        const double v = (double)__ldcg(st.acc + i) / kFix;
+        st.importance[i] = (float)v;
+        ss += (mean - v) * (mean - v);
+    }
+    ss = block_sum_d256(ss, s_red);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        st.losses[0] = E > 1 ? (float)(0.1 * sqrt(ss / (double)(E - 1))) : __int_as_float(0x7fc00000);
+        st.losses[1] = (float)ss;
+        *st.dropped = (long long)__ldcg(st.acc + E);
+    }
+    __syncthreads();  // every thread has read the sums
+    for (int i = threadIdx.x; i <= E; i += blockDim.x) st.acc[i] = 0ull;
+    if (threadIdx.x == 0) *st.ticket = 0;
+}
+
 // SCAN: blk_hist holds each block's raw expert histogram and every CTA derives what it needs itself
 // (E <= kGatherScanMaxE): the prefix of its one or two token blocks, the expert totals and the padded
 // segment offsets; CTA 0 writes count and offset, CTA c writes the padding rows of experts c, c + grid,
@@ -101,7 +169,7 @@ __global__ void __launch_bounds__(32 * kGatherWarps) gather_kernel(
     const T* __restrict__ x, const int* __restrict__ topk_idx, const float* __restrict__ topk_gate,
     const int* __restrict__ blk_hist, int* __restrict__ offset, int* __restrict__ count, int T_, int k, int E,
     int d, int C, int* __restrict__ slot, int* __restrict__ row_token, float* __restrict__ row_gate,
-    T* __restrict__ xd, float* __restrict__ out_zero, int rank_major) {
+    T* __restrict__ xd, float* __restrict__ out_zero, int rank_major, const GatherStats stats) {
     __shared__ int s_pre[2][kGatherScanMaxE];  // prefix of blocks b_lo and b_lo + 1
     __shared__ int s_off[kGatherScanMaxE + 1];
     __shared__ int s_kept[kGatherScanMaxE];
@@ -188,6 +256,7 @@ __global__ void __launch_bounds__(32 * kGatherWarps) gather_kernel(
                 }
             }
     }
+    int s_final = -1;  // this pair's slot (the same in every lane of the warp)
     if (p < npairs) {
         int s = -1, r = -1;
         if (rk >= 0 && e >= 0 && e < E) {
@@ -204,6 +273,7 @@ __global__ void __launch_bounds__(32 * kGatherWarps) gather_kernel(
                 else s = -1;
             }
         }
+        s_final = s;
         __syncwarp();
         if (lane == 0) {
             slot[p] = s;
@@ -227,6 +297,10 @@ __global__ void __launch_bounds__(32 * kGatherWarps) gather_kernel(
                     if (i0 + j * 32 < nv) dst[i0 + j * 32] = w[j];
             }
         }
+    }
+    if (stats.acc != nullptr) {
+        const bool counted = p < npairs && e >= 0 && e < E;
+        fused_router_stats(stats, E, threadIdx.x >> 5, lane, e, gv, counted, counted && s_final < 0);
     }
     if (out_zero != nullptr) {
         const size_t n4 = (size_t)T_ * d / 4;
@@ -256,7 +330,7 @@ cudaError_t launch_dispatch_rank(const int* topk_idx, int T, int k, int E, int* 
 cudaError_t launch_dispatch_gather(const void* x, int bf16, const int* topk_idx, const float* topk_gate,
                                    const int* blk_hist, int* offset, int* count, bool scan, int T, int k, int E,
                                    int d, int C, int* slot, int* row_token, float* row_gate, void* x_dispatched,
-                                   float* out_to_zero, int rank_major, cudaStream_t s) {
+                                   float* out_to_zero, int rank_major, const GatherStats& stats, cudaStream_t s) {
     if (T <= 0) return cudaSuccess;
     if (scan && (E > kGatherScanMaxE || rank_major)) return cudaErrorInvalidValue;
     const long npairs = (long)T * k;
@@ -267,17 +341,17 @@ cudaError_t launch_dispatch_gather(const void* x, int bf16, const int* topk_idx,
         auto xo = static_cast<bf16_t*>(x_dispatched);
         if (scan)
             return launch_pdl(gather_kernel<bf16_t, true>, grid, block, 0, s, xp, topk_idx, topk_gate, blk_hist,
-                              offset, count, T, k, E, d, C, slot, row_token, row_gate, xo, out_to_zero, rank_major);
+                              offset, count, T, k, E, d, C, slot, row_token, row_gate, xo, out_to_zero, rank_major, stats);
         return launch_pdl(gather_kernel<bf16_t, false>, grid, block, 0, s, xp, topk_idx, topk_gate, blk_hist, offset,
-                          count, T, k, E, d, C, slot, row_token, row_gate, xo, out_to_zero, rank_major);
+                          count, T, k, E, d, C, slot, row_token, row_gate, xo, out_to_zero, rank_major, stats);
     }
     auto xp = static_cast<const float*>(x);
     auto xo = static_cast<float*>(x_dispatched);
     if (scan)
         return launch_pdl(gather_kernel<float, true>, grid, block, 0, s, xp, topk_idx, topk_gate, blk_hist, offset,
-                          count, T, k, E, d, C, slot, row_token, row_gate, xo, out_to_zero, rank_major);
+                          count, T, k, E, d, C, slot, row_token, row_gate, xo, out_to_zero, rank_major, stats);
     return launch_pdl(gather_kernel<float, false>, grid, block, 0, s, xp, topk_idx, topk_gate, blk_hist, offset,
-                      count, T, k, E, d, C, slot, row_token, row_gate, xo, out_to_zero, rank_major);
+                      count, T, k, E, d, C, slot, row_token, row_gate, xo, out_to_zero, rank_major, stats);
 }
 
 }  // namespace moe

@@ -127,7 +127,7 @@ moe_status moe_dispatch_static_scratch(const moe_config* cfg, const void* x, con
         return MOE_ERR_CUDA;
     if (launch_dispatch_gather(x, bf16, topk_idx, topk_gate, hist, expert_offset, nullptr, false, T, k, E, d, Ceff,
                                slot, row_token,
-                               row_gate, x_dispatched, nullptr, rank_major, s) != cudaSuccess)
+                               row_gate, x_dispatched, nullptr, rank_major, GatherStats{}, s) != cudaSuccess)
         return MOE_ERR_CUDA;
     return MOE_OK;
 }

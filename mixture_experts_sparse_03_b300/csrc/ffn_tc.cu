@@ -689,8 +689,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 // bf16 B buffers, and signal it; the MMAs (kind::f16) and the epilogue are those of gemm_tc_kernel.  HBM
 // carries one byte per weight.  Barriers: FULL / EMPTY (staging ring), BREADY (count: the converter
 // warps) / BEMPTY (bf16 buffers, freed by the MMA's commit), TFULL / TEMPTY (accumulators), LAST.
-constexpr int kF8Stages = 4;
-constexpr int kF8Bufs = 2;
+#ifndef MOE_FP8_STAGES
+#define MOE_FP8_STAGES 4
+#endif
+#ifndef MOE_FP8_BUFS
+#define MOE_FP8_BUFS 2
+#endif
+constexpr int kF8Stages = MOE_FP8_STAGES;  // staging ring: bf16 A and the B codes
+constexpr int kF8Bufs = MOE_FP8_BUFS;      // bf16 B buffers the converter warps fill
 constexpr uint32_t kB8Bytes = kBN * kBK;                 // 16 KiB of codes per stage
 constexpr uint32_t kF8StageBytes = kABytes + kB8Bytes;   // 32 KiB
 constexpr int kF8ConvWarps = 8;

@@ -100,12 +100,21 @@ inline int dispatch_hist_blocks(int T, int k, int rank_major) {
 // scan = false: blk_hist holds the scanned block prefixes and offset the segment offsets (from the rank
 // step's scan, in (rank, token) order when rank_major); scan = true (token order only) (E <= kGatherScanMaxE): blk_hist holds the raw block histograms and the
 // gather does the scan's work itself -- it writes count (if not null), offset and the padding rows
+// router statistics fused into the gather: acc [E + 1] (expert sums as multiples of 2^-32, then the drop
+// count) and ticket zero on entry (reset by the last CTA); results: importance [E], losses [2], dropped
+struct GatherStats {
+    unsigned long long* acc;  // nullptr: no statistics
+    int* ticket;
+    float* importance;
+    float* losses;
+    long long* dropped;
+};
 constexpr int kGatherScanMaxE = 64;
 constexpr int kGatherScanMaxHist = 2048;  // ints of histogram every gather CTA reads
 cudaError_t launch_dispatch_gather(const void* x, int bf16, const int* topk_idx, const float* topk_gate,
                                    const int* blk_hist, int* offset, int* count, bool scan, int T, int k, int E,
                                    int d, int C, int* slot, int* row_token, float* row_gate, void* x_dispatched,
-                                   float* out_to_zero, int rank_major, cudaStream_t s);
+                                   float* out_to_zero, int rank_major, const GatherStats& stats, cudaStream_t s);
 
 // ---- expert FFN -------------------------------------------------------------------------------
 // mode: 0 = up projection (+b1, GELU, store hidden), 1 = down projection to y (fp32),
