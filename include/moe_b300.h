@@ -353,8 +353,8 @@ MOE_API moe_status moe_device_status(void* workspace, size_t workspace_bytes, in
  * call, and events[i] right after the i-th such kernel, until `capacity` events are used; n kernels
  * thus use n + 1 events and kernel i ran between events[i] and events[i+1].  moe_trace_count()
  * returns how many events the current (or, once turned off, the last) trace recorded.  events == NULL
- * turns the hook off.  Events are recorded with cudaEventRecordExternal, so a call made while `stream`
- * is being captured puts event-record nodes into the graph and every replay of that graph times its
+ * turns the hook off.  While `stream` is being captured the events are recorded with
+ * cudaEventRecordExternal, so the graph gets event-record nodes and every replay of it times its
  * kernels with no host gaps between them.  Not thread-safe; meant for benchmarks.
  * Every compute entry point also opens an NVTX range named after itself for the length of the call
  * (a no-op unless a profiler is attached). */

@@ -32,7 +32,7 @@ struct Plan {
     GateGemmPlan gg;    // tensor-core logits GEMM (bf16 layers)
     int64_t rows;
     size_t o_err, o_idx, o_gate, o_slot, o_hist, o_count, o_off, o_rtok, o_rgate, o_xd, o_h, o_y, o_part, o_xn2,
-        o_wn2, o_rq, o_cosv, o_stats, o_fstats_out, total;
+        o_wn2, o_rq, o_cosv, o_fstats_out, total;
     size_t hdr_bytes;  // error word, its info, tickets and the cosine gate's expert flags: zeroed per call
 };
 
@@ -110,9 +110,10 @@ moe_status make_plan(const moe_config* c, Plan* pl) {
     const bool cos_tc = P.bf16 && P.gate == MOE_GATE_COSINE;  // cosine gates never take the fused path
     P.stats = (c->flags & MOE_FLAG_ROUTER_STATS) != 0;
     const size_t cos_flags = cos_tc ? 4 * (size_t)P.E : 0;
-    // the fused statistics' accumulators (E + 1 uint64) and ticket sit in the header, zeroed per call
+    // the router statistics' accumulators (E + 1 uint64) and ticket sit in the header, zeroed with it by
+    // one memset per call (moe_router_stats, and moe_forward with the statistics fused in)
     const size_t fstats_at = (16 + cos_flags + 7) / 8 * 8;
-    P.hdr_bytes = P.stats ? fstats_at + 8 * (size_t)(P.E + 1) + 8 : 16 + cos_flags;
+    P.hdr_bytes = fstats_at + 8 * (size_t)(P.E + 1) + 8;
     P.o_err = take(P.hdr_bytes);
     P.o_fstats = P.o_err + fstats_at;
     P.o_idx = take(4 * tk);
@@ -132,7 +133,6 @@ moe_status make_plan(const moe_config* c, Plan* pl) {
     P.o_wn2 = take(P.bf16 ? 4 * (size_t)P.gg.S * np : 0);
     P.o_rq = take(P.bf16 && !P.gg.fused ? 4 * (size_t)P.T * kRescoreInts : 0);
     P.o_cosv = take(cos_tc ? 8 * (size_t)P.E * P.d : 0);
-    P.o_stats = take(8 * (size_t)(P.E + 1) + 16);  // router statistics: expert sums, drop count, ticket
     P.o_fstats_out = take(P.stats ? 4 * (size_t)P.E + 16 : 0);  // fused statistics: importance, losses, drops
     P.total = o;
     *pl = P;
@@ -153,11 +153,14 @@ int g_capacity = 0;
 int g_recorded = 0;
 
 // A failed record (e.g. an event that was never created) turns the hook off and clears the error, so
-// tracing can never change the status of a launch; moe_trace_count() then shows the shortfall.  The
-// records are external: under stream capture each becomes an event-record node of the graph, so a
+// tracing can never change the status of a launch; moe_trace_count() then shows the shortfall.  Under
+// stream capture the records are external, so each becomes an event-record node of the graph and a
 // replayed graph times its kernels without host gaps between them.
 void trace_record(int i, cudaStream_t s) {
-    if (cudaEventRecordWithFlags(static_cast<cudaEvent_t>(g_events[i]), s, cudaEventRecordExternal) != cudaSuccess) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) cs = cudaStreamCaptureStatusNone;
+    const unsigned flags = cs == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : cudaEventRecordDefault;
+    if (cudaEventRecordWithFlags(static_cast<cudaEvent_t>(g_events[i]), s, flags) != cudaSuccess) {
         cudaGetLastError();
         g_events = nullptr;
         return;
@@ -786,9 +789,8 @@ moe_status moe_router_stats(const moe_config* cfg, const int32_t* topk_idx, cons
     if ((slot && !aligned16(slot)) || (dropped && (reinterpret_cast<uintptr_t>(dropped) & 7))) return MOE_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     int* err = at<int>(workspace, P.o_err);
-    void* scratch = at<void>(workspace, P.o_stats);
-    if (cudaMemsetAsync(err, 0, 16, s) != cudaSuccess) return MOE_ERR_CUDA;
-    if (cudaMemsetAsync(scratch, 0, 8 * (size_t)(P.E + 1) + 16, s) != cudaSuccess) return MOE_ERR_CUDA;
+    void* scratch = at<void>(workspace, P.o_fstats);  // in the header: one memset clears both
+    if (cudaMemsetAsync(err, 0, P.hdr_bytes, s) != cudaSuccess) return MOE_ERR_CUDA;
     return launch(s, [&] {
         return launch_router_stats(topk_idx, topk_gate, slot, P.T, P.k, P.E, scratch, err, importance, losses,
                                    reinterpret_cast<long long*>(dropped), s);

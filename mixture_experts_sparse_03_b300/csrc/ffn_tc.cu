@@ -683,25 +683,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---- the single-SM GEMM with block-FP8 weights ----------------------------------------------------
 // The expert weight arrives as FP8 E4M3 codes ([E, N, K], one byte each) with one fp32 scale per 128 x 128
-// block ([E, N/128, K/128]).  The producer loads each stage's 256 x 64 codes by TMA (no swizzle: 64-byte
-// rows) next to the bf16 A tile; eight converter warps turn them into bf16 (code value x scale, exact for
-// power-of-two scales), written in the 128-byte-swizzled K-major layout the MMA reads, into one of two
-// bf16 B buffers, and signal it; the MMAs (kind::f16) and the epilogue are those of gemm_tc_kernel.  HBM
-// carries one byte per weight.  Barriers: FULL / EMPTY (staging ring), BREADY (count: the converter
-// warps) / BEMPTY (bf16 buffers, freed by the MMA's commit), TFULL / TEMPTY (accumulators), LAST.
-#ifndef MOE_FP8_STAGES
-#define MOE_FP8_STAGES 4
-#endif
-#ifndef MOE_FP8_BUFS
-#define MOE_FP8_BUFS 2
-#endif
-constexpr int kF8Stages = MOE_FP8_STAGES;  // staging ring: bf16 A and the B codes
-constexpr int kF8Bufs = MOE_FP8_BUFS;      // bf16 B buffers the converter warps fill
-constexpr uint32_t kB8Bytes = kBN * kBK;                 // 16 KiB of codes per stage
-constexpr uint32_t kF8StageBytes = kABytes + kB8Bytes;   // 32 KiB
+// block ([E, N/128, K/128]).  HBM carries one byte per weight, and the codes come from DRAM while the
+// activations (A) mostly come from L2, so they travel in separate rings: a deep ring of code tiles
+// (256 x 64 bytes, no swizzle) that keeps enough bytes in flight to cover the DRAM latency, and a short
+// ring of bf16 A tiles, each fed by its own producer thread.  Eight converter warps turn each code tile
+// into bf16 (code value x scale, exact for power-of-two scales) in the 128-byte-swizzled K-major layout
+// the MMA reads, into one of two bf16 B buffers, then release the code tile; the MMAs (kind::f16) and the
+// epilogue are those of gemm_tc_kernel.  Barriers: FULLA / EMPTYA (A ring), FULLB / EMPTYB (code ring,
+// released by the converter warps), BREADY / BEMPTY (bf16 buffers, freed by the MMA's commit), TFULL /
+// TEMPTY (accumulators), LAST.
+constexpr int kF8ARing = 2;
+constexpr int kF8BRingMax = 8;
+constexpr int kF8Bufs = 2;
+constexpr uint32_t kB8Bytes = kBN * kBK;  // 16 KiB of codes per K block
 constexpr int kF8ConvWarps = 8;
-constexpr int kF8Threads = kThreads + 32 * kF8ConvWarps;  // 448
-constexpr int kF8Block = 128;                            // scale block edge
+constexpr int kF8Threads = kThreads + 32 * kF8ConvWarps + 32;  // + converters + the A producer: 480
+constexpr int kF8Block = 128;                                  // scale block edge
 
 // 16 E4M3 codes (one row's K block of 16) times `scale` -> 16 bf16 in two 16-byte chunks
 __device__ __forceinline__ void e4m3x16_to_bf16(const uint4 v, float scale, uint4& lo, uint4& hi) {
@@ -725,12 +722,15 @@ __global__ void __launch_bounds__(kF8Threads, 1)
     gemm_fp8w_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB8,
                      const TcArgs a) {
     extern __shared__ uint8_t smem_raw[];
+    const int NB = a.stages;  // depth of the code ring (host: as deep as shared memory allows, <= 8)
     uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    uint8_t* sStage = base;                                  // [stage]: A (bf16) then the B codes
-    uint8_t* sBb = base + kF8Stages * kF8StageBytes;         // [buffer]: bf16 B, 128-byte swizzle
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sBb + kF8Bufs * kBBytes);
-    constexpr int FULL = 0, EMPTY = kF8Stages, BREADY = 2 * kF8Stages, BEMPTY = 2 * kF8Stages + kF8Bufs,
-                  TFULL = 2 * kF8Stages + 2 * kF8Bufs, TEMPTY = TFULL + 2, LAST = TFULL + 4, NBARS = TFULL + 5;
+    uint8_t* sA = base;                              // [kF8ARing] bf16 A tiles, 128-byte swizzle
+    uint8_t* sBb = sA + kF8ARing * kABytes;          // [kF8Bufs] bf16 B tiles, 128-byte swizzle
+    uint8_t* sB8 = sBb + kF8Bufs * kBBytes;          // [NB] code tiles
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sB8 + NB * kB8Bytes);
+    const int FULLA = 0, EMPTYA = kF8ARing, BREADY = 2 * kF8ARing, BEMPTY = BREADY + kF8Bufs,
+              TFULL = BEMPTY + kF8Bufs, TEMPTY = TFULL + 2, LAST = TEMPTY + 2, FULLB = LAST + 1, EMPTYB = FULLB + NB,
+              NBARS = EMPTYB + NB;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + NBARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
     int* s_off = reinterpret_cast<int*>(tmem_holder + 4);
@@ -743,9 +743,9 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmB8);
         *abort_flag = 0;
-        for (int i = 0; i < kF8Stages; ++i) {
-            mbar_init(bar(FULL + i), 1);
-            mbar_init(bar(EMPTY + i), 1);
+        for (int i = 0; i < kF8ARing; ++i) {
+            mbar_init(bar(FULLA + i), 1);
+            mbar_init(bar(EMPTYA + i), 1);
         }
         for (int i = 0; i < kF8Bufs; ++i) {
             mbar_init(bar(BREADY + i), kF8ConvWarps);
@@ -756,6 +756,10 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             mbar_init(bar(TEMPTY + i), 4);
         }
         mbar_init(bar(LAST), 1);
+        for (int i = 0; i < NB; ++i) {
+            mbar_init(bar(FULLB + i), 1);
+            mbar_init(bar(EMPTYB + i), kF8ConvWarps);
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) tmem_alloc(smem_u32(tmem_holder), kTmemCols);
@@ -772,33 +776,41 @@ __global__ void __launch_bounds__(kF8Threads, 1)
     const int n_tiles = (a.N + kBN - 1) / kBN;
     const int num_tiles = m_tiles * n_tiles;
     const int k_iters = a.K / kBK;
+    const int a_warp = kF8Threads / 32 - 1;  // the last warp issues the A loads
 
-    if (warp == 0) {
+    if (warp == 0 || warp == a_warp) {
+        // warp 0: the code tiles, NB deep; the last warp: the A tiles, kF8ARing deep
         if (lane == 0) {
+            const bool is_b = warp == 0;
+            const int depth = is_b ? NB : kF8ARing;
+            const int FULL = is_b ? FULLB : FULLA, EMPTY = is_b ? EMPTYB : EMPTYA;
             int stage = 0;
             uint32_t phase = 0;
-            uint32_t issued_phase[kF8Stages];
-            bool issued[kF8Stages];
-            for (int i = 0; i < kF8Stages; ++i) { issued[i] = false; issued_phase[i] = 0; }
+            uint32_t issued_phase[kF8BRingMax];
+            bool issued[kF8BRingMax];
+            for (int i = 0; i < kF8BRingMax; ++i) { issued[i] = false; issued_phase[i] = 0; }
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
                 const int m0 = (tile / n_tiles) * kBM, n0 = (tile % n_tiles) * kBN;
                 const int e = expert_of_row(s_off, a.E, m0);
                 for (int kb = 0; kb < k_iters; ++kb) {
                     if (!mbar_wait(bar(EMPTY + stage), phase ^ 1u, abort_flag)) { ok = false; break; }
-                    mbar_expect_tx(bar(FULL + stage), kF8StageBytes);
-                    uint8_t* st = sStage + stage * kF8StageBytes;
-                    tma_load_2d(smem_u32(st), &tmA, bar(FULL + stage), kb * kBK, m0);
-                    tma_load_3d(smem_u32(st + kABytes), &tmB8, bar(FULL + stage), kb * kBK, n0, e);
+                    if (is_b) {
+                        mbar_expect_tx(bar(FULL + stage), kB8Bytes);
+                        tma_load_3d(smem_u32(sB8 + stage * kB8Bytes), &tmB8, bar(FULL + stage), kb * kBK, n0, e);
+                    } else {
+                        mbar_expect_tx(bar(FULL + stage), kABytes);
+                        tma_load_2d(smem_u32(sA + stage * kABytes), &tmA, bar(FULL + stage), kb * kBK, m0);
+                    }
                     issued[stage] = true;
                     issued_phase[stage] = phase;
-                    if (++stage == kF8Stages) { stage = 0; phase ^= 1u; }
+                    if (++stage == depth) { stage = 0; phase ^= 1u; }
                 }
             }
             if (!ok) {
                 record_error(a.err, kErrTimeout, kWhereGemmProducer);
                 *abort_flag = 1;
-                for (int i = 0; i < kF8Stages; ++i)
+                for (int i = 0; i < depth; ++i)
                     if (issued[i]) mbar_wait_bounded(bar(FULL + i), issued_phase[i]);
             }
         }
@@ -816,21 +828,21 @@ __global__ void __launch_bounds__(kF8Threads, 1)
                 fence_after();
                 const uint32_t d_tmem = tmem_base + acc * kBN;
                 for (int kb = 0; kb < k_iters; ++kb) {
-                    if (!mbar_wait(bar(FULL + stage), phase, abort_flag) ||
+                    if (!mbar_wait(bar(FULLA + stage), phase, abort_flag) ||
                         !mbar_wait(bar(BREADY + buf), bphase, abort_flag)) {
                         ok = false;
                         break;
                     }
                     fence_after();
-                    const uint64_t ad = smem_desc_sw128(smem_u32(sStage + stage * kF8StageBytes));
+                    const uint64_t ad = smem_desc_sw128(smem_u32(sA + stage * kABytes));
                     const uint64_t bd = smem_desc_sw128(smem_u32(sBb + buf * kBBytes));
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk)
                         mma_bf16(d_tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc, (kb | kk) != 0);
                     any = true;
-                    commit(bar(EMPTY + stage));
+                    commit(bar(EMPTYA + stage));
                     commit(bar(BEMPTY + buf));
-                    if (++stage == kF8Stages) { stage = 0; phase ^= 1u; }
+                    if (++stage == kF8ARing) { stage = 0; phase ^= 1u; }
                     if (++buf == kF8Bufs) { buf = 0; bphase ^= 1u; }
                 }
                 if (ok) commit(bar(TFULL + acc));
@@ -874,7 +886,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         }
     } else {
         // converter warps: thread ct handles 16-byte pieces ct, ct + 256, ct + 512, ct + 768 of the
-        // stage's 256 x 64 codes (row = piece / 4, K bytes 16 * (piece % 4) ..), rows 64 apart
+        // 256 x 64 codes (row = piece / 4, K bytes 16 * (piece % 4) ..), rows 64 apart
         const int ct = threadIdx.x - kThreads;
         const int r0 = ct >> 2, j = ct & 3;
         const int nbn = a.N / kF8Block, nbk = a.K / kF8Block;
@@ -885,18 +897,18 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             const int m0 = (tile / n_tiles) * kBM, n0 = (tile % n_tiles) * kBN;
             const int e = expert_of_row(s_off, a.E, m0);
             for (int kb = 0; kb < k_iters; ++kb) {
-                // the two 128-row scale blocks of this stage's 256 weight rows (rows past N are zero codes)
+                // the two 128-row scale blocks of this tile's 256 weight rows (rows past N are zero codes)
                 const int nb0 = n0 / kF8Block, kbs = (kb * kBK) / kF8Block;
                 const float* sp = a.scale + ((size_t)e * nbn) * nbk + kbs;
                 const float sc0 = nb0 < nbn ? __ldg(sp + (size_t)nb0 * nbk) : 0.f;
                 const float sc1 = nb0 + 1 < nbn ? __ldg(sp + (size_t)(nb0 + 1) * nbk) : 0.f;
-                const bool got = mbar_wait(bar(FULL + stage), phase, abort_flag) &&
+                const bool got = mbar_wait(bar(FULLB + stage), phase, abort_flag) &&
                                  mbar_wait(bar(BEMPTY + buf), bphase ^ 1u, abort_flag);
                 if (!__all_sync(0xffffffffu, got)) {
                     ok = false;
                     break;
                 }
-                const uint8_t* src = sStage + stage * kF8StageBytes + kABytes;
+                const uint8_t* src = sB8 + stage * kB8Bytes;
                 uint8_t* dst = sBb + buf * kBBytes;
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
@@ -910,8 +922,11 @@ __global__ void __launch_bounds__(kF8Threads, 1)
                 }
                 fence_proxy_async_smem();  // the MMA reads these bytes through the async proxy
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(BREADY + buf));
-                if (++stage == kF8Stages) { stage = 0; phase ^= 1u; }
+                if (lane == 0) {
+                    mbar_arrive(bar(BREADY + buf));
+                    mbar_arrive(bar(EMPTYB + stage));  // the code tile is read: its stage may refill
+                }
+                if (++stage == NB) { stage = 0; phase ^= 1u; }
                 if (++buf == kF8Bufs) { buf = 0; bphase ^= 1u; }
             }
         }
@@ -1068,9 +1083,16 @@ cudaError_t launch_wgrad_tc(const WgradParams& P, cudaStream_t s) {
     return launch_pdl(gemm_wgrad_kernel, dim3(grid), dim3(kThreads), smem, s, ma, mb, a);
 }
 
-size_t ffn_fp8_smem_bytes(int E) {
-    return 1024 + (size_t)kF8Stages * kF8StageBytes + (size_t)kF8Bufs * kBBytes +
-           (2 * kF8Stages + 2 * kF8Bufs + 5) * 8 + 16 + 4 * (size_t)(E + 1) + kBiasSmem;
+size_t ffn_fp8_smem_bytes(int E, bool bias, int nb) {
+    return 1024 + (size_t)kF8ARing * kABytes + (size_t)kF8Bufs * kBBytes + (size_t)nb * kB8Bytes +
+           (2 * kF8ARing + 2 * kF8Bufs + 5 + 2 * nb) * 8 + 16 + 4 * (size_t)(E + 1) + (bias ? kBiasSmem : 0);
+}
+
+// the code ring as deep as shared memory allows (at most kF8BRingMax, at least 2)
+int fp8_ring_depth(int E, bool bias) {
+    int nb = kF8BRingMax;
+    while (nb > 2 && ffn_fp8_smem_bytes(E, bias, nb) > 227 * 1024) --nb;
+    return nb;
 }
 
 cudaError_t launch_ffn_tc(const FfnParams& P, cudaStream_t s) {
@@ -1081,9 +1103,11 @@ cudaError_t launch_ffn_tc(const FfnParams& P, cudaStream_t s) {
     if (P.w_scale != nullptr) {  // block-FP8 weights: byte codes, single-SM tiles
         if (P.K % kF8Block || P.N % kF8Block) return cudaErrorInvalidValue;
         if (!tma_map_kind(P.W, (uint64_t)P.K, (uint64_t)P.N, (uint64_t)P.E, kBN, 1, &mb)) return cudaErrorInvalidValue;
+        const int nb = fp8_ring_depth(P.E, P.bias != nullptr);
         TcArgs a8{P.offset, P.row_token, P.row_gate, static_cast<const bf16_t*>(P.bias), P.C, P.out,
-                  P.E, P.K, P.N, P.mode, P.err, P.w_scale, kF8Stages, static_cast<bf16_t*>(P.aux), 0};
-        const size_t smem8 = ffn_fp8_smem_bytes(P.E);
+                  P.E, P.K, P.N, P.mode, P.err, P.w_scale, nb, static_cast<bf16_t*>(P.aux), 0};
+        const size_t smem8 = ffn_fp8_smem_bytes(P.E, P.bias != nullptr, nb);
+        if (smem8 > 227 * 1024) return cudaErrorInvalidValue;
         cudaError_t e8 = cudaFuncSetAttribute(gemm_fp8w_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem8);
         if (e8 != cudaSuccess) return e8;
         const int64_t tiles8 = (P.rows_cap / kBM) * (int64_t)((P.N + kBN - 1) / kBN);

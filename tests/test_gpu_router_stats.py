@@ -81,3 +81,41 @@ def test_router_stats_flags_bad_gates():
     st, _ = b.moe_device_status(ws, ws.numel())
     assert b.STATUS[st] == "MOE_ERR_DEVICE_CHECK"
     assert np.allclose(imp.cpu().numpy(), [63 * 0.5, 63 * 0.5, 0.0, 0.0])
+
+
+FUSED_CASES = CASES[:5] + [small_workload(T=300, d=128, h=256, E=8, k=2, capacity_factor=0.7, priority="rank"),
+                           WORKLOADS["bf16_e8_k2"], WORKLOADS["bf16_noisy_e64"]]
+
+
+@pytest.mark.parametrize("wl", FUSED_CASES, ids=lambda w: "%s_%s_T%d_E%d_k%d_%s" % (w.gate, w.dtype, w.T, w.E, w.k,
+                                                                                    w.priority))
+def test_router_stats_fused_into_forward(wl):
+    """moe_forward with MOE_FLAG_ROUTER_STATS: the statistics come out of the forward's own dispatch kernel
+    (the launch count does not change), equal bit for bit to the standalone moe_router_stats on the same
+    routing (both sum the gates exactly in fixed point), on two calls in a row (the last CTA resets the
+    accumulators); the layer output is the same bits as without the flag."""
+    _, tg = P.inputs(wl)
+    c0 = b.config(wl)
+    c = b.config(wl, flags=b.FLAG_ROUTER_STATS)
+    assert b.moe_forward_launches(c) == b.moe_forward_launches(c0)
+    dev = torch.device("cuda", 0)
+    ws = b.workspace(c, dev)
+    plain, _ = P.run_forward(wl, tg)
+    for call in range(2):
+        out = torch.full((wl.T, wl.d), float("nan"), dtype=torch.float32, device=dev)
+        b.forward(c, tg, out=out, ws=ws)
+        imp = torch.full((wl.E,), float("nan"), dtype=torch.float32, device=dev)
+        losses = torch.full((2,), -1.0, dtype=torch.float32, device=dev)
+        dropped = torch.full((1,), -7, dtype=torch.int64, device=dev)
+        b.check(b.moe_router_stats_result(c, ws, ws.numel(), imp, losses, dropped), "moe_router_stats_result")
+        st, info = b.moe_device_status(ws, ws.numel())
+        assert st == 0, (b.STATUS[st], info)
+        assert np.array_equal(out.cpu().numpy().view(np.int32), plain.view(np.int32))
+        if call == 0:
+            g = P.run_steps(wl, tg)
+            simp, slosses, sdrop = _stats(wl, g)
+        assert np.array_equal(imp.cpu().numpy().view(np.int32), simp.view(np.int32)), call
+        assert np.array_equal(losses.cpu().numpy().view(np.int32), slosses.view(np.int32)), call
+        assert int(dropped.cpu()[0]) == sdrop
+    # a config without the flag has nothing to read
+    assert b.moe_router_stats_result(c0, ws, ws.numel(), imp, losses, dropped) == 1
