@@ -49,6 +49,9 @@ constexpr double kTcErr = 32.0;
 // expected rows per expert (T * k / E) from which the expert GEMMs run on pairs of SMs by default
 constexpr int kPairMinRows = 2048;
 
+// byte offset of the int64 drop count in the fused statistics' results (after E + 2 floats)
+size_t fstats_drop_at(int E) { return (4 * (size_t)E + 8 + 7) / 8 * 8; }
+
 moe_status make_plan(const moe_config* c, Plan* pl) {
     if (c == nullptr) return MOE_ERR_INVALID_ARG;
     Plan P{};
@@ -133,7 +136,8 @@ moe_status make_plan(const moe_config* c, Plan* pl) {
     P.o_wn2 = take(P.bf16 ? 4 * (size_t)P.gg.S * np : 0);
     P.o_rq = take(P.bf16 && !P.gg.fused ? 4 * (size_t)P.T * kRescoreInts : 0);
     P.o_cosv = take(cos_tc ? 8 * (size_t)P.E * P.d : 0);
-    P.o_fstats_out = take(P.stats ? 4 * (size_t)P.E + 16 : 0);  // fused statistics: importance, losses, drops
+    // fused statistics: importance [E] and losses [2] fp32, then the drop count (int64, 8-byte aligned)
+    P.o_fstats_out = take(P.stats ? fstats_drop_at(P.E) + 8 : 0);
     P.total = o;
     *pl = P;
     return MOE_OK;
@@ -408,7 +412,7 @@ moe_status route_and_dispatch(const Plan& P, const moe_config* cfg, const void* 
         st.ticket = reinterpret_cast<int*>(st.acc + P.E + 1);
         st.importance = at<float>(workspace, P.o_fstats_out);
         st.losses = st.importance + P.E;
-        st.dropped = reinterpret_cast<long long*>(at<char>(workspace, P.o_fstats_out) + 4 * (size_t)P.E + 8);
+        st.dropped = reinterpret_cast<long long*>(at<char>(workspace, P.o_fstats_out) + fstats_drop_at(P.E));
     }
     return launch(s, [&] {
         return launch_dispatch_gather(x, P.bf16, idx, gate, hist, off, count, gather_scan, P.T, P.k, P.E, P.d, P.Ceff,
@@ -809,7 +813,7 @@ moe_status moe_router_stats_result(const moe_config* cfg, const void* workspace,
         return MOE_ERR_CUDA;
     if (losses && cudaMemcpyAsync(losses, res + 4 * (size_t)P.E, 8, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
         return MOE_ERR_CUDA;
-    if (dropped && cudaMemcpyAsync(dropped, res + 4 * (size_t)P.E + 8, 8, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+    if (dropped && cudaMemcpyAsync(dropped, res + fstats_drop_at(P.E), 8, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
         return MOE_ERR_CUDA;
     return MOE_OK;
 }
