@@ -539,7 +539,8 @@ moe_status backward_impl(const moe_config* cfg, const void* x, const void* w_gat
     // 2. dY = gate * dout per row; the gates' and scores' gradient per token
     void* dy = at<void>(ws, B.o_dy);
     void* dS = at<void>(ws, B.o_dS);
-    MOE_TRY(launch(s, [&] { return launch_bwd_dy(dout, rtok, rgate, R, d, dy, s); }));
+    const int* rows_used = off + E;  // offset[E]: rows past it were never dispatched
+    MOE_TRY(launch(s, [&] { return launch_bwd_dy(dout, rtok, rgate, R, d, rows_used, dy, s); }));
     MOE_TRY(launch(s, [&] {
         return launch_bwd_gate(dout, y, idx, gate, slot, off, logits, noise_eps, T, B.Tp, d, E, P.k,
                                P.gate == MOE_GATE_NOISY, P.norm == MOE_GATE_NORM_ALL, B.NpP, dS, s);
@@ -548,8 +549,8 @@ moe_status backward_impl(const moe_config* cfg, const void* x, const void* w_gat
     void* w1T = at<void>(ws, B.o_w1T);
     void* w2T = at<void>(ws, B.o_w2T);
     void* dz = at<void>(ws, B.o_dz);
-    MOE_TRY(launch(s, [&] { return launch_transpose(w2, w2T, E, d, h, d, nullptr, s); }));
-    MOE_TRY(launch(s, [&] { return launch_transpose(w1, w1T, E, h, d, h, nullptr, s); }));
+    MOE_TRY(launch(s, [&] { return launch_transpose(w2, w2T, E, d, h, d, nullptr, nullptr, s); }));
+    MOE_TRY(launch(s, [&] { return launch_transpose(w1, w1T, E, h, d, h, nullptr, nullptr, s); }));
     FfnParams da{};
     da.A = dy; da.W = w2T; da.offset = off; da.row_token = rtok; da.row_gate = rgate; da.C = dz;
     da.aux = at<void>(ws, B.o_z); da.E = E; da.K = d; da.N = h; da.bf16 = 1; da.mode = 3; da.rows_cap = P.rows;
@@ -576,10 +577,10 @@ moe_status backward_impl(const moe_config* cfg, const void* x, const void* w_gat
     void* hT = at<void>(ws, B.o_hT);
     void* dyT = at<void>(ws, B.o_dyT);
     void* dzT = at<void>(ws, B.o_dzT);
-    MOE_TRY(launch(s, [&] { return launch_transpose(dy, dyT, 1, R, d, B.Rp, rtok, s); }));
-    MOE_TRY(launch(s, [&] { return launch_transpose(hb, hT, 1, R, h, B.Rp, rtok, s); }));
-    MOE_TRY(launch(s, [&] { return launch_transpose(dz, dzT, 1, R, h, B.Rp, rtok, s); }));
-    MOE_TRY(launch(s, [&] { return launch_transpose(xd, xdT, 1, R, d, B.Rp, rtok, s); }));
+    MOE_TRY(launch(s, [&] { return launch_transpose(dy, dyT, 1, R, d, B.Rp, rtok, rows_used, s); }));
+    MOE_TRY(launch(s, [&] { return launch_transpose(hb, hT, 1, R, h, B.Rp, rtok, rows_used, s); }));
+    MOE_TRY(launch(s, [&] { return launch_transpose(dz, dzT, 1, R, h, B.Rp, rtok, rows_used, s); }));
+    MOE_TRY(launch(s, [&] { return launch_transpose(xd, xdT, 1, R, d, B.Rp, rtok, rows_used, s); }));
     MOE_TRY(launch(s, [&] {
         return launch_wgrad_tc(WgradParams{dyT, hT, off, dw2, E, d, h, (int64_t)B.Rp, err}, s);
     }));
@@ -590,8 +591,8 @@ moe_status backward_impl(const moe_config* cfg, const void* x, const void* w_gat
     void* dST = at<void>(ws, B.o_dST);
     void* xT = at<void>(ws, B.o_xT);
     float* dwcat = at<float>(ws, B.o_dwcat);
-    MOE_TRY(launch(s, [&] { return launch_transpose(dS, dST, 1, B.Tp, B.NpP, B.Tp, nullptr, s); }));
-    MOE_TRY(launch(s, [&] { return launch_transpose(x, xT, 1, T, d, B.Tp, nullptr, s); }));
+    MOE_TRY(launch(s, [&] { return launch_transpose(dS, dST, 1, B.Tp, B.NpP, B.Tp, nullptr, nullptr, s); }));
+    MOE_TRY(launch(s, [&] { return launch_transpose(x, xT, 1, T, d, B.Tp, nullptr, nullptr, s); }));
     MOE_TRY(launch(s, [&] {
         return launch_wgrad_tc(WgradParams{dST, xT, off2, dwcat, 1, B.Np, d, (int64_t)B.Tp, err}, s);
     }));

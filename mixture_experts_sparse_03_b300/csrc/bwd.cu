@@ -19,10 +19,12 @@ namespace {
 
 constexpr int kTile = 32;
 
-// dst[b][c][r] = src[b][r][c] for r < R (0 where row_mask[r] < 0), 0 for R <= r < Rp; a 32 x 32 tile per
-// block through shared memory (both global sides coalesced)
+// dst[b][c][r] = src[b][r][c] for r < R (0 where row_mask[r] < 0), 0 for R <= r < Rp; with a mask, the rows
+// from *row_limit on (dispatched rows past the last expert's segment, whose row_token was never written)
+// are 0 too.  A 32 x 32 tile per block through shared memory (both global sides coalesced).
 __global__ void __launch_bounds__(kTile * 8) transpose_kernel(const bf16_t* __restrict__ src, bf16_t* __restrict__ dst,
-                                                             int R, int C, int Rp, const int* __restrict__ row_mask) {
+                                                             int R, int C, int Rp, const int* __restrict__ row_mask,
+                                                             const int* __restrict__ row_limit) {
     __shared__ bf16_t tile[kTile][kTile + 2];
     pdl_wait();
     pdl_trigger();
@@ -30,10 +32,11 @@ __global__ void __launch_bounds__(kTile * 8) transpose_kernel(const bf16_t* __re
     const int r0 = blockIdx.y * kTile, c0 = blockIdx.x * kTile;
     const bf16_t* s = src + (size_t)b * R * C;
     bf16_t* o = dst + (size_t)b * C * Rp;
+    const int rl = row_mask != nullptr ? min(R, *row_limit) : R;
     for (int i = threadIdx.y; i < kTile; i += 8) {
         const int r = r0 + i, c = c0 + threadIdx.x;
         bf16_t v = 0;
-        if (r < R && c < C && (row_mask == nullptr || row_mask[r] >= 0)) v = s[(size_t)r * C + c];
+        if (r < rl && c < C && (row_mask == nullptr || row_mask[r] >= 0)) v = s[(size_t)r * C + c];
         tile[i][threadIdx.x] = v;
     }
     __syncthreads();
@@ -43,15 +46,16 @@ __global__ void __launch_bounds__(kTile * 8) transpose_kernel(const bf16_t* __re
     }
 }
 
-// dY[r][:] = gate_r * dout[token_r][:] in bf16 (a warp per row, 8 columns per lane per step)
+// dY[r][:] = gate_r * dout[token_r][:] in bf16 (a warp per row, 8 columns per lane per step); rows of
+// padding and rows from *row_limit on (past the last expert's segment: row_token never written) get 0
 __global__ void __launch_bounds__(256) dy_kernel(const float* __restrict__ dout, const int* __restrict__ row_token,
                                                 const float* __restrict__ row_gate, int rows, int d,
-                                                bf16_t* __restrict__ dY) {
+                                                const int* __restrict__ row_limit, bf16_t* __restrict__ dY) {
     pdl_wait();
     pdl_trigger();
     const int r = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     if (r >= rows) return;
-    const int t = row_token[r];
+    const int t = r < *row_limit ? row_token[r] : -1;
     const float g = t >= 0 ? row_gate[r] : 0.f;
     uint4* dst = reinterpret_cast<uint4*>(dY + (size_t)r * d);
     for (int c = lane * 8; c < d; c += 256) {
@@ -188,17 +192,18 @@ __global__ void iota_rows_kernel(int* __restrict__ rows, int T, int Tp, int* __r
 }  // namespace
 
 cudaError_t launch_transpose(const void* src, void* dst, int B, int R, int C, int Rp, const int* row_mask,
-                             cudaStream_t s) {
+                             const int* row_limit, cudaStream_t s) {
     if (B <= 0 || Rp <= 0 || C <= 0) return cudaSuccess;
+    if (row_mask != nullptr && row_limit == nullptr) return cudaErrorInvalidValue;
     const dim3 grid((C + kTile - 1) / kTile, (Rp + kTile - 1) / kTile, B), block(kTile, 8);
     return launch_pdl(transpose_kernel, grid, block, 0, s, static_cast<const bf16_t*>(src), static_cast<bf16_t*>(dst),
-                      R, C, Rp, row_mask);
+                      R, C, Rp, row_mask, row_limit);
 }
 
-cudaError_t launch_bwd_dy(const float* dout, const int* row_token, const float* row_gate, int rows, int d, void* dY,
-                          cudaStream_t s) {
+cudaError_t launch_bwd_dy(const float* dout, const int* row_token, const float* row_gate, int rows, int d,
+                          const int* row_limit, void* dY, cudaStream_t s) {
     if (rows <= 0) return cudaSuccess;
-    return launch_pdl(dy_kernel, dim3((rows + 7) / 8), dim3(256), 0, s, dout, row_token, row_gate, rows, d,
+    return launch_pdl(dy_kernel, dim3((rows + 7) / 8), dim3(256), 0, s, dout, row_token, row_gate, rows, d, row_limit,
                       static_cast<bf16_t*>(dY));
 }
 

@@ -692,8 +692,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // epilogue are those of gemm_tc_kernel.  Barriers: FULLA / EMPTYA (A ring), FULLB / EMPTYB (code ring,
 // released by the converter warps), BREADY / BEMPTY (bf16 buffers, freed by the MMA's commit), TFULL /
 // TEMPTY (accumulators), LAST.
-constexpr int kF8ARing = 2;
-constexpr int kF8BRingMax = 8;
+constexpr int kF8ARing = 4;     // A tiles come from L2: a few stages cover its latency
+constexpr int kF8BRingMax = 8;  // code tiles come from DRAM: as many as fit
 constexpr int kF8Bufs = 2;
 constexpr uint32_t kB8Bytes = kBN * kBK;  // 16 KiB of codes per K block
 constexpr int kF8ConvWarps = 8;
@@ -896,12 +896,20 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
             const int m0 = (tile / n_tiles) * kBM, n0 = (tile % n_tiles) * kBN;
             const int e = expert_of_row(s_off, a.E, m0);
+            // the two 128-row scale blocks of this tile's 256 weight rows (rows past N are zero codes); the
+            // scales of the next K block are loaded one iteration ahead, so their latency stays hidden
+            const int nb0 = n0 / kF8Block;
+            const float* sp = a.scale + ((size_t)e * nbn) * nbk;
+            auto load_scales = [&](int kb_, float& s0, float& s1) {
+                const int kbs = (kb_ * kBK) / kF8Block;
+                s0 = nb0 < nbn ? __ldg(sp + (size_t)nb0 * nbk + kbs) : 0.f;
+                s1 = nb0 + 1 < nbn ? __ldg(sp + (size_t)(nb0 + 1) * nbk + kbs) : 0.f;
+            };
+            float nsc0, nsc1;
+            load_scales(0, nsc0, nsc1);
             for (int kb = 0; kb < k_iters; ++kb) {
-                // the two 128-row scale blocks of this tile's 256 weight rows (rows past N are zero codes)
-                const int nb0 = n0 / kF8Block, kbs = (kb * kBK) / kF8Block;
-                const float* sp = a.scale + ((size_t)e * nbn) * nbk + kbs;
-                const float sc0 = nb0 < nbn ? __ldg(sp + (size_t)nb0 * nbk) : 0.f;
-                const float sc1 = nb0 + 1 < nbn ? __ldg(sp + (size_t)(nb0 + 1) * nbk) : 0.f;
+                const float sc0 = nsc0, sc1 = nsc1;
+                if (kb + 1 < k_iters) load_scales(kb + 1, nsc0, nsc1);
                 const bool got = mbar_wait(bar(FULLB + stage), phase, abort_flag) &&
                                  mbar_wait(bar(BEMPTY + buf), bphase ^ 1u, abort_flag);
                 if (!__all_sync(0xffffffffu, got)) {

@@ -163,12 +163,13 @@ cudaError_t launch_combine(const float* y, const int* slot, const int* offset, c
 cudaError_t launch_zero(float* p, size_t n, cudaStream_t s);
 
 // ---- backward (bwd.cu) ------------------------------------------------------------------------------
-// dst[b][c][r] = src[b][r][c] (bf16) for r < R, zero where row_mask[r] < 0 (if given) and for R <= r < Rp
+// dst[b][c][r] = src[b][r][c] (bf16) for r < R, zero for R <= r < Rp; with row_mask, zero where
+// row_mask[r] < 0 and from row *row_limit on (device int: the dispatched rows in use, offset[E])
 cudaError_t launch_transpose(const void* src, void* dst, int B, int R, int C, int Rp, const int* row_mask,
-                             cudaStream_t s);
-// dY[r] = row_gate[r] * dout[row_token[r]] in bf16 (zero for padding rows)
-cudaError_t launch_bwd_dy(const float* dout, const int* row_token, const float* row_gate, int rows, int d, void* dY,
-                          cudaStream_t s);
+                             const int* row_limit, cudaStream_t s);
+// dY[r] = row_gate[r] * dout[row_token[r]] in bf16 (zero for padding rows and from row *row_limit on)
+cudaError_t launch_bwd_dy(const float* dout, const int* row_token, const float* row_gate, int rows, int d,
+                          const int* row_limit, void* dY, cudaStream_t s);
 // per token: the gates' and scores' gradient, dS [Tp, Np] bf16 = [ds | dn (noisy) | 0]
 cudaError_t launch_bwd_gate(const float* dout, const float* y, const int* topk_idx, const float* topk_gate,
                             const int* slot, const int* offset, const float* logits, const float* eps, int T, int Tp,
