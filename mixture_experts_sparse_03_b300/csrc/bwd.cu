@@ -17,33 +17,45 @@ namespace moe {
 
 namespace {
 
-constexpr int kTile = 32;
-
 // dst[b][c][r] = src[b][r][c] for r < R (0 where row_mask[r] < 0), 0 for R <= r < Rp; with a mask, the rows
 // from *row_limit on (dispatched rows past the last expert's segment, whose row_token was never written)
-// are 0 too.  A 32 x 32 tile per block through shared memory (both global sides coalesced).
-__global__ void __launch_bounds__(kTile * 8) transpose_kernel(const bf16_t* __restrict__ src, bf16_t* __restrict__ dst,
-                                                             int R, int C, int Rp, const int* __restrict__ row_mask,
-                                                             const int* __restrict__ row_limit) {
-    __shared__ bf16_t tile[kTile][kTile + 2];
+// are 0 too.  C and Rp are multiples of 64.  A 64 x 64 tile per block through shared memory: 16-byte
+// loads of 8 consecutive columns, and 32-byte stores of 16 consecutive rows of one output row (each
+// 4-byte word pairs two source rows); the tile's row stride of 33 words keeps both sides' shared-memory
+// accesses within two ways of bank conflict.
+constexpr int kT64 = 64, kTStride = 66;  // bf16 per shared row
+__global__ void __launch_bounds__(256) transpose_kernel(const bf16_t* __restrict__ src, bf16_t* __restrict__ dst,
+                                                       int R, int C, int Rp, const int* __restrict__ row_mask,
+                                                       const int* __restrict__ row_limit) {
+    __shared__ uint32_t tile[kT64 * kTStride / 2];
     pdl_wait();
     pdl_trigger();
-    const int b = blockIdx.z;
-    const int r0 = blockIdx.y * kTile, c0 = blockIdx.x * kTile;
+    const int b = blockIdx.z, t = threadIdx.x;
+    const int r0 = blockIdx.y * kT64, c0 = blockIdx.x * kT64;
     const bf16_t* s = src + (size_t)b * R * C;
     bf16_t* o = dst + (size_t)b * C * Rp;
     const int rl = row_mask != nullptr ? min(R, *row_limit) : R;
-    for (int i = threadIdx.y; i < kTile; i += 8) {
-        const int r = r0 + i, c = c0 + threadIdx.x;
-        bf16_t v = 0;
-        if (r < rl && c < C && (row_mask == nullptr || row_mask[r] >= 0)) v = s[(size_t)r * C + c];
-        tile[i][threadIdx.x] = v;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int idx = t + 256 * i, row = idx >> 3, chunk = idx & 7, r = r0 + row;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (r < rl && (row_mask == nullptr || row_mask[r] >= 0))
+            v = __ldg(reinterpret_cast<const uint4*>(s + (size_t)r * C + c0 + chunk * 8));
+        uint32_t* w = tile + (row * kTStride + chunk * 8) / 2;
+        w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
     }
     __syncthreads();
-    for (int i = threadIdx.y; i < kTile; i += 8) {
-        const int c = c0 + i, r = r0 + threadIdx.x;
-        if (c < C && r < Rp) o[(size_t)c * Rp + r] = tile[threadIdx.x][i];
+    const bf16_t* th = reinterpret_cast<const bf16_t*>(tile);
+    const int c = t >> 2, g = t & 3;  // output row c0 + c, its rows r0 + 16 g .. + 15
+    uint32_t wv[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const int r = 16 * g + 2 * q;
+        wv[q] = (uint32_t)th[r * kTStride + c] | ((uint32_t)th[(r + 1) * kTStride + c] << 16);
     }
+    uint4* out = reinterpret_cast<uint4*>(o + (size_t)(c0 + c) * Rp + r0 + 16 * g);
+    out[0] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+    out[1] = make_uint4(wv[4], wv[5], wv[6], wv[7]);
 }
 
 // dY[r][:] = gate_r * dout[token_r][:] in bf16 (a warp per row, 8 columns per lane per step); rows of
@@ -195,7 +207,8 @@ cudaError_t launch_transpose(const void* src, void* dst, int B, int R, int C, in
                              const int* row_limit, cudaStream_t s) {
     if (B <= 0 || Rp <= 0 || C <= 0) return cudaSuccess;
     if (row_mask != nullptr && row_limit == nullptr) return cudaErrorInvalidValue;
-    const dim3 grid((C + kTile - 1) / kTile, (Rp + kTile - 1) / kTile, B), block(kTile, 8);
+    if (C % kT64 || Rp % kT64) return cudaErrorInvalidValue;
+    const dim3 grid(C / kT64, Rp / kT64, B), block(256);
     return launch_pdl(transpose_kernel, grid, block, 0, s, static_cast<const bf16_t*>(src), static_cast<bf16_t*>(dst),
                       R, C, Rp, row_mask, row_limit);
 }
