@@ -507,8 +507,7 @@ def measure(wl, args, dev, stream, flush, world):
     return res, L
 
 
-BWD_TAIL = ["fwd_up_keep_z", "fwd_down_y", "logits_gemm", "bwd_dy", "bwd_gate_grad", "transpose_w2", "transpose_w1",
-            "bwd_dz_gemm", "bwd_dx_gemm", "iota_rows", "gate_weights_t", "bwd_dx_gate_gemm", "transpose_dy",
+BWD_TAIL = ["fwd_up_keep_z", "fwd_down_y", "logits_gemm", "bwd_dy", "bwd_gate_grad", "bwd_dz_gemm", "bwd_dx_gemm", "iota_rows", "gate_weights_t", "bwd_dx_gate_gemm", "transpose_dy",
             "transpose_h", "transpose_dz", "transpose_xd", "wgrad_w2", "wgrad_w1", "transpose_ds", "transpose_x",
             "wgrad_gate", "colsum_db2", "colsum_db1"]
 

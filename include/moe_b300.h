@@ -305,7 +305,7 @@ MOE_API moe_status moe_forward(const moe_config* cfg, const void* x, const void*
  *   MOE_GATE_NORM_ALL) to the scores, W_g (and for the noisy gate, through eps softplus(x W_n^T), to W_n)
  *   and x.  The call recomputes the forward (routing, dispatch, the expert FFN keeping Z = W1 x + b1 in
  *   bf16) and runs the backward GEMMs on the tensor cores: the data gradients grouped by expert over the
- *   dispatched rows (with transposed copies of W1 and W2), the weight gradients contracting over each
+ *   dispatched rows (reading W1 and W2 as stored, MN-major), the weight gradients contracting over each
  *   expert's rows.  Intermediate gradients (dY = g dout per row, dZ, the scores' gradient) are rounded to
  *   bf16 for the GEMMs; dx is accumulated with fp32 atomics (not bitwise reproducible).
  * Supported: bf16 layers with the softmax or noisy gate (else MOE_ERR_UNSUPPORTED, also for

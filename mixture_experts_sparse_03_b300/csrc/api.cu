@@ -310,6 +310,7 @@ FfnParams ffn_params(const Plan& P, int mode, const void* A, const void* W, cons
     f.rows_cap = P.rows;
     f.err = err;
     f.pair = (w_scale || mode >= 3) ? 0 : P.pair;  // block-FP8 weights and the backward run on single SMs
+    f.max_rows = P.C < P.T ? P.C : P.T;
     return f;
 }
 
@@ -456,8 +457,8 @@ moe_status forward_impl(const moe_config* cfg, const void* x, const void* w_gate
 // ---- backward: its workspace after the forward's ------------------------------------------------------
 struct BwdPlan {
     int Rp, Tp, Np, NpP;  // rows rounded to 64, tokens to 128, gate logits per token (and rounded to 64)
-    size_t o_z, o_dy, o_dz, o_xdT, o_hT, o_dyT, o_dzT, o_w1T, o_w2T, o_logits, o_dS, o_dST, o_xT, o_wcatT, o_dwcat,
-        o_rows, o_off2, total;
+    size_t o_z, o_dy, o_dz, o_xdT, o_hT, o_dyT, o_dzT, o_logits, o_dS, o_dST, o_xT, o_wcatT, o_dwcat, o_rows,
+        o_off2, total;
 };
 
 moe_status make_bwd_plan(const Plan& P, const moe_config* c, BwdPlan* B) {
@@ -477,8 +478,6 @@ moe_status make_bwd_plan(const Plan& P, const moe_config* c, BwdPlan* B) {
     b.o_hT = take((size_t)P.h * b.Rp * 2);
     b.o_dyT = take((size_t)P.d * b.Rp * 2);
     b.o_dzT = take((size_t)P.h * b.Rp * 2);
-    b.o_w1T = take((size_t)P.E * P.d * P.h * 2);
-    b.o_w2T = take((size_t)P.E * P.h * P.d * 2);
     b.o_logits = take((size_t)P.T * b.Np * 4);
     b.o_dS = take((size_t)b.Tp * b.NpP * 2);
     b.o_dST = take((size_t)b.NpP * b.Tp * 2);
@@ -545,19 +544,16 @@ moe_status backward_impl(const moe_config* cfg, const void* x, const void* w_gat
         return launch_bwd_gate(dout, y, idx, gate, slot, off, logits, noise_eps, T, B.Tp, d, E, P.k,
                                P.gate == MOE_GATE_NOISY, P.norm == MOE_GATE_NORM_ALL, B.NpP, dS, s);
     }));
-    // 3. data gradients through the experts: dZ = (dY W2) * GELU'(Z), dx += dZ W1 (scattered to tokens)
-    void* w1T = at<void>(ws, B.o_w1T);
-    void* w2T = at<void>(ws, B.o_w2T);
+    // 3. data gradients through the experts: dZ = (dY W2) * GELU'(Z), dx += dZ W1 (scattered to tokens); the
+    //    GEMMs read W2 [E, d, h] and W1 [E, h, d] as they are, [E, K, N], MN-major
     void* dz = at<void>(ws, B.o_dz);
-    MOE_TRY(launch(s, [&] { return launch_transpose(w2, w2T, E, d, h, d, nullptr, nullptr, s); }));
-    MOE_TRY(launch(s, [&] { return launch_transpose(w1, w1T, E, h, d, h, nullptr, nullptr, s); }));
     FfnParams da{};
-    da.A = dy; da.W = w2T; da.offset = off; da.row_token = rtok; da.row_gate = rgate; da.C = dz;
+    da.A = dy; da.W = w2; da.w_kn = 1; da.offset = off; da.row_token = rtok; da.row_gate = rgate; da.C = dz;
     da.aux = at<void>(ws, B.o_z); da.E = E; da.K = d; da.N = h; da.bf16 = 1; da.mode = 3; da.rows_cap = P.rows;
     da.err = err;
     MOE_TRY(run_ffn(P, cfg, da, s));
     FfnParams dxe{};
-    dxe.A = dz; dxe.W = w1T; dxe.offset = off; dxe.row_token = rtok; dxe.row_gate = rgate; dxe.out = dx;
+    dxe.A = dz; dxe.W = w1; dxe.w_kn = 1; dxe.offset = off; dxe.row_token = rtok; dxe.row_gate = rgate; dxe.out = dx;
     dxe.E = E; dxe.K = h; dxe.N = d; dxe.bf16 = 1; dxe.mode = 5; dxe.rows_cap = P.rows; dxe.err = err;
     MOE_TRY(run_ffn(P, cfg, dxe, s));
     // 4. data gradient through the gate: dx += dS [W_g ; W_n]

@@ -57,6 +57,7 @@ struct TcArgs {
     int stages;          // SM-pair kernel: depth of its TMA ring
     bf16_t* aux;         // modes 3 / 4: the pre-activations Z [rows, N] (read / written)
     int M;               // weight-gradient kernel: rows of each expert's output [M, N]
+    int b_mn;            // single-SM kernel: B is [E, K, N] (N contiguous), read MN-major
 };
 
 using namespace tc;
@@ -234,7 +235,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!mbar_wait(bar(EMPTY + stage), phase ^ 1u, abort_flag)) { ok = false; break; }
                     mbar_expect_tx(bar(FULL + stage), kStageBytes);
                     tma_load_2d(smem_u32(sA + stage * kABytes), &tmA, bar(FULL + stage), kb * kBK, m0);
-                    tma_load_3d(smem_u32(sB + stage * kBBytes), &tmB, bar(FULL + stage), kb * kBK, n0, e);
+                    if (a.b_mn) {  // four boxes of 64 N-columns x 64 K-rows
+#pragma unroll
+                        for (int j = 0; j < kBN / 64; ++j)
+                            tma_load_3d(smem_u32(sB + stage * kBBytes + j * 8192), &tmB, bar(FULL + stage), n0 + 64 * j,
+                                        kb * kBK, e);
+                    } else {
+                        tma_load_3d(smem_u32(sB + stage * kBBytes), &tmB, bar(FULL + stage), kb * kBK, n0, e);
+                    }
                     issued[stage] = true;
                     issued_phase[stage] = phase;
                     if (++stage == kStages) { stage = 0; phase ^= 1u; }
@@ -252,7 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16(kBM, kBN);
+            const uint32_t idesc = idesc_bf16(kBM, kBN) | (a.b_mn ? kIdescBMnMajor : 0u);
             int stage = 0;
             uint32_t phase = 0;
             int local = 0;
@@ -267,10 +275,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!mbar_wait(bar(FULL + stage), phase, abort_flag)) { ok = false; break; }
                     fence_after();
                     const uint64_t ad = smem_desc_sw128(smem_u32(sA + stage * kABytes));
-                    const uint64_t bd = smem_desc_sw128(smem_u32(sB + stage * kBBytes));
+                    // K-major B: a K step of 16 is 32 bytes along the row; MN-major: 16 rows of 128 bytes
+                    const uint64_t bd = a.b_mn ? smem_desc_sw128_mn(smem_u32(sB + stage * kBBytes))
+                                               : smem_desc_sw128(smem_u32(sB + stage * kBBytes));
+                    const uint64_t bstep = a.b_mn ? (2048 >> 4) : 2;
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk)
-                        mma_bf16(d_tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc, (kb | kk) != 0);
+                        mma_bf16(d_tmem, ad + (uint64_t)(kk * 2), bd + bstep * kk, idesc, (kb | kk) != 0);
                     any = true;
                     commit(bar(EMPTY + stage));
                     if (++stage == kStages) { stage = 0; phase ^= 1u; }
@@ -688,17 +699,35 @@ __global__ void __launch_bounds__(kThreads, 1)
 // (256 x 64 bytes, no swizzle) that keeps enough bytes in flight to cover the DRAM latency, and a short
 // ring of bf16 A tiles, each fed by its own producer thread.  Eight converter warps turn each code tile
 // into bf16 (code value x scale, exact for power-of-two scales) in the 128-byte-swizzled K-major layout
-// the MMA reads, into one of two bf16 B buffers, then release the code tile; the MMAs (kind::f16) and the
-// epilogue are those of gemm_tc_kernel.  Barriers: FULLA / EMPTYA (A ring), FULLB / EMPTYB (code ring,
-// released by the converter warps), BREADY / BEMPTY (bf16 buffers, freed by the MMA's commit), TFULL /
-// TEMPTY (accumulators), LAST.
+// the MMA reads, into one of a few bf16 B buffers, then release the code tile; the MMAs (kind::f16) and
+// the epilogue are those of gemm_tc_kernel.  In the swapped kernel (at most 64 rows per expert) the
+// converters form two groups that take alternate K blocks, so that one group's chain of waits, loads,
+// conversion, proxy fence and arrival overlaps the other's.  Barriers: FULLA / EMPTYA (A ring), FULLB /
+// EMPTYB (code ring, released by the converter warps), BREADY / BEMPTY (bf16 buffers, freed by the MMA's
+// commit), TFULL / TEMPTY (accumulators), LAST.
 constexpr int kF8ARing = 4;     // A tiles come from L2: a few stages cover its latency
-constexpr int kF8BRingMax = 8;  // code tiles come from DRAM: as many as fit
-constexpr int kF8Bufs = 2;
+constexpr int kF8BRingMax = 12;  // code tiles come from DRAM: as many as fit
+#ifndef MOE_F8_SWAP_GROUPS
+#define MOE_F8_SWAP_GROUPS 2
+#endif
+#ifndef MOE_F8_SWAP_BUFS
+#define MOE_F8_SWAP_BUFS 4
+#endif
+// widened-weight buffers (bf16 tiles in shared memory; in the swapped kernel, A operands in tensor memory)
+// and converter groups: each group widens every kGroups-th K block, so that the groups' chains of waits,
+// loads, conversion, fence and arrival overlap; a group needs a buffer of its own
+__host__ __device__ constexpr int f8_bufs(bool swap) { return swap ? MOE_F8_SWAP_BUFS : 2; }
+__host__ __device__ constexpr int f8_groups(bool swap) { return swap ? MOE_F8_SWAP_GROUPS : 1; }
 constexpr uint32_t kB8Bytes = kBN * kBK;  // 16 KiB of codes per K block
-constexpr int kF8ConvWarps = 8;
-constexpr int kF8Threads = kThreads + 32 * kF8ConvWarps + 32;  // + converters + the A producer: 480
+// converter warps: 8 in the 128-row kernel (its registers allow no more); 8 per group in the swapped one
+// (a warp per lane quarter and half of the 256-row tile)
+__host__ __device__ constexpr int f8_conv_warps(bool swap) { return swap ? 8 * f8_groups(true) : 8; }
+// + the converters + the A producer: 480 threads (swapped kernel, two groups: 736)
+__host__ __device__ constexpr int f8_threads(bool swap) { return kThreads + 32 * f8_conv_warps(swap) + 32; }
 constexpr int kF8Block = 128;                                  // scale block edge
+constexpr int kSwapRows = 64;                                  // swapped kernel: rows per tile (MMA N)
+constexpr uint32_t kSwapABytes = kSwapRows * kBK * 2;          // its A tiles: 8 KiB
+constexpr int kSwapTmemA = 256;  // swapped kernel: first tensor-memory column of the widened weights
 
 // 16 E4M3 codes (one row's K block of 16) times `scale` -> 16 bf16 in two 16-byte chunks
 __device__ __forceinline__ void e4m3x16_to_bf16(const uint4 v, float scale, uint4& lo, uint4& hi) {
@@ -718,18 +747,31 @@ __device__ __forceinline__ void e4m3x16_to_bf16(const uint4 v, float scale, uint
     hi = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
-__global__ void __launch_bounds__(kF8Threads, 1)
+// kSwap (few rows per expert, e.g. decode): the roles of the operands swap.  The weights become the MMA's
+// M side (two M = 128 halves of the 256-row code tile) and the expert's rows the N side, 64 rows a tile
+// (a 64-row chunk of the expert's segment; chunks past its last real row are skipped by every role), so
+// the tensor work per weight byte follows the real rows instead of 128-row padded tiles; the epilogue
+// reads the accumulator transposed (a lane per output feature, a column per row).
+template <bool kSwap>
+__global__ void __launch_bounds__(f8_threads(kSwap), 1)
     gemm_fp8w_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB8,
                      const TcArgs a) {
     extern __shared__ uint8_t smem_raw[];
+    constexpr int kConvWarps = f8_conv_warps(kSwap), kNThreads = f8_threads(kSwap);
+    constexpr int kBufs = f8_bufs(kSwap), kGroups = f8_groups(kSwap), kGroupWarps = kConvWarps / kGroups;
+    static_assert(kGroups >= 1 && kBufs >= kGroups && kBufs >= 2 && kConvWarps % kGroups == 0 &&
+                      (1024 % (32 * kGroupWarps)) == 0 && kGroupWarps <= 16,
+                  "converter groups");
+    static_assert(!kSwap || (kGroupWarps == 8 && kSwapTmemA + kBufs * 64 <= 512), "swapped kernel's tensor memory");
     const int NB = a.stages;  // depth of the code ring (host: as deep as shared memory allows, <= 8)
     uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    constexpr uint32_t kASlot = kSwap ? kSwapABytes : kABytes;
     uint8_t* sA = base;                              // [kF8ARing] bf16 A tiles, 128-byte swizzle
-    uint8_t* sBb = sA + kF8ARing * kABytes;          // [kF8Bufs] bf16 B tiles, 128-byte swizzle
-    uint8_t* sB8 = sBb + kF8Bufs * kBBytes;          // [NB] code tiles
+    uint8_t* sBb = sA + kF8ARing * kASlot;           // [kBufs] bf16 B tiles, 128-byte swizzle (not swapped)
+    uint8_t* sB8 = sBb + (kSwap ? 0 : kBufs * kBBytes);  // [NB] code tiles (swapped: 64-byte swizzle)
     uint64_t* bars = reinterpret_cast<uint64_t*>(sB8 + NB * kB8Bytes);
-    const int FULLA = 0, EMPTYA = kF8ARing, BREADY = 2 * kF8ARing, BEMPTY = BREADY + kF8Bufs,
-              TFULL = BEMPTY + kF8Bufs, TEMPTY = TFULL + 2, LAST = TEMPTY + 2, FULLB = LAST + 1, EMPTYB = FULLB + NB,
+    const int FULLA = 0, EMPTYA = kF8ARing, BREADY = 2 * kF8ARing, BEMPTY = BREADY + kBufs,
+              TFULL = BEMPTY + kBufs, TEMPTY = TFULL + 2, LAST = TEMPTY + 2, FULLB = LAST + 1, EMPTYB = FULLB + NB,
               NBARS = EMPTYB + NB;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + NBARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
@@ -747,8 +789,8 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             mbar_init(bar(FULLA + i), 1);
             mbar_init(bar(EMPTYA + i), 1);
         }
-        for (int i = 0; i < kF8Bufs; ++i) {
-            mbar_init(bar(BREADY + i), kF8ConvWarps);
+        for (int i = 0; i < kBufs; ++i) {
+            mbar_init(bar(BREADY + i), kGroupWarps);
             mbar_init(bar(BEMPTY + i), 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -758,25 +800,36 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         mbar_init(bar(LAST), 1);
         for (int i = 0; i < NB; ++i) {
             mbar_init(bar(FULLB + i), 1);
-            mbar_init(bar(EMPTYB + i), kF8ConvWarps);
+            mbar_init(bar(EMPTYB + i), kGroupWarps);
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == 1) tmem_alloc(smem_u32(tmem_holder), kTmemCols);
+    // swapped: 2 accumulators x 2 halves x 64 rows, then kBufs widened A operands (2 halves x 32 columns)
+    constexpr uint32_t kCols = kTmemCols;
+    if (warp == 1) tmem_alloc(smem_u32(tmem_holder), kCols);
     pdl_wait();
     pdl_trigger();
-    for (int i = threadIdx.x; i <= a.E; i += kF8Threads) s_off[i] = a.offset[i];
+    for (int i = threadIdx.x; i <= a.E; i += kNThreads) s_off[i] = a.offset[i];
     fence_before();
     __syncthreads();
     fence_after();
     const uint32_t tmem_base = *tmem_holder;
 
     const int total_rows = s_off[a.E];
-    const int m_tiles = total_rows / kBM;
+    constexpr int kRowsPerTile = kSwap ? kSwapRows : kBM;
+    const int m_tiles = total_rows / kRowsPerTile;
     const int n_tiles = (a.N + kBN - 1) / kBN;
     const int num_tiles = m_tiles * n_tiles;
     const int k_iters = a.K / kBK;
-    const int a_warp = kF8Threads / 32 - 1;  // the last warp issues the A loads
+    // tile -> first row, first weight row, expert; a swapped tile whose first row is padding holds no real
+    // row (real rows are a prefix of each segment) and is skipped by every role alike
+    auto tile_at = [&](int tile, int& m0, int& n0, int& e) {
+        m0 = (tile / n_tiles) * kRowsPerTile;
+        n0 = (tile % n_tiles) * kBN;
+        e = expert_of_row(s_off, a.E, m0);
+        return !kSwap || a.row_token[m0] >= 0;
+    };
+    const int a_warp = kNThreads / 32 - 1;  // the last warp issues the A loads
 
     if (warp == 0 || warp == a_warp) {
         // warp 0: the code tiles, NB deep; the last warp: the A tiles, kF8ARing deep
@@ -791,16 +844,16 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             for (int i = 0; i < kF8BRingMax; ++i) { issued[i] = false; issued_phase[i] = 0; }
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-                const int m0 = (tile / n_tiles) * kBM, n0 = (tile % n_tiles) * kBN;
-                const int e = expert_of_row(s_off, a.E, m0);
+                int m0, n0, e;
+                if (!tile_at(tile, m0, n0, e)) continue;
                 for (int kb = 0; kb < k_iters; ++kb) {
                     if (!mbar_wait(bar(EMPTY + stage), phase ^ 1u, abort_flag)) { ok = false; break; }
                     if (is_b) {
                         mbar_expect_tx(bar(FULL + stage), kB8Bytes);
                         tma_load_3d(smem_u32(sB8 + stage * kB8Bytes), &tmB8, bar(FULL + stage), kb * kBK, n0, e);
                     } else {
-                        mbar_expect_tx(bar(FULL + stage), kABytes);
-                        tma_load_2d(smem_u32(sA + stage * kABytes), &tmA, bar(FULL + stage), kb * kBK, m0);
+                        mbar_expect_tx(bar(FULL + stage), kASlot);
+                        tma_load_2d(smem_u32(sA + stage * kASlot), &tmA, bar(FULL + stage), kb * kBK, m0);
                     }
                     issued[stage] = true;
                     issued_phase[stage] = phase;
@@ -816,17 +869,20 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16(kBM, kBN);
+            constexpr uint32_t idesc = kSwap ? idesc_bf16(128, kSwapRows) : idesc_bf16(kBM, kBN);
             int stage = 0, buf = 0;
             uint32_t phase = 0, bphase = 0;
             int local = 0;
             bool ok = true, any = false;
-            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x, ++local) {
+            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+                int m0, n0, e;
+                if (!tile_at(tile, m0, n0, e)) continue;
                 const int acc = local & 1;
                 const uint32_t acc_phase = (local >> 1) & 1;
+                ++local;
                 if (!mbar_wait(bar(TEMPTY + acc), acc_phase ^ 1u, abort_flag)) { ok = false; break; }
                 fence_after();
-                const uint32_t d_tmem = tmem_base + acc * kBN;
+                const uint32_t d_tmem = tmem_base + acc * (kSwap ? 2 * kSwapRows : kBN);
                 for (int kb = 0; kb < k_iters; ++kb) {
                     if (!mbar_wait(bar(FULLA + stage), phase, abort_flag) ||
                         !mbar_wait(bar(BREADY + buf), bphase, abort_flag)) {
@@ -834,16 +890,28 @@ __global__ void __launch_bounds__(kF8Threads, 1)
                         break;
                     }
                     fence_after();
-                    const uint64_t ad = smem_desc_sw128(smem_u32(sA + stage * kABytes));
+                    const uint64_t ad = smem_desc_sw128(smem_u32(sA + stage * kASlot));
                     const uint64_t bd = smem_desc_sw128(smem_u32(sBb + buf * kBBytes));
+                    if constexpr (kSwap) {
+                        // D[half] (128 weight rows x 64 rows) += W[half] (A operand, tensor memory: 32 columns
+                        // of bf16 pairs per half, 8 per K step of 16) x X^T (B operand, shared memory)
+                        const uint32_t wa = tmem_base + (uint32_t)(kSwapTmemA + buf * 64);
 #pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk)
-                        mma_bf16(d_tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc, (kb | kk) != 0);
+                        for (int kk = 0; kk < kBK / 16; ++kk) {
+                            mma_bf16_tmem_a(d_tmem, wa + kk * 8, ad + (uint64_t)(kk * 2), idesc, (kb | kk) != 0);
+                            mma_bf16_tmem_a(d_tmem + kSwapRows, wa + 32 + kk * 8, ad + (uint64_t)(kk * 2), idesc,
+                                            (kb | kk) != 0);
+                        }
+                    } else {
+#pragma unroll
+                        for (int kk = 0; kk < kBK / 16; ++kk)
+                            mma_bf16(d_tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc, (kb | kk) != 0);
+                    }
                     any = true;
                     commit(bar(EMPTYA + stage));
                     commit(bar(BEMPTY + buf));
                     if (++stage == kF8ARing) { stage = 0; phase ^= 1u; }
-                    if (++buf == kF8Bufs) { buf = 0; bphase ^= 1u; }
+                    if (++buf == kBufs) { buf = 0; bphase ^= 1u; }
                 }
                 if (ok) commit(bar(TFULL + acc));
             }
@@ -855,6 +923,60 @@ __global__ void __launch_bounds__(kF8Threads, 1)
                 commit(bar(LAST));
                 mbar_wait_bounded(bar(LAST), 0);
             }
+        }
+    } else if (kSwap && warp < kThreads / 32) {
+        // a lane per output feature n (TMEM lane), a column per row of the 64-row chunk
+        const int q = warp & 3;
+        const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+        int local = 0;
+        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+            int m0, n0, e;
+            if (!tile_at(tile, m0, n0, e)) continue;
+            const int acc = local & 1;
+            const uint32_t acc_phase = (local >> 1) & 1;
+            ++local;
+            const int tok_lo = a.row_token[m0 + lane], tok_hi = a.row_token[m0 + 32 + lane];
+            const float g_lo = (a.mode == 2 && tok_lo >= 0) ? a.row_gate[m0 + lane] : 0.f;
+            const float g_hi = (a.mode == 2 && tok_hi >= 0) ? a.row_gate[m0 + 32 + lane] : 0.f;
+            const bool ok = __all_sync(0xffffffffu, mbar_wait(bar(TFULL + acc), acc_phase, abort_flag));
+            if (!ok) {
+                if (lane == 0) {
+                    record_error(a.err, kErrTimeout, kWhereGemmEpilogue);
+                    *abort_flag = 1;
+                }
+                break;
+            }
+            fence_after();
+#pragma unroll 1
+            for (int hf = 0; hf < 2; ++hf) {
+                const int n = n0 + hf * 128 + q * 32 + lane;
+                const float bn = (a.bias != nullptr && n < a.N) ? bf16_to_f32(a.bias[(size_t)e * a.N + n]) : 0.f;
+#pragma unroll 1
+                for (int jh = 0; jh < 2; ++jh) {
+                    uint32_t v[32];
+                    __syncwarp();
+                    tmem_ld32(tmem_base + lane_base + (uint32_t)(acc * 2 * kSwapRows + hf * kSwapRows + jh * 32), v);
+                    for (int j = 0; j < 32; ++j) {
+                        const int tok = __shfl_sync(0xffffffffu, jh ? tok_hi : tok_lo, j);
+                        if (tok < 0) continue;  // padding row (the same for the whole warp)
+                        const float gj = __shfl_sync(0xffffffffu, jh ? g_hi : g_lo, j);
+                        if (n >= a.N) continue;
+                        const int r = m0 + jh * 32 + j;
+                        const float f = __uint_as_float(v[j]) + bn;
+                        if (a.mode == 0) {
+                            static_cast<bf16_t*>(a.C)[(size_t)r * a.N + n] =
+                                (bf16_t)(pack_bf16x2(gelu_erf(f), 0.f) & 0xffffu);
+                        } else if (a.mode == 1) {
+                            static_cast<float*>(a.C)[(size_t)r * a.N + n] = f;
+                        } else {
+                            atomicAdd(a.out + (size_t)tok * a.N + n, gj * f);
+                        }
+                    }
+                }
+            }
+            fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(TEMPTY + acc));
         }
     } else if (warp < kThreads / 32) {
         const int q = warp & 3;
@@ -884,20 +1006,92 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(TEMPTY + acc));
         }
-    } else {
-        // converter warps: thread ct handles 16-byte pieces ct, ct + 256, ct + 512, ct + 768 of the
-        // 256 x 64 codes (row = piece / 4, K bytes 16 * (piece % 4) ..), rows 64 apart
-        const int ct = threadIdx.x - kThreads;
-        const int r0 = ct >> 2, j = ct & 3;
+    } else if constexpr (kSwap) {
+        // converter warps (swapped kernel), kGroups groups of 8: group g widens the K blocks whose running count
+        // over the CTA's tiles is g mod kGroups.  Warp (half hf, lane quarter q) widens weight rows
+        // hf * 128 + q * 32 + lane: each thread one row of 64 codes (four 16-byte chunks; the 64-byte swizzle of
+        // the code tiles puts chunk c of row r at c ^ ((r >> 1) & 3), so a quarter warp's loads hit all banks),
+        // and stores its 32 bf16 pairs into its lane of the tensor-memory A operand.
+        const int cw = warp - kThreads / 32;
+        const int grp = cw / 8, hf = (cw % 8) >> 2, q = warp & 3;
+        const int row = hf * 128 + q * 32 + lane;
+        const int swz = (row >> 1) & 3;
+        const uint32_t tl = (uint32_t)(q * 32) << 16;
         const int nbn = a.N / kF8Block, nbk = a.K / kF8Block;
-        int stage = 0, buf = 0;
+        int stage = grp, buf = grp;
         uint32_t phase = 0, bphase = 0;
+        int count = 0;
         bool ok = true;
         for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-            const int m0 = (tile / n_tiles) * kBM, n0 = (tile % n_tiles) * kBN;
-            const int e = expert_of_row(s_off, a.E, m0);
+            int m0, n0, e;
+            if (!tile_at(tile, m0, n0, e)) continue;
+            // this row's 128-row scale block (rows past N are zero codes); its scale for the group's next K
+            // block is loaded one iteration ahead
+            const int nb = n0 / kF8Block + hf;
+            const float* sp = a.scale + ((size_t)e * nbn + nb) * nbk;
+            const bool has = nb < nbn;
+            const int kb_first = (grp - count % kGroups + kGroups) % kGroups;
+            count += k_iters;
+            float nsc = 0.f;
+            if (has && kb_first < k_iters) nsc = __ldg(sp + (kb_first * kBK) / kF8Block);
+            for (int kb = kb_first; kb < k_iters; kb += kGroups) {
+                const float sc = nsc;
+                if (has && kb + kGroups < k_iters) nsc = __ldg(sp + ((kb + kGroups) * kBK) / kF8Block);
+                const bool got = mbar_wait(bar(FULLB + stage), phase, abort_flag) &&
+                                 mbar_wait(bar(BEMPTY + buf), bphase ^ 1u, abort_flag);
+                if (!__all_sync(0xffffffffu, got)) {
+                    ok = false;
+                    break;
+                }
+                fence_after();  // the MMAs that read this buffer before have finished (their commit)
+                const uint8_t* src = sB8 + stage * kB8Bytes + row * kBK;
+                uint4 v[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) v[c] = *reinterpret_cast<const uint4*>(src + ((c ^ swz) << 4));
+                uint32_t o[32];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint4 lo, hi;
+                    e4m3x16_to_bf16(v[c], sc, lo, hi);
+                    o[8 * c + 0] = lo.x; o[8 * c + 1] = lo.y; o[8 * c + 2] = lo.z; o[8 * c + 3] = lo.w;
+                    o[8 * c + 4] = hi.x; o[8 * c + 5] = hi.y; o[8 * c + 6] = hi.z; o[8 * c + 7] = hi.w;
+                }
+                tmem_st32(tmem_base + tl + (uint32_t)(kSwapTmemA + buf * 64 + hf * 32), o);
+                tmem_wait_st();
+                fence_before();  // the MMA thread reads these columns after the barrier below
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(bar(BREADY + buf));
+                    mbar_arrive(bar(EMPTYB + stage));
+                }
+                stage += kGroups;
+                if (stage >= NB) { stage -= NB; phase ^= 1u; }
+                buf += kGroups;
+                if (buf >= kBufs) { buf -= kBufs; bphase ^= 1u; }
+            }
+        }
+        if (!ok && lane == 0) {
+            record_error(a.err, kErrTimeout, kWhereGemmProducer);
+            *abort_flag = 1;
+        }
+    } else {
+        // converter warps, kGroups groups of kGroupWarps: group g widens the K blocks whose running count over
+        // the CTA's tiles is g mod kGroups; its thread gt handles the 16-byte pieces gt + i * 32 * kGroupWarps
+        // of the 256 x 64 codes (row = piece / 4, K bytes 16 * (piece % 4) ..), rows 8 * kGroupWarps apart
+        constexpr int kPieces = 1024 / (32 * kGroupWarps), kRowStep = 8 * kGroupWarps;
+        const int ct = threadIdx.x - kThreads;
+        const int grp = ct / (32 * kGroupWarps), gt = ct % (32 * kGroupWarps);
+        const int r0 = gt >> 2, j = gt & 3;
+        const int nbn = a.N / kF8Block, nbk = a.K / kF8Block;
+        int stage = grp, buf = grp;  // ring positions of K block number grp (the host keeps NB >= kGroups)
+        uint32_t phase = 0, bphase = 0;
+        int count = 0;  // K blocks of the tiles before this one
+        bool ok = true;
+        for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+            int m0, n0, e;
+            if (!tile_at(tile, m0, n0, e)) continue;
             // the two 128-row scale blocks of this tile's 256 weight rows (rows past N are zero codes); the
-            // scales of the next K block are loaded one iteration ahead, so their latency stays hidden
+            // scales of the group's next K block are loaded one of its iterations ahead
             const int nb0 = n0 / kF8Block;
             const float* sp = a.scale + ((size_t)e * nbn) * nbk;
             auto load_scales = [&](int kb_, float& s0, float& s1) {
@@ -905,11 +1099,13 @@ __global__ void __launch_bounds__(kF8Threads, 1)
                 s0 = nb0 < nbn ? __ldg(sp + (size_t)nb0 * nbk + kbs) : 0.f;
                 s1 = nb0 + 1 < nbn ? __ldg(sp + (size_t)(nb0 + 1) * nbk + kbs) : 0.f;
             };
-            float nsc0, nsc1;
-            load_scales(0, nsc0, nsc1);
-            for (int kb = 0; kb < k_iters; ++kb) {
+            const int kb_first = (grp - count % kGroups + kGroups) % kGroups;
+            count += k_iters;
+            float nsc0 = 0.f, nsc1 = 0.f;
+            if (kb_first < k_iters) load_scales(kb_first, nsc0, nsc1);
+            for (int kb = kb_first; kb < k_iters; kb += kGroups) {
                 const float sc0 = nsc0, sc1 = nsc1;
-                if (kb + 1 < k_iters) load_scales(kb + 1, nsc0, nsc1);
+                if (kb + kGroups < k_iters) load_scales(kb + kGroups, nsc0, nsc1);
                 const bool got = mbar_wait(bar(FULLB + stage), phase, abort_flag) &&
                                  mbar_wait(bar(BEMPTY + buf), bphase ^ 1u, abort_flag);
                 if (!__all_sync(0xffffffffu, got)) {
@@ -919,11 +1115,11 @@ __global__ void __launch_bounds__(kF8Threads, 1)
                 const uint8_t* src = sB8 + stage * kB8Bytes;
                 uint8_t* dst = sBb + buf * kBBytes;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int r = r0 + 64 * i;
+                for (int i = 0; i < kPieces; ++i) {
+                    const int r = r0 + kRowStep * i;
                     const uint4 v = *reinterpret_cast<const uint4*>(src + r * kBK + j * 16);
                     uint4 lo, hi;
-                    e4m3x16_to_bf16(v, i < 2 ? sc0 : sc1, lo, hi);
+                    e4m3x16_to_bf16(v, r < kF8Block ? sc0 : sc1, lo, hi);
                     uint8_t* drow = dst + (r >> 3) * 1024 + (r & 7) * 128;
                     *reinterpret_cast<uint4*>(drow + (((2 * j) ^ (r & 7)) << 4)) = lo;
                     *reinterpret_cast<uint4*>(drow + (((2 * j + 1) ^ (r & 7)) << 4)) = hi;
@@ -934,8 +1130,10 @@ __global__ void __launch_bounds__(kF8Threads, 1)
                     mbar_arrive(bar(BREADY + buf));
                     mbar_arrive(bar(EMPTYB + stage));  // the code tile is read: its stage may refill
                 }
-                if (++stage == NB) { stage = 0; phase ^= 1u; }
-                if (++buf == kF8Bufs) { buf = 0; bphase ^= 1u; }
+                stage += kGroups;
+                if (stage >= NB) { stage -= NB; phase ^= 1u; }
+                buf += kGroups;
+                if (buf >= kBufs) { buf -= kBufs; bphase ^= 1u; }
             }
         }
         if (!ok && lane == 0) {
@@ -946,7 +1144,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
     fence_before();
     __syncthreads();
     fence_after();
-    if (warp == 1) tmem_free(tmem_base, kTmemCols);
+    if (warp == 1) tmem_free(tmem_base, kCols);
 }
 
 // ---- host side ----------------------------------------------------------------------------------
@@ -968,7 +1166,7 @@ struct MapKey {
     const void* ptr;
     uint64_t d0, d1, d2;
     uint32_t b1;
-    uint32_t kind;  // 0: bf16, 128-byte swizzle; 1: bytes, no swizzle
+    uint32_t kind;  // 0: bf16, 128-byte swizzle; 1: bytes, no swizzle; 2: bytes, 64-byte swizzle
     bool operator==(const MapKey& o) const {
         return ptr == o.ptr && d0 == o.d0 && d1 == o.d1 && d2 == o.d2 && b1 == o.b1 && kind == o.kind;
     }
@@ -1001,7 +1199,8 @@ bool tma_map_kind(const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2, uint32
     cuuint32_t es[3] = {1, 1, 1};
     CUresult r = fn(&m, kind == 0 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, rank,
                     const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    kind == 0 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                    kind == 0 ? CU_TENSOR_MAP_SWIZZLE_128B
+                              : (kind == 2 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE),
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return false;
     MapEntry& slot = g_maps[g_maps_next];
@@ -1091,15 +1290,17 @@ cudaError_t launch_wgrad_tc(const WgradParams& P, cudaStream_t s) {
     return launch_pdl(gemm_wgrad_kernel, dim3(grid), dim3(kThreads), smem, s, ma, mb, a);
 }
 
-size_t ffn_fp8_smem_bytes(int E, bool bias, int nb) {
-    return 1024 + (size_t)kF8ARing * kABytes + (size_t)kF8Bufs * kBBytes + (size_t)nb * kB8Bytes +
-           (2 * kF8ARing + 2 * kF8Bufs + 5 + 2 * nb) * 8 + 16 + 4 * (size_t)(E + 1) + (bias ? kBiasSmem : 0);
+size_t ffn_fp8_smem_bytes(int E, bool bias, int nb, bool swap) {
+    return 1024 + (size_t)kF8ARing * (swap ? kSwapABytes : kABytes) + (swap ? 0 : (size_t)f8_bufs(swap) * kBBytes) +
+           (size_t)nb * kB8Bytes + (2 * kF8ARing + 2 * f8_bufs(swap) + 5 + 2 * nb) * 8 + 16 +
+           4 * (size_t)(E + 1) + (bias && !swap ? kBiasSmem : 0);
 }
 
-// the code ring as deep as shared memory allows (at most kF8BRingMax, at least 2)
-int fp8_ring_depth(int E, bool bias) {
+// the code ring as deep as shared memory allows (at most kF8BRingMax, at least 2 and the converter groups)
+int fp8_ring_depth(int E, bool bias, bool swap) {
+    const int lo = f8_groups(swap) > 2 ? f8_groups(swap) : 2;
     int nb = kF8BRingMax;
-    while (nb > 2 && ffn_fp8_smem_bytes(E, bias, nb) > 227 * 1024) --nb;
+    while (nb > lo && ffn_fp8_smem_bytes(E, bias, nb, swap) > 227 * 1024) --nb;
     return nb;
 }
 
@@ -1107,23 +1308,35 @@ cudaError_t launch_ffn_tc(const FfnParams& P, cudaStream_t s) {
     if (!P.bf16) return cudaErrorInvalidValue;
     if (P.rows_cap <= 0) return cudaSuccess;
     CUtensorMap ma, mb;
-    if (!tma_map_bf16(P.A, (uint64_t)P.K, (uint64_t)P.rows_cap, 0, kBM, &ma)) return cudaErrorInvalidValue;
     if (P.w_scale != nullptr) {  // block-FP8 weights: byte codes, single-SM tiles
         if (P.K % kF8Block || P.N % kF8Block) return cudaErrorInvalidValue;
-        if (!tma_map_kind(P.W, (uint64_t)P.K, (uint64_t)P.N, (uint64_t)P.E, kBN, 1, &mb)) return cudaErrorInvalidValue;
-        const int nb = fp8_ring_depth(P.E, P.bias != nullptr);
+        // no expert holds more than 64 rows (decode): the swapped kernel, 64-row chunks of each segment
+        const bool swap = P.max_rows > 0 && P.max_rows <= kSwapRows;
+        const int rows_box = swap ? kSwapRows : kBM;
+        if (!tma_map_bf16(P.A, (uint64_t)P.K, (uint64_t)P.rows_cap, 0, rows_box, &ma)) return cudaErrorInvalidValue;
+        if (!tma_map_kind(P.W, (uint64_t)P.K, (uint64_t)P.N, (uint64_t)P.E, kBN, swap ? 2 : 1, &mb))
+            return cudaErrorInvalidValue;
+        const bool bias = P.bias != nullptr;
+        const int nb = fp8_ring_depth(P.E, bias, swap);
         TcArgs a8{P.offset, P.row_token, P.row_gate, static_cast<const bf16_t*>(P.bias), P.C, P.out,
                   P.E, P.K, P.N, P.mode, P.err, P.w_scale, nb, static_cast<bf16_t*>(P.aux), 0};
-        const size_t smem8 = ffn_fp8_smem_bytes(P.E, P.bias != nullptr, nb);
+        const size_t smem8 = ffn_fp8_smem_bytes(P.E, bias, nb, swap);
         if (smem8 > 227 * 1024) return cudaErrorInvalidValue;
-        cudaError_t e8 = cudaFuncSetAttribute(gemm_fp8w_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem8);
+        auto kern8 = swap ? gemm_fp8w_kernel<true> : gemm_fp8w_kernel<false>;
+        cudaError_t e8 = cudaFuncSetAttribute(kern8, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem8);
         if (e8 != cudaSuccess) return e8;
-        const int64_t tiles8 = (P.rows_cap / kBM) * (int64_t)((P.N + kBN - 1) / kBN);
+        const int64_t tiles8 = (P.rows_cap / rows_box) * (int64_t)((P.N + kBN - 1) / kBN);
         int grid8 = device_sm_count();
         if (tiles8 < grid8) grid8 = (int)(tiles8 > 0 ? tiles8 : 1);
-        return launch_pdl(gemm_fp8w_kernel, dim3(grid8), dim3(kF8Threads), smem8, s, ma, mb, a8);
+        return launch_pdl(kern8, dim3(grid8), dim3(f8_threads(swap)), smem8, s, ma, mb, a8);
     }
-    if (!tma_map_bf16(P.W, (uint64_t)P.K, (uint64_t)P.N, (uint64_t)P.E, kBN, &mb)) return cudaErrorInvalidValue;
+    if (!tma_map_bf16(P.A, (uint64_t)P.K, (uint64_t)P.rows_cap, 0, kBM, &ma)) return cudaErrorInvalidValue;
+    if (P.w_kn) {  // W [E, K, N]: boxes of 64 N-columns x 64 K-rows, single-SM kernel only
+        if (P.pair || P.N % 64) return cudaErrorInvalidValue;
+        if (!tma_map_bf16(P.W, (uint64_t)P.N, (uint64_t)P.K, (uint64_t)P.E, 64, &mb)) return cudaErrorInvalidValue;
+    } else if (!tma_map_bf16(P.W, (uint64_t)P.K, (uint64_t)P.N, (uint64_t)P.E, kBN, &mb)) {
+        return cudaErrorInvalidValue;
+    }
     TcArgs a;
     a.offset = P.offset;
     a.row_token = P.row_token;
@@ -1140,6 +1353,7 @@ cudaError_t launch_ffn_tc(const FfnParams& P, cudaStream_t s) {
     a.stages = kStages;
     a.aux = static_cast<bf16_t*>(P.aux);
     a.M = 0;
+    a.b_mn = P.w_kn;
     if (P.pair) {
         // pairs of SMs: B boxes of 128 weight rows (half of a 256-wide tile), grid = 2 x the clusters that fit
         CUtensorMap mb2;

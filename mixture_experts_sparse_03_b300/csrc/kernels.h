@@ -136,8 +136,10 @@ struct FfnParams {
     int* err;
     const float* w_scale;     // block-FP8 weights: W holds E4M3 codes, w_scale [E, N/128, K/128]; else nullptr
     void* aux;                // modes 3 / 4 (backward): pre-activations Z [rows, N] bf16
+    int max_rows;             // most rows any expert holds (its capacity, at most the token count); 0: unknown
+    int w_kn;                 // W is [E, K, N] instead (bf16, single-SM tensor-core kernel): read MN-major
 };
-size_t ffn_fp8_smem_bytes(int E, bool bias, int ring);
+size_t ffn_fp8_smem_bytes(int E, bool bias, int ring, bool swap);
 // weight gradients grouped along K (ffn_tc.cu): dW[e] [M, N] fp32 = sum over the rows r of expert e
 // (offset[e] <= r < offset[e+1], multiples of 128) of At[m][r] Bt[n][r]; At [M, rows], Bt [N, rows] bf16
 struct WgradParams {

@@ -141,3 +141,60 @@ def test_full_size_decode_fp8():
     ref = oracle_out_fp8(wl, tc, tg, scores, idx, slot, toks)
     err = P.check_output(wl, out, ref, toks)
     print("decode fp8: max per-token relative error %.3e over %d tokens" % (err, wl.T))
+
+
+def _one_hot_fp8_layer(T, cap, rows_per_expert, seed):
+    """An FFN step whose every output is one dequantised W2 code times 8, so that the widening of the
+    codes is checked bit for bit.  Row r of expert e (local index i) holds the unit vector x = e_i; W1[e]
+    has the code of 8.0 (0x50, scale 1) at (j_i, i) and zeros elsewhere, so W1 x = 8 e_j and GELU(8)
+    rounds to 8 in bf16; then y = 8 * W2[e][:, j] exactly (one product per output, no bias).  W2's
+    columns cycle through all 254 non-NaN E4M3 codes (zeros, subnormals, both signs) and its 128 x 128
+    blocks carry different power-of-two scales."""
+    d, h, E = 128, 256, len(rows_per_expert)
+    wl = small_workload(T=T, d=d, h=h, E=E, k=1, capacity=cap, bias="none", weights="fp8_block")
+    c = b.config(wl)
+    rows = b.moe_dispatch_rows(c)
+    rng = np.random.default_rng(seed)
+    valid = np.array([v for v in range(256) if v not in (0x7F, 0xFF)], dtype=np.uint8)
+    off = np.zeros(E + 1, dtype=np.int32)
+    for e, n in enumerate(rows_per_expert):
+        off[e + 1] = off[e] + -(-n // 128) * 128
+    assert off[E] <= rows
+    xd = np.zeros((rows, d), dtype=np.float32)
+    rtok = np.full(rows, -1, dtype=np.int32)
+    w1 = np.zeros((E, h, d), dtype=np.uint8)
+    w2 = np.zeros((E, d, h), dtype=np.uint8)
+    jsel = {}
+    for e, n in enumerate(rows_per_expert):
+        js = rng.permutation(h)[:n]
+        for i in range(n):
+            r = off[e] + i
+            xd[r, i] = 1.0
+            rtok[r] = (e * 131 + i) % T
+            w1[e, js[i], i] = 0x50  # 8.0
+            jsel[r] = (e, js[i])
+        w2[e] = valid[(np.arange(d)[:, None] * 7 + np.arange(h)[None, :] * 3 + 17 * e) % len(valid)]
+    s1 = np.ones((E, h // 128, d // 128), dtype=np.float32)
+    s2 = np.ldexp(1.0, rng.integers(-12, 4, size=(E, d // 128, h // 128))).astype(np.float32)
+    w2dq = oracle.dequant_block_fp8(w2, s2)
+    expect = {r: 8.0 * w2dq[e, :, j] for r, (e, j) in jsel.items()}
+    ws = b.workspace(c, "cuda")
+    t = lambda a, dt=None: torch.as_tensor(a).to("cuda") if dt is None else torch.as_tensor(a).to("cuda", dt)  # noqa
+    y = torch.full((rows, d), float("nan"), dtype=torch.float32, device="cuda")
+    b.check(b.moe_expert_ffn_fp8(c, t(xd, torch.bfloat16), t(off), t(rtok), t(np.ones(rows, np.float32)), t(w1),
+                                 t(s1), None, t(w2), t(s2), None, y, None, ws, ws.numel()), "moe_expert_ffn_fp8")
+    st, info = b.moe_device_status(ws, ws.numel())
+    assert st == 0, (b.STATUS[st], info)
+    yh = y.cpu().numpy()
+    for r, ref in expect.items():
+        assert np.array_equal(yh[r], ref.astype(np.float32)), (r, np.flatnonzero(yh[r] != ref.astype(np.float32))[:8])
+
+
+@pytest.mark.parametrize("case", [
+    (64, 64, [64, 37, 1]),     # at most 64 rows per expert: the swapped kernel (64-row chunks)
+    (256, 128, [128, 100]),    # 128-row tiles
+    (256, 128, [65, 3, 128]),  # 128-row tiles, ragged
+], ids=["swapped", "tiles", "ragged"])
+def test_fp8_every_code_exact(case):
+    T, cap, rows_per_expert = case
+    _one_hot_fp8_layer(T, cap, rows_per_expert, seed=len(rows_per_expert))
