@@ -82,6 +82,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
     ap.add_argument("--only", action="store_true", help="measure the chosen workload only (no 'workloads' key)")
+    ap.add_argument("--skip-backward", action="store_true",
+                    help="profiling aid: leave out the backward timing (its CUDA-graph replay)")
     ap.add_argument("--experts", type=int, default=0,
                     help="profiling aid: the chosen workload with this many experts and T scaled to keep the rows "
                          "per expert (the same per-expert GEMM shapes on a smaller device footprint); implies --only")
@@ -738,7 +740,7 @@ def run_ours(args, rank, world, local):
 
     res, L = measure(wl, args, dev, stream, flush, world)
     router_stats = router_stats_timing(L, stream)
-    backward = backward_timing(L, flush, min(args.steps, 10))
+    backward = None if args.skip_backward else backward_timing(L, flush, min(args.steps, 10))
     e2e_value, h2d, d2h = e2e_timing(L, flush, args.steps, world)
 
     cpu = None
