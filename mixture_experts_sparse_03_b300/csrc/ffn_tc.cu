@@ -533,6 +533,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 // and Bt [N, rows] (2-D maps), so the MMAs are those of gemm_tc_kernel; padding rows are zero in both.
 // Tiles (e, m-tile, n-tile) are dealt to one CTA per SM; a tile of an expert without rows stores zeros.
 // The epilogue stores fp32 rows m < M of dW[e] (mode 1 of epilogue_cols on the row e * M + m).
+constexpr int kWgStageStride = 36;                                  // floats per staged row
+constexpr size_t kWgStageBytes = 4 * 32 * kWgStageStride * sizeof(float);  // 4 epilogue warps
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const TcArgs a) {
@@ -544,6 +546,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 5);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
     int* s_off = reinterpret_cast<int*>(tmem_holder + 4);
+    // per epilogue warp a 32 x 32 fp32 staging tile (rows 36 floats apart: conflict-free 16-byte accesses
+    // both row-wise and column-wise), so that each output row leaves as whole 128-byte lines
+    float* s_stage = reinterpret_cast<float*>(
+        (reinterpret_cast<uintptr_t>(s_off + a.E + 1) + 15) & ~static_cast<uintptr_t>(15));
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     auto bar = [&](int i) { return smem_u32(bars + i); };
@@ -675,8 +681,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             fence_after();
             if (nk > 0) {
-                epilogue_cols(a, tmem_base + lane_base + (uint32_t)(acc * kBN), e * a.M + m, m < a.M ? 0 : -1, 0.f,
-                              nullptr, n0, 0, kBN);
+                // each 32-column chunk: this thread's row into the staging tile, then 4 rows x 128 bytes per
+                // store instruction (8 lanes a row)
+                float* stg = s_stage + q * (32 * kWgStageStride);
+                const int mr = (lane & 7) * 4;
+#pragma unroll 1
+                for (int c0 = 0; c0 < kBN; c0 += 32) {
+                    uint32_t v[32];
+                    __syncwarp();
+                    tmem_ld32(tmem_base + lane_base + (uint32_t)(acc * kBN + c0), v);
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4)
+                        *reinterpret_cast<float4*>(stg + lane * kWgStageStride + j) =
+                            make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]), __uint_as_float(v[j + 2]),
+                                        __uint_as_float(v[j + 3]));
+                    __syncwarp();
+                    const int n = n0 + c0 + mr;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int rr = 4 * i + (lane >> 3);
+                        const int mrow = m0 + q * 32 + rr;
+                        const float4 val = *reinterpret_cast<const float4*>(stg + rr * kWgStageStride + mr);
+                        if (mrow < a.M && n < a.N)
+                            __stcs(reinterpret_cast<float4*>(static_cast<float*>(a.C) + ((size_t)e * a.M + mrow) * a.N + n),
+                                   val);
+                    }
+                }
             } else if (m < a.M) {  // an expert without rows: its gradient is zero
                 float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.C) + ((size_t)e * a.M + m) * a.N + n0);
                 for (int c = 0; c < kBN && n0 + c < a.N; c += 4) dst[c / 4] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -1281,7 +1311,9 @@ cudaError_t launch_wgrad_tc(const WgradParams& P, cudaStream_t s) {
     a.M = P.M;
     a.mode = 1;
     a.err = P.err;
-    const size_t smem = 1024 + (size_t)kStages * kStageBytes + (2 * kStages + 5) * 8 + 16 + 4 * (size_t)(P.E + 1);
+    const size_t smem = 1024 + (size_t)kStages * kStageBytes + (2 * kStages + 5) * 8 + 16 + 4 * (size_t)(P.E + 1) + 16 +
+                        kWgStageBytes;
+    if (smem > 227 * 1024) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(gemm_wgrad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int64_t tiles = (int64_t)P.E * ((P.M + kBM - 1) / kBM) * ((P.N + kBN - 1) / kBN);
