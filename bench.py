@@ -509,9 +509,9 @@ def measure(wl, args, dev, stream, flush, world):
     return res, L
 
 
-BWD_TAIL = ["fwd_up_keep_z", "fwd_down_y", "logits_gemm", "bwd_dy", "bwd_gate_grad", "bwd_dz_gemm", "bwd_dx_gemm", "iota_rows", "gate_weights_t", "bwd_dx_gate_gemm", "transpose_dy",
-            "transpose_h", "transpose_dz", "transpose_xd", "wgrad_w2", "wgrad_w1", "transpose_ds", "transpose_x",
-            "wgrad_gate", "colsum_db2", "colsum_db1"]
+BWD_TAIL = ["fwd_up_keep_z", "fwd_down_y", "logits_gemm", "bwd_dy", "bwd_gate_grad", "bwd_dz_gemm",
+            "bwd_dx_gemm", "iota_rows", "gate_weights_t", "bwd_dx_gate_gemm", "zero_pad_rows", "wgrad_w2",
+            "wgrad_w1", "wgrad_gate", "colsum_db2", "colsum_db1"]
 
 
 def backward_timing(L, flush, steps):

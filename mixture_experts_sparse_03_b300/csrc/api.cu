@@ -456,15 +456,13 @@ moe_status forward_impl(const moe_config* cfg, const void* x, const void* w_gate
 
 // ---- backward: its workspace after the forward's ------------------------------------------------------
 struct BwdPlan {
-    int Rp, Tp, Np, NpP;  // rows rounded to 64, tokens to 128, gate logits per token (and rounded to 64)
-    size_t o_z, o_dy, o_dz, o_xdT, o_hT, o_dyT, o_dzT, o_logits, o_dS, o_dST, o_xT, o_wcatT, o_dwcat, o_rows,
-        o_off2, total;
+    int Tp, Np, NpP;  // tokens rounded to 128, gate logits per token (and rounded to 64)
+    size_t o_z, o_dy, o_dz, o_logits, o_dS, o_wcatT, o_dwcat, o_rows, o_off2, total;
 };
 
 moe_status make_bwd_plan(const Plan& P, const moe_config* c, BwdPlan* B) {
     if (!P.bf16 || P.gate == MOE_GATE_COSINE || (c->flags & MOE_FLAG_SIMT_FFN)) return MOE_ERR_UNSUPPORTED;
     BwdPlan b{};
-    b.Rp = (int)((P.rows + 63) / 64 * 64);
     b.Tp = (P.T + 127) / 128 * 128;
     b.Np = P.gate == MOE_GATE_NOISY ? 2 * P.E : P.E;
     b.NpP = (b.Np + 63) / 64 * 64;
@@ -474,14 +472,8 @@ moe_status make_bwd_plan(const Plan& P, const moe_config* c, BwdPlan* B) {
     b.o_z = take(R * P.h * 2);
     b.o_dy = take(R * P.d * 2);
     b.o_dz = take(R * P.h * 2);
-    b.o_xdT = take((size_t)P.d * b.Rp * 2);
-    b.o_hT = take((size_t)P.h * b.Rp * 2);
-    b.o_dyT = take((size_t)P.d * b.Rp * 2);
-    b.o_dzT = take((size_t)P.h * b.Rp * 2);
     b.o_logits = take((size_t)P.T * b.Np * 4);
     b.o_dS = take((size_t)b.Tp * b.NpP * 2);
-    b.o_dST = take((size_t)b.NpP * b.Tp * 2);
-    b.o_xT = take((size_t)P.d * b.Tp * 2);
     b.o_wcatT = take((size_t)P.d * b.NpP * 2);
     b.o_dwcat = take((size_t)b.Np * P.d * 4);
     b.o_rows = take((size_t)b.Tp * 4);
@@ -568,29 +560,20 @@ moe_status backward_impl(const moe_config* cfg, const void* x, const void* w_gat
     dxg.A = dS; dxg.W = wcatT; dxg.offset = off2; dxg.row_token = rows_id; dxg.out = dx;
     dxg.E = 1; dxg.K = B.NpP; dxg.N = d; dxg.bf16 = 1; dxg.mode = 5; dxg.rows_cap = B.Tp; dxg.err = err;
     MOE_TRY(run_ffn(P, cfg, dxg, s));
-    // 5. weight gradients, contracting over each expert's rows: dW2 = dY^T H, dW1 = dZ^T X_d
-    void* xdT = at<void>(ws, B.o_xdT);
-    void* hT = at<void>(ws, B.o_hT);
-    void* dyT = at<void>(ws, B.o_dyT);
-    void* dzT = at<void>(ws, B.o_dzT);
-    MOE_TRY(launch(s, [&] { return launch_transpose(dy, dyT, 1, R, d, B.Rp, rtok, rows_used, s); }));
-    MOE_TRY(launch(s, [&] { return launch_transpose(hb, hT, 1, R, h, B.Rp, rtok, rows_used, s); }));
-    MOE_TRY(launch(s, [&] { return launch_transpose(dz, dzT, 1, R, h, B.Rp, rtok, rows_used, s); }));
-    MOE_TRY(launch(s, [&] { return launch_transpose(xd, xdT, 1, R, d, B.Rp, rtok, rows_used, s); }));
+    // 5. weight gradients, contracting over each expert's rows: dW2 = dY^T H, dW1 = dZ^T X_d, with the
+    //    operands read as stored ([rows, d] or [rows, h], MN-major); their padding rows are zeroed first (dY's
+    //    already are)
+    MOE_TRY(launch(s, [&] { return launch_zero_pad_rows(xd, d, hb, h, dz, h, R, rtok, rows_used, s); }));
     MOE_TRY(launch(s, [&] {
-        return launch_wgrad_tc(WgradParams{dyT, hT, off, dw2, E, d, h, (int64_t)B.Rp, err}, s);
+        return launch_wgrad_tc(WgradParams{dy, hb, off, dw2, E, d, h, (int64_t)R, (int64_t)R, err}, s);
     }));
     MOE_TRY(launch(s, [&] {
-        return launch_wgrad_tc(WgradParams{dzT, xdT, off, dw1, E, h, d, (int64_t)B.Rp, err}, s);
+        return launch_wgrad_tc(WgradParams{dz, xd, off, dw1, E, h, d, (int64_t)R, (int64_t)R, err}, s);
     }));
-    // 6. gate weight gradients: [dW_g ; dW_n] = dS^T x, contracting over the tokens
-    void* dST = at<void>(ws, B.o_dST);
-    void* xT = at<void>(ws, B.o_xT);
+    // 6. gate weight gradients: [dW_g ; dW_n] = dS^T x, contracting over the tokens (x's rows past T read as 0)
     float* dwcat = at<float>(ws, B.o_dwcat);
-    MOE_TRY(launch(s, [&] { return launch_transpose(dS, dST, 1, B.Tp, B.NpP, B.Tp, nullptr, nullptr, s); }));
-    MOE_TRY(launch(s, [&] { return launch_transpose(x, xT, 1, T, d, B.Tp, nullptr, nullptr, s); }));
     MOE_TRY(launch(s, [&] {
-        return launch_wgrad_tc(WgradParams{dST, xT, off2, dwcat, 1, B.Np, d, (int64_t)B.Tp, err}, s);
+        return launch_wgrad_tc(WgradParams{dS, x, off2, dwcat, 1, B.Np, d, (int64_t)B.Tp, (int64_t)T, err, B.NpP}, s);
     }));
     if (cudaMemcpyAsync(dw_gate, dwcat, (size_t)E * d * 4, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
         return MOE_ERR_CUDA;

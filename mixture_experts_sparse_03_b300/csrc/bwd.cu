@@ -7,8 +7,8 @@
 //   gate_grad_kernel  per token: dg_j = dout_t . y_r for its kept pairs, the scores' gradient through the
 //                     softmax (over the k chosen scores, or over all E), and for the noisy gate the noise
 //                     logits' gradient ds eps sigmoid(x W_n^T); a bf16 row [ds | dn | 0] per token
-//   transpose_kernel  K-major copies for the GEMMs that contract over rows (weight gradients) or over the
-//                     weights' other dimension (data gradients): [B][R][C] -> [B][C][Rp], masked rows zero
+//   zero_pad_rows     zeros in the padding rows of X_d, H and dZ, which the weight-gradient GEMMs contract
+//                     over together with the real rows
 //   segment_colsum    bias gradients: column sums of dY / dZ over each expert's row segment (fp32)
 #include "common.cuh"
 #include "kernels.h"
@@ -17,45 +17,23 @@ namespace moe {
 
 namespace {
 
-// dst[b][c][r] = src[b][r][c] for r < R (0 where row_mask[r] < 0), 0 for R <= r < Rp; with a mask, the rows
-// from *row_limit on (dispatched rows past the last expert's segment, whose row_token was never written)
-// are 0 too.  C and Rp are multiples of 64.  A 64 x 64 tile per block through shared memory: 16-byte
-// loads of 8 consecutive columns, and 32-byte stores of 16 consecutive rows of one output row (each
-// 4-byte word pairs two source rows); the tile's row stride of 33 words keeps both sides' shared-memory
-// accesses within two ways of bank conflict.
-constexpr int kT64 = 64, kTStride = 66;  // bf16 per shared row
-__global__ void __launch_bounds__(256) transpose_kernel(const bf16_t* __restrict__ src, bf16_t* __restrict__ dst,
-                                                       int R, int C, int Rp, const int* __restrict__ row_mask,
-                                                       const int* __restrict__ row_limit) {
-    __shared__ uint32_t tile[kT64 * kTStride / 2];
+// Padding rows (row_token < 0) below *row_limit of up to three bf16 buffers [rows, w_i] (w_i a multiple of 8,
+// or a null buffer) become zero: a warp per row, 16-byte stores; real rows are not touched.
+__global__ void __launch_bounds__(256) zero_pad_rows_kernel(bf16_t* __restrict__ p0, int w0, bf16_t* __restrict__ p1,
+                                                           int w1, bf16_t* __restrict__ p2, int w2, int rows,
+                                                           const int* __restrict__ row_token,
+                                                           const int* __restrict__ row_limit) {
     pdl_wait();
     pdl_trigger();
-    const int b = blockIdx.z, t = threadIdx.x;
-    const int r0 = blockIdx.y * kT64, c0 = blockIdx.x * kT64;
-    const bf16_t* s = src + (size_t)b * R * C;
-    bf16_t* o = dst + (size_t)b * C * Rp;
-    const int rl = row_mask != nullptr ? min(R, *row_limit) : R;
+    const int r = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (r >= rows || r >= *row_limit || row_token[r] >= 0) return;
+    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+    bf16_t* const ps[3] = {p0, p1, p2};
+    const int ws[3] = {w0, w1, w2};
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const int idx = t + 256 * i, row = idx >> 3, chunk = idx & 7, r = r0 + row;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (r < rl && (row_mask == nullptr || row_mask[r] >= 0))
-            v = __ldg(reinterpret_cast<const uint4*>(s + (size_t)r * C + c0 + chunk * 8));
-        uint32_t* w = tile + (row * kTStride + chunk * 8) / 2;
-        w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
-    }
-    __syncthreads();
-    const bf16_t* th = reinterpret_cast<const bf16_t*>(tile);
-    const int c = t >> 2, g = t & 3;  // output row c0 + c, its rows r0 + 16 g .. + 15
-    uint32_t wv[8];
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-        const int r = 16 * g + 2 * q;
-        wv[q] = (uint32_t)th[r * kTStride + c] | ((uint32_t)th[(r + 1) * kTStride + c] << 16);
-    }
-    uint4* out = reinterpret_cast<uint4*>(o + (size_t)(c0 + c) * Rp + r0 + 16 * g);
-    out[0] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-    out[1] = make_uint4(wv[4], wv[5], wv[6], wv[7]);
+    for (int b = 0; b < 3; ++b)
+        if (ps[b] != nullptr)
+            for (int c = lane * 8; c < ws[b]; c += 256) *reinterpret_cast<uint4*>(ps[b] + (size_t)r * ws[b] + c) = z;
 }
 
 // dY[r][:] = gate_r * dout[token_r][:] in bf16 (a warp per row, 8 columns per lane per step); rows of
@@ -203,14 +181,11 @@ __global__ void iota_rows_kernel(int* __restrict__ rows, int T, int Tp, int* __r
 
 }  // namespace
 
-cudaError_t launch_transpose(const void* src, void* dst, int B, int R, int C, int Rp, const int* row_mask,
-                             const int* row_limit, cudaStream_t s) {
-    if (B <= 0 || Rp <= 0 || C <= 0) return cudaSuccess;
-    if (row_mask != nullptr && row_limit == nullptr) return cudaErrorInvalidValue;
-    if (C % kT64 || Rp % kT64) return cudaErrorInvalidValue;
-    const dim3 grid(C / kT64, Rp / kT64, B), block(256);
-    return launch_pdl(transpose_kernel, grid, block, 0, s, static_cast<const bf16_t*>(src), static_cast<bf16_t*>(dst),
-                      R, C, Rp, row_mask, row_limit);
+cudaError_t launch_zero_pad_rows(void* p0, int w0, void* p1, int w1, void* p2, int w2, int rows,
+                                 const int* row_token, const int* row_limit, cudaStream_t s) {
+    if (rows <= 0) return cudaSuccess;
+    return launch_pdl(zero_pad_rows_kernel, dim3((rows + 7) / 8), dim3(256), 0, s, static_cast<bf16_t*>(p0), w0,
+                      static_cast<bf16_t*>(p1), w1, static_cast<bf16_t*>(p2), w2, rows, row_token, row_limit);
 }
 
 cudaError_t launch_bwd_dy(const float* dout, const int* row_token, const float* row_gate, int rows, int d,

@@ -529,10 +529,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 // ---- weight gradients: GEMMs grouped along K ------------------------------------------------------------
 // dW[e] [M, N] = sum over the dispatched rows r of expert e of A[r][m] B[r][n], i.e. the contraction runs over
-// the expert's own row segment [off[e], off[e+1]).  Both operands arrive transposed, K-major: At [M, rows]
-// and Bt [N, rows] (2-D maps), so the MMAs are those of gemm_tc_kernel; padding rows are zero in both.
-// Tiles (e, m-tile, n-tile) are dealt to one CTA per SM; a tile of an expert without rows stores zeros.
-// The epilogue stores fp32 rows m < M of dW[e] (mode 1 of epilogue_cols on the row e * M + m).
+// the expert's own row segment [off[e], off[e+1]).  Both operands are read as stored, A [rows, M] and
+// B [rows, N] row-major: MN-major tiles, A as two and B as four TMA boxes of 64 columns x 64 rows per
+// K step (the descriptors of gemm_tc_kernel's MN-major B, instruction-descriptor bits 15 and 16); padding
+// rows hold zeros in both.  Tiles (e, m-tile, n-tile) are dealt to one CTA per SM; a tile of an expert
+// without rows stores zeros.  The epilogue stores fp32 rows m < M of dW[e].
 constexpr int kWgStageStride = 36;                                  // floats per staged row
 constexpr size_t kWgStageBytes = 4 * 32 * kWgStageStride * sizeof(float);  // 4 epilogue warps
 __global__ void __launch_bounds__(kThreads, 1)
@@ -606,8 +607,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kb = 0; kb < nk; ++kb) {
                     if (!mbar_wait(bar(EMPTY + stage), phase ^ 1u, abort_flag)) { ok = false; break; }
                     mbar_expect_tx(bar(FULL + stage), kStageBytes);
-                    tma_load_2d(smem_u32(sA + stage * kABytes), &tmA, bar(FULL + stage), k0 + kb * kBK, m0);
-                    tma_load_2d(smem_u32(sB + stage * kBBytes), &tmB, bar(FULL + stage), k0 + kb * kBK, n0);
+                    const int kr = k0 + kb * kBK;
+#pragma unroll
+                    for (int j = 0; j < kBM / 64; ++j)
+                        tma_load_2d(smem_u32(sA + stage * kABytes + j * 8192), &tmA, bar(FULL + stage), m0 + 64 * j, kr);
+#pragma unroll
+                    for (int j = 0; j < kBN / 64; ++j)
+                        tma_load_2d(smem_u32(sB + stage * kBBytes + j * 8192), &tmB, bar(FULL + stage), n0 + 64 * j, kr);
                     issued[stage] = true;
                     issued_phase[stage] = phase;
                     if (++stage == kStages) { stage = 0; phase ^= 1u; }
@@ -622,7 +628,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16(kBM, kBN);
+            constexpr uint32_t idesc = idesc_bf16(kBM, kBN) | kIdescAMnMajor | kIdescBMnMajor;
             int stage = 0;
             uint32_t phase = 0;
             int local = 0;
@@ -638,11 +644,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kb = 0; kb < nk; ++kb) {
                     if (!mbar_wait(bar(FULL + stage), phase, abort_flag)) { ok = false; break; }
                     fence_after();
-                    const uint64_t ad = smem_desc_sw128(smem_u32(sA + stage * kABytes));
-                    const uint64_t bd = smem_desc_sw128(smem_u32(sB + stage * kBBytes));
+                    // MN-major operands: a K step of 16 is 16 rows of 128 bytes
+                    const uint64_t ad = smem_desc_sw128_mn(smem_u32(sA + stage * kABytes));
+                    const uint64_t bd = smem_desc_sw128_mn(smem_u32(sB + stage * kBBytes));
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk)
-                        mma_bf16(d_tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc, (kb | kk) != 0);
+                        mma_bf16(d_tmem, ad + (uint64_t)(kk * 128), bd + (uint64_t)(kk * 128), idesc, (kb | kk) != 0);
                     any = true;
                     commit(bar(EMPTY + stage));
                     if (++stage == kStages) { stage = 0; phase ^= 1u; }
@@ -1299,9 +1306,11 @@ int pair_stages(int E, bool bias) {
 
 cudaError_t launch_wgrad_tc(const WgradParams& P, cudaStream_t s) {
     if (P.M <= 0 || P.N <= 0 || P.E <= 0) return cudaSuccess;
-    CUtensorMap ma, mb;
-    if (!tma_map_bf16(P.At, (uint64_t)P.rows, (uint64_t)P.M, 0, kBM, &ma)) return cudaErrorInvalidValue;
-    if (!tma_map_bf16(P.Bt, (uint64_t)P.rows, (uint64_t)P.N, 0, kBN, &mb)) return cudaErrorInvalidValue;
+    const int a_ld = P.a_ld > 0 ? P.a_ld : P.M;
+    if (a_ld < P.M || a_ld % 8 || P.N % 8 || P.rows <= 0 || P.rows_b <= 0) return cudaErrorInvalidValue;
+    CUtensorMap ma, mb;  // boxes of 64 columns x 64 rows
+    if (!tma_map_bf16(P.A, (uint64_t)a_ld, (uint64_t)P.rows, 0, 64, &ma)) return cudaErrorInvalidValue;
+    if (!tma_map_bf16(P.B, (uint64_t)P.N, (uint64_t)P.rows_b, 0, 64, &mb)) return cudaErrorInvalidValue;
     TcArgs a{};
     a.offset = P.offset;
     a.C = P.dW;

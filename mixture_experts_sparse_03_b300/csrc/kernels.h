@@ -141,15 +141,17 @@ struct FfnParams {
 };
 size_t ffn_fp8_smem_bytes(int E, bool bias, int ring, bool swap);
 // weight gradients grouped along K (ffn_tc.cu): dW[e] [M, N] fp32 = sum over the rows r of expert e
-// (offset[e] <= r < offset[e+1], multiples of 128) of At[m][r] Bt[n][r]; At [M, rows], Bt [N, rows] bf16
+// (offset[e] <= r < offset[e+1], multiples of 64) of A[r][m] B[r][n], both operands read MN-major
 struct WgradParams {
-    const void* At;
-    const void* Bt;
+    const void* A;      // [rows, M] bf16, row-major (M contiguous)
+    const void* B;      // [rows_b, N] bf16, row-major (N contiguous); rows_b <= rows: the rest reads as 0
     const int* offset;  // [E+1]
     float* dW;          // [E, M, N]
     int E, M, N;
-    int64_t rows;       // columns of At and Bt (a multiple of 64)
+    int64_t rows;       // rows of A (segments of offset lie below it; multiples of 64)
+    int64_t rows_b;     // rows of B
     int* err;
+    int a_ld;           // elements per row of A (>= M, a multiple of 8); 0: M
 };
 cudaError_t launch_wgrad_tc(const WgradParams& p, cudaStream_t s);
 cudaError_t launch_ffn_simt(const FfnParams& p, cudaStream_t s);
@@ -167,8 +169,10 @@ cudaError_t launch_zero(float* p, size_t n, cudaStream_t s);
 // ---- backward (bwd.cu) ------------------------------------------------------------------------------
 // dst[b][c][r] = src[b][r][c] (bf16) for r < R, zero for R <= r < Rp; with row_mask, zero where
 // row_mask[r] < 0 and from row *row_limit on (device int: the dispatched rows in use, offset[E])
-cudaError_t launch_transpose(const void* src, void* dst, int B, int R, int C, int Rp, const int* row_mask,
-                             const int* row_limit, cudaStream_t s);
+// padding rows (row_token < 0, below *row_limit) of up to three bf16 row-major buffers [rows, width_i] set
+// to zero, so that contractions over whole row segments see exact zeros there
+cudaError_t launch_zero_pad_rows(void* p0, int w0, void* p1, int w1, void* p2, int w2, int rows,
+                                 const int* row_token, const int* row_limit, cudaStream_t s);
 // dY[r] = row_gate[r] * dout[row_token[r]] in bf16 (zero for padding rows and from row *row_limit on)
 cudaError_t launch_bwd_dy(const float* dout, const int* row_token, const float* row_gate, int rows, int d,
                           const int* row_limit, void* dY, cudaStream_t s);

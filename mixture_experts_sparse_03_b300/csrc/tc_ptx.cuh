@@ -281,6 +281,7 @@ __device__ __forceinline__ uint64_t smem_desc_sw128_mn(uint32_t addr) {
     d |= (uint64_t)2 << 61;
     return d;
 }
+constexpr uint32_t kIdescAMnMajor = 1u << 15;  // instruction descriptor bit: A is MN-major
 constexpr uint32_t kIdescBMnMajor = 1u << 16;  // instruction descriptor bit: B is MN-major
 // instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major, M x N
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
