@@ -13,8 +13,10 @@
 //              tcgen05.mma (M = 128, N = 256, K = 16, kind::f16) and tcgen05.commit to release smem
 //              stages and to hand finished accumulators to the epilogue
 //   warps 2-5  epilogue, one warp per TMEM lane quarter (32 rows): tcgen05.ld of the accumulator, then
-//              bias, GELU or gate scaling and the stores (see epilogue_cols), while the MMA warp fills
-//              the other accumulator
+//              bias, GELU or gate scaling and the stores, while the MMA warp fills the other accumulator;
+//              the bf16 row outputs (H, and Z in the backward's recomputation) go through a per-warp
+//              staging tile so that each store instruction writes whole 64-byte row pieces of 8 rows
+//              (epilogue_staged), the other modes store from each thread's row (epilogue_cols)
 // Every mbarrier wait is bounded: on expiry the kernel records MOE_ERR_DEVICE_TIMEOUT in the error
 // word, all roles stop, the producer waits (bounded) for its copies in flight, the MMA warp waits for
 // its last MMAs, and the TMEM is freed before the CTA exits.
@@ -43,6 +45,8 @@ __device__ __forceinline__ void* smem_bias_base(int* s_off, int nints) {
     return reinterpret_cast<void*>((reinterpret_cast<uintptr_t>(s_off + nints) + 15) & ~uintptr_t(15));
 }
 constexpr size_t kBiasSmem = 4 * kBN * sizeof(float) + 16;  // 4 epilogue warps x kBN floats, + alignment
+// single-SM kernel: per epilogue warp two 32-row x 64-byte staging tiles for its bf16 outputs (and Z)
+constexpr size_t kOutStageSmem = 4 * 2 * 2048 + 16;
 
 struct TcArgs {
     const int* offset;
@@ -150,6 +154,101 @@ __device__ __forceinline__ void epilogue_cols(const TcArgs& a, uint32_t taddr, i
     }
 }
 
+// Epilogue of the bf16 modes (0: H = GELU(acc + b1); 4: Z = acc + b1 and H = GELU(Z); 3: dZ = acc * GELU'(Z)),
+// 32 columns at a time through this warp's staging tiles (two of 32 rows x 64 bytes; 16-byte chunk c of row t
+// at t * 64 + ((c ^ ((t >> 1) & 3)) << 4), so that a quarter warp's 16-byte accesses hit distinct banks both
+// along a row and down a column): each thread fills its own row (r0 + lane, token tok), then every store
+// instruction writes 8 rows x 64 bytes, four lanes a row; in mode 3 the Z chunk comes in the same way.  Rows
+// with tok < 0 are neither loaded nor stored.  All lanes call this (tcgen05.ld and the shuffles are warp-wide).
+template <bool kBwd>
+__device__ __forceinline__ void epilogue_staged(const TcArgs& a, uint32_t taddr, int r0, int tok, const float* sbias,
+                                                int n0, uint8_t* stg, int lane) {
+    uint8_t* s0 = stg;         // the output tile (H, or Z in mode 4, or dZ)
+    uint8_t* s1 = stg + 2048;  // mode 4: H; mode 3: the Z chunk read
+    const int wsw = (lane >> 1) & 3;
+    const int rl = lane >> 2, cc = lane & 3;
+    for (int c0 = 0; c0 < kBN; c0 += 32) {
+        const int n = n0 + c0;
+        if (n >= a.N) break;  // N is a multiple of 32: the whole chunk is in or out (the same for the warp)
+        __syncwarp();         // the previous chunk's reads of the tiles are done
+        if (kBwd && a.mode == 3) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int rr = 8 * i + rl;
+                const int rt = __shfl_sync(0xffffffffu, tok, rr);
+                uint4 z = make_uint4(0u, 0u, 0u, 0u);
+                if (rt >= 0) z = __ldg(reinterpret_cast<const uint4*>(a.aux + (size_t)(r0 + rr) * a.N + n) + cc);
+                *reinterpret_cast<uint4*>(s1 + rr * 64 + ((cc ^ ((rr >> 1) & 3)) << 4)) = z;
+            }
+        }
+        uint32_t v[32];
+        tmem_ld32(taddr + (uint32_t)c0, v);
+        float f[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
+        if (sbias) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 4) {
+                const float4 bb = *reinterpret_cast<const float4*>(sbias + c0 + j);
+                f[j] += bb.x;
+                f[j + 1] += bb.y;
+                f[j + 2] += bb.z;
+                f[j + 3] += bb.w;
+            }
+        }
+        __syncwarp();  // mode 3: the Z chunk is in s1
+        uint32_t o0[16], o1[16];
+        if (kBwd && a.mode == 3) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const uint4 zz = *reinterpret_cast<const uint4*>(s1 + lane * 64 + ((c ^ wsw) << 4));
+                const uint32_t zw[4] = {zz.x, zz.y, zz.z, zz.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int j = 8 * c + 2 * i;
+                    o0[4 * c + i] = pack_bf16x2(f[j] * gelu_grad(bf16_lo(zw[i])), f[j + 1] * gelu_grad(bf16_hi(zw[i])));
+                }
+            }
+        } else if (kBwd && a.mode == 4) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                o0[i] = pack_bf16x2(f[2 * i], f[2 * i + 1]);
+                o1[i] = pack_bf16x2(gelu_erf(f[2 * i]), gelu_erf(f[2 * i + 1]));
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) o0[i] = pack_bf16x2(gelu_erf(f[2 * i]), gelu_erf(f[2 * i + 1]));
+        }
+        const bool two = kBwd && a.mode == 4;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            *reinterpret_cast<uint4*>(s0 + lane * 64 + ((c ^ wsw) << 4)) =
+                make_uint4(o0[4 * c], o0[4 * c + 1], o0[4 * c + 2], o0[4 * c + 3]);
+            if (two)
+                *reinterpret_cast<uint4*>(s1 + lane * 64 + ((c ^ wsw) << 4)) =
+                    make_uint4(o1[4 * c], o1[4 * c + 1], o1[4 * c + 2], o1[4 * c + 3]);
+        }
+        __syncwarp();
+        // destinations: mode 0 / 3 -> C; mode 4 -> Z in aux (s0) and H in C (s1)
+        bf16_t* d0 = two ? a.aux : static_cast<bf16_t*>(a.C);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int rr = 8 * i + rl;
+            const int rt = __shfl_sync(0xffffffffu, tok, rr);
+            const int off = rr * 64 + ((cc ^ ((rr >> 1) & 3)) << 4);
+            const uint4 w0 = *reinterpret_cast<const uint4*>(s0 + off);
+            if (rt >= 0) {
+                uint4* g0 = reinterpret_cast<uint4*>(d0 + (size_t)(r0 + rr) * a.N + n) + cc;
+                if (a.mode == 0) __stcs(g0, w0);  // streaming: the hidden rows should not push the weights out of L2
+                else *g0 = w0;
+                if (two)
+                    *(reinterpret_cast<uint4*>(static_cast<bf16_t*>(a.C) + (size_t)(r0 + rr) * a.N + n) + cc) =
+                        *reinterpret_cast<const uint4*>(s1 + off);
+            }
+        }
+    }
+}
+
 // One warp stages the bias slice of a tile (kBN columns from n0 of expert e's bias) as fp32 in its own
 // shared-memory buffer: eight columns per lane, one 16-byte load each (N is a multiple of 64).
 __device__ __forceinline__ const float* stage_bias(const TcArgs& a, float* wbias, int e, int n0, int lane) {
@@ -169,7 +268,9 @@ __device__ __forceinline__ const float* stage_bias(const TcArgs& a, float* wbias
     return wbias;
 }
 
-template <bool kBwd>
+// kStaged: the bf16 row-output modes (0, 4) with the staged epilogue; the other modes are compiled apart from
+// it, so that each keeps its own register allocation
+template <bool kBwd, bool kStaged>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const TcArgs a) {
     extern __shared__ uint8_t smem_raw[];
@@ -183,6 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
     int* s_off = reinterpret_cast<int*>(tmem_holder + 4);
     float* s_bias = reinterpret_cast<float*>(smem_bias_base(s_off, a.E + 1));  // [4 warps][kBN]
+    uint8_t* s_out = reinterpret_cast<uint8_t*>(smem_bias_base(reinterpret_cast<int*>(s_bias), 4 * kBN));  // [4][4 KiB]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     auto bar = [&](int i) { return smem_u32(bars + i); };
@@ -321,7 +423,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             fence_after();
-            epilogue_cols<kBwd>(a, tmem_base + lane_base + (uint32_t)(acc * kBN), r, tok, g, sb, n0, 0, kBN);
+            if constexpr (kStaged)
+                epilogue_staged<kBwd>(a, tmem_base + lane_base + (uint32_t)(acc * kBN), m0 + q * 32, tok, sb, n0,
+                                      s_out + q * 4096, lane);
+            else
+                epilogue_cols<kBwd>(a, tmem_base + lane_base + (uint32_t)(acc * kBN), r, tok, g, sb, n0, 0, kBN);
             fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(TEMPTY + acc));
@@ -1292,7 +1398,8 @@ int device_sm_count() {
 }
 
 size_t ffn_tc_smem_bytes(int E) {
-    return 1024 + (size_t)kStages * kStageBytes + (2 * kStages + 5) * 8 + 16 + 4 * (size_t)(E + 1) + kBiasSmem;
+    return 1024 + (size_t)kStages * kStageBytes + (2 * kStages + 5) * 8 + 16 + 4 * (size_t)(E + 1) + kBiasSmem +
+           kOutStageSmem;
 }
 
 size_t ffn_tc_pair_smem_bytes(int E, bool bias, int ns) {
@@ -1410,8 +1517,9 @@ cudaError_t launch_ffn_tc(const FfnParams& P, cudaStream_t s) {
             return launch_pdl(gemm_tc_pair_kernel, dim3(2 * pairs), dim3(kThreads), smem2, s, ma, mb2, a);
     }
     const size_t smem = ffn_tc_smem_bytes(P.E);
-    const bool bwd = P.mode >= 3;
-    auto kern = bwd ? gemm_tc_kernel<true> : gemm_tc_kernel<false>;
+    const bool bwd = P.mode >= 3, staged = P.mode == 0 || P.mode == 4;
+    auto kern = bwd ? (staged ? gemm_tc_kernel<true, true> : gemm_tc_kernel<true, false>)
+                    : (staged ? gemm_tc_kernel<false, true> : gemm_tc_kernel<false, false>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int64_t max_tiles = (P.rows_cap / kBM) * (int64_t)((P.N + kBN - 1) / kBN);
