@@ -581,8 +581,8 @@ moe_status backward_impl(const moe_config* cfg, const void* x, const void* w_gat
         cudaMemcpyAsync(dw_noise, dwcat + (size_t)E * d, (size_t)E * d * 4, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
         return MOE_ERR_CUDA;
     // 7. bias gradients: column sums over each expert's rows
-    if (db2) MOE_TRY(launch(s, [&] { return launch_segment_colsum(dy, off, rtok, E, d, db2, s); }));
-    if (db1) MOE_TRY(launch(s, [&] { return launch_segment_colsum(dz, off, rtok, E, h, db1, s); }));
+    if (db2) MOE_TRY(launch(s, [&] { return launch_segment_colsum(dy, off, E, d, db2, s); }));
+    if (db1) MOE_TRY(launch(s, [&] { return launch_segment_colsum(dz, off, E, h, db1, s); }));
     return MOE_OK;
 }
 

@@ -9,7 +9,8 @@
 //                     logits' gradient ds eps sigmoid(x W_n^T); a bf16 row [ds | dn | 0] per token
 //   zero_pad_rows     zeros in the padding rows of X_d, H and dZ, which the weight-gradient GEMMs contract
 //                     over together with the real rows
-//   segment_colsum    bias gradients: column sums of dY / dZ over each expert's row segment (fp32)
+//   segment_colsum    bias gradients: column sums of dY / dZ over each expert's row segment (fp32; their
+//                     padding rows are zero)
 #include "common.cuh"
 #include "kernels.h"
 
@@ -141,19 +142,47 @@ __global__ void __launch_bounds__(256) gate_grad_kernel(const float* __restrict_
     for (int c = (noisy ? 2 * E : E) + lane; c < Np; c += 32) row[c] = 0;
 }
 
-// db[e][c] = sum over the real rows r in [offset[e], offset[e+1]) (row_token[r] >= 0) of src[r][c] (fp32),
-// a thread per column
+// db[e][c] = sum over the rows r in [offset[e], offset[e+1]) of src[r][c] (fp32; the padding rows of src hold
+// zeros).  A CTA per (256 columns, expert): warp w sums the rows w, w + 8, ... of the segment, eight columns a
+// lane (16-byte loads, two rows in flight), then the eight warps' partials are added in warp order
+// (deterministic).
 __global__ void __launch_bounds__(256) segment_colsum_kernel(const bf16_t* __restrict__ src, const int* __restrict__ offset,
-                                                            const int* __restrict__ row_token, int C,
-                                                            float* __restrict__ db) {
+                                                            int C, float* __restrict__ db) {
+    __shared__ float part[8][256];
     pdl_wait();
     pdl_trigger();
-    const int e = blockIdx.y, c = blockIdx.x * 256 + threadIdx.x;
-    if (c >= C) return;
-    float s = 0.f;
-    for (int r = offset[e]; r < offset[e + 1]; ++r)
-        if (row_token[r] >= 0) s += bf16_to_f32(src[(size_t)r * C + c]);
-    db[(size_t)e * C + c] = s;
+    const int e = blockIdx.y, w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int c0 = blockIdx.x * 256 + lane * 8;
+    float acc[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+    if (c0 < C) {
+        const int r1 = offset[e + 1];
+        int r = offset[e] + w;
+        for (; r + 8 < r1; r += 16) {
+            float a[8], b[8];
+            load8(src + (size_t)r * C + c0, a);
+            load8(src + (size_t)(r + 8) * C + c0, b);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[j] += a[j] + b[j];
+        }
+        if (r < r1) {
+            float a[8];
+            load8(src + (size_t)r * C + c0, a);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[j] += a[j];
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) part[w][lane * 8 + j] = acc[j];
+    __syncthreads();
+    const int c = blockIdx.x * 256 + threadIdx.x;
+    if (c < C) {
+        float t = 0.f;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) t += part[q][threadIdx.x];
+        db[(size_t)e * C + c] = t;
+    }
 }
 
 // WcatT [d][Np] = [W_g ; W_n ; 0]^T (a thread per element; the gate weights are small)
@@ -203,11 +232,11 @@ cudaError_t launch_bwd_gate(const float* dout, const float* y, const int* topk_i
                       logits, eps, T, Tp, d, E, k, noisy, norm_all, Np, static_cast<bf16_t*>(dS));
 }
 
-cudaError_t launch_segment_colsum(const void* src, const int* offset, const int* row_token, int E, int C, float* db,
-                                  cudaStream_t s) {
+cudaError_t launch_segment_colsum(const void* src, const int* offset, int E, int C, float* db, cudaStream_t s) {
     if (E <= 0 || C <= 0) return cudaSuccess;
+    if (C % 8) return cudaErrorInvalidValue;
     return launch_pdl(segment_colsum_kernel, dim3((C + 255) / 256, E), dim3(256), 0, s, static_cast<const bf16_t*>(src),
-                      offset, row_token, C, db);
+                      offset, C, db);
 }
 
 cudaError_t launch_gate_weights_t(const void* wg, const void* wn, int E, int d, int Np, void* out, cudaStream_t s) {

@@ -180,9 +180,8 @@ cudaError_t launch_bwd_dy(const float* dout, const int* row_token, const float* 
 cudaError_t launch_bwd_gate(const float* dout, const float* y, const int* topk_idx, const float* topk_gate,
                             const int* slot, const int* offset, const float* logits, const float* eps, int T, int Tp,
                             int d, int E, int k, int noisy, int norm_all, int Np, void* dS, cudaStream_t s);
-// db[e][c] = column sums of src [rows, C] (bf16) over expert e's real rows (row_token >= 0)
-cudaError_t launch_segment_colsum(const void* src, const int* offset, const int* row_token, int E, int C, float* db,
-                                  cudaStream_t s);
+// db[e][c] = column sums of src [rows, C] (bf16) over expert e's row segment (its padding rows hold zeros)
+cudaError_t launch_segment_colsum(const void* src, const int* offset, int E, int C, float* db, cudaStream_t s);
 // out [d][Np] = [W_g ; W_n ; 0]^T
 cudaError_t launch_gate_weights_t(const void* wg, const void* wn, int E, int d, int Np, void* out, cudaStream_t s);
 // rows[i] = i for i < T, -1 up to Tp; off2 = {0, Tp}
