@@ -108,6 +108,7 @@ class Oracle:
             "oracle_dequant_block_fp8": ([I, I, I, P, P, P], None),
             "oracle_backward": ([I, I, I, I, I, I, I, I, I, I] + [P] * 16, None),
             "oracle_router_stats": ([I, I, I, P, P, P, P, P, P, P], None),
+            "oracle_backward_sampled": ([I] * 8 + [P] * 13 + [I, P, P, I, P, P, P, I, P, P, P], None),
         }
         for name, (args, res) in sigs.items():
             fn = getattr(lib, name)
@@ -237,6 +238,42 @@ class Oracle:
                                  _ptr(out["db1"]), _ptr(out["dw2"]), _ptr(out["db2"]))
         return out
 
+    def backward_sampled(self, spec, t, dout, tokens, s1, s2):
+        """Single outputs of backward() for layers too large for the whole of it: dx rows of `tokens`,
+        (dW1[e][n][m], db1[e][n]) for each (e, n, m) of s1 and (dW2[e][m][n], db2[e][m]) for each (e, m, n) of
+        s2, all float64, from the whole layer's routing (scores, top-k, capacity dispatch).  Returns a dict
+        with dx [len(tokens), d], dw1, db1 [len(s1)], dw2, db2 [len(s2)]."""
+        gate = _GATE_CODES[spec["gate"]]
+        if gate == GATE_COSINE:
+            raise NotImplementedError("the oracle's backward covers the softmax and noisy gates")
+        xs, wg, wn, a1, c1, a2, c2 = (_raw(t.get(n)) for n in ("x", "w_gate", "w_noise", "w1", "b1", "w2", "b2"))
+        dt = _same_dtype(xs, wg, wn, a1, c1, a2, c2)
+        T, d = xs[0].shape
+        E, h, _ = a1[0].shape
+        k = spec["k"]
+        scores = self.gate_scores(spec["gate"], t["x"], t.get("w_gate"), t.get("w_noise"), t.get("eps"))
+        idx, gw = self.topk(scores, k, spec["norm"])
+        C = self.capacity(T, E, k, spec.get("capacity_factor", 1.0), spec.get("capacity", -1))
+        slot, _ = self.dispatch(idx, E, C, spec.get("priority", "token"))
+        ep = None
+        if gate == GATE_NOISY:
+            ep = t["eps"].detach().cpu().numpy() if hasattr(t["eps"], "detach") else t["eps"]
+            ep = np.ascontiguousarray(ep, dtype=np.float32)
+        go = dout.detach().cpu().numpy() if hasattr(dout, "detach") else dout
+        go = np.ascontiguousarray(go, dtype=np.float64)
+        tok = np.ascontiguousarray(tokens, dtype=np.int32)
+        q1 = np.ascontiguousarray(np.asarray(s1, dtype=np.int32).reshape(-1, 3))
+        q2 = np.ascontiguousarray(np.asarray(s2, dtype=np.int32).reshape(-1, 3))
+        out = dict(dx=np.empty((len(tok), d)), dw1=np.empty(len(q1)), db1=np.empty(len(q1)), dw2=np.empty(len(q2)),
+                   db2=np.empty(len(q2)))
+        self.lib.oracle_backward_sampled(gate, _NORM_CODES[spec["norm"]], T, d, h, E, k, dt, _ptr(xs[0]), _ptr(wg[0]),
+                                         _ptr(wn[0]), _ptr(ep), _ptr(a1[0]), _ptr(c1[0]), _ptr(a2[0]), _ptr(c2[0]),
+                                         _ptr(go), _ptr(scores), _ptr(idx), _ptr(gw), _ptr(slot), len(tok), _ptr(tok),
+                                         _ptr(out["dx"]), len(q1), _ptr(q1), _ptr(out["dw1"]), _ptr(out["db1"]),
+                                         len(q2), _ptr(q2), _ptr(out["dw2"]), _ptr(out["db2"]))
+        out.update(idx=idx, slot=slot)
+        return out
+
     def router_stats(self, idx, gate, E, slot=None):
         """Router statistics: (importance float64 [E], expert_importance_loss, load_balance_loss, dropped)."""
         idx = np.ascontiguousarray(idx, dtype=np.int32)
@@ -322,6 +359,10 @@ def dequant_block_fp8(*a, **kw):
 
 def backward(*a, **kw):
     return default().backward(*a, **kw)
+
+
+def backward_sampled(*a, **kw):
+    return default().backward_sampled(*a, **kw)
 
 
 def route(*a, **kw):

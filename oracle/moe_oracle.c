@@ -422,3 +422,138 @@ void oracle_backward(int gate_type, int norm, int T, int d, int h, int E, int k,
     free(scores); free(idx); free(gate); free(slot); free(count);
     free(z); free(a); free(da); free(dg); free(ds); free(p);
 }
+
+/* Single entries of the backward above, for layers too large for the whole of it (test support): the same
+ * definitions, evaluated one output at a time from the routing of the whole layer (scores, idx, gate,
+ * slot, as oracle_gate_scores / oracle_topk / oracle_dispatch give them).
+ *   dx_rows[i][:]  = dx of token tok[i]: for each of its kept pairs, W1[e]^T dz with
+ *                    dz = (W2[e]^T g dout_t) * GELU'(z), plus the scores' gradient through W_g (and W_n)
+ *   dw1_v[i], db1_v[i] = dW1[e][n][m] and db1[e][n] for (e, n, m) = s1[3i .. 3i+2]: sums over the kept pairs
+ *                    (t, e) of dz_t[n] x_t[m] and dz_t[n]
+ *   dw2_v[i], db2_v[i] = dW2[e][m][n] and db2[e][m] for (e, m, n) = s2[3i .. 3i+2]: sums over the kept pairs
+ *                    of g dout_t[m] GELU(z_t[n]) and g dout_t[m]
+ * Pairs are visited in token order, ranks in order, as in oracle_backward. */
+static void pair_hidden(int d, int h, int dtype, const void *x, size_t xo, const void *w1, const void *b1, size_t e,
+                        int n, double *z_out)
+{
+    double z = dot_rows(x, xo, dtype, w1, (e * h + n) * (size_t)d, dtype, d);
+    if (b1 != NULL) z = z + elem(b1, e * (size_t)h + n, dtype);
+    *z_out = z;
+}
+
+void oracle_backward_sampled(int gate_type, int norm, int T, int d, int h, int E, int k, int dtype,
+                             const void *x, const void *w_gate, const void *w_noise, const float *eps,
+                             const void *w1, const void *b1, const void *w2, const void *b2, const double *dout,
+                             const double *scores, const int32_t *idx, const double *gate, const int32_t *slot,
+                             int nt, const int32_t *tok, double *dx_rows, int n1, const int32_t *s1, double *dw1_v,
+                             double *db1_v, int n2, const int32_t *s2, double *dw2_v, double *db2_v)
+{
+    double *z = (double *)malloc(sizeof(double) * (size_t)h);
+    double *a = (double *)malloc(sizeof(double) * (size_t)h);
+    double *da = (double *)malloc(sizeof(double) * (size_t)h);
+    double *dg = (double *)malloc(sizeof(double) * (size_t)k);
+    double *ds = (double *)malloc(sizeof(double) * (size_t)E);
+    double *p = (double *)malloc(sizeof(double) * (size_t)E);
+    for (int i = 0; i < nt; ++i) {
+        const int t = tok[i];
+        const size_t xo = (size_t)t * d;
+        const double *go = dout + xo;
+        double *gx = dx_rows + (size_t)i * d;
+        for (int m = 0; m < d; ++m) gx[m] = 0.0;
+        for (int j = 0; j < k; ++j) {
+            const size_t q = (size_t)t * k + j;
+            dg[j] = 0.0;
+            if (slot[q] < 0) continue;
+            const size_t e = (size_t)idx[q];
+            const double g = gate[q];
+            for (int n = 0; n < h; ++n) {
+                pair_hidden(d, h, dtype, x, xo, w1, b1, e, n, &z[n]);
+                a[n] = gelu_erf(z[n]);
+                da[n] = 0.0;
+            }
+            for (int m = 0; m < d; ++m) {
+                double y = 0.0;
+                for (int n = 0; n < h; ++n) y += a[n] * elem(w2, (e * d + m) * (size_t)h + n, dtype);
+                if (b2) y += elem(b2, e * d + m, dtype);
+                dg[j] += go[m] * y;
+                const double dy = g * go[m];
+                for (int n = 0; n < h; ++n) da[n] += elem(w2, (e * d + m) * (size_t)h + n, dtype) * dy;
+            }
+            for (int n = 0; n < h; ++n) {
+                const double dzn = da[n] * gelu_grad(z[n]);
+                for (int m = 0; m < d; ++m) gx[m] += elem(w1, (e * h + n) * (size_t)d + m, dtype) * dzn;
+            }
+        }
+        for (int e = 0; e < E; ++e) ds[e] = 0.0;
+        if (norm == NORM_TOPK) {
+            double sum = 0.0;
+            for (int j = 0; j < k; ++j) sum += gate[(size_t)t * k + j] * dg[j];
+            for (int j = 0; j < k; ++j) {
+                const size_t q = (size_t)t * k + j;
+                ds[idx[q]] = gate[q] * (dg[j] - sum);
+            }
+        } else {
+            const double *s = scores + (size_t)t * E;
+            double mx = s[0], den = 0.0;
+            for (int e = 1; e < E; ++e) if (s[e] > mx) mx = s[e];
+            for (int e = 0; e < E; ++e) p[e] = exp(s[e] - mx);
+            for (int e = 0; e < E; ++e) den += p[e];
+            for (int e = 0; e < E; ++e) p[e] /= den;
+            for (int j = 0; j < k; ++j) {
+                const double gj = gate[(size_t)t * k + j];
+                const int ej = idx[(size_t)t * k + j];
+                for (int e = 0; e < E; ++e) ds[e] += dg[j] * gj * ((e == ej ? 1.0 : 0.0) - p[e]);
+            }
+        }
+        for (int e = 0; e < E; ++e) {
+            if (ds[e] == 0.0) continue;
+            for (int m = 0; m < d; ++m) gx[m] = gx[m] + ds[e] * elem(w_gate, (size_t)e * d + m, dtype);
+            if (gate_type == GATE_NOISY) {
+                const double nl = dot_rows(x, xo, dtype, w_noise, (size_t)e * d, dtype, d);
+                const double ept = (double)eps[(size_t)t * E + e];
+                const double dn = ds[e] * ept * sigmoid(nl);
+                for (int m = 0; m < d; ++m) gx[m] += dn * elem(w_noise, (size_t)e * d + m, dtype);
+            }
+        }
+    }
+    for (int i = 0; i < n1; ++i) {
+        const size_t e = (size_t)s1[3 * i];
+        const int n = s1[3 * i + 1], m = s1[3 * i + 2];
+        double w = 0.0, b = 0.0;
+        for (int t = 0; t < T; ++t)
+            for (int j = 0; j < k; ++j) {
+                const size_t q = (size_t)t * k + j;
+                if (slot[q] < 0 || (size_t)idx[q] != e) continue;
+                const size_t xo = (size_t)t * d;
+                double zn;
+                pair_hidden(d, h, dtype, x, xo, w1, b1, e, n, &zn);
+                double dan = 0.0;
+                for (int mm = 0; mm < d; ++mm)
+                    dan += elem(w2, (e * d + mm) * (size_t)h + n, dtype) * (gate[q] * dout[xo + mm]);
+                const double dzn = dan * gelu_grad(zn);
+                w += dzn * elem(x, xo + m, dtype);
+                b += dzn;
+            }
+        dw1_v[i] = w;
+        db1_v[i] = b;
+    }
+    for (int i = 0; i < n2; ++i) {
+        const size_t e = (size_t)s2[3 * i];
+        const int m = s2[3 * i + 1], n = s2[3 * i + 2];
+        double w = 0.0, b = 0.0;
+        for (int t = 0; t < T; ++t)
+            for (int j = 0; j < k; ++j) {
+                const size_t q = (size_t)t * k + j;
+                if (slot[q] < 0 || (size_t)idx[q] != e) continue;
+                const size_t xo = (size_t)t * d;
+                double zn;
+                pair_hidden(d, h, dtype, x, xo, w1, b1, e, n, &zn);
+                const double dy = gate[q] * dout[xo + m];
+                w += dy * gelu_erf(zn);
+                b += dy;
+            }
+        dw2_v[i] = w;
+        db2_v[i] = b;
+    }
+    free(z); free(a); free(da); free(dg); free(ds); free(p);
+}

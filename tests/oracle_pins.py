@@ -259,6 +259,34 @@ def pin_backward_finite_differences(o):
     assert dropped_somewhere  # the capacity cases do drop pairs
 
 
+def pin_backward_sampled_equals_whole(o):
+    """The single-output backward (for layers too large for the whole one) against the whole backward, which
+    the finite differences above pin: dx rows and dW1 / db1 / dW2 / db2 entries agree to rounding, for both
+    gates and normalisations, with capacity drops, on bf16 layers."""
+    rng = np.random.default_rng(13)
+    dropped = False
+    for gate, norm, k, cap, seed in (("softmax", "topk", 2, 2, 31), ("noisy", "topk", 2, 2, 32),
+                                     ("softmax", "all", 1, 8, 33)):
+        t, dout = _fd_layer(seed, gate)
+        tb = {n: (v.to(torch.bfloat16) if n != "eps" and v is not None else v) for n, v in t.items()}
+        spec = dict(gate=gate, norm=norm, k=k, E=4, capacity=cap, capacity_factor=1.0, temperature=1.0,
+                    priority="token")
+        whole = o.backward(spec, tb, dout)
+        T, d = tb["x"].shape
+        E, h, _ = tb["w1"].shape
+        toks = rng.choice(T, size=4, replace=False)
+        s1 = [(int(rng.integers(E)), int(rng.integers(h)), int(rng.integers(d))) for _ in range(10)]
+        s2 = [(int(rng.integers(E)), int(rng.integers(d)), int(rng.integers(h))) for _ in range(10)]
+        part = o.backward_sampled(spec, tb, dout, toks, s1, s2)
+        assert np.allclose(part["dx"], whole["dx"][toks], rtol=1e-12, atol=1e-14)
+        assert np.allclose(part["dw1"], [whole["dw1"][e, n, m] for e, n, m in s1], rtol=1e-12, atol=1e-14)
+        assert np.allclose(part["db1"], [whole["db1"][e, n] for e, n, _ in s1], rtol=1e-12, atol=1e-14)
+        assert np.allclose(part["dw2"], [whole["dw2"][e, m, n] for e, m, n in s2], rtol=1e-12, atol=1e-14)
+        assert np.allclose(part["db2"], [whole["db2"][e, m] for e, m, _ in s2], rtol=1e-12, atol=1e-14)
+        dropped = dropped or bool((part["slot"] < 0).any())
+    assert dropped  # some case drops pairs
+
+
 def pin_gelu_normal_cdf(o):
     """Identity weights make the expert return GELU(x) itself; GELU(z) = z Phi(z) with Phi from a table."""
     g = GOLDEN["gelu_normal_cdf"]

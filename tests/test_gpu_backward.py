@@ -79,3 +79,44 @@ def test_backward_rejects_cosine_and_fp32():
     wl32 = small_workload(T=16, d=64, h=64, E=4, k=2, dtype="f32")
     assert b.moe_backward_workspace_size(b.config(wl32)) == 0
     assert b.lib.moe_backward(ctypes.byref(b.config(wl32)), *([None] * 17), 0, None) == 2
+
+
+def test_backward_full_size_sampled():
+    """moe_backward on the E = 64 noisy layer at full size (T = 16384, d = 2048, h = 8192, top-2) against the
+    oracle's single-output backward (pinned against its whole backward): the dx rows of 6 tokens, 16 entries
+    each of dW1 / db1 and dW2 / db2 in experts with rows, normwise per group as above."""
+    from mixture_experts_sparse_03_b300.inputs import WORKLOADS
+
+    wl = WORKLOADS["bf16_noisy_e64"]
+    tg = make_inputs(wl, device="cuda", expert_device="cuda")
+    tc = {k: (v.cpu() if v is not None else None) for k, v in tg.items()}
+    dout = torch.randn(wl.T, wl.d, generator=torch.Generator().manual_seed(wl.seed + 100))
+    c = b.config(wl)
+    n = b.moe_backward_workspace_size(c)
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    T, d, h, E = wl.T, wl.d, wl.h, wl.E
+    f = lambda *s: torch.full(s, float("nan"), dtype=torch.float32, device="cuda")  # noqa: E731
+    g = dict(dx=f(T, d), dw_gate=f(E, d), dw_noise=f(E, d), dw1=f(E, h, d), db1=f(E, h), dw2=f(E, d, h), db2=f(E, d))
+    b.check(b.moe_backward(c, tg["x"], tg["w_gate"], tg["w_noise"], tg["eps"], tg["w1"], tg.get("b1"), tg["w2"],
+                           tg.get("b2"), dout.cuda(), g["dx"], g["dw_gate"], g["dw_noise"], g["dw1"], g["db1"],
+                           g["dw2"], g["db2"], ws, n), "moe_backward")
+    st, info = b.moe_device_status(ws, n)
+    assert st == 0, (b.STATUS[st], info)
+    rng = np.random.default_rng(17)
+    toks = rng.choice(T, size=6, replace=False)
+    s1 = [(int(rng.integers(E)), int(rng.integers(h)), int(rng.integers(d))) for _ in range(16)]
+    s2 = [(int(rng.integers(E)), int(rng.integers(d)), int(rng.integers(h))) for _ in range(16)]
+    want = oracle.backward_sampled(wl.spec(), tc, dout.double(), toks, s1, s2)
+    assert (want["slot"] >= 0).sum() > 0
+    ix = lambda t, idx: t[tuple(torch.as_tensor(list(a), device="cuda") for a in zip(*idx))].cpu().numpy()  # noqa
+    got = dict(dx=g["dx"][torch.as_tensor(toks, device="cuda")].cpu().numpy(),
+               dw1=ix(g["dw1"], s1), db1=ix(g["db1"], [(e, n_) for e, n_, _ in s1]),
+               dw2=ix(g["dw2"], s2), db2=ix(g["db2"], [(e, m) for e, m, _ in s2]))
+    report = {}
+    for k, gv in got.items():
+        ref = want[k]
+        assert np.isfinite(gv).all(), k
+        report[k] = np.abs(gv.astype(np.float64) - ref).max() / max(np.abs(ref).max(), 1e-30)
+    print(" ".join("%s %.2e" % kv for kv in sorted(report.items())))
+    for k, err in report.items():
+        assert err <= TOL, (k, err, report)

@@ -59,6 +59,10 @@ MUTANTS = [
     ("drops_counts_kept", "if (slot && slot[i] < 0) ++drops;", "if (slot && slot[i] >= 0) ++drops;"),
     ("bf16_widening_wrong_half", "uint32_t bits = (uint32_t)((const uint16_t *)base)[i] << 16;",
      "uint32_t bits = (uint32_t)((const uint16_t *)base)[i] << 15;"),
+    ("sampled_dw1_drops_gelu_grad", "const double dzn = dan * gelu_grad(zn);", "const double dzn = dan;"),
+    ("sampled_dw2_drops_gate", "const double dy = gate[q] * dout[xo + m];", "const double dy = dout[xo + m];"),
+    ("sampled_dx_noise_sign", "for (int m = 0; m < d; ++m) gx[m] += dn * elem(w_noise, (size_t)e * d + m, dtype);",
+     "for (int m = 0; m < d; ++m) gx[m] -= dn * elem(w_noise, (size_t)e * d + m, dtype);"),
 ]
 
 
