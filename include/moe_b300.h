@@ -107,7 +107,9 @@ typedef struct moe_config {
 #define MOE_FLAG_SIMT_FFN         1
 #define MOE_FLAG_UNFUSED_COMBINE  2
 /* The bf16 expert GEMMs run either on single SMs (128 x 256 tiles) or on pairs of SMs (256 x 256 tiles,
- * tcgen05 cta_group::2); by default pairs are used when T * k / E >= 2048.  These flags force one. */
+ * tcgen05 cta_group::2); by default pairs are used when T * k / E >= 2048 or when d <= 1024 and
+ * T * k / E >= 1024, and for the second (down) projection alone when 512 <= d <= 1024 and
+ * T * k / E >= 512.  These flags force one. */
 #define MOE_FLAG_FFN_ONE_SM       4
 #define MOE_FLAG_FFN_SM_PAIR      8
 /* Capacity priority.  By default slots are handed out in token order (token t's pairs before token

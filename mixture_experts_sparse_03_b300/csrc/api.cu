@@ -29,6 +29,7 @@ struct Plan {
     int nblk_hist;      // blocks of the dispatch histogram: of 32 tokens, or of 32 (rank, token) pairs
     int N0, N1;         // gate logits from the first / second weight tensor
     int pair;           // expert GEMMs on pairs of SMs
+    int pair_down;      // the down projection (K = h) on pairs of SMs
     GateGemmPlan gg;    // tensor-core logits GEMM (bf16 layers)
     int64_t rows;
     size_t o_err, o_idx, o_gate, o_slot, o_hist, o_count, o_off, o_rtok, o_rgate, o_xd, o_h, o_y, o_part, o_xn2,
@@ -105,8 +106,13 @@ moe_status make_plan(const moe_config* c, Plan* pl) {
     P.fused = P.k <= 2 && !(c->flags & MOE_FLAG_UNFUSED_COMBINE);
     // pairs of SMs pay off when experts get many rows: their 256-row tiles waste at most 128 rows per
     // expert, against 2x the rows each weight byte serves
+    // (measured: with d <= 1024 and 1024 rows per expert both GEMMs gain on pairs, the step 4 %; with 512
+    // rows per expert only the down projection, where K = h is long and N = d short)
+    const bool auto_ok = !(c->flags & MOE_FLAG_FFN_ONE_SM);
+    const int64_t pairs_tk = (int64_t)P.T * P.k;
     P.pair = (c->flags & MOE_FLAG_FFN_SM_PAIR) ||
-             (!(c->flags & MOE_FLAG_FFN_ONE_SM) && (int64_t)P.T * P.k >= (int64_t)kPairMinRows * P.E);
+             (auto_ok && (pairs_tk >= (int64_t)kPairMinRows * P.E || (P.d <= 1024 && pairs_tk >= 1024 * (int64_t)P.E)));
+    P.pair_down = P.pair || (auto_ok && P.d >= 512 && P.d <= 1024 && pairs_tk >= 512 * (int64_t)P.E);
     size_t o = 0;
     auto take = [&](size_t bytes) { size_t r = o; o = up(o + bytes); return r; };
     const size_t tk = (size_t)P.T * P.k;
@@ -309,7 +315,8 @@ FfnParams ffn_params(const Plan& P, int mode, const void* A, const void* W, cons
     f.mode = mode;
     f.rows_cap = P.rows;
     f.err = err;
-    f.pair = (w_scale || mode >= 3) ? 0 : P.pair;  // block-FP8 weights and the backward run on single SMs
+    // block-FP8 weights and the backward run on single SMs
+    f.pair = (w_scale || mode >= 3) ? 0 : (up_proj ? P.pair : P.pair_down);
     f.max_rows = P.C < P.T ? P.C : P.T;
     return f;
 }
