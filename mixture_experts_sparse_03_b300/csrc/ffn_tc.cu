@@ -249,6 +249,50 @@ __device__ __forceinline__ void epilogue_staged(const TcArgs& a, uint32_t taddr,
     }
 }
 
+// Epilogue of mode 3 (dZ = acc * GELU'(Z), bf16, no bias) for one accumulator row (TMEM lane = this thread's
+// row r, token tok): the Z chunk of the next 32 columns is loaded while this chunk is computed, so that the
+// latency of the Z loads overlaps the arithmetic instead of stalling every chunk.
+__device__ __forceinline__ void epilogue_dz(const TcArgs& a, uint32_t taddr, int r, int tok, int n0) {
+    const bf16_t* zrow = a.aux + (size_t)r * a.N;
+    bf16_t* drow = static_cast<bf16_t*>(a.C) + (size_t)r * a.N;
+    uint4 zc[4], zn[4];
+    const bool live = tok >= 0;
+    if (live && n0 < a.N) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) zc[i] = __ldg(reinterpret_cast<const uint4*>(zrow + n0) + i);
+    }
+    for (int c0 = 0; c0 < kBN; c0 += 32) {
+        const int n = n0 + c0;
+        uint32_t v[32];
+        __syncwarp();
+        tmem_ld32(taddr + (uint32_t)c0, v);
+        if (n >= a.N) continue;  // the same for the warp: N is a multiple of 32
+        const bool more = live && c0 + 32 < kBN && n + 32 < a.N;
+        if (more) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) zn[i] = __ldg(reinterpret_cast<const uint4*>(zrow + n + 32) + i);
+        }
+        if (live) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t zw[4] = {zc[i].x, zc[i].y, zc[i].z, zc[i].w};
+                uint32_t o[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int j = 8 * i + 2 * q;
+                    o[q] = pack_bf16x2(__uint_as_float(v[j]) * gelu_grad(bf16_lo(zw[q])),
+                                       __uint_as_float(v[j + 1]) * gelu_grad(bf16_hi(zw[q])));
+                }
+                reinterpret_cast<uint4*>(drow + n)[i] = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+        }
+        if (more) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) zc[i] = zn[i];
+        }
+    }
+}
+
 // One warp stages the bias slice of a tile (kBN columns from n0 of expert e's bias) as fp32 in its own
 // shared-memory buffer: eight columns per lane, one 16-byte load each (N is a multiple of 64).
 __device__ __forceinline__ const float* stage_bias(const TcArgs& a, float* wbias, int e, int n0, int lane) {
@@ -426,6 +470,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if constexpr (kStaged)
                 epilogue_staged<kBwd>(a, tmem_base + lane_base + (uint32_t)(acc * kBN), m0 + q * 32, tok, sb, n0,
                                       s_out + q * 4096, lane);
+            else if (kBwd && a.mode == 3)
+                epilogue_dz(a, tmem_base + lane_base + (uint32_t)(acc * kBN), r, tok, n0);
             else
                 epilogue_cols<kBwd>(a, tmem_base + lane_base + (uint32_t)(acc * kBN), r, tok, g, sb, n0, 0, kBN);
             fence_before();
