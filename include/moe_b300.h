@@ -57,7 +57,7 @@ extern "C" {
 typedef int32_t moe_status;
 #define MOE_OK                  0
 #define MOE_ERR_INVALID_ARG     1 /* a pointer, size or enum is out of its documented range          */
-#define MOE_ERR_UNSUPPORTED     2 /* valid in principle, outside what this build implements          */
+#define MOE_ERR_UNSUPPORTED     2 /* valid in principle, outside what the library implements         */
 #define MOE_ERR_WORKSPACE       3 /* workspace NULL, misaligned or smaller than moe_workspace_size() */
 #define MOE_ERR_CUDA            4 /* a CUDA runtime call failed (launch, memset, descriptor encode)  */
 #define MOE_ERR_DEVICE_CHECK    5 /* a kernel's own bounds check failed (see moe_device_status)      */
