@@ -33,6 +33,7 @@ namespace {
 using namespace gate;
 
 constexpr int kBT = kTokensPerBlock;  // tokens per CTA, one warp each
+constexpr int kFewExperts = 16;       // cosine scores with at most this many experts: lanes split u
 constexpr int kSelThreads = 32 * kBT;
 constexpr int kSel = kMaxTopK + 1;
 
@@ -189,6 +190,31 @@ __global__ void __launch_bounds__(kSelThreads) gate_select_kernel(const GatePara
             const float rel = nu > 2.f * Dl ? (2.f * p + 8.f) * kU + 2.f * Dl / (nu - Dl) : INFINITY;
             const float nuc = fmaxf(nu, 1e-12f);
             const T* emb = static_cast<const T*>(P.emb);
+            if (stage && E <= kFewExperts) {
+                // few experts: the lanes split u instead (components lane, lane + 32, ...) and each keeps a
+                // partial dot for every expert, reduced across the warp at the end -- all 32 lanes busy
+                // instead of E; a p-term sum in another order stays within the same (2p + 8) u bound
+                float acc[kFewExperts];
+#pragma unroll
+                for (int q = 0; q < kFewExperts; ++q) acc[q] = 0.f;
+                for (int j = lane; j < p; j += 32) {
+                    const float u = Lr[j];
+                    const float* er = embs + j * (E + 1);
+#pragma unroll
+                    for (int q = 0; q < kFewExperts; ++q)
+                        if (q < E) acc[q] = fmaf(u, er[q], acc[q]);
+                }
+#pragma unroll
+                for (int q = 0; q < kFewExperts; ++q) {
+                    if (q >= E) break;
+                    const float dot = warp_sum(acc[q]);
+                    if (lane == q) {
+                        const float sv = dot / (nuc * fmaxf(embn[q], 1e-12f)) * P.inv_temp;
+                        sc[q] = sv;
+                        dmax = fmaxf(dmax, rel * P.inv_temp + 4.f * kU * fabsf(sv));
+                    }
+                }
+            } else
             for (int e = lane; e < E; e += 32) {
                 float dot = 0.f;
                 // four interleaved partial sums (p is a multiple of 8): u is read four components at a
