@@ -164,15 +164,15 @@ MOE_API moe_status moe_route(const moe_config* cfg, const void* x, const void* w
 
 /* ---- step 1 alone: gate logits ---------------------------------------------------------------- */
 /* The gate GEMM of a MOE_BF16 layer on the tensor cores (tcgen05: exact bf16 products, fp32
- * accumulation within each 64-wide block of d, blocks added in float-float on the CUDA cores):
+ * accumulation within each 128-wide chunk of d, chunks added with compensated sums on the CUDA cores):
  *   SOFTMAX  logits [T, E]      = x W_g^T     (the single linear layer before the softmax, "How sparse
  *                                              activation improves efficiency", section 2.1)
  *   NOISY    logits [T, 2E]     = [x W_g^T, x W_n^T]  (clean and noise logits of NoisyTopKGating,
  *                                              "MoE sparse-compute acceleration", section 2.1)
  *   COSINE   logits [T, cos_dim] = x P^T      (the projection of Tutel's cosine_top)
- * fp32, row-major, overwritten.  Error: |logit - exact| <= 32 * 2^-23 * sum_i |x_i w_i|, the bound
- * moe_route assumes for this GEMM (21 * 2^-23 from the measured rounding of the tensor cores, with a
- * margin).  noise_eps and expert_emb are not used.  MOE_F32 layers return MOE_ERR_UNSUPPORTED (their logits are computed inside
+ * fp32, row-major, overwritten.  Error: |logit - exact| <= 64 * 2^-23 * sum_i |x_i w_i|, the bound
+ * moe_route assumes for this GEMM (44.5 * 2^-23 from the measured rounding of the tensor cores and the
+ * compensated sums, with a margin).  noise_eps and expert_emb are not used.  MOE_F32 layers return MOE_ERR_UNSUPPORTED (their logits are computed inside
  * moe_route's CUDA-core kernel). */
 MOE_API moe_status moe_gate_logits(const moe_config* cfg, const void* x, const void* w_gate, const void* w_noise,
                            const void* proj, float* logits, void* workspace, size_t workspace_bytes,

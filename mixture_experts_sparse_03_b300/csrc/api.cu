@@ -42,10 +42,12 @@ struct Plan {
 // products to the fp32 accumulator after aligning all 17 addends to the largest one's exponent e on a
 // grid of 2^(e-25), sums them exactly and truncates the result to fp32, so a step errs by at most
 // 17 * 2^-25 * max|addend| + 2^-23 * |result| <= 5.25 * 2^-23 * (sum of |x_i w_i| so far in the
-// accumulator).  The logits GEMM starts a fresh accumulator every 64-wide K block (4 steps) and adds the
-// blocks in float-float, so the whole dot product errs by at most 21 * 2^-23 * sum |x_i w_i|; the
-// constant leaves a 1.5x margin.  Summing S fp32 split partials adds S * 2^-24 * sum |x_i w_i|.
-constexpr double kTcErr = 32.0;
+// accumulator).  The logits GEMM starts a fresh accumulator every 128-wide chunk of K (8 steps), so each
+// chunk errs by at most 42 * 2^-23 * (its sum of |x_i w_i|), and adds the chunks with compensated (Kahan)
+// summation, which errs by at most 2u * sum |chunk| (u = 2^-24), its correction term by no more, and the
+// final rounding by u: the whole dot product errs by at most 44.5 * 2^-23 * sum |x_i w_i|; the constant
+// leaves a 1.44x margin.  Summing S fp32 split partials adds S * 2^-24 * sum |x_i w_i|.
+constexpr double kTcErr = 64.0;
 
 // expected rows per expert (T * k / E) from which the expert GEMMs run on pairs of SMs by default
 constexpr int kPairMinRows = 2048;

@@ -103,6 +103,14 @@ __device__ __forceinline__ void ff_add(float& hi, float& lo, float ohi, float ol
     hi = s;
     lo += se + olo;
 }
+// Kahan's compensated summation, (hi, lo) += v with lo the running correction of hi: over n addends the
+// result hi + lo errs by at most 2u * sum |v| + O(n u^2) (u = 2^-24), at four additions per addend
+__device__ __forceinline__ void kahan_add(float& hi, float& lo, float v) {
+    const float y = v + lo;
+    const float t = hi + y;
+    lo = y - (t - hi);
+    hi = t;
+}
 __device__ __forceinline__ void ff_warp_sum(float& hi, float& lo) {
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
@@ -110,6 +118,14 @@ __device__ __forceinline__ void ff_warp_sum(float& hi, float& lo) {
         float ol = __shfl_xor_sync(0xffffffffu, lo, off);
         ff_add(hi, lo, oh, ol);
     }
+}
+
+// named CTA barrier `id` over `count` threads (whole warps): arrive without waiting, or wait for all
+__device__ __forceinline__ void named_bar_arrive(int id, int count) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 __device__ __forceinline__ float warp_sum(float v) {

@@ -9,18 +9,22 @@
 // (gate.cu) sums the partials, scores, picks the top-k, and re-scores near ties exactly.
 //
 // Grid (m-tile, n-tile, split): 128 tokens x BN logits x a range of 64-wide K blocks per CTA.  The
-// weight rows are one or two tensors (w_gate, then w_noise for the noisy gate); an n-tile never
-// straddles them.  Small token counts split K across CTAs so that about one CTA per SM streams the
-// weights; the splits' partials are summed in a fixed order by the selection kernel (deterministic).
+// weight rows are one or two tensors (w_gate, then w_noise for the noisy gate); an n-tile holds both
+// halves only when each has the same <= 64 rows (a multiple of 8): two TMA boxes fill the tile, w_gate's
+// rows then w_noise's, so that x is read once per token tile.  Tiles are up to 128 logits wide when
+// 64-wide ones would need more than one wave of CTAs.  Small token counts split K across CTAs so that
+// about one CTA per SM streams the weights; the splits' partials are summed in a fixed order by the
+// selection kernel (deterministic).
 //
-// CTA = 6 warps: warp 0 issues the TMA loads into a ring of stages; warp 1 allocates TMEM and one lane
-// issues the MMAs, each 64-wide K block into a fresh accumulator (two, alternating); warps 2-5 add
-// every block's accumulator into float-float sums (so the tensor cores' fp32 rounding only ever spans
-// 64 products and the error bound does not grow with d), compute the squared norms of the x rows
-// (n-tile 0) and weight rows (m-tile 0) from the shared-memory tiles -- the selection kernel bounds
-// each logit's error by them -- and store the logits.
+// CTA = 12 warps: warp 0 issues the TMA loads into a ring of stages; warp 1 allocates TMEM and one lane
+// issues the MMAs, each 128-wide chunk of K (two blocks) into a fresh accumulator (up to 8 in rotation,
+// 512 TMEM columns); warps 2-9 (a TMEM lane quarter each, and one of two 64-column halves of the tile) add
+// every chunk's accumulator into compensated (Kahan) sums, so the tensor cores' fp32 rounding only ever
+// spans 128 products and the error bound does not grow with d; warps 10-11 compute the squared norms of the x
+// rows (n-tile 0) and weight rows (m-tile 0) from the shared-memory tiles -- the selection kernel bounds
+// each logit's error by them.  The logits leave through a shared-memory staging tile, a row at a time.
 // When one CTA can hold every logit of its tokens (softmax gate, E <= 64) the selection runs in the same
-// launch: a cluster of up to four CTAs per 128-token tile splits K, the CTAs add their float-float
+// launch: a cluster of up to four CTAs per 128-token tile splits K, the CTAs add their compensated
 // partials through distributed shared memory, and each selects its share of the rows, a warp per token
 // (select_row): top-k, near-tie re-scoring, gates; then the dispatch's pair ranks and block histograms,
 // and the dispatch scan in the last CTA -- the whole gate in one launch.
@@ -43,15 +47,19 @@ using gate::order_key;
 
 constexpr int kGM = 128, kGK = 64;
 constexpr int kGMaxStages = 12;  // TMA ring depth: as many stages as fit (the CTAs are few and latency-bound)
-constexpr int kGThreads = 320;  // producer, MMA, 4 accumulation warps, 4 norm warps
-constexpr int kGChunks = 8;     // TMEM accumulators the MMAs rotate through
-constexpr int kGMaxBN = 64;  // logits per n-tile: the epilogue holds 64 float-float sums per row
+constexpr int kGThreads = 384;  // producer, MMA, 8 accumulation warps, 2 norm warps
+constexpr int kGAccWarps = 8, kGNormWarp0 = 10;
+constexpr int kGChunks = 8;     // TMEM accumulators the MMAs rotate through (at most; 512 columns in all)
+constexpr int kGKChunk = 2;     // 64-wide K blocks an accumulator sums (8 MMA steps) before it is added
+constexpr int kGMaxBN = 128;    // logits per n-tile: two accumulation warps per row, 64 compensated sums each
+constexpr int kGFusedMaxBN = 64;  // fused selection: every logit of a token in one accumulation warp
+constexpr int kGStageStride = 64 + 4;  // epilogue staging: floats per row (16-byte stores conflict-free)
 constexpr uint32_t kGABytes = kGM * kGK * 2;  // 16 KiB
 constexpr int kGMaxCluster = 4;  // fused gate: CTAs splitting K per token tile (at most one per row quarter)
 
-// fused gate: each CTA's float-float partial logits (hi [BN][128], lo [BN][128], column-major so that a
-// warp reads 32 consecutive rows), x-row norms [128] and weight-row norms [kGMaxBN] over its K range
-__host__ __device__ constexpr size_t red_bytes(int BN) { return (size_t)(2 * BN * kGM + kGM + kGMaxBN) * 4; }
+// fused gate: each CTA's compensated partial logits (hi [BN][128], lo [BN][128], column-major so that a
+// warp reads 32 consecutive rows), x-row norms [128] and weight-row norms [kGFusedMaxBN] over its K range
+__host__ __device__ constexpr size_t red_bytes(int BN) { return (size_t)(2 * BN * kGM + kGM + kGFusedMaxBN) * 4; }
 
 struct GemmArgs {
     float* part;       // [S][T][Np]
@@ -61,6 +69,8 @@ struct GemmArgs {
     const bf16_t* w0;  // [N0, d]
     const bf16_t* w1;  // [N1, d] or nullptr
     int T, d, N0, N1, Np, BN, nt0, per, kb, stages;
+    int both;          // 1: one n-tile holds w_gate's N0 rows, then w_noise's N1 = N0 rows
+    int nch;           // TMEM accumulators in rotation
     int* err;
 };
 
@@ -86,7 +96,7 @@ __device__ __forceinline__ float sumsq_tile_row(const uint8_t* row, int r) {
 }
 
 constexpr int kGWarps = kGThreads / 32;
-constexpr int kLgStride = kGMaxBN + 1;  // row stride of the logits staged for the selection
+constexpr int kLgStride = kGFusedMaxBN + 1;  // row stride of the logits staged for the selection
 
 // Fused selection smem (softmax gate, all logits of a token in one CTA): per row the top-(k+1) values
 // and ids and the chosen ids, the rows' x norms and the weight-row norms, per warp the contenders of a
@@ -96,13 +106,13 @@ struct FusedSmem {
     int seli[kGM][kMaxTopK + 1];
     int fidx[kGM][kMaxTopK];
     float xn2[kGM];
-    float wn2[kGMaxBN];
+    float wn2[kGFusedMaxBN];
     int cand[kGWarps][kMaxCand];
     double ex[kGWarps][kMaxCand];
-    int running[4][kGMaxBN];
+    int running[4][kGFusedMaxBN];
     int part[kGThreads];
-    int padded[kGMaxBN + 1];
-    int kept[kGMaxBN];
+    int padded[kGFusedMaxBN + 1];
+    int kept[kGFusedMaxBN];
     int wsum[33];
     int last;
 };
@@ -249,9 +259,9 @@ __global__ void __launch_bounds__(kGThreads, 1)
     const int mt = FUSED ? blockIdx.y : blockIdx.x, nt = FUSED ? 0 : blockIdx.y;
     const int split = FUSED ? blockIdx.x : blockIdx.z;
     const int cs = FUSED ? (int)gridDim.x : 1;
-    const bool second = nt >= a.nt0;                        // tile of w_noise (noisy gate)
+    const bool second = !a.both && nt >= a.nt0;             // tile of w_noise (noisy gate)
     const int n_local = (second ? nt - a.nt0 : nt) * a.BN;  // first weight row of the tile
-    const int n_map = second ? a.N1 : a.N0;                 // rows of that weight tensor
+    const int n_map = a.both ? a.BN : second ? a.N1 : a.N0;  // rows of that weight tensor (both: of the two)
     const int col0 = (second ? a.N0 : 0) + n_local;         // first output column
     const int m0 = mt * kGM;
     const int kb0 = split * a.per, kb1 = min(a.kb, kb0 + a.per);
@@ -260,8 +270,9 @@ __global__ void __launch_bounds__(kGThreads, 1)
     const bool x_norms = FUSED || (a.xn2_part != nullptr && nt == 0);
     const bool w_norms = FUSED || (a.wn2_part != nullptr && mt == 0);
     const bool readers = x_norms || w_norms;  // the norm warps read the smem tiles too
+    const int nch = a.nch;
     uint32_t tcols = 32;
-    while (tcols < (uint32_t)(kGChunks * a.BN)) tcols <<= 1;
+    while (tcols < (uint32_t)(nch * a.BN)) tcols <<= 1;
 
     if (threadIdx.x == 0) {
         prefetch_tmap(&tmA);
@@ -269,11 +280,11 @@ __global__ void __launch_bounds__(kGThreads, 1)
         *abort_flag = 0;
         for (int s = 0; s < NS; ++s) {
             mbar_init(bar(FULL + s), 1);
-            mbar_init(bar(EMPTY + s), readers ? 5 : 1);
+            mbar_init(bar(EMPTY + s), readers ? 3 : 1);  // the MMAs' commit and the two norm warps
         }
         for (int s = 0; s < kGChunks; ++s) {
             mbar_init(bar(CFULL + s), 1);
-            mbar_init(bar(CEMPTY + s), 4);
+            mbar_init(bar(CEMPTY + s), a.BN > 64 ? 8 : 4);  // the accumulation warps with columns
         }
         mbar_init(bar(LAST), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -286,7 +297,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
     pdl_wait();  // the set-up above overlaps the previous kernel; its outputs are read below
     pdl_trigger();
 
-    float hi[BNC], lo[BNC];  // accumulation warps: the float-float logits of row r
+    float hi[BNC], lo[BNC];  // accumulation warps: the compensated sums (value hi + lo) of row r
 #pragma unroll
     for (int j = 0; j < BNC; ++j) hi[j] = lo[j] = 0.f;
     if (warp == 0) {
@@ -304,6 +315,9 @@ __global__ void __launch_bounds__(kGThreads, 1)
                 mbar_expect_tx(bar(FULL + stage), stage_bytes);
                 tma_load_2d(smem_u32(st), &tmA, bar(FULL + stage), kb * kGK, m0);
                 tma_load_2d(smem_u32(st + kGABytes), mb, bar(FULL + stage), kb * kGK, n_local);
+                if (a.both)  // w_noise's rows below w_gate's (N0 a multiple of 8: whole swizzle atoms)
+                    tma_load_2d(smem_u32(st + kGABytes + (uint32_t)a.N0 * 128u), &tmB1, bar(FULL + stage),
+                                kb * kGK, 0);
                 issued[stage] = true;
                 issued_phase[stage] = phase;
                 if (++stage == NS) { stage = 0; phase ^= 1u; }
@@ -317,16 +331,17 @@ __global__ void __launch_bounds__(kGThreads, 1)
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            // each 64-wide K block goes to a fresh accumulator (kGChunks of them, in turn), which the
-            // accumulation warps add into float-float sums: the tensor cores' rounding only ever spans 64
-            // products, and the MMAs run up to kGChunks blocks ahead of the additions
+            // each chunk of kGKChunk K blocks (128 products) goes to a fresh accumulator (nch of them, in
+            // turn), which the accumulation warps add into compensated sums: the tensor cores' rounding only
+            // ever spans 128 products, and the MMAs run up to nch chunks ahead of the additions
             const uint32_t idesc = idesc_bf16(kGM, a.BN);
             bool ok = true, any = false;
             int stage = 0;
             uint32_t phase = 0;
             for (int i = 0; i < nkb; ++i) {
-                const int buf = i % kGChunks;
-                if (!mbar_wait(bar(CEMPTY + buf), ((i / kGChunks) & 1) ^ 1u, abort_flag)) { ok = false; break; }
+                const int ci = i / kGKChunk, buf = ci % nch;
+                const bool first = i % kGKChunk == 0, last = i % kGKChunk == kGKChunk - 1 || i == nkb - 1;
+                if (first && !mbar_wait(bar(CEMPTY + buf), ((ci / nch) & 1) ^ 1u, abort_flag)) { ok = false; break; }
                 if (!mbar_wait(bar(FULL + stage), phase, abort_flag)) { ok = false; break; }
                 fence_after();
                 uint8_t* st = base + stage * stage_bytes;
@@ -335,10 +350,10 @@ __global__ void __launch_bounds__(kGThreads, 1)
                 const uint32_t d_tmem = tmem_base + (uint32_t)(buf * a.BN);
 #pragma unroll
                 for (int kk = 0; kk < kGK / 16; ++kk)
-                    mma_bf16(d_tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc, kk != 0);
+                    mma_bf16(d_tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc, !first || kk != 0);
                 any = true;
                 commit(bar(EMPTY + stage));
-                commit(bar(CFULL + buf));
+                if (last) commit(bar(CFULL + buf));
                 if (++stage == NS) { stage = 0; phase ^= 1u; }
             }
             if (!ok) {
@@ -350,10 +365,11 @@ __global__ void __launch_bounds__(kGThreads, 1)
                 mbar_wait_bounded(bar(LAST), 0);
             }
         }
-    } else if (warp >= 6) {
-        // norm warps: squared norms of the x rows and weight rows over this CTA's K range, from the tiles
-        const int nr = threadIdx.x - 192;  // 0..127
-        float xs = 0.f, wsq = 0.f;
+    } else if (warp >= kGNormWarp0) {
+        // norm warps: squared norms of the x rows and weight rows over this CTA's K range, from the tiles;
+        // thread nr takes rows nr and nr + 64
+        const int nr = threadIdx.x - 32 * kGNormWarp0;  // 0..63
+        float xs0 = 0.f, xs1 = 0.f, ws0 = 0.f, ws1 = 0.f;
         bool ok = true;
         int stage = 0;
         uint32_t phase = 0;
@@ -361,8 +377,12 @@ __global__ void __launch_bounds__(kGThreads, 1)
             ok = __all_sync(0xffffffffu, mbar_wait(bar(FULL + stage), phase, abort_flag));
             if (!ok) break;
             const uint8_t* st = base + stage * stage_bytes;
-            if (x_norms) xs += sumsq_tile_row(st + nr * 128, nr);
-            if (w_norms && nr < a.BN) wsq += sumsq_tile_row(st + kGABytes + nr * 128, nr);
+            if (x_norms) {
+                xs0 += sumsq_tile_row(st + nr * 128, nr);
+                xs1 += sumsq_tile_row(st + (nr + 64) * 128, nr + 64);
+            }
+            if (w_norms && nr < a.BN) ws0 += sumsq_tile_row(st + kGABytes + nr * 128, nr);
+            if (w_norms && nr + 64 < a.BN) ws1 += sumsq_tile_row(st + kGABytes + (nr + 64) * 128, nr + 64);
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(EMPTY + stage));
             if (++stage == NS) { stage = 0; phase ^= 1u; }
@@ -373,40 +393,47 @@ __global__ void __launch_bounds__(kGThreads, 1)
                 *abort_flag = 1;
             }
         } else if constexpr (!FUSED) {
-            if (x_norms && m0 + nr < a.T) a.xn2_part[(size_t)split * a.T + m0 + nr] = xs;
-            if (w_norms && nr < ncols) a.wn2_part[(size_t)split * a.Np + col0 + nr] = wsq;
+            if (x_norms && m0 + nr < a.T) a.xn2_part[(size_t)split * a.T + m0 + nr] = xs0;
+            if (x_norms && m0 + nr + 64 < a.T) a.xn2_part[(size_t)split * a.T + m0 + nr + 64] = xs1;
+            if (w_norms && nr < ncols) a.wn2_part[(size_t)split * a.Np + col0 + nr] = ws0;
+            if (w_norms && nr + 64 < ncols) a.wn2_part[(size_t)split * a.Np + col0 + nr + 64] = ws1;
         } else {
-            red[2 * a.BN * kGM + nr] = xs;
-            if (nr < kGMaxBN) red[2 * a.BN * kGM + kGM + nr] = nr < ncols ? wsq : 0.f;
+            red[2 * a.BN * kGM + nr] = xs0;
+            red[2 * a.BN * kGM + nr + 64] = xs1;
+            red[2 * a.BN * kGM + kGM + nr] = nr < ncols ? ws0 : 0.f;  // fused: BN <= 64
         }
+        // the stage ring is read no more: the accumulation warps may stage the logits in it
+        if constexpr (!FUSED) named_bar_arrive(1, 32 * (kGAccWarps + 2));
     } else {
-        // accumulation warps: one per TMEM lane quarter (32 rows)
+        // accumulation warps: a TMEM lane quarter (32 rows) and a 64-column half of the tile each
         const int q = warp & 3;
         const int r = q * 32 + lane;
-        // G = 64 / BNC accumulators per round: their TMEM loads are in flight together, then added
+        const int cb = ((warp - 2) >> 2) * 64;  // the warp's first column
+        const bool active = cb < a.BN;          // tiles of <= 64 logits leave warps 6-9 idle
+        // G = 64 / BNC accumulators per round: their TMEM loads are in flight together, then added.
+        // Compensated summation (Kahan: value = hi + lo, lo the running correction): the sum of n blocks
+        // errs by at most 2u * sum |block| + O(n u^2) (Higham, Accuracy and Stability of Numerical
+        // Algorithms, section 4.3) at four additions per block.
         constexpr int G = 64 / BNC;
+        const int nck = (nkb + kGKChunk - 1) / kGKChunk;  // accumulator chunks
         bool ok = true;
-        for (int i0 = 0; i0 < nkb && ok; i0 += G) {
-            const int ng = min(G, nkb - i0);
+        for (int i0 = 0; i0 < nck && ok && active; i0 += G) {
+            const int ng = min(G, nck - i0);
             for (int j = 0; j < ng && ok; ++j)
-                ok = __all_sync(0xffffffffu, mbar_wait(bar(CFULL + (i0 + j) % kGChunks), ((i0 + j) / kGChunks) & 1,
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(CFULL + (i0 + j) % nch), ((i0 + j) / nch) & 1,
                                                        abort_flag));
             if (!ok) break;
             fence_after();
             if constexpr (BNC == 64) {  // one accumulator per round, loaded 16 columns at a time
-                const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)((i0 % kGChunks) * a.BN);
+                const uint32_t tb =
+                    tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)((i0 % nch) * a.BN + cb);
 #pragma unroll
                 for (int c0 = 0; c0 < 64; c0 += 16) {
-                    if (c0 < a.BN) {
+                    if (cb + c0 < a.BN) {
                         uint32_t v[16];
                         tmem_ld16(tb + (uint32_t)c0, v);
 #pragma unroll
-                        for (int c = 0; c < 16; ++c) {
-                            float s_, e_;
-                            two_sum(hi[c0 + c], __uint_as_float(v[c]), s_, e_);
-                            hi[c0 + c] = s_;
-                            lo[c0 + c] += e_;
-                        }
+                        for (int c = 0; c < 16; ++c) kahan_add(hi[c0 + c], lo[c0 + c], __uint_as_float(v[c]));
                     }
                 }
             } else {
@@ -417,24 +444,19 @@ __global__ void __launch_bounds__(kGThreads, 1)
                 for (int c0 = 0; c0 < BNC; c0 += 16)
                     if (j < ng && c0 < a.BN)
                         tmem_ld16_async(tmem_base + ((uint32_t)(q * 32) << 16) +
-                                            (uint32_t)(((i0 + j) % kGChunks) * a.BN + c0),
+                                            (uint32_t)(((i0 + j) % nch) * a.BN + c0),
                                         *reinterpret_cast<uint32_t(*)[16]>(&v[j][c0]));
             tmem_wait_ld();
 #pragma unroll
             for (int j = 0; j < G; ++j)
 #pragma unroll
                 for (int c = 0; c < BNC; ++c)
-                    if (j < ng && c < a.BN) {  // blocks added in K order
-                        float s_, e_;
-                        two_sum(hi[c], __uint_as_float(v[j][c]), s_, e_);
-                        hi[c] = s_;
-                        lo[c] += e_;
-                    }
+                    if (j < ng && c < a.BN) kahan_add(hi[c], lo[c], __uint_as_float(v[j][c]));  // K order
             }
             fence_before();
             __syncwarp();
             if (lane == 0)
-                for (int j = 0; j < ng; ++j) mbar_arrive(bar(CEMPTY + (i0 + j) % kGChunks));
+                for (int j = 0; j < ng; ++j) mbar_arrive(bar(CEMPTY + (i0 + j) % nch));
         }
         if (!ok) {
             if (lane == 0) {
@@ -443,14 +465,27 @@ __global__ void __launch_bounds__(kGThreads, 1)
             }
         }
         if constexpr (!FUSED) {
-            const int row = m0 + r;
-            if (ok && row < a.T) {
-                float* dst = a.part + ((size_t)split * a.T + row) * a.Np + col0;
+            // through a staging tile in the (finished) stage ring: each thread writes its row, then the
+            // warp stores row after row, 128 contiguous bytes per instruction
+            named_bar_sync(1, 32 * (kGAccWarps + 2));  // every norm warp is done with the ring
+            float* stg = reinterpret_cast<float*>(base) + (size_t)(warp - 2) * 32 * kGStageStride;
+            const int wcols = min(min(BNC, a.BN - cb), ncols - cb);
+            if (ok && active && wcols > 0) {
 #pragma unroll
-                for (int j = 0; j < BNC; ++j)
-                    if (j < ncols) dst[j] = hi[j] + lo[j];
+                for (int j = 0; j < BNC; j += 4)
+                    *reinterpret_cast<float4*>(stg + lane * kGStageStride + j) =
+                        make_float4(hi[j] + lo[j], hi[j + 1] + lo[j + 1], hi[j + 2] + lo[j + 2], hi[j + 3] + lo[j + 3]);
+                __syncwarp();
+                const int rows = min(32, a.T - (m0 + q * 32));
+                float* dst = a.part + ((size_t)split * a.T + m0 + q * 32) * a.Np + col0 + cb;
+#pragma unroll
+                for (int rr = 0; rr < 32; ++rr)
+#pragma unroll
+                    for (int c0 = 0; c0 < BNC; c0 += 32)
+                        if (rr < rows && c0 + lane < wcols)
+                            dst[(size_t)rr * a.Np + c0 + lane] = stg[rr * kGStageStride + c0 + lane];
             }
-        } else {
+        } else if (active) {
 #pragma unroll
             for (int j = 0; j < BNC; ++j)
                 if (j < a.BN) {
@@ -503,7 +538,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
                 if (j < a.BN) lg[r * kLgStride + j] = hi[j] + lo[j];
             fs.xn2[r] = xs;
             if (q == split) {  // the first quarter's warp also sums the weight-row norms
-                for (int j = lane; j < kGMaxBN; j += 32) {
+                for (int j = lane; j < kGFusedMaxBN; j += 32) {
                     float w = 0.f;
                     for (int c = 0; c < cs; ++c)
                         w += static_cast<const float*>(__cluster_map_shared_rank(red, (unsigned)c))[2 * a.BN * kGM + kGM + j];
@@ -557,22 +592,33 @@ __global__ void __launch_bounds__(kGThreads, 1)
 
 GateGemmPlan gate_gemm_plan(int T, int d, int N0, int N1, int sms, bool fuse_select) {
     GateGemmPlan g{};
-    g.fused = fuse_select && N1 == 0 && N0 <= kGMaxBN;
+    g.fused = fuse_select && N1 == 0 && N0 <= kGFusedMaxBN;
     g.cs = 1;
     if (g.fused) {
-        // a cluster of cs CTAs per token tile splits K; their float-float partials meet in shared memory,
+        // a cluster of cs CTAs per token tile splits K; their compensated partials meet in shared memory,
         // so the selecting CTA still sees every logit of its tokens.  As many as keep one wave.
         const long mtiles = (T + kGM - 1) / kGM;
         for (int c = kGMaxCluster; c > 1; c >>= 1)
             if (c <= d / kGK && mtiles * c <= sms) { g.cs = c; break; }
         sms = 1;  // no split-K partials in global memory
     }
-    const int nmax = N0 > N1 ? N0 : N1;
-    g.BN = nmax >= kGMaxBN ? kGMaxBN : (nmax + 15) / 16 * 16;
-    if (g.BN < 16) g.BN = 16;
-    g.nt0 = (N0 + g.BN - 1) / g.BN;
-    g.nt1 = N1 > 0 ? (N1 + g.BN - 1) / g.BN : 0;
     g.mt = (T + kGM - 1) / kGM;
+    const int nmax = N0 > N1 ? N0 : N1;
+    // 64-wide tiles, or up to 128 wide when 64-wide ones would take more than one wave
+    const long tiles64 = (long)g.mt * ((N0 + 63) / 64 + (N1 + 63) / 64);
+    const int bn_max = !g.fused && tiles64 > sms ? kGMaxBN : kGFusedMaxBN;
+    g.both = !g.fused && N1 == N0 && 2 * N0 <= bn_max && N0 % 8 == 0;
+    if (g.both) {
+        g.BN = 2 * N0;  // one tile: w_gate's rows, then w_noise's
+        g.nt0 = 1;
+        g.nt1 = 0;
+    } else {
+        g.BN = nmax >= bn_max ? bn_max : (nmax + 15) / 16 * 16;
+        if (g.BN < 16) g.BN = 16;
+        g.nt0 = (N0 + g.BN - 1) / g.BN;
+        g.nt1 = N1 > 0 ? (N1 + g.BN - 1) / g.BN : 0;
+    }
+    g.nch = 512 / g.BN < kGChunks ? 512 / g.BN : kGChunks;
     g.kb = d / kGK;
     g.Np = N0 + N1;
     const long tiles = (long)g.mt * (g.nt0 + g.nt1);
@@ -587,8 +633,10 @@ GateGemmPlan gate_gemm_plan(int T, int d, int N0, int N1, int sms, bool fuse_sel
     g.stages = (int)((200 * 1024 - fixed) / (stage_bytes + 16));
     if (g.stages > kGMaxStages) g.stages = kGMaxStages;
     if (g.stages > g.per) g.stages = g.per < 2 ? 2 : g.per;
-    // the fused selection stages the tile's logits in the stage ring once the K loop is done
-    while (g.fused && (size_t)g.stages * stage_bytes < (size_t)kGM * kLgStride * 4) ++g.stages;
+    // after the K loop the stage ring holds the fused selection's logits, or the epilogue's staging tiles
+    const size_t after = g.fused ? (size_t)kGM * kLgStride * 4
+                                 : (size_t)(g.BN > 64 ? kGAccWarps : 4) * 32 * kGStageStride * 4;
+    while ((size_t)g.stages * stage_bytes < after) ++g.stages;
     g.smem = fixed + (size_t)g.stages * (stage_bytes + 16);
     return g;
 }
@@ -599,9 +647,10 @@ cudaError_t launch_gate_gemm(const GateGemmPlan& g, const void* x, const void* w
     if (T <= 0) return cudaSuccess;
     CUtensorMap ma, mb0, mb1;
     if (!tma_map_bf16(x, (uint64_t)d, (uint64_t)T, 0, kGM, &ma)) return cudaErrorInvalidValue;
-    if (!tma_map_bf16(w0, (uint64_t)d, (uint64_t)N0, 0, (uint32_t)g.BN, &mb0)) return cudaErrorInvalidValue;
+    const uint32_t box_rows = (uint32_t)(g.both ? N0 : g.BN);
+    if (!tma_map_bf16(w0, (uint64_t)d, (uint64_t)N0, 0, box_rows, &mb0)) return cudaErrorInvalidValue;
     if (N1 > 0) {
-        if (!tma_map_bf16(w1, (uint64_t)d, (uint64_t)N1, 0, (uint32_t)g.BN, &mb1)) return cudaErrorInvalidValue;
+        if (!tma_map_bf16(w1, (uint64_t)d, (uint64_t)N1, 0, box_rows, &mb1)) return cudaErrorInvalidValue;
     } else {
         mb1 = mb0;
     }
@@ -622,6 +671,8 @@ cudaError_t launch_gate_gemm(const GateGemmPlan& g, const void* x, const void* w
     a.per = g.per;
     a.kb = g.kb;
     a.stages = g.stages;
+    a.both = g.both ? 1 : 0;
+    a.nch = g.nch;
     a.err = err;
     const dim3 grid = g.fused ? dim3(g.cs, g.mt, 1) : dim3(g.mt, g.nt0 + g.nt1, g.S);
     if (g.fused && sel == nullptr) return cudaErrorInvalidValue;
@@ -652,7 +703,7 @@ cudaError_t launch_gate_gemm(const GateGemmPlan& g, const void* x, const void* w
             : g.BN <= 32 ? go(gate_gemm_kernel<true, 32>, *sel) : go(gate_gemm_kernel<true, 64>, *sel);
     else
         e = g.BN <= 16 ? go(gate_gemm_kernel<false, 16>, none)
-            : g.BN <= 32 ? go(gate_gemm_kernel<false, 32>, none) : go(gate_gemm_kernel<false, 64>, none);
+            : g.BN <= 32 ? go(gate_gemm_kernel<false, 32>, none) : go(gate_gemm_kernel<false, 64>, none);  // per warp
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

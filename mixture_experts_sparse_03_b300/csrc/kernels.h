@@ -63,7 +63,9 @@ cudaError_t launch_gate_rescore(const GateParams& p, cudaStream_t s);   // works
 constexpr int kGateMaxSplits = 8;
 constexpr int kPlanSms = 148;  // SM count the split-K plan (and so the workspace size) assumes
 struct GateGemmPlan {
-    int BN;        // logits per n-tile (multiple of 16, <= 256)
+    int BN;        // logits per n-tile (multiple of 16, <= 128)
+    bool both;     // one n-tile holds both weight tensors' rows (N0 == N1, a multiple of 8, 2 N0 <= 128)
+    int nch;       // TMEM accumulators the MMAs rotate through
     int nt0, nt1;  // n-tiles over the first / second weight tensor
     int mt;        // 128-token tiles
     int kb;        // 64-wide K blocks
