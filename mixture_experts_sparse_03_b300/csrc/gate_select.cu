@@ -5,7 +5,9 @@
 //   select   one warp per token, 32 tokens per CTA: sums the token's partials in split order and forms
 //            the scores -- softmax gate: the logit; noisy gate: clean + eps * softplus(noise)
 //            (NoisyTopKGating, "MoE sparse-compute acceleration", section 2.1); cosine gate:
-//            cos(u, e_j) / temperature with u = x P^T (Tutel's cosine_top) -- with a bound on each
+//            cos(u, e_j) / temperature with u = x P^T (Tutel's cosine_top), the dot products u . e_j of
+//            the CTA's 32 tokens computed together from shared memory, 4 tokens x 4 experts a lane
+//            in registers (the warp per token keeps the norms and the selection) -- with a bound on each
 //            score's error from the tensor-core accumulation bound cb |x| |w|, and picks the top-(k+1)
 //            by warp-shuffle argmax (ties -> lower expert id).  If two of them lie within twice the
 //            bound, the token goes to a global queue with its contenders (every expert within twice the
@@ -33,13 +35,21 @@ namespace {
 using namespace gate;
 
 constexpr int kBT = kTokensPerBlock;  // tokens per CTA, one warp each
-constexpr int kFewExperts = 16;       // cosine scores with at most this many experts: lanes split u
 constexpr int kSelThreads = 32 * kBT;
 constexpr int kSel = kMaxTopK + 1;
 
 struct SelLayout {
-    size_t logits, sc, wn2, embs, embn, selv, seli, cand, total;
+    size_t logits, sc, wn2, embs, embn, tokn, cpart, selv, seli, cand, total;
 };
+
+// cosine scores from staged embeddings: the dot products u . e of the CTA's 32 tokens are split over
+// kCosSlices ranges of the p components, a warp per (range, group of kCosGroup experts), lane = token
+constexpr int kCosSlices = 8;
+constexpr int kCosGroup = 16;
+// row stride of the staged logits: the cosine gate's u rows are padded to an odd length so that the
+// score loop's 32 lanes (32 token rows, one component each) fall in distinct banks
+__host__ __device__ inline int sel_ld(int gate, int N) { return gate == kGateCosine ? N + 1 : N; }
+__host__ __device__ inline int e32(int E) { return (E + kCosGroup - 1) / kCosGroup * kCosGroup; }
 
 __host__ __device__ inline size_t al16(size_t v) { return (v + 15) / 16 * 16; }
 
@@ -49,11 +59,13 @@ __host__ __device__ inline SelLayout sel_layout(int gate, int E, int p, int stag
     SelLayout L;
     size_t o = 0;
     auto take = [&](size_t bytes, size_t al) { o = (o + al - 1) / al * al; size_t r = o; o += bytes; return r; };
-    L.logits = take(4 * (size_t)kBT * N, 16);
+    L.logits = take(4 * (size_t)kBT * sel_ld(gate, N), 16);
     L.sc = take(cos ? 4 * (size_t)kBT * E : 0, 16);
     L.wn2 = take(4 * (size_t)N, 16);
-    L.embs = take(stage ? 4 * (size_t)p * (E + 1) : 0, 16);
+    L.embs = take(stage ? 4 * (size_t)p * e32(E) : 0, 16);  // transposed [p][E rounded up to 16], zero-filled
     L.embn = take(cos ? 4 * (size_t)E : 0, 16);
+    L.tokn = take(cos ? 4 * 2 * (size_t)kBT : 0, 16);
+    L.cpart = take(stage ? 4 * (size_t)kCosSlices * kBT * e32(E) : 0, 16);
     L.selv = take(4 * kBT * kSel, 16);
     L.seli = take(4 * kBT * kSel, 16);
     L.cand = take(4 * kBT * kMaxCand, 16);
@@ -72,6 +84,9 @@ __global__ void __launch_bounds__(kSelThreads) gate_select_kernel(const GatePara
     float* wn2 = reinterpret_cast<float*>(smem + L.wn2);
     float* embs = reinterpret_cast<float*>(smem + L.embs);
     float* embn = reinterpret_cast<float*>(smem + L.embn);
+    float* tok_nuc = reinterpret_cast<float*>(smem + L.tokn);  // cosine: per token max(|u|, tiny)
+    float* tok_rel = tok_nuc + kBT;                              // and the relative error bound of its cosines
+    float* cpart = reinterpret_cast<float*>(smem + L.cpart);     // cosine: [slice][token][expert] partial dots
     float* selv_all = reinterpret_cast<float*>(smem + L.selv);
     int* seli_all = reinterpret_cast<int*>(smem + L.seli);
     int* cand_all = reinterpret_cast<int*>(smem + L.cand);
@@ -81,6 +96,7 @@ __global__ void __launch_bounds__(kSelThreads) gate_select_kernel(const GatePara
     const int ntok = min(kBT, P.T - tok0);
     const int E = P.E, k = P.k;
     const int N = GATE == kGateSoftmax ? E : GATE == kGateNoisy ? 2 * E : P.p;
+    const int ldL = sel_ld(GATE, N);
 
     // ---- CTA: weight-row squared norms (sum of the split partials); cosine: embedding norms
     for (int n = tid; n < N; n += kSelThreads) {
@@ -107,25 +123,47 @@ __global__ void __launch_bounds__(kSelThreads) gate_select_kernel(const GatePara
             s = warp_sum(s);
             if (lane == 0) embn[e] = sqrtf(s);
         }
-        // the embeddings transposed into shared memory, rows padded to E + 1 so that neither these
-        // stores (consecutive threads: consecutive j) nor the score loop's loads (lanes: experts) conflict
-        if (stage)
-            for (int i = tid; i < P.p * E; i += kSelThreads) {
-                const int e = i / P.p, j = i - e * P.p;
-                embs[j * (E + 1) + e] = load1(emb + (size_t)e * P.p + j);
+        // the embeddings transposed into shared memory as fp32 [p][E32] (E32: E rounded up to 16, the
+        // extra columns zero), so that the score loop reads 4 experts of a component with one broadcast
+        // 16-byte load; consecutive threads take consecutive experts (p is a multiple of 8)
+        if (stage) {
+            const int E32 = e32(E), pc = P.p / 8;
+            for (int i = tid; i < E32 * pc; i += kSelThreads) {
+                const int e = i % E32, j = (i / E32) * 8;
+                float v[8];
+                if (e < E) {
+                    load8(emb + (size_t)e * P.p + j, v);
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) v[q] = 0.f;
+                }
+#pragma unroll
+                for (int q = 0; q < 8; ++q) embs[(size_t)(j + q) * E32 + e] = v[q];
             }
+        }
     }
     __syncthreads();
 
-    // ---- one warp per token
+    // ---- one warp per token: the partial logits summed, and the scores (cosine with staged embeddings:
+    // the norms of u here, the scores by the whole CTA below)
     const int tt = warp, t = tok0 + tt;
     float* selv = selv_all + tt * kSel;
     int* seli = seli_all + tt * kSel;
     int* cand = cand_all + tt * kMaxCand;
+    float* Lr = logits + (size_t)tt * ldL;
+    float* sc = GATE == kGateCosine ? scs + (size_t)tt * E : Lr;  // scores (in place unless cosine)
+    const bool blocked = GATE == kGateCosine && stage;  // CTA-wide score step between two barriers
+    float dmax = 0.f;
     if (tt < ntok) {
-        float* Lr = logits + (size_t)tt * N;
         float xq = 0.f;
         for (int sp = lane; sp < P.S; sp += 32) xq += P.xn2p[(size_t)sp * P.T + t];
+        // the noisy gate's eps entries of experts lane and lane + 32 are loaded now, with the partials,
+        // instead of after them (further ones when they are needed)
+        float ep0 = 0.f, ep1 = 0.f;
+        if (GATE == kGateNoisy) {
+            if (lane < E) ep0 = P.eps[(size_t)t * E + lane];
+            if (lane + 32 < E) ep1 = P.eps[(size_t)t * E + lane + 32];
+        }
         // the splits' partials, summed in split order: a lane takes columns lane + 32 c, eight columns
         // of two splits (sixteen loads) in flight at a time
         {
@@ -158,14 +196,12 @@ __global__ void __launch_bounds__(kSelThreads) gate_select_kernel(const GatePara
         }
         const float xn = sqrtf(warp_sum(xq));
         __syncwarp();
-        float* sc = GATE == kGateCosine ? scs + (size_t)tt * E : Lr;  // scores (in place unless cosine)
-        float dmax = 0.f;
         if (GATE == kGateSoftmax) {
             for (int e = lane; e < E; e += 32) dmax = fmaxf(dmax, P.cb * xn * sqrtf(wn2[e]) + 4.f * kU * fabsf(Lr[e]));
         } else if (GATE == kGateNoisy) {
             for (int e = lane; e < E; e += 32) {
                 const float c = Lr[e], z = Lr[E + e];
-                const float ep = P.eps[(size_t)t * E + e];
+                const float ep = e == lane ? ep0 : e == lane + 32 ? ep1 : P.eps[(size_t)t * E + e];
                 const float sp = softplus_f(z);
                 const float s = fmaf(ep, sp, c);
                 sc[e] = s;
@@ -189,61 +225,84 @@ __global__ void __launch_bounds__(kSelThreads) gate_select_kernel(const GatePara
             // |cos(u~, e) - cos(u, e)| <= 2 |u~ - u| / |u|; the fp32 dot, norms and division add (2p + 8) u
             const float rel = nu > 2.f * Dl ? (2.f * p + 8.f) * kU + 2.f * Dl / (nu - Dl) : INFINITY;
             const float nuc = fmaxf(nu, 1e-12f);
-            const T* emb = static_cast<const T*>(P.emb);
-            if (stage && E <= kFewExperts) {
-                // few experts: the lanes split u instead (components lane, lane + 32, ...) and each keeps a
-                // partial dot for every expert, reduced across the warp at the end -- all 32 lanes busy
-                // instead of E; a p-term sum in another order stays within the same (2p + 8) u bound
-                float acc[kFewExperts];
-#pragma unroll
-                for (int q = 0; q < kFewExperts; ++q) acc[q] = 0.f;
-                for (int j = lane; j < p; j += 32) {
-                    const float u = Lr[j];
-                    const float* er = embs + j * (E + 1);
-#pragma unroll
-                    for (int q = 0; q < kFewExperts; ++q)
-                        if (q < E) acc[q] = fmaf(u, er[q], acc[q]);
+            if (blocked) {
+                if (lane == 0) {
+                    tok_nuc[tt] = nuc;
+                    tok_rel[tt] = rel;
                 }
-#pragma unroll
-                for (int q = 0; q < kFewExperts; ++q) {
-                    if (q >= E) break;
-                    const float dot = warp_sum(acc[q]);
-                    if (lane == q) {
-                        const float sv = dot / (nuc * fmaxf(embn[q], 1e-12f)) * P.inv_temp;
-                        sc[q] = sv;
-                        dmax = fmaxf(dmax, rel * P.inv_temp + 4.f * kU * fabsf(sv));
-                    }
-                }
-            } else
-            for (int e = lane; e < E; e += 32) {
-                float dot = 0.f;
-                // four interleaved partial sums (p is a multiple of 8): u is read four components at a
-                // time (one broadcast 16-byte load) and the four FMA chains overlap; the error stays
-                // within the (2p + 8) u bound of a p-term dot product
-                float d4[4] = {0.f, 0.f, 0.f, 0.f};
-                if (stage) {
-#pragma unroll 2
-                    for (int j = 0; j < p; j += 4) {
-                        const float4 u4 = *reinterpret_cast<const float4*>(Lr + j);
-                        d4[0] = fmaf(u4.x, embs[(j + 0) * (E + 1) + e], d4[0]);
-                        d4[1] = fmaf(u4.y, embs[(j + 1) * (E + 1) + e], d4[1]);
-                        d4[2] = fmaf(u4.z, embs[(j + 2) * (E + 1) + e], d4[2]);
-                        d4[3] = fmaf(u4.w, embs[(j + 3) * (E + 1) + e], d4[3]);
-                    }
-                } else {
+            } else {
+                const T* emb = static_cast<const T*>(P.emb);
+                for (int e = lane; e < E; e += 32) {
+                    // four interleaved partial sums (p is a multiple of 8); the error stays within the
+                    // (2p + 8) u bound of a p-term dot product
+                    float d4[4] = {0.f, 0.f, 0.f, 0.f};
                     for (int j = 0; j < p; j += 8) {
                         float ev[8];
                         load8(emb + (size_t)e * p + j, ev);
 #pragma unroll
                         for (int q = 0; q < 8; ++q) d4[q & 3] = fmaf(Lr[j + q], ev[q], d4[q & 3]);
                     }
+                    const float dot = (d4[0] + d4[1]) + (d4[2] + d4[3]);
+                    const float s = dot / (nuc * fmaxf(embn[e], 1e-12f)) * P.inv_temp;
+                    sc[e] = s;
+                    dmax = fmaxf(dmax, rel * P.inv_temp + 4.f * kU * fabsf(s));
                 }
-                dot = (d4[0] + d4[1]) + (d4[2] + d4[3]);
-                const float s = dot / (nuc * fmaxf(embn[e], 1e-12f)) * P.inv_temp;
-                sc[e] = s;
-                dmax = fmaxf(dmax, rel * P.inv_temp + 4.f * kU * fabsf(s));
             }
         }
+    }
+    if (blocked) {
+        // cosine scores of the CTA's tokens: warp task (expert group g of kCosGroup, component range r)
+        // covers the 32 tokens, lane (a, b) four tokens a + 8 i and four experts 4 b + q of the group, their
+        // 16 partial dots in registers: per component four loads of u (eight distinct rows, odd stride:
+        // conflict-free) and four of the experts' values (four distinct addresses) for 16 FMAs.  The ranges'
+        // partial sums are then added in range order; a p-term dot product summed in this order stays within
+        // the (2p + 8) u bound.
+        __syncthreads();
+        const int p = P.p, E32 = e32(E), ngr = E32 / kCosGroup, jl = p / kCosSlices;  // p: a multiple of 8
+        const int la = lane & 7, lb = lane >> 3;
+        for (int task = warp; task < ngr * kCosSlices; task += kBT) {
+            const int g = task / kCosSlices, r = task % kCosSlices;
+            float acc[4][4];
+#pragma unroll
+            for (int a = 0; a < 4; ++a)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) acc[a][q] = 0.f;
+            const float* ur = logits + (size_t)la * ldL;
+            const float* er = embs + g * kCosGroup + 4 * lb;
+#pragma unroll 2
+            for (int j = r * jl; j < (r + 1) * jl; ++j) {
+                float u[4], ev[4];
+#pragma unroll
+                for (int a = 0; a < 4; ++a) u[a] = ur[(size_t)(8 * a) * ldL + j];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) ev[q] = er[(size_t)j * E32 + q];
+#pragma unroll
+                for (int a = 0; a < 4; ++a)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) acc[a][q] = fmaf(u[a], ev[q], acc[a][q]);
+            }
+#pragma unroll
+            for (int a = 0; a < 4; ++a)
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    cpart[((size_t)r * kBT + la + 8 * a) * E32 + g * kCosGroup + 4 * lb + q] = acc[a][q];
+        }
+        __syncthreads();
+        for (int i = tid; i < ntok * E; i += kSelThreads) {
+            const int tq = i / E, e = i - tq * E;
+            float dot = 0.f;
+#pragma unroll
+            for (int r = 0; r < kCosSlices; ++r) dot += cpart[((size_t)r * kBT + tq) * E32 + e];
+            scs[(size_t)tq * E + e] = dot / (tok_nuc[tq] * fmaxf(embn[e], 1e-12f)) * P.inv_temp;
+        }
+        __syncthreads();
+        if (tt < ntok) {
+            float smax = 0.f;
+            for (int e = lane; e < E; e += 32) smax = fmaxf(smax, fabsf(sc[e]));
+            dmax = tok_rel[tt] * P.inv_temp + 4.f * kU * smax;
+        }
+    }
+    if (tt < ntok) {
         dmax = warp_max(dmax) * 1.0625f;
         __syncwarp();
 
