@@ -330,13 +330,28 @@ moe_status run_ffn(const Plan& P, const moe_config* c, const FfnParams& f, cudaS
 
 // expert FFN + (fused or separate) combine, shared by moe_expert_ffn(_fp8) and moe_forward(_fp8); s1 / s2
 // are the block scales of FP8 weights (nullptr: bf16 / fp32 weights)
+// whether the up projection's kernel clears `out` for the fused combine while it runs: the single-SM
+// tensor-core kernel (bf16 weights, not on pairs of SMs), and only where its work hides the 4 d bytes per
+// token (rows x h at least 8192 per token: the headline layer's up projection runs ~40x longer than the
+// clearing, `bf16_cosine_skew`'s ~5x, where it measured +4 us against the gather's -4 us); otherwise the
+// gather clears it
+bool up_clears_out(const Plan& P, const moe_config* c, const float* s1) {
+    return P.fused && P.bf16 && !(c->flags & MOE_FLAG_SIMT_FFN) && s1 == nullptr && !P.pair &&
+           (int64_t)P.rows * P.h >= (int64_t)8192 * P.T;
+}
+
 moe_status ffn_and_combine(const Plan& P, const moe_config* c, const void* xd, const int* off, const int* rtok,
                            const float* rgate, const void* w1, const float* s1, const void* b1, const void* w2,
                            const float* s2, const void* b2, float* y, float* out, bool fused, void* ws,
-                           cudaStream_t s) {
+                           cudaStream_t s, bool clear_out = false) {
     int* err = at<int>(ws, P.o_err);
     void* hbuf = at<void>(ws, P.o_h);
-    MOE_TRY(run_ffn(P, c, ffn_params(P, 0, xd, w1, s1, b1, off, rtok, rgate, hbuf, nullptr, err), s));
+    FfnParams up = ffn_params(P, 0, xd, w1, s1, b1, off, rtok, rgate, hbuf, nullptr, err);
+    if (clear_out) {
+        up.zero = out;
+        up.zero_n = (int64_t)P.T * P.d;
+    }
+    MOE_TRY(run_ffn(P, c, up, s));
     if (fused) return run_ffn(P, c, ffn_params(P, 2, hbuf, w2, s2, b2, off, rtok, rgate, nullptr, out, err), s);
     return run_ffn(P, c, ffn_params(P, 1, hbuf, w2, s2, b2, off, rtok, rgate, y, nullptr, err), s);
 }
@@ -456,9 +471,13 @@ moe_status forward_impl(const moe_config* cfg, const void* x, const void* w_gate
     float* y = at<float>(workspace, P.o_y);
     // error word, its info, the block tickets and the cosine gate's expert flags start at zero
     if (cudaMemsetAsync(err, 0, P.hdr_bytes, s) != cudaSuccess) return MOE_ERR_CUDA;
-    MOE_TRY(route_and_dispatch(P, cfg, x, w_gate, w_noise, noise_eps, proj, expert_emb, count, P.fused ? out : nullptr,
-                               workspace, s));
-    MOE_TRY(ffn_and_combine(P, cfg, xd, off, rtok, rgate, w1, s1, b1, w2, s2, b2, y, out, P.fused != 0, workspace, s));
+    // the fused combine adds into `out`, cleared first: by the up projection's kernel when it can (in the
+    // GEMM's shadow), else by the gather
+    const bool clear_in_up = up_clears_out(P, cfg, s1);
+    MOE_TRY(route_and_dispatch(P, cfg, x, w_gate, w_noise, noise_eps, proj, expert_emb, count,
+                               P.fused && !clear_in_up ? out : nullptr, workspace, s));
+    MOE_TRY(ffn_and_combine(P, cfg, xd, off, rtok, rgate, w1, s1, b1, w2, s2, b2, y, out, P.fused != 0, workspace, s,
+                            clear_in_up));
     if (!P.fused) MOE_TRY(launch(s, [&] { return launch_combine(y, slot, off, idx, gate, P.T, P.k, P.d, out, s); }));
     return MOE_OK;
 }

@@ -62,6 +62,8 @@ struct TcArgs {
     bf16_t* aux;         // modes 3 / 4: the pre-activations Z [rows, N] (read / written)
     int M;               // weight-gradient kernel: rows of each expert's output [M, N]
     int b_mn;            // single-SM kernel: B is [E, K, N] (N contiguous), read MN-major
+    float* zero;         // single-SM kernel, forward bf16 row output: cleared by one extra warp, or nullptr
+    long long zero_n4;   // its length in float4
 };
 
 using namespace tc;
@@ -313,9 +315,12 @@ __device__ __forceinline__ const float* stage_bias(const TcArgs& a, float* wbias
 }
 
 // kStaged: the bf16 row-output modes (0, 4) with the staged epilogue; the other modes are compiled apart from
-// it, so that each keeps its own register allocation
+// it, so that each keeps its own register allocation.  The forward's up projection (mode 0) has a seventh
+// warp that clears a buffer (TcArgs::zero: the fp32 output the fused combine then adds into) while the
+// GEMM runs: its 4 bytes per output element are written in the GEMM's shadow, not by the gather.
+__host__ __device__ constexpr int tc_threads(bool bwd, bool staged) { return kThreads + (!bwd && staged ? 32 : 0); }
 template <bool kBwd, bool kStaged>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(tc_threads(kBwd, kStaged), 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const TcArgs a) {
     extern __shared__ uint8_t smem_raw[];
     // the 128-byte swizzle atoms need 1024-byte aligned tiles in the shared address space
@@ -354,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     pdl_wait();  // the set-up above overlaps the previous kernel; its outputs are read from here on
     pdl_trigger();
-    for (int i = threadIdx.x; i <= a.E; i += kThreads) s_off[i] = a.offset[i];
+    for (int i = threadIdx.x; i <= a.E; i += blockDim.x) s_off[i] = a.offset[i];
     fence_before();
     __syncthreads();
     fence_after();
@@ -441,6 +446,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (any) {  // all MMAs this thread issued have finished once LAST completes
                 commit(bar(LAST));
                 mbar_wait_bounded(bar(LAST), 0);
+            }
+        }
+    } else if (warp == kThreads / 32) {
+        // the clearing warp (forward up projection only): its CTA's share of the buffer, 16 bytes a lane
+        if constexpr (!kBwd && kStaged) {
+            if (a.zero != nullptr) {
+                const long long per = (a.zero_n4 + gridDim.x - 1) / gridDim.x;
+                const long long z0 = (long long)blockIdx.x * per, z1 = min(a.zero_n4, z0 + per);
+                float4* z = reinterpret_cast<float4*>(a.zero);
+                for (long long i = z0 + lane; i < z1; i += 32) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
             }
         }
     } else {
@@ -1500,7 +1515,8 @@ int fp8_ring_depth(int E, bool bias, bool swap) {
 
 cudaError_t launch_ffn_tc(const FfnParams& P, cudaStream_t s) {
     if (!P.bf16) return cudaErrorInvalidValue;
-    if (P.rows_cap <= 0) return cudaSuccess;
+    if (P.w_scale != nullptr && P.zero != nullptr) return cudaErrorInvalidValue;
+    if (P.rows_cap <= 0) return P.zero != nullptr ? cudaMemsetAsync(P.zero, 0, (size_t)P.zero_n * 4, s) : cudaSuccess;
     CUtensorMap ma, mb;
     if (P.w_scale != nullptr) {  // block-FP8 weights: byte codes, single-SM tiles
         if (P.K % kF8Block || P.N % kF8Block) return cudaErrorInvalidValue;
@@ -1548,6 +1564,11 @@ cudaError_t launch_ffn_tc(const FfnParams& P, cudaStream_t s) {
     a.aux = static_cast<bf16_t*>(P.aux);
     a.M = 0;
     a.b_mn = P.w_kn;
+    a.zero = nullptr;
+    a.zero_n4 = 0;
+    if (P.zero != nullptr && (P.pair || P.mode != 0 || P.zero_n % 4 != 0 ||
+                              (reinterpret_cast<uintptr_t>(P.zero) & 15)))
+        return cudaErrorInvalidValue;  // only the single-SM up projection clears a buffer
     if (P.pair) {
         // pairs of SMs: B boxes of 128 weight rows (half of a 256-wide tile), grid = 2 x the clusters that fit
         CUtensorMap mb2;
@@ -1571,7 +1592,16 @@ cudaError_t launch_ffn_tc(const FfnParams& P, cudaStream_t s) {
     const int64_t max_tiles = (P.rows_cap / kBM) * (int64_t)((P.N + kBN - 1) / kBN);
     int grid = device_sm_count();
     if (max_tiles < grid) grid = (int)(max_tiles > 0 ? max_tiles : 1);
-    return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, s, ma, mb, a);
+    if (P.zero != nullptr) {
+        if (2 * grid < device_sm_count()) {  // few tiles: the CTAs' clearing warps would be too few
+            cudaError_t ez = cudaMemsetAsync(P.zero, 0, (size_t)P.zero_n * 4, s);
+            if (ez != cudaSuccess) return ez;
+        } else {
+            a.zero = P.zero;
+            a.zero_n4 = P.zero_n / 4;
+        }
+    }
+    return launch_pdl(kern, dim3(grid), dim3(tc_threads(bwd, staged)), smem, s, ma, mb, a);
 }
 
 }  // namespace moe

@@ -140,6 +140,8 @@ struct FfnParams {
     void* aux;                // modes 3 / 4 (backward): pre-activations Z [rows, N] bf16
     int max_rows;             // most rows any expert holds (its capacity, at most the token count); 0: unknown
     int w_kn;                 // W is [E, K, N] instead (bf16, single-SM tensor-core kernel): read MN-major
+    float* zero;              // mode 0, single-SM tensor-core kernel: an fp32 buffer of zero_n floats (a multiple
+    int64_t zero_n;           // of 4, 16-byte aligned) that one extra warp per CTA clears meanwhile, or nullptr
 };
 size_t ffn_fp8_smem_bytes(int E, bool bias, int ring, bool swap);
 // weight gradients grouped along K (ffn_tc.cu): dW[e] [M, N] fp32 = sum over the rows r of expert e

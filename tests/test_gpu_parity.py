@@ -161,6 +161,15 @@ def test_all_dropped_outputs_zero():
     assert np.all(out == 0.0) and count.sum() == 100
 
 
+@pytest.mark.parametrize("cf", [1.2, 0.3])
+def test_output_cleared_by_the_up_projection(cf):
+    """A layer whose up projection is long enough (rows x h >= 8192 per token) clears the fused combine's
+    output inside the up projection's kernel instead of the gather: every token's output, dropped ones
+    included (exactly zero), still matches the oracle after a call that leaves `out` dirty."""
+    wl = small_workload(T=256, d=128, h=4096, E=4, k=2, capacity_factor=cf)
+    _full_check(wl)
+
+
 def test_heavy_drops_and_bias():
     wl = small_workload(T=400, d=64, h=128, E=4, k=2, capacity_factor=0.25, bias="normal")
     _full_check(wl)
