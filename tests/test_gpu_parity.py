@@ -232,14 +232,16 @@ def _logits_error_ratio(wl, tc, tg):
 
 @pytest.mark.parametrize("gate,E,p,d,T", [("softmax", 8, 0, 1024, 300), ("noisy", 37, 0, 256, 200),
                                           ("cosine", 10, 256, 512, 129), ("softmax", 256, 0, 7168, 64),
-                                          ("noisy", 64, 0, 320, 9733), ("cosine", 32, 256, 256, 4900)])
+                                          ("noisy", 64, 0, 320, 9733), ("cosine", 32, 256, 256, 4900),
+                                          ("softmax", 100, 0, 256, 9500)])
 def test_gate_logits_within_assumed_tensor_core_bound(gate, E, p, d, T):
     """The tensor-core logits GEMM against the exact products' sum: the routing step assumes
     |error| <= 64 * 2^-23 * sum |x_i w_i| and re-scores near ties inside twice that, so the observed
     error must sit well inside it (here: below an eighth of it).  The last two cases need more than one
     wave of 64-logit tiles, so the GEMM takes 128-logit tiles (the noisy gate's two weight tensors in one
-    tile; the cosine projection in two), with a ragged last token tile and an odd number of K blocks
-    (d = 320: two two-block accumulator chunks and a one-block chunk)."""
+    tile; the cosine projection in two; 100 softmax logits in one 112-wide tile, whose second column half
+    is partly empty), with a ragged last token tile and an odd number of K blocks (d = 320: two two-block
+    accumulator chunks and a one-block chunk)."""
     wl = small_workload(T=T, d=d, h=64, E=E, k=2, gate=gate, cos_dim=p or 32, capacity_factor=1.0)
     tc, tg = P.inputs(wl)
     ratio = _logits_error_ratio(wl, tc, tg)
