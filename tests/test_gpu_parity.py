@@ -161,6 +161,14 @@ def test_all_dropped_outputs_zero():
     assert np.all(out == 0.0) and count.sum() == 100
 
 
+@pytest.mark.parametrize("gate,E", [("softmax", 100), ("noisy", 64)])
+def test_wide_gate_tiles_full_layer(gate, E):
+    """Enough tokens that the gate GEMM takes its one-wave tiles (100 softmax logits in a 112-wide tile;
+    the noisy gate's 64 + 64 rows in one tile): routing, dispatch and outputs against the oracle."""
+    wl = small_workload(T=9500, d=256, h=64, E=E, k=2, gate=gate, capacity_factor=1.2)
+    _full_check(wl)
+
+
 @pytest.mark.parametrize("cf", [1.2, 0.3])
 def test_output_cleared_by_the_up_projection(cf):
     """A layer whose up projection is long enough (rows x h >= 8192 per token) clears the fused combine's
